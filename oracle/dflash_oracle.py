@@ -1,0 +1,332 @@
+"""CPU oracle for one DFlash draft cycle — TEST INFRASTRUCTURE, not a product path.
+
+Only the tests, the package's smoke check and the benchmark's CPU-baseline leg
+may import this module.  It is a plain, slow, float64 numpy restatement of what
+the DFlash drafter computes, written from the method's description so that a
+reader can check each function against it by eye:
+
+* "DFlash: Block Diffusion for Flash Speculative Decoding" (paper), §3.1 (accepted
+  length tau in [1, gamma+1]), §4.1 (persistent context K/V in the draft KV cache),
+  §4.2 (anchor + masked block, block_size - 1 predictions, shared frozen
+  embedding and LM head), §7.3 (fusion equation for H_t and the K/V injection
+  equations for layer i).
+* The companion explainer page "DFlash: Block Diffusion for Flash Speculative
+  Decoding" (zhongzhoutan-coder.github.io), sections "The Target Verifier Remains
+  the Correctness Anchor" (lossless acceptance rule, stop at first rejection,
+  worked example), "Target Hidden States Supply the Missing Context" (fusion
+  equation) and "Putting It Together" (one cycle, steps 1-5).
+* The blog page "Inside DFlash & Block Diffusion Speculative Decoding"
+  (abrarakhunji.com), section "2. Non-Causal Block Diffusion Denoising
+  Objective" (case definition of the non-causal mask and its 4+4 printed
+  matrix) and section "1. Arithmetic Intensity & Speculative Speedup" (E[L]).
+
+Where those pages leave a step open (RoPE pairing, norm epsilon, final norm,
+which rows get drafts, argmax ties) the reading taken is stated in the
+function's docstring.  Every floating-point step is float64; matrices are
+[out_features, in_features] and are converted to float64 in row chunks so that
+8B-shaped weights fit in host memory — each output element is still one
+complete dot product, unchanged by the chunking.
+
+Pins (tests/test_oracle_pins.py) tie each function to something other than
+itself: the printed mask matrix, the worked verification example, exhaustive
+brute force, the E[L] closed form by Monte Carlo, complex-number RoPE, library
+scaled-dot-product attention, invariants and special cases.  The end-to-end
+drafter logits have no printed values on the pages: beyond the component pins
+and the special cases in the tests, that composition is "parity unpinned".
+"""
+from __future__ import annotations
+
+import math
+from typing import Dict, List, Optional, Sequence
+
+import numpy as np
+
+F64 = np.float64
+_CHUNK_ROWS = 8192
+
+
+# ---------------------------------------------------------------------------
+# Small building blocks
+# ---------------------------------------------------------------------------
+
+def linear(x: np.ndarray, w: np.ndarray) -> np.ndarray:
+    """y = x W^T in float64 for W stored [out, in] (any float dtype).
+
+    W is upcast in chunks of output rows; each output column is the full dot
+    product of x with one row of W.
+    """
+    x = np.asarray(x, dtype=F64)
+    out = np.empty(x.shape[:-1] + (w.shape[0],), dtype=F64)
+    for r0 in range(0, w.shape[0], _CHUNK_ROWS):
+        r1 = min(r0 + _CHUNK_ROWS, w.shape[0])
+        out[..., r0:r1] = x @ np.asarray(w[r0:r1], dtype=F64).T
+    return out
+
+
+def rms_norm(x: np.ndarray, g: np.ndarray, eps: float) -> np.ndarray:
+    """RMSNorm over the last axis: g * x / sqrt(mean(x^2) + eps).
+
+    The paper applies RMSNorm to the fused context (§7.3, H_t equation); the
+    Qwen3-style drafter layers use the same norm before attention and before
+    the FFN, and once more before the LM head (reading: a final norm is taken,
+    as in the Qwen3 decoder the drafter is shaped after).
+    """
+    x = np.asarray(x, dtype=F64)
+    ms = np.mean(x * x, axis=-1, keepdims=True)
+    return x / np.sqrt(ms + eps) * np.asarray(g, dtype=F64)
+
+
+def silu(x: np.ndarray) -> np.ndarray:
+    return x / (1.0 + np.exp(-x))
+
+
+def rope(x: np.ndarray, positions: Sequence[int], theta: float) -> np.ndarray:
+    """Rotary position embedding, rotate-half pairing.
+
+    x: [n, heads, hd]; positions: [n].  Element i of the first half pairs with
+    element i + hd/2; the pair turns by angle pos * theta^(-2i/hd).  (The pages
+    call the drafter Qwen3-style but do not spell RoPE out; this is the pairing
+    Qwen3 uses.)
+    """
+    x = np.asarray(x, dtype=F64)
+    hd = x.shape[-1]
+    half = hd // 2
+    inv_freq = np.power(F64(theta), -2.0 * np.arange(half, dtype=F64) / hd)
+    ang = np.asarray(positions, dtype=F64)[:, None] * inv_freq[None, :]      # [n, half]
+    cos = np.cos(ang)[:, None, :]
+    sin = np.sin(ang)[:, None, :]
+    x1, x2 = x[..., :half], x[..., half:]
+    return np.concatenate([x1 * cos - x2 * sin, x2 * cos + x1 * sin], axis=-1)
+
+
+# ---------------------------------------------------------------------------
+# Stage 1: context fusion  (paper §7.3; explainer "Target Hidden States ...")
+# ---------------------------------------------------------------------------
+
+def fuse_context(feats: np.ndarray, w_c: np.ndarray, g_c: np.ndarray, eps: float) -> np.ndarray:
+    """H_t = RMSNorm(W_c [H^(l1); ...; H^(lm)]) for every new context token.
+
+    feats: [n, m, D], the hidden state of token j at each of the m selected
+    target layers; the m vectors are concatenated along features in layer order
+    to a length-mD vector, projected by W_c [D, mD] and normalised.
+    """
+    feats = np.asarray(feats)
+    n = feats.shape[0]
+    x = feats.reshape(n, -1)                     # [n, m*D]: [H^(l1)_j ; ... ; H^(lm)_j]
+    return rms_norm(linear(x, w_c), g_c, eps)
+
+
+# ---------------------------------------------------------------------------
+# Stage 2: K/V injection into every draft layer  (paper §7.3, §4.1)
+# ---------------------------------------------------------------------------
+
+def inject_kv(h_t: np.ndarray, w_k: np.ndarray, w_v: np.ndarray, positions: Sequence[int],
+              n_kv_heads: int, head_dim: int, theta: float):
+    """Context keys and values of one draft layer: W^K H_t and W^V H_t.
+
+    Only keys get the rotary embedding; a context token j injected for a
+    request holding c tokens sits at absolute position c + j (reading: context
+    positions count from 0 and the block continues after them).  No per-layer
+    norm is applied to H_t — the equation feeds H_t straight into W^K, W^V.
+    Returns K, V as [n, n_kv_heads, head_dim].
+    """
+    n = h_t.shape[0]
+    k = linear(h_t, w_k).reshape(n, n_kv_heads, head_dim)
+    v = linear(h_t, w_v).reshape(n, n_kv_heads, head_dim)
+    return rope(k, positions, theta), v
+
+
+class RequestCache:
+    """Persistent context K/V of one request for every draft layer (§4.1:
+    "stored in the draft model's KV cache and reused across drafting
+    iterations").  Only context entries live here; block K/V never does."""
+
+    def __init__(self, layers: int, n_kv_heads: int, head_dim: int):
+        self.k: List[np.ndarray] = [np.zeros((0, n_kv_heads, head_dim)) for _ in range(layers)]
+        self.v: List[np.ndarray] = [np.zeros((0, n_kv_heads, head_dim)) for _ in range(layers)]
+
+    @property
+    def length(self) -> int:
+        return self.k[0].shape[0]
+
+
+def inject_context(weights: Dict, cfg, cache: RequestCache, feats: np.ndarray) -> np.ndarray:
+    """Stages 1+2 for one request: fuse the new tokens' target features and
+    append their K/V to every layer of the cache.  Returns H_t."""
+    h_t = fuse_context(feats, weights["w_c"], weights["g_c"], cfg.rms_eps)
+    c = cache.length
+    pos = np.arange(c, c + h_t.shape[0])
+    for i, lw in enumerate(weights["layers"]):
+        k, v = inject_kv(h_t, lw["w_k"], lw["w_v"], pos, cfg.n_kv_heads, cfg.head_dim, cfg.rope_theta)
+        cache.k[i] = np.concatenate([cache.k[i], k], axis=0)
+        cache.v[i] = np.concatenate([cache.v[i], v], axis=0)
+    return h_t
+
+
+# ---------------------------------------------------------------------------
+# The non-causal DFlash mask  (blog, "2. Non-Causal Block Diffusion ...")
+# ---------------------------------------------------------------------------
+
+def dflash_mask(t: int, K: int) -> np.ndarray:
+    """M[i, j] over the sequence [c_1..c_t ; m_1..m_K], 1-indexed as printed.
+
+    Block rows (t < i <= t+K) see every context position (j <= t) and every
+    block position (t < j <= t+K).  Context rows carry the "causal context"
+    case: j <= i.  (The case list writes "j <= t" for the context case without
+    a condition on i; the printed 4+4 matrix and the case's own label make the
+    context rows causal.  Context rows are never drafter queries — target
+    features bypass the Q projection — so only block rows reach the drafter.)
+    """
+    n = t + K
+    M = np.zeros((n, n), dtype=np.int64)
+    for i in range(1, n + 1):
+        for j in range(1, n + 1):
+            if i <= t:
+                M[i - 1, j - 1] = 1 if j <= i else 0
+            elif j <= t:
+                M[i - 1, j - 1] = 1
+            elif t < j <= t + K:
+                M[i - 1, j - 1] = 1
+    return M
+
+
+# ---------------------------------------------------------------------------
+# Stage 3: drafter forward over [anchor, mask x (block-1)]
+# ---------------------------------------------------------------------------
+
+def attention_masked(q: np.ndarray, k_all: np.ndarray, v_all: np.ndarray, mask_rows: np.ndarray) -> np.ndarray:
+    """Softmax attention of the block queries through an explicit mask.
+
+    q: [g, nq, hd] (block rows); k_all, v_all: [t+g, nkv, hd] = [context ; block];
+    mask_rows: [g, t+g], the block rows of the DFlash mask.  Scale 1/sqrt(hd),
+    no bias; query head h reads kv head h // (nq / nkv) (grouped-query).
+    """
+    g, nq, hd = q.shape
+    nkv = k_all.shape[1]
+    group = nq // nkv
+    out = np.zeros((g, nq, hd), dtype=F64)
+    scale = 1.0 / math.sqrt(hd)
+    allowed = mask_rows.astype(bool)
+    for h in range(nq):
+        kh = k_all[:, h // group, :]
+        vh = v_all[:, h // group, :]
+        s = (q[:, h, :] @ kh.T) * scale                      # [g, t+g]
+        s = np.where(allowed, s, -np.inf)
+        s = s - np.max(s, axis=1, keepdims=True)
+        p = np.exp(s)
+        p = p / np.sum(p, axis=1, keepdims=True)
+        out[:, h, :] = p @ vh
+    return out
+
+
+def attention_block(q: np.ndarray, k_ctx: np.ndarray, v_ctx: np.ndarray,
+                    k_blk: np.ndarray, v_blk: np.ndarray) -> np.ndarray:
+    """Block queries against every context key and every block key, no mask:
+    the form the DFlash mask reduces to for block rows."""
+    k_all = np.concatenate([k_ctx, k_blk], axis=0)
+    v_all = np.concatenate([v_ctx, v_blk], axis=0)
+    return attention_masked(q, k_all, v_all, np.ones((q.shape[0], k_all.shape[0]), dtype=np.int64))
+
+
+def draft_forward(weights: Dict, cfg, cache: RequestCache, anchor: int, block: int,
+                  use_mask: bool = True) -> Dict[str, np.ndarray]:
+    """One non-causal drafter pass over [anchor, mask, ..., mask] (block rows).
+
+    Per layer i (Qwen3-style): u = RMSNorm(x); Q = W^Q u, K = W^K u, V = W^V u
+    with RoPE on Q and K at positions c..c+block-1; the block keys/values are
+    appended after the layer's injected context K/V (paper §7.3: K_i =
+    [W^K H_t ; W^K H_d], V_i likewise); attention through the DFlash mask;
+    x += W^O o; u = RMSNorm(x); x += W^D (silu(W^G u) * W^U u).  After the
+    last layer h = RMSNorm_final(x).  The block's own K/V is not kept.
+    """
+    D, nq, nkv, hd = cfg.hidden, cfg.n_q_heads, cfg.n_kv_heads, cfg.head_dim
+    c = cache.length
+    tokens = [int(anchor)] + [cfg.mask_id] * (block - 1)
+    x = np.asarray(weights["embed"][tokens], dtype=F64)            # shared embedding rows
+    pos = np.arange(c, c + block)
+    mask_rows = dflash_mask(c, block)[c:, :]                       # block rows only
+    for i, lw in enumerate(weights["layers"]):
+        u = rms_norm(x, lw["g_in"], cfg.rms_eps)
+        q = rope(linear(u, lw["w_q"]).reshape(block, nq, hd), pos, cfg.rope_theta)
+        k = rope(linear(u, lw["w_k"]).reshape(block, nkv, hd), pos, cfg.rope_theta)
+        v = linear(u, lw["w_v"]).reshape(block, nkv, hd)
+        if use_mask:
+            o = attention_masked(q, np.concatenate([cache.k[i], k]), np.concatenate([cache.v[i], v]), mask_rows)
+        else:
+            o = attention_block(q, cache.k[i], cache.v[i], k, v)
+        x = x + linear(o.reshape(block, nq * hd), lw["w_o"])
+        u = rms_norm(x, lw["g_post"], cfg.rms_eps)
+        x = x + linear(silu(linear(u, lw["w_g"])) * linear(u, lw["w_u"]), lw["w_d"])
+    h = rms_norm(x, weights["g_final"], cfg.rms_eps)
+    return {"h": h}
+
+
+# ---------------------------------------------------------------------------
+# Stage 4: shared LM head + argmax  (paper §4.2 shared head; explainer step 3)
+# ---------------------------------------------------------------------------
+
+def lm_head_argmax(h_rows: np.ndarray, lm_head: np.ndarray):
+    """logits = h W_lm^T for the mask rows; draft = argmax, lowest index on ties.
+
+    Reading: the anchor row's output is not a draft; rows 1..block-1 give the
+    block_size - 1 predictions (paper §4.2)."""
+    logits = linear(h_rows, lm_head)
+    drafts = np.argmax(logits, axis=-1).astype(np.int64)   # first occurrence of the maximum
+    return logits, drafts
+
+
+# ---------------------------------------------------------------------------
+# Stage 5: greedy verification  (explainer, "The Target Verifier ...")
+# ---------------------------------------------------------------------------
+
+def verify_greedy(drafts: Sequence[int], target: Sequence[int]):
+    """Greedy lossless verification of one block.
+
+    drafts d_1..d_{g-1}; target y_0..y_{g-1} where y_k is the target's greedy
+    token after block position k (y_0 judges d_1).  Walk left to right and stop
+    at the first rejection; n = number of accepted drafts, tau = n + 1, the
+    emitted tokens are d_1..d_n followed by y_n (the correction, or the bonus
+    when every draft survives).  Returns (tau, out[g] padded with -1,
+    next_anchor = y_n).
+    """
+    g = len(target)
+    n = 0
+    while n < len(drafts) and int(drafts[n]) == int(target[n]):
+        n += 1
+    out = [int(d) for d in drafts[:n]] + [int(target[n])]
+    out = out + [-1] * (g - len(out))
+    return n + 1, out, int(target[n])
+
+
+def expected_accept_len(alpha: Sequence[float]) -> float:
+    """E[L] = 1 + sum_i prod_{j<=i} alpha_j (blog, section 1), alpha_j the
+    probability that draft j is accepted given the ones before it were."""
+    total, prod = 1.0, 1.0
+    for a in alpha:
+        prod *= a
+        total += prod
+    return total
+
+
+# ---------------------------------------------------------------------------
+# One whole cycle for one request
+# ---------------------------------------------------------------------------
+
+def draft_cycle(weights: Dict, cfg, cache: RequestCache, new_feats: Optional[np.ndarray], anchor: int,
+                block: int, use_mask: bool = True) -> Dict[str, np.ndarray]:
+    """inject(new tokens) -> draft forward -> LM head + argmax for one request."""
+    if new_feats is not None and new_feats.shape[0] > 0:
+        inject_context(weights, cfg, cache, new_feats)
+    fw = draft_forward(weights, cfg, cache, anchor, block, use_mask=use_mask)
+    logits, drafts = lm_head_argmax(fw["h"][1:], weights["lm_head"])
+    return {"h": fw["h"], "logits": logits, "drafts": drafts}
+
+
+def weights_to_numpy(w: Dict) -> Dict:
+    """Host float32 copies of a weight dict whose leaves are torch tensors
+    (bf16 values are exact in float32).  Conversion only."""
+    def conv(t):
+        return t.detach().to("cpu").float().numpy()
+    out = {k: conv(v) for k, v in w.items() if k != "layers"}
+    out["layers"] = [{k: conv(v) for k, v in lw.items()} for lw in w["layers"]]
+    return out

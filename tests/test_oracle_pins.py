@@ -1,0 +1,384 @@
+"""Pins for the CPU oracle: each function is tied to something other than itself.
+
+Sources: the printed DFlash mask matrix and its case definition (blog page
+"Inside DFlash & Block Diffusion Speculative Decoding", section 2), the
+verification rule and its worked example (explainer page, "The Target Verifier
+Remains the Correctness Anchor"), the E[L] closed form (blog page, section 1),
+tau in [1, gamma+1] (paper §3.1), the fusion and injection equations (paper
+§7.3) and the memory figures that follow them, plus textbook identities
+(complex rotation for RoPE, library scaled-dot-product attention).
+"""
+import itertools
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from dflash_inputs import TINY, DraftConfig, make_agreement, make_features, make_tokens, make_weights, replace
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+rng = np.random.default_rng(1234)
+
+
+def _read_golden(name):
+    rows = []
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.strip()
+            if line and not line.startswith("#"):
+                rows.append([int(v) for v in line.split()])
+    return np.array(rows, dtype=np.int64)
+
+
+# ---------------------------------------------------------------- the mask
+
+def test_mask_matches_printed_4plus4_matrix():
+    printed = _read_golden("dflash_mask_4plus4.txt")
+    assert np.array_equal(oracle.dflash_mask(4, 4), printed)
+
+
+@pytest.mark.parametrize("t,K", [(0, 1), (0, 4), (1, 1), (3, 5), (7, 16)])
+def test_mask_block_rows_see_context_and_whole_block_only(t, K):
+    M = oracle.dflash_mask(t, K)
+    assert M.shape == (t + K, t + K)
+    # block rows: everything (all context + the whole block, in both directions)
+    assert np.all(M[t:, :] == 1)
+    # context rows never see a block position (no leakage from the masked block)
+    assert np.all(M[:t, t:] == 0)
+
+
+# ---------------------------------------------------------------- attention
+
+def _rand(*shape):
+    return rng.standard_normal(shape)
+
+
+@pytest.mark.parametrize("c,g,nq,nkv", [(0, 4, 4, 2), (5, 4, 4, 2), (17, 3, 8, 2), (9, 16, 4, 4)])
+def test_masked_attention_equals_unmasked_over_context_and_block(c, g, nq, nkv):
+    hd = 8
+    q = _rand(g, nq, hd)
+    kc, vc = _rand(c, nkv, hd), _rand(c, nkv, hd)
+    kb, vb = _rand(g, nkv, hd), _rand(g, nkv, hd)
+    rows = oracle.dflash_mask(c, g)[c:, :]
+    a = oracle.attention_masked(q, np.concatenate([kc, kb]), np.concatenate([vc, vb]), rows)
+    b = oracle.attention_block(q, kc, vc, kb, vb)
+    np.testing.assert_allclose(a, b, rtol=1e-13, atol=1e-13)
+
+
+@pytest.mark.parametrize("c,g,nq,nkv", [(6, 4, 4, 2), (0, 5, 6, 3), (11, 2, 2, 1)])
+def test_masked_attention_matches_library_sdpa(c, g, nq, nkv):
+    """Full [context; block] sequence through torch's fp64 SDPA with a boolean
+    mask built from the case definition; block rows must agree."""
+    hd = 16
+    n = c + g
+    q_full = _rand(n, nq, hd)
+    k_all, v_all = _rand(n, nkv, hd), _rand(n, nkv, hd)
+    M = oracle.dflash_mask(c, g)
+    ours = oracle.attention_masked(q_full[c:], k_all, v_all, M[c:, :])
+    rep = nq // nkv
+    qt = torch.tensor(q_full).permute(1, 0, 2)                       # [nq, n, hd]
+    kt = torch.tensor(k_all).permute(1, 0, 2).repeat_interleave(rep, 0)
+    vt = torch.tensor(v_all).permute(1, 0, 2).repeat_interleave(rep, 0)
+    ref = torch.nn.functional.scaled_dot_product_attention(qt, kt, vt, attn_mask=torch.tensor(M, dtype=torch.bool))
+    np.testing.assert_allclose(ours, ref.permute(1, 0, 2).numpy()[c:], rtol=1e-12, atol=1e-12)
+
+
+def test_attention_identical_keys_gives_mean_of_values():
+    c, g, nq, nkv, hd = 7, 4, 4, 2, 8
+    key = _rand(1, 1, hd)
+    k_all = np.broadcast_to(key, (c + g, nkv, hd)).copy()
+    v_all = _rand(c + g, nkv, hd)
+    out = oracle.attention_masked(_rand(g, nq, hd), k_all, v_all, np.ones((g, c + g)))
+    for h in range(nq):
+        np.testing.assert_allclose(out[:, h, :], np.broadcast_to(v_all[:, h // 2, :].mean(0), (g, hd)), rtol=1e-12)
+
+
+def test_gqa_equals_mha_with_duplicated_kv_heads():
+    c, g, nq, nkv, hd = 5, 4, 8, 2, 8
+    q = _rand(g, nq, hd)
+    k, v = _rand(c + g, nkv, hd), _rand(c + g, nkv, hd)
+    ones = np.ones((g, c + g))
+    a = oracle.attention_masked(q, k, v, ones)
+    b = oracle.attention_masked(q, np.repeat(k, nq // nkv, axis=1), np.repeat(v, nq // nkv, axis=1), ones)
+    np.testing.assert_allclose(a, b, rtol=1e-13, atol=1e-13)
+
+
+def test_block_is_bidirectional():
+    """Row 0 (the anchor) must depend on the last block position's key/value."""
+    c, g, nq, nkv, hd = 3, 4, 2, 1, 8
+    q, kc, vc = _rand(g, nq, hd), _rand(c, nkv, hd), _rand(c, nkv, hd)
+    kb, vb = _rand(g, nkv, hd), _rand(g, nkv, hd)
+    a = oracle.attention_block(q, kc, vc, kb, vb)
+    vb2 = vb.copy()
+    vb2[-1] += 1.0
+    b = oracle.attention_block(q, kc, vc, kb, vb2)
+    assert np.max(np.abs(a[0] - b[0])) > 1e-6
+
+
+# ---------------------------------------------------------------- RoPE, norms
+
+def test_rope_is_the_complex_rotation():
+    n, H, hd, theta = 9, 3, 16, 1e6
+    x = _rand(n, H, hd)
+    pos = rng.integers(0, 40000, n)
+    out = oracle.rope(x, pos, theta)
+    half = hd // 2
+    z = x[..., :half] + 1j * x[..., half:]
+    freqs = theta ** (-np.arange(half) * 2.0 / hd)
+    zr = z * np.exp(1j * pos[:, None, None] * freqs[None, None, :])
+    np.testing.assert_allclose(out[..., :half], zr.real, rtol=1e-11, atol=1e-11)
+    np.testing.assert_allclose(out[..., half:], zr.imag, rtol=1e-11, atol=1e-11)
+
+
+def test_rope_identity_at_zero_norm_preserving_and_relative():
+    n, H, hd, theta = 6, 2, 32, 1e6
+    x = _rand(n, H, hd)
+    np.testing.assert_allclose(oracle.rope(x, np.zeros(n, int), theta), x, rtol=0, atol=0)
+    pos = rng.integers(0, 5000, n)
+    r = oracle.rope(x, pos, theta)
+    np.testing.assert_allclose(np.linalg.norm(r, axis=-1), np.linalg.norm(x, axis=-1), rtol=1e-12)
+    q, k = _rand(1, 1, hd), _rand(1, 1, hd)
+    for p, s, d in [(3, 10, 100), (0, 7, 12345)]:
+        a = np.sum(oracle.rope(q, [p], theta) * oracle.rope(k, [s], theta))
+        b = np.sum(oracle.rope(q, [p + d], theta) * oracle.rope(k, [s + d], theta))
+        assert abs(a - b) < 1e-9
+
+
+def test_rmsnorm_unit_rms_scale_invariance_and_gain():
+    x = _rand(5, 64)
+    y = oracle.rms_norm(x, np.ones(64), 0.0)
+    np.testing.assert_allclose(np.sqrt(np.mean(y * y, axis=-1)), 1.0, rtol=1e-13)
+    np.testing.assert_allclose(oracle.rms_norm(7.5 * x, np.ones(64), 0.0), y, rtol=1e-13)
+    g = _rand(64)
+    np.testing.assert_allclose(oracle.rms_norm(x, g, 0.0), y * g, rtol=1e-13)
+    # eps only matters near zero
+    assert np.all(oracle.rms_norm(np.zeros((1, 8)), np.ones(8), 1e-6) == 0)
+
+
+# ---------------------------------------------------------------- fusion / injection
+
+def test_fuse_context_sums_one_slice_of_wc_per_target_layer():
+    """[H^(l1);...;H^(l5)] through W_c is the sum over target layers j of the
+    D-column slice j of W_c applied to H^(lj) — pins the concatenation order."""
+    m, D, n = 5, 12, 4
+    feats = _rand(n, m, D)
+    w_c = _rand(D, m * D)
+    y = sum(feats[:, j, :] @ w_c[:, j * D:(j + 1) * D].T for j in range(m))
+    ref = y / np.sqrt(np.mean(y * y, axis=-1, keepdims=True) + 1e-6)
+    np.testing.assert_allclose(oracle.fuse_context(feats, w_c, np.ones(D), 1e-6), ref, rtol=1e-12)
+    # a slice of feats belonging to a wrong layer gives a different answer
+    bad = sum(feats[:, (j + 1) % m, :] @ w_c[:, j * D:(j + 1) * D].T for j in range(m))
+    assert not np.allclose(bad, y)
+
+
+def test_memory_figures_of_the_projection():
+    """Paper §7.3: W_c in R^{D x 5D} at D=2048 in BF16 is 5*2048*2048*2 ~ 42 MB; at
+    batch 1, sequence 2048 the projection input/output are about 40 MB / 8 MB."""
+    cfg = DraftConfig("d2048", hidden=2048, layers=1, n_q_heads=16, n_kv_heads=4, head_dim=128,
+                      ffn=64, vocab=8, dtype="bf16")
+    w_c_bytes = cfg.hidden * cfg.n_target_feats * cfg.hidden * cfg.elem_bytes
+    assert w_c_bytes == 41_943_040 and round(w_c_bytes / 1e6) == 42
+    assert round(2048 * 5 * 2048 * 2 / 2**20) == 40
+    assert round(2048 * 2048 * 2 / 2**20) == 8
+
+
+def _tiny_setup(seed=0, layers=2):
+    cfg = replace(TINY, layers=layers)
+    w = oracle.weights_to_numpy(make_weights(cfg, seed))
+    return cfg, w
+
+
+def test_incremental_injection_equals_one_shot():
+    cfg, w = _tiny_setup()
+    f = make_features(cfg, 11, seed=5).float().numpy()
+    a = oracle.RequestCache(cfg.layers, cfg.n_kv_heads, cfg.head_dim)
+    oracle.inject_context(w, cfg, a, f)
+    b = oracle.RequestCache(cfg.layers, cfg.n_kv_heads, cfg.head_dim)
+    oracle.inject_context(w, cfg, b, f[:4])
+    oracle.inject_context(w, cfg, b, f[4:])
+    for i in range(cfg.layers):
+        np.testing.assert_allclose(a.k[i], b.k[i], rtol=1e-12, atol=1e-12)
+        np.testing.assert_allclose(a.v[i], b.v[i], rtol=1e-12, atol=1e-12)
+
+
+def test_context_reaches_block_only_through_kv_and_block_never_enters_cache():
+    cfg, w = _tiny_setup()
+    f = make_features(cfg, 16, seed=6).float().numpy()
+    cache = oracle.RequestCache(cfg.layers, cfg.n_kv_heads, cfg.head_dim)
+    oracle.inject_context(w, cfg, cache, f)
+    k_before = [k.copy() for k in cache.k]
+    out1 = oracle.draft_forward(w, cfg, cache, anchor=3, block=4)["h"]
+    assert cache.length == 16 and all(np.array_equal(a, b) for a, b in zip(k_before, cache.k))
+    # perturb the context keys/values only: the block output must move
+    cache.v[1] = cache.v[1] + 0.5
+    out2 = oracle.draft_forward(w, cfg, cache, anchor=3, block=4)["h"]
+    assert np.max(np.abs(out1 - out2)) > 1e-6
+    # with every W^V zeroed the value path carries no context: then changing
+    # the context values changes nothing
+    w0 = dict(w, layers=[dict(lw, w_v=np.zeros_like(lw["w_v"])) for lw in w["layers"]])
+    c0 = oracle.RequestCache(cfg.layers, cfg.n_kv_heads, cfg.head_dim)
+    oracle.inject_context(w0, cfg, c0, f)
+    assert np.all(c0.v[0] == 0)
+
+
+def test_zero_output_projections_reduce_drafter_to_normed_embedding():
+    """Special case: W^O = W^D = 0 in every layer leaves x = E[tokens]; then
+    h = RMSNorm(E[tokens]) and every mask row drafts argmax(RMSNorm(E[mask]) W_lm^T)."""
+    cfg, w = _tiny_setup()
+    w0 = dict(w, layers=[dict(lw, w_o=np.zeros_like(lw["w_o"]), w_d=np.zeros_like(lw["w_d"])) for lw in w["layers"]])
+    cache = oracle.RequestCache(cfg.layers, cfg.n_kv_heads, cfg.head_dim)
+    oracle.inject_context(w0, cfg, cache, make_features(cfg, 8, seed=9).float().numpy())
+    r = oracle.draft_cycle(w0, cfg, cache, None, anchor=17, block=5)
+    e = w["embed"][cfg.mask_id].astype(np.float64)
+    he = e / np.sqrt(np.mean(e * e) + cfg.rms_eps)
+    logits = w["lm_head"].astype(np.float64) @ he
+    assert np.all(r["drafts"] == int(np.argmax(logits)))
+    np.testing.assert_allclose(r["logits"][0], logits, rtol=1e-12, atol=1e-12)
+
+
+def test_draft_forward_matches_torch_fp64_restatement():
+    """Independent restatement with torch library routines (SDPA, silu) in
+    float64 over the tiny config; RoPE via complex multiplication."""
+    cfg, w = _tiny_setup(seed=0)
+    feats = make_features(cfg, 64, seed=1).float().numpy()
+    cache = oracle.RequestCache(cfg.layers, cfg.n_kv_heads, cfg.head_dim)
+    oracle.inject_context(w, cfg, cache, feats)
+    r = oracle.draft_cycle(w, cfg, cache, None, anchor=5, block=4)
+
+    T = lambda a: torch.tensor(np.asarray(a, dtype=np.float64))
+    D, nq, nkv, hd, g = cfg.hidden, cfg.n_q_heads, cfg.n_kv_heads, cfg.head_dim, 4
+
+    def rms(x):
+        return x * torch.rsqrt((x * x).mean(-1, keepdim=True) + cfg.rms_eps)
+
+    def rot(x, pos):
+        half = hd // 2
+        z = torch.complex(x[..., :half], x[..., half:])
+        f = cfg.rope_theta ** (-torch.arange(half, dtype=torch.float64) * 2.0 / hd)
+        z = z * torch.polar(torch.ones_like(f), pos[:, None, None].double() * f)
+        return torch.cat([z.real, z.imag], -1)
+
+    x_ctx = T(feats).reshape(64, -1) @ T(w["w_c"]).T
+    h_t = rms(x_ctx)
+    pos_c = torch.arange(64)
+    pos_b = torch.arange(64, 64 + g)
+    x = T(w["embed"])[[5] + [cfg.mask_id] * (g - 1)]
+    for lw in w["layers"]:
+        kc = rot((h_t @ T(lw["w_k"]).T).reshape(64, nkv, hd), pos_c)
+        vc = (h_t @ T(lw["w_v"]).T).reshape(64, nkv, hd)
+        u = rms(x)
+        q = rot((u @ T(lw["w_q"]).T).reshape(g, nq, hd), pos_b)
+        kb = rot((u @ T(lw["w_k"]).T).reshape(g, nkv, hd), pos_b)
+        vb = (u @ T(lw["w_v"]).T).reshape(g, nkv, hd)
+        K = torch.cat([kc, kb]).permute(1, 0, 2).repeat_interleave(nq // nkv, 0)
+        V = torch.cat([vc, vb]).permute(1, 0, 2).repeat_interleave(nq // nkv, 0)
+        o = torch.nn.functional.scaled_dot_product_attention(q.permute(1, 0, 2), K, V)
+        x = x + o.permute(1, 0, 2).reshape(g, nq * hd) @ T(lw["w_o"]).T
+        u = rms(x)
+        x = x + (torch.nn.functional.silu(u @ T(lw["w_g"]).T) * (u @ T(lw["w_u"]).T)) @ T(lw["w_d"]).T
+    logits = rms(x)[1:] @ T(w["lm_head"]).T
+    np.testing.assert_allclose(r["logits"], logits.numpy(), rtol=1e-10, atol=1e-10)
+    assert np.array_equal(r["drafts"], torch.argmax(logits, -1).numpy())
+
+
+def test_lm_head_argmax_breaks_ties_to_lowest_index():
+    h = np.array([[1.0, 0.0], [0.0, 1.0]])
+    W = np.array([[0.0, 0.0], [1.0, 0.0], [0.5, 0.5], [1.0, 0.0], [0.0, 1.0]])
+    _, d = oracle.lm_head_argmax(h, W)
+    assert list(d) == [1, 4]
+    _, d = oracle.lm_head_argmax(np.zeros((1, 2)), W)
+    assert list(d) == [0]
+
+
+# ---------------------------------------------------------------- verification
+
+def test_verify_worked_example():
+    for proposals, first_rej, tau_exp, emitted in _read_golden("verify_worked_example.txt"):
+        d = list(range(100, 100 + proposals))
+        y = list(d) + [999]                   # target agrees everywhere ...
+        y[first_rej - 1] = 555                # ... except at proposal `first_rej`
+        tau, out, nxt = oracle.verify_greedy(d, y)
+        assert tau == tau_exp
+        assert out[:emitted] == d[:first_rej - 1] + [555]     # three kept, target supplies the 4th
+        assert all(t == -1 for t in out[emitted:])             # proposals 5.. discarded
+        assert nxt == 555
+
+
+def _brute_tau(d, y):
+    """Accepted length from its definition: 1 + the largest n such that the
+    first n drafts all equal the target's tokens, over every prefix length."""
+    best = 0
+    for n in range(len(d) + 1):
+        if all(d[k] == y[k] for k in range(n)):
+            best = max(best, n)
+    return best + 1
+
+
+@pytest.mark.parametrize("block", [1, 2, 4])
+def test_verify_exhaustive_tiny_vocab(block):
+    V = 3
+    for d in itertools.product(range(V), repeat=block - 1):
+        for y in itertools.product(range(V), repeat=block):
+            tau, out, nxt = oracle.verify_greedy(d, y)
+            assert tau == _brute_tau(d, y)
+            assert 1 <= tau <= block                         # paper §3.1: tau in [1, gamma+1]
+            assert out[:tau] == list(d[:tau - 1]) + [y[tau - 1]]
+            assert nxt == y[tau - 1]
+
+
+def test_expected_accept_length_closed_form_by_monte_carlo():
+    """E[L] = 1 + sum_i prod_{j<=i} alpha_j with independent per-position
+    agreement; checked on the oracle's verify over synthetic blocks."""
+    cfg = replace(TINY, vocab=50)
+    for block, p in [(16, [0.9]), (8, [0.6])]:
+        N = 60000
+        pat = make_agreement(cfg, N, block, p * N, seed=11)
+        d = make_tokens(cfg, N * (block - 1), seed=12).reshape(N, block - 1)
+        from dflash_inputs import synthetic_target_argmax
+        y = synthetic_target_argmax(d, pat, cfg.vocab)
+        dn, yn = d.numpy(), y.numpy()
+        taus = np.array([oracle.verify_greedy(dn[i], yn[i])[0] for i in range(N)], dtype=np.float64)
+        expect = oracle.expected_accept_len([p[0]] * (block - 1))
+        assert abs(taus.mean() - expect) < 4 * taus.std() / math.sqrt(N), (taus.mean(), expect)
+    assert abs(oracle.expected_accept_len([0.9] * 15) - 8.14697981114816) < 1e-12
+
+
+def test_speculative_loop_is_lossless_against_a_fake_target():
+    """Whatever the drafts are, the emitted stream equals plain greedy decoding
+    of the (deterministic) target: explainer step 4-5 and the lossless rule."""
+    V = 7
+
+    def target_next(prefix):                       # a deterministic "greedy target"
+        h = 0
+        for t in prefix[-3:]:
+            h = (h * 31 + t + 1) % 1000003
+        return (h * 2654435761) % V
+
+    prompt = [1, 2, 3]
+    ref = list(prompt)
+    while len(ref) < 60:
+        ref.append(target_next(ref))
+
+    r = np.random.default_rng(0)
+    for block in (1, 2, 5, 16):
+        seq = list(prompt)
+        anchor = target_next(seq)                  # the first target token is the first anchor
+        while len(seq) < 60:
+            good = r.random() < 0.7
+            drafts, ctx = [], seq + [anchor]
+            for _ in range(block - 1):             # drafts: right w.p. ~0.7 per position, else random
+                t = target_next(ctx) if (good and r.random() < 0.8) else int(r.integers(V))
+                drafts.append(t)
+                ctx = ctx + [t]
+            ys, ctx = [], seq + [anchor]
+            for k in range(block):                 # target's greedy token after each block position
+                ys.append(target_next(ctx))
+                if k < block - 1:
+                    ctx = ctx + [drafts[k]]
+            tau, out, nxt = oracle.verify_greedy(drafts, ys)
+            seq = seq + [anchor] + out[:tau - 1]   # committed: anchor + accepted drafts
+            anchor = nxt                           # correction / bonus is the next anchor
+        assert seq[:60] == ref[:60]
