@@ -1,0 +1,404 @@
+#!/usr/bin/env python
+"""Benchmark of the DFlash draft cycle on GB300: drafted tokens/s and cycle latency.
+
+One step = one whole draft cycle on device-resident inputs: inject the
+previous cycle's tau committed tokens (context fusion + K/V injection into
+every draft layer), draft a block (non-causal drafter pass + shared LM head
+argmax), let the synthetic target answer (seeded agreement pattern), verify
+greedily.  value = drafted tokens/s = batch * (block - 1) / cycle time, summed
+over ranks (weak scaling: each rank drafts for its own requests; requests are
+independent, so there is no collective on the data path).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload 8b_bs1]
+    python bench.py --impl reference ...     # the CPU oracle on the host cores
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from dflash_inputs import (make_agreement, make_features, make_tokens, make_weights, seed_for,  # noqa: E402
+                           synthetic_target_argmax, workloads)
+
+METRIC = "drafted tokens/s & draft-cycle latency at bs1/bs32; % of HBM or TC roofline"
+UNIT = "drafted tokens/s"
+GEMM_STAGES = ("fuse", "inject", "qkv", "o", "gateup", "down", "lmhead")
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="dflash", choices=["dflash", "reference"])
+    ap.add_argument("--workload", default="8b_bs1")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def load_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), "measured"
+    except Exception:
+        return 6800.0, 1900.0, "fallback"
+
+
+# ---------------------------------------------------------------- clocks
+class Clocks:
+    """nvidia-smi sampler running while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(prefix="clocks_", suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- algorithmic bytes
+def gemm_bytes_per_cycle(cfg, B: int, block: int, inject_rows: int) -> dict:
+    """Algorithmic DRAM bytes of each GEMM stage in one cycle: every weight
+    byte once, activations in, outputs out (fp32 residual read + write)."""
+    es = cfg.elem_bytes
+    D, L, m = cfg.hidden, cfg.layers, cfg.n_target_feats
+    hq, hk, F, V = cfg.n_q_heads * cfg.head_dim, cfg.n_kv_heads * cfg.head_dim, cfg.ffn, cfg.vocab
+    R, Rm, n = B * block, B * (block - 1), inject_rows
+    return {
+        "fuse": es * D * m * D + es * n * m * D + 4 * n * D,
+        "inject": es * L * 2 * hk * D + es * n * D + es * n * L * 2 * hk,
+        "qkv": L * (es * (hq + 2 * hk) * D + es * R * D + es * R * (hq + 2 * hk)),
+        "o": L * (es * D * hq + es * R * hq + 8 * R * D),
+        "gateup": L * (es * 2 * F * D + es * R * D + es * R * F),
+        "down": L * (es * D * F + es * R * F + 8 * R * D),
+        "lmhead": es * V * D + es * Rm * D + 8 * Rm,
+    }
+
+
+# ---------------------------------------------------------------- the GPU arm
+class Cycle:
+    """Device-resident draft cycle of one workload through the C ABI."""
+
+    def __init__(self, wl, total_cycles: int, rank: int):
+        import block_diffusion_drafter_dflash_gb300 as df
+        self.df = df
+        self.wl, cfg = wl, wl.cfg
+        self.cfg = cfg
+        B, block = wl.batch, wl.block
+        self.B, self.block = B, block
+        seed = wl.seed + 100000 * rank
+        self.weights = make_weights(cfg, seed, device="cuda")
+        self.model = df.Model(cfg, self.weights)
+        self.cap = max(wl.ctx) + block * (total_cycles + 2)
+        self.cache = df.Cache(self.model, B, self.cap)
+        self.rows = B * block
+        setup_chunk = min(sum(wl.ctx), 16384)
+        self.ws = df.dflash_workspace(self.model, B, self.cap, block, max(self.rows, setup_chunk))
+        # setup injection of each request's context, in chunks of at most setup_chunk rows
+        for b, c in enumerate(wl.ctx):
+            for s in range(0, c, setup_chunk):
+                n = min(setup_chunk, c - s)
+                counts = [0] * B
+                counts[b] = n
+                f = make_features(cfg, n, seed=seed + 17 * b + s, device="cuda")
+                df.dflash_inject_context(self.model, self.cache, f, torch.tensor(counts, dtype=torch.int32,
+                                                                                 device="cuda"), counts, n, self.ws)
+        torch.cuda.synchronize()
+        # per-cycle inputs: a small pool of feature blocks and one agreement pattern per cycle
+        self.feat_pool = [make_features(cfg, self.rows, seed=seed + 999 + i, device="cuda") for i in range(4)]
+        self.patterns = [make_agreement(cfg, B, block, wl.accept_p, seed=seed_for(wl, i, 5) + rank, device="cuda")
+                         for i in range(total_cycles)]
+        self.tau = torch.full((B,), wl.first_inject, dtype=torch.int32, device="cuda")
+        self.anchor = make_tokens(cfg, B, seed=seed + 3, device="cuda")
+        self.drafts = torch.empty((B, block - 1), dtype=torch.int32, device="cuda")
+        self.out = torch.empty((B, block), dtype=torch.int32, device="cuda")
+        self.next_anchor = torch.empty((B,), dtype=torch.int32, device="cuda")
+        self.i = 0
+        self.tau_sum = 0
+
+    def step(self, feats=None, pattern=None):
+        df = self.df
+        f = feats if feats is not None else self.feat_pool[self.i % len(self.feat_pool)]
+        pat = pattern if pattern is not None else self.patterns[self.i % len(self.patterns)]
+        df.dflash_inject_context(self.model, self.cache, f, self.tau, None, self.rows, self.ws)
+        df.dflash_draft_block(self.model, self.cache, self.anchor, self.block, self.drafts, None, self.ws)
+        y = synthetic_target_argmax(self.drafts, pat, self.cfg.vocab)          # the (synthetic) target
+        df.dflash_verify_greedy(self.drafts, y, self.tau, self.out, self.next_anchor)
+        self.anchor.copy_(self.next_anchor)
+        self.i += 1
+
+
+def run_gpu(args, rank, world, local):
+    import block_diffusion_drafter_dflash_gb300 as df
+    torch.cuda.set_device(local)
+    wl = workloads()[args.workload]
+    W, K = args.warmup, args.steps
+    total = 3 * (W + K) + 4
+    cyc = Cycle(wl, total, rank)
+    dist = world > 1 and torch.distributed.is_initialized()
+
+    def barrier():
+        if dist:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+
+    for _ in range(W):
+        cyc.step()
+    barrier()
+    clocks = Clocks(local)
+    clocks.start()
+    n0 = df.dflash_launch_count()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    t0.record()
+    for _ in range(K):
+        cyc.step()
+    t1.record()
+    barrier()
+    launches = df.dflash_launch_count() - n0
+    clk = clocks.stop()
+    ms = t0.elapsed_time(t1) / K
+    if dist:
+        tt = torch.tensor([ms], device="cuda")
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        ms = float(tt.item())
+    drafted = wl.batch * (wl.block - 1)
+    value = world * drafted / (ms / 1e3)
+
+    # profiled pass: CUDA events around each launch, per stage
+    df.dflash_profile_start(cyc.model, 8192)
+    for _ in range(K):
+        cyc.step()
+    prof = df.dflash_profile_stop(cyc.model)
+    gb = gemm_bytes_per_cycle(wl.cfg, wl.batch, wl.block, cyc.rows)
+    gemm_ms = sum(prof[s][0] for s in GEMM_STAGES) / K
+    gemm_bytes = sum(gb.values())
+    hbm, bf16, src = load_peaks()
+    achieved = gemm_bytes / (gemm_ms / 1e3) / 1e9
+    roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
+                "frac": round(achieved / hbm, 4), "traffic": None,
+                "kernel": "projection GEMMs (all launches of one cycle)", "peak_source": src,
+                "algorithmic_bytes_per_cycle": gemm_bytes, "kernel_ms_per_cycle": round(gemm_ms, 4)}
+    stages = {s: {"ms_per_cycle": round(v[0] / K, 4), "launches_per_cycle": v[1] / K} for s, v in prof.items()}
+    cycle_roof_ms = (gemm_bytes + kv_bytes(wl)) / (hbm * 1e9) * 1e3
+
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(cyc, K, wl, barrier, world)
+
+    result = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": K, "warmup": W,
+        "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": wl.cfg.dtype, "data": "synthetic (seeded N(0,0.02) weights, N(0,1) target features, "
+                                       "seeded target agreement)",
+        "config": {"workload": wl.name, "drafter": wl.cfg.name, "batch_per_gpu": wl.batch, "block": wl.block,
+                   "ctx": wl.ctx if len(wl.ctx) <= 4 else f"{min(wl.ctx)}..{max(wl.ctx)} ({len(wl.ctx)} requests)",
+                   "l2": "inputs larger than L2 (weights streamed every cycle)",
+                   "mean_tau": None, "cycle_roofline_ms": round(cycle_roof_ms, 4),
+                   "cycle_frac_of_hbm_roofline": round(cycle_roof_ms / ms, 4)},
+        "roofline": roofline, "stages": stages, "gpu_launches": int(launches), "clocks": clk, "e2e": e2e,
+    }
+    return result, cyc
+
+
+def kv_bytes(wl) -> int:
+    c = wl.cfg
+    return 2 * c.layers * c.n_kv_heads * c.head_dim * c.elem_bytes * sum(wl.ctx)
+
+
+def run_e2e(cyc, K, wl, barrier, world):
+    """Same cycle through the public API with the step's inputs copied from
+    pinned host memory and its results read back every step."""
+    cfg = wl.cfg
+    feats_h = cyc.feat_pool[0].cpu().pin_memory()
+    feats_d = torch.empty_like(cyc.feat_pool[0])
+    pats_h = [(p.match.cpu().pin_memory(), p.off.cpu().pin_memory(), p.bonus.cpu().pin_memory())
+              for p in cyc.patterns[:8]]
+    p0 = cyc.patterns[0]
+    pat_d = type(p0)(match=torch.empty_like(p0.match), off=torch.empty_like(p0.off), bonus=torch.empty_like(p0.bonus))
+    out_h = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in (cyc.drafts, cyc.tau, cyc.out, cyc.next_anchor)]
+    h2d = feats_h.numel() * feats_h.element_size() + sum(sum(t.numel() * t.element_size() for t in p)
+                                                          for p in pats_h[:1])
+    d2h = sum(t.numel() * t.element_size() for t in out_h)
+    barrier()
+    t0 = time.perf_counter()
+    for i in range(K):
+        feats_d.copy_(feats_h, non_blocking=True)
+        m, o, b = pats_h[i % len(pats_h)]
+        pat_d.match.copy_(m, non_blocking=True)
+        pat_d.off.copy_(o, non_blocking=True)
+        pat_d.bonus.copy_(b, non_blocking=True)
+        cyc.step(feats=feats_d, pattern=pat_d)
+        for h, d in zip(out_h, (cyc.drafts, cyc.tau, cyc.out, cyc.next_anchor)):
+            h.copy_(d, non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+    barrier()
+    ms = (time.perf_counter() - t0) * 1e3 / K
+    if world > 1 and torch.distributed.is_initialized():
+        tt = torch.tensor([ms], device="cuda")
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        ms = float(tt.item())
+    return {"value": round(world * wl.batch * (wl.block - 1) / (ms / 1e3), 2), "unit": UNIT,
+            "ms_per_step": round(ms, 4), "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+
+
+# ---------------------------------------------------------------- the oracle (CPU)
+def cores_used() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+class OracleCycle:
+    """The CPU oracle on one request of the workload (context injected once,
+    then whole cycles: inject tau tokens, draft, argmax, verify)."""
+
+    def __init__(self, wl, weights_gpu=None):
+        import oracle
+        self.o = oracle
+        self.wl, self.cfg = wl, wl.cfg
+        w = weights_gpu if weights_gpu is not None else make_weights(wl.cfg, wl.seed, device="cuda")
+        self.hw = oracle.weights_to_host(w)
+        self.cache = oracle.RequestCache(self.cfg.layers, self.cfg.n_kv_heads, self.cfg.head_dim)
+        ctx = wl.ctx[0]
+        feats = make_features(self.cfg, ctx, seed=wl.seed + 17, device="cuda").cpu()
+        for s in range(0, ctx, 4096):
+            oracle.inject_context(self.hw, self.cfg, self.cache, feats[s:s + 4096])
+        self.tau = wl.first_inject
+        self.anchor = int(make_tokens(self.cfg, 1, seed=wl.seed + 3).item())
+        self.new = make_features(self.cfg, wl.block, seed=wl.seed + 999).cpu()
+        self.i = 0
+
+    def step(self):
+        o, wl = self.o, self.wl
+        r = o.draft_cycle(self.hw, self.cfg, self.cache, self.new[:self.tau], self.anchor, wl.block)
+        pat = make_agreement(self.cfg, 1, wl.block, wl.accept_p[:1], seed=seed_for(wl, self.i, 5))
+        y = synthetic_target_argmax(torch.tensor(r["drafts"], dtype=torch.int32).reshape(1, -1), pat, self.cfg.vocab)
+        tau, _, nxt = o.verify_greedy(r["drafts"], y[0].tolist())
+        self.tau, self.anchor = tau, nxt
+        self.i += 1
+
+
+def cpu_baseline(wl, weights_gpu=None, budget_s: float = 25.0):
+    oc = OracleCycle(wl, weights_gpu)
+    t0 = time.perf_counter()
+    n = 0
+    while True:
+        oc.step()
+        n += 1
+        if time.perf_counter() - t0 > budget_s * 0.5 or n >= 3:
+            break
+    dt = (time.perf_counter() - t0) / n
+    return {"value": round((wl.block - 1) / dt, 4), "unit": UNIT, "cores": cores_used(), "kind": "oracle",
+            "sample": f"{n} whole cycle(s) of request 0 of workload {wl.name} (context {wl.ctx[0]} injected "
+                      f"beforehand, untimed); float64 numpy, BLAS threads on all cores", "s_per_cycle": round(dt, 3)}
+
+
+def run_reference(args, rank, world, local):
+    if rank != 0:
+        return None
+    if torch.cuda.is_available():
+        torch.cuda.set_device(local)
+    wl = workloads()[args.workload]
+    oc = OracleCycle(wl, None)
+    for _ in range(args.warmup):
+        oc.step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oc.step()
+    dt = (time.perf_counter() - t0) / args.steps
+    value = (wl.block - 1) / dt
+    sample = (f"each step one whole cycle of request 0 of workload {wl.name} "
+              f"({'all' if wl.batch == 1 else f'1 of {wl.batch}'} requests)")
+    return {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 2), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": wl.name, "drafter": wl.cfg.name, "batch_per_gpu": wl.batch, "block": wl.block},
+            "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": cores_used(), "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    args = parse()
+    rank, world, local = dist_env()
+    if world > 1 and not torch.distributed.is_initialized():
+        backend = "nccl" if args.impl == "dflash" else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        torch.distributed.init_process_group(backend)
+    if args.impl == "reference":
+        res = run_reference(args, rank, world, local)
+    else:
+        res, cyc = run_gpu(args, rank, world, local)
+        if rank == 0 and not args.no_cpu_baseline:
+            res["cpu_baseline"] = cpu_baseline(workloads()[args.workload], cyc.weights)
+    if rank == 0 and res is not None:
+        print(json.dumps(res), flush=True)
+    if world > 1 and torch.distributed.is_initialized():
+        torch.distributed.barrier()
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,225 @@
+"""GB300 (sm_103a) DFlash draft cycle: thin Python binding over the C ABI.
+
+The functions below carry the C ABI's names and only marshal arguments (torch
+tensors -> device pointers, the current torch stream -> cudaStream_t); every
+step of the cycle — context fusion, K/V injection, the non-causal drafter
+pass, the LM head argmax and greedy verification — runs in the CUDA library
+``libdflash_gb300.so`` built from ``csrc/``.  There is no CPU fallback: if the
+library is missing, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+from typing import Optional
+
+import torch
+
+from . import _abi
+from ._abi import DFlashError, check, lib
+
+__all__ = ["DFlashError", "Model", "Cache", "lib", "dflash_model_create", "dflash_cache_init",
+           "dflash_workspace_bytes", "dflash_workspace", "dflash_inject_context", "dflash_draft_block",
+           "dflash_verify_greedy", "dflash_get_status", "dflash_clear_status", "dflash_version",
+           "dflash_launch_count", "dflash_profile_start", "dflash_profile_stop"]
+
+
+def _stream_ptr(stream: Optional[torch.cuda.Stream]) -> ctypes.c_void_p:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("expected a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError("expected a contiguous tensor")
+    return t.data_ptr()
+
+
+def _config_struct(cfg) -> _abi.Config:
+    mask = cfg.mask_id if hasattr(cfg, "mask_id") else cfg.mask_token_id
+    return _abi.Config(hidden=cfg.hidden, layers=cfg.layers, n_q_heads=cfg.n_q_heads, n_kv_heads=cfg.n_kv_heads,
+                       head_dim=cfg.head_dim, ffn=cfg.ffn, vocab=cfg.vocab, n_target_feats=cfg.n_target_feats,
+                       max_block=cfg.max_block, rope_theta=float(cfg.rope_theta), rms_eps=float(cfg.rms_eps),
+                       mask_token_id=int(mask), dtype=_abi.DTYPE_F32 if cfg.dtype == "fp32" else _abi.DTYPE_BF16)
+
+
+def dflash_version() -> int:
+    return lib().dflash_version()
+
+
+class Model:
+    """A created dflash_model; keeps the borrowed weight tensors alive."""
+
+    def __init__(self, cfg, weights: dict):
+        self.cfg = cfg
+        self.weights = weights
+        self.dtype = torch.float32 if cfg.dtype == "fp32" else torch.bfloat16
+        tensors = [weights[k] for k in ("embed", "lm_head", "w_c", "g_c", "g_final")]
+        for lw in weights["layers"]:
+            tensors += list(lw.values())
+        for t in tensors:
+            if t.dtype != self.dtype or not t.is_cuda or not t.is_contiguous():
+                raise ValueError("weights must be contiguous CUDA tensors of the model dtype")
+        self._layers = (_abi.LayerWeights * cfg.layers)(*[
+            _abi.LayerWeights(**{k: lw[k].data_ptr() for k in ("g_in", "w_q", "w_k", "w_v", "w_o", "g_post",
+                                                                "w_g", "w_u", "w_d")})
+            for lw in weights["layers"]])
+        w = _abi.Weights(embed=weights["embed"].data_ptr(), lm_head=weights["lm_head"].data_ptr(),
+                         w_c=weights["w_c"].data_ptr(), g_c=weights["g_c"].data_ptr(),
+                         g_final=weights["g_final"].data_ptr(), layers=self._layers)
+        self._cfg = _config_struct(cfg)
+        h = ctypes.c_void_p()
+        check(lib().dflash_model_create(ctypes.byref(self._cfg), ctypes.byref(w), ctypes.byref(h)),
+              "dflash_model_create")
+        self.handle = h
+
+    def close(self):
+        if getattr(self, "handle", None) is not None and self.handle.value:
+            lib().dflash_model_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+class Cache:
+    """A dflash_cache carved out of a torch-owned device buffer."""
+
+    def __init__(self, model: Model, batch: int, capacity: int, stream=None):
+        self.model, self.batch, self.capacity = model, batch, capacity
+        nbytes = lib().dflash_cache_bytes(ctypes.byref(model._cfg), batch, capacity)
+        if nbytes == 0:
+            raise ValueError("invalid cache shape")
+        self.buffer = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+        h = ctypes.c_void_p()
+        check(lib().dflash_cache_init(model.handle, self.buffer.data_ptr(), nbytes, batch, capacity,
+                                      _stream_ptr(stream), ctypes.byref(h)), "dflash_cache_init")
+        self.handle = h
+        k, v, ln = ctypes.c_size_t(), ctypes.c_size_t(), ctypes.c_size_t()
+        check(lib().dflash_cache_layout(h, ctypes.byref(k), ctypes.byref(v), ctypes.byref(ln)), "dflash_cache_layout")
+        self.k_off, self.v_off, self.len_off = k.value, v.value, ln.value
+
+    def _kv_view(self, off: int) -> torch.Tensor:
+        c = self.model.cfg
+        es = self.model.dtype.itemsize
+        n = self.batch * c.layers * c.n_kv_heads * self.capacity * c.head_dim
+        return self.buffer[off:off + n * es].view(self.model.dtype).view(
+            self.batch, c.layers, c.n_kv_heads, self.capacity, c.head_dim)
+
+    def k(self) -> torch.Tensor:
+        """View [batch][layers][n_kv_heads][capacity][head_dim] of the context keys."""
+        return self._kv_view(self.k_off)
+
+    def v(self) -> torch.Tensor:
+        return self._kv_view(self.v_off)
+
+    def ctx_len(self) -> torch.Tensor:
+        return self.buffer[self.len_off:self.len_off + 4 * self.batch].view(torch.int32)
+
+    def set_lengths(self, lengths, stream=None):
+        arr = (ctypes.c_int32 * self.batch)(*[int(v) for v in lengths])
+        check(lib().dflash_cache_set_lengths(self.handle, arr, _stream_ptr(stream)), "dflash_cache_set_lengths")
+
+    def close(self):
+        if getattr(self, "handle", None) is not None and self.handle.value:
+            lib().dflash_cache_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def dflash_model_create(cfg, weights: dict) -> Model:
+    return Model(cfg, weights)
+
+
+def dflash_cache_init(model: Model, batch: int, capacity: int, stream=None) -> Cache:
+    return Cache(model, batch, capacity, stream)
+
+
+def dflash_workspace_bytes(model: Model, batch: int, capacity: int, block_size: int, max_inject_rows: int) -> int:
+    return int(lib().dflash_workspace_bytes(model.handle, batch, capacity, block_size, max_inject_rows))
+
+
+def dflash_workspace(model: Model, batch: int, capacity: int, block_size: int, max_inject_rows: int) -> torch.Tensor:
+    n = dflash_workspace_bytes(model, batch, capacity, block_size, max_inject_rows)
+    if n == 0:
+        raise ValueError("invalid workspace shape")
+    return torch.empty(n, dtype=torch.uint8, device="cuda")
+
+
+def dflash_inject_context(model: Model, cache: Cache, feats: torch.Tensor, n_new_dev: torch.Tensor,
+                          n_new_host=None, max_rows: Optional[int] = None, workspace: torch.Tensor = None,
+                          stream=None) -> None:
+    """feats [max_rows, m, D] (model dtype), n_new_dev int32 [batch] on the device."""
+    if n_new_dev.dtype != torch.int32 or feats.dtype != model.dtype:
+        raise ValueError("n_new_dev must be int32 and feats of the model dtype")
+    rows = feats.shape[0] if max_rows is None else int(max_rows)
+    host = None
+    if n_new_host is not None:
+        host = (ctypes.c_int32 * cache.batch)(*[int(v) for v in n_new_host])
+    check(lib().dflash_inject_context(model.handle, cache.handle, _ptr(feats), _ptr(n_new_dev), host, rows,
+                                      _ptr(workspace), workspace.numel(), _stream_ptr(stream)),
+          "dflash_inject_context")
+
+
+def dflash_draft_block(model: Model, cache: Cache, anchor_dev: torch.Tensor, block_size: int,
+                       draft_dev: torch.Tensor, logits_dev: Optional[torch.Tensor] = None,
+                       workspace: torch.Tensor = None, stream=None) -> None:
+    """anchor_dev int32 [batch]; draft_dev int32 [batch, block-1]; logits_dev fp32 [batch, block-1, V] or None."""
+    if anchor_dev.dtype != torch.int32 or draft_dev.dtype != torch.int32:
+        raise ValueError("anchor_dev and draft_dev must be int32")
+    if logits_dev is not None and logits_dev.dtype != torch.float32:
+        raise ValueError("logits_dev must be float32")
+    check(lib().dflash_draft_block(model.handle, cache.handle, _ptr(anchor_dev), int(block_size), _ptr(draft_dev),
+                                   _ptr(logits_dev), _ptr(workspace), workspace.numel(), _stream_ptr(stream)),
+          "dflash_draft_block")
+
+
+def dflash_verify_greedy(draft_dev: torch.Tensor, target_argmax_dev: torch.Tensor, accept_len_dev: torch.Tensor,
+                         out_tokens_dev: torch.Tensor, next_anchor_dev: torch.Tensor, stream=None) -> None:
+    """draft int32 [B, g-1], target int32 [B, g] -> tau [B], out [B, g], next anchor [B] (all int32)."""
+    B, g = target_argmax_dev.shape
+    for t in (draft_dev, target_argmax_dev, accept_len_dev, out_tokens_dev, next_anchor_dev):
+        if t.dtype != torch.int32:
+            raise ValueError("verify tensors must be int32")
+    check(lib().dflash_verify_greedy(_ptr(draft_dev), _ptr(target_argmax_dev), B, g, _ptr(accept_len_dev),
+                                     _ptr(out_tokens_dev), _ptr(next_anchor_dev), _stream_ptr(stream)),
+          "dflash_verify_greedy")
+
+
+def dflash_get_status(model: Model, stream=None) -> int:
+    st = ctypes.c_int32(0)
+    check(lib().dflash_get_status(model.handle, _stream_ptr(stream), ctypes.byref(st)), "dflash_get_status")
+    return st.value
+
+
+def dflash_clear_status(model: Model, stream=None) -> None:
+    check(lib().dflash_clear_status(model.handle, _stream_ptr(stream)), "dflash_clear_status")
+
+
+def dflash_launch_count() -> int:
+    """Kernel launches made by the library in this process."""
+    return int(lib().dflash_launch_count())
+
+
+def dflash_profile_start(model: Model, max_launches: int = 4096) -> None:
+    check(lib().dflash_profile_start(model.handle, int(max_launches)), "dflash_profile_start")
+
+
+def dflash_profile_stop(model: Model, stream=None) -> dict:
+    """{stage: (milliseconds, launches)} recorded since dflash_profile_start."""
+    n = len(_abi.STAGES)
+    ms = (ctypes.c_float * n)()
+    cnt = (ctypes.c_int32 * n)()
+    check(lib().dflash_profile_stop(model.handle, _stream_ptr(stream), ms, cnt, n), "dflash_profile_stop")
+    return {name: (float(ms[i]), int(cnt[i])) for i, name in enumerate(_abi.STAGES)}

@@ -1,0 +1,597 @@
+// C ABI of the DFlash draft-cycle library: argument checks, memory plans and
+// the launch sequence of each stage.  Every step of the cycle runs in the
+// kernels of this library; this file only validates and orders launches.
+#include <algorithm>
+#include <atomic>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "gemm.cuh"
+#include "kernels.cuh"
+
+using namespace dflash;
+
+namespace {
+// CUDA event pairs around each launch while profiling is on.
+struct Profiler {
+  bool on = false;
+  int used = 0;                    // events used so far (2 per launch)
+  std::vector<cudaEvent_t> ev;
+  std::vector<int> stage;          // stage of each recorded launch
+};
+std::atomic<uint64_t> g_launch_count{0};
+}  // namespace
+
+struct dflash_model {
+  dflash_config cfg;
+  const void* embed;
+  const void* lm_head;
+  const void* w_c;
+  const void* g_c;
+  const void* g_final;
+  std::vector<dflash_layer_weights> layers;
+  int device;
+  int sms;
+  int32_t* status_dev;     // device status word (first device-detected error)
+  double* inv_freq_dev;    // RoPE frequencies theta^(-2i/hd), i < hd/2
+  Profiler prof;
+};
+
+struct dflash_cache {
+  const dflash_model* model;
+  char* base;
+  size_t bytes;
+  int batch;
+  int cap;
+  size_t k_off, v_off, len_off;
+  std::vector<int32_t> len_host;  // host mirror of ctx_len, exact while len_known
+  bool len_known;
+};
+
+namespace {
+
+thread_local std::string g_last_error;
+
+int32_t fail(int32_t code, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return code;
+}
+
+int32_t cuda_fail(cudaError_t e, const char* what) {
+  return fail(DFLASH_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+#define DF_CUDA(call, what)                              \
+  do {                                                   \
+    cudaError_t e_ = (call);                             \
+    if (e_ != cudaSuccess) return cuda_fail(e_, what);   \
+  } while (0)
+
+// Launch `call` (which makes `kernels` kernel launches) for profiler stage
+// `stage`, with an event pair around it while profiling is on.
+#define DF_LAUNCH(stg, kernels, call, what)                                         \
+  do {                                                                                \
+    Profiler& pr_ = const_cast<dflash_model*>(m)->prof;                               \
+    const bool rec_ = pr_.on && pr_.used + 2 <= (int)pr_.ev.size();                   \
+    if (rec_) DF_CUDA(cudaEventRecord(pr_.ev[pr_.used], s), "profiler event");        \
+    DF_CUDA((call), what);                                                            \
+    g_launch_count += (kernels);                                                      \
+    if (rec_) {                                                                       \
+      DF_CUDA(cudaEventRecord(pr_.ev[pr_.used + 1], s), "profiler event");            \
+      pr_.stage.push_back(stg);                                                       \
+      pr_.used += 2;                                                                  \
+    }                                                                                 \
+  } while (0)
+
+size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
+
+int32_t check_config(const dflash_config* c) {
+  if (!c) return fail(DFLASH_ERR_INVALID_ARG, "config is NULL");
+  if (c->dtype != DFLASH_DTYPE_F32 && c->dtype != DFLASH_DTYPE_BF16)
+    return fail(DFLASH_ERR_INVALID_ARG, "dtype %d is not DFLASH_DTYPE_F32 or DFLASH_DTYPE_BF16", c->dtype);
+  if (c->hidden <= 0 || c->hidden % kTileN) return fail(DFLASH_ERR_SHAPE, "hidden %d must be a positive multiple of 128", c->hidden);
+  if (c->layers <= 0 || c->layers > kMaxSeg / 2) return fail(DFLASH_ERR_SHAPE, "layers %d must be in [1, %d]", c->layers, kMaxSeg / 2);
+  if (c->head_dim != 64 && c->head_dim != 128) return fail(DFLASH_ERR_SHAPE, "head_dim %d must be 64 or 128", c->head_dim);
+  if (c->n_q_heads <= 0 || c->n_kv_heads <= 0 || c->n_q_heads % c->n_kv_heads)
+    return fail(DFLASH_ERR_SHAPE, "n_q_heads %d must be a positive multiple of n_kv_heads %d", c->n_q_heads, c->n_kv_heads);
+  if ((c->n_q_heads * c->head_dim) % kTileN || (c->n_kv_heads * c->head_dim) % kTileN)
+    return fail(DFLASH_ERR_SHAPE, "n_q_heads*head_dim and n_kv_heads*head_dim must be multiples of 128");
+  if (c->ffn <= 0 || c->ffn % kHalfN) return fail(DFLASH_ERR_SHAPE, "ffn %d must be a positive multiple of 64", c->ffn);
+  if (c->vocab <= 0 || c->vocab % kTileN) return fail(DFLASH_ERR_SHAPE, "vocab %d must be a positive multiple of 128", c->vocab);
+  if (c->n_target_feats < 1 || c->n_target_feats > 8) return fail(DFLASH_ERR_SHAPE, "n_target_feats %d must be in [1, 8]", c->n_target_feats);
+  if (c->max_block < 1 || c->max_block > kMaxBlock) return fail(DFLASH_ERR_SHAPE, "max_block %d must be in [1, %d]", c->max_block, kMaxBlock);
+  if ((c->n_q_heads / c->n_kv_heads) * c->max_block > attention_max_rows())
+    return fail(DFLASH_ERR_SHAPE, "(n_q_heads/n_kv_heads)*max_block must be <= %d", attention_max_rows());
+  if (c->mask_token_id < 0 || c->mask_token_id >= c->vocab) return fail(DFLASH_ERR_INVALID_ARG, "mask_token_id %d out of [0, vocab)", c->mask_token_id);
+  if (!(c->rope_theta > 1.0f) || !(c->rms_eps >= 0.0f)) return fail(DFLASH_ERR_INVALID_ARG, "rope_theta must be > 1 and rms_eps >= 0");
+  return DFLASH_OK;
+}
+
+int32_t check_device(const dflash_model* m) {
+  int dev = -1;
+  DF_CUDA(cudaGetDevice(&dev), "cudaGetDevice");
+  if (dev != m->device) return fail(DFLASH_ERR_INVALID_ARG, "current device %d is not the model's device %d", dev, m->device);
+  return DFLASH_OK;
+}
+
+// ---------------------------------------------------------------- workspace plan
+struct WsPlan {
+  size_t total;
+  size_t rowinfo, yf, ht;                                      // injection
+  size_t x, u, q, kb, vb, opart, ml, o, a, hm, slots;          // drafter
+  size_t partial, counters;                                    // split-K scratch
+  int counters_n;
+  int attn_splits, attn_chunk;
+  GemmPlan g_fuse, g_inject, g_qkv, g_o, g_gu, g_down, g_lm;
+};
+
+// One call's scratch: the injection part when max_rows > 0, the drafter part
+// when block > 0.  Each call lays out only its own regions from offset 0, so a
+// single workspace of max(inject, draft) bytes serves both on one stream.
+WsPlan plan_ws(const dflash_model* m, int B, int cap, int block, int max_rows) {
+  const dflash_config& c = m->cfg;
+  const size_t es = c.dtype == DFLASH_DTYPE_F32 ? 4 : 2;
+  const int D = c.hidden, hq = c.n_q_heads * c.head_dim, hk = c.n_kv_heads * c.head_dim, F = c.ffn;
+  const int R = B * block, Rm = B * std::max(block - 1, 0);
+  WsPlan p{};
+  std::vector<const GemmPlan*> used;
+  if (max_rows > 0) {
+    p.g_fuse = plan_gemm(c.dtype, max_rows, c.n_target_feats * D, D / kTileN, m->sms);
+    p.g_inject = plan_gemm(c.dtype, max_rows, D, c.layers * 2 * (hk / kTileN), m->sms);
+    used = {&p.g_fuse, &p.g_inject};
+  }
+  if (block > 0) {
+    p.g_qkv = plan_gemm(c.dtype, R, D, (hq + 2 * hk) / kTileN, m->sms);
+    p.g_o = plan_gemm(c.dtype, R, hq, D / kTileN, m->sms);
+    p.g_gu = plan_gemm(c.dtype, R, D, F / kHalfN, m->sms);
+    p.g_down = plan_gemm(c.dtype, R, F, D / kTileN, m->sms);
+    p.g_lm = plan_gemm(c.dtype, std::max(Rm, 1), D, c.vocab / kTileN, m->sms);
+    used.insert(used.end(), {&p.g_qkv, &p.g_o, &p.g_gu, &p.g_down, &p.g_lm});
+  }
+  size_t partial = 0;
+  int counters = 0;
+  for (const GemmPlan* g : used) {
+    partial = std::max(partial, g->partial_floats);
+    counters = std::max(counters, g->counters);
+  }
+  size_t off = 0;
+  auto take = [&](size_t bytes) { size_t o = off; off += align256(std::max<size_t>(bytes, 1)); return o; };
+  if (max_rows > 0) {
+    p.rowinfo = take(sizeof(int2) * (size_t)max_rows);
+    p.yf = take(sizeof(float) * (size_t)max_rows * D);
+    p.ht = take(es * (size_t)max_rows * D);
+  }
+  if (block > 0) {
+    // attention splits: enough CTAs to cover the device twice over
+    const int keys = cap + block;
+    const int groups = std::max(1, B * c.n_kv_heads);
+    const int want = std::max(1, (2 * m->sms + groups - 1) / groups);
+    int chunk = (keys + want - 1) / want;
+    chunk = std::max(64, (chunk + 31) / 32 * 32);
+    p.attn_chunk = chunk;
+    p.attn_splits = (keys + chunk - 1) / chunk;
+    p.x = take(sizeof(float) * (size_t)R * D);
+    p.u = take(es * (size_t)R * D);
+    p.q = take(es * (size_t)R * hq);
+    p.kb = take(es * (size_t)R * hk);
+    p.vb = take(es * (size_t)R * hk);
+    p.opart = take(sizeof(float) * (size_t)B * c.n_q_heads * block * p.attn_splits * c.head_dim);
+    p.ml = take(sizeof(float2) * (size_t)B * c.n_q_heads * block * p.attn_splits);
+    p.o = take(es * (size_t)R * hq);
+    p.a = take(es * (size_t)R * F);
+    p.hm = take(es * (size_t)std::max(Rm, 1) * D);
+    p.slots = take(sizeof(unsigned long long) * (size_t)std::max(Rm, 1));
+  }
+  p.partial = take(sizeof(float) * partial);
+  p.counters = take(sizeof(int) * (size_t)counters);
+  p.counters_n = counters;
+  p.total = off;
+  return p;
+}
+
+GemmProblem make_problem(const void* x, int ldx, int M, int K) {
+  GemmProblem p{};
+  p.x = x;
+  p.ldx = ldx;
+  p.M = M;
+  p.K = K;
+  return p;
+}
+
+void add_seg(GemmProblem& p, const void* w0, const void* w1, int tiles, int paired, int tag) {
+  GemmSeg& s = p.seg[p.nseg++];
+  s.w0 = w0;
+  s.w1 = w1;
+  s.tiles = tiles;
+  s.tile_begin = p.total_tiles;
+  s.paired = paired;
+  s.tag = tag;
+  p.total_tiles += tiles;
+}
+
+template <typename T>
+int32_t run_inject(const dflash_model* m, dflash_cache* cache, const void* feats, const int32_t* n_new, int max_rows,
+                   char* ws, const WsPlan& P, cudaStream_t s) {
+  const dflash_config& c = m->cfg;
+  const int D = c.hidden, hk = c.n_kv_heads * c.head_dim;
+  int2* rowinfo = reinterpret_cast<int2*>(ws + P.rowinfo);
+  float* yf = reinterpret_cast<float*>(ws + P.yf);
+  T* ht = reinterpret_cast<T*>(ws + P.ht);
+  float* partial = reinterpret_cast<float*>(ws + P.partial);
+  int* counters = reinterpret_cast<int*>(ws + P.counters);
+  int32_t* ctx_len = reinterpret_cast<int32_t*>(cache->base + cache->len_off);
+
+  DF_LAUNCH(DFLASH_STAGE_OTHER, 1,
+            inject_prep_launch(n_new, ctx_len, cache->batch, max_rows, cache->cap, rowinfo, counters, P.counters_n,
+                               m->status_dev, s), "inject_prep");
+  GemmProblem pf = make_problem(feats, c.n_target_feats * D, max_rows, c.n_target_feats * D);
+  add_seg(pf, m->w_c, m->w_c, D / kTileN, 0, 0);
+  apply_plan(pf, P.g_fuse, partial, counters);
+  DF_LAUNCH(DFLASH_STAGE_FUSE, 1, (gemm_launch<T, EpiStoreF32>(pf, P.g_fuse, EpiStoreF32{yf, D}, s)), "fusion GEMM");
+  DF_LAUNCH(DFLASH_STAGE_OTHER, 1,
+            fuse_norm_launch<T>(yf, static_cast<const T*>(m->g_c), c.rms_eps, rowinfo, max_rows, D, ht, s),
+            "fusion norm");
+
+  GemmProblem pi = make_problem(ht, D, max_rows, D);
+  for (int l = 0; l < c.layers; ++l) {
+    add_seg(pi, m->layers[l].w_k, m->layers[l].w_k, hk / kTileN, 0, 2 * l);
+    add_seg(pi, m->layers[l].w_v, m->layers[l].w_v, hk / kTileN, 0, 2 * l + 1);
+  }
+  apply_plan(pi, P.g_inject, partial, counters);
+  EpiInject<T> ei{reinterpret_cast<T*>(cache->base + cache->k_off), reinterpret_cast<T*>(cache->base + cache->v_off),
+                  rowinfo, m->inv_freq_dev, c.layers, c.n_kv_heads, c.head_dim, cache->cap};
+  DF_LAUNCH(DFLASH_STAGE_INJECT, 1, (gemm_launch<T, EpiInject<T>>(pi, P.g_inject, ei, s)), "injection GEMM");
+  return DFLASH_OK;
+}
+
+template <typename T>
+int32_t run_draft(const dflash_model* m, const dflash_cache* cache, const int32_t* anchor, int block, int32_t* drafts,
+                  float* logits, char* ws, const WsPlan& P, cudaStream_t s) {
+  const dflash_config& c = m->cfg;
+  const int B = cache->batch, D = c.hidden, F = c.ffn;
+  const int hq = c.n_q_heads * c.head_dim, hk = c.n_kv_heads * c.head_dim;
+  const int R = B * block, Rm = B * (block - 1);
+  float* x = reinterpret_cast<float*>(ws + P.x);
+  T* u = reinterpret_cast<T*>(ws + P.u);
+  T* q = reinterpret_cast<T*>(ws + P.q);
+  T* kb = reinterpret_cast<T*>(ws + P.kb);
+  T* vb = reinterpret_cast<T*>(ws + P.vb);
+  T* o = reinterpret_cast<T*>(ws + P.o);
+  T* a = reinterpret_cast<T*>(ws + P.a);
+  T* hm = reinterpret_cast<T*>(ws + P.hm);
+  unsigned long long* slots = reinterpret_cast<unsigned long long*>(ws + P.slots);
+  float* partial = reinterpret_cast<float*>(ws + P.partial);
+  int* counters = reinterpret_cast<int*>(ws + P.counters);
+  const int32_t* ctx_len = reinterpret_cast<const int32_t*>(cache->base + cache->len_off);
+
+  DF_LAUNCH(DFLASH_STAGE_OTHER, 1, embed_norm_launch<T>(static_cast<const T*>(m->embed), anchor, c.mask_token_id, c.vocab, B, block, D,
+                               static_cast<const T*>(m->layers[0].g_in), c.rms_eps, x, u, counters, P.counters_n,
+                               m->status_dev, s),
+          "embedding");
+  for (int l = 0; l < c.layers; ++l) {
+    const dflash_layer_weights& L = m->layers[l];
+    GemmProblem pq = make_problem(u, D, R, D);
+    add_seg(pq, L.w_q, L.w_q, hq / kTileN, 0, 0);
+    add_seg(pq, L.w_k, L.w_k, hk / kTileN, 0, 1);
+    add_seg(pq, L.w_v, L.w_v, hk / kTileN, 0, 2);
+    apply_plan(pq, P.g_qkv, partial, counters);
+    EpiQKV<T> eq{q, kb, vb, ctx_len, m->inv_freq_dev, block, c.n_q_heads, c.n_kv_heads, c.head_dim};
+    DF_LAUNCH(DFLASH_STAGE_QKV, 1, (gemm_launch<T, EpiQKV<T>>(pq, P.g_qkv, eq, s)), "QKV GEMM");
+
+    AttnParams ap{};
+    ap.q = q; ap.kb = kb; ap.vb = vb;
+    ap.kc = cache->base + cache->k_off;
+    ap.vc = cache->base + cache->v_off;
+    ap.ctx_len = ctx_len;
+    ap.layer = l; ap.layers = c.layers; ap.cap = cache->cap;
+    ap.B = B; ap.nq = c.n_q_heads; ap.nkv = c.n_kv_heads; ap.hd = c.head_dim; ap.block = block;
+    ap.chunk = P.attn_chunk; ap.splits = P.attn_splits;
+    ap.opart = reinterpret_cast<float*>(ws + P.opart);
+    ap.ml = reinterpret_cast<float2*>(ws + P.ml);
+    ap.out = o;
+    ap.scale = 1.0f / sqrtf((float)c.head_dim);
+    DF_LAUNCH(DFLASH_STAGE_ATTN, 2, attention_launch<T>(ap, s), "attention");
+
+    GemmProblem po = make_problem(o, hq, R, hq);
+    add_seg(po, L.w_o, L.w_o, D / kTileN, 0, 0);
+    apply_plan(po, P.g_o, partial, counters);
+    DF_LAUNCH(DFLASH_STAGE_O, 1, (gemm_launch<T, EpiResidual>(po, P.g_o, EpiResidual{x, D}, s)), "O GEMM");
+    DF_LAUNCH(DFLASH_STAGE_OTHER, 1, rmsnorm_launch<T>(x, static_cast<const T*>(L.g_post), c.rms_eps, R, D, u, s),
+              "post-attention norm");
+
+    GemmProblem pg = make_problem(u, D, R, D);
+    add_seg(pg, L.w_g, L.w_u, F / kHalfN, 1, 0);
+    apply_plan(pg, P.g_gu, partial, counters);
+    DF_LAUNCH(DFLASH_STAGE_GATEUP, 1, (gemm_launch<T, EpiSwiGLU<T>>(pg, P.g_gu, EpiSwiGLU<T>{a, F}, s)),
+              "gate/up GEMM");
+
+    GemmProblem pd = make_problem(a, F, R, F);
+    add_seg(pd, L.w_d, L.w_d, D / kTileN, 0, 0);
+    apply_plan(pd, P.g_down, partial, counters);
+    DF_LAUNCH(DFLASH_STAGE_DOWN, 1, (gemm_launch<T, EpiResidual>(pd, P.g_down, EpiResidual{x, D}, s)), "down GEMM");
+    if (l + 1 < c.layers)
+      DF_LAUNCH(DFLASH_STAGE_OTHER, 1,
+                rmsnorm_launch<T>(x, static_cast<const T*>(m->layers[l + 1].g_in), c.rms_eps, R, D, u, s),
+                "input norm");
+  }
+  if (Rm == 0) return DFLASH_OK;
+  DF_LAUNCH(DFLASH_STAGE_OTHER, 1,
+            final_norm_launch<T>(x, static_cast<const T*>(m->g_final), c.rms_eps, B, block, D, hm, slots, s),
+            "final norm");
+  GemmProblem pl = make_problem(hm, D, Rm, D);
+  add_seg(pl, m->lm_head, m->lm_head, c.vocab / kTileN, 0, 0);
+  apply_plan(pl, P.g_lm, partial, counters);
+  DF_LAUNCH(DFLASH_STAGE_LMHEAD, 1, (gemm_launch<T, EpiArgmax>(pl, P.g_lm, EpiArgmax{slots, logits, c.vocab}, s)),
+            "LM head GEMM");
+  DF_LAUNCH(DFLASH_STAGE_OTHER, 1, argmax_finalize_launch(slots, Rm, drafts, s), "argmax");
+  return DFLASH_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int32_t dflash_version(void) { return 100; }
+
+const char* dflash_last_error(void) { return g_last_error.c_str(); }
+
+int32_t dflash_model_create(const dflash_config* cfg, const dflash_weights* w, dflash_model** out) {
+  if (!out) return fail(DFLASH_ERR_INVALID_ARG, "out is NULL");
+  *out = nullptr;
+  int32_t rc = check_config(cfg);
+  if (rc) return rc;
+  if (!w || !w->embed || !w->lm_head || !w->w_c || !w->g_c || !w->g_final || !w->layers)
+    return fail(DFLASH_ERR_INVALID_ARG, "a top-level weight pointer is NULL");
+  for (int l = 0; l < cfg->layers; ++l) {
+    const dflash_layer_weights& L = w->layers[l];
+    if (!L.g_in || !L.w_q || !L.w_k || !L.w_v || !L.w_o || !L.g_post || !L.w_g || !L.w_u || !L.w_d)
+      return fail(DFLASH_ERR_INVALID_ARG, "a weight pointer of layer %d is NULL", l);
+  }
+  dflash_model* m = new dflash_model();
+  m->cfg = *cfg;
+  m->embed = w->embed;
+  m->lm_head = w->lm_head;
+  m->w_c = w->w_c;
+  m->g_c = w->g_c;
+  m->g_final = w->g_final;
+  m->layers.assign(w->layers, w->layers + cfg->layers);
+  cudaError_t e = cudaGetDevice(&m->device);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&m->sms, cudaDevAttrMultiProcessorCount, m->device);
+  if (e == cudaSuccess) e = cudaMalloc(&m->status_dev, sizeof(int32_t));
+  if (e == cudaSuccess) e = cudaMemset(m->status_dev, 0, sizeof(int32_t));
+  const int half = cfg->head_dim / 2;
+  std::vector<double> inv(half);
+  for (int i = 0; i < half; ++i) inv[i] = std::pow((double)cfg->rope_theta, -2.0 * i / cfg->head_dim);
+  if (e == cudaSuccess) e = cudaMalloc(&m->inv_freq_dev, sizeof(double) * half);
+  if (e == cudaSuccess) e = cudaMemcpy(m->inv_freq_dev, inv.data(), sizeof(double) * half, cudaMemcpyHostToDevice);
+  if (e == cudaSuccess)
+    e = cfg->dtype == DFLASH_DTYPE_F32
+            ? attention_prepare<float>((cfg->n_q_heads / cfg->n_kv_heads) * cfg->max_block, cfg->head_dim)
+            : attention_prepare<__nv_bfloat16>((cfg->n_q_heads / cfg->n_kv_heads) * cfg->max_block, cfg->head_dim);
+  if (e != cudaSuccess) {
+    dflash_model_destroy(m);
+    return cuda_fail(e, "model state");
+  }
+  *out = m;
+  return DFLASH_OK;
+}
+
+int32_t dflash_model_destroy(dflash_model* m) {
+  if (!m) return DFLASH_OK;
+  if (m->status_dev) cudaFree(m->status_dev);
+  if (m->inv_freq_dev) cudaFree(m->inv_freq_dev);
+  for (cudaEvent_t e : m->prof.ev) cudaEventDestroy(e);
+  delete m;
+  return DFLASH_OK;
+}
+
+int32_t dflash_get_status(const dflash_model* m, dflash_stream_t stream, int32_t* status_host) {
+  if (!m || !status_host) return fail(DFLASH_ERR_INVALID_ARG, "model or status_host is NULL");
+  DF_CUDA(cudaMemcpyAsync(status_host, m->status_dev, sizeof(int32_t), cudaMemcpyDeviceToHost, (cudaStream_t)stream),
+          "status read");
+  DF_CUDA(cudaStreamSynchronize((cudaStream_t)stream), "status sync");
+  return DFLASH_OK;
+}
+
+int32_t dflash_clear_status(const dflash_model* m, dflash_stream_t stream) {
+  if (!m) return fail(DFLASH_ERR_INVALID_ARG, "model is NULL");
+  DF_CUDA(cudaMemsetAsync(m->status_dev, 0, sizeof(int32_t), (cudaStream_t)stream), "status clear");
+  return DFLASH_OK;
+}
+
+size_t dflash_cache_bytes(const dflash_config* cfg, int32_t batch, int32_t capacity) {
+  if (check_config(cfg) != DFLASH_OK || batch < 0 || capacity < 0) return 0;
+  const size_t es = cfg->dtype == DFLASH_DTYPE_F32 ? 4 : 2;
+  const size_t kv = es * (size_t)batch * cfg->layers * cfg->n_kv_heads * (size_t)capacity * cfg->head_dim;
+  return align256(kv) * 2 + align256(sizeof(int32_t) * std::max(batch, 1));
+}
+
+int32_t dflash_cache_init(const dflash_model* m, void* dev_mem, size_t bytes, int32_t batch, int32_t capacity,
+                          dflash_stream_t stream, dflash_cache** out) {
+  if (!out) return fail(DFLASH_ERR_INVALID_ARG, "out is NULL");
+  *out = nullptr;
+  if (!m || !dev_mem) return fail(DFLASH_ERR_INVALID_ARG, "model or dev_mem is NULL");
+  if (batch <= 0 || capacity <= 0) return fail(DFLASH_ERR_INVALID_ARG, "batch %d and capacity %d must be positive", batch, capacity);
+  if (batch > 4096) return fail(DFLASH_ERR_SHAPE, "batch %d > 4096", batch);
+  if (reinterpret_cast<uintptr_t>(dev_mem) % 256) return fail(DFLASH_ERR_INVALID_ARG, "dev_mem must be 256-byte aligned");
+  const size_t need = dflash_cache_bytes(&m->cfg, batch, capacity);
+  if (bytes < need) return fail(DFLASH_ERR_CAPACITY, "cache memory %zu bytes < %zu needed", bytes, need);
+  int32_t rc = check_device(m);
+  if (rc) return rc;
+  const size_t es = m->cfg.dtype == DFLASH_DTYPE_F32 ? 4 : 2;
+  const size_t kv = es * (size_t)batch * m->cfg.layers * m->cfg.n_kv_heads * (size_t)capacity * m->cfg.head_dim;
+  dflash_cache* c = new dflash_cache();
+  c->model = m;
+  c->base = static_cast<char*>(dev_mem);
+  c->bytes = bytes;
+  c->batch = batch;
+  c->cap = capacity;
+  c->k_off = 0;
+  c->v_off = align256(kv);
+  c->len_off = 2 * align256(kv);
+  c->len_host.assign(batch, 0);
+  c->len_known = true;
+  cudaError_t e = cudaMemsetAsync(c->base + c->len_off, 0, sizeof(int32_t) * batch, (cudaStream_t)stream);
+  if (e != cudaSuccess) {
+    delete c;
+    return cuda_fail(e, "cache init");
+  }
+  *out = c;
+  return DFLASH_OK;
+}
+
+int32_t dflash_cache_destroy(dflash_cache* c) {
+  delete c;
+  return DFLASH_OK;
+}
+
+int32_t dflash_cache_layout(const dflash_cache* c, size_t* k_off, size_t* v_off, size_t* len_off) {
+  if (!c || !k_off || !v_off || !len_off) return fail(DFLASH_ERR_INVALID_ARG, "NULL argument");
+  *k_off = c->k_off;
+  *v_off = c->v_off;
+  *len_off = c->len_off;
+  return DFLASH_OK;
+}
+
+int32_t dflash_cache_set_lengths(dflash_cache* c, const int32_t* len_host, dflash_stream_t stream) {
+  if (!c || !len_host) return fail(DFLASH_ERR_INVALID_ARG, "cache or ctx_len_host is NULL");
+  for (int b = 0; b < c->batch; ++b)
+    if (len_host[b] < 0 || len_host[b] > c->cap)
+      return fail(DFLASH_ERR_CAPACITY, "ctx_len[%d] = %d outside [0, %d]", b, len_host[b], c->cap);
+  DF_CUDA(cudaMemcpyAsync(c->base + c->len_off, len_host, sizeof(int32_t) * c->batch, cudaMemcpyHostToDevice,
+                          (cudaStream_t)stream), "set lengths");
+  c->len_host.assign(len_host, len_host + c->batch);
+  c->len_known = true;
+  return DFLASH_OK;
+}
+
+size_t dflash_workspace_bytes(const dflash_model* m, int32_t batch, int32_t capacity, int32_t block_size,
+                              int32_t max_inject_rows) {
+  if (!m || batch <= 0 || capacity < 0 || block_size < 1 || block_size > m->cfg.max_block || max_inject_rows < 0) return 0;
+  return std::max(plan_ws(m, batch, capacity, 0, max_inject_rows).total, plan_ws(m, batch, capacity, block_size, 0).total);
+}
+
+int32_t dflash_inject_context(const dflash_model* m, dflash_cache* cache, const void* feats, const int32_t* n_new_dev,
+                              const int32_t* n_new_host, int32_t max_rows, void* workspace, size_t ws_bytes,
+                              dflash_stream_t stream) {
+  if (!m || !cache) return fail(DFLASH_ERR_INVALID_ARG, "model or cache is NULL");
+  if (cache->model != m) return fail(DFLASH_ERR_INVALID_ARG, "cache was made for another model");
+  if (max_rows < 0) return fail(DFLASH_ERR_INVALID_ARG, "max_rows %d < 0", max_rows);
+  if (!n_new_dev) return fail(DFLASH_ERR_INVALID_ARG, "n_new_dev is NULL");
+  if (max_rows > 0 && (!feats || !workspace)) return fail(DFLASH_ERR_INVALID_ARG, "feats or workspace is NULL");
+  int32_t rc = check_device(m);
+  if (rc) return rc;
+  if (n_new_host) {
+    long total = 0;
+    for (int b = 0; b < cache->batch; ++b) {
+      if (n_new_host[b] < 0) return fail(DFLASH_ERR_INVALID_ARG, "n_new[%d] = %d < 0", b, n_new_host[b]);
+      total += n_new_host[b];
+      if (cache->len_known && cache->len_host[b] + (long)n_new_host[b] > cache->cap)
+        return fail(DFLASH_ERR_CAPACITY, "request %d: %d + %d tokens exceed capacity %d", b, cache->len_host[b],
+                    n_new_host[b], cache->cap);
+    }
+    if (total > max_rows) return fail(DFLASH_ERR_SHAPE, "sum of n_new (%ld) > max_rows (%d)", total, max_rows);
+  }
+  if (max_rows == 0) return DFLASH_OK;
+  const WsPlan P = plan_ws(m, cache->batch, cache->cap, 0, max_rows);
+  if (ws_bytes < P.total) return fail(DFLASH_ERR_WORKSPACE, "workspace %zu bytes < %zu needed", ws_bytes, P.total);
+  cudaStream_t s = (cudaStream_t)stream;
+  rc = m->cfg.dtype == DFLASH_DTYPE_F32
+           ? run_inject<float>(m, cache, feats, n_new_dev, max_rows, static_cast<char*>(workspace), P, s)
+           : run_inject<__nv_bfloat16>(m, cache, feats, n_new_dev, max_rows, static_cast<char*>(workspace), P, s);
+  if (rc) return rc;
+  if (n_new_host) {
+    if (cache->len_known)
+      for (int b = 0; b < cache->batch; ++b) cache->len_host[b] += n_new_host[b];
+  } else {
+    cache->len_known = false;
+  }
+  return DFLASH_OK;
+}
+
+int32_t dflash_draft_block(const dflash_model* m, const dflash_cache* cache, const int32_t* anchor_dev,
+                           int32_t block_size, int32_t* draft_dev, float* logits_dev, void* workspace,
+                           size_t ws_bytes, dflash_stream_t stream) {
+  if (!m || !cache) return fail(DFLASH_ERR_INVALID_ARG, "model or cache is NULL");
+  if (cache->model != m) return fail(DFLASH_ERR_INVALID_ARG, "cache was made for another model");
+  if (block_size < 1 || block_size > m->cfg.max_block)
+    return fail(DFLASH_ERR_SHAPE, "block_size %d outside [1, %d]", block_size, m->cfg.max_block);
+  if (!anchor_dev || !workspace) return fail(DFLASH_ERR_INVALID_ARG, "anchor_dev or workspace is NULL");
+  if (block_size > 1 && !draft_dev) return fail(DFLASH_ERR_INVALID_ARG, "draft_dev is NULL");
+  int32_t rc = check_device(m);
+  if (rc) return rc;
+  const WsPlan P = plan_ws(m, cache->batch, cache->cap, block_size, 0);
+  if (ws_bytes < P.total) return fail(DFLASH_ERR_WORKSPACE, "workspace %zu bytes < %zu needed", ws_bytes, P.total);
+  cudaStream_t s = (cudaStream_t)stream;
+  return m->cfg.dtype == DFLASH_DTYPE_F32
+             ? run_draft<float>(m, cache, anchor_dev, block_size, draft_dev, logits_dev, static_cast<char*>(workspace), P, s)
+             : run_draft<__nv_bfloat16>(m, cache, anchor_dev, block_size, draft_dev, logits_dev,
+                                        static_cast<char*>(workspace), P, s);
+}
+
+int32_t dflash_verify_greedy(const int32_t* draft_dev, const int32_t* target_argmax_dev, int32_t batch,
+                             int32_t block_size, int32_t* accept_len_dev, int32_t* out_tokens_dev,
+                             int32_t* next_anchor_dev, dflash_stream_t stream) {
+  if (batch < 0) return fail(DFLASH_ERR_INVALID_ARG, "batch %d < 0", batch);
+  if (block_size < 1 || block_size > kMaxBlock) return fail(DFLASH_ERR_SHAPE, "block_size %d outside [1, %d]", block_size, kMaxBlock);
+  if (batch == 0) return DFLASH_OK;
+  if ((block_size > 1 && !draft_dev) || !target_argmax_dev || !accept_len_dev || !out_tokens_dev || !next_anchor_dev)
+    return fail(DFLASH_ERR_INVALID_ARG, "a device pointer is NULL");
+  DF_CUDA(verify_launch(draft_dev, target_argmax_dev, batch, block_size, accept_len_dev, out_tokens_dev,
+                        next_anchor_dev, (cudaStream_t)stream), "verify");
+  g_launch_count += 1;
+  return DFLASH_OK;
+}
+
+uint64_t dflash_launch_count(void) { return g_launch_count.load(); }
+
+int32_t dflash_profile_start(dflash_model* m, int32_t max_launches) {
+  if (!m || max_launches <= 0) return fail(DFLASH_ERR_INVALID_ARG, "model is NULL or max_launches <= 0");
+  int32_t rc = check_device(m);
+  if (rc) return rc;
+  Profiler& p = m->prof;
+  while ((int)p.ev.size() < 2 * max_launches) {
+    cudaEvent_t e;
+    DF_CUDA(cudaEventCreate(&e), "cudaEventCreate");
+    p.ev.push_back(e);
+  }
+  p.used = 0;
+  p.stage.clear();
+  p.on = true;
+  return DFLASH_OK;
+}
+
+int32_t dflash_profile_stop(dflash_model* m, dflash_stream_t stream, float* ms_by_stage, int32_t* launches_by_stage,
+                            int32_t n_stages) {
+  if (!m || !ms_by_stage || !launches_by_stage || n_stages <= 0 || n_stages > DFLASH_NUM_STAGES)
+    return fail(DFLASH_ERR_INVALID_ARG, "bad profile_stop arguments");
+  Profiler& p = m->prof;
+  p.on = false;
+  DF_CUDA(cudaStreamSynchronize((cudaStream_t)stream), "profile sync");
+  for (int i = 0; i < n_stages; ++i) {
+    ms_by_stage[i] = 0.f;
+    launches_by_stage[i] = 0;
+  }
+  for (size_t i = 0; i < p.stage.size(); ++i) {
+    float ms = 0.f;
+    DF_CUDA(cudaEventElapsedTime(&ms, p.ev[2 * i], p.ev[2 * i + 1]), "cudaEventElapsedTime");
+    if (p.stage[i] < n_stages) {
+      ms_by_stage[p.stage[i]] += ms;
+      launches_by_stage[p.stage[i]] += 1;
+    }
+  }
+  p.used = 0;
+  p.stage.clear();
+  return DFLASH_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,170 @@
+// Non-causal block attention of the drafter (split-KV, online softmax).
+//
+// For request b and kv head h the query rows are the (nq/nkv) query heads of
+// the group times the block positions; the keys are the request's injected
+// context K (cache) followed by the block's own K.  No mask is needed: under
+// the DFlash mask a block row sees every context position and every block
+// position.  The key range is cut into splits; each CTA keeps a running max,
+// a running sum and an unnormalised output per row, and a second kernel merges
+// the splits exactly (log-sum-exp rescaling).
+#include <cfloat>
+
+#include "kernels.cuh"
+
+namespace dflash {
+
+namespace {
+
+constexpr int kAttnThreads = 128;
+constexpr int kKeyTile = 32;
+constexpr int kMaxRows = 128;
+
+__device__ __forceinline__ float warp_max(float v) {
+  for (int o = 16; o; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+__device__ __forceinline__ float warp_sum(float v) {
+  for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kAttnThreads) attn_split_kernel(const __grid_constant__ AttnParams p) {
+  extern __shared__ float sm[];
+  const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
+  const int G = p.nq / p.nkv, rows = G * p.block, hd = p.hd;
+  const int c = p.ctx_len[b];
+  const int total = c + p.block;
+  const int j0 = split * p.chunk, j1 = min(total, j0 + p.chunk);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = kAttnThreads / 32;
+
+  float* Qs = sm;                       // [rows][hd]
+  float* Os = Qs + rows * hd;           // [rows][hd]
+  float* Ks = Os + rows * hd;           // [kKeyTile][hd+1]
+  float* Vs = Ks + kKeyTile * (hd + 1); // [kKeyTile][hd]
+  float* Ms = Vs + kKeyTile * hd;       // [rows]
+  float* Ls = Ms + rows;                // [rows]
+
+  const T* q = static_cast<const T*>(p.q);
+  for (int e = threadIdx.x; e < rows * hd; e += kAttnThreads) {
+    int r = e / hd, d = e - r * hd, g = r / p.block, k = r - g * p.block;
+    int qh = kvh * G + g;
+    Qs[e] = to_f32(q[(((size_t)b * p.nq + qh) * p.block + k) * hd + d]) * p.scale;
+    Os[e] = 0.f;
+  }
+  for (int r = threadIdx.x; r < rows; r += kAttnThreads) {
+    Ms[r] = -FLT_MAX;
+    Ls[r] = 0.f;
+  }
+
+  const T* kc = static_cast<const T*>(p.kc) + (((size_t)b * p.layers + p.layer) * p.nkv + kvh) * p.cap * hd;
+  const T* vc = static_cast<const T*>(p.vc) + (((size_t)b * p.layers + p.layer) * p.nkv + kvh) * p.cap * hd;
+  const T* kb = static_cast<const T*>(p.kb) + ((size_t)b * p.nkv + kvh) * p.block * hd;
+  const T* vb = static_cast<const T*>(p.vb) + ((size_t)b * p.nkv + kvh) * p.block * hd;
+
+  for (int jt = j0; jt < j1; jt += kKeyTile) {
+    const int n = min(kKeyTile, j1 - jt);
+    __syncthreads();
+    for (int e = threadIdx.x; e < n * hd; e += kAttnThreads) {
+      int jj = e / hd, d = e - jj * hd, j = jt + jj;
+      float kv, vv;
+      if (j < c) {
+        kv = to_f32(kc[(size_t)j * hd + d]);
+        vv = to_f32(vc[(size_t)j * hd + d]);
+      } else {
+        kv = to_f32(kb[(size_t)(j - c) * hd + d]);
+        vv = to_f32(vb[(size_t)(j - c) * hd + d]);
+      }
+      Ks[jj * (hd + 1) + d] = kv;
+      Vs[jj * hd + d] = vv;
+    }
+    __syncthreads();
+    for (int r = warp; r < rows; r += nwarps) {
+      float s = -FLT_MAX;
+      if (lane < n) {
+        s = 0.f;
+        const float* qr = Qs + r * hd;
+        const float* kr = Ks + lane * (hd + 1);
+        for (int d = 0; d < hd; ++d) s = fmaf(qr[d], kr[d], s);
+      }
+      const float m_old = Ms[r];
+      const float m_new = fmaxf(m_old, warp_max(s));
+      const float pj = lane < n ? __expf(s - m_new) : 0.f;
+      const float alpha = __expf(m_old - m_new);
+      const float lsum = warp_sum(pj);
+      for (int d = lane; d < hd; d += 32) {
+        float acc = Os[r * hd + d] * alpha;
+        for (int j = 0; j < n; ++j) acc = fmaf(__shfl_sync(0xffffffffu, pj, j), Vs[j * hd + d], acc);
+        Os[r * hd + d] = acc;
+      }
+      __syncwarp();
+      if (lane == 0) {
+        Ms[r] = m_new;
+        Ls[r] = Ls[r] * alpha + lsum;
+      }
+      __syncwarp();
+    }
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < rows * hd; e += kAttnThreads) {
+    int r = e / hd, d = e - r * hd, g = r / p.block, k = r - g * p.block;
+    size_t row = (((size_t)b * p.nq + kvh * G + g) * p.block + k) * p.splits + split;
+    p.opart[row * hd + d] = Os[e];
+    if (d == 0) p.ml[row] = make_float2(Ms[r], Ls[r]);
+  }
+}
+
+// One CTA per (request, query head, block position): merge the splits.
+template <typename T>
+__global__ void attn_combine_kernel(const __grid_constant__ AttnParams p) {
+  const int row = blockIdx.x;  // ((b*nq + qh)*block + k)
+  const int k = row % p.block, qh = (row / p.block) % p.nq, b = row / (p.block * p.nq);
+  const float2* ml = p.ml + (size_t)row * p.splits;
+  float M = -FLT_MAX;
+  for (int s = 0; s < p.splits; ++s)
+    if (ml[s].y > 0.f) M = fmaxf(M, ml[s].x);
+  float L = 0.f;
+  for (int s = 0; s < p.splits; ++s)
+    if (ml[s].y > 0.f) L += ml[s].y * __expf(ml[s].x - M);
+  const float inv = 1.f / L;
+  T* out = static_cast<T*>(p.out) + ((size_t)b * p.block + k) * p.nq * p.hd + (size_t)qh * p.hd;
+  for (int d = threadIdx.x; d < p.hd; d += blockDim.x) {
+    float acc = 0.f;
+    for (int s = 0; s < p.splits; ++s)
+      if (ml[s].y > 0.f) acc += p.opart[((size_t)row * p.splits + s) * p.hd + d] * __expf(ml[s].x - M);
+    out[d] = from_f32<T>(acc * inv);
+  }
+}
+
+size_t attn_smem_bytes(int rows, int hd) {
+  return sizeof(float) * ((size_t)2 * rows * hd + kKeyTile * (hd + 1) + (size_t)kKeyTile * hd + 2 * rows);
+}
+
+}  // namespace
+
+int attention_max_rows() { return kMaxRows; }
+
+template <typename T>
+cudaError_t attention_prepare(int rows, int hd) {
+  return cudaFuncSetAttribute(attn_split_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              (int)attn_smem_bytes(rows, hd));
+}
+
+template <typename T>
+cudaError_t attention_launch(const AttnParams& p, cudaStream_t s) {
+  if (p.B <= 0) return cudaSuccess;
+  const int rows = (p.nq / p.nkv) * p.block;
+  const size_t smem = attn_smem_bytes(rows, p.hd);
+  attn_split_kernel<T><<<dim3(p.splits, p.nkv, p.B), kAttnThreads, smem, s>>>(p);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  attn_combine_kernel<T><<<p.B * p.nq * p.block, 128, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+template cudaError_t attention_prepare<float>(int, int);
+template cudaError_t attention_prepare<__nv_bfloat16>(int, int);
+template cudaError_t attention_launch<float>(const AttnParams&, cudaStream_t);
+template cudaError_t attention_launch<__nv_bfloat16>(const AttnParams&, cudaStream_t);
+
+}  // namespace dflash

@@ -1,0 +1,228 @@
+// Row-wise kernels of the draft cycle: embedding gather, RMSNorms, the
+// injection row map, argmax read-out and greedy verification.
+#include "kernels.cuh"
+
+namespace dflash {
+
+namespace {
+
+constexpr int kRowThreads = 256;
+
+__device__ __forceinline__ float block_sum(float v, float* red) {
+  for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  __syncthreads();
+  if (lane == 0) red[warp] = v;
+  __syncthreads();
+  float t = 0.f;
+  for (int w = 0; w < (int)(blockDim.x >> 5); ++w) t += red[w];
+  return t;
+}
+
+// u = x * rsqrt(mean(x^2) + eps) * g for one row held in fp32.
+template <typename T>
+__device__ __forceinline__ void norm_row(const float* x, const T* g, float eps, int D, T* u, float* red) {
+  float ss = 0.f;
+  for (int i = threadIdx.x; i < D; i += blockDim.x) ss = fmaf(x[i], x[i], ss);
+  const float r = rsqrtf(block_sum(ss, red) / (float)D + eps);
+  for (int i = threadIdx.x; i < D; i += blockDim.x) u[i] = from_f32<T>(x[i] * r * to_f32(g[i]));
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kRowThreads) embed_norm_kernel(const T* embed, const int32_t* anchor, int mask_id,
+                                                                 int vocab, int block, int D, const T* g, float eps,
+                                                                 float* x, T* u, int* zero_ptr, int zero_n,
+                                                                 int32_t* status) {
+  __shared__ float red[32];
+  const int row = blockIdx.x, b = row / block, k = row - b * block;
+  if (zero_ptr)
+    for (int i = row * blockDim.x + threadIdx.x; i < zero_n; i += gridDim.x * blockDim.x) zero_ptr[i] = 0;
+  int tok = k == 0 ? anchor[b] : mask_id;
+  if (tok < 0 || tok >= vocab) {  // an anchor outside the vocabulary: flag it, read row 0
+    if (threadIdx.x == 0) report_status(status, DFLASH_ERR_INVALID_ARG);
+    tok = 0;
+  }
+  const T* e = embed + (size_t)tok * D;
+  float* xr = x + (size_t)row * D;
+  for (int i = threadIdx.x; i < D; i += blockDim.x) xr[i] = to_f32(e[i]);
+  __syncthreads();
+  norm_row(xr, g, eps, D, u + (size_t)row * D, red);
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kRowThreads) rmsnorm_kernel(const float* x, const T* g, float eps, int D, T* u) {
+  __shared__ float red[32];
+  norm_row(x + (size_t)blockIdx.x * D, g, eps, D, u + (size_t)blockIdx.x * D, red);
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kRowThreads) final_norm_kernel(const float* x, const T* g, float eps, int block,
+                                                                 int D, T* hm, unsigned long long* slots) {
+  __shared__ float red[32];
+  const int r = blockIdx.x;                   // compact mask-row index
+  const int b = r / (block - 1), k = r - b * (block - 1) + 1;
+  if (threadIdx.x == 0) slots[r] = 0ull;
+  norm_row(x + ((size_t)b * block + k) * D, g, eps, D, hm + (size_t)r * D, red);
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kRowThreads) fuse_norm_kernel(const float* y, const T* g, float eps,
+                                                                const int2* rowinfo, int D, T* ht) {
+  __shared__ float red[32];
+  const int row = blockIdx.x;
+  if (rowinfo[row].x < 0) {
+    for (int i = threadIdx.x; i < D; i += blockDim.x) ht[(size_t)row * D + i] = from_f32<T>(0.f);
+    return;
+  }
+  norm_row(y + (size_t)row * D, g, eps, D, ht + (size_t)row * D, red);
+}
+
+// One CTA: exclusive scan of n_new, per-row (request, position), ctx_len update.
+__global__ void __launch_bounds__(1024) inject_prep_kernel(const int32_t* n_new, int32_t* ctx_len, int B,
+                                                           int max_rows, int cap, int2* rowinfo, int* zero_ptr,
+                                                           int zero_n, int32_t* status) {
+  extern __shared__ int sh[];  // [B] offsets, [B] base positions, [B] accepted counts
+  int* off = sh;
+  int* base = sh + B;
+  int* cnt = sh + 2 * B;
+  for (int i = threadIdx.x; i < zero_n; i += blockDim.x) zero_ptr[i] = 0;
+  if (threadIdx.x == 0) {
+    int acc = 0;
+    for (int b = 0; b < B; ++b) {
+      int n = n_new[b];
+      if (n < 0) n = 0;
+      int c = ctx_len[b];
+      int fit = n;
+      if (c + fit > cap) {
+        fit = max(0, cap - c);
+        report_status(status, DFLASH_ERR_CAPACITY);
+      }
+      if (acc + n > max_rows) {  // rows beyond the launch are dropped
+        report_status(status, DFLASH_ERR_CAPACITY);
+        n = max(0, max_rows - acc);
+        fit = min(fit, n);
+      }
+      off[b] = acc;
+      base[b] = c;
+      cnt[b] = fit;
+      acc += n;
+      ctx_len[b] = c + fit;
+    }
+  }
+  __syncthreads();
+  for (int r = threadIdx.x; r < max_rows; r += blockDim.x) {
+    int2 ri = make_int2(-1, -1);
+    // the request owning row r: last b with off[b] <= r
+    int lo = 0, hi = B - 1, own = -1;
+    while (lo <= hi) {
+      int mid = (lo + hi) >> 1;
+      if (off[mid] <= r) {
+        own = mid;
+        lo = mid + 1;
+      } else {
+        hi = mid - 1;
+      }
+    }
+    if (own >= 0) {
+      int j = r - off[own];
+      if (j < cnt[own]) ri = make_int2(own, base[own] + j);
+    }
+    rowinfo[r] = ri;
+  }
+}
+
+__global__ void argmax_finalize_kernel(const unsigned long long* slots, int rows, int32_t* drafts) {
+  int r = blockIdx.x * blockDim.x + threadIdx.x;
+  if (r < rows) drafts[r] = unpack_argmax_index(slots[r]);
+}
+
+// One warp per request: n = leading positions where d_{k+1} == y_k.
+__global__ void verify_kernel(const int32_t* draft, const int32_t* target, int B, int block, int32_t* accept_len,
+                              int32_t* out_tokens, int32_t* next_anchor) {
+  const int lane = threadIdx.x & 31;
+  const int b = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (b >= B) return;
+  const int nd = block - 1;
+  const int32_t* d = draft + (size_t)b * nd;
+  const int32_t* y = target + (size_t)b * block;
+  const bool mismatch = lane < nd && d[lane] != y[lane];
+  const unsigned bad = __ballot_sync(0xffffffffu, mismatch);
+  const int n = bad ? __ffs(bad) - 1 : nd;
+  const int yn = y[n];
+  int32_t* out = out_tokens + (size_t)b * block;
+  if (lane < block) out[lane] = lane < n ? d[lane] : (lane == n ? yn : -1);
+  if (lane == 0) {
+    accept_len[b] = n + 1;
+    next_anchor[b] = yn;
+  }
+}
+
+}  // namespace
+
+template <typename T>
+cudaError_t embed_norm_launch(const T* embed, const int32_t* anchor, int mask_id, int vocab, int B, int block, int D,
+                              const T* g, float eps, float* x, T* u, int* zero_ptr, int zero_n, int32_t* status,
+                              cudaStream_t s) {
+  if (B * block == 0) return cudaSuccess;
+  embed_norm_kernel<T><<<B * block, kRowThreads, 0, s>>>(embed, anchor, mask_id, vocab, block, D, g, eps, x, u,
+                                                         zero_ptr, zero_n, status);
+  return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t rmsnorm_launch(const float* x, const T* g, float eps, int rows, int D, T* u, cudaStream_t s) {
+  if (rows == 0) return cudaSuccess;
+  rmsnorm_kernel<T><<<rows, kRowThreads, 0, s>>>(x, g, eps, D, u);
+  return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t final_norm_launch(const float* x, const T* g, float eps, int B, int block, int D, T* hm,
+                              unsigned long long* slots, cudaStream_t s) {
+  if (B * (block - 1) == 0) return cudaSuccess;
+  final_norm_kernel<T><<<B * (block - 1), kRowThreads, 0, s>>>(x, g, eps, block, D, hm, slots);
+  return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t fuse_norm_launch(const float* y, const T* g, float eps, const int2* rowinfo, int rows, int D, T* ht,
+                             cudaStream_t s) {
+  if (rows == 0) return cudaSuccess;
+  fuse_norm_kernel<T><<<rows, kRowThreads, 0, s>>>(y, g, eps, rowinfo, D, ht);
+  return cudaGetLastError();
+}
+
+cudaError_t inject_prep_launch(const int32_t* n_new, int32_t* ctx_len, int B, int max_rows, int cap, int2* rowinfo,
+                               int* zero_ptr, int zero_n, int32_t* status, cudaStream_t s) {
+  inject_prep_kernel<<<1, 1024, 3 * B * sizeof(int), s>>>(n_new, ctx_len, B, max_rows, cap, rowinfo, zero_ptr, zero_n,
+                                                          status);
+  return cudaGetLastError();
+}
+
+cudaError_t argmax_finalize_launch(const unsigned long long* slots, int rows, int32_t* drafts, cudaStream_t s) {
+  if (rows == 0) return cudaSuccess;
+  argmax_finalize_kernel<<<(rows + 255) / 256, 256, 0, s>>>(slots, rows, drafts);
+  return cudaGetLastError();
+}
+
+cudaError_t verify_launch(const int32_t* draft, const int32_t* target, int B, int block, int32_t* accept_len,
+                          int32_t* out_tokens, int32_t* next_anchor, cudaStream_t s) {
+  if (B == 0) return cudaSuccess;
+  const int warps = 4;
+  verify_kernel<<<(B + warps - 1) / warps, 32 * warps, 0, s>>>(draft, target, B, block, accept_len, out_tokens,
+                                                               next_anchor);
+  return cudaGetLastError();
+}
+
+#define DFLASH_EW_INST(T)                                                                                        \
+  template cudaError_t embed_norm_launch<T>(const T*, const int32_t*, int, int, int, int, int, const T*, float,     \
+                                            float*, T*, int*, int, int32_t*, cudaStream_t);                       \
+  template cudaError_t rmsnorm_launch<T>(const float*, const T*, float, int, int, T*, cudaStream_t);              \
+  template cudaError_t final_norm_launch<T>(const float*, const T*, float, int, int, int, T*, unsigned long long*, \
+                                            cudaStream_t);                                                        \
+  template cudaError_t fuse_norm_launch<T>(const float*, const T*, float, const int2*, int, int, T*, cudaStream_t);
+
+DFLASH_EW_INST(float)
+DFLASH_EW_INST(__nv_bfloat16)
+
+}  // namespace dflash

@@ -1,0 +1,29 @@
+// GEMM launch interface shared by the host orchestration and the kernels.
+#pragma once
+
+#include "common.cuh"
+#include "epilogue.cuh"
+
+namespace dflash {
+
+// How one GEMM launch is cut: token rows per CTA tile, split-K.
+struct GemmPlan {
+  int tc;               // 1: tcgen05 tensor-core kernel, 0: CUDA-core kernel
+  int bm;               // token rows per CTA tile
+  int token_tiles;
+  int splits;
+  int kblocks_per_split;  // 64-column blocks of K per split
+  size_t partial_floats;  // split-K scratch floats (0 if splits == 1)
+  int counters;           // split-K tile counters (0 if splits == 1)
+};
+
+// Decide the cut for an M x (tiles*128) x K product on a device with `sms` SMs.
+GemmPlan plan_gemm(int dtype, int M, int K, int tiles, int sms);
+
+// Fill the plan's fields into the problem (splits, kblocks, scratch pointers).
+void apply_plan(GemmProblem& p, const GemmPlan& plan, float* partial, int* counters);
+
+template <typename T, class Epi>
+cudaError_t gemm_launch(const GemmProblem& p, const GemmPlan& plan, const Epi& epi, cudaStream_t s);
+
+}  // namespace dflash

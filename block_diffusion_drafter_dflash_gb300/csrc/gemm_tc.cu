@@ -1,0 +1,306 @@
+// Tensor-core projection GEMM for sm_100-family GPUs (tcgen05 + TMA + TMEM).
+//
+// Swap-AB form: the weight tile is the MMA's M side and the token rows are
+// its N side,
+//     D[128 features x BN tokens] += W[128 x 64] . X[BN x 64]^T   per stage,
+// so one kernel covers batch 1 (BN = 16: weight streaming, HBM-bound) and
+// batch 32 (BN = 256: dense, tensor-bound).  One thread issues TMA loads of
+// both operands (128-B swizzle, K-major) into a ring of shared-memory stages;
+// one thread issues tcgen05.mma into a tensor-memory accumulator and frees
+// each stage with tcgen05.commit; all four warps then read the accumulator
+// back (tcgen05.ld) and run the fused epilogue.  Split-K writes fp32 partial
+// tiles; the last CTA of a tile (atomic ticket, no waiting) sums them in split
+// order and runs the epilogue, so results do not depend on scheduling.
+// Every mbarrier wait is bounded: on expiry the kernel sets
+// DFLASH_ERR_TIMEOUT in the status word, skips its output and still frees
+// its tensor memory.
+#include <cuda.h>
+
+#include <algorithm>
+
+#include "gemm.cuh"
+#include "ptx.cuh"
+
+namespace dflash {
+
+namespace {
+
+template <int BN>
+struct TcCfg {
+  static constexpr int kStages = BN <= 64 ? 5 : 4;
+  static constexpr int kABytes = kTileN * 128;        // 128 rows x 64 bf16
+  static constexpr int kBBytes = BN * 128;            // BN rows x 64 bf16
+  static constexpr int kStageBytes = kABytes + kBBytes;
+  static constexpr int kTmemCols = BN <= 32 ? 32 : BN;
+  static constexpr int kChunk = BN < 32 ? BN : 32;    // token columns per epilogue pass
+  static constexpr int kBarBytes = 256;
+  static constexpr int kSmem = 1024 + kStages * kStageBytes + kBarBytes;
+  static_assert(kStageBytes % 1024 == 0, "stages must keep 1024-B alignment");
+  static_assert(kTileN * (kChunk + 1) * 4 <= kStages * kStageBytes, "epilogue tile must fit the stages");
+};
+
+constexpr long long kWaitBudget = 4000000000LL;  // SM cycles (~2 s): far beyond any legal wait
+
+template <int BN, class Epi>
+__global__ void __launch_bounds__(128, 1) gemm_tc_kernel(const __grid_constant__ CUtensorMap xmap,
+                                                         const __grid_constant__ GemmProblem p,
+                                                         const __grid_constant__ Epi epi, int32_t* status) {
+  using C = TcCfg<BN>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kStages * C::kStageBytes);
+  uint64_t* empty = full + C::kStages;
+  uint64_t* accf = empty + C::kStages;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accf + 1);
+  int* flags = reinterpret_cast<int*>(tmem_slot + 1);   // [0] abort, [1] last split, [2] loads issued
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int gtile = blockIdx.x, split = blockIdx.y, mt = blockIdx.z;
+  const int m0 = mt * BN, mc = min(BN, p.M - m0);
+  const int si = find_seg(p, gtile);
+  const GemmSeg& sg = p.seg[si];
+  const int tis = gtile - sg.tile_begin;
+  const int kb0 = split * p.kblocks_per_split;
+  const int nk = min(p.K / 64, kb0 + p.kblocks_per_split) - kb0;
+  const CUtensorMap* wmaps = static_cast<const CUtensorMap*>(p.wmaps);
+  const CUtensorMap* map0 = wmaps + sg.map0;
+  const CUtensorMap* map1 = wmaps + (sg.paired ? sg.map1 : sg.map0);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::kStages; ++s) {
+      ptx::mbar_init(full + s, 1);
+      ptx::mbar_init(empty + s, 1);
+    }
+    ptx::mbar_init(accf, 1);
+    flags[0] = 0;
+    flags[1] = 0;
+    flags[2] = 0;
+    ptx::fence_mbar_init();
+    ptx::prefetch_tmap(&xmap);
+    ptx::prefetch_tmap(map0);
+    ptx::prefetch_tmap(map1);
+  }
+  if (warp == 1) ptx::tmem_alloc(tmem_slot, C::kTmemCols);
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0 && lane == 0) {
+    // ---- TMA producer
+    const uint64_t pol_w = ptx::policy_evict_first(), pol_x = ptx::policy_evict_last();
+    const int r0 = half_first_row(sg, tis, 0), r1 = half_first_row(sg, tis, 1);
+    int issued = 0;
+    for (int i = 0; i < nk; ++i) {
+      const int s = i % C::kStages;
+      if (i >= C::kStages && !ptx::mbar_wait(empty + s, ((i / C::kStages) & 1) ^ 1, kWaitBudget, status)) {
+        flags[0] = 1;
+        break;
+      }
+      uint8_t* a = smem + s * C::kStageBytes;
+      ptx::mbar_arrive_expect_tx(full + s, C::kStageBytes);
+      const int kx = (kb0 + i) * 64;
+      ptx::tma_load_2d(a, map0, full + s, kx, r0, pol_w);
+      ptx::tma_load_2d(a + kHalfN * 128, map1, full + s, kx, r1, pol_w);
+      ptx::tma_load_2d(a + C::kABytes, &xmap, full + s, kx, m0, pol_x);
+      ++issued;
+    }
+    flags[2] = issued;
+  } else if (warp == 1 && lane == 0) {
+    // ---- MMA issuer
+    constexpr uint32_t idesc = ptx::idesc_bf16_f32(kTileN, BN);
+    for (int i = 0; i < nk; ++i) {
+      const int s = i % C::kStages;
+      if (!ptx::mbar_wait(full + s, (i / C::kStages) & 1, kWaitBudget, status)) {
+        flags[0] = 1;
+        break;
+      }
+      ptx::tc_fence_after();
+      const uint64_t ad = ptx::smem_desc_sw128(smem + s * C::kStageBytes);
+      const uint64_t bd = ptx::smem_desc_sw128(smem + s * C::kStageBytes + C::kABytes);
+#pragma unroll
+      for (int k = 0; k < 4; ++k)   // 4 x K=16 per 64-column stage; +32 B per step inside the swizzle row
+        ptx::mma_bf16(tmem, ad + 2 * k, bd + 2 * k, idesc, (i | k) != 0 ? 1u : 0u);
+      ptx::mma_commit(empty + s);
+    }
+    ptx::mma_commit(accf);
+  }
+  __syncwarp();
+
+  // ---- epilogue (all 4 warps; warp w owns accumulator lanes 32w..32w+31)
+  const bool ok = ptx::mbar_wait(accf, 0, kWaitBudget, status);
+  ptx::tc_fence_after();
+  __syncthreads();
+  const bool abort = !ok || flags[0] != 0;
+  float* st = reinterpret_cast<float*>(smem);   // [128][kChunk+1], reuses the drained stages
+  constexpr int ld = C::kChunk + 1;
+  const int n = warp * 32 + lane;
+  const uint32_t trow = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+
+  if (!abort) {
+    if (p.splits == 1) {
+      for (int c0 = 0; c0 < mc; c0 += C::kChunk) {
+        float v[C::kChunk];
+#pragma unroll
+        for (int h = 0; h < C::kChunk; h += 16) ptx::tmem_ld16(trow + c0 + h, v + h);
+#pragma unroll
+        for (int j = 0; j < C::kChunk; ++j) st[n * ld + j] = v[j];
+        __syncthreads();
+        epi(st, ld, m0 + c0, min(C::kChunk, mc - c0), gtile, sg, tis);
+        __syncthreads();
+      }
+    } else {
+      const size_t ntot = static_cast<size_t>(p.total_tiles) * kTileN;
+      for (int c0 = 0; c0 < mc; c0 += C::kChunk) {
+        float v[C::kChunk];
+#pragma unroll
+        for (int h = 0; h < C::kChunk; h += 16) ptx::tmem_ld16(trow + c0 + h, v + h);
+#pragma unroll
+        for (int j = 0; j < C::kChunk; ++j)
+          if (c0 + j < mc)
+            p.partial[(static_cast<size_t>(split) * p.M + m0 + c0 + j) * ntot + static_cast<size_t>(gtile) * kTileN + n] =
+                v[j];
+      }
+      __threadfence();
+      __syncthreads();
+      if (threadIdx.x == 0) {
+        int* c = p.counters + mt * p.total_tiles + gtile;
+        const int old = atomicAdd(c, 1);
+        flags[1] = old == p.splits - 1;
+        if (flags[1]) *c = 0;   // ready for the next launch
+      }
+      __syncthreads();
+      if (flags[1]) {
+        __threadfence();
+        for (int c0 = 0; c0 < mc; c0 += C::kChunk) {
+          const int cc = min(C::kChunk, mc - c0);
+          for (int j = 0; j < cc; ++j) {
+            float s = 0.f;
+            for (int sp = 0; sp < p.splits; ++sp)
+              s += __ldcg(p.partial + (static_cast<size_t>(sp) * p.M + m0 + c0 + j) * ntot +
+                          static_cast<size_t>(gtile) * kTileN + n);
+            st[n * ld + j] = s;
+          }
+          __syncthreads();
+          epi(st, ld, m0 + c0, cc, gtile, sg, tis);
+          __syncthreads();
+        }
+      }
+    }
+  } else if (threadIdx.x == 0) {
+    // a wait ran out: let every load this CTA issued land before the CTA exits
+    const int issued = flags[2];
+    for (int i = max(0, issued - C::kStages); i < issued; ++i)
+      ptx::mbar_wait(full + (i % C::kStages), (i / C::kStages) & 1, kWaitBudget, status);
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, C::kTmemCols);
+  }
+}
+
+// ---------------------------------------------------------------- host side
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(f);
+  }
+  return fn;
+}
+
+template <int BN, class Epi>
+cudaError_t launch_bn(const GemmProblem& p, const GemmPlan& plan, const Epi& epi, cudaStream_t s) {
+  using C = TcCfg<BN>;
+  static bool attr_set = false;   // per instantiation; the attribute is per device function
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<BN, Epi>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  CUtensorMap xmap;
+  if (!encode_activation_map(&xmap, p.x, p.K, p.M, p.ldx, BN)) return cudaErrorInvalidValue;
+  dim3 grid(p.total_tiles, plan.splits, plan.token_tiles);
+  gemm_tc_kernel<BN, Epi><<<grid, 128, C::kSmem, s>>>(xmap, p, epi, p.status);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+bool encode_weight_map(void* map, const void* base, int inner, int rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)inner * 2};
+  cuuint32_t box[2] = {64, (cuuint32_t)kHalfN};
+  cuuint32_t es[2] = {1, 1};
+  return fn(static_cast<CUtensorMap*>(map), CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims,
+            strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool encode_activation_map(void* map, const void* base, int inner, int rows, int row_stride, int box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)row_stride * 2};
+  cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
+  cuuint32_t es[2] = {1, 1};
+  return fn(static_cast<CUtensorMap*>(map), CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims,
+            strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+size_t tensor_map_bytes() { return sizeof(CUtensorMap); }
+
+GemmPlan plan_gemm_tc(int M, int K, int tiles, int sms) {
+  GemmPlan g{};
+  g.tc = 1;
+  g.bm = M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : M <= 128 ? 128 : 256;
+  g.token_tiles = (M + g.bm - 1) / g.bm;
+  const int cps = g.bm <= 64 ? 2 : 1;   // CTAs resident per SM (shared-memory bound)
+  const int kblocks = K / 64;
+  const long ctas = (long)tiles * g.token_tiles;
+  int splits = (int)std::max(1L, (long)sms * cps / ctas);
+  splits = std::min(splits, std::max(1, kblocks / 4));
+  g.kblocks_per_split = (kblocks + splits - 1) / splits;
+  g.splits = (kblocks + g.kblocks_per_split - 1) / g.kblocks_per_split;
+  g.partial_floats = g.splits > 1 ? (size_t)g.splits * M * tiles * kTileN : 0;
+  g.counters = g.splits > 1 ? g.token_tiles * tiles : 0;
+  return g;
+}
+
+template <class Epi>
+cudaError_t gemm_tc_launch(const GemmProblem& p, const GemmPlan& plan, const Epi& epi, cudaStream_t s) {
+  switch (plan.bm) {
+    case 16: return launch_bn<16, Epi>(p, plan, epi, s);
+    case 32: return launch_bn<32, Epi>(p, plan, epi, s);
+    case 64: return launch_bn<64, Epi>(p, plan, epi, s);
+    case 128: return launch_bn<128, Epi>(p, plan, epi, s);
+    case 256: return launch_bn<256, Epi>(p, plan, epi, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+template cudaError_t gemm_tc_launch<EpiStoreF32>(const GemmProblem&, const GemmPlan&, const EpiStoreF32&, cudaStream_t);
+template cudaError_t gemm_tc_launch<EpiResidual>(const GemmProblem&, const GemmPlan&, const EpiResidual&, cudaStream_t);
+template cudaError_t gemm_tc_launch<EpiSwiGLU<__nv_bfloat16>>(const GemmProblem&, const GemmPlan&,
+                                                              const EpiSwiGLU<__nv_bfloat16>&, cudaStream_t);
+template cudaError_t gemm_tc_launch<EpiQKV<__nv_bfloat16>>(const GemmProblem&, const GemmPlan&,
+                                                           const EpiQKV<__nv_bfloat16>&, cudaStream_t);
+template cudaError_t gemm_tc_launch<EpiInject<__nv_bfloat16>>(const GemmProblem&, const GemmPlan&,
+                                                              const EpiInject<__nv_bfloat16>&, cudaStream_t);
+template cudaError_t gemm_tc_launch<EpiArgmax>(const GemmProblem&, const GemmPlan&, const EpiArgmax&, cudaStream_t);
+
+}  // namespace dflash

@@ -1,0 +1,68 @@
+// Launchers of the non-GEMM kernels of the draft cycle.
+#pragma once
+
+#include "common.cuh"
+
+namespace dflash {
+
+// ---------------------------------------------------------------- attention
+// Block queries of one draft layer against [context K/V of the cache ; block K/V]
+// (no mask: every block row sees all context and the whole block).
+struct AttnParams {
+  const void* q;        // [B][nq][block][hd]   (RoPE applied)
+  const void* kb;       // [B][nkv][block][hd]  (RoPE applied)
+  const void* vb;       // [B][nkv][block][hd]
+  const void* kc;       // cache K [B][layers][nkv][cap][hd]
+  const void* vc;       // cache V
+  const int32_t* ctx_len;
+  int layer, layers, cap;
+  int B, nq, nkv, hd, block;
+  int chunk;            // keys per split (context + block keys counted together)
+  int splits;
+  float* opart;         // [B][nq][block][splits][hd] unnormalised partial outputs
+  float2* ml;           // [B][nq][block][splits] (running max, running sum)
+  void* out;            // [B*block][nq*hd] dtype
+  float scale;          // 1/sqrt(hd)
+};
+
+template <typename T> cudaError_t attention_launch(const AttnParams& p, cudaStream_t s);
+// One-time per-device setup (shared-memory opt-in) for up to `rows` query rows.
+template <typename T> cudaError_t attention_prepare(int rows, int hd);
+int attention_max_rows();   // largest (nq/nkv)*block the kernel accepts
+
+// ---------------------------------------------------------------- elementwise
+// x[row] = E[token(row)], token = anchor[b] at block position 0 else mask_id;
+// u[row] = RMSNorm(x[row]) * g.  Also zeroes `zero_n` ints at `zero_ptr`.
+// An anchor outside [0, vocab) sets DFLASH_ERR_INVALID_ARG in `status`.
+template <typename T>
+cudaError_t embed_norm_launch(const T* embed, const int32_t* anchor, int mask_id, int vocab, int B, int block, int D,
+                              const T* g, float eps, float* x, T* u, int* zero_ptr, int zero_n, int32_t* status,
+                              cudaStream_t s);
+
+// u[row] = RMSNorm(x[row]) * g for `rows` rows.
+template <typename T>
+cudaError_t rmsnorm_launch(const float* x, const T* g, float eps, int rows, int D, T* u, cudaStream_t s);
+
+// Final norm of the mask rows only (block position >= 1), compacted to
+// hm[b*(block-1) + k-1]; zeroes the argmax slots of those rows.
+template <typename T>
+cudaError_t final_norm_launch(const float* x, const T* g, float eps, int B, int block, int D, T* hm,
+                              unsigned long long* slots, cudaStream_t s);
+
+// H_t[row] = RMSNorm(y[row]) * g_c for rows with rowinfo[row].x >= 0, 0 otherwise.
+template <typename T>
+cudaError_t fuse_norm_launch(const float* y, const T* g, float eps, const int2* rowinfo, int rows, int D, T* ht,
+                             cudaStream_t s);
+
+// Row -> (request, position) map of an injection and the ctx_len update.
+cudaError_t inject_prep_launch(const int32_t* n_new, int32_t* ctx_len, int B, int max_rows, int cap,
+                               int2* rowinfo, int* zero_ptr, int zero_n, int32_t* status, cudaStream_t s);
+
+// drafts[row] = index packed in slots[row].
+cudaError_t argmax_finalize_launch(const unsigned long long* slots, int rows, int32_t* drafts, cudaStream_t s);
+
+// Greedy verification, one warp per request.
+cudaError_t verify_launch(const int32_t* draft, const int32_t* target, int B, int block, int32_t* accept_len,
+                          int32_t* out_tokens, int32_t* next_anchor, cudaStream_t s);
+
+}  // namespace dflash

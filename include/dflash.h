@@ -1,0 +1,246 @@
+/*
+ * dflash.h — C ABI of the GB300 (sm_103a) DFlash draft-cycle library.
+ *
+ * One draft cycle of the DFlash block-diffusion drafter ("DFlash: Block
+ * Diffusion for Flash Speculative Decoding", §4.1 Inference, §7.3 KV Injection
+ * Mechanism; explainer page of the same name, "Putting It Together") is:
+ *
+ *   dflash_inject_context  stages 1+2: fuse the m target-layer hidden states of
+ *                          newly committed tokens into H_t and append
+ *                          W^K_i H_t (RoPE'd) and W^V_i H_t to every draft
+ *                          layer's persistent context cache;
+ *   dflash_draft_block     stages 3+4: one non-causal drafter pass over
+ *                          [anchor, mask x (block_size-1)] and the shared LM
+ *                          head with argmax -> block_size-1 draft tokens;
+ *   dflash_verify_greedy   stage 5: greedy lossless verification against the
+ *                          target's argmax -> accepted length tau, emitted
+ *                          tokens and the next anchor.
+ *
+ * Conventions (all entry points):
+ *  - Every pointer named *_dev, every weight and the cache/workspace memory is
+ *    DEVICE memory owned by the caller; pointers named *_host are host memory.
+ *    Nothing is copied: weight pointers are borrowed for the model's lifetime.
+ *  - Matrices are row-major [out_features, in_features] (the Linear layout).
+ *    Storage type of weights, features, cache and activations is the model's
+ *    dtype (DFLASH_DTYPE_F32 or DFLASH_DTYPE_BF16); accumulation is fp32.
+ *  - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy
+ *    default stream).  Arguments are validated on the host before any launch;
+ *    a non-zero return means nothing was launched, and dflash_last_error()
+ *    gives a message.  Errors only the device can see (a cache that would
+ *    overflow, a bounded wait that ran out) set the model's device status word,
+ *    read with dflash_get_status().
+ *  - No entry point allocates device memory except dflash_model_create (a few
+ *    hundred bytes of model state).  Scratch memory is the caller's workspace.
+ *  - Integer token ids are int32 in [0, vocab).
+ */
+#ifndef DFLASH_H_
+#define DFLASH_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Opaque stream handle, ABI-compatible with cudaStream_t. */
+typedef struct CUstream_st* dflash_stream_t;
+
+/* Return codes. */
+#define DFLASH_OK 0
+#define DFLASH_ERR_INVALID_ARG (-1) /* null pointer, bad enum, negative size      */
+#define DFLASH_ERR_SHAPE (-2)       /* shape the kernels do not support            */
+#define DFLASH_ERR_CAPACITY (-3)    /* cache would overflow its capacity           */
+#define DFLASH_ERR_CUDA (-4)        /* a CUDA runtime call failed                  */
+#define DFLASH_ERR_TIMEOUT (-5)     /* (device status) a bounded wait ran out      */
+#define DFLASH_ERR_UNSUPPORTED (-6) /* feature not built for this device           */
+#define DFLASH_ERR_WORKSPACE (-7)   /* workspace smaller than dflash_workspace_bytes */
+
+#define DFLASH_DTYPE_F32 0
+#define DFLASH_DTYPE_BF16 1
+
+/* Drafter shape.  Paper §5 Implementation: 5 draft layers, block size 16,
+ * m = 5 target feature layers; §7.3: W_c in R^{D x mD}.  Qwen3-style layer:
+ * RMSNorm, GQA attention with RoPE (rotate-half pairing), SwiGLU FFN.
+ * Supported: hidden % 128 == 0, head_dim in {64, 128}, n_q_heads % n_kv_heads
+ * == 0, ffn % 64 == 0, vocab % 128 == 0, n_target_feats in [1, 8],
+ * 1 <= max_block <= 32. */
+typedef struct {
+  int32_t hidden;         /* D */
+  int32_t layers;         /* draft layers */
+  int32_t n_q_heads;
+  int32_t n_kv_heads;
+  int32_t head_dim;
+  int32_t ffn;            /* SwiGLU width F */
+  int32_t vocab;          /* V (shared embedding and LM head rows) */
+  int32_t n_target_feats; /* m */
+  int32_t max_block;      /* largest block_size accepted by dflash_draft_block */
+  float rope_theta;
+  float rms_eps;
+  int32_t mask_token_id;  /* embedding row used at every masked block position */
+  int32_t dtype;          /* DFLASH_DTYPE_* */
+} dflash_config;
+
+/* Device pointers of one draft layer (borrowed).  Shapes with
+ * Hq = n_q_heads*head_dim, Hk = n_kv_heads*head_dim:
+ *   g_in [D], w_q [Hq,D], w_k [Hk,D], w_v [Hk,D], w_o [D,Hq],
+ *   g_post [D], w_g [F,D], w_u [F,D], w_d [D,F]. */
+typedef struct {
+  const void* g_in;
+  const void* w_q;
+  const void* w_k;
+  const void* w_v;
+  const void* w_o;
+  const void* g_post;
+  const void* w_g;
+  const void* w_u;
+  const void* w_d;
+} dflash_layer_weights;
+
+/* Device pointers of the whole drafter (borrowed): embed [V,D] and
+ * lm_head [V,D] (shared with the target, paper §4.2), w_c [D, m*D], g_c [D]
+ * (fusion RMSNorm gain), g_final [D] (norm before the LM head).  `layers` is a
+ * HOST array of `layers` entries, copied by dflash_model_create. */
+typedef struct {
+  const void* embed;
+  const void* lm_head;
+  const void* w_c;
+  const void* g_c;
+  const void* g_final;
+  const dflash_layer_weights* layers;
+} dflash_weights;
+
+typedef struct dflash_model dflash_model;
+typedef struct dflash_cache dflash_cache;
+
+/* Library version (major*10000 + minor*100 + patch). */
+int32_t dflash_version(void);
+
+/* Thread-local message of the last failed call on this thread ("" if none). */
+const char* dflash_last_error(void);
+
+/* Validate `cfg`, copy it and the weight pointers, allocate the model's small
+ * device state (status word, RoPE frequency table) on the current device and
+ * prepare the tensor-core operand descriptors of every weight matrix.
+ * On success *out owns that state until dflash_model_destroy. */
+int32_t dflash_model_create(const dflash_config* cfg, const dflash_weights* w, dflash_model** out);
+int32_t dflash_model_destroy(dflash_model* model);
+
+/* Device status word: DFLASH_OK, or the first device-detected error since the
+ * last clear (DFLASH_ERR_CAPACITY, DFLASH_ERR_TIMEOUT).  Synchronises `stream`. */
+int32_t dflash_get_status(const dflash_model* model, dflash_stream_t stream, int32_t* status_host);
+int32_t dflash_clear_status(const dflash_model* model, dflash_stream_t stream);
+
+/* --- persistent draft KV cache (paper §4.1: context K/V stored in the draft
+ * model's KV cache and reused across drafting iterations) ----------------------
+ * Layout inside the caller's block of device memory (each region 256-B aligned):
+ *   K [batch][layers][n_kv_heads][capacity][head_dim]   (dtype, RoPE applied)
+ *   V [batch][layers][n_kv_heads][capacity][head_dim]   (dtype)
+ *   ctx_len int32 [batch]                                (tokens held per request)
+ * Only context entries live in the cache; a block's own K/V never does. */
+size_t dflash_cache_bytes(const dflash_config* cfg, int32_t batch, int32_t capacity);
+
+/* Carve a cache for `batch` requests of up to `capacity` tokens out of
+ * `dev_mem` (>= dflash_cache_bytes) and zero every ctx_len on `stream`. */
+int32_t dflash_cache_init(const dflash_model* model, void* dev_mem, size_t bytes, int32_t batch,
+                          int32_t capacity, dflash_stream_t stream, dflash_cache** out);
+int32_t dflash_cache_destroy(dflash_cache* cache);
+
+/* Byte offsets of the K, V and ctx_len regions from dev_mem. */
+int32_t dflash_cache_layout(const dflash_cache* cache, size_t* k_off, size_t* v_off, size_t* len_off);
+
+/* Overwrite every request's ctx_len from host memory (e.g. to drop a request
+ * or rewind).  Entries must lie in [0, capacity]. */
+int32_t dflash_cache_set_lengths(dflash_cache* cache, const int32_t* ctx_len_host, dflash_stream_t stream);
+
+/* --- workspace ----------------------------------------------------------------
+ * Bytes of caller-owned device scratch that dflash_inject_context (with up to
+ * `max_inject_rows` rows) and dflash_draft_block (with `block_size`) need for a
+ * cache of `batch` requests and `capacity` tokens.  One workspace may serve
+ * every call on one stream; calls that overlap on the GPU need separate ones. */
+size_t dflash_workspace_bytes(const dflash_model* model, int32_t batch, int32_t capacity, int32_t block_size,
+                              int32_t max_inject_rows);
+
+/* --- stage 1+2: context fusion and K/V injection ------------------------------
+ * Paper §7.3: H_t = RMSNorm(W_c [H^(l1); ...; H^(lm)]);  per layer i the context
+ * keys/values W^K_i H_t and W^V_i H_t; §4.1: persistent in the cache.
+ *   feats       [max_rows][m][D] (dtype): the new tokens' target hidden states,
+ *               request 0's rows first, then request 1's, ... (packed).
+ *   n_new_dev   int32 [batch] device: rows per request this call.
+ *   n_new_host  int32 [batch] host copy of n_new_dev, or NULL.  When given, the
+ *               host checks sum <= max_rows and capacity exactly and returns
+ *               DFLASH_ERR_CAPACITY without launching; when NULL (e.g. the
+ *               counts come from dflash_verify_greedy on the device) the device
+ *               drops rows that do not fit and sets DFLASH_ERR_CAPACITY in the
+ *               status word.
+ *   max_rows    rows the launch covers (>= sum of n_new); rows past the sum are
+ *               ignored.
+ * Token j of request b is placed at position ctx_len[b] + j (RoPE position of
+ * its key) and ctx_len[b] grows by n_new[b]. */
+int32_t dflash_inject_context(const dflash_model* model, dflash_cache* cache, const void* feats,
+                              const int32_t* n_new_dev, const int32_t* n_new_host, int32_t max_rows,
+                              void* workspace, size_t workspace_bytes, dflash_stream_t stream);
+
+/* --- stage 3+4: drafter forward pass, shared LM head, argmax -------------------
+ * Paper §4.2 / explainer step 3: block = [anchor, mask x (block_size-1)] at
+ * positions ctx_len[b] .. ctx_len[b]+block_size-1; every block row attends to
+ * all of the request's context K/V and to every block row (no causal mask);
+ * per layer RMSNorm -> Q,K,V (+RoPE) -> GQA attention -> W_O + residual ->
+ * RMSNorm -> SwiGLU -> W_D + residual; then RMSNorm and the LM head on the
+ * block_size-1 mask rows; draft = argmax (lowest token id on ties).
+ *   anchor_dev  int32 [batch]: the clean anchor token of each request.
+ *   draft_dev   int32 [batch][block_size-1]: written.
+ *   logits_dev  fp32 [batch][block_size-1][vocab] or NULL: written if given.
+ * The cache is read, never written. */
+int32_t dflash_draft_block(const dflash_model* model, const dflash_cache* cache, const int32_t* anchor_dev,
+                           int32_t block_size, int32_t* draft_dev, float* logits_dev, void* workspace,
+                           size_t workspace_bytes, dflash_stream_t stream);
+
+/* --- stage 5: greedy lossless verification -----------------------------------
+ * Explainer, "The Target Verifier Remains the Correctness Anchor": accept drafts
+ * left to right while they equal the target's greedy token, stop at the first
+ * rejection; paper §3.1: tau in [1, gamma+1] counts the target's own token.
+ *   draft_dev          int32 [batch][block_size-1]   d_1..d_{g-1}
+ *   target_argmax_dev  int32 [batch][block_size]     y_0..y_{g-1}, y_k = target's
+ *                      greedy token after block position k (y_0 judges d_1)
+ *   accept_len_dev     int32 [batch] written: tau = n + 1, n = leading matches
+ *   out_tokens_dev     int32 [batch][block_size] written: d_1..d_n, y_n, then -1
+ *   next_anchor_dev    int32 [batch] written: y_n (correction or bonus)
+ * Needs no model; batch may be 0 (no launch). */
+int32_t dflash_verify_greedy(const int32_t* draft_dev, const int32_t* target_argmax_dev, int32_t batch,
+                             int32_t block_size, int32_t* accept_len_dev, int32_t* out_tokens_dev,
+                             int32_t* next_anchor_dev, dflash_stream_t stream);
+
+/* --- tracing -------------------------------------------------------------------
+ * Kernel launches made by this library in this process (every entry point,
+ * every device), for launch accounting. */
+uint64_t dflash_launch_count(void);
+
+/* Stage ids reported by the profiler. */
+#define DFLASH_STAGE_FUSE 0     /* fusion GEMM (W_c)                          */
+#define DFLASH_STAGE_INJECT 1   /* K/V injection GEMM (all layers)            */
+#define DFLASH_STAGE_QKV 2      /* drafter Q/K/V GEMMs                        */
+#define DFLASH_STAGE_ATTN 3     /* block attention (split + merge)            */
+#define DFLASH_STAGE_O 4        /* W_O GEMMs                                  */
+#define DFLASH_STAGE_GATEUP 5   /* W_G/W_U GEMMs with SwiGLU                  */
+#define DFLASH_STAGE_DOWN 6     /* W_D GEMMs                                  */
+#define DFLASH_STAGE_LMHEAD 7   /* LM head GEMM with argmax                   */
+#define DFLASH_STAGE_OTHER 8    /* embedding, norms, row maps, argmax read-out */
+#define DFLASH_NUM_STAGES 9
+
+/* Start recording a CUDA event pair around each launch the model's entry
+ * points make (up to max_launches launches), on the stream each call is given.
+ * Meant for measurement runs, not for stream capture. */
+int32_t dflash_profile_start(dflash_model* model, int32_t max_launches);
+
+/* Synchronise `stream`, stop recording and return per stage the summed launch
+ * time in milliseconds and the launch count (arrays of n_stages entries,
+ * n_stages <= DFLASH_NUM_STAGES). */
+int32_t dflash_profile_stop(dflash_model* model, dflash_stream_t stream, float* ms_by_stage,
+                            int32_t* launches_by_stage, int32_t n_stages);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DFLASH_H_ */

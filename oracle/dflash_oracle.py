@@ -42,7 +42,14 @@ from typing import Dict, List, Optional, Sequence
 import numpy as np
 
 F64 = np.float64
-_CHUNK_ROWS = 8192
+_CHUNK_ELEMS = 1 << 25
+
+
+def _f64(a) -> np.ndarray:
+    """float64 copy of a numpy array or a host torch tensor (conversion only)."""
+    if hasattr(a, "detach"):
+        return a.detach().to("cpu").float().numpy().astype(F64)
+    return np.asarray(a, dtype=F64)
 
 
 # ---------------------------------------------------------------------------
@@ -57,9 +64,10 @@ def linear(x: np.ndarray, w: np.ndarray) -> np.ndarray:
     """
     x = np.asarray(x, dtype=F64)
     out = np.empty(x.shape[:-1] + (w.shape[0],), dtype=F64)
-    for r0 in range(0, w.shape[0], _CHUNK_ROWS):
-        r1 = min(r0 + _CHUNK_ROWS, w.shape[0])
-        out[..., r0:r1] = x @ np.asarray(w[r0:r1], dtype=F64).T
+    step = max(1, _CHUNK_ELEMS // max(1, w.shape[1]))
+    for r0 in range(0, w.shape[0], step):
+        r1 = min(r0 + step, w.shape[0])
+        out[..., r0:r1] = x @ _f64(w[r0:r1]).T
     return out
 
 
@@ -73,7 +81,7 @@ def rms_norm(x: np.ndarray, g: np.ndarray, eps: float) -> np.ndarray:
     """
     x = np.asarray(x, dtype=F64)
     ms = np.mean(x * x, axis=-1, keepdims=True)
-    return x / np.sqrt(ms + eps) * np.asarray(g, dtype=F64)
+    return x / np.sqrt(ms + eps) * _f64(g)
 
 
 def silu(x: np.ndarray) -> np.ndarray:
@@ -110,7 +118,7 @@ def fuse_context(feats: np.ndarray, w_c: np.ndarray, g_c: np.ndarray, eps: float
     target layers; the m vectors are concatenated along features in layer order
     to a length-mD vector, projected by W_c [D, mD] and normalised.
     """
-    feats = np.asarray(feats)
+    feats = _f64(feats)
     n = feats.shape[0]
     x = feats.reshape(n, -1)                     # [n, m*D]: [H^(l1)_j ; ... ; H^(lm)_j]
     return rms_norm(linear(x, w_c), g_c, eps)
@@ -242,7 +250,7 @@ def draft_forward(weights: Dict, cfg, cache: RequestCache, anchor: int, block: i
     D, nq, nkv, hd = cfg.hidden, cfg.n_q_heads, cfg.n_kv_heads, cfg.head_dim
     c = cache.length
     tokens = [int(anchor)] + [cfg.mask_id] * (block - 1)
-    x = np.asarray(weights["embed"][tokens], dtype=F64)            # shared embedding rows
+    x = _f64(weights["embed"][tokens])                             # shared embedding rows
     pos = np.arange(c, c + block)
     mask_rows = dflash_mask(c, block)[c:, :]                       # block rows only
     for i, lw in enumerate(weights["layers"]):
@@ -320,6 +328,16 @@ def draft_cycle(weights: Dict, cfg, cache: RequestCache, new_feats: Optional[np.
     fw = draft_forward(weights, cfg, cache, anchor, block, use_mask=use_mask)
     logits, drafts = lm_head_argmax(fw["h"][1:], weights["lm_head"])
     return {"h": fw["h"], "logits": logits, "drafts": drafts}
+
+
+def weights_to_host(w: Dict) -> Dict:
+    """Host copies of a weight dict of torch tensors, dtype kept (bf16 stays
+    bf16; every oracle step upcasts what it reads to float64)."""
+    def conv(t):
+        return t.detach().to("cpu")
+    out = {k: conv(v) for k, v in w.items() if k != "layers"}
+    out["layers"] = [{k: conv(v) for k, v in lw.items()} for lw in w["layers"]]
+    return out
 
 
 def weights_to_numpy(w: Dict) -> Dict:

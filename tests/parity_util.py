@@ -1,0 +1,120 @@
+"""Helpers shared by the GPU parity tests: run the CUDA path through the C ABI
+and the CPU oracle on the same seeded inputs, then compare."""
+from __future__ import annotations
+
+from dataclasses import dataclass
+from typing import List, Optional
+
+import numpy as np
+import torch
+
+import oracle
+from dflash_inputs import (DraftConfig, make_agreement, make_features, make_tokens, make_weights,
+                           synthetic_target_argmax)
+
+FP32_TOL = 1e-4
+BF16_TOL = 2e-2
+ARGMAX_MARGIN = 1e-2
+
+
+def tol(cfg: DraftConfig) -> float:
+    return FP32_TOL if cfg.dtype == "fp32" else BF16_TOL
+
+
+def row_rel_err(gpu: np.ndarray, ref: np.ndarray) -> float:
+    """max over rows of max_v |g - o| / max_v |o| (rows = all but the last axis)."""
+    g = np.asarray(gpu, dtype=np.float64).reshape(-1, gpu.shape[-1])
+    o = np.asarray(ref, dtype=np.float64).reshape(-1, ref.shape[-1])
+    if g.shape[0] == 0:
+        return 0.0
+    den = np.maximum(np.max(np.abs(o), axis=1), 1e-30)
+    return float(np.max(np.max(np.abs(g - o), axis=1) / den))
+
+
+def argmax_check(gpu_drafts: np.ndarray, ref_logits: np.ndarray, margin: float = ARGMAX_MARGIN):
+    """(checked, mismatched, excluded) rows; rows whose oracle top-1 minus
+    top-2 logit is <= margin are excluded (a near-tie)."""
+    lg = np.asarray(ref_logits, dtype=np.float64).reshape(-1, ref_logits.shape[-1])
+    d = np.asarray(gpu_drafts).reshape(-1)
+    top2 = np.sort(lg, axis=1)[:, -2:]
+    gap = top2[:, 1] - top2[:, 0]
+    ref = np.argmax(lg, axis=1)
+    ok_rows = gap > margin
+    mism = int(np.sum((d != ref) & ok_rows))
+    return int(np.sum(ok_rows)), mism, int(np.sum(~ok_rows))
+
+
+@dataclass
+class GpuSide:
+    weights: dict
+    model: object
+    cache: object
+    ws: torch.Tensor
+
+
+def make_gpu(cfg: DraftConfig, seed: int, batch: int, capacity: int, block: int, max_rows: int) -> GpuSide:
+    import block_diffusion_drafter_dflash_gb300 as df
+    w = make_weights(cfg, seed, device="cuda")
+    model = df.Model(cfg, w)
+    cache = df.Cache(model, batch, capacity)
+    ws = df.dflash_workspace(model, batch, capacity, block, max_rows)
+    return GpuSide(w, model, cache, ws)
+
+
+def features_for(cfg: DraftConfig, counts: List[int], seed: int) -> List[torch.Tensor]:
+    """Per-request target features [n_b, m, D] on the GPU (seeded per request)."""
+    return [make_features(cfg, n, seed=seed + 31 * b, device="cuda") for b, n in enumerate(counts)]
+
+
+def gpu_inject(g: GpuSide, feats: List[torch.Tensor], max_rows: Optional[int] = None, host_counts: bool = True,
+               n_new_dev: Optional[torch.Tensor] = None):
+    import block_diffusion_drafter_dflash_gb300 as df
+    counts = [int(f.shape[0]) for f in feats]
+    packed = torch.cat(feats, 0).contiguous() if sum(counts) else torch.empty(
+        (0,) + tuple(feats[0].shape[1:]), dtype=feats[0].dtype, device="cuda")
+    rows = max_rows if max_rows is not None else max(sum(counts), 1)
+    if packed.shape[0] < rows:
+        pad = torch.zeros((rows - packed.shape[0],) + tuple(packed.shape[1:]), dtype=packed.dtype, device="cuda")
+        packed = torch.cat([packed, pad], 0).contiguous()
+    if n_new_dev is None:
+        n_new_dev = torch.tensor(counts, dtype=torch.int32, device="cuda")
+    df.dflash_inject_context(g.model, g.cache, packed, n_new_dev, counts if host_counts else None, rows, g.ws)
+
+
+def gpu_draft(g: GpuSide, anchors: torch.Tensor, block: int, want_logits: bool = True):
+    import block_diffusion_drafter_dflash_gb300 as df
+    B = anchors.shape[0]
+    drafts = torch.full((B, max(block - 1, 0)), -7, dtype=torch.int32, device="cuda")
+    logits = torch.empty((B, max(block - 1, 0), g.model.cfg.vocab), dtype=torch.float32, device="cuda") \
+        if want_logits else None
+    df.dflash_draft_block(g.model, g.cache, anchors, block, drafts, logits, g.ws)
+    return drafts, logits
+
+
+def oracle_caches(cfg: DraftConfig, batch: int) -> List[oracle.RequestCache]:
+    return [oracle.RequestCache(cfg.layers, cfg.n_kv_heads, cfg.head_dim) for _ in range(batch)]
+
+
+def compare_cache(g: GpuSide, caches: List[oracle.RequestCache], t: float, layers=None) -> float:
+    """Worst relative error of the injected context K/V, per (request, layer, head) slab."""
+    K, V = g.cache.k().float().cpu().numpy(), g.cache.v().float().cpu().numpy()
+    lens = g.cache.ctx_len().cpu().numpy()
+    worst = 0.0
+    for b, oc in enumerate(caches):
+        assert lens[b] == oc.length, (b, lens[b], oc.length)
+        for l in (range(len(oc.k)) if layers is None else layers):
+            c = oc.length
+            if c == 0:
+                continue
+            ok = np.transpose(oc.k[l], (1, 0, 2))          # [nkv, c, hd]
+            ov = np.transpose(oc.v[l], (1, 0, 2))
+            worst = max(worst, row_rel_err(K[b, l, :, :c, :].reshape(-1, c * ok.shape[-1]), ok.reshape(-1, c * ok.shape[-1])))
+            worst = max(worst, row_rel_err(V[b, l, :, :c, :].reshape(-1, c * ov.shape[-1]), ov.reshape(-1, c * ov.shape[-1])))
+    assert worst <= t, f"cache relative error {worst:.3e} > {t:.1e}"
+    return worst
+
+
+def synthetic_target(cfg, drafts_cpu: torch.Tensor, accept_p, seed: int) -> torch.Tensor:
+    B, nd = drafts_cpu.shape
+    pat = make_agreement(cfg, B, nd + 1, accept_p, seed=seed)
+    return synthetic_target_argmax(drafts_cpu, pat, cfg.vocab)
