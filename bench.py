@@ -118,19 +118,20 @@ class Clocks:
 # ---------------------------------------------------------------- algorithmic bytes
 def gemm_bytes_per_cycle(cfg, B: int, block: int, inject_rows: int) -> dict:
     """Algorithmic DRAM bytes of each GEMM stage in one cycle: every weight
-    byte once, activations in, outputs out (fp32 residual read + write)."""
-    es = cfg.elem_bytes
+    byte once, activations in (4 bytes a value: fp32, or a bf16 hi/lo pair),
+    outputs out (fp32; the residual stream is read and written)."""
+    es, ea = cfg.elem_bytes, 4
     D, L, m = cfg.hidden, cfg.layers, cfg.n_target_feats
     hq, hk, F, V = cfg.n_q_heads * cfg.head_dim, cfg.n_kv_heads * cfg.head_dim, cfg.ffn, cfg.vocab
     R, Rm, n = B * block, B * (block - 1), inject_rows
     return {
         "fuse": es * D * m * D + es * n * m * D + 4 * n * D,
-        "inject": es * L * 2 * hk * D + es * n * D + es * n * L * 2 * hk,
-        "qkv": L * (es * (hq + 2 * hk) * D + es * R * D + es * R * (hq + 2 * hk)),
-        "o": L * (es * D * hq + es * R * hq + 8 * R * D),
-        "gateup": L * (es * 2 * F * D + es * R * D + es * R * F),
-        "down": L * (es * D * F + es * R * F + 8 * R * D),
-        "lmhead": es * V * D + es * Rm * D + 8 * Rm,
+        "inject": es * L * 2 * hk * D + ea * n * D + 4 * n * L * 2 * hk,
+        "qkv": L * (es * (hq + 2 * hk) * D + ea * R * D + 4 * R * (hq + 2 * hk)),
+        "o": L * (es * D * hq + ea * R * hq + 8 * R * D),
+        "gateup": L * (es * 2 * F * D + ea * R * D + ea * R * F),
+        "down": L * (es * D * F + ea * R * F + 8 * R * D),
+        "lmhead": es * V * D + ea * Rm * D + 8 * Rm,
     }
 
 
@@ -261,8 +262,9 @@ def run_gpu(args, rank, world, local):
 
 
 def kv_bytes(wl) -> int:
+    """Context K/V read by the block attention in one cycle (fp32 cache)."""
     c = wl.cfg
-    return 2 * c.layers * c.n_kv_heads * c.head_dim * c.elem_bytes * sum(wl.ctx)
+    return 2 * c.layers * c.n_kv_heads * c.head_dim * 4 * sum(wl.ctx)
 
 
 def run_e2e(cyc, K, wl, barrier, world):

@@ -107,9 +107,8 @@ class Cache:
 
     def _kv_view(self, off: int) -> torch.Tensor:
         c = self.model.cfg
-        es = self.model.dtype.itemsize
         n = self.batch * c.layers * c.n_kv_heads * self.capacity * c.head_dim
-        return self.buffer[off:off + n * es].view(self.model.dtype).view(
+        return self.buffer[off:off + n * 4].view(torch.float32).view(
             self.batch, c.layers, c.n_kv_heads, self.capacity, c.head_dim)
 
     def k(self) -> torch.Tensor:

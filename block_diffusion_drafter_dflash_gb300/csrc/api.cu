@@ -6,6 +6,7 @@
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <string>
 #include <vector>
@@ -38,8 +39,15 @@ struct dflash_model {
   int sms;
   int32_t* status_dev;     // device status word (first device-detected error)
   double* inv_freq_dev;    // RoPE frequencies theta^(-2i/hd), i < hd/2
+  void* tmaps_dev;         // tensor maps of every weight matrix (bf16 models)
+  int use_tc;              // bf16 projections on the tcgen05 kernel
   Profiler prof;
 };
+
+// Index of a weight matrix's tensor map: 0 lm_head, 1 w_c, then 7 per layer.
+enum { kMapLm = 0, kMapWc = 1, kMapLayer0 = 2 };
+enum { kMapQ = 0, kMapK, kMapV, kMapO, kMapG, kMapU, kMapD, kMapsPerLayer };
+inline int layer_map(int l, int which) { return kMapLayer0 + kMapsPerLayer * l + which; }
 
 struct dflash_cache {
   const dflash_model* model;
@@ -140,21 +148,23 @@ struct WsPlan {
 WsPlan plan_ws(const dflash_model* m, int B, int cap, int block, int max_rows) {
   const dflash_config& c = m->cfg;
   const size_t es = c.dtype == DFLASH_DTYPE_F32 ? 4 : 2;
+  const int pl = c.dtype == DFLASH_DTYPE_F32 ? 1 : 2;   // activation planes
+  const size_t ea = es * pl;                             // bytes per activation element
   const int D = c.hidden, hq = c.n_q_heads * c.head_dim, hk = c.n_kv_heads * c.head_dim, F = c.ffn;
   const int R = B * block, Rm = B * std::max(block - 1, 0);
   WsPlan p{};
   std::vector<const GemmPlan*> used;
   if (max_rows > 0) {
-    p.g_fuse = plan_gemm(c.dtype, max_rows, c.n_target_feats * D, D / kTileN, m->sms);
-    p.g_inject = plan_gemm(c.dtype, max_rows, D, c.layers * 2 * (hk / kTileN), m->sms);
+    p.g_fuse = plan_gemm(c.dtype, max_rows, c.n_target_feats * D, D / kTileN, m->sms, m->use_tc, 1);
+    p.g_inject = plan_gemm(c.dtype, max_rows, D, c.layers * 2 * (hk / kTileN), m->sms, m->use_tc, pl);
     used = {&p.g_fuse, &p.g_inject};
   }
   if (block > 0) {
-    p.g_qkv = plan_gemm(c.dtype, R, D, (hq + 2 * hk) / kTileN, m->sms);
-    p.g_o = plan_gemm(c.dtype, R, hq, D / kTileN, m->sms);
-    p.g_gu = plan_gemm(c.dtype, R, D, F / kHalfN, m->sms);
-    p.g_down = plan_gemm(c.dtype, R, F, D / kTileN, m->sms);
-    p.g_lm = plan_gemm(c.dtype, std::max(Rm, 1), D, c.vocab / kTileN, m->sms);
+    p.g_qkv = plan_gemm(c.dtype, R, D, (hq + 2 * hk) / kTileN, m->sms, m->use_tc, pl);
+    p.g_o = plan_gemm(c.dtype, R, hq, D / kTileN, m->sms, m->use_tc, pl);
+    p.g_gu = plan_gemm(c.dtype, R, D, F / kHalfN, m->sms, m->use_tc, pl);
+    p.g_down = plan_gemm(c.dtype, R, F, D / kTileN, m->sms, m->use_tc, pl);
+    p.g_lm = plan_gemm(c.dtype, std::max(Rm, 1), D, c.vocab / kTileN, m->sms, m->use_tc, pl);
     used.insert(used.end(), {&p.g_qkv, &p.g_o, &p.g_gu, &p.g_down, &p.g_lm});
   }
   size_t partial = 0;
@@ -168,7 +178,7 @@ WsPlan plan_ws(const dflash_model* m, int B, int cap, int block, int max_rows) {
   if (max_rows > 0) {
     p.rowinfo = take(sizeof(int2) * (size_t)max_rows);
     p.yf = take(sizeof(float) * (size_t)max_rows * D);
-    p.ht = take(es * (size_t)max_rows * D);
+    p.ht = take(ea * (size_t)max_rows * D);
   }
   if (block > 0) {
     // attention splits: enough CTAs to cover the device twice over
@@ -180,15 +190,15 @@ WsPlan plan_ws(const dflash_model* m, int B, int cap, int block, int max_rows) {
     p.attn_chunk = chunk;
     p.attn_splits = (keys + chunk - 1) / chunk;
     p.x = take(sizeof(float) * (size_t)R * D);
-    p.u = take(es * (size_t)R * D);
-    p.q = take(es * (size_t)R * hq);
-    p.kb = take(es * (size_t)R * hk);
-    p.vb = take(es * (size_t)R * hk);
+    p.u = take(ea * (size_t)R * D);
+    p.q = take(sizeof(float) * (size_t)R * hq);
+    p.kb = take(sizeof(float) * (size_t)R * hk);
+    p.vb = take(sizeof(float) * (size_t)R * hk);
     p.opart = take(sizeof(float) * (size_t)B * c.n_q_heads * block * p.attn_splits * c.head_dim);
     p.ml = take(sizeof(float2) * (size_t)B * c.n_q_heads * block * p.attn_splits);
-    p.o = take(es * (size_t)R * hq);
-    p.a = take(es * (size_t)R * F);
-    p.hm = take(es * (size_t)std::max(Rm, 1) * D);
+    p.o = take(ea * (size_t)R * hq);
+    p.a = take(ea * (size_t)R * F);
+    p.hm = take(ea * (size_t)std::max(Rm, 1) * D);
     p.slots = take(sizeof(unsigned long long) * (size_t)std::max(Rm, 1));
   }
   p.partial = take(sizeof(float) * partial);
@@ -198,19 +208,27 @@ WsPlan plan_ws(const dflash_model* m, int B, int cap, int block, int max_rows) {
   return p;
 }
 
-GemmProblem make_problem(const void* x, int ldx, int M, int K) {
+// X is `planes` planes of [M][ldx], plane_stride elements apart.
+GemmProblem make_problem(const dflash_model* m, const void* x, int ldx, int M, int K, int planes = 1,
+                         size_t plane_stride = 0) {
   GemmProblem p{};
   p.x = x;
   p.ldx = ldx;
+  p.planes = planes;
+  p.plane_stride = plane_stride;
   p.M = M;
   p.K = K;
+  p.wmaps = m->tmaps_dev;
+  p.status = m->status_dev;
   return p;
 }
 
-void add_seg(GemmProblem& p, const void* w0, const void* w1, int tiles, int paired, int tag) {
+void add_seg(GemmProblem& p, const void* w0, int map0, const void* w1, int map1, int tiles, int paired, int tag) {
   GemmSeg& s = p.seg[p.nseg++];
   s.w0 = w0;
   s.w1 = w1;
+  s.map0 = map0;
+  s.map1 = map1;
   s.tiles = tiles;
   s.tile_begin = p.total_tiles;
   s.paired = paired;
@@ -223,6 +241,7 @@ int32_t run_inject(const dflash_model* m, dflash_cache* cache, const void* feats
                    char* ws, const WsPlan& P, cudaStream_t s) {
   const dflash_config& c = m->cfg;
   const int D = c.hidden, hk = c.n_kv_heads * c.head_dim;
+  const int pl = ActPlanes<T>::n;
   int2* rowinfo = reinterpret_cast<int2*>(ws + P.rowinfo);
   float* yf = reinterpret_cast<float*>(ws + P.yf);
   T* ht = reinterpret_cast<T*>(ws + P.ht);
@@ -233,23 +252,24 @@ int32_t run_inject(const dflash_model* m, dflash_cache* cache, const void* feats
   DF_LAUNCH(DFLASH_STAGE_OTHER, 1,
             inject_prep_launch(n_new, ctx_len, cache->batch, max_rows, cache->cap, rowinfo, counters, P.counters_n,
                                m->status_dev, s), "inject_prep");
-  GemmProblem pf = make_problem(feats, c.n_target_feats * D, max_rows, c.n_target_feats * D);
-  add_seg(pf, m->w_c, m->w_c, D / kTileN, 0, 0);
+  GemmProblem pf = make_problem(m, feats, c.n_target_feats * D, max_rows, c.n_target_feats * D);
+  add_seg(pf, m->w_c, kMapWc, m->w_c, kMapWc, D / kTileN, 0, 0);
   apply_plan(pf, P.g_fuse, partial, counters);
   DF_LAUNCH(DFLASH_STAGE_FUSE, 1, (gemm_launch<T, EpiStoreF32>(pf, P.g_fuse, EpiStoreF32{yf, D}, s)), "fusion GEMM");
   DF_LAUNCH(DFLASH_STAGE_OTHER, 1,
-            fuse_norm_launch<T>(yf, static_cast<const T*>(m->g_c), c.rms_eps, rowinfo, max_rows, D, ht, s),
+            fuse_norm_launch<T>(yf, static_cast<const T*>(m->g_c), c.rms_eps, rowinfo, max_rows, D, ht,
+                                (size_t)max_rows * D, s),
             "fusion norm");
 
-  GemmProblem pi = make_problem(ht, D, max_rows, D);
+  GemmProblem pi = make_problem(m, ht, D, max_rows, D, pl, (size_t)max_rows * D);
   for (int l = 0; l < c.layers; ++l) {
-    add_seg(pi, m->layers[l].w_k, m->layers[l].w_k, hk / kTileN, 0, 2 * l);
-    add_seg(pi, m->layers[l].w_v, m->layers[l].w_v, hk / kTileN, 0, 2 * l + 1);
+    add_seg(pi, m->layers[l].w_k, layer_map(l, kMapK), m->layers[l].w_k, layer_map(l, kMapK), hk / kTileN, 0, 2 * l);
+    add_seg(pi, m->layers[l].w_v, layer_map(l, kMapV), m->layers[l].w_v, layer_map(l, kMapV), hk / kTileN, 0, 2 * l + 1);
   }
   apply_plan(pi, P.g_inject, partial, counters);
-  EpiInject<T> ei{reinterpret_cast<T*>(cache->base + cache->k_off), reinterpret_cast<T*>(cache->base + cache->v_off),
-                  rowinfo, m->inv_freq_dev, c.layers, c.n_kv_heads, c.head_dim, cache->cap};
-  DF_LAUNCH(DFLASH_STAGE_INJECT, 1, (gemm_launch<T, EpiInject<T>>(pi, P.g_inject, ei, s)), "injection GEMM");
+  EpiInject ei{reinterpret_cast<float*>(cache->base + cache->k_off), reinterpret_cast<float*>(cache->base + cache->v_off),
+               rowinfo, m->inv_freq_dev, c.layers, c.n_kv_heads, c.head_dim, cache->cap};
+  DF_LAUNCH(DFLASH_STAGE_INJECT, 1, (gemm_launch<T, EpiInject>(pi, P.g_inject, ei, s)), "injection GEMM");
   return DFLASH_OK;
 }
 
@@ -260,11 +280,12 @@ int32_t run_draft(const dflash_model* m, const dflash_cache* cache, const int32_
   const int B = cache->batch, D = c.hidden, F = c.ffn;
   const int hq = c.n_q_heads * c.head_dim, hk = c.n_kv_heads * c.head_dim;
   const int R = B * block, Rm = B * (block - 1);
+  const int pl = ActPlanes<T>::n;
   float* x = reinterpret_cast<float*>(ws + P.x);
   T* u = reinterpret_cast<T*>(ws + P.u);
-  T* q = reinterpret_cast<T*>(ws + P.q);
-  T* kb = reinterpret_cast<T*>(ws + P.kb);
-  T* vb = reinterpret_cast<T*>(ws + P.vb);
+  float* q = reinterpret_cast<float*>(ws + P.q);
+  float* kb = reinterpret_cast<float*>(ws + P.kb);
+  float* vb = reinterpret_cast<float*>(ws + P.vb);
   T* o = reinterpret_cast<T*>(ws + P.o);
   T* a = reinterpret_cast<T*>(ws + P.a);
   T* hm = reinterpret_cast<T*>(ws + P.hm);
@@ -274,23 +295,24 @@ int32_t run_draft(const dflash_model* m, const dflash_cache* cache, const int32_
   const int32_t* ctx_len = reinterpret_cast<const int32_t*>(cache->base + cache->len_off);
 
   DF_LAUNCH(DFLASH_STAGE_OTHER, 1, embed_norm_launch<T>(static_cast<const T*>(m->embed), anchor, c.mask_token_id, c.vocab, B, block, D,
-                               static_cast<const T*>(m->layers[0].g_in), c.rms_eps, x, u, counters, P.counters_n,
+                               static_cast<const T*>(m->layers[0].g_in), c.rms_eps, x, u, (size_t)R * D, counters,
+                               P.counters_n,
                                m->status_dev, s),
           "embedding");
   for (int l = 0; l < c.layers; ++l) {
     const dflash_layer_weights& L = m->layers[l];
-    GemmProblem pq = make_problem(u, D, R, D);
-    add_seg(pq, L.w_q, L.w_q, hq / kTileN, 0, 0);
-    add_seg(pq, L.w_k, L.w_k, hk / kTileN, 0, 1);
-    add_seg(pq, L.w_v, L.w_v, hk / kTileN, 0, 2);
+    GemmProblem pq = make_problem(m, u, D, R, D, pl, (size_t)R * D);
+    add_seg(pq, L.w_q, layer_map(l, kMapQ), L.w_q, layer_map(l, kMapQ), hq / kTileN, 0, 0);
+    add_seg(pq, L.w_k, layer_map(l, kMapK), L.w_k, layer_map(l, kMapK), hk / kTileN, 0, 1);
+    add_seg(pq, L.w_v, layer_map(l, kMapV), L.w_v, layer_map(l, kMapV), hk / kTileN, 0, 2);
     apply_plan(pq, P.g_qkv, partial, counters);
-    EpiQKV<T> eq{q, kb, vb, ctx_len, m->inv_freq_dev, block, c.n_q_heads, c.n_kv_heads, c.head_dim};
-    DF_LAUNCH(DFLASH_STAGE_QKV, 1, (gemm_launch<T, EpiQKV<T>>(pq, P.g_qkv, eq, s)), "QKV GEMM");
+    EpiQKV eq{q, kb, vb, ctx_len, m->inv_freq_dev, block, c.n_q_heads, c.n_kv_heads, c.head_dim};
+    DF_LAUNCH(DFLASH_STAGE_QKV, 1, (gemm_launch<T, EpiQKV>(pq, P.g_qkv, eq, s)), "QKV GEMM");
 
     AttnParams ap{};
     ap.q = q; ap.kb = kb; ap.vb = vb;
-    ap.kc = cache->base + cache->k_off;
-    ap.vc = cache->base + cache->v_off;
+    ap.kc = reinterpret_cast<const float*>(cache->base + cache->k_off);
+    ap.vc = reinterpret_cast<const float*>(cache->base + cache->v_off);
     ap.ctx_len = ctx_len;
     ap.layer = l; ap.layers = c.layers; ap.cap = cache->cap;
     ap.B = B; ap.nq = c.n_q_heads; ap.nkv = c.n_kv_heads; ap.hd = c.head_dim; ap.block = block;
@@ -298,41 +320,69 @@ int32_t run_draft(const dflash_model* m, const dflash_cache* cache, const int32_
     ap.opart = reinterpret_cast<float*>(ws + P.opart);
     ap.ml = reinterpret_cast<float2*>(ws + P.ml);
     ap.out = o;
+    ap.out_plane = (size_t)R * hq;
     ap.scale = 1.0f / sqrtf((float)c.head_dim);
     DF_LAUNCH(DFLASH_STAGE_ATTN, 2, attention_launch<T>(ap, s), "attention");
 
-    GemmProblem po = make_problem(o, hq, R, hq);
-    add_seg(po, L.w_o, L.w_o, D / kTileN, 0, 0);
+    GemmProblem po = make_problem(m, o, hq, R, hq, pl, (size_t)R * hq);
+    add_seg(po, L.w_o, layer_map(l, kMapO), L.w_o, layer_map(l, kMapO), D / kTileN, 0, 0);
     apply_plan(po, P.g_o, partial, counters);
     DF_LAUNCH(DFLASH_STAGE_O, 1, (gemm_launch<T, EpiResidual>(po, P.g_o, EpiResidual{x, D}, s)), "O GEMM");
-    DF_LAUNCH(DFLASH_STAGE_OTHER, 1, rmsnorm_launch<T>(x, static_cast<const T*>(L.g_post), c.rms_eps, R, D, u, s),
+    DF_LAUNCH(DFLASH_STAGE_OTHER, 1,
+              rmsnorm_launch<T>(x, static_cast<const T*>(L.g_post), c.rms_eps, R, D, u, (size_t)R * D, s),
               "post-attention norm");
 
-    GemmProblem pg = make_problem(u, D, R, D);
-    add_seg(pg, L.w_g, L.w_u, F / kHalfN, 1, 0);
+    GemmProblem pg = make_problem(m, u, D, R, D, pl, (size_t)R * D);
+    add_seg(pg, L.w_g, layer_map(l, kMapG), L.w_u, layer_map(l, kMapU), F / kHalfN, 1, 0);
     apply_plan(pg, P.g_gu, partial, counters);
-    DF_LAUNCH(DFLASH_STAGE_GATEUP, 1, (gemm_launch<T, EpiSwiGLU<T>>(pg, P.g_gu, EpiSwiGLU<T>{a, F}, s)),
+    DF_LAUNCH(DFLASH_STAGE_GATEUP, 1, (gemm_launch<T, EpiSwiGLU<T>>(pg, P.g_gu, EpiSwiGLU<T>{a, F, (size_t)R * F}, s)),
               "gate/up GEMM");
 
-    GemmProblem pd = make_problem(a, F, R, F);
-    add_seg(pd, L.w_d, L.w_d, D / kTileN, 0, 0);
+    GemmProblem pd = make_problem(m, a, F, R, F, pl, (size_t)R * F);
+    add_seg(pd, L.w_d, layer_map(l, kMapD), L.w_d, layer_map(l, kMapD), D / kTileN, 0, 0);
     apply_plan(pd, P.g_down, partial, counters);
     DF_LAUNCH(DFLASH_STAGE_DOWN, 1, (gemm_launch<T, EpiResidual>(pd, P.g_down, EpiResidual{x, D}, s)), "down GEMM");
     if (l + 1 < c.layers)
       DF_LAUNCH(DFLASH_STAGE_OTHER, 1,
-                rmsnorm_launch<T>(x, static_cast<const T*>(m->layers[l + 1].g_in), c.rms_eps, R, D, u, s),
+                rmsnorm_launch<T>(x, static_cast<const T*>(m->layers[l + 1].g_in), c.rms_eps, R, D, u, (size_t)R * D, s),
                 "input norm");
   }
   if (Rm == 0) return DFLASH_OK;
   DF_LAUNCH(DFLASH_STAGE_OTHER, 1,
-            final_norm_launch<T>(x, static_cast<const T*>(m->g_final), c.rms_eps, B, block, D, hm, slots, s),
+            final_norm_launch<T>(x, static_cast<const T*>(m->g_final), c.rms_eps, B, block, D, hm, (size_t)Rm * D, slots,
+                                 s),
             "final norm");
-  GemmProblem pl = make_problem(hm, D, Rm, D);
-  add_seg(pl, m->lm_head, m->lm_head, c.vocab / kTileN, 0, 0);
-  apply_plan(pl, P.g_lm, partial, counters);
-  DF_LAUNCH(DFLASH_STAGE_LMHEAD, 1, (gemm_launch<T, EpiArgmax>(pl, P.g_lm, EpiArgmax{slots, logits, c.vocab}, s)),
+  GemmProblem plm = make_problem(m, hm, D, Rm, D, pl, (size_t)Rm * D);
+  add_seg(plm, m->lm_head, kMapLm, m->lm_head, kMapLm, c.vocab / kTileN, 0, 0);
+  apply_plan(plm, P.g_lm, partial, counters);
+  DF_LAUNCH(DFLASH_STAGE_LMHEAD, 1, (gemm_launch<T, EpiArgmax>(plm, P.g_lm, EpiArgmax{slots, logits, c.vocab}, s)),
             "LM head GEMM");
   DF_LAUNCH(DFLASH_STAGE_OTHER, 1, argmax_finalize_launch(slots, Rm, drafts, s), "argmax");
+  return DFLASH_OK;
+}
+
+// Tensor maps of every weight matrix, copied once to device memory.
+int32_t build_weight_maps(dflash_model* m) {
+  const dflash_config& c = m->cfg;
+  const int D = c.hidden, hq = c.n_q_heads * c.head_dim, hk = c.n_kv_heads * c.head_dim, F = c.ffn;
+  const size_t mb = tensor_map_bytes();
+  const int n = kMapLayer0 + kMapsPerLayer * c.layers;
+  std::vector<unsigned char> host(mb * n);
+  auto enc = [&](int idx, const void* w, int inner, int rows) {
+    if (reinterpret_cast<uintptr_t>(w) % 16) return false;
+    return encode_weight_map(host.data() + mb * idx, w, inner, rows);
+  };
+  bool ok = enc(kMapLm, m->lm_head, D, c.vocab) && enc(kMapWc, m->w_c, c.n_target_feats * D, D);
+  for (int l = 0; ok && l < c.layers; ++l) {
+    const dflash_layer_weights& L = m->layers[l];
+    ok = enc(layer_map(l, kMapQ), L.w_q, D, hq) && enc(layer_map(l, kMapK), L.w_k, D, hk) &&
+         enc(layer_map(l, kMapV), L.w_v, D, hk) && enc(layer_map(l, kMapO), L.w_o, hq, D) &&
+         enc(layer_map(l, kMapG), L.w_g, D, F) && enc(layer_map(l, kMapU), L.w_u, D, F) &&
+         enc(layer_map(l, kMapD), L.w_d, F, D);
+  }
+  if (!ok) return fail(DFLASH_ERR_UNSUPPORTED, "could not encode weight tensor maps (16-B aligned weights needed)");
+  DF_CUDA(cudaMalloc(&m->tmaps_dev, host.size()), "tensor maps");
+  DF_CUDA(cudaMemcpy(m->tmaps_dev, host.data(), host.size(), cudaMemcpyHostToDevice), "tensor maps");
   return DFLASH_OK;
 }
 
@@ -381,6 +431,15 @@ int32_t dflash_model_create(const dflash_config* cfg, const dflash_weights* w, d
     dflash_model_destroy(m);
     return cuda_fail(e, "model state");
   }
+  const char* gemm_env = std::getenv("DFLASH_GEMM");
+  m->use_tc = cfg->dtype == DFLASH_DTYPE_BF16 && !(gemm_env && std::strcmp(gemm_env, "simt") == 0);
+  if (m->use_tc) {
+    rc = build_weight_maps(m);
+    if (rc) {
+      dflash_model_destroy(m);
+      return rc;
+    }
+  }
   *out = m;
   return DFLASH_OK;
 }
@@ -389,6 +448,7 @@ int32_t dflash_model_destroy(dflash_model* m) {
   if (!m) return DFLASH_OK;
   if (m->status_dev) cudaFree(m->status_dev);
   if (m->inv_freq_dev) cudaFree(m->inv_freq_dev);
+  if (m->tmaps_dev) cudaFree(m->tmaps_dev);
   for (cudaEvent_t e : m->prof.ev) cudaEventDestroy(e);
   delete m;
   return DFLASH_OK;
@@ -410,8 +470,7 @@ int32_t dflash_clear_status(const dflash_model* m, dflash_stream_t stream) {
 
 size_t dflash_cache_bytes(const dflash_config* cfg, int32_t batch, int32_t capacity) {
   if (check_config(cfg) != DFLASH_OK || batch < 0 || capacity < 0) return 0;
-  const size_t es = cfg->dtype == DFLASH_DTYPE_F32 ? 4 : 2;
-  const size_t kv = es * (size_t)batch * cfg->layers * cfg->n_kv_heads * (size_t)capacity * cfg->head_dim;
+  const size_t kv = sizeof(float) * (size_t)batch * cfg->layers * cfg->n_kv_heads * (size_t)capacity * cfg->head_dim;
   return align256(kv) * 2 + align256(sizeof(int32_t) * std::max(batch, 1));
 }
 
@@ -427,8 +486,7 @@ int32_t dflash_cache_init(const dflash_model* m, void* dev_mem, size_t bytes, in
   if (bytes < need) return fail(DFLASH_ERR_CAPACITY, "cache memory %zu bytes < %zu needed", bytes, need);
   int32_t rc = check_device(m);
   if (rc) return rc;
-  const size_t es = m->cfg.dtype == DFLASH_DTYPE_F32 ? 4 : 2;
-  const size_t kv = es * (size_t)batch * m->cfg.layers * m->cfg.n_kv_heads * (size_t)capacity * m->cfg.head_dim;
+  const size_t kv = sizeof(float) * (size_t)batch * m->cfg.layers * m->cfg.n_kv_heads * (size_t)capacity * m->cfg.head_dim;
   dflash_cache* c = new dflash_cache();
   c->model = m;
   c->base = static_cast<char*>(dev_mem);

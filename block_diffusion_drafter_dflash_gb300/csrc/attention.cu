@@ -8,10 +8,15 @@
 // a running sum and an unnormalised output per row, and a second kernel merges
 // the splits exactly (log-sum-exp rescaling).
 #include <cfloat>
+#include <type_traits>
 
 #include "kernels.cuh"
 
 namespace dflash {
+
+// tensor-core split kernel for bf16 models (attention_mma.cu)
+cudaError_t attention_mma_prepare(int hd);
+cudaError_t attention_mma_split_launch(const AttnParams& p, cudaStream_t s);
 
 namespace {
 
@@ -45,11 +50,11 @@ __global__ void __launch_bounds__(kAttnThreads) attn_split_kernel(const __grid_c
   float* Ms = Vs + kKeyTile * hd;       // [rows]
   float* Ls = Ms + rows;                // [rows]
 
-  const T* q = static_cast<const T*>(p.q);
+  const float* q = p.q;
   for (int e = threadIdx.x; e < rows * hd; e += kAttnThreads) {
     int r = e / hd, d = e - r * hd, g = r / p.block, k = r - g * p.block;
     int qh = kvh * G + g;
-    Qs[e] = to_f32(q[(((size_t)b * p.nq + qh) * p.block + k) * hd + d]) * p.scale;
+    Qs[e] = q[(((size_t)b * p.nq + qh) * p.block + k) * hd + d] * p.scale;
     Os[e] = 0.f;
   }
   for (int r = threadIdx.x; r < rows; r += kAttnThreads) {
@@ -57,10 +62,10 @@ __global__ void __launch_bounds__(kAttnThreads) attn_split_kernel(const __grid_c
     Ls[r] = 0.f;
   }
 
-  const T* kc = static_cast<const T*>(p.kc) + (((size_t)b * p.layers + p.layer) * p.nkv + kvh) * p.cap * hd;
-  const T* vc = static_cast<const T*>(p.vc) + (((size_t)b * p.layers + p.layer) * p.nkv + kvh) * p.cap * hd;
-  const T* kb = static_cast<const T*>(p.kb) + ((size_t)b * p.nkv + kvh) * p.block * hd;
-  const T* vb = static_cast<const T*>(p.vb) + ((size_t)b * p.nkv + kvh) * p.block * hd;
+  const float* kc = p.kc + (((size_t)b * p.layers + p.layer) * p.nkv + kvh) * p.cap * hd;
+  const float* vc = p.vc + (((size_t)b * p.layers + p.layer) * p.nkv + kvh) * p.cap * hd;
+  const float* kb = p.kb + ((size_t)b * p.nkv + kvh) * p.block * hd;
+  const float* vb = p.vb + ((size_t)b * p.nkv + kvh) * p.block * hd;
 
   for (int jt = j0; jt < j1; jt += kKeyTile) {
     const int n = min(kKeyTile, j1 - jt);
@@ -69,11 +74,11 @@ __global__ void __launch_bounds__(kAttnThreads) attn_split_kernel(const __grid_c
       int jj = e / hd, d = e - jj * hd, j = jt + jj;
       float kv, vv;
       if (j < c) {
-        kv = to_f32(kc[(size_t)j * hd + d]);
-        vv = to_f32(vc[(size_t)j * hd + d]);
+        kv = kc[(size_t)j * hd + d];
+        vv = vc[(size_t)j * hd + d];
       } else {
-        kv = to_f32(kb[(size_t)(j - c) * hd + d]);
-        vv = to_f32(vb[(size_t)(j - c) * hd + d]);
+        kv = kb[(size_t)(j - c) * hd + d];
+        vv = vb[(size_t)(j - c) * hd + d];
       }
       Ks[jj * (hd + 1) + d] = kv;
       Vs[jj * hd + d] = vv;
@@ -127,12 +132,13 @@ __global__ void attn_combine_kernel(const __grid_constant__ AttnParams p) {
   for (int s = 0; s < p.splits; ++s)
     if (ml[s].y > 0.f) L += ml[s].y * __expf(ml[s].x - M);
   const float inv = 1.f / L;
-  T* out = static_cast<T*>(p.out) + ((size_t)b * p.block + k) * p.nq * p.hd + (size_t)qh * p.hd;
+  T* out = static_cast<T*>(p.out);
+  const size_t base = ((size_t)b * p.block + k) * p.nq * p.hd + (size_t)qh * p.hd;
   for (int d = threadIdx.x; d < p.hd; d += blockDim.x) {
     float acc = 0.f;
     for (int s = 0; s < p.splits; ++s)
       if (ml[s].y > 0.f) acc += p.opart[((size_t)row * p.splits + s) * p.hd + d] * __expf(ml[s].x - M);
-    out[d] = from_f32<T>(acc * inv);
+    put_act(out, p.out_plane, base + d, acc * inv);
   }
 }
 
@@ -146,6 +152,7 @@ int attention_max_rows() { return kMaxRows; }
 
 template <typename T>
 cudaError_t attention_prepare(int rows, int hd) {
+  if constexpr (std::is_same<T, __nv_bfloat16>::value) return attention_mma_prepare(hd);
   return cudaFuncSetAttribute(attn_split_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               (int)attn_smem_bytes(rows, hd));
 }
@@ -153,10 +160,14 @@ cudaError_t attention_prepare(int rows, int hd) {
 template <typename T>
 cudaError_t attention_launch(const AttnParams& p, cudaStream_t s) {
   if (p.B <= 0) return cudaSuccess;
-  const int rows = (p.nq / p.nkv) * p.block;
-  const size_t smem = attn_smem_bytes(rows, p.hd);
-  attn_split_kernel<T><<<dim3(p.splits, p.nkv, p.B), kAttnThreads, smem, s>>>(p);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e;
+  if constexpr (std::is_same<T, __nv_bfloat16>::value) {
+    e = attention_mma_split_launch(p, s);
+  } else {
+    const int rows = (p.nq / p.nkv) * p.block;
+    attn_split_kernel<T><<<dim3(p.splits, p.nkv, p.B), kAttnThreads, attn_smem_bytes(rows, p.hd), s>>>(p);
+    e = cudaGetLastError();
+  }
   if (e != cudaSuccess) return e;
   attn_combine_kernel<T><<<p.B * p.nq * p.block, 128, 0, s>>>(p);
   return cudaGetLastError();

@@ -23,6 +23,27 @@ template <typename T> __device__ __forceinline__ T from_f32(float v);
 template <> __device__ __forceinline__ float from_f32<float>(float v) { return v; }
 template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float v) { return __float2bfloat16_rn(v); }
 
+// ---------------------------------------------------------------- activations
+// Every tensor handed from one step of the cycle to the next is kept at fp32
+// precision.  fp32 models store it as fp32 (one plane).  bf16 models store
+// each value v as two bf16 planes, hi = bf16(v) and lo = bf16(v - hi), which
+// the tensor cores consume as two operands against the same (exact) bf16
+// weights: hi*W + lo*W carries ~16 significant bits of v instead of 8.
+template <typename T> struct ActPlanes;
+template <> struct ActPlanes<float> { static constexpr int n = 1; };
+template <> struct ActPlanes<__nv_bfloat16> { static constexpr int n = 2; };
+
+__device__ __forceinline__ void put_act(float* base, size_t /*plane*/, size_t i, float v) { base[i] = v; }
+__device__ __forceinline__ void put_act(__nv_bfloat16* base, size_t plane, size_t i, float v) {
+  const __nv_bfloat16 hi = __float2bfloat16_rn(v);
+  base[i] = hi;
+  base[plane + i] = __float2bfloat16_rn(v - __bfloat162float(hi));
+}
+__device__ __forceinline__ float get_act(const float* base, size_t /*plane*/, size_t i) { return base[i]; }
+__device__ __forceinline__ float get_act(const __nv_bfloat16* base, size_t plane, size_t i) {
+  return __bfloat162float(base[i]) + __bfloat162float(base[plane + i]);
+}
+
 // ---------------------------------------------------------------- device status
 // First device-detected error wins; later ones are dropped.
 __device__ __forceinline__ void report_status(int32_t* status, int32_t code) {
@@ -62,6 +83,7 @@ __device__ __forceinline__ int unpack_argmax_index(unsigned long long k) {
 struct GemmSeg {
   const void* w0;
   const void* w1;
+  int map0, map1;  // tensor-map indices of w0 / w1 (tensor-core path)
   int tiles;       // 128-feature output tiles in this segment
   int tile_begin;  // first global tile index of this segment
   int paired;
@@ -69,8 +91,10 @@ struct GemmSeg {
 };
 
 struct GemmProblem {
-  const void* x;   // activations [M][K], row stride ldx elements
+  const void* x;   // activations: `planes` planes of [M][K], row stride ldx elements
   int ldx;
+  int planes;          // 1, or 2 for a hi/lo bf16 pair
+  size_t plane_stride; // elements from plane 0 to plane 1 (a multiple of ldx)
   int M;
   int K;
   int nseg;
@@ -79,6 +103,8 @@ struct GemmProblem {
   int kblocks_per_split;   // in units of 64 columns of K
   float* partial;      // [splits][M][total_tiles*128] when splits > 1
   int* counters;       // [token tiles][total_tiles], zero between launches
+  const void* wmaps;   // device array of weight tensor maps (tensor-core path)
+  int32_t* status;     // device status word
   GemmSeg seg[kMaxSeg];
 };
 

@@ -19,20 +19,22 @@ __device__ __forceinline__ float block_sum(float v, float* red) {
   return t;
 }
 
-// u = x * rsqrt(mean(x^2) + eps) * g for one row held in fp32.
+// u = x * rsqrt(mean(x^2) + eps) * g for one row held in fp32; u is a GEMM
+// activation operand (planes `plane` elements apart).
 template <typename T>
-__device__ __forceinline__ void norm_row(const float* x, const T* g, float eps, int D, T* u, float* red) {
+__device__ __forceinline__ void norm_row(const float* x, const T* g, float eps, int D, T* u, size_t plane,
+                                         float* red) {
   float ss = 0.f;
   for (int i = threadIdx.x; i < D; i += blockDim.x) ss = fmaf(x[i], x[i], ss);
   const float r = rsqrtf(block_sum(ss, red) / (float)D + eps);
-  for (int i = threadIdx.x; i < D; i += blockDim.x) u[i] = from_f32<T>(x[i] * r * to_f32(g[i]));
+  for (int i = threadIdx.x; i < D; i += blockDim.x) put_act(u, plane, i, x[i] * r * to_f32(g[i]));
 }
 
 template <typename T>
 __global__ void __launch_bounds__(kRowThreads) embed_norm_kernel(const T* embed, const int32_t* anchor, int mask_id,
                                                                  int vocab, int block, int D, const T* g, float eps,
-                                                                 float* x, T* u, int* zero_ptr, int zero_n,
-                                                                 int32_t* status) {
+                                                                 float* x, T* u, size_t plane, int* zero_ptr,
+                                                                 int zero_n, int32_t* status) {
   __shared__ float red[32];
   const int row = blockIdx.x, b = row / block, k = row - b * block;
   if (zero_ptr)
@@ -46,35 +48,37 @@ __global__ void __launch_bounds__(kRowThreads) embed_norm_kernel(const T* embed,
   float* xr = x + (size_t)row * D;
   for (int i = threadIdx.x; i < D; i += blockDim.x) xr[i] = to_f32(e[i]);
   __syncthreads();
-  norm_row(xr, g, eps, D, u + (size_t)row * D, red);
+  norm_row(xr, g, eps, D, u + (size_t)row * D, plane, red);
 }
 
 template <typename T>
-__global__ void __launch_bounds__(kRowThreads) rmsnorm_kernel(const float* x, const T* g, float eps, int D, T* u) {
+__global__ void __launch_bounds__(kRowThreads) rmsnorm_kernel(const float* x, const T* g, float eps, int D, T* u,
+                                                              size_t plane) {
   __shared__ float red[32];
-  norm_row(x + (size_t)blockIdx.x * D, g, eps, D, u + (size_t)blockIdx.x * D, red);
+  norm_row(x + (size_t)blockIdx.x * D, g, eps, D, u + (size_t)blockIdx.x * D, plane, red);
 }
 
 template <typename T>
 __global__ void __launch_bounds__(kRowThreads) final_norm_kernel(const float* x, const T* g, float eps, int block,
-                                                                 int D, T* hm, unsigned long long* slots) {
+                                                                 int D, T* hm, size_t plane,
+                                                                 unsigned long long* slots) {
   __shared__ float red[32];
   const int r = blockIdx.x;                   // compact mask-row index
   const int b = r / (block - 1), k = r - b * (block - 1) + 1;
   if (threadIdx.x == 0) slots[r] = 0ull;
-  norm_row(x + ((size_t)b * block + k) * D, g, eps, D, hm + (size_t)r * D, red);
+  norm_row(x + ((size_t)b * block + k) * D, g, eps, D, hm + (size_t)r * D, plane, red);
 }
 
 template <typename T>
 __global__ void __launch_bounds__(kRowThreads) fuse_norm_kernel(const float* y, const T* g, float eps,
-                                                                const int2* rowinfo, int D, T* ht) {
+                                                                const int2* rowinfo, int D, T* ht, size_t plane) {
   __shared__ float red[32];
   const int row = blockIdx.x;
   if (rowinfo[row].x < 0) {
-    for (int i = threadIdx.x; i < D; i += blockDim.x) ht[(size_t)row * D + i] = from_f32<T>(0.f);
+    for (int i = threadIdx.x; i < D; i += blockDim.x) put_act(ht, plane, (size_t)row * D + i, 0.f);
     return;
   }
-  norm_row(y + (size_t)row * D, g, eps, D, ht + (size_t)row * D, red);
+  norm_row(y + (size_t)row * D, g, eps, D, ht + (size_t)row * D, plane, red);
 }
 
 // One CTA: exclusive scan of n_new, per-row (request, position), ctx_len update.
@@ -161,34 +165,34 @@ __global__ void verify_kernel(const int32_t* draft, const int32_t* target, int B
 
 template <typename T>
 cudaError_t embed_norm_launch(const T* embed, const int32_t* anchor, int mask_id, int vocab, int B, int block, int D,
-                              const T* g, float eps, float* x, T* u, int* zero_ptr, int zero_n, int32_t* status,
-                              cudaStream_t s) {
+                              const T* g, float eps, float* x, T* u, size_t plane, int* zero_ptr, int zero_n,
+                              int32_t* status, cudaStream_t s) {
   if (B * block == 0) return cudaSuccess;
-  embed_norm_kernel<T><<<B * block, kRowThreads, 0, s>>>(embed, anchor, mask_id, vocab, block, D, g, eps, x, u,
+  embed_norm_kernel<T><<<B * block, kRowThreads, 0, s>>>(embed, anchor, mask_id, vocab, block, D, g, eps, x, u, plane,
                                                          zero_ptr, zero_n, status);
   return cudaGetLastError();
 }
 
 template <typename T>
-cudaError_t rmsnorm_launch(const float* x, const T* g, float eps, int rows, int D, T* u, cudaStream_t s) {
+cudaError_t rmsnorm_launch(const float* x, const T* g, float eps, int rows, int D, T* u, size_t plane, cudaStream_t s) {
   if (rows == 0) return cudaSuccess;
-  rmsnorm_kernel<T><<<rows, kRowThreads, 0, s>>>(x, g, eps, D, u);
+  rmsnorm_kernel<T><<<rows, kRowThreads, 0, s>>>(x, g, eps, D, u, plane);
   return cudaGetLastError();
 }
 
 template <typename T>
-cudaError_t final_norm_launch(const float* x, const T* g, float eps, int B, int block, int D, T* hm,
+cudaError_t final_norm_launch(const float* x, const T* g, float eps, int B, int block, int D, T* hm, size_t plane,
                               unsigned long long* slots, cudaStream_t s) {
   if (B * (block - 1) == 0) return cudaSuccess;
-  final_norm_kernel<T><<<B * (block - 1), kRowThreads, 0, s>>>(x, g, eps, block, D, hm, slots);
+  final_norm_kernel<T><<<B * (block - 1), kRowThreads, 0, s>>>(x, g, eps, block, D, hm, plane, slots);
   return cudaGetLastError();
 }
 
 template <typename T>
 cudaError_t fuse_norm_launch(const float* y, const T* g, float eps, const int2* rowinfo, int rows, int D, T* ht,
-                             cudaStream_t s) {
+                             size_t plane, cudaStream_t s) {
   if (rows == 0) return cudaSuccess;
-  fuse_norm_kernel<T><<<rows, kRowThreads, 0, s>>>(y, g, eps, rowinfo, D, ht);
+  fuse_norm_kernel<T><<<rows, kRowThreads, 0, s>>>(y, g, eps, rowinfo, D, ht, plane);
   return cudaGetLastError();
 }
 
@@ -216,11 +220,12 @@ cudaError_t verify_launch(const int32_t* draft, const int32_t* target, int B, in
 
 #define DFLASH_EW_INST(T)                                                                                        \
   template cudaError_t embed_norm_launch<T>(const T*, const int32_t*, int, int, int, int, int, const T*, float,     \
-                                            float*, T*, int*, int, int32_t*, cudaStream_t);                       \
-  template cudaError_t rmsnorm_launch<T>(const float*, const T*, float, int, int, T*, cudaStream_t);              \
-  template cudaError_t final_norm_launch<T>(const float*, const T*, float, int, int, int, T*, unsigned long long*, \
-                                            cudaStream_t);                                                        \
-  template cudaError_t fuse_norm_launch<T>(const float*, const T*, float, const int2*, int, int, T*, cudaStream_t);
+                                            float*, T*, size_t, int*, int, int32_t*, cudaStream_t);               \
+  template cudaError_t rmsnorm_launch<T>(const float*, const T*, float, int, int, T*, size_t, cudaStream_t);      \
+  template cudaError_t final_norm_launch<T>(const float*, const T*, float, int, int, int, T*, size_t,              \
+                                            unsigned long long*, cudaStream_t);                                   \
+  template cudaError_t fuse_norm_launch<T>(const float*, const T*, float, const int2*, int, int, T*, size_t,      \
+                                           cudaStream_t);
 
 DFLASH_EW_INST(float)
 DFLASH_EW_INST(__nv_bfloat16)

@@ -38,17 +38,19 @@ struct EpiResidual {
 
 // a[row][j] = silu(gate_j) * up_j for a paired (W_G, W_U) tile: features
 // 0..63 of the tile are gate rows 64t.., features 64..127 the matching up rows.
+// `a` is the next GEMM's activation operand (planes `plane` elements apart).
 template <typename T>
 struct EpiSwiGLU {
   T* a;
   int lda;
+  size_t plane;
   __device__ __forceinline__ void operator()(const float* t, int ld, int m0, int mc, int, const GemmSeg&,
                                              int tis) const {
     for (int idx = threadIdx.x; idx < mc * kHalfN; idx += blockDim.x) {
       int m = idx / kHalfN, c = idx % kHalfN;
       float g = t[c * ld + m], u = t[(c + kHalfN) * ld + m];
       float s = g / (1.0f + __expf(-g));
-      a[(size_t)(m0 + m) * lda + (size_t)tis * kHalfN + c] = from_f32<T>(s * u);
+      put_act(a, plane, (size_t)(m0 + m) * lda + (size_t)tis * kHalfN + c, s * u);
     }
   }
 };
@@ -67,52 +69,50 @@ __device__ __forceinline__ float rope_apply(const float* t, int ld, int m, int n
 }
 
 // Block Q/K/V of one draft layer: tag 0 = Q, 1 = K, 2 = V.  Row = b*block + k
-// sits at position ctx_len[b] + k; Q and K get RoPE.  Outputs are
+// sits at position ctx_len[b] + k; Q and K get RoPE.  Outputs are fp32,
 // head-major [b][head][k][hd].
-template <typename T>
 struct EpiQKV {
-  T* q;
-  T* kb;
-  T* vb;
+  float* q;
+  float* kb;
+  float* vb;
   const int32_t* ctx_len;
   const double* inv_freq;
   int block, nq, nkv, hd;
   __device__ __forceinline__ void operator()(const float* t, int ld, int m0, int mc, int, const GemmSeg& sg,
                                              int tis) const {
     const int tag = sg.tag;
-    T* dst = tag == 0 ? q : (tag == 1 ? kb : vb);
+    float* dst = tag == 0 ? q : (tag == 1 ? kb : vb);
     const int nh = tag == 0 ? nq : nkv;
     for (int idx = threadIdx.x; idx < mc * kTileN; idx += blockDim.x) {
       int m = idx / kTileN, n = idx % kTileN;
       int row = m0 + m, b = row / block, k = row - b * block;
       int feat = tis * kTileN + n, head = feat / hd, d = feat - head * hd;
       float v = tag == 2 ? t[n * ld + m] : rope_apply(t, ld, m, n, d, hd, ctx_len[b] + k, inv_freq);
-      dst[(((size_t)b * nh + head) * block + k) * hd + d] = from_f32<T>(v);
+      dst[(((size_t)b * nh + head) * block + k) * hd + d] = v;
     }
   }
 };
 
 // Context K/V injection: tag = 2*layer + (0: K, 1: V).  rowinfo[row] =
 // (request, position) or (-1, -1) for padding rows.  Writes the cache
-// [b][layer][kvh][pos][hd]; K gets RoPE at its absolute position.
-template <typename T>
+// [b][layer][kvh][pos][hd] (fp32); K gets RoPE at its absolute position.
 struct EpiInject {
-  T* kc;
-  T* vc;
+  float* kc;
+  float* vc;
   const int2* rowinfo;
   const double* inv_freq;
   int layers, nkv, hd, cap;
   __device__ __forceinline__ void operator()(const float* t, int ld, int m0, int mc, int, const GemmSeg& sg,
                                              int tis) const {
     const int layer = sg.tag >> 1, is_v = sg.tag & 1;
-    T* dst = is_v ? vc : kc;
+    float* dst = is_v ? vc : kc;
     for (int idx = threadIdx.x; idx < mc * kTileN; idx += blockDim.x) {
       int m = idx / kTileN, n = idx % kTileN;
       int2 ri = rowinfo[m0 + m];
       if (ri.x < 0) continue;
       int feat = tis * kTileN + n, head = feat / hd, d = feat - head * hd;
       float v = is_v ? t[n * ld + m] : rope_apply(t, ld, m, n, d, hd, ri.y, inv_freq);
-      dst[((((size_t)ri.x * layers + layer) * nkv + head) * cap + ri.y) * hd + d] = from_f32<T>(v);
+      dst[((((size_t)ri.x * layers + layer) * nkv + head) * cap + ri.y) * hd + d] = v;
     }
   }
 };

@@ -7,6 +7,7 @@
 // atomic ticket, no waiting) adds the partials in split order — so results do
 // not depend on scheduling — and runs the epilogue.
 #include <algorithm>
+#include <type_traits>
 
 #include "gemm.cuh"
 
@@ -50,7 +51,10 @@ __global__ void __launch_bounds__(kSimtThreads) gemm_simt_kernel(const __grid_co
     }
     for (int e = tid; e < kSimtBM * kSimtBK; e += kSimtThreads) {
       int m = e / kSimtBK, kk = e % kSimtBK;
-      sx[m][kk] = m < mc ? to_f32(X[(size_t)(m0 + m) * p.ldx + k0 + kk]) : 0.f;
+      float v = 0.f;
+      if (m < mc)
+        for (int pl = 0; pl < p.planes; ++pl) v += to_f32(X[pl * p.plane_stride + (size_t)(m0 + m) * p.ldx + k0 + kk]);
+      sx[m][kk] = v;
     }
     __syncthreads();
 #pragma unroll 8
@@ -100,10 +104,11 @@ __global__ void __launch_bounds__(kSimtThreads) gemm_simt_kernel(const __grid_co
 
 }  // namespace
 
-GemmPlan plan_gemm(int dtype, int M, int K, int tiles, int sms) {
-  (void)dtype;
+GemmPlan plan_gemm(int dtype, int M, int K, int tiles, int sms, int tc, int planes) {
+  if (dtype == DFLASH_DTYPE_BF16 && tc) return plan_gemm_tc(M, K, tiles, sms, planes);
   GemmPlan g{};
   g.tc = 0;
+  g.planes = planes;
   g.bm = kSimtBM;
   g.token_tiles = (M + kSimtBM - 1) / kSimtBM;
   const int kblocks = K / 64;
@@ -127,6 +132,9 @@ void apply_plan(GemmProblem& p, const GemmPlan& plan, float* partial, int* count
 template <typename T, class Epi>
 cudaError_t gemm_launch(const GemmProblem& p, const GemmPlan& plan, const Epi& epi, cudaStream_t s) {
   if (p.M <= 0 || p.total_tiles <= 0) return cudaSuccess;
+  if constexpr (std::is_same<T, __nv_bfloat16>::value) {
+    if (plan.tc) return gemm_tc_launch<Epi>(p, plan, epi, s);
+  }
   dim3 grid(p.total_tiles, plan.splits, plan.token_tiles);
   gemm_simt_kernel<T, Epi><<<grid, kSimtThreads, 0, s>>>(p, epi);
   return cudaGetLastError();
@@ -139,10 +147,10 @@ cudaError_t gemm_launch(const GemmProblem& p, const GemmPlan& plan, const Epi& e
                                                    cudaStream_t);                                       \
   template cudaError_t gemm_launch<T, EpiSwiGLU<T>>(const GemmProblem&, const GemmPlan&,                 \
                                                     const EpiSwiGLU<T>&, cudaStream_t);                 \
-  template cudaError_t gemm_launch<T, EpiQKV<T>>(const GemmProblem&, const GemmPlan&, const EpiQKV<T>&,  \
+  template cudaError_t gemm_launch<T, EpiQKV>(const GemmProblem&, const GemmPlan&, const EpiQKV&,        \
+                                              cudaStream_t);                                            \
+  template cudaError_t gemm_launch<T, EpiInject>(const GemmProblem&, const GemmPlan&, const EpiInject&,  \
                                                  cudaStream_t);                                         \
-  template cudaError_t gemm_launch<T, EpiInject<T>>(const GemmProblem&, const GemmPlan&,                 \
-                                                    const EpiInject<T>&, cudaStream_t);                 \
   template cudaError_t gemm_launch<T, EpiArgmax>(const GemmProblem&, const GemmPlan&, const EpiArgmax&,  \
                                                  cudaStream_t);
 

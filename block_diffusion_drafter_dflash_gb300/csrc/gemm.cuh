@@ -9,6 +9,7 @@ namespace dflash {
 // How one GEMM launch is cut: token rows per CTA tile, split-K.
 struct GemmPlan {
   int tc;               // 1: tcgen05 tensor-core kernel, 0: CUDA-core kernel
+  int planes;           // activation planes the kernel reads
   int bm;               // token rows per CTA tile
   int token_tiles;
   int splits;
@@ -18,7 +19,20 @@ struct GemmPlan {
 };
 
 // Decide the cut for an M x (tiles*128) x K product on a device with `sms` SMs.
-GemmPlan plan_gemm(int dtype, int M, int K, int tiles, int sms);
+// bf16 products use the tcgen05 kernel unless `tc` is 0.
+// `planes` = activation planes (2 for a hi/lo bf16 pair).
+GemmPlan plan_gemm(int dtype, int M, int K, int tiles, int sms, int tc, int planes);
+GemmPlan plan_gemm_tc(int M, int K, int tiles, int sms, int planes);
+
+// Tensor maps (CUtensorMap, 128 B each) for the tensor-core kernel: a weight
+// matrix [rows][inner] bf16 read in 64x64 boxes, and an activation matrix
+// [rows][row_stride] bf16 read in 64 x box_rows boxes.  128-byte swizzle.
+bool encode_weight_map(void* map, const void* base, int inner, int rows);
+bool encode_activation_map(void* map, const void* base, int inner, int rows, int row_stride, int box_rows);
+size_t tensor_map_bytes();
+
+template <class Epi>
+cudaError_t gemm_tc_launch(const GemmProblem& p, const GemmPlan& plan, const Epi& epi, cudaStream_t s);
 
 // Fill the plan's fields into the problem (splits, kblocks, scratch pointers).
 void apply_plan(GemmProblem& p, const GemmPlan& plan, float* partial, int* counters);

@@ -2,9 +2,11 @@
 //
 // Swap-AB form: the weight tile is the MMA's M side and the token rows are
 // its N side,
-//     D[128 features x BN tokens] += W[128 x 64] . X[BN x 64]^T   per stage,
+//     D[128 features x PL*BN] += W[128 x 64] . [X_hi ; X_lo][PL*BN x 64]^T   per stage,
 // so one kernel covers batch 1 (BN = 16: weight streaming, HBM-bound) and
-// batch 32 (BN = 256: dense, tensor-bound).  One thread issues TMA loads of
+// batch 32 (BN = 128: dense, tensor-bound).  Activations carried as a hi/lo
+// bf16 pair (PL = 2) occupy two row blocks of the N side; the epilogue adds
+// the two accumulator columns of each token.  One thread issues TMA loads of
 // both operands (128-B swizzle, K-major) into a ring of shared-memory stages;
 // one thread issues tcgen05.mma into a tensor-memory accumulator and frees
 // each stage with tcgen05.commit; all four warps then read the accumulator
@@ -25,27 +27,44 @@ namespace dflash {
 
 namespace {
 
-template <int BN>
+template <int BN, int PL>
 struct TcCfg {
-  static constexpr int kStages = BN <= 64 ? 5 : 4;
+  static constexpr int kN = BN * PL;                  // MMA N
+  static constexpr int kStages = kN <= 64 ? 5 : 4;
   static constexpr int kABytes = kTileN * 128;        // 128 rows x 64 bf16
-  static constexpr int kBBytes = BN * 128;            // BN rows x 64 bf16
+  static constexpr int kBBytes = kN * 128;            // PL*BN rows x 64 bf16
   static constexpr int kStageBytes = kABytes + kBBytes;
-  static constexpr int kTmemCols = BN <= 32 ? 32 : BN;
+  static constexpr int kTmemCols = kN <= 32 ? 32 : kN;
   static constexpr int kChunk = BN < 32 ? BN : 32;    // token columns per epilogue pass
   static constexpr int kBarBytes = 256;
   static constexpr int kSmem = 1024 + kStages * kStageBytes + kBarBytes;
   static_assert(kStageBytes % 1024 == 0, "stages must keep 1024-B alignment");
+  static_assert(kN <= 256 && kN % 16 == 0, "MMA N must be a multiple of 16 up to 256");
   static_assert(kTileN * (kChunk + 1) * 4 <= kStages * kStageBytes, "epilogue tile must fit the stages");
 };
 
-constexpr long long kWaitBudget = 4000000000LL;  // SM cycles (~2 s): far beyond any legal wait
+// Accumulator columns c0..c0+CH-1 of this warp's lanes; with a hi/lo operand
+// pair the lo block (columns BN..2BN-1) is added.
+template <int BN, int PL, int CH>
+__device__ __forceinline__ void load_acc(uint32_t trow, int c0, float* v) {
+#pragma unroll
+  for (int h = 0; h < CH; h += 16) ptx::tmem_ld16(trow + c0 + h, v + h);
+  if constexpr (PL == 2) {
+    float w[CH];
+#pragma unroll
+    for (int h = 0; h < CH; h += 16) ptx::tmem_ld16(trow + BN + c0 + h, w + h);
+#pragma unroll
+    for (int j = 0; j < CH; ++j) v[j] += w[j];
+  }
+}
 
-template <int BN, class Epi>
+constexpr long long kWaitBudget = 200000000LL;   // SM cycles (~0.1 s): far beyond any legal wait
+
+template <int BN, int PL, class Epi>
 __global__ void __launch_bounds__(128, 1) gemm_tc_kernel(const __grid_constant__ CUtensorMap xmap,
                                                          const __grid_constant__ GemmProblem p,
                                                          const __grid_constant__ Epi epi, int32_t* status) {
-  using C = TcCfg<BN>;
+  using C = TcCfg<BN, PL>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kStages * C::kStageBytes);
@@ -102,13 +121,16 @@ __global__ void __launch_bounds__(128, 1) gemm_tc_kernel(const __grid_constant__
       const int kx = (kb0 + i) * 64;
       ptx::tma_load_2d(a, map0, full + s, kx, r0, pol_w);
       ptx::tma_load_2d(a + kHalfN * 128, map1, full + s, kx, r1, pol_w);
-      ptx::tma_load_2d(a + C::kABytes, &xmap, full + s, kx, m0, pol_x);
+      const int prow = static_cast<int>(p.plane_stride / p.ldx);
+#pragma unroll
+      for (int pl = 0; pl < PL; ++pl)
+        ptx::tma_load_2d(a + C::kABytes + pl * BN * 128, &xmap, full + s, kx, pl * prow + m0, pol_x);
       ++issued;
     }
     flags[2] = issued;
   } else if (warp == 1 && lane == 0) {
     // ---- MMA issuer
-    constexpr uint32_t idesc = ptx::idesc_bf16_f32(kTileN, BN);
+    constexpr uint32_t idesc = ptx::idesc_bf16_f32(kTileN, C::kN);
     for (int i = 0; i < nk; ++i) {
       const int s = i % C::kStages;
       if (!ptx::mbar_wait(full + s, (i / C::kStages) & 1, kWaitBudget, status)) {
@@ -141,8 +163,7 @@ __global__ void __launch_bounds__(128, 1) gemm_tc_kernel(const __grid_constant__
     if (p.splits == 1) {
       for (int c0 = 0; c0 < mc; c0 += C::kChunk) {
         float v[C::kChunk];
-#pragma unroll
-        for (int h = 0; h < C::kChunk; h += 16) ptx::tmem_ld16(trow + c0 + h, v + h);
+        load_acc<BN, PL, C::kChunk>(trow, c0, v);
 #pragma unroll
         for (int j = 0; j < C::kChunk; ++j) st[n * ld + j] = v[j];
         __syncthreads();
@@ -153,8 +174,7 @@ __global__ void __launch_bounds__(128, 1) gemm_tc_kernel(const __grid_constant__
       const size_t ntot = static_cast<size_t>(p.total_tiles) * kTileN;
       for (int c0 = 0; c0 < mc; c0 += C::kChunk) {
         float v[C::kChunk];
-#pragma unroll
-        for (int h = 0; h < C::kChunk; h += 16) ptx::tmem_ld16(trow + c0 + h, v + h);
+        load_acc<BN, PL, C::kChunk>(trow, c0, v);
 #pragma unroll
         for (int j = 0; j < C::kChunk; ++j)
           if (c0 + j < mc)
@@ -220,19 +240,23 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-template <int BN, class Epi>
+template <int BN, int PL, class Epi>
 cudaError_t launch_bn(const GemmProblem& p, const GemmPlan& plan, const Epi& epi, cudaStream_t s) {
-  using C = TcCfg<BN>;
+  using C = TcCfg<BN, PL>;
   static bool attr_set = false;   // per instantiation; the attribute is per device function
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<BN, Epi>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+    cudaError_t e =
+        cudaFuncSetAttribute(gemm_tc_kernel<BN, PL, Epi>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
+  if (p.planes != PL || p.plane_stride % p.ldx) return cudaErrorInvalidValue;
+  // one map over both planes: plane 1 starts plane_stride/ldx rows after plane 0
+  const int rows = PL == 1 ? p.M : static_cast<int>(p.plane_stride / p.ldx) + p.M;
   CUtensorMap xmap;
-  if (!encode_activation_map(&xmap, p.x, p.K, p.M, p.ldx, BN)) return cudaErrorInvalidValue;
+  if (!encode_activation_map(&xmap, p.x, p.K, rows, p.ldx, BN)) return cudaErrorInvalidValue;
   dim3 grid(p.total_tiles, plan.splits, plan.token_tiles);
-  gemm_tc_kernel<BN, Epi><<<grid, 128, C::kSmem, s>>>(xmap, p, epi, p.status);
+  gemm_tc_kernel<BN, PL, Epi><<<grid, 128, C::kSmem, s>>>(xmap, p, epi, p.status);
   return cudaGetLastError();
 }
 
@@ -264,12 +288,15 @@ bool encode_activation_map(void* map, const void* base, int inner, int rows, int
 
 size_t tensor_map_bytes() { return sizeof(CUtensorMap); }
 
-GemmPlan plan_gemm_tc(int M, int K, int tiles, int sms) {
+GemmPlan plan_gemm_tc(int M, int K, int tiles, int sms, int planes) {
   GemmPlan g{};
   g.tc = 1;
+  g.planes = planes;
+  const int bm_max = planes == 2 ? 128 : 256;   // MMA N = planes * bm <= 256
   g.bm = M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : M <= 128 ? 128 : 256;
+  g.bm = std::min(g.bm, bm_max);
   g.token_tiles = (M + g.bm - 1) / g.bm;
-  const int cps = g.bm <= 64 ? 2 : 1;   // CTAs resident per SM (shared-memory bound)
+  const int cps = g.bm * planes <= 32 ? 2 : 1;   // CTAs resident per SM (shared-memory bound)
   const int kblocks = K / 64;
   const long ctas = (long)tiles * g.token_tiles;
   int splits = (int)std::max(1L, (long)sms * cps / ctas);
@@ -283,12 +310,21 @@ GemmPlan plan_gemm_tc(int M, int K, int tiles, int sms) {
 
 template <class Epi>
 cudaError_t gemm_tc_launch(const GemmProblem& p, const GemmPlan& plan, const Epi& epi, cudaStream_t s) {
+  if (plan.planes == 1) {   // operands that are exact in bf16 (target features)
+    switch (plan.bm) {
+      case 16: return launch_bn<16, 1, Epi>(p, plan, epi, s);
+      case 32: return launch_bn<32, 1, Epi>(p, plan, epi, s);
+      case 64: return launch_bn<64, 1, Epi>(p, plan, epi, s);
+      case 128: return launch_bn<128, 1, Epi>(p, plan, epi, s);
+      case 256: return launch_bn<256, 1, Epi>(p, plan, epi, s);
+      default: return cudaErrorInvalidValue;
+    }
+  }
   switch (plan.bm) {
-    case 16: return launch_bn<16, Epi>(p, plan, epi, s);
-    case 32: return launch_bn<32, Epi>(p, plan, epi, s);
-    case 64: return launch_bn<64, Epi>(p, plan, epi, s);
-    case 128: return launch_bn<128, Epi>(p, plan, epi, s);
-    case 256: return launch_bn<256, Epi>(p, plan, epi, s);
+    case 16: return launch_bn<16, 2, Epi>(p, plan, epi, s);
+    case 32: return launch_bn<32, 2, Epi>(p, plan, epi, s);
+    case 64: return launch_bn<64, 2, Epi>(p, plan, epi, s);
+    case 128: return launch_bn<128, 2, Epi>(p, plan, epi, s);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -297,10 +333,8 @@ template cudaError_t gemm_tc_launch<EpiStoreF32>(const GemmProblem&, const GemmP
 template cudaError_t gemm_tc_launch<EpiResidual>(const GemmProblem&, const GemmPlan&, const EpiResidual&, cudaStream_t);
 template cudaError_t gemm_tc_launch<EpiSwiGLU<__nv_bfloat16>>(const GemmProblem&, const GemmPlan&,
                                                               const EpiSwiGLU<__nv_bfloat16>&, cudaStream_t);
-template cudaError_t gemm_tc_launch<EpiQKV<__nv_bfloat16>>(const GemmProblem&, const GemmPlan&,
-                                                           const EpiQKV<__nv_bfloat16>&, cudaStream_t);
-template cudaError_t gemm_tc_launch<EpiInject<__nv_bfloat16>>(const GemmProblem&, const GemmPlan&,
-                                                              const EpiInject<__nv_bfloat16>&, cudaStream_t);
+template cudaError_t gemm_tc_launch<EpiQKV>(const GemmProblem&, const GemmPlan&, const EpiQKV&, cudaStream_t);
+template cudaError_t gemm_tc_launch<EpiInject>(const GemmProblem&, const GemmPlan&, const EpiInject&, cudaStream_t);
 template cudaError_t gemm_tc_launch<EpiArgmax>(const GemmProblem&, const GemmPlan&, const EpiArgmax&, cudaStream_t);
 
 }  // namespace dflash

@@ -9,11 +9,11 @@ namespace dflash {
 // Block queries of one draft layer against [context K/V of the cache ; block K/V]
 // (no mask: every block row sees all context and the whole block).
 struct AttnParams {
-  const void* q;        // [B][nq][block][hd]   (RoPE applied)
-  const void* kb;       // [B][nkv][block][hd]  (RoPE applied)
-  const void* vb;       // [B][nkv][block][hd]
-  const void* kc;       // cache K [B][layers][nkv][cap][hd]
-  const void* vc;       // cache V
+  const float* q;       // [B][nq][block][hd]   (RoPE applied)
+  const float* kb;      // [B][nkv][block][hd]  (RoPE applied)
+  const float* vb;      // [B][nkv][block][hd]
+  const float* kc;      // cache K [B][layers][nkv][cap][hd]
+  const float* vc;      // cache V
   const int32_t* ctx_len;
   int layer, layers, cap;
   int B, nq, nkv, hd, block;
@@ -21,7 +21,8 @@ struct AttnParams {
   int splits;
   float* opart;         // [B][nq][block][splits][hd] unnormalised partial outputs
   float2* ml;           // [B][nq][block][splits] (running max, running sum)
-  void* out;            // [B*block][nq*hd] dtype
+  void* out;            // [B*block][nq*hd]: the W_O GEMM's activation operand
+  size_t out_plane;     // elements between its hi and lo planes
   float scale;          // 1/sqrt(hd)
 };
 
@@ -34,25 +35,27 @@ int attention_max_rows();   // largest (nq/nkv)*block the kernel accepts
 // x[row] = E[token(row)], token = anchor[b] at block position 0 else mask_id;
 // u[row] = RMSNorm(x[row]) * g.  Also zeroes `zero_n` ints at `zero_ptr`.
 // An anchor outside [0, vocab) sets DFLASH_ERR_INVALID_ARG in `status`.
+// Outputs written as GEMM activation operands (`plane` = elements between the
+// hi and lo planes of a bf16 model; unused for fp32).
 template <typename T>
 cudaError_t embed_norm_launch(const T* embed, const int32_t* anchor, int mask_id, int vocab, int B, int block, int D,
-                              const T* g, float eps, float* x, T* u, int* zero_ptr, int zero_n, int32_t* status,
-                              cudaStream_t s);
+                              const T* g, float eps, float* x, T* u, size_t plane, int* zero_ptr, int zero_n,
+                              int32_t* status, cudaStream_t s);
 
 // u[row] = RMSNorm(x[row]) * g for `rows` rows.
 template <typename T>
-cudaError_t rmsnorm_launch(const float* x, const T* g, float eps, int rows, int D, T* u, cudaStream_t s);
+cudaError_t rmsnorm_launch(const float* x, const T* g, float eps, int rows, int D, T* u, size_t plane, cudaStream_t s);
 
 // Final norm of the mask rows only (block position >= 1), compacted to
 // hm[b*(block-1) + k-1]; zeroes the argmax slots of those rows.
 template <typename T>
-cudaError_t final_norm_launch(const float* x, const T* g, float eps, int B, int block, int D, T* hm,
+cudaError_t final_norm_launch(const float* x, const T* g, float eps, int B, int block, int D, T* hm, size_t plane,
                               unsigned long long* slots, cudaStream_t s);
 
 // H_t[row] = RMSNorm(y[row]) * g_c for rows with rowinfo[row].x >= 0, 0 otherwise.
 template <typename T>
 cudaError_t fuse_norm_launch(const float* y, const T* g, float eps, const int2* rowinfo, int rows, int D, T* ht,
-                             cudaStream_t s);
+                             size_t plane, cudaStream_t s);
 
 // Row -> (request, position) map of an injection and the ctx_len update.
 cudaError_t inject_prep_launch(const int32_t* n_new, int32_t* ctx_len, int B, int max_rows, int cap,

@@ -42,17 +42,22 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 }
 
 // Wait for phase `parity` of `bar` for at most ~`budget` SM clock cycles.
-// Returns false (and sets `timeout` in the device status) if the budget runs out.
+// Returns false if the budget runs out (and sets DFLASH_ERR_TIMEOUT in the
+// device status word), or as soon as another CTA has already reported a
+// timeout there, so that a broken launch drains quickly.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, long long budget, int32_t* status) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
-  while (!mbar_try_wait(bar, parity)) {
-    if (clock64() - t0 > budget) {
-      report_status(status, DFLASH_ERR_TIMEOUT);
-      return false;
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 255) == 0) {
+      if (status && *reinterpret_cast<volatile int32_t*>(status) == DFLASH_ERR_TIMEOUT) return false;
+      if (clock64() - t0 > budget) {
+        report_status(status, DFLASH_ERR_TIMEOUT);
+        return false;
+      }
     }
   }
-  return true;
 }
 
 // ---------------------------------------------------------------- TMA

@@ -21,8 +21,11 @@
  *    DEVICE memory owned by the caller; pointers named *_host are host memory.
  *    Nothing is copied: weight pointers are borrowed for the model's lifetime.
  *  - Matrices are row-major [out_features, in_features] (the Linear layout).
- *    Storage type of weights, features, cache and activations is the model's
- *    dtype (DFLASH_DTYPE_F32 or DFLASH_DTYPE_BF16); accumulation is fp32.
+ *    Weights and target features are stored in the model's dtype
+ *    (DFLASH_DTYPE_F32 or DFLASH_DTYPE_BF16).  Everything computed from them —
+ *    the context K/V cache and every activation — is kept at fp32 precision and
+ *    accumulated in fp32 (bf16 models feed the tensor cores each activation as
+ *    a hi + lo bf16 pair against the exact bf16 weights).
  *  - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy
  *    default stream).  Arguments are validated on the host before any launch;
  *    a non-zero return means nothing was launched, and dflash_last_error()
@@ -134,8 +137,8 @@ int32_t dflash_clear_status(const dflash_model* model, dflash_stream_t stream);
 /* --- persistent draft KV cache (paper §4.1: context K/V stored in the draft
  * model's KV cache and reused across drafting iterations) ----------------------
  * Layout inside the caller's block of device memory (each region 256-B aligned):
- *   K [batch][layers][n_kv_heads][capacity][head_dim]   (dtype, RoPE applied)
- *   V [batch][layers][n_kv_heads][capacity][head_dim]   (dtype)
+ *   K [batch][layers][n_kv_heads][capacity][head_dim]   (fp32, RoPE applied)
+ *   V [batch][layers][n_kv_heads][capacity][head_dim]   (fp32)
  *   ctx_len int32 [batch]                                (tokens held per request)
  * Only context entries live in the cache; a block's own K/V never does. */
 size_t dflash_cache_bytes(const dflash_config* cfg, int32_t batch, int32_t capacity);

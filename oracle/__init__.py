@@ -7,5 +7,5 @@ which passages of the DFlash pages each function follows.
 from .dflash_oracle import *  # noqa: F401,F403
 from .dflash_oracle import (RequestCache, attention_block, attention_masked, dflash_mask, draft_cycle,
                             draft_forward, expected_accept_len, fuse_context, inject_context, inject_kv,
-                            linear, lm_head_argmax, rms_norm, rope, silu, verify_greedy, weights_to_host,
+                            linear, lm_head_argmax, rms_norm, rope, silu, store, verify_greedy, weights_to_host,
                             weights_to_numpy)

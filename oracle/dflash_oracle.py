@@ -52,6 +52,27 @@ def _f64(a) -> np.ndarray:
     return np.asarray(a, dtype=F64)
 
 
+def store(x: np.ndarray, mode: str = "f64") -> np.ndarray:
+    """Round values to the storage type a drafter keeps its activations in.
+
+    "f64": no rounding (the exact definition).  "fp32": round to float32.
+    "bf16": round to float32, then to bfloat16 (round to nearest, ties to
+    even, on the upper 16 bits) — a bf16 drafter keeps every tensor handed
+    from one step to the next in bf16 while accumulating in float32.  The
+    result is returned as float64.
+    """
+    if mode == "f64":
+        return x
+    f = np.asarray(x, dtype=np.float32)
+    if mode == "fp32":
+        return f.astype(F64)
+    if mode != "bf16":
+        raise ValueError(mode)
+    u = f.view(np.uint32).astype(np.uint64)
+    u = (u + 0x7FFF + ((u >> 16) & 1)) & 0xFFFF0000
+    return u.astype(np.uint32).view(np.float32).astype(F64)
+
+
 # ---------------------------------------------------------------------------
 # Small building blocks
 # ---------------------------------------------------------------------------
@@ -111,7 +132,7 @@ def rope(x: np.ndarray, positions: Sequence[int], theta: float) -> np.ndarray:
 # Stage 1: context fusion  (paper §7.3; explainer "Target Hidden States ...")
 # ---------------------------------------------------------------------------
 
-def fuse_context(feats: np.ndarray, w_c: np.ndarray, g_c: np.ndarray, eps: float) -> np.ndarray:
+def fuse_context(feats: np.ndarray, w_c: np.ndarray, g_c: np.ndarray, eps: float, mode: str = "f64") -> np.ndarray:
     """H_t = RMSNorm(W_c [H^(l1); ...; H^(lm)]) for every new context token.
 
     feats: [n, m, D], the hidden state of token j at each of the m selected
@@ -121,7 +142,7 @@ def fuse_context(feats: np.ndarray, w_c: np.ndarray, g_c: np.ndarray, eps: float
     feats = _f64(feats)
     n = feats.shape[0]
     x = feats.reshape(n, -1)                     # [n, m*D]: [H^(l1)_j ; ... ; H^(lm)_j]
-    return rms_norm(linear(x, w_c), g_c, eps)
+    return store(rms_norm(linear(x, w_c), g_c, eps), mode)
 
 
 # ---------------------------------------------------------------------------
@@ -129,7 +150,7 @@ def fuse_context(feats: np.ndarray, w_c: np.ndarray, g_c: np.ndarray, eps: float
 # ---------------------------------------------------------------------------
 
 def inject_kv(h_t: np.ndarray, w_k: np.ndarray, w_v: np.ndarray, positions: Sequence[int],
-              n_kv_heads: int, head_dim: int, theta: float):
+              n_kv_heads: int, head_dim: int, theta: float, mode: str = "f64"):
     """Context keys and values of one draft layer: W^K H_t and W^V H_t.
 
     Only keys get the rotary embedding; a context token j injected for a
@@ -141,7 +162,7 @@ def inject_kv(h_t: np.ndarray, w_k: np.ndarray, w_v: np.ndarray, positions: Sequ
     n = h_t.shape[0]
     k = linear(h_t, w_k).reshape(n, n_kv_heads, head_dim)
     v = linear(h_t, w_v).reshape(n, n_kv_heads, head_dim)
-    return rope(k, positions, theta), v
+    return store(rope(k, positions, theta), mode), store(v, mode)
 
 
 class RequestCache:
@@ -158,14 +179,15 @@ class RequestCache:
         return self.k[0].shape[0]
 
 
-def inject_context(weights: Dict, cfg, cache: RequestCache, feats: np.ndarray) -> np.ndarray:
+def inject_context(weights: Dict, cfg, cache: RequestCache, feats: np.ndarray, mode: str = "f64") -> np.ndarray:
     """Stages 1+2 for one request: fuse the new tokens' target features and
-    append their K/V to every layer of the cache.  Returns H_t."""
-    h_t = fuse_context(feats, weights["w_c"], weights["g_c"], cfg.rms_eps)
+    append their K/V to every layer of the cache.  Returns H_t.  `mode` is the
+    storage rounding of H_t and of the cached K/V (see `store`)."""
+    h_t = fuse_context(feats, weights["w_c"], weights["g_c"], cfg.rms_eps, mode)
     c = cache.length
     pos = np.arange(c, c + h_t.shape[0])
     for i, lw in enumerate(weights["layers"]):
-        k, v = inject_kv(h_t, lw["w_k"], lw["w_v"], pos, cfg.n_kv_heads, cfg.head_dim, cfg.rope_theta)
+        k, v = inject_kv(h_t, lw["w_k"], lw["w_v"], pos, cfg.n_kv_heads, cfg.head_dim, cfg.rope_theta, mode)
         cache.k[i] = np.concatenate([cache.k[i], k], axis=0)
         cache.v[i] = np.concatenate([cache.v[i], v], axis=0)
     return h_t
@@ -237,7 +259,7 @@ def attention_block(q: np.ndarray, k_ctx: np.ndarray, v_ctx: np.ndarray,
 
 
 def draft_forward(weights: Dict, cfg, cache: RequestCache, anchor: int, block: int,
-                  use_mask: bool = True) -> Dict[str, np.ndarray]:
+                  use_mask: bool = True, mode: str = "f64") -> Dict[str, np.ndarray]:
     """One non-causal drafter pass over [anchor, mask, ..., mask] (block rows).
 
     Per layer i (Qwen3-style): u = RMSNorm(x); Q = W^Q u, K = W^K u, V = W^V u
@@ -246,6 +268,9 @@ def draft_forward(weights: Dict, cfg, cache: RequestCache, anchor: int, block: i
     [W^K H_t ; W^K H_d], V_i likewise); attention through the DFlash mask;
     x += W^O o; u = RMSNorm(x); x += W^D (silu(W^G u) * W^U u).  After the
     last layer h = RMSNorm_final(x).  The block's own K/V is not kept.
+    `mode` rounds every tensor handed from one step to the next (normed
+    inputs, Q/K/V, attention output, SwiGLU product, h) to a storage type; the
+    residual stream x stays exact.
     """
     D, nq, nkv, hd = cfg.hidden, cfg.n_q_heads, cfg.n_kv_heads, cfg.head_dim
     c = cache.length
@@ -254,18 +279,18 @@ def draft_forward(weights: Dict, cfg, cache: RequestCache, anchor: int, block: i
     pos = np.arange(c, c + block)
     mask_rows = dflash_mask(c, block)[c:, :]                       # block rows only
     for i, lw in enumerate(weights["layers"]):
-        u = rms_norm(x, lw["g_in"], cfg.rms_eps)
-        q = rope(linear(u, lw["w_q"]).reshape(block, nq, hd), pos, cfg.rope_theta)
-        k = rope(linear(u, lw["w_k"]).reshape(block, nkv, hd), pos, cfg.rope_theta)
-        v = linear(u, lw["w_v"]).reshape(block, nkv, hd)
+        u = store(rms_norm(x, lw["g_in"], cfg.rms_eps), mode)
+        q = store(rope(linear(u, lw["w_q"]).reshape(block, nq, hd), pos, cfg.rope_theta), mode)
+        k = store(rope(linear(u, lw["w_k"]).reshape(block, nkv, hd), pos, cfg.rope_theta), mode)
+        v = store(linear(u, lw["w_v"]).reshape(block, nkv, hd), mode)
         if use_mask:
             o = attention_masked(q, np.concatenate([cache.k[i], k]), np.concatenate([cache.v[i], v]), mask_rows)
         else:
             o = attention_block(q, cache.k[i], cache.v[i], k, v)
-        x = x + linear(o.reshape(block, nq * hd), lw["w_o"])
-        u = rms_norm(x, lw["g_post"], cfg.rms_eps)
-        x = x + linear(silu(linear(u, lw["w_g"])) * linear(u, lw["w_u"]), lw["w_d"])
-    h = rms_norm(x, weights["g_final"], cfg.rms_eps)
+        x = x + linear(store(o, mode).reshape(block, nq * hd), lw["w_o"])
+        u = store(rms_norm(x, lw["g_post"], cfg.rms_eps), mode)
+        x = x + linear(store(silu(linear(u, lw["w_g"])) * linear(u, lw["w_u"]), mode), lw["w_d"])
+    h = store(rms_norm(x, weights["g_final"], cfg.rms_eps), mode)
     return {"h": h}
 
 
@@ -321,11 +346,11 @@ def expected_accept_len(alpha: Sequence[float]) -> float:
 # ---------------------------------------------------------------------------
 
 def draft_cycle(weights: Dict, cfg, cache: RequestCache, new_feats: Optional[np.ndarray], anchor: int,
-                block: int, use_mask: bool = True) -> Dict[str, np.ndarray]:
+                block: int, use_mask: bool = True, mode: str = "f64") -> Dict[str, np.ndarray]:
     """inject(new tokens) -> draft forward -> LM head + argmax for one request."""
     if new_feats is not None and new_feats.shape[0] > 0:
-        inject_context(weights, cfg, cache, new_feats)
-    fw = draft_forward(weights, cfg, cache, anchor, block, use_mask=use_mask)
+        inject_context(weights, cfg, cache, new_feats, mode)
+    fw = draft_forward(weights, cfg, cache, anchor, block, use_mask=use_mask, mode=mode)
     logits, drafts = lm_head_argmax(fw["h"][1:], weights["lm_head"])
     return {"h": fw["h"], "logits": logits, "drafts": drafts}
 

@@ -95,6 +95,29 @@ def oracle_caches(cfg: DraftConfig, batch: int) -> List[oracle.RequestCache]:
     return [oracle.RequestCache(cfg.layers, cfg.n_kv_heads, cfg.head_dim) for _ in range(batch)]
 
 
+class OracleSide:
+    """The exact float64 oracle for each request of a batch."""
+
+    def __init__(self, cfg: DraftConfig, weights_host: dict, batch: int):
+        self.cfg, self.w = cfg, weights_host
+        self.exact = oracle_caches(cfg, batch)
+
+    def inject(self, b: int, feats) -> None:
+        oracle.inject_context(self.w, self.cfg, self.exact[b], feats)
+
+    def check_request(self, b: int, anchor: int, block: int, gpu_logits: np.ndarray, gpu_drafts: np.ndarray):
+        """Assert the logits tolerance and argmax parity (drafts identical where
+        the oracle's top-2 margin exceeds 1e-2); returns the statistics."""
+        r = oracle.draft_cycle(self.w, self.cfg, self.exact[b], None, anchor, block)
+        err = row_rel_err(gpu_logits, r["logits"]) if block > 1 else 0.0
+        checked, mism, excl = argmax_check(gpu_drafts, r["logits"]) if block > 1 else (0, 0, 0)
+        agree = int(np.sum(np.asarray(gpu_drafts).reshape(-1) == r["drafts"])) if block > 1 else 0
+        stats = dict(request=b, rel_err=err, checked=checked, mismatched=mism, excluded=excl, agree_all_rows=agree)
+        assert err <= tol(self.cfg), f"logits relative error {stats}"
+        assert mism == 0, f"drafts differ from the oracle: {stats}"
+        return stats
+
+
 def compare_cache(g: GpuSide, caches: List[oracle.RequestCache], t: float, layers=None) -> float:
     """Worst relative error of the injected context K/V, per (request, layer, head) slab."""
     K, V = g.cache.k().float().cpu().numpy(), g.cache.v().float().cpu().numpy()

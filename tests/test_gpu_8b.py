@@ -11,25 +11,19 @@ import torch
 
 import oracle
 from dflash_inputs import QWEN3_8B, make_features, make_tokens, workloads
-from parity_util import (BF16_TOL, argmax_check, compare_cache, features_for, gpu_draft, gpu_inject, make_gpu,
-                         oracle_caches, row_rel_err, synthetic_target)
+from parity_util import BF16_TOL, OracleSide, compare_cache, features_for, gpu_draft, gpu_inject, make_gpu, \
+    synthetic_target
 
 pytestmark = pytest.mark.gpu
 
 
-def _check_requests(cfg, g, hw, caches, anchors, block, which, drafts=None, logits=None):
+def _check_requests(orc, g, anchors, block, which, drafts=None, logits=None):
     if drafts is None:
         drafts, logits = gpu_draft(g, anchors, block)
         torch.cuda.synchronize()
     an = anchors.cpu().numpy()
-    stats = []
-    for b in which:
-        r = oracle.draft_cycle(hw, cfg, caches[b], None, int(an[b]), block)
-        err = row_rel_err(logits[b].cpu().numpy(), r["logits"])
-        checked, mism, excl = argmax_check(drafts[b].cpu().numpy(), r["logits"])
-        stats.append((b, err, checked, mism, excl))
-        assert err <= BF16_TOL, f"request {b}: logits relative error {err:.3e}"
-        assert mism == 0, f"request {b}: {mism} of {checked} drafts differ (excluded near-ties: {excl})"
+    stats = [orc.check_request(b, int(an[b]), block, logits[b].cpu().numpy(), drafts[b].cpu().numpy()) for b in which]
+    print(stats)
     return drafts, logits, stats
 
 
@@ -37,14 +31,13 @@ def test_8b_bs1_two_cycles():
     wl = workloads()["8b_bs1"]
     cfg, block, ctx = wl.cfg, wl.block, wl.ctx[0]
     g = make_gpu(cfg, seed=wl.seed, batch=1, capacity=ctx + 4 * block, block=block, max_rows=ctx)
-    hw = oracle.weights_to_host(g.weights)
-    caches = oracle_caches(cfg, 1)
+    orc = OracleSide(cfg, oracle.weights_to_host(g.weights), 1)
     feats = features_for(cfg, [ctx], seed=wl.seed + 1)
     gpu_inject(g, feats)
-    oracle.inject_context(hw, cfg, caches[0], feats[0].cpu())
-    compare_cache(g, caches, BF16_TOL)
+    orc.inject(0, feats[0].cpu())
+    compare_cache(g, orc.exact, BF16_TOL)
     anchors = make_tokens(cfg, 1, seed=wl.seed + 2, device="cuda")
-    drafts, _, _ = _check_requests(cfg, g, hw, caches, anchors, block, [0])
+    drafts, _, _ = _check_requests(orc, g, anchors, block, [0])
 
     import block_diffusion_drafter_dflash_gb300 as df
     y = synthetic_target(cfg, drafts.cpu(), wl.accept_p, seed=wl.seed + 3).cuda()
@@ -56,9 +49,9 @@ def test_8b_bs1_two_cycles():
     assert int(tau.item()) == t_o and out.cpu().tolist()[0] == o_o and int(nxt.item()) == n_o
     new = make_features(cfg, block, seed=wl.seed + 4, device="cuda")
     gpu_inject(g, [new], max_rows=block, host_counts=False, n_new_dev=tau)
-    oracle.inject_context(hw, cfg, caches[0], new[:t_o].cpu())
-    compare_cache(g, caches, BF16_TOL)
-    _check_requests(cfg, g, hw, caches, nxt, block, [0])
+    orc.inject(0, new[:t_o].cpu())
+    compare_cache(g, orc.exact, BF16_TOL)
+    _check_requests(orc, g, nxt, block, [0])
     assert df.dflash_get_status(g.model) == 0
 
 
@@ -74,14 +67,13 @@ def test_8b_bs32_ragged_sampled_requests():
     torch.cuda.synchronize()
     order = np.argsort(wl.ctx)
     which = [int(order[0]), int(order[len(order) // 2])]          # shortest and a median-length request
-    hw = oracle.weights_to_host(g.weights)
-    caches = oracle_caches(cfg, B)
+    orc = OracleSide(cfg, oracle.weights_to_host(g.weights), B)
     for b in which:
-        oracle.inject_context(hw, cfg, caches[b], feats[b].cpu())
+        orc.inject(b, feats[b].cpu())
     del feats
     lens = g.cache.ctx_len().cpu().numpy()
     assert list(lens) == wl.ctx
-    _check_requests(cfg, g, hw, caches, anchors, block, which, drafts, logits)
+    _check_requests(orc, g, anchors, block, which, drafts, logits)
 
 
 def test_8b_long_context_sampled_request():
@@ -95,10 +87,9 @@ def test_8b_long_context_sampled_request():
     drafts, logits = gpu_draft(g, anchors, block)
     torch.cuda.synchronize()
     which = [B - 1]
-    hw = oracle.weights_to_host(g.weights)
-    caches = oracle_caches(cfg, B)
+    orc = OracleSide(cfg, oracle.weights_to_host(g.weights), B)
     f = feats[which[0]].cpu()
     del feats
     for s in range(0, ctx, 4096):          # incremental injection equals one-shot injection (oracle pin)
-        oracle.inject_context(hw, cfg, caches[which[0]], f[s:s + 4096])
-    _check_requests(cfg, g, hw, caches, anchors, block, which, drafts, logits)
+        orc.inject(which[0], f[s:s + 4096])
+    _check_requests(orc, g, anchors, block, which, drafts, logits)

@@ -10,40 +10,33 @@ import torch
 
 import oracle
 from dflash_inputs import TINY, make_features, make_tokens, replace
-from parity_util import (argmax_check, compare_cache, features_for, gpu_draft, gpu_inject, make_gpu, oracle_caches,
-                         row_rel_err, synthetic_target, tol)
+from parity_util import (OracleSide, compare_cache, features_for, gpu_draft, gpu_inject, make_gpu, synthetic_target,
+                         tol)
 
 pytestmark = pytest.mark.gpu
 
 
-def _cycle_compare(cfg, g, hw, caches, anchors, block):
+def _cycle_compare(orc, g, anchors, block):
     drafts, logits = gpu_draft(g, anchors, block)
     torch.cuda.synchronize()
     an = anchors.cpu().numpy()
     lg, dr = logits.cpu().numpy(), drafts.cpu().numpy()
-    worst = 0.0
-    for b, oc in enumerate(caches):
-        r = oracle.draft_cycle(hw, cfg, oc, None, int(an[b]), block)
-        if block > 1:
-            worst = max(worst, row_rel_err(lg[b], r["logits"]))
-            checked, mism, _ = argmax_check(dr[b], r["logits"])
-            assert mism == 0, f"request {b}: {mism} of {checked} drafts differ"
-    assert worst <= tol(cfg), f"logits relative error {worst:.3e}"
+    for b in range(len(an)):
+        orc.check_request(b, int(an[b]), block, lg[b], dr[b])
     return drafts
 
 
-def test_tiny_config_one_cycle_then_incremental_injection():
-    cfg = TINY
+@pytest.mark.parametrize("cfg", [TINY, replace(TINY, name="tiny-bf16", dtype="bf16")], ids=["fp32", "bf16"])
+def test_tiny_config_one_cycle_then_incremental_injection(cfg):
     block, ctx = 4, 64
     g = make_gpu(cfg, seed=0, batch=1, capacity=128, block=block, max_rows=64)
-    hw = oracle.weights_to_numpy(g.weights)
-    caches = oracle_caches(cfg, 1)
+    orc = OracleSide(cfg, oracle.weights_to_numpy(g.weights), 1)
     feats = features_for(cfg, [ctx], seed=1)
     gpu_inject(g, feats)
-    oracle.inject_context(hw, cfg, caches[0], feats[0].cpu().numpy())
-    compare_cache(g, caches, tol(cfg))
+    orc.inject(0, feats[0].float().cpu().numpy())
+    compare_cache(g, orc.exact, tol(cfg))
     anchors = make_tokens(cfg, 1, seed=2, device="cuda")
-    drafts = _cycle_compare(cfg, g, hw, caches, anchors, block)
+    drafts = _cycle_compare(orc, g, anchors, block)
 
     # verify against a synthetic target, then inject the tau committed tokens
     # using the device-side accepted lengths (no host copy of the counts)
@@ -57,29 +50,31 @@ def test_tiny_config_one_cycle_then_incremental_injection():
     assert int(tau.item()) == t_o and out.cpu().tolist()[0] == o_o and int(nxt.item()) == n_o
     new = make_features(cfg, block, seed=4, device="cuda")          # features of up to `block` committed tokens
     gpu_inject(g, [new], max_rows=block, host_counts=False, n_new_dev=tau)
-    oracle.inject_context(hw, cfg, caches[0], new[:t_o].cpu().numpy())
-    compare_cache(g, caches, tol(cfg))
-    _cycle_compare(cfg, g, hw, caches, nxt, block)
+    orc.inject(0, new[:t_o].float().cpu().numpy())
+    compare_cache(g, orc.exact, tol(cfg))
+    _cycle_compare(orc, g, nxt, block)
     import block_diffusion_drafter_dflash_gb300 as df2
     assert df2.dflash_get_status(g.model) == 0
 
 
+TINY_BF16 = replace(TINY, name="tiny-bf16", dtype="bf16")
+
+
+@pytest.mark.parametrize("cfg", [TINY, TINY_BF16], ids=["fp32", "bf16"])
 @pytest.mark.parametrize("block", [1, 3, 17, 32])
 @pytest.mark.parametrize("ctxs", [[0, 1, 65], [130]])
-def test_tiny_ragged_batches_and_block_sizes(block, ctxs):
-    cfg = TINY
+def test_tiny_ragged_batches_and_block_sizes(cfg, block, ctxs):
     B = len(ctxs)
     g = make_gpu(cfg, seed=5, batch=B, capacity=160, block=block, max_rows=max(1, sum(ctxs)))
-    hw = oracle.weights_to_numpy(g.weights)
-    caches = oracle_caches(cfg, B)
+    orc = OracleSide(cfg, oracle.weights_to_numpy(g.weights), B)
     feats = features_for(cfg, ctxs, seed=6)
     gpu_inject(g, feats)
     for b in range(B):
         if ctxs[b]:
-            oracle.inject_context(hw, cfg, caches[b], feats[b].cpu().numpy())
-    compare_cache(g, caches, tol(cfg))
+            orc.inject(b, feats[b].float().cpu().numpy())
+    compare_cache(g, orc.exact, tol(cfg))
     anchors = make_tokens(cfg, B, seed=7, device="cuda")
-    _cycle_compare(cfg, g, hw, caches, anchors, block)
+    _cycle_compare(orc, g, anchors, block)
 
 
 def test_capacity_is_guarded_on_host_and_device():

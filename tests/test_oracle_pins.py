@@ -382,3 +382,35 @@ def test_speculative_loop_is_lossless_against_a_fake_target():
             seq = seq + [anchor] + out[:tau - 1]   # committed: anchor + accepted drafts
             anchor = nxt                           # correction / bonus is the next anchor
         assert seq[:60] == ref[:60]
+
+
+# ---------------------------------------------------------------- storage rounding
+
+def test_store_rounding_matches_library_conversions():
+    """bf16 storage = torch's float32 -> bfloat16 conversion (round to nearest
+    even), applied after rounding to float32; fp32 storage = float32 cast."""
+    x = np.concatenate([rng.standard_normal(20000) * 10.0 ** rng.integers(-8, 8, 20000),
+                        np.array([0.0, -0.0, 1.0, 1.0 + 2.0 ** -8, 1.0 + 3 * 2.0 ** -8, 65504.0, -3.0e-38])])
+    f32 = x.astype(np.float32)
+    ref = torch.tensor(f32).to(torch.bfloat16).float().numpy().astype(np.float64)
+    np.testing.assert_array_equal(oracle.store(x, "bf16"), ref)
+    np.testing.assert_array_equal(oracle.store(x, "fp32"), f32.astype(np.float64))
+    assert oracle.store(x, "f64") is x
+    # ties go to even: 1 + 2^-8 sits halfway between two bf16 neighbours
+    assert oracle.store(np.array([1.0 + 2.0 ** -8]), "bf16")[0] == 1.0
+    assert oracle.store(np.array([1.0 + 3 * 2.0 ** -8]), "bf16")[0] == 1.0 + 2.0 ** -6
+
+
+def test_storage_mode_only_rounds_between_steps():
+    """With fp32 storage the drafter stays within float32 rounding of the
+    exact definition, and bf16 storage within bf16 rounding (tiny config)."""
+    cfg, w = _tiny_setup()
+    f = make_features(cfg, 16, seed=3).float().numpy()
+    res = {}
+    for mode in ("f64", "fp32", "bf16"):
+        c = oracle.RequestCache(cfg.layers, cfg.n_kv_heads, cfg.head_dim)
+        res[mode] = oracle.draft_cycle(w, cfg, c, f, anchor=9, block=4, mode=mode)["logits"]
+    scale = np.max(np.abs(res["f64"]))
+    assert np.max(np.abs(res["fp32"] - res["f64"])) / scale < 1e-5
+    err = np.max(np.abs(res["bf16"] - res["f64"])) / scale
+    assert 1e-5 < err < 5e-2
