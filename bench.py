@@ -29,8 +29,8 @@ if ROOT not in sys.path:
 
 import torch  # noqa: E402
 
-from dflash_inputs import (make_agreement, make_features, make_tokens, make_weights, seed_for,  # noqa: E402
-                           synthetic_target_argmax, workloads)
+from dflash_inputs import (AgreementPattern, make_agreement, make_features, make_tokens, make_weights,  # noqa: E402
+                           seed_for, synthetic_target_argmax, workloads)
 
 METRIC = "drafted tokens/s & draft-cycle latency at bs1/bs32; % of HBM or TC roofline"
 UNIT = "drafted tokens/s"
@@ -40,8 +40,8 @@ GEMM_STAGES = ("fuse", "inject", "qkv", "o", "gateup", "down", "lmhead")
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=30)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=500)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="dflash", choices=["dflash", "reference"])
     ap.add_argument("--workload", default="8b_bs1")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -137,7 +137,12 @@ def gemm_bytes_per_cycle(cfg, B: int, block: int, inject_rows: int) -> dict:
 
 # ---------------------------------------------------------------- the GPU arm
 class Cycle:
-    """Device-resident draft cycle of one workload through the C ABI."""
+    """Device-resident draft cycle of one workload through the C ABI.
+
+    Every per-cycle input lives on the device: the target features of the
+    committed tokens, and a stack of seeded agreement patterns indexed by a
+    device-side counter, so that one cycle can be captured in a CUDA graph and
+    replayed."""
 
     def __init__(self, wl, total_cycles: int, rank: int):
         import block_diffusion_drafter_dflash_gb300 as df
@@ -164,28 +169,48 @@ class Cycle:
                 df.dflash_inject_context(self.model, self.cache, f, torch.tensor(counts, dtype=torch.int32,
                                                                                  device="cuda"), counts, n, self.ws)
         torch.cuda.synchronize()
-        # per-cycle inputs: a small pool of feature blocks and one agreement pattern per cycle
-        self.feat_pool = [make_features(cfg, self.rows, seed=seed + 999 + i, device="cuda") for i in range(4)]
-        self.patterns = [make_agreement(cfg, B, block, wl.accept_p, seed=seed_for(wl, i, 5) + rank, device="cuda")
-                         for i in range(total_cycles)]
+        self.feats = make_features(cfg, self.rows, seed=seed + 999, device="cuda")
+        P = 16
+        pats = [make_agreement(cfg, B, block, wl.accept_p, seed=seed_for(wl, i, 5) + rank, device="cuda")
+                for i in range(P)]
+        self.match = torch.stack([p.match for p in pats]).contiguous()
+        self.off = torch.stack([p.off for p in pats]).contiguous()
+        self.bonus = torch.stack([p.bonus for p in pats]).contiguous()
+        self.P = P
+        self.pidx = torch.zeros(1, dtype=torch.long, device="cuda")
         self.tau = torch.full((B,), wl.first_inject, dtype=torch.int32, device="cuda")
+        self.tau_acc = torch.zeros(1, dtype=torch.long, device="cuda")
         self.anchor = make_tokens(cfg, B, seed=seed + 3, device="cuda")
         self.drafts = torch.empty((B, block - 1), dtype=torch.int32, device="cuda")
         self.out = torch.empty((B, block), dtype=torch.int32, device="cuda")
         self.next_anchor = torch.empty((B,), dtype=torch.int32, device="cuda")
-        self.i = 0
-        self.tau_sum = 0
+        self.graph = None
 
-    def step(self, feats=None, pattern=None):
+    def step(self):
         df = self.df
-        f = feats if feats is not None else self.feat_pool[self.i % len(self.feat_pool)]
-        pat = pattern if pattern is not None else self.patterns[self.i % len(self.patterns)]
-        df.dflash_inject_context(self.model, self.cache, f, self.tau, None, self.rows, self.ws)
+        df.dflash_inject_context(self.model, self.cache, self.feats, self.tau, None, self.rows, self.ws)
         df.dflash_draft_block(self.model, self.cache, self.anchor, self.block, self.drafts, None, self.ws)
+        pat = AgreementPattern(match=self.match.index_select(0, self.pidx)[0],
+                               off=self.off.index_select(0, self.pidx)[0],
+                               bonus=self.bonus.index_select(0, self.pidx)[0])
         y = synthetic_target_argmax(self.drafts, pat, self.cfg.vocab)          # the (synthetic) target
         df.dflash_verify_greedy(self.drafts, y, self.tau, self.out, self.next_anchor)
         self.anchor.copy_(self.next_anchor)
-        self.i += 1
+        self.tau_acc.add_(self.tau.sum())
+        self.pidx.add_(1)
+        self.pidx.remainder_(self.P)
+
+    def capture(self):
+        """Capture one cycle in a CUDA graph (after eager warm-up)."""
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            self.step()
+        torch.cuda.synchronize()
+        self.graph = g
+
+    def replay(self):
+        self.graph.replay()
 
 
 def run_gpu(args, rank, world, local):
@@ -193,7 +218,7 @@ def run_gpu(args, rank, world, local):
     torch.cuda.set_device(local)
     wl = workloads()[args.workload]
     W, K = args.warmup, args.steps
-    total = 3 * (W + K) + 4
+    total = W + 2 * K + 40
     cyc = Cycle(wl, total, rank)
     dist = world > 1 and torch.distributed.is_initialized()
 
@@ -204,20 +229,26 @@ def run_gpu(args, rank, world, local):
 
     for _ in range(W):
         cyc.step()
+    n0 = df.dflash_launch_count()
+    cyc.capture()                                 # one cycle as a CUDA graph
+    launches_per_cycle = df.dflash_launch_count() - n0
+    for _ in range(2):
+        cyc.replay()
     barrier()
     clocks = Clocks(local)
     clocks.start()
-    n0 = df.dflash_launch_count()
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    cyc.tau_acc.zero_()
     barrier()
     t0.record()
     for _ in range(K):
-        cyc.step()
+        cyc.replay()
     t1.record()
     barrier()
-    launches = df.dflash_launch_count() - n0
+    launches = launches_per_cycle * K
     clk = clocks.stop()
     ms = t0.elapsed_time(t1) / K
+    mean_tau = float(cyc.tau_acc.item()) / (K * wl.batch)
     if dist:
         tt = torch.tensor([ms], device="cuda")
         torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
@@ -225,13 +256,14 @@ def run_gpu(args, rank, world, local):
     drafted = wl.batch * (wl.block - 1)
     value = world * drafted / (ms / 1e3)
 
-    # profiled pass: CUDA events around each launch, per stage
-    df.dflash_profile_start(cyc.model, 8192)
-    for _ in range(K):
+    # profiled pass (eager launches): CUDA events around each launch, per stage
+    KP = min(K, 20)
+    df.dflash_profile_start(cyc.model, 100 * KP)
+    for _ in range(KP):
         cyc.step()
     prof = df.dflash_profile_stop(cyc.model)
     gb = gemm_bytes_per_cycle(wl.cfg, wl.batch, wl.block, cyc.rows)
-    gemm_ms = sum(prof[s][0] for s in GEMM_STAGES) / K
+    gemm_ms = sum(prof[s][0] for s in GEMM_STAGES) / KP
     gemm_bytes = sum(gb.values())
     hbm, bf16, src = load_peaks()
     achieved = gemm_bytes / (gemm_ms / 1e3) / 1e9
@@ -239,7 +271,7 @@ def run_gpu(args, rank, world, local):
                 "frac": round(achieved / hbm, 4), "traffic": None,
                 "kernel": "projection GEMMs (all launches of one cycle)", "peak_source": src,
                 "algorithmic_bytes_per_cycle": gemm_bytes, "kernel_ms_per_cycle": round(gemm_ms, 4)}
-    stages = {s: {"ms_per_cycle": round(v[0] / K, 4), "launches_per_cycle": v[1] / K} for s, v in prof.items()}
+    stages = {s: {"ms_per_cycle": round(v[0] / KP, 4), "launches_per_cycle": v[1] / KP} for s, v in prof.items()}
     cycle_roof_ms = (gemm_bytes + kv_bytes(wl)) / (hbm * 1e9) * 1e3
 
     e2e = None
@@ -254,7 +286,9 @@ def run_gpu(args, rank, world, local):
         "config": {"workload": wl.name, "drafter": wl.cfg.name, "batch_per_gpu": wl.batch, "block": wl.block,
                    "ctx": wl.ctx if len(wl.ctx) <= 4 else f"{min(wl.ctx)}..{max(wl.ctx)} ({len(wl.ctx)} requests)",
                    "l2": "inputs larger than L2 (weights streamed every cycle)",
-                   "mean_tau": None, "cycle_roofline_ms": round(cycle_roof_ms, 4),
+                   "timing": "CUDA-graph replay of whole cycles; per-stage times from an eager pass with events",
+                   "mean_tau": round(mean_tau, 3), "accepted_tokens_per_s": round(world * mean_tau * wl.batch / (ms / 1e3), 1),
+                   "cycle_roofline_ms": round(cycle_roof_ms, 4),
                    "cycle_frac_of_hbm_roofline": round(cycle_roof_ms / ms, 4)},
         "roofline": roofline, "stages": stages, "gpu_launches": int(launches), "clocks": clk, "e2e": e2e,
     }
@@ -268,29 +302,29 @@ def kv_bytes(wl) -> int:
 
 
 def run_e2e(cyc, K, wl, barrier, world):
-    """Same cycle through the public API with the step's inputs copied from
-    pinned host memory and its results read back every step."""
-    cfg = wl.cfg
-    feats_h = cyc.feat_pool[0].cpu().pin_memory()
-    feats_d = torch.empty_like(cyc.feat_pool[0])
-    pats_h = [(p.match.cpu().pin_memory(), p.off.cpu().pin_memory(), p.bonus.cpu().pin_memory())
-              for p in cyc.patterns[:8]]
-    p0 = cyc.patterns[0]
-    pat_d = type(p0)(match=torch.empty_like(p0.match), off=torch.empty_like(p0.off), bonus=torch.empty_like(p0.bonus))
-    out_h = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in (cyc.drafts, cyc.tau, cyc.out, cyc.next_anchor)]
-    h2d = feats_h.numel() * feats_h.element_size() + sum(sum(t.numel() * t.element_size() for t in p)
-                                                          for p in pats_h[:1])
+    """Same cycle through the public API (graph replay of the C-ABI calls) with
+    the step's inputs — target features of the committed tokens and the
+    target's agreement pattern — copied from pinned host memory, and its
+    results (drafts, tau, emitted tokens, next anchor) read back, every step."""
+    feats_h = cyc.feats.cpu().pin_memory()
+    pats_h = [(cyc.match[i].cpu().pin_memory(), cyc.off[i].cpu().pin_memory(), cyc.bonus[i].cpu().pin_memory())
+              for i in range(cyc.P)]
+    outs = (cyc.drafts, cyc.tau, cyc.out, cyc.next_anchor)
+    out_h = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in outs]
+    h2d = feats_h.numel() * feats_h.element_size() + sum(t.numel() * t.element_size() for t in pats_h[0])
     d2h = sum(t.numel() * t.element_size() for t in out_h)
+    cyc.pidx.zero_()
     barrier()
     t0 = time.perf_counter()
     for i in range(K):
-        feats_d.copy_(feats_h, non_blocking=True)
-        m, o, b = pats_h[i % len(pats_h)]
-        pat_d.match.copy_(m, non_blocking=True)
-        pat_d.off.copy_(o, non_blocking=True)
-        pat_d.bonus.copy_(b, non_blocking=True)
-        cyc.step(feats=feats_d, pattern=pat_d)
-        for h, d in zip(out_h, (cyc.drafts, cyc.tau, cyc.out, cyc.next_anchor)):
+        slot = i % cyc.P
+        cyc.feats.copy_(feats_h, non_blocking=True)
+        m, o, b = pats_h[slot]
+        cyc.match[slot].copy_(m, non_blocking=True)
+        cyc.off[slot].copy_(o, non_blocking=True)
+        cyc.bonus[slot].copy_(b, non_blocking=True)
+        cyc.replay()
+        for h, d in zip(out_h, outs):
             h.copy_(d, non_blocking=True)
         torch.cuda.current_stream().synchronize()
     barrier()

@@ -59,6 +59,7 @@ SIGNATURES = {
     "dflash_draft_block": (c_i32, [c_ptr, c_ptr, c_ptr, c_i32, c_ptr, c_ptr, c_ptr, c_size, c_ptr]),
     "dflash_verify_greedy": (c_i32, [c_ptr, c_ptr, c_i32, c_i32, c_ptr, c_ptr, c_ptr, c_ptr]),
     "dflash_launch_count": (ctypes.c_uint64, []),
+    "dflash_trace_read": (c_i32, [c_ptr, ctypes.POINTER(ctypes.c_uint64), c_size]),
     "dflash_profile_start": (c_i32, [c_ptr, c_i32]),
     "dflash_profile_stop": (c_i32, [c_ptr, c_ptr, ctypes.POINTER(ctypes.c_float), c_i32p, c_i32]),
 }

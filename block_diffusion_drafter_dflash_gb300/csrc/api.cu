@@ -41,6 +41,9 @@ struct dflash_model {
   double* inv_freq_dev;    // RoPE frequencies theta^(-2i/hd), i < hd/2
   void* tmaps_dev;         // tensor maps of every weight matrix (bf16 models)
   int use_tc;              // bf16 projections on the tcgen05 kernel
+  unsigned long long* trace_dev;  // GEMM timestamps (DFLASH_TRACE_GEMM=<launch index>)
+  long trace_target;
+  long gemm_launches;
   Profiler prof;
 };
 
@@ -100,13 +103,16 @@ int32_t cuda_fail(cudaError_t e, const char* what) {
     }                                                                                 \
   } while (0)
 
+constexpr size_t kTraceEntries = 8u << 16;   // 8 timestamps for up to 65536 CTAs
+
 size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
 
 int32_t check_config(const dflash_config* c) {
   if (!c) return fail(DFLASH_ERR_INVALID_ARG, "config is NULL");
   if (c->dtype != DFLASH_DTYPE_F32 && c->dtype != DFLASH_DTYPE_BF16)
     return fail(DFLASH_ERR_INVALID_ARG, "dtype %d is not DFLASH_DTYPE_F32 or DFLASH_DTYPE_BF16", c->dtype);
-  if (c->hidden <= 0 || c->hidden % kTileN) return fail(DFLASH_ERR_SHAPE, "hidden %d must be a positive multiple of 128", c->hidden);
+  if (c->hidden <= 0 || c->hidden % kTileN || c->hidden > 8192)
+    return fail(DFLASH_ERR_SHAPE, "hidden %d must be a positive multiple of 128, at most 8192", c->hidden);
   if (c->layers <= 0 || c->layers > kMaxSeg / 2) return fail(DFLASH_ERR_SHAPE, "layers %d must be in [1, %d]", c->layers, kMaxSeg / 2);
   if (c->head_dim != 64 && c->head_dim != 128) return fail(DFLASH_ERR_SHAPE, "head_dim %d must be 64 or 128", c->head_dim);
   if (c->n_q_heads <= 0 || c->n_kv_heads <= 0 || c->n_q_heads % c->n_kv_heads)
@@ -220,6 +226,10 @@ GemmProblem make_problem(const dflash_model* m, const void* x, int ldx, int M, i
   p.K = K;
   p.wmaps = m->tmaps_dev;
   p.status = m->status_dev;
+  if (m->trace_dev) {   // timestamps of one chosen GEMM launch
+    dflash_model* mm = const_cast<dflash_model*>(m);
+    p.trace = mm->gemm_launches++ == mm->trace_target ? mm->trace_dev : nullptr;
+  }
   return p;
 }
 
@@ -431,6 +441,14 @@ int32_t dflash_model_create(const dflash_config* cfg, const dflash_weights* w, d
     dflash_model_destroy(m);
     return cuda_fail(e, "model state");
   }
+  if (const char* tr = std::getenv("DFLASH_TRACE_GEMM")) {
+    m->trace_target = std::atol(tr);
+    if (cudaMalloc(&m->trace_dev, kTraceEntries * sizeof(unsigned long long)) != cudaSuccess ||
+        cudaMemset(m->trace_dev, 0, kTraceEntries * sizeof(unsigned long long)) != cudaSuccess) {
+      dflash_model_destroy(m);
+      return fail(DFLASH_ERR_CUDA, "trace buffer");
+    }
+  }
   const char* gemm_env = std::getenv("DFLASH_GEMM");
   m->use_tc = cfg->dtype == DFLASH_DTYPE_BF16 && !(gemm_env && std::strcmp(gemm_env, "simt") == 0);
   if (m->use_tc) {
@@ -449,6 +467,7 @@ int32_t dflash_model_destroy(dflash_model* m) {
   if (m->status_dev) cudaFree(m->status_dev);
   if (m->inv_freq_dev) cudaFree(m->inv_freq_dev);
   if (m->tmaps_dev) cudaFree(m->tmaps_dev);
+  if (m->trace_dev) cudaFree(m->trace_dev);
   for (cudaEvent_t e : m->prof.ev) cudaEventDestroy(e);
   delete m;
   return DFLASH_OK;
@@ -611,6 +630,14 @@ int32_t dflash_verify_greedy(const int32_t* draft_dev, const int32_t* target_arg
 }
 
 uint64_t dflash_launch_count(void) { return g_launch_count.load(); }
+
+int32_t dflash_trace_read(const dflash_model* m, uint64_t* host, size_t n) {
+  if (!m || !host) return fail(DFLASH_ERR_INVALID_ARG, "NULL argument");
+  if (!m->trace_dev) return fail(DFLASH_ERR_UNSUPPORTED, "GEMM tracing is off (set DFLASH_TRACE_GEMM)");
+  n = std::min(n, kTraceEntries);
+  DF_CUDA(cudaMemcpy(host, m->trace_dev, n * sizeof(uint64_t), cudaMemcpyDeviceToHost), "trace read");
+  return DFLASH_OK;
+}
 
 int32_t dflash_profile_start(dflash_model* m, int32_t max_launches) {
   if (!m || max_launches <= 0) return fail(DFLASH_ERR_INVALID_ARG, "model is NULL or max_launches <= 0");

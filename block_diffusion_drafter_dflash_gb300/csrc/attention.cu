@@ -36,6 +36,8 @@ __device__ __forceinline__ float warp_sum(float v) {
 template <typename T>
 __global__ void __launch_bounds__(kAttnThreads) attn_split_kernel(const __grid_constant__ AttnParams p) {
   extern __shared__ float sm[];
+  griddep_wait();
+  griddep_trigger();
   const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
   const int G = p.nq / p.nkv, rows = G * p.block, hd = p.hd;
   const int c = p.ctx_len[b];
@@ -119,27 +121,56 @@ __global__ void __launch_bounds__(kAttnThreads) attn_split_kernel(const __grid_c
   }
 }
 
-// One CTA per (request, query head, block position): merge the splits.
+// One CTA of 128 threads per (request, query head, block position): merge the
+// splits.  The per-split (max, sum) pairs are read in parallel and reduced in
+// shared memory; each thread then adds one output dimension over all splits.
 template <typename T>
-__global__ void attn_combine_kernel(const __grid_constant__ AttnParams p) {
-  const int row = blockIdx.x;  // ((b*nq + qh)*block + k)
+__global__ void __launch_bounds__(128) attn_combine_kernel(const __grid_constant__ AttnParams p) {
+  extern __shared__ float w[];                 // [splits] weights, then 8 floats of scratch
+  float* red = w + p.splits;
+  griddep_wait();
+  griddep_trigger();
+  const int row = blockIdx.x;                  // ((b*nq + qh)*block + k)
   const int k = row % p.block, qh = (row / p.block) % p.nq, b = row / (p.block * p.nq);
   const float2* ml = p.ml + (size_t)row * p.splits;
-  float M = -FLT_MAX;
-  for (int s = 0; s < p.splits; ++s)
-    if (ml[s].y > 0.f) M = fmaxf(M, ml[s].x);
-  float L = 0.f;
-  for (int s = 0; s < p.splits; ++s)
-    if (ml[s].y > 0.f) L += ml[s].y * __expf(ml[s].x - M);
-  const float inv = 1.f / L;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  float mx = -FLT_MAX;
+  for (int sp = threadIdx.x; sp < p.splits; sp += blockDim.x) {
+    const float2 v = ml[sp];
+    w[sp] = v.y > 0.f ? v.x : -FLT_MAX;
+    mx = fmaxf(mx, w[sp]);
+  }
+  for (int o = 16; o; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  if (lane == 0) red[warp] = mx;
+  __syncthreads();
+  const float M = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
+  __syncthreads();
+  float l = 0.f;
+  for (int sp = threadIdx.x; sp < p.splits; sp += blockDim.x) {
+    const float2 v = ml[sp];
+    const float e = v.y > 0.f ? __expf(v.x - M) : 0.f;
+    w[sp] = e;
+    l += e * v.y;
+  }
+  for (int o = 16; o; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
+  if (lane == 0) red[4 + warp] = l;
+  __syncthreads();
+  const float inv = 1.f / ((red[4] + red[5]) + (red[6] + red[7]));
+  const int d = threadIdx.x;
+  if (d >= p.hd) return;
+  const float* src = p.opart + (size_t)row * p.splits * p.hd + d;
+  float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+  int sp = 0;
+  for (; sp + 4 <= p.splits; sp += 4) {
+    a0 += w[sp] * src[(size_t)sp * p.hd];
+    a1 += w[sp + 1] * src[(size_t)(sp + 1) * p.hd];
+    a2 += w[sp + 2] * src[(size_t)(sp + 2) * p.hd];
+    a3 += w[sp + 3] * src[(size_t)(sp + 3) * p.hd];
+  }
+  for (; sp < p.splits; ++sp) a0 += w[sp] * src[(size_t)sp * p.hd];
   T* out = static_cast<T*>(p.out);
   const size_t base = ((size_t)b * p.block + k) * p.nq * p.hd + (size_t)qh * p.hd;
-  for (int d = threadIdx.x; d < p.hd; d += blockDim.x) {
-    float acc = 0.f;
-    for (int s = 0; s < p.splits; ++s)
-      if (ml[s].y > 0.f) acc += p.opart[((size_t)row * p.splits + s) * p.hd + d] * __expf(ml[s].x - M);
-    put_act(out, p.out_plane, base + d, acc * inv);
-  }
+  put_act(out, p.out_plane, base + d, ((a0 + a1) + (a2 + a3)) * inv);
 }
 
 size_t attn_smem_bytes(int rows, int hd) {
@@ -165,12 +196,12 @@ cudaError_t attention_launch(const AttnParams& p, cudaStream_t s) {
     e = attention_mma_split_launch(p, s);
   } else {
     const int rows = (p.nq / p.nkv) * p.block;
-    attn_split_kernel<T><<<dim3(p.splits, p.nkv, p.B), kAttnThreads, attn_smem_bytes(rows, p.hd), s>>>(p);
-    e = cudaGetLastError();
+    e = launch_pdl(attn_split_kernel<T>, dim3(p.splits, p.nkv, p.B), dim3(kAttnThreads), attn_smem_bytes(rows, p.hd),
+                   s, p);
   }
   if (e != cudaSuccess) return e;
-  attn_combine_kernel<T><<<p.B * p.nq * p.block, 128, 0, s>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(attn_combine_kernel<T>, dim3(p.B * p.nq * p.block), dim3(128), (p.splits + 8) * sizeof(float), s,
+                    p);
 }
 
 template cudaError_t attention_prepare<float>(int, int);

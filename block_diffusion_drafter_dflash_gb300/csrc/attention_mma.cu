@@ -93,6 +93,8 @@ __global__ void __launch_bounds__(NW * 32) attn_mma_kernel(const __grid_constant
   uint8_t* vhi = klo + C::kTileB;
   uint8_t* vlo = vhi + C::kTileB;
 
+  griddep_wait();
+  griddep_trigger();
   const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
   const int G = p.nq / p.nkv, rows = G * p.block;
   const int c = p.ctx_len[b];
@@ -292,8 +294,7 @@ __global__ void __launch_bounds__(NW * 32) attn_mma_kernel(const __grid_constant
 template <int HD, int NW>
 cudaError_t launch_one(const AttnParams& p, cudaStream_t s) {
   using C = MmaCfg<HD, NW>;
-  attn_mma_kernel<HD, NW><<<dim3(p.splits, p.nkv, p.B), C::kThreads, C::kSmem, s>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(attn_mma_kernel<HD, NW>, dim3(p.splits, p.nkv, p.B), dim3(C::kThreads), C::kSmem, s, p);
 }
 
 template <int HD, int NW>

@@ -4,6 +4,8 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
 
 #include "../../include/dflash.h"
 
@@ -13,6 +15,40 @@ constexpr int kTileN = 128;      // output features per GEMM tile (two 64-row ha
 constexpr int kHalfN = 64;
 constexpr int kMaxSeg = 16;      // weight matrices one GEMM launch may read
 constexpr int kMaxBlock = 32;    // largest block_size (a warp per request in verify)
+
+// ---------------------------------------------------------------- dependent launches
+// Kernels of the cycle are launched with programmatic dependent launch: a
+// kernel may become resident while its predecessor drains, prefetch what does
+// not depend on it (weights), and must call griddep_wait() before it reads or
+// writes anything an earlier kernel of the stream touches.  griddep_trigger()
+// lets the successor launch once every CTA of this grid has started.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+inline bool pdl_enabled() {
+  static int on = -1;
+  if (on < 0) {
+    const char* e = getenv("DFLASH_PDL");
+    on = (e && strcmp(e, "0") == 0) ? 0 : 1;
+  }
+  return on == 1;
+}
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                              Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl_enabled() ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
 
 // ---------------------------------------------------------------- scalar types
 template <typename T> __device__ __forceinline__ float to_f32(T v);
@@ -38,6 +74,29 @@ __device__ __forceinline__ void put_act(__nv_bfloat16* base, size_t plane, size_
   const __nv_bfloat16 hi = __float2bfloat16_rn(v);
   base[i] = hi;
   base[plane + i] = __float2bfloat16_rn(v - __bfloat162float(hi));
+}
+// four consecutive values (i a multiple of 4)
+__device__ __forceinline__ void put_act4(float* base, size_t /*plane*/, size_t i, float4 v) {
+  *reinterpret_cast<float4*>(base + i) = v;
+}
+__device__ __forceinline__ void put_act4(__nv_bfloat16* base, size_t plane, size_t i, float4 v) {
+  __nv_bfloat162 h0 = __floats2bfloat162_rn(v.x, v.y), h1 = __floats2bfloat162_rn(v.z, v.w);
+  float2 f0 = __bfloat1622float2(h0), f1 = __bfloat1622float2(h1);
+  __nv_bfloat162 l0 = __floats2bfloat162_rn(v.x - f0.x, v.y - f0.y), l1 = __floats2bfloat162_rn(v.z - f1.x, v.w - f1.y);
+  uint2 hi, lo;
+  hi.x = *reinterpret_cast<uint32_t*>(&h0);
+  hi.y = *reinterpret_cast<uint32_t*>(&h1);
+  lo.x = *reinterpret_cast<uint32_t*>(&l0);
+  lo.y = *reinterpret_cast<uint32_t*>(&l1);
+  *reinterpret_cast<uint2*>(base + i) = hi;
+  *reinterpret_cast<uint2*>(base + plane + i) = lo;
+}
+__device__ __forceinline__ float4 load4(const float* p) { return *reinterpret_cast<const float4*>(p); }
+__device__ __forceinline__ float4 load4(const __nv_bfloat16* p) {
+  uint2 r = *reinterpret_cast<const uint2*>(p);
+  float2 a = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&r.x));
+  float2 b = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&r.y));
+  return make_float4(a.x, a.y, b.x, b.y);
 }
 __device__ __forceinline__ float get_act(const float* base, size_t /*plane*/, size_t i) { return base[i]; }
 __device__ __forceinline__ float get_act(const __nv_bfloat16* base, size_t plane, size_t i) {
@@ -105,6 +164,7 @@ struct GemmProblem {
   int* counters;       // [token tiles][total_tiles], zero between launches
   const void* wmaps;   // device array of weight tensor maps (tensor-core path)
   int32_t* status;     // device status word
+  unsigned long long* trace;   // per-CTA timestamps (8 per CTA) or nullptr
   GemmSeg seg[kMaxSeg];
 };
 

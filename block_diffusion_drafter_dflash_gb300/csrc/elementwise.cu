@@ -19,15 +19,52 @@ __device__ __forceinline__ float block_sum(float v, float* red) {
   return t;
 }
 
-// u = x * rsqrt(mean(x^2) + eps) * g for one row held in fp32; u is a GEMM
+// Each row kernel keeps its row in registers: thread t holds float4s
+// t, t+256, ... (at most kMaxV4 of them, so D <= 4*256*kMaxV4), all loads are
+// issued before the first use, and the row is read once.
+constexpr int kMaxV4 = 8;
+
+struct RowRegs {
+  float4 v[kMaxV4];
+};
+
+// ss = sum of squares of the row held in r (nv float4s in the row)
+__device__ __forceinline__ float row_sumsq(const RowRegs& r, int nv) {
+  float ss = 0.f;
+#pragma unroll
+  for (int i = 0; i < kMaxV4; ++i) {
+    const int idx = threadIdx.x + i * blockDim.x;
+    if (idx < nv) ss += r.v[i].x * r.v[i].x + r.v[i].y * r.v[i].y + r.v[i].z * r.v[i].z + r.v[i].w * r.v[i].w;
+  }
+  return ss;
+}
+
+// u = x * rsqrt(mean(x^2) + eps) * g for a row held in registers; u is a GEMM
 // activation operand (planes `plane` elements apart).
 template <typename T>
-__device__ __forceinline__ void norm_row(const float* x, const T* g, float eps, int D, T* u, size_t plane,
-                                         float* red) {
-  float ss = 0.f;
-  for (int i = threadIdx.x; i < D; i += blockDim.x) ss = fmaf(x[i], x[i], ss);
-  const float r = rsqrtf(block_sum(ss, red) / (float)D + eps);
-  for (int i = threadIdx.x; i < D; i += blockDim.x) put_act(u, plane, i, x[i] * r * to_f32(g[i]));
+__device__ __forceinline__ void norm_store(const RowRegs& r, const T* g, float eps, int D, T* u, size_t plane,
+                                           float* red) {
+  const int nv = D >> 2;
+  const float rs = rsqrtf(block_sum(row_sumsq(r, nv), red) / (float)D + eps);
+#pragma unroll
+  for (int i = 0; i < kMaxV4; ++i) {
+    const int idx = threadIdx.x + i * blockDim.x;
+    if (idx < nv) {
+      const float4 gg = load4(g + 4 * idx);
+      const float4 x = r.v[i];
+      put_act4(u, plane, 4 * (size_t)idx, make_float4(x.x * rs * gg.x, x.y * rs * gg.y, x.z * rs * gg.z, x.w * rs * gg.w));
+    }
+  }
+}
+
+template <typename T>
+__device__ __forceinline__ void load_row(const T* x, int D, RowRegs& r) {
+  const int nv = D >> 2;
+#pragma unroll
+  for (int i = 0; i < kMaxV4; ++i) {
+    const int idx = threadIdx.x + i * blockDim.x;
+    if (idx < nv) r.v[i] = load4(x + 4 * idx);
+  }
 }
 
 template <typename T>
@@ -36,6 +73,8 @@ __global__ void __launch_bounds__(kRowThreads) embed_norm_kernel(const T* embed,
                                                                  float* x, T* u, size_t plane, int* zero_ptr,
                                                                  int zero_n, int32_t* status) {
   __shared__ float red[32];
+  griddep_wait();
+  griddep_trigger();
   const int row = blockIdx.x, b = row / block, k = row - b * block;
   if (zero_ptr)
     for (int i = row * blockDim.x + threadIdx.x; i < zero_n; i += gridDim.x * blockDim.x) zero_ptr[i] = 0;
@@ -44,18 +83,26 @@ __global__ void __launch_bounds__(kRowThreads) embed_norm_kernel(const T* embed,
     if (threadIdx.x == 0) report_status(status, DFLASH_ERR_INVALID_ARG);
     tok = 0;
   }
-  const T* e = embed + (size_t)tok * D;
+  RowRegs r;
+  load_row(embed + (size_t)tok * D, D, r);
   float* xr = x + (size_t)row * D;
-  for (int i = threadIdx.x; i < D; i += blockDim.x) xr[i] = to_f32(e[i]);
-  __syncthreads();
-  norm_row(xr, g, eps, D, u + (size_t)row * D, plane, red);
+#pragma unroll
+  for (int i = 0; i < kMaxV4; ++i) {
+    const int idx = threadIdx.x + i * blockDim.x;
+    if (idx < (D >> 2)) *reinterpret_cast<float4*>(xr + 4 * idx) = r.v[i];
+  }
+  norm_store(r, g, eps, D, u + (size_t)row * D, plane, red);
 }
 
 template <typename T>
 __global__ void __launch_bounds__(kRowThreads) rmsnorm_kernel(const float* x, const T* g, float eps, int D, T* u,
                                                               size_t plane) {
   __shared__ float red[32];
-  norm_row(x + (size_t)blockIdx.x * D, g, eps, D, u + (size_t)blockIdx.x * D, plane, red);
+  griddep_wait();
+  griddep_trigger();
+  RowRegs r;
+  load_row(x + (size_t)blockIdx.x * D, D, r);
+  norm_store(r, g, eps, D, u + (size_t)blockIdx.x * D, plane, red);
 }
 
 template <typename T>
@@ -63,22 +110,31 @@ __global__ void __launch_bounds__(kRowThreads) final_norm_kernel(const float* x,
                                                                  int D, T* hm, size_t plane,
                                                                  unsigned long long* slots) {
   __shared__ float red[32];
+  griddep_wait();
+  griddep_trigger();
   const int r = blockIdx.x;                   // compact mask-row index
   const int b = r / (block - 1), k = r - b * (block - 1) + 1;
   if (threadIdx.x == 0) slots[r] = 0ull;
-  norm_row(x + ((size_t)b * block + k) * D, g, eps, D, hm + (size_t)r * D, plane, red);
+  RowRegs v;
+  load_row(x + ((size_t)b * block + k) * D, D, v);
+  norm_store(v, g, eps, D, hm + (size_t)r * D, plane, red);
 }
 
 template <typename T>
 __global__ void __launch_bounds__(kRowThreads) fuse_norm_kernel(const float* y, const T* g, float eps,
                                                                 const int2* rowinfo, int D, T* ht, size_t plane) {
   __shared__ float red[32];
+  griddep_wait();
+  griddep_trigger();
   const int row = blockIdx.x;
   if (rowinfo[row].x < 0) {
-    for (int i = threadIdx.x; i < D; i += blockDim.x) put_act(ht, plane, (size_t)row * D + i, 0.f);
+    for (int i = threadIdx.x; i < (D >> 2); i += blockDim.x)
+      put_act4(ht, plane, (size_t)row * D + 4 * i, make_float4(0.f, 0.f, 0.f, 0.f));
     return;
   }
-  norm_row(y + (size_t)row * D, g, eps, D, ht + (size_t)row * D, plane, red);
+  RowRegs r;
+  load_row(y + (size_t)row * D, D, r);
+  norm_store(r, g, eps, D, ht + (size_t)row * D, plane, red);
 }
 
 // One CTA: exclusive scan of n_new, per-row (request, position), ctx_len update.
@@ -89,6 +145,8 @@ __global__ void __launch_bounds__(1024) inject_prep_kernel(const int32_t* n_new,
   int* off = sh;
   int* base = sh + B;
   int* cnt = sh + 2 * B;
+  griddep_wait();
+  griddep_trigger();
   for (int i = threadIdx.x; i < zero_n; i += blockDim.x) zero_ptr[i] = 0;
   if (threadIdx.x == 0) {
     int acc = 0;
@@ -136,6 +194,8 @@ __global__ void __launch_bounds__(1024) inject_prep_kernel(const int32_t* n_new,
 }
 
 __global__ void argmax_finalize_kernel(const unsigned long long* slots, int rows, int32_t* drafts) {
+  griddep_wait();
+  griddep_trigger();
   int r = blockIdx.x * blockDim.x + threadIdx.x;
   if (r < rows) drafts[r] = unpack_argmax_index(slots[r]);
 }
@@ -143,6 +203,8 @@ __global__ void argmax_finalize_kernel(const unsigned long long* slots, int rows
 // One warp per request: n = leading positions where d_{k+1} == y_k.
 __global__ void verify_kernel(const int32_t* draft, const int32_t* target, int B, int block, int32_t* accept_len,
                               int32_t* out_tokens, int32_t* next_anchor) {
+  griddep_wait();
+  griddep_trigger();
   const int lane = threadIdx.x & 31;
   const int b = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (b >= B) return;
@@ -168,54 +230,48 @@ cudaError_t embed_norm_launch(const T* embed, const int32_t* anchor, int mask_id
                               const T* g, float eps, float* x, T* u, size_t plane, int* zero_ptr, int zero_n,
                               int32_t* status, cudaStream_t s) {
   if (B * block == 0) return cudaSuccess;
-  embed_norm_kernel<T><<<B * block, kRowThreads, 0, s>>>(embed, anchor, mask_id, vocab, block, D, g, eps, x, u, plane,
-                                                         zero_ptr, zero_n, status);
-  return cudaGetLastError();
+  return launch_pdl(embed_norm_kernel<T>, dim3(B * block), dim3(kRowThreads), 0, s, embed, anchor, mask_id, vocab, block,
+                    D, g, eps, x, u, plane, zero_ptr, zero_n, status);
 }
 
 template <typename T>
 cudaError_t rmsnorm_launch(const float* x, const T* g, float eps, int rows, int D, T* u, size_t plane, cudaStream_t s) {
   if (rows == 0) return cudaSuccess;
-  rmsnorm_kernel<T><<<rows, kRowThreads, 0, s>>>(x, g, eps, D, u, plane);
-  return cudaGetLastError();
+  return launch_pdl(rmsnorm_kernel<T>, dim3(rows), dim3(kRowThreads), 0, s, x, g, eps, D, u, plane);
 }
 
 template <typename T>
 cudaError_t final_norm_launch(const float* x, const T* g, float eps, int B, int block, int D, T* hm, size_t plane,
                               unsigned long long* slots, cudaStream_t s) {
   if (B * (block - 1) == 0) return cudaSuccess;
-  final_norm_kernel<T><<<B * (block - 1), kRowThreads, 0, s>>>(x, g, eps, block, D, hm, plane, slots);
-  return cudaGetLastError();
+  return launch_pdl(final_norm_kernel<T>, dim3(B * (block - 1)), dim3(kRowThreads), 0, s, x, g, eps, block, D, hm, plane,
+                    slots);
 }
 
 template <typename T>
 cudaError_t fuse_norm_launch(const float* y, const T* g, float eps, const int2* rowinfo, int rows, int D, T* ht,
                              size_t plane, cudaStream_t s) {
   if (rows == 0) return cudaSuccess;
-  fuse_norm_kernel<T><<<rows, kRowThreads, 0, s>>>(y, g, eps, rowinfo, D, ht, plane);
-  return cudaGetLastError();
+  return launch_pdl(fuse_norm_kernel<T>, dim3(rows), dim3(kRowThreads), 0, s, y, g, eps, rowinfo, D, ht, plane);
 }
 
 cudaError_t inject_prep_launch(const int32_t* n_new, int32_t* ctx_len, int B, int max_rows, int cap, int2* rowinfo,
                                int* zero_ptr, int zero_n, int32_t* status, cudaStream_t s) {
-  inject_prep_kernel<<<1, 1024, 3 * B * sizeof(int), s>>>(n_new, ctx_len, B, max_rows, cap, rowinfo, zero_ptr, zero_n,
-                                                          status);
-  return cudaGetLastError();
+  return launch_pdl(inject_prep_kernel, dim3(1), dim3(1024), 3 * B * sizeof(int), s, n_new, ctx_len, B, max_rows, cap,
+                    rowinfo, zero_ptr, zero_n, status);
 }
 
 cudaError_t argmax_finalize_launch(const unsigned long long* slots, int rows, int32_t* drafts, cudaStream_t s) {
   if (rows == 0) return cudaSuccess;
-  argmax_finalize_kernel<<<(rows + 255) / 256, 256, 0, s>>>(slots, rows, drafts);
-  return cudaGetLastError();
+  return launch_pdl(argmax_finalize_kernel, dim3((rows + 255) / 256), dim3(256), 0, s, slots, rows, drafts);
 }
 
 cudaError_t verify_launch(const int32_t* draft, const int32_t* target, int B, int block, int32_t* accept_len,
                           int32_t* out_tokens, int32_t* next_anchor, cudaStream_t s) {
   if (B == 0) return cudaSuccess;
   const int warps = 4;
-  verify_kernel<<<(B + warps - 1) / warps, 32 * warps, 0, s>>>(draft, target, B, block, accept_len, out_tokens,
-                                                               next_anchor);
-  return cudaGetLastError();
+  return launch_pdl(verify_kernel, dim3((B + warps - 1) / warps), dim3(32 * warps), 0, s, draft, target, B, block,
+                    accept_len, out_tokens, next_anchor);
 }
 
 #define DFLASH_EW_INST(T)                                                                                        \

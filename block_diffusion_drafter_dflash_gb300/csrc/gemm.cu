@@ -37,6 +37,8 @@ __global__ void __launch_bounds__(kSimtThreads) gemm_simt_kernel(const __grid_co
   const int k_begin = split * p.kblocks_per_split * 64;
   const int k_end = min(p.K, k_begin + p.kblocks_per_split * 64);
   const T* X = static_cast<const T*>(p.x);
+  griddep_wait();
+  griddep_trigger();
 
   float acc[8];
 #pragma unroll
@@ -136,8 +138,7 @@ cudaError_t gemm_launch(const GemmProblem& p, const GemmPlan& plan, const Epi& e
     if (plan.tc) return gemm_tc_launch<Epi>(p, plan, epi, s);
   }
   dim3 grid(p.total_tiles, plan.splits, plan.token_tiles);
-  gemm_simt_kernel<T, Epi><<<grid, kSimtThreads, 0, s>>>(p, epi);
-  return cudaGetLastError();
+  return launch_pdl(gemm_simt_kernel<T, Epi>, grid, dim3(kSimtThreads), 0, s, p, epi);
 }
 
 #define DFLASH_GEMM_INST(T)                                                                            \

@@ -84,6 +84,15 @@ __global__ void __launch_bounds__(128, 1) gemm_tc_kernel(const __grid_constant__
   const CUtensorMap* wmaps = static_cast<const CUtensorMap*>(p.wmaps);
   const CUtensorMap* map0 = wmaps + sg.map0;
   const CUtensorMap* map1 = wmaps + (sg.paired ? sg.map1 : sg.map0);
+  // optional timestamps: [0] start, [1] set up, [2] first stage landed,
+  // [3] last stage landed, [4] accumulator ready, [5] done, [6] SM, [7] reduced
+  unsigned long long* tr = p.trace ? p.trace + 8 * ((size_t)(blockIdx.z * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x)
+                                   : nullptr;
+  if (tr && threadIdx.x == 0) {
+    tr[0] = ptx::globaltimer();
+    tr[6] = ptx::smid();
+    tr[7] = 0;
+  }
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::kStages; ++s) {
@@ -104,27 +113,46 @@ __global__ void __launch_bounds__(128, 1) gemm_tc_kernel(const __grid_constant__
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  griddep_trigger();
+  if (tr && threadIdx.x == 0) tr[1] = ptx::globaltimer();
 
   if (warp == 0 && lane == 0) {
-    // ---- TMA producer
+    // ---- TMA producer.  The weight tiles of the first stages do not depend
+    // on earlier kernels and are requested before griddep_wait(), so they
+    // stream in while the previous kernel drains.
     const uint64_t pol_w = ptx::policy_evict_first(), pol_x = ptx::policy_evict_last();
     const int r0 = half_first_row(sg, tis, 0), r1 = half_first_row(sg, tis, 1);
-    int issued = 0;
-    for (int i = 0; i < nk; ++i) {
+    const int prow = static_cast<int>(p.plane_stride / p.ldx);
+    auto load_w = [&](int i) {
+      uint8_t* a = smem + (i % C::kStages) * C::kStageBytes;
+      const int kx = (kb0 + i) * 64;
+      ptx::tma_load_2d(a, map0, full + i % C::kStages, kx, r0, pol_w);
+      ptx::tma_load_2d(a + kHalfN * 128, map1, full + i % C::kStages, kx, r1, pol_w);
+    };
+    auto load_x = [&](int i) {
+      uint8_t* b = smem + (i % C::kStages) * C::kStageBytes + C::kABytes;
+      const int kx = (kb0 + i) * 64;
+#pragma unroll
+      for (int pl = 0; pl < PL; ++pl)
+        ptx::tma_load_2d(b + pl * BN * 128, &xmap, full + i % C::kStages, kx, pl * prow + m0, pol_x);
+    };
+    const int pre = min(nk, C::kStages);
+    for (int i = 0; i < pre; ++i) {
+      ptx::mbar_arrive_expect_tx(full + i, C::kStageBytes);
+      load_w(i);
+    }
+    griddep_wait();
+    for (int i = 0; i < pre; ++i) load_x(i);
+    int issued = pre;
+    for (int i = pre; i < nk; ++i) {
       const int s = i % C::kStages;
-      if (i >= C::kStages && !ptx::mbar_wait(empty + s, ((i / C::kStages) & 1) ^ 1, kWaitBudget, status)) {
+      if (!ptx::mbar_wait(empty + s, ((i / C::kStages) & 1) ^ 1, kWaitBudget, status)) {
         flags[0] = 1;
         break;
       }
-      uint8_t* a = smem + s * C::kStageBytes;
       ptx::mbar_arrive_expect_tx(full + s, C::kStageBytes);
-      const int kx = (kb0 + i) * 64;
-      ptx::tma_load_2d(a, map0, full + s, kx, r0, pol_w);
-      ptx::tma_load_2d(a + kHalfN * 128, map1, full + s, kx, r1, pol_w);
-      const int prow = static_cast<int>(p.plane_stride / p.ldx);
-#pragma unroll
-      for (int pl = 0; pl < PL; ++pl)
-        ptx::tma_load_2d(a + C::kABytes + pl * BN * 128, &xmap, full + s, kx, pl * prow + m0, pol_x);
+      load_w(i);
+      load_x(i);
       ++issued;
     }
     flags[2] = issued;
@@ -137,6 +165,7 @@ __global__ void __launch_bounds__(128, 1) gemm_tc_kernel(const __grid_constant__
         flags[0] = 1;
         break;
       }
+      if (tr && (i == 0 || i == nk - 1)) tr[i == 0 ? 2 : 3] = ptx::globaltimer();
       ptx::tc_fence_after();
       const uint64_t ad = ptx::smem_desc_sw128(smem + s * C::kStageBytes);
       const uint64_t bd = ptx::smem_desc_sw128(smem + s * C::kStageBytes + C::kABytes);
@@ -150,10 +179,12 @@ __global__ void __launch_bounds__(128, 1) gemm_tc_kernel(const __grid_constant__
   __syncwarp();
 
   // ---- epilogue (all 4 warps; warp w owns accumulator lanes 32w..32w+31)
+  griddep_wait();
   const bool ok = ptx::mbar_wait(accf, 0, kWaitBudget, status);
   ptx::tc_fence_after();
   __syncthreads();
   const bool abort = !ok || flags[0] != 0;
+  if (tr && threadIdx.x == 0) tr[4] = ptx::globaltimer();
   float* st = reinterpret_cast<float*>(smem);   // [128][kChunk+1], reuses the drained stages
   constexpr int ld = C::kChunk + 1;
   const int n = warp * 32 + lane;
@@ -192,15 +223,24 @@ __global__ void __launch_bounds__(128, 1) gemm_tc_kernel(const __grid_constant__
       __syncthreads();
       if (flags[1]) {
         __threadfence();
+        // thread n sums feature n of every row of the chunk over all splits;
+        // the loads of one split are independent, so a chunk costs about one
+        // L2 round trip per split
+        const size_t sstride = static_cast<size_t>(p.M) * ntot;
         for (int c0 = 0; c0 < mc; c0 += C::kChunk) {
           const int cc = min(C::kChunk, mc - c0);
-          for (int j = 0; j < cc; ++j) {
-            float s = 0.f;
-            for (int sp = 0; sp < p.splits; ++sp)
-              s += __ldcg(p.partial + (static_cast<size_t>(sp) * p.M + m0 + c0 + j) * ntot +
-                          static_cast<size_t>(gtile) * kTileN + n);
-            st[n * ld + j] = s;
+          const float* base = p.partial + static_cast<size_t>(m0 + c0) * ntot + static_cast<size_t>(gtile) * kTileN + n;
+          float acc[C::kChunk];
+#pragma unroll
+          for (int j = 0; j < C::kChunk; ++j) acc[j] = 0.f;
+          for (int sp = 0; sp < p.splits; ++sp) {
+            const float* src = base + sp * sstride;
+#pragma unroll
+            for (int j = 0; j < C::kChunk; ++j)
+              if (j < cc) acc[j] += __ldcg(src + static_cast<size_t>(j) * ntot);
           }
+#pragma unroll
+          for (int j = 0; j < C::kChunk; ++j) st[n * ld + j] = acc[j];
           __syncthreads();
           epi(st, ld, m0 + c0, cc, gtile, sg, tis);
           __syncthreads();
@@ -216,6 +256,10 @@ __global__ void __launch_bounds__(128, 1) gemm_tc_kernel(const __grid_constant__
 
   ptx::tc_fence_before();
   __syncthreads();
+  if (tr && threadIdx.x == 0) {
+    tr[5] = ptx::globaltimer();
+    tr[7] = flags[1];
+  }
   if (warp == 1) {
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem, C::kTmemCols);
@@ -256,8 +300,7 @@ cudaError_t launch_bn(const GemmProblem& p, const GemmPlan& plan, const Epi& epi
   CUtensorMap xmap;
   if (!encode_activation_map(&xmap, p.x, p.K, rows, p.ldx, BN)) return cudaErrorInvalidValue;
   dim3 grid(p.total_tiles, plan.splits, plan.token_tiles);
-  gemm_tc_kernel<BN, PL, Epi><<<grid, 128, C::kSmem, s>>>(xmap, p, epi, p.status);
-  return cudaGetLastError();
+  return launch_pdl(gemm_tc_kernel<BN, PL, Epi>, grid, dim3(128), C::kSmem, s, xmap, p, epi, p.status);
 }
 
 }  // namespace

@@ -219,6 +219,15 @@ int32_t dflash_verify_greedy(const int32_t* draft_dev, const int32_t* target_arg
  * every device), for launch accounting. */
 uint64_t dflash_launch_count(void);
 
+/* Per-CTA timestamps of one projection GEMM launch, for performance work.
+ * When the environment variable DFLASH_TRACE_GEMM=<k> is set at model
+ * creation, the model's k-th GEMM launch (counting from 0) records, for every
+ * CTA c, 8 values at host[8c .. 8c+7]: globaltimer ns at start, after set-up,
+ * when the first and the last K stage landed, when the accumulator was ready
+ * and at the end; the SM id; 1 if the CTA ran the split-K reduction.
+ * Copies min(n, 8*65536) values; DFLASH_ERR_UNSUPPORTED when tracing is off. */
+int32_t dflash_trace_read(const dflash_model* model, uint64_t* host, size_t n);
+
 /* Stage ids reported by the profiler. */
 #define DFLASH_STAGE_FUSE 0     /* fusion GEMM (W_c)                          */
 #define DFLASH_STAGE_INJECT 1   /* K/V injection GEMM (all layers)            */
