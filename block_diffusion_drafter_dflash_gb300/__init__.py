@@ -20,7 +20,7 @@ from ._abi import DFlashError, check, lib
 __all__ = ["DFlashError", "Model", "Cache", "lib", "dflash_model_create", "dflash_cache_init",
            "dflash_workspace_bytes", "dflash_workspace", "dflash_inject_context", "dflash_draft_block",
            "dflash_verify_greedy", "dflash_get_status", "dflash_clear_status", "dflash_version",
-           "dflash_launch_count", "dflash_profile_start", "dflash_profile_stop"]
+           "dflash_launch_count", "dflash_profile_start", "dflash_profile_stop", "dflash_inject_context_noalloc"]
 
 
 def _stream_ptr(stream: Optional[torch.cuda.Stream]) -> ctypes.c_void_p:
@@ -169,6 +169,20 @@ def dflash_inject_context(model: Model, cache: Cache, feats: torch.Tensor, n_new
     check(lib().dflash_inject_context(model.handle, cache.handle, _ptr(feats), _ptr(n_new_dev), host, rows,
                                       _ptr(workspace), workspace.numel(), _stream_ptr(stream)),
           "dflash_inject_context")
+
+
+def dflash_inject_context_noalloc(model: Model, cache: Cache, feats: torch.Tensor, n_new_dev: torch.Tensor,
+                                  n_new_host=None, max_rows: Optional[int] = None, stream=None) -> None:
+    """dflash_inject_context without a workspace, for callers that cannot
+    allocate device memory: the library's fixed static scratch is used."""
+    if n_new_dev.dtype != torch.int32 or feats.dtype != model.dtype:
+        raise ValueError("n_new_dev must be int32 and feats of the model dtype")
+    rows = feats.shape[0] if max_rows is None else int(max_rows)
+    host = None
+    if n_new_host is not None:
+        host = (ctypes.c_int32 * cache.batch)(*[int(v) for v in n_new_host])
+    check(lib().dflash_inject_context_noalloc(model.handle, cache.handle, _ptr(feats), _ptr(n_new_dev), host, rows,
+                                              _stream_ptr(stream)), "dflash_inject_context_noalloc")
 
 
 def dflash_draft_block(model: Model, cache: Cache, anchor_dev: torch.Tensor, block_size: int,

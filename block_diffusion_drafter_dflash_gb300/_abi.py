@@ -57,6 +57,8 @@ SIGNATURES = {
     "dflash_workspace_bytes": (c_size, [c_ptr, c_i32, c_i32, c_i32, c_i32]),
     "dflash_inject_context": (c_i32, [c_ptr, c_ptr, c_ptr, c_ptr, c_i32p, c_i32, c_ptr, c_size, c_ptr]),
     "dflash_draft_block": (c_i32, [c_ptr, c_ptr, c_ptr, c_i32, c_ptr, c_ptr, c_ptr, c_size, c_ptr]),
+    "dflash_noalloc_scratch_bytes": (c_size, []),
+    "dflash_inject_context_noalloc": (c_i32, [c_ptr, c_ptr, c_ptr, c_ptr, c_i32p, c_i32, c_ptr]),
     "dflash_verify_greedy": (c_i32, [c_ptr, c_ptr, c_i32, c_i32, c_ptr, c_ptr, c_ptr, c_ptr]),
     "dflash_launch_count": (ctypes.c_uint64, []),
     "dflash_trace_read": (c_i32, [c_ptr, ctypes.POINTER(ctypes.c_uint64), c_size]),

@@ -4,6 +4,7 @@
 #include <algorithm>
 #include <atomic>
 #include <cmath>
+#include <mutex>
 #include <cstdarg>
 #include <cstdio>
 #include <cstdlib>
@@ -676,6 +677,89 @@ int32_t dflash_profile_stop(dflash_model* m, dflash_stream_t stream, float* ms_b
   }
   p.used = 0;
   p.stage.clear();
+  return DFLASH_OK;
+}
+
+// ---------------------------------------------------------------------------
+// Allocation-free variant of dflash_inject_context (scratch in a static array).
+// ---------------------------------------------------------------------------
+}  // extern "C"
+
+namespace {
+
+// Scratch of dflash_inject_context_noalloc.  A file-scope device array: every
+// GPU that loads this library holds it until the process exits.  In host code
+// the name is only a stand-in for the symbol, never a device address.
+constexpr size_t kNoAllocScratchBytes = size_t(8) << 20;
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mu;
+void* g_noalloc_ptr[kMaxDevices] = {};
+
+// Device address of the scratch array on the current device, looked up once
+// per device (with that device current) and then reused.
+int32_t noalloc_scratch(int dev, void** out) {
+  if (dev < 0 || dev >= kMaxDevices) return fail(DFLASH_ERR_UNSUPPORTED, "device %d out of range", dev);
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (!g_noalloc_ptr[dev]) {
+    void* p = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(noalloc scratch)");
+    g_noalloc_ptr[dev] = p;
+  }
+  *out = g_noalloc_ptr[dev];
+  return DFLASH_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t dflash_noalloc_scratch_bytes(void) { return kNoAllocScratchBytes; }
+
+int32_t dflash_inject_context_noalloc(const dflash_model* m, dflash_cache* cache, const void* feats,
+                                      const int32_t* n_new_dev, const int32_t* n_new_host, int32_t max_rows,
+                                      dflash_stream_t stream) {
+  if (!m || !cache) return fail(DFLASH_ERR_INVALID_ARG, "model or cache is NULL");
+  if (cache->model != m) return fail(DFLASH_ERR_INVALID_ARG, "cache was made for another model");
+  if (max_rows < 0) return fail(DFLASH_ERR_INVALID_ARG, "max_rows %d < 0", max_rows);
+  if (!n_new_dev) return fail(DFLASH_ERR_INVALID_ARG, "n_new_dev is NULL");
+  if (max_rows > 0 && !feats) return fail(DFLASH_ERR_INVALID_ARG, "feats is NULL");
+  int32_t rc = check_device(m);
+  if (rc) return rc;
+  if (n_new_host) {
+    long total = 0;
+    for (int b = 0; b < cache->batch; ++b) {
+      if (n_new_host[b] < 0) return fail(DFLASH_ERR_INVALID_ARG, "n_new[%d] = %d < 0", b, n_new_host[b]);
+      total += n_new_host[b];
+      if (cache->len_known && cache->len_host[b] + (long)n_new_host[b] > cache->cap)
+        return fail(DFLASH_ERR_CAPACITY, "request %d: %d + %d tokens exceed capacity %d", b, cache->len_host[b],
+                    n_new_host[b], cache->cap);
+    }
+    if (total > max_rows) return fail(DFLASH_ERR_SHAPE, "sum of n_new (%ld) > max_rows (%d)", total, max_rows);
+  }
+  if (max_rows == 0) return DFLASH_OK;
+  const WsPlan P = plan_ws(m, cache->batch, cache->cap, 0, max_rows);
+  if (P.total > kNoAllocScratchBytes)
+    return fail(DFLASH_ERR_CAPACITY,
+                "dflash_inject_context_noalloc: %d rows need %zu bytes of scratch, more than the fixed %zu; "
+                "inject fewer rows per call or use dflash_inject_context with a workspace",
+                max_rows, P.total, kNoAllocScratchBytes);
+  void* scratch = nullptr;
+  rc = noalloc_scratch(m->device, &scratch);
+  if (rc) return rc;
+  cudaStream_t s = (cudaStream_t)stream;
+  rc = m->cfg.dtype == DFLASH_DTYPE_F32
+           ? run_inject<float>(m, cache, feats, n_new_dev, max_rows, static_cast<char*>(scratch), P, s)
+           : run_inject<__nv_bfloat16>(m, cache, feats, n_new_dev, max_rows, static_cast<char*>(scratch), P, s);
+  if (rc) return rc;
+  if (n_new_host) {
+    if (cache->len_known)
+      for (int b = 0; b < cache->batch; ++b) cache->len_host[b] += n_new_host[b];
+  } else {
+    cache->len_known = false;
+  }
   return DFLASH_OK;
 }
 

@@ -184,6 +184,31 @@ int32_t dflash_inject_context(const dflash_model* model, dflash_cache* cache, co
                               const int32_t* n_new_dev, const int32_t* n_new_host, int32_t max_rows,
                               void* workspace, size_t workspace_bytes, dflash_stream_t stream);
 
+/* --- allocation-free injection --------------------------------------------------
+ * The paper has no counterpart to this entry point; it exists for callers that
+ * cannot allocate device memory, so cannot provide the workspace that
+ * dflash_inject_context needs: code that runs under a fixed, already committed
+ * memory budget, runtimes that hand the library only the buffers of the
+ * request being served, or hosts without access to a device allocator.
+ *
+ * Same arguments, results and checks as dflash_inject_context, minus the
+ * workspace: the scratch lives in one file-scope device array of
+ * dflash_noalloc_scratch_bytes() bytes (8 MiB) that every GPU loading this
+ * library holds until the process exits.  No call allocates or frees memory.
+ *   - A launch whose scratch plan exceeds that size (an 8B-shaped drafter
+ *     fits about 40 injected rows) returns DFLASH_ERR_CAPACITY without
+ *     launching; inject fewer rows per call.
+ *   - The first call on a device looks the array's device address up with
+ *     cudaGetSymbolAddress (with that device current) and caches it; make that
+ *     first call before any stream capture.
+ *   - Every call on a device shares the one array and leaves the last call's
+ *     contents in it (what must start at zero is cleared by each call), so
+ *     calls that overlap on the GPU — two streams, or two threads — race. */
+size_t dflash_noalloc_scratch_bytes(void);
+int32_t dflash_inject_context_noalloc(const dflash_model* model, dflash_cache* cache, const void* feats,
+                                      const int32_t* n_new_dev, const int32_t* n_new_host, int32_t max_rows,
+                                      dflash_stream_t stream);
+
 /* --- stage 3+4: drafter forward pass, shared LM head, argmax -------------------
  * Paper §4.2 / explainer step 3: block = [anchor, mask x (block_size-1)] at
  * positions ctx_len[b] .. ctx_len[b]+block_size-1; every block row attends to
