@@ -65,6 +65,24 @@ def load_peaks():
         return 6800.0, 1900.0, "fallback"
 
 
+# ---------------------------------------------------------------- multi-rank aggregation
+def max_over_ranks(value: float, device="cpu") -> float:
+    """The largest `value` over all ranks (the slowest rank's time); the value
+    itself when there is one rank."""
+    dist = torch.distributed
+    if dist.is_available() and dist.is_initialized() and dist.get_world_size() > 1:
+        t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+    return float(value)
+
+
+def job_throughput(ms_per_step_max: float, drafted_per_rank_step: int, world: int) -> float:
+    """Whole-job drafted tokens/s: every rank drafts for its own requests each
+    step; the job's step takes as long as its slowest rank."""
+    return world * drafted_per_rank_step / (ms_per_step_max / 1e3)
+
+
 # ---------------------------------------------------------------- clocks
 class Clocks:
     """nvidia-smi sampler running while the timed region runs."""
@@ -247,14 +265,10 @@ def run_gpu(args, rank, world, local):
     barrier()
     launches = launches_per_cycle * K
     clk = clocks.stop()
-    ms = t0.elapsed_time(t1) / K
+    ms = max_over_ranks(t0.elapsed_time(t1) / K, "cuda")
     mean_tau = float(cyc.tau_acc.item()) / (K * wl.batch)
-    if dist:
-        tt = torch.tensor([ms], device="cuda")
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        ms = float(tt.item())
     drafted = wl.batch * (wl.block - 1)
-    value = world * drafted / (ms / 1e3)
+    value = job_throughput(ms, drafted, world)
 
     # profiled pass (eager launches): CUDA events around each launch, per stage
     KP = min(K, 20)
@@ -328,12 +342,8 @@ def run_e2e(cyc, K, wl, barrier, world):
             h.copy_(d, non_blocking=True)
         torch.cuda.current_stream().synchronize()
     barrier()
-    ms = (time.perf_counter() - t0) * 1e3 / K
-    if world > 1 and torch.distributed.is_initialized():
-        tt = torch.tensor([ms], device="cuda")
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        ms = float(tt.item())
-    return {"value": round(world * wl.batch * (wl.block - 1) / (ms / 1e3), 2), "unit": UNIT,
+    ms = max_over_ranks((time.perf_counter() - t0) * 1e3 / K, "cuda")
+    return {"value": round(job_throughput(ms, wl.batch * (wl.block - 1), world), 2), "unit": UNIT,
             "ms_per_step": round(ms, 4), "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
 
 

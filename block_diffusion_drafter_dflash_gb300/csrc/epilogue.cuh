@@ -22,16 +22,28 @@ struct EpiStoreF32 {
   }
 };
 
-// x[row][feature] += acc  (fp32 residual stream; W_O and W_D outputs)
+// x[row][feature] += acc  (fp32 residual stream; W_O and W_D outputs).
+// Thread n owns feature n of a group of rows: the residual values of 8 rows
+// are loaded before any is stored, so the loads overlap.
 struct EpiResidual {
   float* x;
   int ldx;
   __device__ __forceinline__ void operator()(const float* t, int ld, int m0, int mc, int gtile, const GemmSeg&,
                                              int) const {
-    for (int idx = threadIdx.x; idx < mc * kTileN; idx += blockDim.x) {
-      int m = idx / kTileN, n = idx % kTileN;
-      float* p = x + (size_t)(m0 + m) * ldx + (size_t)gtile * kTileN + n;
-      *p = *p + t[n * ld + m];
+    const int n = threadIdx.x & (kTileN - 1), step = blockDim.x / kTileN;
+    float* col = x + (size_t)gtile * kTileN + n;
+    for (int mb = threadIdx.x / kTileN; mb < mc; mb += 8 * step) {
+      float v[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int m = mb + j * step;
+        if (m < mc) v[j] = col[(size_t)(m0 + m) * ldx];
+      }
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int m = mb + j * step;
+        if (m < mc) col[(size_t)(m0 + m) * ldx] = v[j] + t[n * ld + m];
+      }
     }
   }
 };
@@ -87,7 +99,7 @@ struct EpiQKV {
       int m = idx / kTileN, n = idx % kTileN;
       int row = m0 + m, b = row / block, k = row - b * block;
       int feat = tis * kTileN + n, head = feat / hd, d = feat - head * hd;
-      float v = tag == 2 ? t[n * ld + m] : rope_apply(t, ld, m, n, d, hd, ctx_len[b] + k, inv_freq);
+      float v = tag == 2 ? t[n * ld + m] : rope_apply(t, ld, m, n, d, hd, __ldg(ctx_len + b) + k, inv_freq);
       dst[(((size_t)b * nh + head) * block + k) * hd + d] = v;
     }
   }
@@ -108,7 +120,7 @@ struct EpiInject {
     float* dst = is_v ? vc : kc;
     for (int idx = threadIdx.x; idx < mc * kTileN; idx += blockDim.x) {
       int m = idx / kTileN, n = idx % kTileN;
-      int2 ri = rowinfo[m0 + m];
+      int2 ri = __ldg(rowinfo + m0 + m);
       if (ri.x < 0) continue;
       int feat = tis * kTileN + n, head = feat / hd, d = feat - head * hd;
       float v = is_v ? t[n * ld + m] : rope_apply(t, ld, m, n, d, hd, ri.y, inv_freq);

@@ -223,24 +223,60 @@ __global__ void __launch_bounds__(128, 1) gemm_tc_kernel(const __grid_constant__
       __syncthreads();
       if (flags[1]) {
         __threadfence();
-        // thread n sums feature n of every row of the chunk over all splits;
-        // the loads of one split are independent, so a chunk costs about one
-        // L2 round trip per split
+        // thread t sums features 4(t%32)..+3 of rows t/32, t/32+4, ... over
+        // all splits with 16-byte loads, 4 splits' loads in flight at a time
         const size_t sstride = static_cast<size_t>(p.M) * ntot;
+        const int fq = (threadIdx.x & 31) * 4, r0 = threadIdx.x >> 5;
+        constexpr int kRows = C::kChunk / 4;
         for (int c0 = 0; c0 < mc; c0 += C::kChunk) {
           const int cc = min(C::kChunk, mc - c0);
-          const float* base = p.partial + static_cast<size_t>(m0 + c0) * ntot + static_cast<size_t>(gtile) * kTileN + n;
-          float acc[C::kChunk];
+          const float* base =
+              p.partial + static_cast<size_t>(m0 + c0) * ntot + static_cast<size_t>(gtile) * kTileN + fq;
+          float4 acc[kRows];
 #pragma unroll
-          for (int j = 0; j < C::kChunk; ++j) acc[j] = 0.f;
-          for (int sp = 0; sp < p.splits; ++sp) {
-            const float* src = base + sp * sstride;
+          for (int i = 0; i < kRows; ++i) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+          int sp = 0;
+          for (; sp + 4 <= p.splits; sp += 4) {
+            float4 v[4][kRows];
 #pragma unroll
-            for (int j = 0; j < C::kChunk; ++j)
-              if (j < cc) acc[j] += __ldcg(src + static_cast<size_t>(j) * ntot);
+            for (int u = 0; u < 4; ++u)
+#pragma unroll
+              for (int i = 0; i < kRows; ++i) {
+                const int r = r0 + 4 * i;
+                v[u][i] = r < cc ? __ldcg(reinterpret_cast<const float4*>(base + (sp + u) * sstride +
+                                                                          static_cast<size_t>(r) * ntot))
+                                 : make_float4(0.f, 0.f, 0.f, 0.f);
+              }
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+#pragma unroll
+              for (int i = 0; i < kRows; ++i) {
+                acc[i].x += v[u][i].x;
+                acc[i].y += v[u][i].y;
+                acc[i].z += v[u][i].z;
+                acc[i].w += v[u][i].w;
+              }
           }
+          for (; sp < p.splits; ++sp)
 #pragma unroll
-          for (int j = 0; j < C::kChunk; ++j) st[n * ld + j] = acc[j];
+            for (int i = 0; i < kRows; ++i) {
+              const int r = r0 + 4 * i;
+              if (r < cc) {
+                const float4 v = __ldcg(reinterpret_cast<const float4*>(base + sp * sstride + static_cast<size_t>(r) * ntot));
+                acc[i].x += v.x;
+                acc[i].y += v.y;
+                acc[i].z += v.z;
+                acc[i].w += v.w;
+              }
+            }
+#pragma unroll
+          for (int i = 0; i < kRows; ++i) {
+            const int r = r0 + 4 * i;
+            st[(fq + 0) * ld + r] = acc[i].x;
+            st[(fq + 1) * ld + r] = acc[i].y;
+            st[(fq + 2) * ld + r] = acc[i].z;
+            st[(fq + 3) * ld + r] = acc[i].w;
+          }
           __syncthreads();
           epi(st, ld, m0 + c0, cc, gtile, sg, tis);
           __syncthreads();
