@@ -29,8 +29,8 @@ if ROOT not in sys.path:
 
 import torch  # noqa: E402
 
-from dflash_inputs import (AgreementPattern, make_agreement, make_features, make_tokens, make_weights,  # noqa: E402
-                           seed_for, synthetic_target_argmax, workloads)
+from dflash_inputs import (make_agreement, make_features, make_tokens, make_weights, seed_for,  # noqa: E402
+                           synthetic_target_argmax, workloads)
 
 METRIC = "drafted tokens/s & draft-cycle latency at bs1/bs32; % of HBM or TC roofline"
 UNIT = "drafted tokens/s"
@@ -200,23 +200,20 @@ class Cycle:
         self.tau_acc = torch.zeros(1, dtype=torch.long, device="cuda")
         self.anchor = make_tokens(cfg, B, seed=seed + 3, device="cuda")
         self.drafts = torch.empty((B, block - 1), dtype=torch.int32, device="cuda")
+        self.y = torch.empty((B, block), dtype=torch.int32, device="cuda")
         self.out = torch.empty((B, block), dtype=torch.int32, device="cuda")
-        self.next_anchor = torch.empty((B,), dtype=torch.int32, device="cuda")
+        self.next_anchor = self.anchor            # verification writes the next anchor in place
         self.graph = None
 
     def step(self):
         df = self.df
         df.dflash_inject_context(self.model, self.cache, self.feats, self.tau, None, self.rows, self.ws)
         df.dflash_draft_block(self.model, self.cache, self.anchor, self.block, self.drafts, None, self.ws)
-        pat = AgreementPattern(match=self.match.index_select(0, self.pidx)[0],
-                               off=self.off.index_select(0, self.pidx)[0],
-                               bonus=self.bonus.index_select(0, self.pidx)[0])
-        y = synthetic_target_argmax(self.drafts, pat, self.cfg.vocab)          # the (synthetic) target
-        df.dflash_verify_greedy(self.drafts, y, self.tau, self.out, self.next_anchor)
-        self.anchor.copy_(self.next_anchor)
-        self.tau_acc.add_(self.tau.sum())
-        self.pidx.add_(1)
-        self.pidx.remainder_(self.P)
+        # the (synthetic) target's greedy tokens for this block; also adds the
+        # previous cycle's accepted lengths to tau_acc
+        df.dflash_synthetic_target(self.drafts, self.match, self.off, self.bonus, self.pidx, self.y,
+                                   self.cfg.vocab, tau=self.tau, tau_sum=self.tau_acc)
+        df.dflash_verify_greedy(self.drafts, self.y, self.tau, self.out, self.anchor)
 
     def capture(self):
         """Capture one cycle in a CUDA graph (after eager warm-up)."""

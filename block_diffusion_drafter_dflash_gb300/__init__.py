@@ -210,6 +210,21 @@ def dflash_verify_greedy(draft_dev: torch.Tensor, target_argmax_dev: torch.Tenso
           "dflash_verify_greedy")
 
 
+def dflash_synthetic_target(drafts: torch.Tensor, match: torch.Tensor, off: torch.Tensor, bonus: torch.Tensor,
+                            pattern_idx: torch.Tensor, target_out: torch.Tensor, vocab: int,
+                            tau: Optional[torch.Tensor] = None, tau_sum: Optional[torch.Tensor] = None,
+                            stream=None) -> None:
+    """Benchmark utility: the synthetic target's answer for stacked agreement
+    patterns (match bool/uint8 [P,B,g-1], off int32 [P,B,g-1], bonus int32
+    [P,B]) selected by the device counter pattern_idx (int64 [1])."""
+    P, B = bonus.shape
+    g = target_out.shape[1]
+    m = match.view(torch.uint8) if match.dtype == torch.bool else match
+    check(lib().dflash_synthetic_target(_ptr(drafts) if g > 1 else None, _ptr(m), _ptr(off), _ptr(bonus), P,
+                                        _ptr(pattern_idx), _ptr(tau), _ptr(tau_sum), B, g, int(vocab),
+                                        _ptr(target_out), _stream_ptr(stream)), "dflash_synthetic_target")
+
+
 def dflash_get_status(model: Model, stream=None) -> int:
     st = ctypes.c_int32(0)
     check(lib().dflash_get_status(model.handle, _stream_ptr(stream), ctypes.byref(st)), "dflash_get_status")

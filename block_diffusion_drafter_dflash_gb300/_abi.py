@@ -61,6 +61,8 @@ SIGNATURES = {
     "dflash_inject_context_noalloc": (c_i32, [c_ptr, c_ptr, c_ptr, c_ptr, c_i32p, c_i32, c_ptr]),
     "dflash_verify_greedy": (c_i32, [c_ptr, c_ptr, c_i32, c_i32, c_ptr, c_ptr, c_ptr, c_ptr]),
     "dflash_launch_count": (ctypes.c_uint64, []),
+    "dflash_synthetic_target": (c_i32, [c_ptr, c_ptr, c_ptr, c_ptr, c_i32, c_ptr, c_ptr, c_ptr, c_i32, c_i32, c_i32,
+                                        c_ptr, c_ptr]),
     "dflash_trace_read": (c_i32, [c_ptr, ctypes.POINTER(ctypes.c_uint64), c_size]),
     "dflash_profile_start": (c_i32, [c_ptr, c_i32]),
     "dflash_profile_stop": (c_i32, [c_ptr, c_ptr, ctypes.POINTER(ctypes.c_float), c_i32p, c_i32]),

@@ -141,8 +141,8 @@ int32_t check_device(const dflash_model* m) {
 // ---------------------------------------------------------------- workspace plan
 struct WsPlan {
   size_t total;
-  size_t rowinfo, yf, ht;                                      // injection
-  size_t x, u, q, kb, vb, opart, ml, o, a, hm, slots;          // drafter
+  size_t rowinfo, yf, ht, rope_c;                              // injection
+  size_t x, u, q, kb, vb, opart, ml, o, a, hm, slots, rope_q;  // drafter
   size_t partial, counters;                                    // split-K scratch
   int counters_n;
   int attn_splits, attn_chunk;
@@ -186,6 +186,7 @@ WsPlan plan_ws(const dflash_model* m, int B, int cap, int block, int max_rows) {
     p.rowinfo = take(sizeof(int2) * (size_t)max_rows);
     p.yf = take(sizeof(float) * (size_t)max_rows * D);
     p.ht = take(ea * (size_t)max_rows * D);
+    p.rope_c = take(sizeof(float2) * (size_t)max_rows * (c.head_dim / 2));
   }
   if (block > 0) {
     // attention splits: enough CTAs to cover the device twice over
@@ -207,6 +208,7 @@ WsPlan plan_ws(const dflash_model* m, int B, int cap, int block, int max_rows) {
     p.a = take(ea * (size_t)R * F);
     p.hm = take(ea * (size_t)std::max(Rm, 1) * D);
     p.slots = take(sizeof(unsigned long long) * (size_t)std::max(Rm, 1));
+    p.rope_q = take(sizeof(float2) * (size_t)R * (c.head_dim / 2));
   }
   p.partial = take(sizeof(float) * partial);
   p.counters = take(sizeof(int) * (size_t)counters);
@@ -269,7 +271,8 @@ int32_t run_inject(const dflash_model* m, dflash_cache* cache, const void* feats
   DF_LAUNCH(DFLASH_STAGE_FUSE, 1, (gemm_launch<T, EpiStoreF32>(pf, P.g_fuse, EpiStoreF32{yf, D}, s)), "fusion GEMM");
   DF_LAUNCH(DFLASH_STAGE_OTHER, 1,
             fuse_norm_launch<T>(yf, static_cast<const T*>(m->g_c), c.rms_eps, rowinfo, max_rows, D, ht,
-                                (size_t)max_rows * D, s),
+                                (size_t)max_rows * D, m->inv_freq_dev, c.head_dim,
+                                reinterpret_cast<float2*>(ws + P.rope_c), s),
             "fusion norm");
 
   GemmProblem pi = make_problem(m, ht, D, max_rows, D, pl, (size_t)max_rows * D);
@@ -279,7 +282,7 @@ int32_t run_inject(const dflash_model* m, dflash_cache* cache, const void* feats
   }
   apply_plan(pi, P.g_inject, partial, counters);
   EpiInject ei{reinterpret_cast<float*>(cache->base + cache->k_off), reinterpret_cast<float*>(cache->base + cache->v_off),
-               rowinfo, m->inv_freq_dev, c.layers, c.n_kv_heads, c.head_dim, cache->cap};
+               rowinfo, reinterpret_cast<const float2*>(ws + P.rope_c), c.layers, c.n_kv_heads, c.head_dim, cache->cap};
   DF_LAUNCH(DFLASH_STAGE_INJECT, 1, (gemm_launch<T, EpiInject>(pi, P.g_inject, ei, s)), "injection GEMM");
   return DFLASH_OK;
 }
@@ -307,8 +310,8 @@ int32_t run_draft(const dflash_model* m, const dflash_cache* cache, const int32_
 
   DF_LAUNCH(DFLASH_STAGE_OTHER, 1, embed_norm_launch<T>(static_cast<const T*>(m->embed), anchor, c.mask_token_id, c.vocab, B, block, D,
                                static_cast<const T*>(m->layers[0].g_in), c.rms_eps, x, u, (size_t)R * D, counters,
-                               P.counters_n,
-                               m->status_dev, s),
+                               P.counters_n, m->status_dev, ctx_len, m->inv_freq_dev, c.head_dim,
+                               reinterpret_cast<float2*>(ws + P.rope_q), s),
           "embedding");
   for (int l = 0; l < c.layers; ++l) {
     const dflash_layer_weights& L = m->layers[l];
@@ -317,7 +320,8 @@ int32_t run_draft(const dflash_model* m, const dflash_cache* cache, const int32_
     add_seg(pq, L.w_k, layer_map(l, kMapK), L.w_k, layer_map(l, kMapK), hk / kTileN, 0, 1);
     add_seg(pq, L.w_v, layer_map(l, kMapV), L.w_v, layer_map(l, kMapV), hk / kTileN, 0, 2);
     apply_plan(pq, P.g_qkv, partial, counters);
-    EpiQKV eq{q, kb, vb, ctx_len, m->inv_freq_dev, block, c.n_q_heads, c.n_kv_heads, c.head_dim};
+    EpiQKV eq{q, kb, vb, reinterpret_cast<const float2*>(ws + P.rope_q), block, c.n_q_heads, c.n_kv_heads,
+              c.head_dim};
     DF_LAUNCH(DFLASH_STAGE_QKV, 1, (gemm_launch<T, EpiQKV>(pq, P.g_qkv, eq, s)), "QKV GEMM");
 
     AttnParams ap{};
@@ -631,6 +635,24 @@ int32_t dflash_verify_greedy(const int32_t* draft_dev, const int32_t* target_arg
 }
 
 uint64_t dflash_launch_count(void) { return g_launch_count.load(); }
+
+int32_t dflash_synthetic_target(const int32_t* draft_dev, const uint8_t* match_dev, const int32_t* off_dev,
+                                const int32_t* bonus_dev, int32_t n_patterns, int64_t* pattern_idx_dev,
+                                const int32_t* tau_dev, int64_t* tau_sum_dev, int32_t batch, int32_t block_size,
+                                int32_t vocab, int32_t* target_dev, dflash_stream_t stream) {
+  if (batch < 0 || n_patterns <= 0 || vocab <= 0) return fail(DFLASH_ERR_INVALID_ARG, "bad synthetic target sizes");
+  if (block_size < 1 || block_size > kMaxBlock) return fail(DFLASH_ERR_SHAPE, "block_size %d outside [1, %d]", block_size, kMaxBlock);
+  if (batch == 0) return DFLASH_OK;
+  if ((block_size > 1 && (!draft_dev || !match_dev || !off_dev)) || !bonus_dev || !pattern_idx_dev || !target_dev)
+    return fail(DFLASH_ERR_INVALID_ARG, "a device pointer is NULL");
+  DF_CUDA(synthetic_target_launch(draft_dev, match_dev, off_dev, bonus_dev, n_patterns,
+                                  reinterpret_cast<long long*>(pattern_idx_dev), tau_dev,
+                                  reinterpret_cast<long long*>(tau_sum_dev), batch, block_size, vocab, target_dev,
+                                  (cudaStream_t)stream),
+          "synthetic target");
+  g_launch_count += 1;
+  return DFLASH_OK;
+}
 
 int32_t dflash_trace_read(const dflash_model* m, uint64_t* host, size_t n) {
   if (!m || !host) return fail(DFLASH_ERR_INVALID_ARG, "NULL argument");

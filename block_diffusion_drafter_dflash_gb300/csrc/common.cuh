@@ -160,6 +160,7 @@ struct GemmProblem {
   int total_tiles;
   int splits;          // split-K factor (1 = none)
   int kblocks_per_split;   // in units of 64 columns of K
+  int stages;          // shared-memory pipeline depth (tensor-core path)
   float* partial;      // [splits][M][total_tiles*128] when splits > 1
   int* counters;       // [token tiles][total_tiles], zero between launches
   const void* wmaps;   // device array of weight tensor maps (tensor-core path)

@@ -71,13 +71,20 @@ template <typename T>
 __global__ void __launch_bounds__(kRowThreads) embed_norm_kernel(const T* embed, const int32_t* anchor, int mask_id,
                                                                  int vocab, int block, int D, const T* g, float eps,
                                                                  float* x, T* u, size_t plane, int* zero_ptr,
-                                                                 int zero_n, int32_t* status) {
+                                                                 int zero_n, int32_t* status, const int32_t* ctx_len,
+                                                                 const double* inv_freq, int hd, float2* rope) {
   __shared__ float red[32];
   griddep_wait();
   griddep_trigger();
   const int row = blockIdx.x, b = row / block, k = row - b * block;
   if (zero_ptr)
     for (int i = row * blockDim.x + threadIdx.x; i < zero_n; i += gridDim.x * blockDim.x) zero_ptr[i] = 0;
+  const int pos = ctx_len[b] + k;
+  for (int i = threadIdx.x; i < (hd >> 1); i += blockDim.x) {
+    float sn, cs;
+    rope_sincos(pos, inv_freq, i, &sn, &cs);
+    rope[(size_t)row * (hd >> 1) + i] = make_float2(cs, sn);
+  }
   int tok = k == 0 ? anchor[b] : mask_id;
   if (tok < 0 || tok >= vocab) {  // an anchor outside the vocabulary: flag it, read row 0
     if (threadIdx.x == 0) report_status(status, DFLASH_ERR_INVALID_ARG);
@@ -122,11 +129,20 @@ __global__ void __launch_bounds__(kRowThreads) final_norm_kernel(const float* x,
 
 template <typename T>
 __global__ void __launch_bounds__(kRowThreads) fuse_norm_kernel(const float* y, const T* g, float eps,
-                                                                const int2* rowinfo, int D, T* ht, size_t plane) {
+                                                                const int2* rowinfo, int D, T* ht, size_t plane,
+                                                                const double* inv_freq, int hd, float2* rope) {
   __shared__ float red[32];
   griddep_wait();
   griddep_trigger();
   const int row = blockIdx.x;
+  {
+    const int pos = max(rowinfo[row].y, 0);
+    for (int i = threadIdx.x; i < (hd >> 1); i += blockDim.x) {
+      float sn, cs;
+      rope_sincos(pos, inv_freq, i, &sn, &cs);
+      rope[(size_t)row * (hd >> 1) + i] = make_float2(cs, sn);
+    }
+  }
   if (rowinfo[row].x < 0) {
     for (int i = threadIdx.x; i < (D >> 2); i += blockDim.x)
       put_act4(ht, plane, (size_t)row * D + 4 * i, make_float4(0.f, 0.f, 0.f, 0.f));
@@ -223,15 +239,61 @@ __global__ void verify_kernel(const int32_t* draft, const int32_t* target, int B
   }
 }
 
+// Synthetic target for benchmarks and tests (one CTA): pattern p = *pidx,
+// y[b][k] = match ? d : (d + 1 + off) mod V for k < g-1, y[b][g-1] = bonus;
+// adds the previous verification's accepted lengths to *tau_sum; advances p.
+__global__ void __launch_bounds__(1024) synthetic_target_kernel(const int32_t* draft, const uint8_t* match,
+                                                                const int32_t* off, const int32_t* bonus, int npat,
+                                                                long long* pidx, const int32_t* tau,
+                                                                long long* tau_sum, int B, int g, int V, int32_t* y) {
+  griddep_wait();
+  griddep_trigger();
+  __shared__ long long sp;
+  if (threadIdx.x == 0) sp = *pidx;
+  __syncthreads();
+  const long long p = sp;
+  const int nd = g - 1;
+  for (int e = threadIdx.x; e < B * g; e += blockDim.x) {
+    const int b = e / g, k = e - b * g;
+    int v;
+    if (k < nd) {
+      const size_t i = ((size_t)p * B + b) * nd + k;
+      const long long d = draft[(size_t)b * nd + k];
+      v = match[i] ? (int)d : (int)((d + 1 + off[i]) % V);
+    } else {
+      v = bonus[(size_t)p * B + b];
+    }
+    y[e] = v;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    if (tau && tau_sum) {
+      long long t = 0;
+      for (int b = 0; b < B; ++b) t += tau[b];
+      *tau_sum += t;
+    }
+    *pidx = (p + 1) % npat;
+  }
+}
+
 }  // namespace
+
+cudaError_t synthetic_target_launch(const int32_t* draft, const uint8_t* match, const int32_t* off,
+                                    const int32_t* bonus, int npat, long long* pidx, const int32_t* tau,
+                                    long long* tau_sum, int B, int g, int V, int32_t* y, cudaStream_t s) {
+  if (B == 0) return cudaSuccess;
+  return launch_pdl(synthetic_target_kernel, dim3(1), dim3(1024), 0, s, draft, match, off, bonus, npat, pidx, tau,
+                    tau_sum, B, g, V, y);
+}
 
 template <typename T>
 cudaError_t embed_norm_launch(const T* embed, const int32_t* anchor, int mask_id, int vocab, int B, int block, int D,
                               const T* g, float eps, float* x, T* u, size_t plane, int* zero_ptr, int zero_n,
-                              int32_t* status, cudaStream_t s) {
+                              int32_t* status, const int32_t* ctx_len, const double* inv_freq, int hd, float2* rope,
+                              cudaStream_t s) {
   if (B * block == 0) return cudaSuccess;
   return launch_pdl(embed_norm_kernel<T>, dim3(B * block), dim3(kRowThreads), 0, s, embed, anchor, mask_id, vocab, block,
-                    D, g, eps, x, u, plane, zero_ptr, zero_n, status);
+                    D, g, eps, x, u, plane, zero_ptr, zero_n, status, ctx_len, inv_freq, hd, rope);
 }
 
 template <typename T>
@@ -250,9 +312,10 @@ cudaError_t final_norm_launch(const float* x, const T* g, float eps, int B, int 
 
 template <typename T>
 cudaError_t fuse_norm_launch(const float* y, const T* g, float eps, const int2* rowinfo, int rows, int D, T* ht,
-                             size_t plane, cudaStream_t s) {
+                             size_t plane, const double* inv_freq, int hd, float2* rope, cudaStream_t s) {
   if (rows == 0) return cudaSuccess;
-  return launch_pdl(fuse_norm_kernel<T>, dim3(rows), dim3(kRowThreads), 0, s, y, g, eps, rowinfo, D, ht, plane);
+  return launch_pdl(fuse_norm_kernel<T>, dim3(rows), dim3(kRowThreads), 0, s, y, g, eps, rowinfo, D, ht, plane,
+                    inv_freq, hd, rope);
 }
 
 cudaError_t inject_prep_launch(const int32_t* n_new, int32_t* ctx_len, int B, int max_rows, int cap, int2* rowinfo,
@@ -276,12 +339,13 @@ cudaError_t verify_launch(const int32_t* draft, const int32_t* target, int B, in
 
 #define DFLASH_EW_INST(T)                                                                                        \
   template cudaError_t embed_norm_launch<T>(const T*, const int32_t*, int, int, int, int, int, const T*, float,     \
-                                            float*, T*, size_t, int*, int, int32_t*, cudaStream_t);               \
+                                            float*, T*, size_t, int*, int, int32_t*, const int32_t*,              \
+                                            const double*, int, float2*, cudaStream_t);                          \
   template cudaError_t rmsnorm_launch<T>(const float*, const T*, float, int, int, T*, size_t, cudaStream_t);      \
   template cudaError_t final_norm_launch<T>(const float*, const T*, float, int, int, int, T*, size_t,              \
                                             unsigned long long*, cudaStream_t);                                   \
   template cudaError_t fuse_norm_launch<T>(const float*, const T*, float, const int2*, int, int, T*, size_t,      \
-                                           cudaStream_t);
+                                           const double*, int, float2*, cudaStream_t);
 
 DFLASH_EW_INST(float)
 DFLASH_EW_INST(__nv_bfloat16)

@@ -67,64 +67,88 @@ struct EpiSwiGLU {
   }
 };
 
-// Rotate-half RoPE of feature n of a tile holding whole heads of size hd.
-__device__ __forceinline__ float rope_apply(const float* t, int ld, int m, int n, int d, int hd, int pos,
-                                           const double* inv_freq) {
-  const int half = hd >> 1;
-  const float v = t[n * ld + m];
-  const int i = d < half ? d : d - half;
-  const int pn = d < half ? n + half : n - half;
-  const float p = t[pn * ld + m];
-  float s, c;
-  rope_sincos(pos, inv_freq, i, &s, &c);
-  return d < half ? v * c - p * s : v * c + p * s;
-}
+// RoPE in the Q/K/V and injection epilogues is rotate-half: feature d < hd/2
+// pairs with d + hd/2 of the same head (both in the same 128-feature tile),
+// x' = x cos - x_partner sin for the first half, x cos + x_partner sin for the
+// second, with (cos, sin) of the row's position from a per-row table.
 
 // Block Q/K/V of one draft layer: tag 0 = Q, 1 = K, 2 = V.  Row = b*block + k
-// sits at position ctx_len[b] + k; Q and K get RoPE.  Outputs are fp32,
+// sits at position ctx_len[b] + k, whose RoPE (cos, sin) table rope[row][hd/2]
+// was filled by the embedding kernel; Q and K get RoPE.  Outputs are fp32,
 // head-major [b][head][k][hd].
 struct EpiQKV {
   float* q;
   float* kb;
   float* vb;
-  const int32_t* ctx_len;
-  const double* inv_freq;
+  const float2* rope;
   int block, nq, nkv, hd;
+  // thread n owns feature n of the tile; the RoPE entries of 8 rows are
+  // loaded before any store so that their loads overlap
   __device__ __forceinline__ void operator()(const float* t, int ld, int m0, int mc, int, const GemmSeg& sg,
                                              int tis) const {
     const int tag = sg.tag;
     float* dst = tag == 0 ? q : (tag == 1 ? kb : vb);
-    const int nh = tag == 0 ? nq : nkv;
-    for (int idx = threadIdx.x; idx < mc * kTileN; idx += blockDim.x) {
-      int m = idx / kTileN, n = idx % kTileN;
-      int row = m0 + m, b = row / block, k = row - b * block;
-      int feat = tis * kTileN + n, head = feat / hd, d = feat - head * hd;
-      float v = tag == 2 ? t[n * ld + m] : rope_apply(t, ld, m, n, d, hd, __ldg(ctx_len + b) + k, inv_freq);
-      dst[(((size_t)b * nh + head) * block + k) * hd + d] = v;
+    const int nh = tag == 0 ? nq : nkv, half = hd >> 1;
+    const int n = threadIdx.x & (kTileN - 1), step = blockDim.x / kTileN;
+    const int feat = tis * kTileN + n, head = feat / hd, d = feat - head * hd;
+    const int i = d < half ? d : d - half;
+    const int pn = d < half ? n + half : n - half;
+    for (int mb = threadIdx.x / kTileN; mb < mc; mb += 8 * step) {
+      float2 sc[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int m = mb + j * step;
+        sc[j] = (tag != 2 && m < mc) ? __ldg(rope + (size_t)(m0 + m) * half + i) : make_float2(1.f, 0.f);
+      }
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int m = mb + j * step;
+        if (m >= mc) break;
+        const int row = m0 + m, b = row / block, k = row - b * block;
+        const float v = t[n * ld + m], pv = t[pn * ld + m];
+        const float r = tag == 2 ? v : (d < half ? v * sc[j].x - pv * sc[j].y : v * sc[j].x + pv * sc[j].y);
+        dst[(((size_t)b * nh + head) * block + k) * hd + d] = r;
+      }
     }
   }
 };
 
 // Context K/V injection: tag = 2*layer + (0: K, 1: V).  rowinfo[row] =
-// (request, position) or (-1, -1) for padding rows.  Writes the cache
-// [b][layer][kvh][pos][hd] (fp32); K gets RoPE at its absolute position.
+// (request, position) or (-1, -1) for padding rows; rope[row][hd/2] = (cos,
+// sin) at that position.  Writes the cache [b][layer][kvh][pos][hd] (fp32);
+// K gets RoPE at its absolute position.
 struct EpiInject {
   float* kc;
   float* vc;
   const int2* rowinfo;
-  const double* inv_freq;
+  const float2* rope;
   int layers, nkv, hd, cap;
   __device__ __forceinline__ void operator()(const float* t, int ld, int m0, int mc, int, const GemmSeg& sg,
                                              int tis) const {
-    const int layer = sg.tag >> 1, is_v = sg.tag & 1;
+    const int layer = sg.tag >> 1, is_v = sg.tag & 1, half = hd >> 1;
     float* dst = is_v ? vc : kc;
-    for (int idx = threadIdx.x; idx < mc * kTileN; idx += blockDim.x) {
-      int m = idx / kTileN, n = idx % kTileN;
-      int2 ri = __ldg(rowinfo + m0 + m);
-      if (ri.x < 0) continue;
-      int feat = tis * kTileN + n, head = feat / hd, d = feat - head * hd;
-      float v = is_v ? t[n * ld + m] : rope_apply(t, ld, m, n, d, hd, ri.y, inv_freq);
-      dst[((((size_t)ri.x * layers + layer) * nkv + head) * cap + ri.y) * hd + d] = v;
+    const int n = threadIdx.x & (kTileN - 1), step = blockDim.x / kTileN;
+    const int feat = tis * kTileN + n, head = feat / hd, d = feat - head * hd;
+    const int i = d < half ? d : d - half;
+    const int pn = d < half ? n + half : n - half;
+    for (int mb = threadIdx.x / kTileN; mb < mc; mb += 8 * step) {
+      int2 ri[8];
+      float2 sc[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int m = mb + j * step;
+        ri[j] = m < mc ? __ldg(rowinfo + m0 + m) : make_int2(-1, -1);
+        sc[j] = (!is_v && m < mc) ? __ldg(rope + (size_t)(m0 + m) * half + i) : make_float2(1.f, 0.f);
+      }
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int m = mb + j * step;
+        if (m >= mc) break;
+        if (ri[j].x < 0) continue;
+        const float v = t[n * ld + m], pv = t[pn * ld + m];
+        const float r = is_v ? v : (d < half ? v * sc[j].x - pv * sc[j].y : v * sc[j].x + pv * sc[j].y);
+        dst[((((size_t)ri[j].x * layers + layer) * nkv + head) * cap + ri[j].y) * hd + d] = r;
+      }
     }
   }
 };

@@ -127,6 +127,7 @@ GemmPlan plan_gemm(int dtype, int M, int K, int tiles, int sms, int tc, int plan
 void apply_plan(GemmProblem& p, const GemmPlan& plan, float* partial, int* counters) {
   p.splits = plan.splits;
   p.kblocks_per_split = plan.kblocks_per_split;
+  p.stages = plan.stages;
   p.partial = partial;
   p.counters = counters;
 }

@@ -14,6 +14,8 @@ struct GemmPlan {
   int token_tiles;
   int splits;
   int kblocks_per_split;  // 64-column blocks of K per split
+  int stages;             // pipeline depth of the tensor-core kernel
+  size_t smem;            // dynamic shared memory per CTA
   size_t partial_floats;  // split-K scratch floats (0 if splits == 1)
   int counters;           // split-K tile counters (0 if splits == 1)
 };

@@ -19,6 +19,7 @@
 #include <cuda.h>
 
 #include <algorithm>
+#include <cstdlib>
 
 #include "gemm.cuh"
 #include "ptx.cuh"
@@ -27,21 +28,27 @@ namespace dflash {
 
 namespace {
 
+constexpr int kMaxStages = 12;
+constexpr int kBarBytes = 8 * (2 * kMaxStages + 1) + 16;
+constexpr size_t kSmemPerSM = 228 * 1024;     // shared memory of one SM
+constexpr size_t kSmemReservedPerCta = 1024;
+constexpr size_t kSmemMaxPerCta = 227 * 1024;  // opt-in limit of one CTA
+
 template <int BN, int PL>
 struct TcCfg {
   static constexpr int kN = BN * PL;                  // MMA N
-  static constexpr int kStages = kN <= 64 ? 5 : 4;
   static constexpr int kABytes = kTileN * 128;        // 128 rows x 64 bf16
   static constexpr int kBBytes = kN * 128;            // PL*BN rows x 64 bf16
   static constexpr int kStageBytes = kABytes + kBBytes;
   static constexpr int kTmemCols = kN <= 32 ? 32 : kN;
   static constexpr int kChunk = BN < 32 ? BN : 32;    // token columns per epilogue pass
-  static constexpr int kBarBytes = 256;
-  static constexpr int kSmem = 1024 + kStages * kStageBytes + kBarBytes;
   static_assert(kStageBytes % 1024 == 0, "stages must keep 1024-B alignment");
   static_assert(kN <= 256 && kN % 16 == 0, "MMA N must be a multiple of 16 up to 256");
-  static_assert(kTileN * (kChunk + 1) * 4 <= kStages * kStageBytes, "epilogue tile must fit the stages");
+  static_assert(kTileN * (kChunk + 1) * 4 <= kStageBytes, "epilogue tile must fit one stage");
+  static size_t smem(int stages) { return 1024 + (size_t)stages * kStageBytes + kBarBytes; }
 };
+
+size_t stage_bytes(int bm, int planes) { return kTileN * 128 + (size_t)bm * planes * 128; }
 
 // Accumulator columns c0..c0+CH-1 of this warp's lanes; with a hi/lo operand
 // pair the lo block (columns BN..2BN-1) is added.
@@ -67,9 +74,10 @@ __global__ void __launch_bounds__(128, 1) gemm_tc_kernel(const __grid_constant__
   using C = TcCfg<BN, PL>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kStages * C::kStageBytes);
-  uint64_t* empty = full + C::kStages;
-  uint64_t* accf = empty + C::kStages;
+  const int S = p.stages;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)S * C::kStageBytes);
+  uint64_t* empty = full + S;
+  uint64_t* accf = empty + S;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accf + 1);
   int* flags = reinterpret_cast<int*>(tmem_slot + 1);   // [0] abort, [1] last split, [2] loads issued
 
@@ -95,7 +103,7 @@ __global__ void __launch_bounds__(128, 1) gemm_tc_kernel(const __grid_constant__
   }
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < C::kStages; ++s) {
+    for (int s = 0; s < S; ++s) {
       ptx::mbar_init(full + s, 1);
       ptx::mbar_init(empty + s, 1);
     }
@@ -124,19 +132,19 @@ __global__ void __launch_bounds__(128, 1) gemm_tc_kernel(const __grid_constant__
     const int r0 = half_first_row(sg, tis, 0), r1 = half_first_row(sg, tis, 1);
     const int prow = static_cast<int>(p.plane_stride / p.ldx);
     auto load_w = [&](int i) {
-      uint8_t* a = smem + (i % C::kStages) * C::kStageBytes;
+      uint8_t* a = smem + (i % S) * C::kStageBytes;
       const int kx = (kb0 + i) * 64;
-      ptx::tma_load_2d(a, map0, full + i % C::kStages, kx, r0, pol_w);
-      ptx::tma_load_2d(a + kHalfN * 128, map1, full + i % C::kStages, kx, r1, pol_w);
+      ptx::tma_load_2d(a, map0, full + i % S, kx, r0, pol_w);
+      ptx::tma_load_2d(a + kHalfN * 128, map1, full + i % S, kx, r1, pol_w);
     };
     auto load_x = [&](int i) {
-      uint8_t* b = smem + (i % C::kStages) * C::kStageBytes + C::kABytes;
+      uint8_t* b = smem + (i % S) * C::kStageBytes + C::kABytes;
       const int kx = (kb0 + i) * 64;
 #pragma unroll
       for (int pl = 0; pl < PL; ++pl)
-        ptx::tma_load_2d(b + pl * BN * 128, &xmap, full + i % C::kStages, kx, pl * prow + m0, pol_x);
+        ptx::tma_load_2d(b + pl * BN * 128, &xmap, full + i % S, kx, pl * prow + m0, pol_x);
     };
-    const int pre = min(nk, C::kStages);
+    const int pre = min(nk, S);
     for (int i = 0; i < pre; ++i) {
       ptx::mbar_arrive_expect_tx(full + i, C::kStageBytes);
       load_w(i);
@@ -145,8 +153,8 @@ __global__ void __launch_bounds__(128, 1) gemm_tc_kernel(const __grid_constant__
     for (int i = 0; i < pre; ++i) load_x(i);
     int issued = pre;
     for (int i = pre; i < nk; ++i) {
-      const int s = i % C::kStages;
-      if (!ptx::mbar_wait(empty + s, ((i / C::kStages) & 1) ^ 1, kWaitBudget, status)) {
+      const int s = i % S;
+      if (!ptx::mbar_wait(empty + s, ((i / S) & 1) ^ 1, kWaitBudget, status)) {
         flags[0] = 1;
         break;
       }
@@ -160,8 +168,8 @@ __global__ void __launch_bounds__(128, 1) gemm_tc_kernel(const __grid_constant__
     // ---- MMA issuer
     constexpr uint32_t idesc = ptx::idesc_bf16_f32(kTileN, C::kN);
     for (int i = 0; i < nk; ++i) {
-      const int s = i % C::kStages;
-      if (!ptx::mbar_wait(full + s, (i / C::kStages) & 1, kWaitBudget, status)) {
+      const int s = i % S;
+      if (!ptx::mbar_wait(full + s, (i / S) & 1, kWaitBudget, status)) {
         flags[0] = 1;
         break;
       }
@@ -286,8 +294,8 @@ __global__ void __launch_bounds__(128, 1) gemm_tc_kernel(const __grid_constant__
   } else if (threadIdx.x == 0) {
     // a wait ran out: let every load this CTA issued land before the CTA exits
     const int issued = flags[2];
-    for (int i = max(0, issued - C::kStages); i < issued; ++i)
-      ptx::mbar_wait(full + (i % C::kStages), (i / C::kStages) & 1, kWaitBudget, status);
+    for (int i = max(0, issued - S); i < issued; ++i)
+      ptx::mbar_wait(full + (i % S), (i / S) & 1, kWaitBudget, status);
   }
 
   ptx::tc_fence_before();
@@ -325,18 +333,19 @@ cudaError_t launch_bn(const GemmProblem& p, const GemmPlan& plan, const Epi& epi
   using C = TcCfg<BN, PL>;
   static bool attr_set = false;   // per instantiation; the attribute is per device function
   if (!attr_set) {
-    cudaError_t e =
-        cudaFuncSetAttribute(gemm_tc_kernel<BN, PL, Epi>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+    cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<BN, PL, Epi>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)std::min(C::smem(kMaxStages), kSmemMaxPerCta));
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
+  if (p.stages < 1 || p.stages > kMaxStages || C::smem(p.stages) != plan.smem) return cudaErrorInvalidValue;
   if (p.planes != PL || p.plane_stride % p.ldx) return cudaErrorInvalidValue;
   // one map over both planes: plane 1 starts plane_stride/ldx rows after plane 0
   const int rows = PL == 1 ? p.M : static_cast<int>(p.plane_stride / p.ldx) + p.M;
   CUtensorMap xmap;
   if (!encode_activation_map(&xmap, p.x, p.K, rows, p.ldx, BN)) return cudaErrorInvalidValue;
   dim3 grid(p.total_tiles, plan.splits, plan.token_tiles);
-  return launch_pdl(gemm_tc_kernel<BN, PL, Epi>, grid, dim3(128), C::kSmem, s, xmap, p, epi, p.status);
+  return launch_pdl(gemm_tc_kernel<BN, PL, Epi>, grid, dim3(128), C::smem(p.stages), s, xmap, p, epi, p.status);
 }
 
 }  // namespace
@@ -367,7 +376,18 @@ bool encode_activation_map(void* map, const void* base, int inner, int rows, int
 
 size_t tensor_map_bytes() { return sizeof(CUtensorMap); }
 
+// Tuning knobs (environment, read once): DFLASH_TC_STAGES pipeline depth,
+// DFLASH_TC_WAVES target CTAs as a multiple of the resident slots,
+// DFLASH_TC_KMIN fewest 64-column K blocks per split.
+int env_int(const char* name, int dflt) {
+  const char* v = getenv(name);
+  return v ? atoi(v) : dflt;
+}
+
 GemmPlan plan_gemm_tc(int M, int K, int tiles, int sms, int planes) {
+  static const int env_stages = env_int("DFLASH_TC_STAGES", 0);
+  static const int env_waves = env_int("DFLASH_TC_WAVES", 1);
+  static const int env_kmin = env_int("DFLASH_TC_KMIN", 4);
   GemmPlan g{};
   g.tc = 1;
   g.planes = planes;
@@ -375,11 +395,18 @@ GemmPlan plan_gemm_tc(int M, int K, int tiles, int sms, int planes) {
   g.bm = M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : M <= 128 ? 128 : 256;
   g.bm = std::min(g.bm, bm_max);
   g.token_tiles = (M + g.bm - 1) / g.bm;
-  const int cps = g.bm * planes <= 32 ? 2 : 1;   // CTAs resident per SM (shared-memory bound)
+  const int n = g.bm * planes;
+  // deep rings for the weight-streaming shapes (one CTA per SM with ~112 KB of
+  // weights in flight measured best at batch 1), four stages for wide tiles
+  g.stages = env_stages > 0 ? std::min(env_stages, kMaxStages) : (n <= 64 ? 7 : 4);
+  const size_t sb = stage_bytes(g.bm, planes);
+  g.stages = std::min<int>(g.stages, (int)((kSmemMaxPerCta - 1024 - kBarBytes) / sb));
+  g.smem = 1024 + (size_t)g.stages * sb + kBarBytes;
+  const int cps = std::max<int>(1, (int)(kSmemPerSM / (g.smem + kSmemReservedPerCta)));   // CTAs per SM
   const int kblocks = K / 64;
   const long ctas = (long)tiles * g.token_tiles;
-  int splits = (int)std::max(1L, (long)sms * cps / ctas);
-  splits = std::min(splits, std::max(1, kblocks / 4));
+  int splits = (int)std::max(1L, (long)sms * cps * std::max(1, env_waves) / ctas);
+  splits = std::min(splits, std::max(1, kblocks / std::max(1, env_kmin)));
   g.kblocks_per_split = (kblocks + splits - 1) / splits;
   g.splits = (kblocks + g.kblocks_per_split - 1) / g.kblocks_per_split;
   g.partial_floats = g.splits > 1 ? (size_t)g.splits * M * tiles * kTileN : 0;

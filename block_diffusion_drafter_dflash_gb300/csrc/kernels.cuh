@@ -37,10 +37,12 @@ int attention_max_rows();   // largest (nq/nkv)*block the kernel accepts
 // An anchor outside [0, vocab) sets DFLASH_ERR_INVALID_ARG in `status`.
 // Outputs written as GEMM activation operands (`plane` = elements between the
 // hi and lo planes of a bf16 model; unused for fp32).
+// Also fills rope[row][hd/2] = (cos, sin) of position ctx_len[b] + k.
 template <typename T>
 cudaError_t embed_norm_launch(const T* embed, const int32_t* anchor, int mask_id, int vocab, int B, int block, int D,
                               const T* g, float eps, float* x, T* u, size_t plane, int* zero_ptr, int zero_n,
-                              int32_t* status, cudaStream_t s);
+                              int32_t* status, const int32_t* ctx_len, const double* inv_freq, int hd, float2* rope,
+                              cudaStream_t s);
 
 // u[row] = RMSNorm(x[row]) * g for `rows` rows.
 template <typename T>
@@ -52,10 +54,11 @@ template <typename T>
 cudaError_t final_norm_launch(const float* x, const T* g, float eps, int B, int block, int D, T* hm, size_t plane,
                               unsigned long long* slots, cudaStream_t s);
 
-// H_t[row] = RMSNorm(y[row]) * g_c for rows with rowinfo[row].x >= 0, 0 otherwise.
+// H_t[row] = RMSNorm(y[row]) * g_c for rows with rowinfo[row].x >= 0, 0 otherwise;
+// rope[row][hd/2] = (cos, sin) of the row's position.
 template <typename T>
 cudaError_t fuse_norm_launch(const float* y, const T* g, float eps, const int2* rowinfo, int rows, int D, T* ht,
-                             size_t plane, cudaStream_t s);
+                             size_t plane, const double* inv_freq, int hd, float2* rope, cudaStream_t s);
 
 // Row -> (request, position) map of an injection and the ctx_len update.
 cudaError_t inject_prep_launch(const int32_t* n_new, int32_t* ctx_len, int B, int max_rows, int cap,
@@ -63,6 +66,11 @@ cudaError_t inject_prep_launch(const int32_t* n_new, int32_t* ctx_len, int B, in
 
 // drafts[row] = index packed in slots[row].
 cudaError_t argmax_finalize_launch(const unsigned long long* slots, int rows, int32_t* drafts, cudaStream_t s);
+
+// Synthetic target of the benchmark (see dflash_synthetic_target).
+cudaError_t synthetic_target_launch(const int32_t* draft, const uint8_t* match, const int32_t* off,
+                                    const int32_t* bonus, int npat, long long* pidx, const int32_t* tau,
+                                    long long* tau_sum, int B, int g, int V, int32_t* y, cudaStream_t s);
 
 // Greedy verification, one warp per request.
 cudaError_t verify_launch(const int32_t* draft, const int32_t* target, int B, int block, int32_t* accept_len,

@@ -239,6 +239,23 @@ int32_t dflash_verify_greedy(const int32_t* draft_dev, const int32_t* target_arg
                              int32_t block_size, int32_t* accept_len_dev, int32_t* out_tokens_dev,
                              int32_t* next_anchor_dev, dflash_stream_t stream);
 
+/* --- benchmark utility (not part of the method) --------------------------------
+ * The synthetic target the benchmark and tests put between dflash_draft_block
+ * and dflash_verify_greedy in place of a real target model, as one kernel.
+ * With p = *pattern_idx_dev (int64, device), for every request b:
+ *   target[b][k] = draft[b][k]                        if match[p][b][k] != 0
+ *                = (draft[b][k] + 1 + off[p][b][k]) % vocab   otherwise  (k < block-1)
+ *   target[b][block-1] = bonus[p][b]
+ * then *pattern_idx_dev = (p + 1) % n_patterns, and, when tau_dev and
+ * tau_sum_dev are given, *tau_sum_dev += sum_b tau_dev[b] (the accepted
+ * lengths of the previous verification).  match: uint8 [n_patterns][batch][block-1],
+ * off: int32 [n_patterns][batch][block-1], bonus: int32 [n_patterns][batch],
+ * target: int32 [batch][block]. */
+int32_t dflash_synthetic_target(const int32_t* draft_dev, const uint8_t* match_dev, const int32_t* off_dev,
+                                const int32_t* bonus_dev, int32_t n_patterns, int64_t* pattern_idx_dev,
+                                const int32_t* tau_dev, int64_t* tau_sum_dev, int32_t batch, int32_t block_size,
+                                int32_t vocab, int32_t* target_dev, dflash_stream_t stream);
+
 /* --- tracing -------------------------------------------------------------------
  * Kernel launches made by this library in this process (every entry point,
  * every device), for launch accounting. */

@@ -70,3 +70,28 @@ def test_expected_accept_length_monte_carlo_on_kernel(block, p):
     expect = oracle.expected_accept_len([p] * (block - 1))
     assert abs(tau.mean() - expect) < 4 * tau.std() / math.sqrt(N), (tau.mean(), expect)
     assert tau.min() >= 1 and tau.max() <= block
+
+
+@pytest.mark.parametrize("block,B", [(16, 32), (4, 3), (1, 5), (32, 7)])
+def test_synthetic_target_kernel_matches_the_input_recipe(block, B):
+    """The benchmark's one-kernel synthetic target equals dflash_inputs'
+    torch recipe for every stacked pattern, and advances its counters."""
+    import block_diffusion_drafter_dflash_gb300 as df
+    cfg = replace(TINY, vocab=151936)
+    P = 3
+    pats = [make_agreement(cfg, B, block, [0.7] * B, seed=50 + i, device="cuda") for i in range(P)]
+    match = torch.stack([p.match for p in pats]).contiguous()
+    off = torch.stack([p.off for p in pats]).contiguous()
+    bonus = torch.stack([p.bonus for p in pats]).contiguous()
+    d = make_tokens(cfg, B * (block - 1), seed=60, device="cuda").reshape(B, block - 1).contiguous()
+    pidx = torch.zeros(1, dtype=torch.long, device="cuda")
+    tau = torch.arange(1, B + 1, dtype=torch.int32, device="cuda")
+    tau_sum = torch.zeros(1, dtype=torch.long, device="cuda")
+    y = torch.empty((B, block), dtype=torch.int32, device="cuda")
+    for i in range(P + 1):
+        df.dflash_synthetic_target(d, match, off, bonus, pidx, y, cfg.vocab, tau=tau, tau_sum=tau_sum)
+        ref = synthetic_target_argmax(d, pats[i % P], cfg.vocab)
+        assert torch.equal(y, ref), i
+    torch.cuda.synchronize()
+    assert int(pidx.item()) == (P + 1) % P
+    assert int(tau_sum.item()) == (P + 1) * B * (B + 1) // 2
