@@ -153,6 +153,37 @@ def gemm_bytes_per_cycle(cfg, B: int, block: int, inject_rows: int) -> dict:
     }
 
 
+# ---------------------------------------------------------------- measured DRAM traffic
+TRAFFIC_PROFILE = os.path.join(ROOT, "profiles", "gemm_traffic_8b_bs1.md")
+GEMM_SOURCES = ["gemm_tc.cu", "epilogue.cuh", "common.cuh", "ptx.cuh"]
+
+
+def gemm_source_sha1() -> str:
+    import hashlib
+    h = hashlib.sha1()
+    for name in GEMM_SOURCES:
+        with open(os.path.join(ROOT, "block_diffusion_drafter_dflash_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def gemm_traffic_per_cycle(workload: str):
+    """DRAM bytes (read + write) of one cycle's projection GEMMs from the
+    committed ncu summary, or None when it was taken on other GEMM sources
+    or another workload."""
+    try:
+        text = open(TRAFFIC_PROFILE).read()
+    except OSError:
+        return None
+    vals = dict(line.split(":", 1) for line in text.splitlines() if ":" in line and line[:1].isalpha())
+    try:
+        if vals.get("workload", "").strip() != workload or vals.get("source_sha1", "").strip() != gemm_source_sha1():
+            return None
+        return int(vals["traffic_bytes_per_cycle"].strip())
+    except (KeyError, ValueError):
+        return None
+
+
 # ---------------------------------------------------------------- the GPU arm
 class Cycle:
     """Device-resident draft cycle of one workload through the C ABI.
@@ -279,7 +310,7 @@ def run_gpu(args, rank, world, local):
     hbm, bf16, src = load_peaks()
     achieved = gemm_bytes / (gemm_ms / 1e3) / 1e9
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
-                "frac": round(achieved / hbm, 4), "traffic": None,
+                "frac": round(achieved / hbm, 4), "traffic": gemm_traffic_per_cycle(wl.name),
                 "kernel": "projection GEMMs (all launches of one cycle)", "peak_source": src,
                 "algorithmic_bytes_per_cycle": gemm_bytes, "kernel_ms_per_cycle": round(gemm_ms, 4)}
     stages = {s: {"ms_per_cycle": round(v[0] / KP, 4), "launches_per_cycle": v[1] / KP} for s, v in prof.items()}

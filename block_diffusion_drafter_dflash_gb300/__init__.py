@@ -108,11 +108,15 @@ class Cache:
     def _kv_view(self, off: int) -> torch.Tensor:
         c = self.model.cfg
         n = self.batch * c.layers * c.n_kv_heads * self.capacity * c.head_dim
-        return self.buffer[off:off + n * 4].view(torch.float32).view(
-            self.batch, c.layers, c.n_kv_heads, self.capacity, c.head_dim)
+        raw = self.buffer[off:off + n * 4]
+        if self.model.dtype == torch.float32:
+            return raw.view(torch.float32).view(self.batch, c.layers, c.n_kv_heads, self.capacity, c.head_dim)
+        planes = raw.view(torch.bfloat16).view(self.batch, c.layers, c.n_kv_heads, 2, self.capacity, c.head_dim)
+        return planes[:, :, :, 0].float() + planes[:, :, :, 1].float()
 
     def k(self) -> torch.Tensor:
-        """View [batch][layers][n_kv_heads][capacity][head_dim] of the context keys."""
+        """Context keys as fp32 [batch][layers][n_kv_heads][capacity][head_dim]
+        (a view for fp32 models; hi + lo of the two bf16 planes otherwise)."""
         return self._kv_view(self.k_off)
 
     def v(self) -> torch.Tensor:

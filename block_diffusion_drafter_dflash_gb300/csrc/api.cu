@@ -202,8 +202,10 @@ WsPlan plan_ws(const dflash_model* m, int B, int cap, int block, int max_rows) {
     p.q = take(sizeof(float) * (size_t)R * hq);
     p.kb = take(sizeof(float) * (size_t)R * hk);
     p.vb = take(sizeof(float) * (size_t)R * hk);
-    p.opart = take(sizeof(float) * (size_t)B * c.n_q_heads * block * p.attn_splits * c.head_dim);
-    p.ml = take(sizeof(float2) * (size_t)B * c.n_q_heads * block * p.attn_splits);
+    // split partials of the CUDA-core attention (fp32 models); bf16 models merge in shared memory
+    const size_t nsplit = c.dtype == DFLASH_DTYPE_F32 ? (size_t)p.attn_splits : 0;
+    p.opart = take(sizeof(float) * (size_t)B * c.n_q_heads * block * nsplit * c.head_dim);
+    p.ml = take(sizeof(float2) * (size_t)B * c.n_q_heads * block * nsplit);
     p.o = take(ea * (size_t)R * hq);
     p.a = take(ea * (size_t)R * F);
     p.hm = take(ea * (size_t)std::max(Rm, 1) * D);
@@ -281,9 +283,10 @@ int32_t run_inject(const dflash_model* m, dflash_cache* cache, const void* feats
     add_seg(pi, m->layers[l].w_v, layer_map(l, kMapV), m->layers[l].w_v, layer_map(l, kMapV), hk / kTileN, 0, 2 * l + 1);
   }
   apply_plan(pi, P.g_inject, partial, counters);
-  EpiInject ei{reinterpret_cast<float*>(cache->base + cache->k_off), reinterpret_cast<float*>(cache->base + cache->v_off),
-               rowinfo, reinterpret_cast<const float2*>(ws + P.rope_c), c.layers, c.n_kv_heads, c.head_dim, cache->cap};
-  DF_LAUNCH(DFLASH_STAGE_INJECT, 1, (gemm_launch<T, EpiInject>(pi, P.g_inject, ei, s)), "injection GEMM");
+  EpiInject<T> ei{reinterpret_cast<T*>(cache->base + cache->k_off), reinterpret_cast<T*>(cache->base + cache->v_off),
+                  rowinfo, reinterpret_cast<const float2*>(ws + P.rope_c), c.layers, c.n_kv_heads, c.head_dim,
+                  cache->cap};
+  DF_LAUNCH(DFLASH_STAGE_INJECT, 1, (gemm_launch<T, EpiInject<T>>(pi, P.g_inject, ei, s)), "injection GEMM");
   return DFLASH_OK;
 }
 
@@ -298,8 +301,8 @@ int32_t run_draft(const dflash_model* m, const dflash_cache* cache, const int32_
   float* x = reinterpret_cast<float*>(ws + P.x);
   T* u = reinterpret_cast<T*>(ws + P.u);
   float* q = reinterpret_cast<float*>(ws + P.q);
-  float* kb = reinterpret_cast<float*>(ws + P.kb);
-  float* vb = reinterpret_cast<float*>(ws + P.vb);
+  T* kb = reinterpret_cast<T*>(ws + P.kb);
+  T* vb = reinterpret_cast<T*>(ws + P.vb);
   T* o = reinterpret_cast<T*>(ws + P.o);
   T* a = reinterpret_cast<T*>(ws + P.a);
   T* hm = reinterpret_cast<T*>(ws + P.hm);
@@ -320,14 +323,14 @@ int32_t run_draft(const dflash_model* m, const dflash_cache* cache, const int32_
     add_seg(pq, L.w_k, layer_map(l, kMapK), L.w_k, layer_map(l, kMapK), hk / kTileN, 0, 1);
     add_seg(pq, L.w_v, layer_map(l, kMapV), L.w_v, layer_map(l, kMapV), hk / kTileN, 0, 2);
     apply_plan(pq, P.g_qkv, partial, counters);
-    EpiQKV eq{q, kb, vb, reinterpret_cast<const float2*>(ws + P.rope_q), block, c.n_q_heads, c.n_kv_heads,
-              c.head_dim};
-    DF_LAUNCH(DFLASH_STAGE_QKV, 1, (gemm_launch<T, EpiQKV>(pq, P.g_qkv, eq, s)), "QKV GEMM");
+    EpiQKV<T> eq{q, kb, vb, reinterpret_cast<const float2*>(ws + P.rope_q), block, c.n_q_heads, c.n_kv_heads,
+                 c.head_dim};
+    DF_LAUNCH(DFLASH_STAGE_QKV, 1, (gemm_launch<T, EpiQKV<T>>(pq, P.g_qkv, eq, s)), "QKV GEMM");
 
     AttnParams ap{};
     ap.q = q; ap.kb = kb; ap.vb = vb;
-    ap.kc = reinterpret_cast<const float*>(cache->base + cache->k_off);
-    ap.vc = reinterpret_cast<const float*>(cache->base + cache->v_off);
+    ap.kc = cache->base + cache->k_off;
+    ap.vc = cache->base + cache->v_off;
     ap.ctx_len = ctx_len;
     ap.layer = l; ap.layers = c.layers; ap.cap = cache->cap;
     ap.B = B; ap.nq = c.n_q_heads; ap.nkv = c.n_kv_heads; ap.hd = c.head_dim; ap.block = block;
@@ -337,7 +340,7 @@ int32_t run_draft(const dflash_model* m, const dflash_cache* cache, const int32_
     ap.out = o;
     ap.out_plane = (size_t)R * hq;
     ap.scale = 1.0f / sqrtf((float)c.head_dim);
-    DF_LAUNCH(DFLASH_STAGE_ATTN, 2, attention_launch<T>(ap, s), "attention");
+    DF_LAUNCH(DFLASH_STAGE_ATTN, (c.dtype == DFLASH_DTYPE_F32 ? 2 : 1), attention_launch<T>(ap, s), "attention");
 
     GemmProblem po = make_problem(m, o, hq, R, hq, pl, (size_t)R * hq);
     add_seg(po, L.w_o, layer_map(l, kMapO), L.w_o, layer_map(l, kMapO), D / kTileN, 0, 0);

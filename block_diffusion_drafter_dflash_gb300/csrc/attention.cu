@@ -14,9 +14,9 @@
 
 namespace dflash {
 
-// tensor-core split kernel for bf16 models (attention_mma.cu)
+// tensor-core cluster kernel for bf16 models (attention_mma.cu)
 cudaError_t attention_mma_prepare(int hd);
-cudaError_t attention_mma_split_launch(const AttnParams& p, cudaStream_t s);
+cudaError_t attention_mma_launch(const AttnParams& p, cudaStream_t s);
 
 namespace {
 
@@ -64,10 +64,10 @@ __global__ void __launch_bounds__(kAttnThreads) attn_split_kernel(const __grid_c
     Ls[r] = 0.f;
   }
 
-  const float* kc = p.kc + (((size_t)b * p.layers + p.layer) * p.nkv + kvh) * p.cap * hd;
-  const float* vc = p.vc + (((size_t)b * p.layers + p.layer) * p.nkv + kvh) * p.cap * hd;
-  const float* kb = p.kb + ((size_t)b * p.nkv + kvh) * p.block * hd;
-  const float* vb = p.vb + ((size_t)b * p.nkv + kvh) * p.block * hd;
+  const float* kc = static_cast<const float*>(p.kc) + (((size_t)b * p.layers + p.layer) * p.nkv + kvh) * p.cap * hd;
+  const float* vc = static_cast<const float*>(p.vc) + (((size_t)b * p.layers + p.layer) * p.nkv + kvh) * p.cap * hd;
+  const float* kb = static_cast<const float*>(p.kb) + ((size_t)b * p.nkv + kvh) * p.block * hd;
+  const float* vb = static_cast<const float*>(p.vb) + ((size_t)b * p.nkv + kvh) * p.block * hd;
 
   for (int jt = j0; jt < j1; jt += kKeyTile) {
     const int n = min(kKeyTile, j1 - jt);
@@ -191,14 +191,12 @@ cudaError_t attention_prepare(int rows, int hd) {
 template <typename T>
 cudaError_t attention_launch(const AttnParams& p, cudaStream_t s) {
   if (p.B <= 0) return cudaSuccess;
-  cudaError_t e;
   if constexpr (std::is_same<T, __nv_bfloat16>::value) {
-    e = attention_mma_split_launch(p, s);
-  } else {
-    const int rows = (p.nq / p.nkv) * p.block;
-    e = launch_pdl(attn_split_kernel<T>, dim3(p.splits, p.nkv, p.B), dim3(kAttnThreads), attn_smem_bytes(rows, p.hd),
-                   s, p);
+    return attention_mma_launch(p, s);   // one launch: the cluster merges its own splits
   }
+  const int rows = (p.nq / p.nkv) * p.block;
+  cudaError_t e = launch_pdl(attn_split_kernel<T>, dim3(p.splits, p.nkv, p.B), dim3(kAttnThreads),
+                             attn_smem_bytes(rows, p.hd), s, p);
   if (e != cudaSuccess) return e;
   return launch_pdl(attn_combine_kernel<T>, dim3(p.B * p.nq * p.block), dim3(128), (p.splits + 8) * sizeof(float), s,
                     p);

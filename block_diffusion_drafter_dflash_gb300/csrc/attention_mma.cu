@@ -1,35 +1,44 @@
 // Tensor-core block attention for bf16 drafters, at fp32-level precision.
 //
-// Same work split as the CUDA-core kernel (one CTA per request, kv head and
-// key split; one warp per 16 query rows of the kv head's group), but the two
-// products run on mma.sync m16n8k16 with each fp32 operand carried as a
-// bf16 pair x = hi + lo:
+// One thread-block cluster of kCluster CTAs per (request, kv head).  The
+// request's keys — its context K/V followed by the block's own K/V — are cut
+// into kCluster contiguous chunks, one per CTA; every CTA runs the whole
+// query group (the nq/nkv heads times the block rows, one warp per 16 rows)
+// over its chunk with an online softmax, then the cluster merges the
+// partial (max, sum, output) rows through distributed shared memory: CTA r
+// finalises rows r, r+kCluster, ...  No global scratch, no second kernel,
+// and the chunking adapts to each request's own context length.
+//
+// K and V are stored as two bf16 planes, x = hi + lo (context cache and block
+// alike), so both products run on mma.sync m16n8k16 as three bf16 products:
 //     S = Q K^T ~ Qhi Khi^T + Qhi Klo^T + Qlo Khi^T
 //     O = P V   ~ Phi Vhi  + Phi Vlo  + Plo Vhi
-// (the dropped lo*lo term is ~2^-16 relative).  K and V tiles of 32 keys are
-// staged as fp32 with cp.async (double buffer), split into hi/lo bf16 tiles
-// in shared memory (XOR-swizzled 16-byte chunks so ldmatrix is conflict
-// free), and consumed with ldmatrix / ldmatrix.trans.  Softmax is online in
-// the log2 domain (Q is pre-scaled by log2(e)/sqrt(hd)); partial (o, m, l)
-// per split are merged by attn_combine_kernel.
+// (the dropped lo*lo term is ~2^-16 relative).  Tiles of 32 keys of the four
+// planes stream through a kStages-deep cp.async ring straight into
+// XOR-swizzled shared memory (16-byte chunks; ldmatrix conflict free).
+// Softmax runs in the log2 domain (Q is pre-scaled by log2(e)/sqrt(hd)).
+#include <cooperative_groups.h>
+
 #include <cfloat>
+#include <cstdlib>
 
 #include "kernels.cuh"
 
 namespace dflash {
 
+namespace cg = cooperative_groups;
+
 namespace {
 
-constexpr int kKeys = 32;              // keys per tile
+constexpr int kKeys = 32;       // keys per tile
+constexpr int kStages = 3;      // cp.async ring depth
 constexpr float kLog2e = 1.4426950408889634f;
-constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kNegBig = -1.0e30f;
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
-// pack two floats into a bf16x2 register (low half = first)
 __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
   __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
   return *reinterpret_cast<uint32_t*>(&v);
@@ -61,13 +70,15 @@ __device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t* r) {
                : "r"(addr));
 }
 
-__device__ __forceinline__ void cp_async16(void* dst, const void* src, bool valid) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_addr(dst)), "l"(src),
-               "r"(valid ? 16 : 0)
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool valid) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(valid ? 16 : 0)
                : "memory");
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
 
 // byte offset of 16-byte chunk `ch` of row `r` in a [rows][HD] bf16 tile
 template <int HD>
@@ -75,56 +86,68 @@ __device__ __forceinline__ int swz(int r, int ch) {
   return r * (HD * 2) + ((ch ^ (r & 7)) << 4);
 }
 
-template <int HD, int NW>
-struct MmaCfg {
+template <int HD, int NW, int CL>
+struct ClusterCfg {
+  static constexpr int kCluster = CL;                         // CTAs per (request, kv head)
   static constexpr int kThreads = NW * 32;
-  static constexpr int kStageF = kKeys * HD;                  // floats per K (or V) staging tile
-  static constexpr int kTileB = kKeys * HD * 2;               // bytes per bf16 tile
-  static constexpr int kSmem = 2 * 2 * kStageF * 4 + 4 * kTileB;   // 2 stages x (K,V) fp32 + Khi,Klo,Vhi,Vlo
+  static constexpr int kRows = NW * 16;                        // query rows (padded)
+  static constexpr int kTileB = kKeys * HD * 2;                // one bf16 plane tile
+  static constexpr int kStageB = 4 * kTileB;                   // Khi, Klo, Vhi, Vlo
+  static constexpr int kRing = kStages * kStageB;
+  static constexpr int kMerge = kRows * HD * 4 + 2 * kRows * 4;  // o, m, l of every row
+  static constexpr int kSmem = kRing > kMerge ? kRing : kMerge;
 };
 
-template <int HD, int NW>
-__global__ void __launch_bounds__(NW * 32) attn_mma_kernel(const __grid_constant__ AttnParams p) {
-  using C = MmaCfg<HD, NW>;
+template <int HD, int NW, int CL>
+__global__ void __launch_bounds__(NW * 32) attn_cluster_kernel(const __grid_constant__ AttnParams p) {
+  using C = ClusterCfg<HD, NW, CL>;
+  constexpr int kCluster = CL;
   extern __shared__ __align__(128) uint8_t sm[];
-  float* stage = reinterpret_cast<float*>(sm);                     // [2][K,V][kKeys][HD]
-  uint8_t* khi = sm + 2 * 2 * C::kStageF * 4;
-  uint8_t* klo = khi + C::kTileB;
-  uint8_t* vhi = klo + C::kTileB;
-  uint8_t* vlo = vhi + C::kTileB;
+  cg::cluster_group cluster = cg::this_cluster();
+  const int rank = (int)cluster.block_rank();
 
   griddep_wait();
   griddep_trigger();
-  const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
+  const int kvh = blockIdx.y, b = blockIdx.z;
   const int G = p.nq / p.nkv, rows = G * p.block;
   const int c = p.ctx_len[b];
   const int total = c + p.block;
-  const int j0 = split * p.chunk, j1 = min(total, j0 + p.chunk);
+  const int per = (total + kCluster - 1) / kCluster;
+  const int chunk = (per + kKeys - 1) / kKeys * kKeys;
+  const int j0 = rank * chunk, j1 = min(total, j0 + chunk);
+  const int ntiles = j0 < j1 ? (j1 - j0 + kKeys - 1) / kKeys : 0;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int g = lane >> 2, t = lane & 3;
 
-  const float* kc = p.kc + (((size_t)b * p.layers + p.layer) * p.nkv + kvh) * p.cap * HD;
-  const float* vc = p.vc + (((size_t)b * p.layers + p.layer) * p.nkv + kvh) * p.cap * HD;
-  const float* kb = p.kb + ((size_t)b * p.nkv + kvh) * p.block * HD;
-  const float* vb = p.vb + ((size_t)b * p.nkv + kvh) * p.block * HD;
+  const size_t cplane = (size_t)p.cap * HD, bplane = (size_t)p.block * HD;
+  const __nv_bfloat16* kc =
+      static_cast<const __nv_bfloat16*>(p.kc) + (((size_t)b * p.layers + p.layer) * p.nkv + kvh) * 2 * cplane;
+  const __nv_bfloat16* vc =
+      static_cast<const __nv_bfloat16*>(p.vc) + (((size_t)b * p.layers + p.layer) * p.nkv + kvh) * 2 * cplane;
+  const __nv_bfloat16* kb = static_cast<const __nv_bfloat16*>(p.kb) + ((size_t)b * p.nkv + kvh) * 2 * bplane;
+  const __nv_bfloat16* vb = static_cast<const __nv_bfloat16*>(p.vb) + ((size_t)b * p.nkv + kvh) * 2 * bplane;
 
-  // issue the fp32 loads of key tile starting at jt into staging buffer `buf`
-  auto load_tile = [&](int jt, int buf) {
-    float* ks = stage + (size_t)buf * 2 * C::kStageF;
-    float* vs = ks + C::kStageF;
-    constexpr int chunks = kKeys * HD / 4;   // 16-byte chunks per tile
-    for (int e = tid; e < chunks; e += C::kThreads) {
-      const int r = e / (HD / 4), col = (e % (HD / 4)) * 4;
-      const int j = jt + r;
-      const bool valid = j < j1;
-      const float* ksrc = kc;
-      const float* vsrc = vc;
-      if (valid) {
-        ksrc = j < c ? kc + (size_t)j * HD + col : kb + (size_t)(j - c) * HD + col;
-        vsrc = j < c ? vc + (size_t)j * HD + col : vb + (size_t)(j - c) * HD + col;
+  // tile it -> ring stage it % kStages: the four planes, 16-byte chunks
+  auto load_tile = [&](int it) {
+    if (it < ntiles) {
+      const int jt = j0 + it * kKeys;
+      const uint32_t base = smem_addr(sm + (it % kStages) * C::kStageB);
+      constexpr int cpr = HD * 2 / 16;                           // chunks per row
+      for (int e = tid; e < 4 * kKeys * cpr; e += C::kThreads) {
+        const int pl = e / (kKeys * cpr), rem = e - pl * kKeys * cpr;
+        const int r = rem / cpr, ch = rem - r * cpr;
+        const int j = jt + r;
+        const bool valid = j < j1;
+        const bool is_v = pl >= 2, lo = pl & 1;
+        const __nv_bfloat16* src = is_v ? vc : kc;
+        if (valid) {
+          if (j < c)
+            src = (is_v ? vc : kc) + lo * cplane + (size_t)j * HD + ch * 8;
+          else
+            src = (is_v ? vb : kb) + lo * bplane + (size_t)(j - c) * HD + ch * 8;
+        }
+        cp_async16(base + pl * C::kTileB + swz<HD>(r, ch), src, valid);
       }
-      cp_async16(ks + r * HD + col, ksrc, valid);
-      cp_async16(vs + r * HD + col, vsrc, valid);
     }
     cp_async_commit();
   };
@@ -158,39 +181,21 @@ __global__ void __launch_bounds__(NW * 32) attn_mma_kernel(const __grid_constant
   for (int i = 0; i < HD / 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
   float m_a = kNegBig, m_b = kNegBig, l_a = 0.f, l_b = 0.f;
 
-  const int ntiles = j0 < j1 ? (j1 - j0 + kKeys - 1) / kKeys : 0;
-  if (ntiles > 0) load_tile(j0, 0);
+#pragma unroll
+  for (int i = 0; i < kStages - 1; ++i) load_tile(i);
+  const int mi = lane >> 3, rr = lane & 7;
   for (int it = 0; it < ntiles; ++it) {
     const int jt = j0 + it * kKeys;
-    cp_async_wait_all();
-    __syncthreads();                          // staging[it&1] landed; hi/lo tiles free
-    if (it + 1 < ntiles) load_tile(jt + kKeys, (it + 1) & 1);
-    {   // split the staged fp32 tile into hi/lo bf16 tiles
-      const float* ks = stage + (size_t)(it & 1) * 2 * C::kStageF;
-      const float* vs = ks + C::kStageF;
-      for (int e = tid; e < kKeys * HD / 4; e += C::kThreads) {
-        const int r = e / (HD / 4), col = (e % (HD / 4)) * 4;
-        const int off = swz<HD>(r, col >> 3) + (col & 7) * 2;
-        float4 kv = *reinterpret_cast<const float4*>(ks + r * HD + col);
-        float4 vv = *reinterpret_cast<const float4*>(vs + r * HD + col);
-        uint32_t h0, l0, h1, l1;
-        split2(kv.x, kv.y, h0, l0);
-        split2(kv.z, kv.w, h1, l1);
-        *reinterpret_cast<uint2*>(khi + off) = make_uint2(h0, h1);
-        *reinterpret_cast<uint2*>(klo + off) = make_uint2(l0, l1);
-        split2(vv.x, vv.y, h0, l0);
-        split2(vv.z, vv.w, h1, l1);
-        *reinterpret_cast<uint2*>(vhi + off) = make_uint2(h0, h1);
-        *reinterpret_cast<uint2*>(vlo + off) = make_uint2(l0, l1);
-      }
-    }
-    __syncthreads();
+    cp_async_wait<kStages - 2>();
+    __syncthreads();                          // tile it landed; stage (it-1) free for tile it+kStages-1
+    load_tile(it + kStages - 1);
+    const uint8_t* st = sm + (it % kStages) * C::kStageB;
+    const uint8_t *khi = st, *klo = st + C::kTileB, *vhi = st + 2 * C::kTileB, *vlo = st + 3 * C::kTileB;
 
     // ---- S = Q K^T for this warp's 16 rows x 32 keys (4 n-blocks of 8 keys)
     float s[4][4];
 #pragma unroll
     for (int nb = 0; nb < 4; ++nb) s[nb][0] = s[nb][1] = s[nb][2] = s[nb][3] = 0.f;
-    const int mi = lane >> 3, rr = lane & 7;
 #pragma unroll
     for (int kk = 0; kk < HD / 16; ++kk) {
 #pragma unroll
@@ -208,7 +213,7 @@ __global__ void __launch_bounds__(NW * 32) attn_mma_kernel(const __grid_constant
         mma16816(s[2 * jp + 1], ql[kk], bh[2], bh[3]);
       }
     }
-    // ---- mask keys past the split's end, online softmax (log2 domain)
+    // ---- mask keys past the chunk, online softmax (log2 domain)
     float mx_a = kNegBig, mx_b = kNegBig;
 #pragma unroll
     for (int nb = 0; nb < 4; ++nb) {
@@ -269,75 +274,136 @@ __global__ void __launch_bounds__(NW * 32) attn_mma_kernel(const __grid_constant
       }
     }
   }
+  cp_async_wait<0>();
+  __syncthreads();                            // the ring is free: reuse it for the merge
 
-  // ---- partial results: unnormalised o, running max (natural log units), sum
+  // ---- publish this CTA's partial rows: o (unnormalised), m, l
 #pragma unroll
   for (int sh = 1; sh <= 2; sh <<= 1) {
     l_a += __shfl_xor_sync(0xffffffffu, l_a, sh);
     l_b += __shfl_xor_sync(0xffffffffu, l_b, sh);
   }
+  float* os = reinterpret_cast<float*>(sm);              // [kRows][HD]
+  float* ms = os + C::kRows * HD;                        // [kRows]
+  float* ls = ms + C::kRows;                             // [kRows]
 #pragma unroll
-  for (int half = 0; half < 2; ++half) {
-    const int r = half ? r_hi : r_lo;
-    if (r >= rows) continue;
+  for (int nb = 0; nb < HD / 8; ++nb) {
+    *reinterpret_cast<float2*>(os + r_lo * HD + nb * 8 + 2 * t) = make_float2(o[nb][0], o[nb][1]);
+    *reinterpret_cast<float2*>(os + r_hi * HD + nb * 8 + 2 * t) = make_float2(o[nb][2], o[nb][3]);
+  }
+  if (t == 0) {
+    ms[r_lo] = ntiles > 0 ? m_a : kNegBig;
+    ms[r_hi] = ntiles > 0 ? m_b : kNegBig;
+    ls[r_lo] = ntiles > 0 ? l_a : 0.f;
+    ls[r_hi] = ntiles > 0 ? l_b : 0.f;
+  }
+  cluster.sync();
+
+  // ---- merge: CTA `rank` finalises rows rank, rank + kCluster, ...
+  __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out);
+  for (int r = rank + warp * kCluster; r < rows; r += NW * kCluster) {
+    float mr[kCluster], lr[kCluster];
+    float M = kNegBig;
+#pragma unroll
+    for (int q = 0; q < kCluster; ++q) {
+      mr[q] = *cluster.map_shared_rank(ms + r, q);
+      lr[q] = *cluster.map_shared_rank(ls + r, q);
+      if (lr[q] > 0.f) M = fmaxf(M, mr[q]);
+    }
+    float L = 0.f;
+#pragma unroll
+    for (int q = 0; q < kCluster; ++q) {
+      mr[q] = lr[q] > 0.f ? exp2f(mr[q] - M) : 0.f;     // weight of rank q
+      L += mr[q] * lr[q];
+    }
+    const float inv = 1.f / L;
     const int gh = r / p.block, k = r - gh * p.block;
-    const size_t row = (((size_t)b * p.nq + kvh * G + gh) * p.block + k) * p.splits + split;
-    const float m = half ? m_b : m_a, l = half ? l_b : l_a;
+    const size_t obase = ((size_t)b * p.block + k) * p.nq * HD + (size_t)(kvh * G + gh) * HD;
+    for (int d = lane; d < HD; d += 32) {
+      float acc = 0.f;
 #pragma unroll
-    for (int nb = 0; nb < HD / 8; ++nb)
-      *reinterpret_cast<float2*>(p.opart + row * HD + nb * 8 + 2 * t) =
-          half ? make_float2(o[nb][2], o[nb][3]) : make_float2(o[nb][0], o[nb][1]);
-    if (t == 0) p.ml[row] = make_float2(ntiles > 0 ? m * kLn2 : -FLT_MAX, ntiles > 0 ? l : 0.f);
+      for (int q = 0; q < kCluster; ++q)
+        if (mr[q] != 0.f) acc += mr[q] * *cluster.map_shared_rank(os + r * HD + d, q);
+      put_act(out, p.out_plane, obase + d, acc * inv);
+    }
+  }
+  cluster.sync();                             // keep every CTA's partials alive until all reads are done
+}
+
+template <int HD, int NW, int CL>
+cudaError_t launch_one(const AttnParams& p, cudaStream_t s) {
+  using C = ClusterCfg<HD, NW, CL>;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(CL, p.nkv, p.B);
+  cfg.blockDim = dim3(C::kThreads);
+  cfg.dynamicSmemBytes = C::kSmem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = CL;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl_enabled() ? 2 : 1;
+  return cudaLaunchKernelEx(&cfg, attn_cluster_kernel<HD, NW, CL>, p);
+}
+
+template <int HD, int NW, int CL>
+cudaError_t prepare_one() {
+  cudaError_t e = cudaFuncSetAttribute(attn_cluster_kernel<HD, NW, CL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       ClusterCfg<HD, NW, CL>::kSmem);
+  if (e == cudaSuccess && CL > 8)
+    e = cudaFuncSetAttribute(attn_cluster_kernel<HD, NW, CL>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  return e;
+}
+
+template <int HD, int CL>
+cudaError_t prepare_hd() {
+  cudaError_t e;
+  if ((e = prepare_one<HD, 1, CL>()) || (e = prepare_one<HD, 2, CL>()) || (e = prepare_one<HD, 4, CL>()) ||
+      (e = prepare_one<HD, 8, CL>()))
+    return e;
+  return cudaSuccess;
+}
+
+template <int HD, int CL>
+cudaError_t launch_hd(const AttnParams& p, cudaStream_t s) {
+  const int rows = (p.nq / p.nkv) * p.block;
+  const int nw = rows <= 16 ? 1 : rows <= 32 ? 2 : rows <= 64 ? 4 : 8;
+  switch (nw) {
+    case 1: return launch_one<HD, 1, CL>(p, s);
+    case 2: return launch_one<HD, 2, CL>(p, s);
+    case 4: return launch_one<HD, 4, CL>(p, s);
+    default: return launch_one<HD, 8, CL>(p, s);
   }
 }
 
-template <int HD, int NW>
-cudaError_t launch_one(const AttnParams& p, cudaStream_t s) {
-  using C = MmaCfg<HD, NW>;
-  return launch_pdl(attn_mma_kernel<HD, NW>, dim3(p.splits, p.nkv, p.B), dim3(C::kThreads), C::kSmem, s, p);
-}
-
-template <int HD, int NW>
-cudaError_t prepare_one() {
-  return cudaFuncSetAttribute(attn_mma_kernel<HD, NW>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              MmaCfg<HD, NW>::kSmem);
+int cluster_choice(const AttnParams& p) {
+  static const char* env = getenv("DFLASH_ATTN_CLUSTER");
+  if (env) return atoi(env) == 16 ? 16 : 8;
+  // 16-CTA clusters when 8-CTA ones would leave most SMs idle
+  return (long)p.B * p.nkv * 8 < 152 ? 16 : 8;
 }
 
 }  // namespace
 
-int attention_mma_key_tile() { return kKeys; }
-
 cudaError_t attention_mma_prepare(int hd) {
-  cudaError_t e = cudaSuccess;
+  cudaError_t e;
   if (hd == 128) {
-    if ((e = prepare_one<128, 1>()) || (e = prepare_one<128, 2>()) || (e = prepare_one<128, 4>()) ||
-        (e = prepare_one<128, 8>()))
-      return e;
+    if ((e = prepare_hd<128, 8>()) || (e = prepare_hd<128, 16>())) return e;
   } else {
-    if ((e = prepare_one<64, 1>()) || (e = prepare_one<64, 2>()) || (e = prepare_one<64, 4>()) ||
-        (e = prepare_one<64, 8>()))
-      return e;
+    if ((e = prepare_hd<64, 8>()) || (e = prepare_hd<64, 16>())) return e;
   }
-  return e;
+  return cudaSuccess;
 }
 
-cudaError_t attention_mma_split_launch(const AttnParams& p, cudaStream_t s) {
-  const int rows = (p.nq / p.nkv) * p.block;
-  const int nw = rows <= 16 ? 1 : rows <= 32 ? 2 : rows <= 64 ? 4 : 8;
-  if (p.hd == 128) {
-    switch (nw) {
-      case 1: return launch_one<128, 1>(p, s);
-      case 2: return launch_one<128, 2>(p, s);
-      case 4: return launch_one<128, 4>(p, s);
-      default: return launch_one<128, 8>(p, s);
-    }
-  }
-  switch (nw) {
-    case 1: return launch_one<64, 1>(p, s);
-    case 2: return launch_one<64, 2>(p, s);
-    case 4: return launch_one<64, 4>(p, s);
-    default: return launch_one<64, 8>(p, s);
-  }
+// Whole attention of one layer (no separate merge kernel).
+cudaError_t attention_mma_launch(const AttnParams& p, cudaStream_t s) {
+  const bool big = cluster_choice(p) == 16;
+  if (p.hd == 128) return big ? launch_hd<128, 16>(p, s) : launch_hd<128, 8>(p, s);
+  return big ? launch_hd<64, 16>(p, s) : launch_hd<64, 8>(p, s);
 }
 
 }  // namespace dflash

@@ -74,12 +74,14 @@ struct EpiSwiGLU {
 
 // Block Q/K/V of one draft layer: tag 0 = Q, 1 = K, 2 = V.  Row = b*block + k
 // sits at position ctx_len[b] + k, whose RoPE (cos, sin) table rope[row][hd/2]
-// was filled by the embedding kernel; Q and K get RoPE.  Outputs are fp32,
-// head-major [b][head][k][hd].
+// was filled by the embedding kernel; Q and K get RoPE.  Q is fp32
+// [b][head][k][hd]; K and V are stored like the context cache, as
+// [b][head][plane][k][hd] of T (two bf16 planes hi, lo for bf16 models).
+template <typename T>
 struct EpiQKV {
   float* q;
-  float* kb;
-  float* vb;
+  T* kb;
+  T* vb;
   const float2* rope;
   int block, nq, nkv, hd;
   // thread n owns feature n of the tile; the RoPE entries of 8 rows are
@@ -87,8 +89,9 @@ struct EpiQKV {
   __device__ __forceinline__ void operator()(const float* t, int ld, int m0, int mc, int, const GemmSeg& sg,
                                              int tis) const {
     const int tag = sg.tag;
-    float* dst = tag == 0 ? q : (tag == 1 ? kb : vb);
+    T* dkv = tag == 1 ? kb : vb;
     const int nh = tag == 0 ? nq : nkv, half = hd >> 1;
+    const int planes = ActPlanes<T>::n;
     const int n = threadIdx.x & (kTileN - 1), step = blockDim.x / kTileN;
     const int feat = tis * kTileN + n, head = feat / hd, d = feat - head * hd;
     const int i = d < half ? d : d - half;
@@ -107,7 +110,10 @@ struct EpiQKV {
         const int row = m0 + m, b = row / block, k = row - b * block;
         const float v = t[n * ld + m], pv = t[pn * ld + m];
         const float r = tag == 2 ? v : (d < half ? v * sc[j].x - pv * sc[j].y : v * sc[j].x + pv * sc[j].y);
-        dst[(((size_t)b * nh + head) * block + k) * hd + d] = r;
+        if (tag == 0)
+          q[(((size_t)b * nh + head) * block + k) * hd + d] = r;
+        else
+          put_act(dkv, (size_t)block * hd, (((size_t)b * nh + head) * planes * block + k) * hd + d, r);
       }
     }
   }
@@ -115,18 +121,20 @@ struct EpiQKV {
 
 // Context K/V injection: tag = 2*layer + (0: K, 1: V).  rowinfo[row] =
 // (request, position) or (-1, -1) for padding rows; rope[row][hd/2] = (cos,
-// sin) at that position.  Writes the cache [b][layer][kvh][pos][hd] (fp32);
-// K gets RoPE at its absolute position.
+// sin) at that position.  Writes the cache [b][layer][kvh][plane][pos][hd] of
+// T (fp32 one plane; bf16 two planes hi, lo); K gets RoPE at its position.
+template <typename T>
 struct EpiInject {
-  float* kc;
-  float* vc;
+  T* kc;
+  T* vc;
   const int2* rowinfo;
   const float2* rope;
   int layers, nkv, hd, cap;
   __device__ __forceinline__ void operator()(const float* t, int ld, int m0, int mc, int, const GemmSeg& sg,
                                              int tis) const {
     const int layer = sg.tag >> 1, is_v = sg.tag & 1, half = hd >> 1;
-    float* dst = is_v ? vc : kc;
+    T* dst = is_v ? vc : kc;
+    const int planes = ActPlanes<T>::n;
     const int n = threadIdx.x & (kTileN - 1), step = blockDim.x / kTileN;
     const int feat = tis * kTileN + n, head = feat / hd, d = feat - head * hd;
     const int i = d < half ? d : d - half;
@@ -147,7 +155,8 @@ struct EpiInject {
         if (ri[j].x < 0) continue;
         const float v = t[n * ld + m], pv = t[pn * ld + m];
         const float r = is_v ? v : (d < half ? v * sc[j].x - pv * sc[j].y : v * sc[j].x + pv * sc[j].y);
-        dst[((((size_t)ri[j].x * layers + layer) * nkv + head) * cap + ri[j].y) * hd + d] = r;
+        put_act(dst, (size_t)cap * hd,
+                ((((size_t)ri[j].x * layers + layer) * nkv + head) * planes * cap + ri[j].y) * hd + d, r);
       }
     }
   }

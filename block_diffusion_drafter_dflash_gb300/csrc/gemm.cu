@@ -149,10 +149,10 @@ cudaError_t gemm_launch(const GemmProblem& p, const GemmPlan& plan, const Epi& e
                                                    cudaStream_t);                                       \
   template cudaError_t gemm_launch<T, EpiSwiGLU<T>>(const GemmProblem&, const GemmPlan&,                 \
                                                     const EpiSwiGLU<T>&, cudaStream_t);                 \
-  template cudaError_t gemm_launch<T, EpiQKV>(const GemmProblem&, const GemmPlan&, const EpiQKV&,        \
-                                              cudaStream_t);                                            \
-  template cudaError_t gemm_launch<T, EpiInject>(const GemmProblem&, const GemmPlan&, const EpiInject&,  \
+  template cudaError_t gemm_launch<T, EpiQKV<T>>(const GemmProblem&, const GemmPlan&, const EpiQKV<T>&,  \
                                                  cudaStream_t);                                         \
+  template cudaError_t gemm_launch<T, EpiInject<T>>(const GemmProblem&, const GemmPlan&,                 \
+                                                    const EpiInject<T>&, cudaStream_t);                 \
   template cudaError_t gemm_launch<T, EpiArgmax>(const GemmProblem&, const GemmPlan&, const EpiArgmax&,  \
                                                  cudaStream_t);
 

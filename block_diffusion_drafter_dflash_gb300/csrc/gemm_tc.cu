@@ -376,9 +376,13 @@ bool encode_activation_map(void* map, const void* base, int inner, int rows, int
 
 size_t tensor_map_bytes() { return sizeof(CUtensorMap); }
 
-// Tuning knobs (environment, read once): DFLASH_TC_STAGES pipeline depth,
-// DFLASH_TC_WAVES target CTAs as a multiple of the resident slots,
-// DFLASH_TC_KMIN fewest 64-column K blocks per split.
+// Plan of one launch from a small streaming model.  For every pipeline depth
+// S (which fixes the CTAs that fit on an SM) and split-K factor, the launch
+// runs in waves of resident CTAs; a CTA streams its weight tiles at
+// min(HBM bandwidth / resident CTAs, bytes in flight / latency), and pays a
+// fixed start cost per wave plus a reduction tail when K is split.  The
+// cheapest plan wins.  DFLASH_TC_STAGES forces S; DFLASH_TC_KMIN is the fewest
+// 64-column K blocks per split (environment, read once).
 int env_int(const char* name, int dflt) {
   const char* v = getenv(name);
   return v ? atoi(v) : dflt;
@@ -386,8 +390,9 @@ int env_int(const char* name, int dflt) {
 
 GemmPlan plan_gemm_tc(int M, int K, int tiles, int sms, int planes) {
   static const int env_stages = env_int("DFLASH_TC_STAGES", 0);
-  static const int env_waves = env_int("DFLASH_TC_WAVES", 1);
   static const int env_kmin = env_int("DFLASH_TC_KMIN", 4);
+  static const int env_splits = env_int("DFLASH_TC_SPLITS", 0);   // force a split factor (experiments)
+  constexpr double kBw = 6.5e12, kLat = 3.2e-6, kStart = 2.0e-6, kReduce = 3.0e-6;
   GemmPlan g{};
   g.tc = 1;
   g.planes = planes;
@@ -395,20 +400,40 @@ GemmPlan plan_gemm_tc(int M, int K, int tiles, int sms, int planes) {
   g.bm = M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : M <= 128 ? 128 : 256;
   g.bm = std::min(g.bm, bm_max);
   g.token_tiles = (M + g.bm - 1) / g.bm;
-  const int n = g.bm * planes;
-  // deep rings for the weight-streaming shapes (one CTA per SM with ~112 KB of
-  // weights in flight measured best at batch 1), four stages for wide tiles
-  g.stages = env_stages > 0 ? std::min(env_stages, kMaxStages) : (n <= 64 ? 7 : 4);
   const size_t sb = stage_bytes(g.bm, planes);
-  g.stages = std::min<int>(g.stages, (int)((kSmemMaxPerCta - 1024 - kBarBytes) / sb));
-  g.smem = 1024 + (size_t)g.stages * sb + kBarBytes;
-  const int cps = std::max<int>(1, (int)(kSmemPerSM / (g.smem + kSmemReservedPerCta)));   // CTAs per SM
+  const int s_max = std::min<int>(kMaxStages, (int)((kSmemMaxPerCta - 1024 - kBarBytes) / sb));
   const int kblocks = K / 64;
-  const long ctas = (long)tiles * g.token_tiles;
-  int splits = (int)std::max(1L, (long)sms * cps * std::max(1, env_waves) / ctas);
-  splits = std::min(splits, std::max(1, kblocks / std::max(1, env_kmin)));
-  g.kblocks_per_split = (kblocks + splits - 1) / splits;
-  g.splits = (kblocks + g.kblocks_per_split - 1) / g.kblocks_per_split;
+  const int kmax = std::max(1, kblocks / std::max(1, env_kmin));
+  const long base = (long)tiles * g.token_tiles;
+  double best = 1e30;
+  for (int S : {3, 4, 5, 6, 7, 8, 10}) {
+    if (env_stages > 0 && S != std::min(env_stages, s_max)) continue;
+    if (S > s_max) continue;
+    const size_t smem = 1024 + (size_t)S * sb + kBarBytes;
+    const long slots = (long)sms * std::max<long>(1, (long)(kSmemPerSM / (smem + kSmemReservedPerCta)));
+    for (int sp = 1; sp <= kmax; ++sp) {
+      if (env_splits > 0 && sp != std::min(env_splits, kmax)) continue;
+      const int kbps = (kblocks + sp - 1) / sp;
+      const int splits = (kblocks + kbps - 1) / kbps;
+      if (splits != sp && env_splits <= 0) continue;
+      const long ctas = base * splits;
+      // HBM side: the weight tile of each stage (activation tiles come from L2)
+      const double wtile = kTileN * 128.0;
+      const double bytes = kbps * wtile, inflight = std::min(S, kbps) * wtile;
+      double t = splits > 1 ? kReduce : 0.0;
+      for (long left = ctas; left > 0; left -= slots) {
+        const long n = std::min(left, slots);
+        t += bytes / std::min(kBw / n, inflight / kLat) + kStart;
+      }
+      if (t < best * 0.999) {
+        best = t;
+        g.stages = S;
+        g.smem = smem;
+        g.kblocks_per_split = kbps;
+        g.splits = splits;
+      }
+    }
+  }
   g.partial_floats = g.splits > 1 ? (size_t)g.splits * M * tiles * kTileN : 0;
   g.counters = g.splits > 1 ? g.token_tiles * tiles : 0;
   return g;
@@ -439,8 +464,10 @@ template cudaError_t gemm_tc_launch<EpiStoreF32>(const GemmProblem&, const GemmP
 template cudaError_t gemm_tc_launch<EpiResidual>(const GemmProblem&, const GemmPlan&, const EpiResidual&, cudaStream_t);
 template cudaError_t gemm_tc_launch<EpiSwiGLU<__nv_bfloat16>>(const GemmProblem&, const GemmPlan&,
                                                               const EpiSwiGLU<__nv_bfloat16>&, cudaStream_t);
-template cudaError_t gemm_tc_launch<EpiQKV>(const GemmProblem&, const GemmPlan&, const EpiQKV&, cudaStream_t);
-template cudaError_t gemm_tc_launch<EpiInject>(const GemmProblem&, const GemmPlan&, const EpiInject&, cudaStream_t);
+template cudaError_t gemm_tc_launch<EpiQKV<__nv_bfloat16>>(const GemmProblem&, const GemmPlan&,
+                                                           const EpiQKV<__nv_bfloat16>&, cudaStream_t);
+template cudaError_t gemm_tc_launch<EpiInject<__nv_bfloat16>>(const GemmProblem&, const GemmPlan&,
+                                                              const EpiInject<__nv_bfloat16>&, cudaStream_t);
 template cudaError_t gemm_tc_launch<EpiArgmax>(const GemmProblem&, const GemmPlan&, const EpiArgmax&, cudaStream_t);
 
 }  // namespace dflash

@@ -8,12 +8,14 @@ namespace dflash {
 // ---------------------------------------------------------------- attention
 // Block queries of one draft layer against [context K/V of the cache ; block K/V]
 // (no mask: every block row sees all context and the whole block).
+// K/V (block and cache) are stored as `planes` planes of the model dtype
+// (fp32: one plane; bf16: hi and lo planes): index [..][plane][pos][hd].
 struct AttnParams {
-  const float* q;       // [B][nq][block][hd]   (RoPE applied)
-  const float* kb;      // [B][nkv][block][hd]  (RoPE applied)
-  const float* vb;      // [B][nkv][block][hd]
-  const float* kc;      // cache K [B][layers][nkv][cap][hd]
-  const float* vc;      // cache V
+  const float* q;       // [B][nq][block][hd] fp32 (RoPE applied)
+  const void* kb;       // [B][nkv][planes][block][hd]  (RoPE applied)
+  const void* vb;       // [B][nkv][planes][block][hd]
+  const void* kc;       // cache K [B][layers][nkv][planes][cap][hd]
+  const void* vc;       // cache V
   const int32_t* ctx_len;
   int layer, layers, cap;
   int B, nq, nkv, hd, block;

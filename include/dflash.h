@@ -137,8 +137,11 @@ int32_t dflash_clear_status(const dflash_model* model, dflash_stream_t stream);
 /* --- persistent draft KV cache (paper §4.1: context K/V stored in the draft
  * model's KV cache and reused across drafting iterations) ----------------------
  * Layout inside the caller's block of device memory (each region 256-B aligned):
- *   K [batch][layers][n_kv_heads][capacity][head_dim]   (fp32, RoPE applied)
- *   V [batch][layers][n_kv_heads][capacity][head_dim]   (fp32)
+ *   fp32 models:  K [batch][layers][n_kv_heads][capacity][head_dim] fp32 (RoPE applied)
+ *   bf16 models:  K [batch][layers][n_kv_heads][2][capacity][head_dim] bf16: planes
+ *                 hi and lo with k = hi + lo (lo = the rounding residual of hi),
+ *                 i.e. fp32-level precision in the same bytes
+ *   V likewise
  *   ctx_len int32 [batch]                                (tokens held per request)
  * Only context entries live in the cache; a block's own K/V never does. */
 size_t dflash_cache_bytes(const dflash_config* cfg, int32_t batch, int32_t capacity);
@@ -196,8 +199,8 @@ int32_t dflash_inject_context(const dflash_model* model, dflash_cache* cache, co
  * dflash_noalloc_scratch_bytes() bytes (8 MiB) that every GPU loading this
  * library holds until the process exits.  No call allocates or frees memory.
  *   - A launch whose scratch plan exceeds that size (an 8B-shaped drafter
- *     fits about 40 injected rows) returns DFLASH_ERR_CAPACITY without
- *     launching; inject fewer rows per call.
+ *     fits the 16 to 32 rows of a cycle's injection) returns
+ *     DFLASH_ERR_CAPACITY without launching; inject fewer rows per call.
  *   - The first call on a device looks the array's device address up with
  *     cudaGetSymbolAddress (with that device current) and caches it; make that
  *     first call before any stream capture.

@@ -33,7 +33,7 @@ def _close(x: torch.Tensor, y: torch.Tensor, t: float) -> float:
                          ids=["tiny-fp32", "tiny-bf16", "8b-bf16"])
 def test_noalloc_injection_matches_workspace_injection_twice(cfg):
     block = 16
-    ctx = 40 if cfg is QWEN3_8B else 64
+    ctx = 24 if cfg is QWEN3_8B else 64
     df, a, cache_b = _pair(cfg, ctx, block)
     # call 1: exact host counts; call 2: counts only on the device, padded rows
     f1 = make_features(cfg, ctx, seed=21, device="cuda")
