@@ -154,30 +154,37 @@ def gemm_bytes_per_cycle(cfg, B: int, block: int, inject_rows: int) -> dict:
 
 
 # ---------------------------------------------------------------- measured DRAM traffic
-TRAFFIC_PROFILE = os.path.join(ROOT, "profiles", "gemm_traffic_8b_bs1.md")
-GEMM_SOURCES = ["gemm_tc.cu", "epilogue.cuh", "common.cuh", "ptx.cuh"]
+# Committed ncu summaries of the dominant kernel's DRAM traffic; each is valid
+# only for the workload and the kernel sources it was taken on.
+TRAFFIC_PROFILES = {
+    "gemm": (os.path.join(ROOT, "profiles", "gemm_traffic_8b_bs1.md"),
+             ["gemm_tc.cu", "epilogue.cuh", "common.cuh", "ptx.cuh"]),
+    "persist": (os.path.join(ROOT, "profiles", "persist_traffic_8b_bs1.md"),
+                ["persist.cu", "persist.cuh", "attn_core.cuh", "epilogue.cuh", "common.cuh", "ptx.cuh"]),
+}
 
 
-def gemm_source_sha1() -> str:
+def source_sha1(names) -> str:
     import hashlib
     h = hashlib.sha1()
-    for name in GEMM_SOURCES:
+    for name in names:
         with open(os.path.join(ROOT, "block_diffusion_drafter_dflash_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()
 
 
-def gemm_traffic_per_cycle(workload: str):
-    """DRAM bytes (read + write) of one cycle's projection GEMMs from the
-    committed ncu summary, or None when it was taken on other GEMM sources
-    or another workload."""
+def measured_traffic(kind: str, workload: str):
+    """DRAM bytes (read + write) per cycle of the kernel(s) `kind` from the
+    committed ncu summary, or None when it was taken on other sources or
+    another workload."""
+    path, sources = TRAFFIC_PROFILES[kind]
     try:
-        text = open(TRAFFIC_PROFILE).read()
+        text = open(path).read()
     except OSError:
         return None
     vals = dict(line.split(":", 1) for line in text.splitlines() if ":" in line and line[:1].isalpha())
     try:
-        if vals.get("workload", "").strip() != workload or vals.get("source_sha1", "").strip() != gemm_source_sha1():
+        if vals.get("workload", "").strip() != workload or vals.get("source_sha1", "").strip() != source_sha1(sources):
             return None
         return int(vals["traffic_bytes_per_cycle"].strip())
     except (KeyError, ValueError):
@@ -305,15 +312,32 @@ def run_gpu(args, rank, world, local):
         cyc.step()
     prof = df.dflash_profile_stop(cyc.model)
     gb = gemm_bytes_per_cycle(wl.cfg, wl.batch, wl.block, cyc.rows)
-    gemm_ms = sum(prof[s][0] for s in GEMM_STAGES) / KP
     gemm_bytes = sum(gb.values())
     hbm, bf16, src = load_peaks()
-    achieved = gemm_bytes / (gemm_ms / 1e3) / 1e9
+    if prof["draft_persist"][1] > 0:
+        # one persistent launch runs the whole drafter pass: every layer's
+        # projections and attention (context K/V read) and the LM head
+        kern_bytes = sum(gb[k] for k in ("qkv", "o", "gateup", "down", "lmhead")) + kv_bytes(wl)
+        kern_ms = prof["draft_persist"][0] / KP
+        kern = "persist_kernel, drafter pass (one launch a cycle)"
+        traffic = measured_traffic("persist", wl.name)
+        extra = {}
+        if prof["inject_persist"][1] > 0:
+            inj_bytes, inj_ms = gb["fuse"] + gb["inject"], prof["inject_persist"][0] / KP
+            extra = {"injection_kernel_GBps": round(inj_bytes / (inj_ms / 1e3) / 1e9, 1),
+                     "injection_kernel_ms_per_cycle": round(inj_ms, 4)}
+    else:
+        kern_bytes = gemm_bytes
+        kern_ms = sum(prof[s][0] for s in GEMM_STAGES) / KP
+        kern = "projection GEMMs (all launches of one cycle)"
+        traffic = measured_traffic("gemm", wl.name)
+        extra = {}
+    achieved = kern_bytes / (kern_ms / 1e3) / 1e9
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
-                "frac": round(achieved / hbm, 4), "traffic": gemm_traffic_per_cycle(wl.name),
-                "kernel": "projection GEMMs (all launches of one cycle)", "peak_source": src,
-                "algorithmic_bytes_per_cycle": gemm_bytes, "kernel_ms_per_cycle": round(gemm_ms, 4)}
-    stages = {s: {"ms_per_cycle": round(v[0] / KP, 4), "launches_per_cycle": v[1] / KP} for s, v in prof.items()}
+                "frac": round(achieved / hbm, 4), "traffic": traffic, "kernel": kern, "peak_source": src,
+                "algorithmic_bytes_per_cycle": kern_bytes, "kernel_ms_per_cycle": round(kern_ms, 4), **extra}
+    stages = {s: {"ms_per_cycle": round(v[0] / KP, 4), "launches_per_cycle": v[1] / KP} for s, v in prof.items()
+              if v[1] > 0}
     cycle_roof_ms = (gemm_bytes + kv_bytes(wl)) / (hbm * 1e9) * 1e3
 
     e2e = None

@@ -68,7 +68,8 @@ SIGNATURES = {
     "dflash_profile_stop": (c_i32, [c_ptr, c_ptr, ctypes.POINTER(ctypes.c_float), c_i32p, c_i32]),
 }
 
-STAGES = ["fuse", "inject", "qkv", "attn", "o", "gateup", "down", "lmhead", "other"]
+STAGES = ["fuse", "inject", "qkv", "attn", "o", "gateup", "down", "lmhead", "other", "inject_persist",
+          "draft_persist"]
 
 
 def lib_path() -> str:

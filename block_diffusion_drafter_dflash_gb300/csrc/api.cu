@@ -14,6 +14,7 @@
 
 #include "gemm.cuh"
 #include "kernels.cuh"
+#include "persist.cuh"
 
 using namespace dflash;
 
@@ -40,10 +41,14 @@ struct dflash_model {
   int sms;
   int32_t* status_dev;     // device status word (first device-detected error)
   double* inv_freq_dev;    // RoPE frequencies theta^(-2i/hd), i < hd/2
-  void* tmaps_dev;         // tensor maps of every weight matrix (bf16 models)
+  void* tmaps_dev;         // tensor maps of every weight matrix (bf16 models), 64-row boxes
+  void* tmaps128_dev;      // the same maps with 128-row boxes (persistent kernel)
   int use_tc;              // bf16 projections on the tcgen05 kernel
+  int persist;             // calls of at most 16 token rows run as one persistent launch
+  int persist_stages;      // its shared-memory ring depth
   unsigned long long* trace_dev;  // GEMM timestamps (DFLASH_TRACE_GEMM=<launch index>)
   long trace_target;
+  int trace_persist;       // DFLASH_TRACE_PERSIST: the persistent drafter records phase timestamps
   long gemm_launches;
   Profiler prof;
 };
@@ -147,7 +152,22 @@ struct WsPlan {
   int counters_n;
   int attn_splits, attn_chunk;
   GemmPlan g_fuse, g_inject, g_qkv, g_o, g_gu, g_down, g_lm;
+  // persistent path: sums of squares, attention chunk partials, tickets + barrier
+  int persist;
+  size_t ssq, aml, tickets;
+  int ntickets, nch;
 };
+
+// The persistent path serves bf16 calls of at most 16 token rows whose
+// attention groups fit 64 query rows.
+bool persist_draft_ok(const dflash_model* m, int B, int block) {
+  const dflash_config& c = m->cfg;
+  return m->persist && B * block <= kPRows && (c.n_q_heads / c.n_kv_heads) * block <= kPAttnRows &&
+         6 * c.layers + 1 <= kPMaxPhases && c.ffn % kTileN == 0;
+}
+bool persist_inject_ok(const dflash_model* m, int max_rows) {
+  return m->persist && max_rows <= kPRows && 1 + 2 * m->cfg.layers <= kPMaxSeg;
+}
 
 // One call's scratch: the injection part when max_rows > 0, the drafter part
 // when block > 0.  Each call lays out only its own regions from offset 0, so a
@@ -160,6 +180,39 @@ WsPlan plan_ws(const dflash_model* m, int B, int cap, int block, int max_rows) {
   const int D = c.hidden, hq = c.n_q_heads * c.head_dim, hk = c.n_kv_heads * c.head_dim, F = c.ffn;
   const int R = B * block, Rm = B * std::max(block - 1, 0);
   WsPlan p{};
+  size_t off = 0;
+  auto take = [&](size_t bytes) { size_t o = off; off += align256(std::max<size_t>(bytes, 1)); return o; };
+  if ((max_rows > 0 && persist_inject_ok(m, max_rows)) || (block > 0 && persist_draft_ok(m, B, block))) {
+    // one persistent launch: activation planes padded to 16 rows, stream-K scratch per CTA
+    const int half = c.head_dim / 2;
+    p.persist = 1;
+    if (max_rows > 0) {
+      p.ntickets = std::max(D / kTileN, c.layers * 2 * (hk / kTileN));
+      p.rowinfo = take(sizeof(int2) * (size_t)max_rows);
+      p.ht = take(2 * 2 * (size_t)kPRows * D);
+      p.rope_c = take(sizeof(float2) * (size_t)kPRows * half);
+    } else {
+      p.ntickets = std::max({(hq + 2 * hk) / kTileN, D / kTileN, F / kTileN, (c.vocab + 255) / 256});
+      const int groups = B * c.n_kv_heads;
+      p.nch = std::max(1, std::min(m->sms / groups, (cap + block + 31) / 32));
+      p.x = take(sizeof(float) * (size_t)kPRows * D);
+      p.u = take(2 * 2 * (size_t)kPRows * D);
+      p.q = take(sizeof(float) * (size_t)R * hq);
+      p.kb = take(2 * 2 * (size_t)R * hk);
+      p.vb = take(2 * 2 * (size_t)R * hk);
+      p.o = take(2 * 2 * (size_t)kPRows * hq);
+      p.a = take(2 * 2 * (size_t)kPRows * F);
+      p.slots = take(sizeof(unsigned long long) * kPRows);
+      p.rope_q = take(sizeof(float2) * (size_t)kPRows * half);
+      p.opart = take(sizeof(float) * (size_t)groups * p.nch * kPAttnRows * c.head_dim);
+      p.aml = take(sizeof(float2) * (size_t)groups * p.nch * kPAttnRows);
+    }
+    p.ssq = take(sizeof(float) * (size_t)(D / kTileN) * kPRows);
+    p.partial = take(sizeof(float) * (size_t)m->sms * 2 * kPRows * 256);
+    p.tickets = take(sizeof(int) * (size_t)(p.ntickets + 1));   // tickets, then the barrier counter
+    p.total = off;
+    return p;
+  }
   std::vector<const GemmPlan*> used;
   if (max_rows > 0) {
     p.g_fuse = plan_gemm(c.dtype, max_rows, c.n_target_feats * D, D / kTileN, m->sms, m->use_tc, 1);
@@ -180,8 +233,6 @@ WsPlan plan_ws(const dflash_model* m, int B, int cap, int block, int max_rows) {
     partial = std::max(partial, g->partial_floats);
     counters = std::max(counters, g->counters);
   }
-  size_t off = 0;
-  auto take = [&](size_t bytes) { size_t o = off; off += align256(std::max<size_t>(bytes, 1)); return o; };
   if (max_rows > 0) {
     p.rowinfo = take(sizeof(int2) * (size_t)max_rows);
     p.yf = take(sizeof(float) * (size_t)max_rows * D);
@@ -379,16 +430,209 @@ int32_t run_draft(const dflash_model* m, const dflash_cache* cache, const int32_
   return DFLASH_OK;
 }
 
+// ---------------------------------------------------------------- persistent path
+struct PhaseBuilder {
+  PParams& p;
+  int add_gemm(int epi, int K, int xmap, int planes, int prow, int scaled, const void* gain) {
+    PPhase& ph = p.ph[p.nphase++];
+    ph = PPhase{};
+    ph.kind = kPhGemm;
+    ph.epi = epi;
+    ph.kb = K / 64;
+    ph.xmap = xmap;
+    ph.planes = planes;
+    ph.prow = prow;
+    ph.scaled = scaled;
+    ph.layer = -1;
+    ph.gain = static_cast<const __nv_bfloat16*>(gain);
+    ph.seg0 = nseg_total();
+    return p.nphase - 1;
+  }
+  void add_other(int kind, int layer) {
+    PPhase& ph = p.ph[p.nphase++];
+    ph = PPhase{};
+    ph.kind = kind;
+    ph.layer = layer;
+  }
+  // segment of `features` output features (per matrix when paired) of the
+  // last projection phase; tile_begin relative to the phase.  Wide segments
+  // (gate/up, the LM head) use 256-feature tiles with the weights on the MMA's
+  // N side; a paired tile is 128 gate + 128 up rows; `ragged` lets the last
+  // tile run past the matrix (its missing rows read as zeros).  The others
+  // use 128-feature tiles with the weights on the M side.
+  bool all_wide = false;   // DFLASH_PERSIST_WIDE=1: every segment that allows it (experiments)
+  void seg(int map0, int map1, int features, int paired, int tag, bool wide = false, bool ragged = false) {
+    PPhase& ph = p.ph[p.nphase - 1];
+    GemmSeg& g = p.seg[ph.seg0 + ph.nseg++];
+    g = GemmSeg{};
+    g.map0 = map0;
+    g.map1 = map1;
+    g.tw = (paired || ragged || ((wide || all_wide) && features % 256 == 0)) ? 256 : 128;
+    g.tiles = paired ? features / 128 : (features + g.tw - 1) / g.tw;
+    g.tile_begin = ph.tiles;
+    g.paired = paired;
+    g.tag = tag;
+    ph.tiles += g.tiles;
+    ++segs;
+  }
+  int segs = 0;
+  int nseg_total() const { return segs; }
+};
+
+int32_t run_inject_persist(const dflash_model* m, dflash_cache* cache, const void* feats, const int32_t* n_new,
+                           int max_rows, char* ws, const WsPlan& P, cudaStream_t s) {
+  const dflash_config& c = m->cfg;
+  const int D = c.hidden, hk = c.n_kv_heads * c.head_dim, F5 = c.n_target_feats * D;
+  int2* rowinfo = reinterpret_cast<int2*>(ws + P.rowinfo);
+  float2* rope = reinterpret_cast<float2*>(ws + P.rope_c);
+  int* tickets = reinterpret_cast<int*>(ws + P.tickets);
+  int32_t* ctx_len = reinterpret_cast<int32_t*>(cache->base + cache->len_off);
+  __nv_bfloat16* ht = reinterpret_cast<__nv_bfloat16*>(ws + P.ht);
+  DF_LAUNCH(DFLASH_STAGE_OTHER, 1,
+            inject_prep_launch(n_new, ctx_len, cache->batch, max_rows, cache->cap, rowinfo, tickets, P.ntickets + 1,
+                               m->status_dev, s, m->inv_freq_dev, c.head_dim, rope),
+            "inject_prep");
+  PParams pp{};
+  if (!encode_activation_map(&pp.xmap[0], feats, F5, max_rows, F5, kPRows) ||
+      !encode_activation_map(&pp.xmap[1], ht, D, 2 * kPRows, D, kPRows))
+    return fail(DFLASH_ERR_INVALID_ARG, "could not encode activation tensor maps (16-B aligned features needed)");
+  pp.wmaps = static_cast<const CUtensorMap*>(m->tmaps128_dev);
+  pp.M = max_rows;
+  pp.D = D;
+  pp.eps = c.rms_eps;
+  pp.stages = m->persist_stages;
+  pp.u = ht;
+  pp.u_plane = (size_t)kPRows * D;
+  pp.ssq = reinterpret_cast<float*>(ws + P.ssq);
+  pp.partial = reinterpret_cast<float*>(ws + P.partial);
+  pp.tickets = tickets;
+  pp.bar = reinterpret_cast<unsigned int*>(tickets + P.ntickets);
+  pp.status = m->status_dev;
+  pp.inject = EpiInject<__nv_bfloat16>{reinterpret_cast<__nv_bfloat16*>(cache->base + cache->k_off),
+                                       reinterpret_cast<__nv_bfloat16*>(cache->base + cache->v_off), rowinfo, rope,
+                                       c.layers, c.n_kv_heads, c.head_dim, cache->cap};
+  pp.block = 1;
+  pp.attn.hd = c.head_dim;
+  PhaseBuilder pb{pp};
+  pb.add_gemm(kEpFuse, F5, 0, 1, 0, 0, m->g_c);
+  pb.seg(kMapWc, kMapWc, D, 0, 0);
+  pb.add_gemm(kEpInject, D, 1, 2, kPRows, 1, nullptr);
+  for (int l = 0; l < c.layers; ++l) {
+    pb.seg(layer_map(l, kMapK), layer_map(l, kMapK), hk, 0, 2 * l);
+    pb.seg(layer_map(l, kMapV), layer_map(l, kMapV), hk, 0, 2 * l + 1);
+  }
+  DF_LAUNCH(DFLASH_STAGE_INJECT_PERSIST, 1, persist_launch(pp, m->sms, c.head_dim, s), "persistent injection");
+  return DFLASH_OK;
+}
+
+int32_t run_draft_persist(const dflash_model* m, const dflash_cache* cache, const int32_t* anchor, int block,
+                          int32_t* drafts, float* logits, char* ws, const WsPlan& P, cudaStream_t s) {
+  const dflash_config& c = m->cfg;
+  const int B = cache->batch, D = c.hidden, F = c.ffn;
+  const int hq = c.n_q_heads * c.head_dim, hk = c.n_kv_heads * c.head_dim;
+  const int R = B * block;
+  float* x = reinterpret_cast<float*>(ws + P.x);
+  __nv_bfloat16* u = reinterpret_cast<__nv_bfloat16*>(ws + P.u);
+  __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(ws + P.o);
+  __nv_bfloat16* a = reinterpret_cast<__nv_bfloat16*>(ws + P.a);
+  float* ssq = reinterpret_cast<float*>(ws + P.ssq);
+  int* tickets = reinterpret_cast<int*>(ws + P.tickets);
+  unsigned long long* slots = reinterpret_cast<unsigned long long*>(ws + P.slots);
+  float2* rope = reinterpret_cast<float2*>(ws + P.rope_q);
+  const int32_t* ctx_len = reinterpret_cast<const int32_t*>(cache->base + cache->len_off);
+
+  DF_LAUNCH(DFLASH_STAGE_OTHER, 1,
+            persist_draft_prep_launch(static_cast<const __nv_bfloat16*>(m->embed), anchor, c.mask_token_id, c.vocab,
+                                      B, block, D, static_cast<const __nv_bfloat16*>(m->layers[0].g_in), x, u,
+                                      (size_t)kPRows * D, ssq, slots, tickets, P.ntickets + 1, m->status_dev, ctx_len,
+                                      m->inv_freq_dev, c.head_dim, rope, s),
+            "embedding");
+  PParams pp{};
+  if (!encode_activation_map(&pp.xmap[0], u, D, 2 * kPRows, D, kPRows) ||
+      !encode_activation_map(&pp.xmap[1], o, hq, 2 * kPRows, hq, kPRows) ||
+      !encode_activation_map(&pp.xmap[2], a, F, 2 * kPRows, F, kPRows))
+    return fail(DFLASH_ERR_CUDA, "could not encode activation tensor maps");
+  pp.wmaps = static_cast<const CUtensorMap*>(m->tmaps128_dev);
+  pp.M = R;
+  pp.D = D;
+  pp.eps = c.rms_eps;
+  pp.stages = m->persist_stages;
+  pp.x = x;
+  pp.u = u;
+  pp.u_plane = (size_t)kPRows * D;
+  pp.ssq = ssq;
+  pp.partial = reinterpret_cast<float*>(ws + P.partial);
+  pp.tickets = tickets;
+  pp.bar = reinterpret_cast<unsigned int*>(tickets + P.ntickets);
+  pp.status = m->status_dev;
+  float* q = reinterpret_cast<float*>(ws + P.q);
+  __nv_bfloat16* kb = reinterpret_cast<__nv_bfloat16*>(ws + P.kb);
+  __nv_bfloat16* vb = reinterpret_cast<__nv_bfloat16*>(ws + P.vb);
+  pp.qkv = EpiQKV<__nv_bfloat16>{q, kb, vb, rope, block, c.n_q_heads, c.n_kv_heads, c.head_dim};
+  pp.swiglu = EpiSwiGLU<__nv_bfloat16>{a, F, (size_t)kPRows * F};
+  pp.slots = slots;
+  pp.logits = logits;
+  pp.drafts = block > 1 ? drafts : nullptr;
+  pp.vocab = c.vocab;
+  pp.block = block;
+  AttnParams& ap = pp.attn;
+  ap.q = q;
+  ap.kb = kb;
+  ap.vb = vb;
+  ap.kc = cache->base + cache->k_off;
+  ap.vc = cache->base + cache->v_off;
+  ap.ctx_len = ctx_len;
+  ap.layers = c.layers;
+  ap.cap = cache->cap;
+  ap.B = B;
+  ap.nq = c.n_q_heads;
+  ap.nkv = c.n_kv_heads;
+  ap.hd = c.head_dim;
+  ap.block = block;
+  ap.splits = P.nch;
+  ap.opart = reinterpret_cast<float*>(ws + P.opart);
+  ap.ml = reinterpret_cast<float2*>(ws + P.aml);
+  ap.out = o;
+  ap.out_plane = (size_t)kPRows * hq;
+  ap.scale = 1.0f / sqrtf((float)c.head_dim);
+
+  PhaseBuilder pb{pp};
+  if (const char* w = std::getenv("DFLASH_PERSIST_WIDE")) pb.all_wide = std::strcmp(w, "1") == 0;
+  for (int l = 0; l < c.layers; ++l) {
+    const dflash_layer_weights& L = m->layers[l];
+    pb.add_gemm(kEpQKV, D, 0, 2, kPRows, 1, nullptr);
+    pb.seg(layer_map(l, kMapQ), layer_map(l, kMapQ), hq, 0, 0);
+    pb.seg(layer_map(l, kMapK), layer_map(l, kMapK), hk, 0, 1);
+    pb.seg(layer_map(l, kMapV), layer_map(l, kMapV), hk, 0, 2);
+    pb.add_other(kPhAttn, l);
+    pb.add_other(kPhMerge, l);
+    pb.add_gemm(kEpResid, hq, 1, 2, kPRows, 0, L.g_post);
+    pb.seg(layer_map(l, kMapO), layer_map(l, kMapO), D, 0, 0);
+    pb.add_gemm(kEpSwiGLU, D, 0, 2, kPRows, 1, nullptr);
+    pb.seg(layer_map(l, kMapG), layer_map(l, kMapU), F, 1, 0, true);
+    pb.add_gemm(kEpResid, F, 2, 2, kPRows, 0, l + 1 < c.layers ? m->layers[l + 1].g_in : m->g_final);
+    pb.seg(layer_map(l, kMapD), layer_map(l, kMapD), D, 0, 0);
+  }
+  if (block > 1) {
+    pb.add_gemm(kEpLM, D, 0, 2, kPRows, 1, nullptr);
+    pb.seg(kMapLm, kMapLm, c.vocab, 0, 0, true, true);
+  }
+  pp.trace = m->trace_persist ? m->trace_dev : nullptr;
+  DF_LAUNCH(DFLASH_STAGE_DRAFT_PERSIST, 1, persist_launch(pp, m->sms, c.head_dim, s), "persistent drafter");
+  return DFLASH_OK;
+}
+
 // Tensor maps of every weight matrix, copied once to device memory.
 int32_t build_weight_maps(dflash_model* m) {
   const dflash_config& c = m->cfg;
   const int D = c.hidden, hq = c.n_q_heads * c.head_dim, hk = c.n_kv_heads * c.head_dim, F = c.ffn;
   const size_t mb = tensor_map_bytes();
   const int n = kMapLayer0 + kMapsPerLayer * c.layers;
-  std::vector<unsigned char> host(mb * n);
+  std::vector<unsigned char> host(mb * n), host128(mb * n);
   auto enc = [&](int idx, const void* w, int inner, int rows) {
     if (reinterpret_cast<uintptr_t>(w) % 16) return false;
-    return encode_weight_map(host.data() + mb * idx, w, inner, rows);
+    return encode_weight_map(host.data() + mb * idx, w, inner, rows) &&
+           encode_weight_map(host128.data() + mb * idx, w, inner, rows, 128);
   };
   bool ok = enc(kMapLm, m->lm_head, D, c.vocab) && enc(kMapWc, m->w_c, c.n_target_feats * D, D);
   for (int l = 0; ok && l < c.layers; ++l) {
@@ -401,6 +645,8 @@ int32_t build_weight_maps(dflash_model* m) {
   if (!ok) return fail(DFLASH_ERR_UNSUPPORTED, "could not encode weight tensor maps (16-B aligned weights needed)");
   DF_CUDA(cudaMalloc(&m->tmaps_dev, host.size()), "tensor maps");
   DF_CUDA(cudaMemcpy(m->tmaps_dev, host.data(), host.size(), cudaMemcpyHostToDevice), "tensor maps");
+  DF_CUDA(cudaMalloc(&m->tmaps128_dev, host128.size()), "tensor maps");
+  DF_CUDA(cudaMemcpy(m->tmaps128_dev, host128.data(), host128.size(), cudaMemcpyHostToDevice), "tensor maps");
   return DFLASH_OK;
 }
 
@@ -449,8 +695,11 @@ int32_t dflash_model_create(const dflash_config* cfg, const dflash_weights* w, d
     dflash_model_destroy(m);
     return cuda_fail(e, "model state");
   }
-  if (const char* tr = std::getenv("DFLASH_TRACE_GEMM")) {
-    m->trace_target = std::atol(tr);
+  const char* tr = std::getenv("DFLASH_TRACE_GEMM");
+  const char* tp = std::getenv("DFLASH_TRACE_PERSIST");
+  m->trace_persist = tp && std::strcmp(tp, "0") != 0;
+  if (tr || m->trace_persist) {
+    m->trace_target = tr ? std::atol(tr) : -1;
     if (cudaMalloc(&m->trace_dev, kTraceEntries * sizeof(unsigned long long)) != cudaSuccess ||
         cudaMemset(m->trace_dev, 0, kTraceEntries * sizeof(unsigned long long)) != cudaSuccess) {
       dflash_model_destroy(m);
@@ -465,6 +714,17 @@ int32_t dflash_model_create(const dflash_config* cfg, const dflash_weights* w, d
       dflash_model_destroy(m);
       return rc;
     }
+    const char* pe = std::getenv("DFLASH_PERSIST");
+    if (!(pe && std::strcmp(pe, "0") == 0) && (cfg->head_dim == 64 || cfg->head_dim == 128) &&
+        cfg->vocab % kTileN == 0) {
+      m->persist_stages = persist_stages(cfg->head_dim);
+      e = persist_prepare(cfg->head_dim);
+      if (e != cudaSuccess) {
+        dflash_model_destroy(m);
+        return cuda_fail(e, "persistent kernel set-up");
+      }
+      m->persist = 1;
+    }
   }
   *out = m;
   return DFLASH_OK;
@@ -475,6 +735,7 @@ int32_t dflash_model_destroy(dflash_model* m) {
   if (m->status_dev) cudaFree(m->status_dev);
   if (m->inv_freq_dev) cudaFree(m->inv_freq_dev);
   if (m->tmaps_dev) cudaFree(m->tmaps_dev);
+  if (m->tmaps128_dev) cudaFree(m->tmaps128_dev);
   if (m->trace_dev) cudaFree(m->trace_dev);
   for (cudaEvent_t e : m->prof.ev) cudaEventDestroy(e);
   delete m;
@@ -562,7 +823,13 @@ int32_t dflash_cache_set_lengths(dflash_cache* c, const int32_t* len_host, dflas
 size_t dflash_workspace_bytes(const dflash_model* m, int32_t batch, int32_t capacity, int32_t block_size,
                               int32_t max_inject_rows) {
   if (!m || batch <= 0 || capacity < 0 || block_size < 1 || block_size > m->cfg.max_block || max_inject_rows < 0) return 0;
-  return std::max(plan_ws(m, batch, capacity, 0, max_inject_rows).total, plan_ws(m, batch, capacity, block_size, 0).total);
+  // smaller calls may take the persistent path, whose scratch differs: cover
+  // every block size up to block_size and injections of up to 16 rows too
+  size_t need = plan_ws(m, batch, capacity, 0, max_inject_rows).total;
+  if (max_inject_rows > 0)
+    need = std::max(need, plan_ws(m, batch, capacity, 0, std::min(max_inject_rows, kPRows)).total);
+  for (int b = 1; b <= block_size; ++b) need = std::max(need, plan_ws(m, batch, capacity, b, 0).total);
+  return need;
 }
 
 int32_t dflash_inject_context(const dflash_model* m, dflash_cache* cache, const void* feats, const int32_t* n_new_dev,
@@ -590,7 +857,8 @@ int32_t dflash_inject_context(const dflash_model* m, dflash_cache* cache, const 
   const WsPlan P = plan_ws(m, cache->batch, cache->cap, 0, max_rows);
   if (ws_bytes < P.total) return fail(DFLASH_ERR_WORKSPACE, "workspace %zu bytes < %zu needed", ws_bytes, P.total);
   cudaStream_t s = (cudaStream_t)stream;
-  rc = m->cfg.dtype == DFLASH_DTYPE_F32
+  rc = P.persist ? run_inject_persist(m, cache, feats, n_new_dev, max_rows, static_cast<char*>(workspace), P, s)
+       : m->cfg.dtype == DFLASH_DTYPE_F32
            ? run_inject<float>(m, cache, feats, n_new_dev, max_rows, static_cast<char*>(workspace), P, s)
            : run_inject<__nv_bfloat16>(m, cache, feats, n_new_dev, max_rows, static_cast<char*>(workspace), P, s);
   if (rc) return rc;
@@ -617,6 +885,8 @@ int32_t dflash_draft_block(const dflash_model* m, const dflash_cache* cache, con
   const WsPlan P = plan_ws(m, cache->batch, cache->cap, block_size, 0);
   if (ws_bytes < P.total) return fail(DFLASH_ERR_WORKSPACE, "workspace %zu bytes < %zu needed", ws_bytes, P.total);
   cudaStream_t s = (cudaStream_t)stream;
+  if (P.persist)
+    return run_draft_persist(m, cache, anchor_dev, block_size, draft_dev, logits_dev, static_cast<char*>(workspace), P, s);
   return m->cfg.dtype == DFLASH_DTYPE_F32
              ? run_draft<float>(m, cache, anchor_dev, block_size, draft_dev, logits_dev, static_cast<char*>(workspace), P, s)
              : run_draft<__nv_bfloat16>(m, cache, anchor_dev, block_size, draft_dev, logits_dev,
@@ -775,7 +1045,8 @@ int32_t dflash_inject_context_noalloc(const dflash_model* m, dflash_cache* cache
   rc = noalloc_scratch(m->device, &scratch);
   if (rc) return rc;
   cudaStream_t s = (cudaStream_t)stream;
-  rc = m->cfg.dtype == DFLASH_DTYPE_F32
+  rc = P.persist ? run_inject_persist(m, cache, feats, n_new_dev, max_rows, static_cast<char*>(scratch), P, s)
+       : m->cfg.dtype == DFLASH_DTYPE_F32
            ? run_inject<float>(m, cache, feats, n_new_dev, max_rows, static_cast<char*>(scratch), P, s)
            : run_inject<__nv_bfloat16>(m, cache, feats, n_new_dev, max_rows, static_cast<char*>(scratch), P, s);
   if (rc) return rc;

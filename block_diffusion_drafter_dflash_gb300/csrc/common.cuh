@@ -147,6 +147,7 @@ struct GemmSeg {
   int tile_begin;  // first global tile index of this segment
   int paired;
   int tag;         // meaning chosen by the epilogue (Q/K/V, layer, ...)
+  int tw;          // persistent kernel: features per tile (128 or 256; paired: 128 gate + 128 up)
 };
 
 struct GemmProblem {

@@ -153,10 +153,12 @@ __global__ void __launch_bounds__(kRowThreads) fuse_norm_kernel(const float* y, 
   norm_store(r, g, eps, D, ht + (size_t)row * D, plane, red);
 }
 
-// One CTA: exclusive scan of n_new, per-row (request, position), ctx_len update.
+// One CTA: exclusive scan of n_new, per-row (request, position), ctx_len
+// update; with `rope`, also the (cos, sin) table of every row's position.
 __global__ void __launch_bounds__(1024) inject_prep_kernel(const int32_t* n_new, int32_t* ctx_len, int B,
                                                            int max_rows, int cap, int2* rowinfo, int* zero_ptr,
-                                                           int zero_n, int32_t* status) {
+                                                           int zero_n, int32_t* status, const double* inv_freq,
+                                                           int hd, float2* rope) {
   extern __shared__ int sh[];  // [B] offsets, [B] base positions, [B] accepted counts
   int* off = sh;
   int* base = sh + B;
@@ -206,6 +208,16 @@ __global__ void __launch_bounds__(1024) inject_prep_kernel(const int32_t* n_new,
       if (j < cnt[own]) ri = make_int2(own, base[own] + j);
     }
     rowinfo[r] = ri;
+  }
+  if (rope) {
+    __syncthreads();   // rowinfo of every row written by this CTA
+    const int half = hd >> 1;
+    for (int e = threadIdx.x; e < max_rows * half; e += blockDim.x) {
+      const int r = e / half, i = e - r * half;
+      float sn, cs;
+      rope_sincos(max(rowinfo[r].y, 0), inv_freq, i, &sn, &cs);
+      rope[e] = make_float2(cs, sn);
+    }
   }
 }
 
@@ -319,9 +331,10 @@ cudaError_t fuse_norm_launch(const float* y, const T* g, float eps, const int2* 
 }
 
 cudaError_t inject_prep_launch(const int32_t* n_new, int32_t* ctx_len, int B, int max_rows, int cap, int2* rowinfo,
-                               int* zero_ptr, int zero_n, int32_t* status, cudaStream_t s) {
+                               int* zero_ptr, int zero_n, int32_t* status, cudaStream_t s, const double* inv_freq,
+                               int hd, float2* rope) {
   return launch_pdl(inject_prep_kernel, dim3(1), dim3(1024), 3 * B * sizeof(int), s, n_new, ctx_len, B, max_rows, cap,
-                    rowinfo, zero_ptr, zero_n, status);
+                    rowinfo, zero_ptr, zero_n, status, inv_freq, hd, rope);
 }
 
 cudaError_t argmax_finalize_launch(const unsigned long long* slots, int rows, int32_t* drafts, cudaStream_t s) {

@@ -1,8 +1,9 @@
 // GEMM epilogues of the draft cycle.  Each one consumes a finished fp32 output
 // tile held in shared memory, feature-major: tile[n * ld + m] for the 128
 // output features n of global tile `gtile` and the token rows m0 .. m0+mc-1.
-// Every thread of the CTA calls the functor; consecutive threads take
-// consecutive features so that global stores are coalesced.
+// Threads tid = 0 .. nth-1 (a multiple of 128) call the functor together;
+// consecutive threads take consecutive features so that global stores are
+// coalesced.
 #pragma once
 
 #include "common.cuh"
@@ -14,8 +15,8 @@ struct EpiStoreF32 {
   float* y;
   int ldy;
   __device__ __forceinline__ void operator()(const float* t, int ld, int m0, int mc, int gtile, const GemmSeg&,
-                                             int) const {
-    for (int idx = threadIdx.x; idx < mc * kTileN; idx += blockDim.x) {
+                                             int, int tid, int nth) const {
+    for (int idx = tid; idx < mc * kTileN; idx += nth) {
       int m = idx / kTileN, n = idx % kTileN;
       y[(size_t)(m0 + m) * ldy + (size_t)gtile * kTileN + n] = t[n * ld + m];
     }
@@ -29,10 +30,10 @@ struct EpiResidual {
   float* x;
   int ldx;
   __device__ __forceinline__ void operator()(const float* t, int ld, int m0, int mc, int gtile, const GemmSeg&,
-                                             int) const {
-    const int n = threadIdx.x & (kTileN - 1), step = blockDim.x / kTileN;
+                                             int, int tid, int nth) const {
+    const int n = tid & (kTileN - 1), step = nth / kTileN;
     float* col = x + (size_t)gtile * kTileN + n;
-    for (int mb = threadIdx.x / kTileN; mb < mc; mb += 8 * step) {
+    for (int mb = tid / kTileN; mb < mc; mb += 8 * step) {
       float v[8];
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
@@ -57,8 +58,8 @@ struct EpiSwiGLU {
   int lda;
   size_t plane;
   __device__ __forceinline__ void operator()(const float* t, int ld, int m0, int mc, int, const GemmSeg&,
-                                             int tis) const {
-    for (int idx = threadIdx.x; idx < mc * kHalfN; idx += blockDim.x) {
+                                             int tis, int tid, int nth) const {
+    for (int idx = tid; idx < mc * kHalfN; idx += nth) {
       int m = idx / kHalfN, c = idx % kHalfN;
       float g = t[c * ld + m], u = t[(c + kHalfN) * ld + m];
       float s = g / (1.0f + __expf(-g));
@@ -87,16 +88,16 @@ struct EpiQKV {
   // thread n owns feature n of the tile; the RoPE entries of 8 rows are
   // loaded before any store so that their loads overlap
   __device__ __forceinline__ void operator()(const float* t, int ld, int m0, int mc, int, const GemmSeg& sg,
-                                             int tis) const {
+                                             int tis, int tid, int nth) const {
     const int tag = sg.tag;
     T* dkv = tag == 1 ? kb : vb;
     const int nh = tag == 0 ? nq : nkv, half = hd >> 1;
     const int planes = ActPlanes<T>::n;
-    const int n = threadIdx.x & (kTileN - 1), step = blockDim.x / kTileN;
+    const int n = tid & (kTileN - 1), step = nth / kTileN;
     const int feat = tis * kTileN + n, head = feat / hd, d = feat - head * hd;
     const int i = d < half ? d : d - half;
     const int pn = d < half ? n + half : n - half;
-    for (int mb = threadIdx.x / kTileN; mb < mc; mb += 8 * step) {
+    for (int mb = tid / kTileN; mb < mc; mb += 8 * step) {
       float2 sc[8];
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
@@ -131,15 +132,15 @@ struct EpiInject {
   const float2* rope;
   int layers, nkv, hd, cap;
   __device__ __forceinline__ void operator()(const float* t, int ld, int m0, int mc, int, const GemmSeg& sg,
-                                             int tis) const {
+                                             int tis, int tid, int nth) const {
     const int layer = sg.tag >> 1, is_v = sg.tag & 1, half = hd >> 1;
     T* dst = is_v ? vc : kc;
     const int planes = ActPlanes<T>::n;
-    const int n = threadIdx.x & (kTileN - 1), step = blockDim.x / kTileN;
+    const int n = tid & (kTileN - 1), step = nth / kTileN;
     const int feat = tis * kTileN + n, head = feat / hd, d = feat - head * hd;
     const int i = d < half ? d : d - half;
     const int pn = d < half ? n + half : n - half;
-    for (int mb = threadIdx.x / kTileN; mb < mc; mb += 8 * step) {
+    for (int mb = tid / kTileN; mb < mc; mb += 8 * step) {
       int2 ri[8];
       float2 sc[8];
 #pragma unroll
@@ -169,14 +170,14 @@ struct EpiArgmax {
   float* logits;  // [rows][vocab] or nullptr
   int vocab;
   __device__ __forceinline__ void operator()(const float* t, int ld, int m0, int mc, int gtile, const GemmSeg&,
-                                             int) const {
+                                             int, int tid, int nth) const {
     if (logits) {
-      for (int idx = threadIdx.x; idx < mc * kTileN; idx += blockDim.x) {
+      for (int idx = tid; idx < mc * kTileN; idx += nth) {
         int m = idx / kTileN, n = idx % kTileN;
         logits[(size_t)(m0 + m) * vocab + (size_t)gtile * kTileN + n] = t[n * ld + m];
       }
     }
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    const int lane = tid & 31, warp = tid >> 5, nw = nth >> 5;
     for (int m = warp; m < mc; m += nw) {
       unsigned long long best = 0ull;
       for (int n = lane; n < kTileN; n += 32) {

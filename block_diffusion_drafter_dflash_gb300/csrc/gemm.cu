@@ -101,7 +101,7 @@ __global__ void __launch_bounds__(kSimtThreads) gemm_simt_kernel(const __grid_co
     }
   }
   __syncthreads();
-  epi(st, ld, m0, mc, gtile, sg, tis);
+  epi(st, ld, m0, mc, gtile, sg, tis, threadIdx.x, blockDim.x);
 }
 
 }  // namespace

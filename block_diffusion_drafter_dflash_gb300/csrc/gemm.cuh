@@ -26,10 +26,11 @@ struct GemmPlan {
 GemmPlan plan_gemm(int dtype, int M, int K, int tiles, int sms, int tc, int planes);
 GemmPlan plan_gemm_tc(int M, int K, int tiles, int sms, int planes);
 
-// Tensor maps (CUtensorMap, 128 B each) for the tensor-core kernel: a weight
-// matrix [rows][inner] bf16 read in 64x64 boxes, and an activation matrix
+// Tensor maps (CUtensorMap, 128 B each) for the tensor-core kernels: a weight
+// matrix [rows][inner] bf16 read in 64 x box_rows boxes (64 for the GEMM
+// kernel, 128 for the persistent one), and an activation matrix
 // [rows][row_stride] bf16 read in 64 x box_rows boxes.  128-byte swizzle.
-bool encode_weight_map(void* map, const void* base, int inner, int rows);
+bool encode_weight_map(void* map, const void* base, int inner, int rows, int box_rows = kHalfN);
 bool encode_activation_map(void* map, const void* base, int inner, int rows, int row_stride, int box_rows);
 size_t tensor_map_bytes();
 

@@ -206,7 +206,7 @@ __global__ void __launch_bounds__(128, 1) gemm_tc_kernel(const __grid_constant__
 #pragma unroll
         for (int j = 0; j < C::kChunk; ++j) st[n * ld + j] = v[j];
         __syncthreads();
-        epi(st, ld, m0 + c0, min(C::kChunk, mc - c0), gtile, sg, tis);
+        epi(st, ld, m0 + c0, min(C::kChunk, mc - c0), gtile, sg, tis, threadIdx.x, blockDim.x);
         __syncthreads();
       }
     } else {
@@ -286,7 +286,7 @@ __global__ void __launch_bounds__(128, 1) gemm_tc_kernel(const __grid_constant__
             st[(fq + 3) * ld + r] = acc[i].w;
           }
           __syncthreads();
-          epi(st, ld, m0 + c0, cc, gtile, sg, tis);
+          epi(st, ld, m0 + c0, cc, gtile, sg, tis, threadIdx.x, blockDim.x);
           __syncthreads();
         }
       }
@@ -350,12 +350,12 @@ cudaError_t launch_bn(const GemmProblem& p, const GemmPlan& plan, const Epi& epi
 
 }  // namespace
 
-bool encode_weight_map(void* map, const void* base, int inner, int rows) {
+bool encode_weight_map(void* map, const void* base, int inner, int rows, int box_rows) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)rows};
   cuuint64_t strides[1] = {(cuuint64_t)inner * 2};
-  cuuint32_t box[2] = {64, (cuuint32_t)kHalfN};
+  cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
   cuuint32_t es[2] = {1, 1};
   return fn(static_cast<CUtensorMap*>(map), CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims,
             strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,

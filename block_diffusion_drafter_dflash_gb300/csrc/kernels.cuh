@@ -62,9 +62,11 @@ template <typename T>
 cudaError_t fuse_norm_launch(const float* y, const T* g, float eps, const int2* rowinfo, int rows, int D, T* ht,
                              size_t plane, const double* inv_freq, int hd, float2* rope, cudaStream_t s);
 
-// Row -> (request, position) map of an injection and the ctx_len update.
+// Row -> (request, position) map of an injection and the ctx_len update;
+// with `rope`, also rope[row][hd/2] = (cos, sin) of the row's position.
 cudaError_t inject_prep_launch(const int32_t* n_new, int32_t* ctx_len, int B, int max_rows, int cap,
-                               int2* rowinfo, int* zero_ptr, int zero_n, int32_t* status, cudaStream_t s);
+                               int2* rowinfo, int* zero_ptr, int zero_n, int32_t* status, cudaStream_t s,
+                               const double* inv_freq = nullptr, int hd = 0, float2* rope = nullptr);
 
 // drafts[row] = index packed in slots[row].
 cudaError_t argmax_finalize_launch(const unsigned long long* slots, int rows, int32_t* drafts, cudaStream_t s);

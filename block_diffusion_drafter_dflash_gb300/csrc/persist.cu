@@ -1,0 +1,839 @@
+// Persistent draft-cycle kernel for bf16 drafters at small batch (at most 16
+// token rows per call): every projection of one API call — for the drafter
+// pass Q/K/V, W_O, gate/up and W_D of every layer and the shared LM head, for
+// an injection the fusion W_c and all layers' W_K/W_V — together with the
+// block attention between them, run as the phases of ONE launch with one CTA
+// per SM, separated by grid-wide barriers.
+//
+// Why: at a few token rows each projection streams its weights once from HBM
+// and does almost no arithmetic.  Launched as one kernel per projection, the
+// weight stream drains and refills at every kernel boundary.  Here the TMA
+// producers of each CTA stream the weight tiles of all phases back to back
+// through a shared-memory ring and run ahead across the barriers (weights do
+// not depend on activations), so HBM keeps working while a phase's inputs are
+// still being produced.
+//
+// MMA orientation.  tcgen05.mma costs about the same time per instruction
+// whatever its N (measured on this part: ~133 SM cycles for M=128 and any N
+// up to 256), so the bigger projections (gate/up, the LM head) put weights on
+// the N side, 256 features per instruction (8 KB of weights per K=16 step),
+// and the token rows on the M side: A rows 0..15 are the activations' hi
+// plane, rows 16..31 the lo plane; rows 32..127 of A are never read back
+// (their accumulator rows are discarded), so that A tile overlaps the
+// stage's own weight tile.  Only TMEM lanes 0..31 (warp 4) then hold results.
+// The small projections (Q/K/V, W_O, W_D, fusion, injection) keep weights on
+// the M side (128 features x 32 token columns an instruction): their tiles
+// are split over fewer CTAs and all four compute warps read the accumulator
+// back, which keeps the phase tail short where it matters more than the
+// tensor-pipe rate.  A stage is [4 KB activations][<=32 KB weights] either way.
+//
+// Roles (256 threads):
+//   warps 0, 3      lane 0: weight producers (even / odd stages), TMA of the
+//                   <=256 x 64 weight tile of each stage (128-row boxes)
+//   warp 1          TMEM allocation (512 columns); lane 0 issues tcgen05.mma
+//   warp 2 lane 0   activation producer: TMA of the 16-row hi/lo activation
+//                   tiles of each stage, once every earlier phase is complete
+//   warps 4..7      accumulator read-back, epilogues, stream-K reductions,
+//                   attention and its merge, grid barriers
+// The accumulator of an output tile (<= 256 TMEM columns) is double-buffered
+// so that the MMAs of one tile overlap the epilogue of the previous one.
+//
+// Work split (stream-K): the (tile, 64-column K block) iterations of a
+// projection are divided evenly over the CTAs.  A tile cut between CTAs
+// leaves fp32 partial tiles; the last of its CTAs to finish (atomic ticket)
+// sums them in CTA order and runs the epilogue, so results do not depend on
+// timing.
+//
+// RMSNorm folds into its neighbours: whoever produces a normed input (the
+// residual-stream epilogues, the fusion epilogue, the draft prologue) writes
+// it multiplied by the norm's gain as hi/lo bf16 planes, plus per (128-feature
+// tile, row) sums of squares; the consuming projection multiplies row m of its
+// accumulator by 1/rms(row m) = (sum_t ssq[t][m] / D + eps)^(-1/2).
+//
+// Data one CTA writes and another reads within the launch (sums of squares,
+// partial tiles, Q, attention partials, the residual stream) is read with
+// L2-only loads (L1 is not coherent across SMs); activations read by TMA are
+// published with a generic-to-async proxy fence on both sides of the barrier.
+//
+// Every wait is bounded (mbarriers, grid barrier): on expiry the kernel sets
+// DFLASH_ERR_TIMEOUT in the status word, waits for its own copies in flight,
+// frees its tensor memory and returns.
+#include <cuda.h>
+
+#include <algorithm>
+
+#include "attn_core.cuh"
+#include "gemm.cuh"
+#include "persist.cuh"
+#include "ptx.cuh"
+
+namespace dflash {
+
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kXBytes = 2 * kPRows * 128;         // activation tile: two 16-row planes (A rows 0..31)
+constexpr int kTwMax = 256;                       // features per tile (MMA N)
+constexpr int kWBox = 128 * 128;                  // one 128-row weight box
+constexpr int kStage = kXBytes + 2 * kWBox;       // 36 KB
+constexpr int kLd = kPRows + 1;                   // staging tile pitch (floats)
+constexpr int kTmemCols = 2 * kTwMax;             // double-buffered 256-column accumulator
+constexpr int kAttnStages = 2;
+constexpr long long kBudget = 200000000LL;        // SM cycles (~0.1 s): far beyond any legal wait
+constexpr size_t kSmemMax = 227 * 1024;
+
+template <int HD>
+struct PCfg {
+  static constexpr int kAttnBytes = kAttnStages * attn::TileCfg<HD>::kStageB;
+  static constexpr int kStaging = kTwMax * kLd * 4;   // epilogue staging tile st[256][kLd]
+  static constexpr int kRegion = kAttnBytes > kStaging ? kAttnBytes : kStaging;
+};
+
+struct PBook {
+  uint64_t fullW[kPMaxStages], fullX[kPMaxStages], empty[kPMaxStages];
+  uint64_t accf[2], accfree[2], mma_done;
+  uint32_t tmem;
+  int flag_acc, flag_tk, flag_bar;
+  float rs[kPRows];
+};
+
+static_assert(kStage % 1024 == 0 && kXBytes % 1024 == 0, "stages keep the 1024-byte swizzle alignment");
+
+size_t region_bytes(int hd) { return hd == 64 ? PCfg<64>::kRegion : PCfg<128>::kRegion; }
+
+// ---------------------------------------------------------------- stream-K bookkeeping
+struct Span {
+  int i0, i1;
+};
+
+__device__ __forceinline__ long long phase_iters(const PPhase& ph) { return (long long)ph.tiles * ph.kb; }
+__device__ __forceinline__ int phase_ctas(const PPhase& ph, int G) {
+  return (int)min((long long)G, phase_iters(ph));
+}
+// iterations [i0, i1) of CTA c (CTAs >= phase_ctas get none)
+__device__ __forceinline__ Span cta_span(const PPhase& ph, int G, int c) {
+  const long long W = phase_iters(ph);
+  const int g = phase_ctas(ph, G);
+  if (c >= g) return {0, 0};
+  return {(int)(c * W / g), (int)((c + 1) * W / g)};
+}
+// the CTA whose span holds iteration i
+__device__ __forceinline__ int cta_of(const PPhase& ph, int G, long long i) {
+  const long long W = phase_iters(ph);
+  const int g = phase_ctas(ph, G);
+  return (int)(((i + 1) * g - 1) / W);
+}
+__device__ __forceinline__ int seg_of(const PParams& p, const PPhase& ph, int t) {
+  int s = ph.seg0;
+  while (s + 1 < ph.seg0 + ph.nseg && t >= p.seg[s + 1].tile_begin) ++s;
+  return s;
+}
+
+// ---------------------------------------------------------------- grid barrier
+__device__ __forceinline__ unsigned int ld_acquire(const unsigned int* p) {
+  unsigned int v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Wait until `target` arrivals have been counted (bounded).
+__device__ bool grid_wait(const unsigned int* bar, unsigned int target, int32_t* status) {
+  if (ld_acquire(bar) >= target) return true;
+  const long long t0 = clock64();
+  for (uint32_t it = 1;; ++it) {
+    __nanosleep(32);
+    if (ld_acquire(bar) >= target) return true;
+    if ((it & 63) == 0) {
+      if (*reinterpret_cast<volatile int32_t*>(status) == DFLASH_ERR_TIMEOUT) return false;
+      if (clock64() - t0 > kBudget) {
+        report_status(status, DFLASH_ERR_TIMEOUT);
+        return false;
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ void csync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+// Optional timestamps (globaltimer ns), per (CTA, phase): [0] compute warps
+// start the phase, [1] they are done with it, [2] / [3] first / last weight
+// load issued, [4] activation loads released, [5] first MMA issued, [6] last
+// MMA of the phase committed, [7] SM id (phase 0 only).
+// [8..11]: SM cycles the MMA issuer waited for weights / activations, and the
+// weight producer (even stages) / activation producer waited for free slots.
+// [12..15]: for the CTA's last piece of the phase: accumulator ready, tile
+// staged, epilogue done or partial published, reduction + epilogue done.
+enum { kTrStart = 0, kTrDone, kTrW0, kTrW1, kTrX0, kTrM0, kTrM1, kTrSm, kTrWaitW, kTrWaitX, kTrWaitWEmpty,
+       kTrWaitXEmpty, kTrAcc, kTrStaged, kTrPub, kTrRed, kTrReadBack, kTrCombined, kTrSlots };
+__device__ __forceinline__ void trace_val(const PParams& p, int cta, int pi, int slot, unsigned long long v) {
+  if (p.trace) p.trace[((size_t)cta * kPMaxPhases + pi) * kTrSlots + slot] = v;
+}
+__device__ __forceinline__ void trace_at(const PParams& p, int cta, int pi, int slot) {
+  if (p.trace) trace_val(p, cta, pi, slot, ptx::globaltimer());
+}
+// mbar_wait that adds the cycles spent to `acc` (for the trace); `sleep`:
+// back off between polls (producers, which run ahead of everything else)
+__device__ __forceinline__ bool wait_timed(uint64_t* bar, uint32_t parity, int32_t* status, long long& acc,
+                                           bool sleep = false) {
+  if (ptx::mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  const bool ok = sleep ? ptx::mbar_wait_sleep(bar, parity, kBudget, status) : ptx::mbar_wait(bar, parity, kBudget, status);
+  acc += clock64() - t0;
+  return ok;
+}
+
+struct ComputeSync {
+  __device__ __forceinline__ void operator()() const { csync(); }
+};
+
+// Wait for the loads of the last use of every ring slot that this producer
+// filled (iterations of parity `par`, or all when par < 0); bounded, and they
+// were issued, so they complete.
+__device__ void drain_slots(uint64_t* full, int issued, int S, int par, int32_t* status) {
+  for (int j = max(0, issued - S); j < issued; ++j)
+    if (par < 0 || (j & 1) == par) ptx::mbar_wait(full + (j % S), (j / S) & 1, kBudget, status);
+}
+
+// ---------------------------------------------------------------- producers and MMA
+// Weight rows of box h (128 rows) of tile `tis` of a segment: unpaired tiles
+// are tw consecutive rows of w0; a paired tile is 128 rows of w0 (SwiGLU gate)
+// then the same 128 rows of w1 (up).
+__device__ __forceinline__ int box_row(const GemmSeg& sg, int tis, int h) {
+  return sg.paired ? 128 * tis : sg.tw * tis + 128 * h;
+}
+
+// Two weight producers (warps 0 and 3) take the even and odd ring iterations:
+// one issuing thread sustains only ~5 TB/s of TMA traffic across the device
+// (its wait-and-issue loop, not bytes in flight, is the limit), two reach the
+// HBM copy rate.  The ring depth is even, so each slot always belongs to the
+// same producer.
+__device__ void weight_producer(const PParams& p, PBook* bk, uint8_t* ring, int G, int cta, int par) {
+  const int S = p.stages;
+  const uint64_t pol = ptx::policy_evict_first();
+  int it = 0;
+  for (int pi = 0; pi < p.nphase; ++pi) {
+    const PPhase& ph = p.ph[pi];
+    if (ph.kind != kPhGemm) continue;
+    const Span sp = cta_span(ph, G, cta);
+    long long we = 0;
+    for (int i = sp.i0; i < sp.i1; ++i, ++it) {
+      if ((it & 1) != par) continue;
+      const int s = it % S;
+      if (it >= S && !wait_timed(&bk->empty[s], ((it / S) & 1) ^ 1, p.status, we, true)) goto done;
+      if (i - sp.i0 < 2) trace_at(p, cta, pi, kTrW0);
+      if (i + 2 >= sp.i1) trace_at(p, cta, pi, kTrW1);
+      {
+        const int t = i / ph.kb, kx = (i - t * ph.kb) * 64;
+        const GemmSeg& sg = p.seg[seg_of(p, ph, t)];
+        const int tis = t - sg.tile_begin, nbox = sg.tw / 128;
+        uint8_t* w = ring + (size_t)s * kStage + kXBytes;
+        ptx::mbar_arrive_expect_tx(&bk->fullW[s], nbox * kWBox);
+        for (int h = 0; h < nbox; ++h)
+          ptx::tma_load_2d(w + h * kWBox, p.wmaps + ((sg.paired && h) ? sg.map1 : sg.map0), &bk->fullW[s], kx,
+                           box_row(sg, tis, h), pol);
+      }
+    }
+    if (par == 0) trace_val(p, cta, pi, kTrWaitWEmpty, we);
+  }
+done:
+  drain_slots(bk->fullW, it, S, par, p.status);
+}
+
+// The activation producer (lane 0 of warp 2): the hi and lo 16-row tiles of
+// each stage's 64-column K block, A rows 0..15 and 16..31.
+__device__ void activation_producer(const PParams& p, PBook* bk, uint8_t* ring, int G, int cta) {
+  const int S = p.stages;
+  const uint64_t pol = ptx::policy_evict_last();
+  int it = 0;
+  long long wx = 0;
+  for (int pi = 0; pi < p.nphase; ++pi) {
+    const PPhase& ph = p.ph[pi];
+    if (ph.kind != kPhGemm) continue;
+    const Span sp = cta_span(ph, G, cta);
+    if (sp.i0 == sp.i1) continue;
+    // the phase's activations exist once every earlier phase is complete
+    if (pi > 0 && !grid_wait(p.bar, (unsigned)pi * (unsigned)G, p.status)) goto done;
+    ptx::fence_proxy_async_global();
+    trace_at(p, cta, pi, kTrX0);
+    wx = 0;
+    for (int i = sp.i0; i < sp.i1; ++i, ++it) {
+      const int s = it % S;
+      if (it >= S && !wait_timed(&bk->empty[s], ((it / S) & 1) ^ 1, p.status, wx, true)) goto done;
+      const int kx = (i % ph.kb) * 64;
+      uint8_t* x = ring + (size_t)s * kStage;
+      ptx::mbar_arrive_expect_tx(&bk->fullX[s], ph.planes * kPRows * 128);
+      for (int pl = 0; pl < ph.planes; ++pl)
+        ptx::tma_load_2d(x + pl * kPRows * 128, &p.xmap[ph.xmap], &bk->fullX[s], kx, pl * ph.prow, pol);
+    }
+    trace_val(p, cta, pi, kTrWaitXEmpty, wx);
+  }
+done:
+  drain_slots(bk->fullX, it, S, -1, p.status);
+}
+
+__device__ void mma_issuer(const PParams& p, PBook* bk, uint8_t* ring, uint32_t tmem, int G, int cta) {
+  const int S = p.stages;
+  int it = 0, seq = 0;
+  bool any = false;
+  for (int pi = 0; pi < p.nphase; ++pi) {
+    const PPhase& ph = p.ph[pi];
+    if (ph.kind != kPhGemm) continue;
+    const Span sp = cta_span(ph, G, cta);
+    long long ww = 0, wxx = 0;
+    for (int i = sp.i0; i < sp.i1;) {
+      const int t = i / ph.kb, k0 = i - t * ph.kb, k1 = min(sp.i1 - t * ph.kb, ph.kb);
+      const bool wide = p.seg[seg_of(p, ph, t)].tw == kTwMax;   // weights on N
+      const uint32_t idesc = wide ? ptx::idesc_bf16_f32(128, kTwMax) : ptx::idesc_bf16_f32(128, kPRows * ph.planes);
+      const int buf = seq & 1, use = seq >> 1;
+      if (use >= 1 && !ptx::mbar_wait(&bk->accfree[buf], (use - 1) & 1, kBudget, p.status)) goto done;
+      ptx::tc_fence_after();
+      const uint32_t d = tmem + buf * kTwMax;
+      for (int kk = k0; kk < k1; ++kk, ++it) {
+        const int s = it % S;
+        if (!wait_timed(&bk->fullW[s], (it / S) & 1, p.status, ww) ||
+            !wait_timed(&bk->fullX[s], (it / S) & 1, p.status, wxx))
+          goto done;
+        ptx::tc_fence_after();
+        if (i == sp.i0 && kk == k0) trace_at(p, cta, pi, kTrM0);
+        uint8_t* st = ring + (size_t)s * kStage;
+        const uint64_t xd = ptx::smem_desc_sw128(st);             // activations (token rows 0..31)
+        const uint64_t wd = ptx::smem_desc_sw128(st + kXBytes);   // weights (tw rows)
+        const uint64_t ad = wide ? xd : wd, bd = wide ? wd : xd;
+#pragma unroll
+        for (int k = 0; k < 4; ++k)   // 4 x K=16 per 64-column stage; +32 B per step inside the swizzle row
+          ptx::mma_bf16(d, ad + 2 * k, bd + 2 * k, idesc, (kk > k0 || k > 0) ? 1u : 0u);
+        ptx::mma_commit(&bk->empty[s]);
+        any = true;
+      }
+      ptx::mma_commit(&bk->accf[buf]);
+      ++seq;
+      i = t * ph.kb + k1;
+      if (i == sp.i1) trace_at(p, cta, pi, kTrM1);
+    }
+    trace_val(p, cta, pi, kTrWaitW, ww);
+    trace_val(p, cta, pi, kTrWaitX, wxx);
+  }
+done:
+  if (any) {   // every MMA issued has finished before the tensor memory is freed
+    ptx::mma_commit(&bk->mma_done);
+    ptx::mbar_wait(&bk->mma_done, 0, kBudget, p.status);
+  }
+}
+
+// ---------------------------------------------------------------- epilogues
+// The staged tile: st[n * kLd + m] for features n < tw of the tile, rows m < M.
+
+// 128 features starting at feature f0 of the output (rows of x / u):
+// out = acc (+ x): x keeps out, planes u keep out * gain, ssq[f0/128][m] = sum
+// of out^2 over the 128 features.  Thread ct owns feature f0 + ct.
+__device__ void epi_norm_out(const PParams& p, const PPhase& ph, int f0, float* st, int ct) {
+  const int f = f0 + ct;
+  const float g = __bfloat162float(ph.gain[f]);
+  const bool resid = ph.epi == kEpResid;
+  float v[kPRows];
+#pragma unroll
+  for (int m = 0; m < kPRows; ++m) v[m] = (m < p.M && resid) ? __ldcg(p.x + (size_t)m * p.D + f) : 0.f;
+#pragma unroll
+  for (int m = 0; m < kPRows; ++m) {
+    if (m >= p.M) break;
+    const float o = v[m] + st[ct * kLd + m];
+    if (resid) p.x[(size_t)m * p.D + f] = o;
+    put_act(p.u, p.u_plane, (size_t)m * p.D + f, o * g);
+    st[ct * kLd + m] = o * o;
+  }
+  csync();
+  // row m = ct / 8 sums features ct%8, ct%8 + 8, ... then across the 8 lanes
+  const int m = ct >> 3, part = ct & 7;
+  float a = 0.f;
+  if (m < p.M)
+    for (int n = part; n < 128; n += 8) a += st[n * kLd + m];
+  a += __shfl_xor_sync(0xffffffffu, a, 1);
+  a += __shfl_xor_sync(0xffffffffu, a, 2);
+  a += __shfl_xor_sync(0xffffffffu, a, 4);
+  if (part == 0 && m < p.M) p.ssq[(f0 / 128) * kPRows + m] = a;
+  csync();
+}
+
+// silu(gate) * up for a paired tile (features 0..127 gate, 128..255 up) into
+// the W_D GEMM's activation planes.
+__device__ void epi_swiglu(const PParams& p, int tis, const float* st, int ct) {
+  const EpiSwiGLU<__nv_bfloat16>& e = p.swiglu;
+  for (int idx = ct; idx < p.M * 128; idx += 128) {
+    const int m = idx >> 7, c = idx & 127;
+    const float g = st[c * kLd + m], u = st[(128 + c) * kLd + m];
+    put_act(e.a, e.plane, (size_t)m * e.lda + (size_t)tis * 128 + c, g / (1.0f + __expf(-g)) * u);
+  }
+}
+
+// Argmax of the tile's logits (features f0 .. f0+tw-1 below the vocabulary)
+// for every mask row (block position >= 1) into slots[row]; optional logits.
+__device__ void epi_lm(const PParams& p, int f0, int tw, const float* st, int ct) {
+  const int lane = ct & 31, w = ct >> 5;
+  const int nv = min(tw, p.vocab - f0);
+  for (int m = w; m < p.M; m += 4) {
+    if (m % p.block == 0) continue;
+    unsigned long long best = 0ull;
+    for (int n = lane; n < nv; n += 32) {
+      const unsigned long long k = pack_argmax(st[n * kLd + m], f0 + n);
+      best = k > best ? k : best;
+    }
+    for (int o = 16; o; o >>= 1) {
+      const unsigned long long other = __shfl_xor_sync(0xffffffffu, best, o);
+      best = other > best ? other : best;
+    }
+    if (lane == 0) atomicMax(p.slots + m, best);
+  }
+  if (p.logits) {
+    for (int idx = ct; idx < p.M * tw; idx += 128) {
+      const int m = idx / tw, n = idx - m * tw;
+      const int b = m / p.block, k = m - b * p.block;
+      if (k == 0 || n >= nv) continue;
+      p.logits[(size_t)(b * (p.block - 1) + k - 1) * p.vocab + (size_t)f0 + n] = st[n * kLd + m];
+    }
+  }
+}
+
+// Epilogue of output tile t (all 128 compute threads; the tile is staged).
+__device__ void run_epilogue(const PParams& p, const PPhase& ph, int t, float* st, int ct) {
+  const GemmSeg& sg = p.seg[seg_of(p, ph, t)];
+  const int tis = t - sg.tile_begin, halves = sg.tw / 128;
+  switch (ph.epi) {
+    case kEpFuse:
+    case kEpResid:   // one segment starting at feature 0
+      for (int h = 0; h < halves; ++h) epi_norm_out(p, ph, tis * sg.tw + h * 128, st + h * 128 * kLd, ct);
+      break;
+    case kEpQKV:
+      for (int h = 0; h < halves; ++h) p.qkv(st + h * 128 * kLd, kLd, 0, p.M, 0, sg, tis * halves + h, ct, 128);
+      break;
+    case kEpInject:
+      for (int h = 0; h < halves; ++h) p.inject(st + h * 128 * kLd, kLd, 0, p.M, 0, sg, tis * halves + h, ct, 128);
+      break;
+    case kEpSwiGLU: epi_swiglu(p, tis, st, ct); break;
+    default: epi_lm(p, tis * sg.tw, sg.tw, st, ct); break;
+  }
+}
+
+// One projection phase, compute-warp side.  Returns false on a timeout.
+__device__ bool gemm_phase(const PParams& p, const PPhase& ph, int pi, PBook* bk, float* st, uint32_t tmem, int G,
+                           int cta, int ct, int& seq) {
+  if (ph.scaled) {
+    const int m = ct >> 3, part = ct & 7, nt = p.D / 128;
+    float a = 0.f;
+    if (m < p.M)
+      for (int t = part; t < nt; t += 8) a += __ldcg(p.ssq + t * kPRows + m);
+    a += __shfl_xor_sync(0xffffffffu, a, 1);
+    a += __shfl_xor_sync(0xffffffffu, a, 2);
+    a += __shfl_xor_sync(0xffffffffu, a, 4);
+    if (part == 0) bk->rs[m] = m < p.M ? rsqrtf(a / (float)p.D + p.eps) : 0.f;
+  }
+  csync();
+  const Span sp = cta_span(ph, G, cta);
+  const int first_tile = sp.i0 / max(ph.kb, 1);
+  for (int i = sp.i0; i < sp.i1;) {
+    const int t = i / ph.kb, k0 = i - t * ph.kb, k1 = min(sp.i1 - t * ph.kb, ph.kb);
+    i = t * ph.kb + k1;
+    const int tw = p.seg[seg_of(p, ph, t)].tw;
+    const int buf = seq & 1, use = seq >> 1;
+    ++seq;
+    const bool last = i == sp.i1;
+    if (ct == 0) bk->flag_acc = ptx::mbar_wait(&bk->accf[buf], use & 1, kBudget, p.status);
+    if (ct == 0 && last) trace_at(p, cta, pi, kTrAcc);
+    csync();
+    if (!bk->flag_acc) return false;
+    const uint32_t tb = tmem + buf * kTwMax;
+    if (tw == kTwMax) {
+      // weights on N: token rows in TMEM lanes 0..15 (hi) and 16..31 (lo), warp 4
+      if (ct < 32) {
+        ptx::tc_fence_after();
+        const float sc = (ct < p.M && ph.scaled) ? bk->rs[ct] : 1.f;
+        for (int c0 = 0; c0 < kTwMax; c0 += 64) {
+          float v[64];
+          ptx::tmem_ld32x2(tb + c0, tb + c0 + 32, v);
+          if (ph.planes == 2) {
+#pragma unroll
+            for (int j = 0; j < 64; ++j) v[j] += __shfl_xor_sync(0xffffffffu, v[j], 16);
+          }
+          if (ct < p.M) {
+#pragma unroll
+            for (int j = 0; j < 64; ++j) st[(c0 + j) * kLd + ct] = v[j] * sc;
+          }
+        }
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (ct == 0) ptx::mbar_arrive(&bk->accfree[buf]);
+        if (ct == 0 && last) trace_at(p, cta, pi, kTrReadBack);
+      }
+    } else {
+      // weights on M: feature ct in TMEM lane ct (warp q owns lanes 32q..),
+      // token columns 0..15 (hi) and 16..31 (lo)
+      ptx::tc_fence_after();
+      float v[kPRows];
+      const uint32_t ta = tb + (static_cast<uint32_t>((ct >> 5) * 32) << 16);
+      ptx::tmem_ld16(ta, v);
+      if (ph.planes == 2) {
+        float w[kPRows];
+        ptx::tmem_ld16(ta + kPRows, w);
+#pragma unroll
+        for (int m = 0; m < kPRows; ++m) v[m] += w[m];
+      }
+      ptx::tc_fence_before();
+#pragma unroll
+      for (int m = 0; m < kPRows; ++m) st[ct * kLd + m] = ph.scaled ? v[m] * bk->rs[m] : v[m];
+    }
+    csync();
+    if (tw != kTwMax) {   // every compute thread has read its lane
+      if (ct == 0) ptx::mbar_arrive(&bk->accfree[buf]);
+    }
+    if (ct == 0 && last) trace_at(p, cta, pi, kTrStaged);
+
+    if (k0 == 0 && k1 == ph.kb) {   // the whole tile is here
+      run_epilogue(p, ph, t, st, ct);
+      csync();
+      if (ct == 0 && last) trace_at(p, cta, pi, kTrPub);
+      continue;
+    }
+    // partial tile [16 rows][256 features]: publish it; the last CTA of the tile
+    // reduces.  Thread ct moves features 4(ct%64)..+3 of rows ct/64, ct/64+2, ...
+    const int fq = 4 * (ct & 63), r0 = ct >> 6;
+    {
+      float* dst = p.partial + (size_t)(cta * 2 + (t == first_tile ? 0 : 1)) * (kPRows * kTwMax);
+      if (fq < tw)
+        for (int m = r0; m < p.M; m += 2)
+          *reinterpret_cast<float4*>(dst + m * kTwMax + fq) =
+              make_float4(st[fq * kLd + m], st[(fq + 1) * kLd + m], st[(fq + 2) * kLd + m], st[(fq + 3) * kLd + m]);
+    }
+    __threadfence();
+    csync();
+    const int cf = cta_of(ph, G, (long long)t * ph.kb), cl = cta_of(ph, G, (long long)(t + 1) * ph.kb - 1);
+    if (ct == 0) {
+      const int old = atomicAdd(p.tickets + t, 1);
+      bk->flag_tk = old == cl - cf;
+    }
+    csync();
+    if (ct == 0 && last) trace_at(p, cta, pi, kTrPub);
+    if (!bk->flag_tk) continue;
+    __threadfence();
+    if (fq < tw) {
+      const long long W = phase_iters(ph);
+      const int g = phase_ctas(ph, G);
+      constexpr int kR = kPRows / 2;   // rows of this thread
+      float4 acc[kR];
+#pragma unroll
+      for (int j = 0; j < kR; ++j) acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+      // pieces in CTA order, three at a time so that their loads overlap
+      for (int c = cf; c <= cl; c += 3) {
+        float4 a[3][kR];
+#pragma unroll
+        for (int u = 0; u < 3; ++u) {
+          const int cu = c + u <= cl ? c + u : c;
+          const float* src =
+              p.partial + (size_t)(cu * 2 + ((int)((cu * W / g) / ph.kb) == t ? 0 : 1)) * (kPRows * kTwMax) + fq;
+#pragma unroll
+          for (int j = 0; j < kR; ++j) {
+            const int m = r0 + 2 * j;
+            a[u][j] = (c + u <= cl && m < p.M) ? __ldcg(reinterpret_cast<const float4*>(src + m * kTwMax))
+                                               : make_float4(0.f, 0.f, 0.f, 0.f);
+          }
+        }
+#pragma unroll
+        for (int j = 0; j < kR; ++j)
+#pragma unroll
+          for (int u = 0; u < 3; ++u) {
+            acc[j].x += a[u][j].x;
+            acc[j].y += a[u][j].y;
+            acc[j].z += a[u][j].z;
+            acc[j].w += a[u][j].w;
+          }
+      }
+#pragma unroll
+      for (int j = 0; j < kR; ++j) {
+        const int m = r0 + 2 * j;
+        if (m < p.M) {
+          st[fq * kLd + m] = acc[j].x;
+          st[(fq + 1) * kLd + m] = acc[j].y;
+          st[(fq + 2) * kLd + m] = acc[j].z;
+          st[(fq + 3) * kLd + m] = acc[j].w;
+        }
+      }
+    }
+    csync();
+    run_epilogue(p, ph, t, st, ct);
+    csync();
+    if (ct == 0) p.tickets[t] = 0;
+    if (ct == 0 && last) trace_at(p, cta, pi, kTrRed);
+  }
+  return true;
+}
+
+// Attention of item = this CTA: (request, kv head, key chunk); partial
+// (unnormalised output, max, sum) rows to global memory.
+template <int HD>
+__device__ void attn_phase(const PParams& p, const PPhase& ph, uint8_t* region, int cta, int ct) {
+  const AttnParams& ap = p.attn;
+  const int nch = ap.splits;
+  const int items = ap.B * ap.nkv * nch;
+  if (cta >= items) return;
+  const int b = cta / (ap.nkv * nch), r = cta - b * ap.nkv * nch, kvh = r / nch, ch = r - kvh * nch;
+  const int c = ap.ctx_len[b], total = c + ap.block;
+  const int per = (total + nch - 1) / nch;
+  const int chunk = (per + attn::kKeys - 1) / attn::kKeys * attn::kKeys;
+  const int j0 = min(total, ch * chunk), j1 = min(total, j0 + chunk);
+  AttnParams a = ap;
+  a.layer = ph.layer;
+  attn::AttnAcc<HD> acc;
+  attn::attn_chunk<HD, 4, kAttnStages>(a, b, kvh, c, j0, j1, region, ct, ComputeSync{}, acc);
+  const int rows = (ap.nq / ap.nkv) * ap.block;
+  const int lane = ct & 31, w = ct >> 5, g = lane >> 2, t = lane & 3;
+  const int r_lo = w * 16 + g, r_hi = r_lo + 8;
+  float* op = ap.opart + (size_t)cta * kPAttnRows * HD;
+#pragma unroll
+  for (int nb = 0; nb < HD / 8; ++nb) {
+    if (r_lo < rows)
+      *reinterpret_cast<float2*>(op + r_lo * HD + nb * 8 + 2 * t) = make_float2(acc.o[nb][0], acc.o[nb][1]);
+    if (r_hi < rows)
+      *reinterpret_cast<float2*>(op + r_hi * HD + nb * 8 + 2 * t) = make_float2(acc.o[nb][2], acc.o[nb][3]);
+  }
+  if (t == 0) {
+    if (r_lo < rows) ap.ml[(size_t)cta * kPAttnRows + r_lo] = make_float2(acc.m_a, acc.l_a);
+    if (r_hi < rows) ap.ml[(size_t)cta * kPAttnRows + r_hi] = make_float2(acc.m_b, acc.l_b);
+  }
+}
+
+// Merge the key chunks of every output row (request, q head, block row) into
+// the W_O GEMM's activation planes; one warp per row.
+template <int HD>
+__device__ void merge_phase(const PParams& p, int G, int cta, int ct) {
+  const AttnParams& ap = p.attn;
+  const int nch = ap.splits, Gq = ap.nq / ap.nkv;
+  const int lane = ct & 31, w = ct >> 5;
+  const int total = ap.B * ap.nq * ap.block;
+  __nv_bfloat16* out = static_cast<__nv_bfloat16*>(ap.out);
+  for (int idx = cta * 4 + w; idx < total; idx += G * 4) {
+    const int b = idx / (ap.nq * ap.block), rem = idx - b * ap.nq * ap.block;
+    const int qh = rem / ap.block, k = rem - qh * ap.block;
+    const int kvh = qh / Gq, r = (qh - kvh * Gq) * ap.block + k;
+    const size_t item0 = ((size_t)b * ap.nkv + kvh) * nch;
+    float M = attn::kNegBig;
+    for (int ch = 0; ch < nch; ++ch) {
+      const float2 ml = __ldcg(ap.ml + (item0 + ch) * kPAttnRows + r);
+      if (ml.y > 0.f) M = fmaxf(M, ml.x);
+    }
+    float L = 0.f, o[HD / 32];
+#pragma unroll
+    for (int j = 0; j < HD / 32; ++j) o[j] = 0.f;
+    for (int ch = 0; ch < nch; ++ch) {
+      const float2 ml = __ldcg(ap.ml + (item0 + ch) * kPAttnRows + r);
+      if (!(ml.y > 0.f)) continue;
+      const float wgt = exp2f(ml.x - M);
+      L += wgt * ml.y;
+      const float* src = ap.opart + ((item0 + ch) * kPAttnRows + r) * HD;
+#pragma unroll
+      for (int j = 0; j < HD / 32; ++j) o[j] += wgt * __ldcg(src + lane + 32 * j);
+    }
+    const float inv = 1.f / L;
+    const size_t obase = ((size_t)b * ap.block + k) * ap.nq * HD + (size_t)qh * HD;
+#pragma unroll
+    for (int j = 0; j < HD / 32; ++j) put_act(out, ap.out_plane, obase + lane + 32 * j, o[j] * inv);
+  }
+}
+
+__device__ void compute_warps(const PParams& p, PBook* bk, uint8_t* region, uint32_t tmem, int G, int cta) {
+  const int ct = threadIdx.x - 128;
+  float* st = reinterpret_cast<float*>(region);
+  int seq = 0;
+  for (int pi = 0; pi < p.nphase; ++pi) {
+    const PPhase& ph = p.ph[pi];
+    if (ct == 0) trace_at(p, cta, pi, kTrStart);
+    if (ph.kind == kPhGemm) {
+      if (!gemm_phase(p, ph, pi, bk, st, tmem, G, cta, ct, seq)) return;
+    } else if (ph.kind == kPhAttn) {
+      if (p.attn.hd == 64)
+        attn_phase<64>(p, ph, region, cta, ct);
+      else
+        attn_phase<128>(p, ph, region, cta, ct);
+    } else {
+      if (p.attn.hd == 64)
+        merge_phase<64>(p, G, cta, ct);
+      else
+        merge_phase<128>(p, G, cta, ct);
+    }
+    // ---- grid barrier: this CTA's writes of the phase are published
+    ptx::fence_proxy_async_global();
+    __threadfence();
+    csync();
+    if (ct == 0) trace_at(p, cta, pi, kTrDone);
+    if (pi + 1 < p.nphase) {
+      if (ct == 0) {
+        atomicAdd(p.bar, 1u);
+        bk->flag_bar = grid_wait(p.bar, (unsigned)(pi + 1) * (unsigned)G, p.status);
+      }
+      csync();
+      if (!bk->flag_bar) return;
+    } else {
+      // the last CTA to finish reads the argmax slots out
+      if (ct == 0) bk->flag_bar = atomicAdd(p.bar, 1u) == (unsigned)p.nphase * (unsigned)G - 1u;
+      csync();
+      if (bk->flag_bar && p.drafts) {
+        __threadfence();
+        for (int m = ct; m < p.M; m += 128) {
+          const int b = m / p.block, k = m - b * p.block;
+          if (k > 0) p.drafts[b * (p.block - 1) + k - 1] = unpack_argmax_index(__ldcg(p.slots + m));
+        }
+      }
+    }
+  }
+}
+
+template <int HD>
+__global__ void __launch_bounds__(kThreads, 1) persist_kernel(const __grid_constant__ PParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int S = p.stages;
+  uint8_t* ring = smem;
+  uint8_t* region = smem + (size_t)S * kStage;
+  PBook* bk = reinterpret_cast<PBook*>(region + PCfg<HD>::kRegion);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int G = gridDim.x, cta = blockIdx.x;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      ptx::mbar_init(&bk->fullW[s], 1);
+      ptx::mbar_init(&bk->fullX[s], 1);
+      ptx::mbar_init(&bk->empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      ptx::mbar_init(&bk->accf[b], 1);
+      ptx::mbar_init(&bk->accfree[b], 1);
+    }
+    ptx::mbar_init(&bk->mma_done, 1);
+    ptx::fence_mbar_init();
+    for (int i = 0; i < kPXMaps; ++i) ptx::prefetch_tmap(&p.xmap[i]);
+  }
+  if (warp == 1) ptx::tmem_alloc(&bk->tmem, kTmemCols);
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = bk->tmem;
+  griddep_trigger();
+  if (threadIdx.x == 0) trace_val(p, cta, 0, kTrSm, ptx::smid());
+
+  if (warp == 0 || warp == 3) {
+    // weights are constant: streaming starts before the previous kernel has finished
+    if (lane == 0) weight_producer(p, bk, ring, G, cta, warp == 0 ? 0 : 1);
+    __syncwarp();
+  } else if (warp == 1) {
+    if (lane == 0) mma_issuer(p, bk, ring, tmem, G, cta);
+    __syncwarp();
+  } else if (warp == 2) {
+    griddep_wait();
+    if (lane == 0) activation_producer(p, bk, ring, G, cta);
+    __syncwarp();
+  } else if (warp >= 4) {
+    griddep_wait();
+    compute_warps(p, bk, region, tmem, G, cta);
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// ---------------------------------------------------------------- draft prologue
+__global__ void __launch_bounds__(256) persist_draft_prep_kernel(
+    const __nv_bfloat16* embed, const int32_t* anchor, int mask_id, int vocab, int block, int D,
+    const __nv_bfloat16* g, float* x, __nv_bfloat16* u, size_t u_plane, float* ssq, unsigned long long* slots,
+    int* zero, int nzero, int32_t* status, const int32_t* ctx_len, const double* inv_freq, int hd, float2* rope) {
+  griddep_wait();
+  griddep_trigger();
+  const int row = blockIdx.x, b = row / block, k = row - b * block;
+  if (row == 0)
+    for (int i = threadIdx.x; i < nzero; i += blockDim.x) zero[i] = 0;
+  if (threadIdx.x == 0) slots[row] = 0ull;
+  const int pos = ctx_len[b] + k;
+  for (int i = threadIdx.x; i < (hd >> 1); i += blockDim.x) {
+    float sn, cs;
+    rope_sincos(pos, inv_freq, i, &sn, &cs);
+    rope[(size_t)row * (hd >> 1) + i] = make_float2(cs, sn);
+  }
+  int tok = k == 0 ? anchor[b] : mask_id;
+  if (tok < 0 || tok >= vocab) {   // an anchor outside the vocabulary: flag it, read row 0
+    if (threadIdx.x == 0) report_status(status, DFLASH_ERR_INVALID_ARG);
+    tok = 0;
+  }
+  const __nv_bfloat16* e = embed + (size_t)tok * D;
+  // warp w covers features [128w + 1024j, +128): one tile of the sums of squares
+  for (int f = threadIdx.x * 4; f < D; f += blockDim.x * 4) {
+    const float4 v = load4(e + f), gg = load4(g + f);
+    *reinterpret_cast<float4*>(x + (size_t)row * D + f) = v;
+    put_act4(u, u_plane, (size_t)row * D + f, make_float4(v.x * gg.x, v.y * gg.y, v.z * gg.z, v.w * gg.w));
+    float sq = v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+    for (int o = 16; o; o >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, o);
+    if ((threadIdx.x & 31) == 0) ssq[(f / kTileN) * kPRows + row] = sq;
+  }
+}
+
+template <int HD>
+cudaError_t launch_hd(const PParams& p, int grid, cudaStream_t s) {
+  const size_t smem = persist_smem(p.stages, HD);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  // programmatic launch on top of the cooperative one where the runtime takes both
+  static int pdl_ok = 1;
+  cfg.numAttrs = (pdl_enabled() && pdl_ok) ? 2 : 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, persist_kernel<HD>, p);
+  if (e != cudaSuccess && cfg.numAttrs == 2) {
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(s, &cs) == cudaSuccess && cs == cudaStreamCaptureStatusNone) {
+      (void)cudaGetLastError();
+      pdl_ok = 0;
+      cfg.numAttrs = 1;
+      e = cudaLaunchKernelEx(&cfg, persist_kernel<HD>, p);
+    }
+  }
+  return e;
+}
+
+}  // namespace
+
+int persist_stages(int hd) {   // even: the two weight producers own alternate slots
+  const size_t fixed = 1024 + region_bytes(hd) + sizeof(PBook);
+  return std::min<int>(kPMaxStages, (int)((kSmemMax - fixed) / kStage)) & ~1;
+}
+
+size_t persist_smem(int stages, int hd) { return 1024 + (size_t)stages * kStage + region_bytes(hd) + sizeof(PBook); }
+
+cudaError_t persist_prepare(int hd) {
+  const int S = persist_stages(hd);
+  if (hd == 64)
+    return cudaFuncSetAttribute(persist_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)persist_smem(S, 64));
+  return cudaFuncSetAttribute(persist_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)persist_smem(S, 128));
+}
+
+cudaError_t persist_launch(const PParams& p, int grid, int hd, cudaStream_t s) {
+  if (p.stages < 2 || p.stages > kPMaxStages || (p.stages & 1) || p.M < 1 || p.M > kPRows || p.nphase < 1 || p.nphase > kPMaxPhases)
+    return cudaErrorInvalidValue;
+  return hd == 64 ? launch_hd<64>(p, grid, s) : launch_hd<128>(p, grid, s);
+}
+
+cudaError_t persist_draft_prep_launch(const __nv_bfloat16* embed, const int32_t* anchor, int mask_id, int vocab,
+                                      int B, int block, int D, const __nv_bfloat16* g, float* x, __nv_bfloat16* u,
+                                      size_t u_plane, float* ssq, unsigned long long* slots, int* zero, int nzero,
+                                      int32_t* status, const int32_t* ctx_len, const double* inv_freq, int hd,
+                                      float2* rope, cudaStream_t s) {
+  return launch_pdl(persist_draft_prep_kernel, dim3(B * block), dim3(256), 0, s, embed, anchor, mask_id, vocab, block,
+                    D, g, x, u, u_plane, ssq, slots, zero, nzero, status, ctx_len, inv_freq, hd, rope);
+}
+
+}  // namespace dflash

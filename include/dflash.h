@@ -161,8 +161,8 @@ int32_t dflash_cache_set_lengths(dflash_cache* cache, const int32_t* ctx_len_hos
 
 /* --- workspace ----------------------------------------------------------------
  * Bytes of caller-owned device scratch that dflash_inject_context (with up to
- * `max_inject_rows` rows) and dflash_draft_block (with `block_size`) need for a
- * cache of `batch` requests and `capacity` tokens.  One workspace may serve
+ * `max_inject_rows` rows) and dflash_draft_block (with any block size up to
+ * `block_size`) need for a cache of `batch` requests and `capacity` tokens.  One workspace may serve
  * every call on one stream; calls that overlap on the GPU need separate ones. */
 size_t dflash_workspace_bytes(const dflash_model* model, int32_t batch, int32_t capacity, int32_t block_size,
                               int32_t max_inject_rows);
@@ -283,7 +283,9 @@ int32_t dflash_trace_read(const dflash_model* model, uint64_t* host, size_t n);
 #define DFLASH_STAGE_DOWN 6     /* W_D GEMMs                                  */
 #define DFLASH_STAGE_LMHEAD 7   /* LM head GEMM with argmax                   */
 #define DFLASH_STAGE_OTHER 8    /* embedding, norms, row maps, argmax read-out */
-#define DFLASH_NUM_STAGES 9
+#define DFLASH_STAGE_INJECT_PERSIST 9  /* one-launch injection (fusion + K/V), <= 16 rows */
+#define DFLASH_STAGE_DRAFT_PERSIST 10  /* one-launch drafter pass (layers + LM head), <= 16 rows */
+#define DFLASH_NUM_STAGES 11
 
 /* Start recording a CUDA event pair around each launch the model's entry
  * points make (up to max_launches launches), on the stream each call is given.
