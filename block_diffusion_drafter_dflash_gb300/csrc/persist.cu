@@ -28,7 +28,7 @@
 // tensor-pipe rate.  A stage is [4 KB activations][<=32 KB weights] either way.
 //
 // Roles (256 threads):
-//   warps 0, 3      lane 0: weight producers (even / odd stages), TMA of the
+//   warps 0, 3      lane 0: weight producers (even / odd ring slots), TMA of the
 //                   <=256 x 64 weight tile of each stage (128-row boxes)
 //   warp 1          TMEM allocation (512 columns); lane 0 issues tcgen05.mma
 //   warp 2 lane 0   activation producer: TMA of the 16-row hi/lo activation
@@ -78,15 +78,12 @@ constexpr int kWBox = 128 * 128;                  // one 128-row weight box
 constexpr int kStage = kXBytes + 2 * kWBox;       // 36 KB
 constexpr int kLd = kPRows + 1;                   // staging tile pitch (floats)
 constexpr int kTmemCols = 2 * kTwMax;             // double-buffered 256-column accumulator
-constexpr int kAttnStages = 2;
 constexpr long long kBudget = 200000000LL;        // SM cycles (~0.1 s): far beyond any legal wait
 constexpr size_t kSmemMax = 227 * 1024;
 
 template <int HD>
 struct PCfg {
-  static constexpr int kAttnBytes = kAttnStages * attn::TileCfg<HD>::kStageB;
-  static constexpr int kStaging = kTwMax * kLd * 4;   // epilogue staging tile st[256][kLd]
-  static constexpr int kRegion = kAttnBytes > kStaging ? kAttnBytes : kStaging;
+  static constexpr int kRegion = kTwMax * kLd * 4;   // epilogue staging tile st[256][kLd]
 };
 
 struct PBook {
@@ -94,6 +91,7 @@ struct PBook {
   uint64_t accf[2], accfree[2], mma_done;
   uint32_t tmem;
   int flag_acc, flag_tk, flag_bar;
+  uint64_t ring_free;   // attention is done with the ring (one phase per attention phase)
   float rs[kPRows];
 };
 
@@ -187,11 +185,11 @@ struct ComputeSync {
 };
 
 // Wait for the loads of the last use of every ring slot that this producer
-// filled (iterations of parity `par`, or all when par < 0); bounded, and they
-// were issued, so they complete.
+// filled (slots of parity `par`, or all when par < 0); bounded, and they were
+// issued, so they complete.
 __device__ void drain_slots(uint64_t* full, int issued, int S, int par, int32_t* status) {
   for (int j = max(0, issued - S); j < issued; ++j)
-    if (par < 0 || (j & 1) == par) ptx::mbar_wait(full + (j % S), (j / S) & 1, kBudget, status);
+    if (par < 0 || ((j % S) & 1) == par) ptx::mbar_wait(full + (j % S), (j / S) & 1, kBudget, status);
 }
 
 // ---------------------------------------------------------------- producers and MMA
@@ -202,23 +200,29 @@ __device__ __forceinline__ int box_row(const GemmSeg& sg, int tis, int h) {
   return sg.paired ? 128 * tis : sg.tw * tis + 128 * h;
 }
 
-// Two weight producers (warps 0 and 3) take the even and odd ring iterations:
+// Two weight producers (warps 0 and 3) own the even and the odd ring slots:
 // one issuing thread sustains only ~5 TB/s of TMA traffic across the device
 // (its wait-and-issue loop, not bytes in flight, is the limit), two reach the
-// HBM copy rate.  The ring depth is even, so each slot always belongs to the
-// same producer.
+// HBM copy rate.
 __device__ void weight_producer(const PParams& p, PBook* bk, uint8_t* ring, int G, int cta, int par) {
   const int S = p.stages;
   const uint64_t pol = ptx::policy_evict_first();
-  int it = 0;
+  int it = 0, attn_seen = 0;
   for (int pi = 0; pi < p.nphase; ++pi) {
     const PPhase& ph = p.ph[pi];
+    if (ph.kind == kPhAttn) {
+      // the attention phase borrows the ring's shared memory: load nothing
+      // more until this CTA's attention is done
+      if (!ptx::mbar_wait_sleep(&bk->ring_free, attn_seen & 1, kBudget, p.status)) goto done;
+      ++attn_seen;
+      continue;
+    }
     if (ph.kind != kPhGemm) continue;
     const Span sp = cta_span(ph, G, cta);
     long long we = 0;
     for (int i = sp.i0; i < sp.i1; ++i, ++it) {
-      if ((it & 1) != par) continue;
       const int s = it % S;
+      if ((s & 1) != par) continue;
       if (it >= S && !wait_timed(&bk->empty[s], ((it / S) & 1) ^ 1, p.status, we, true)) goto done;
       if (i - sp.i0 < 2) trace_at(p, cta, pi, kTrW0);
       if (i + 2 >= sp.i1) trace_at(p, cta, pi, kTrW1);
@@ -567,8 +571,10 @@ __device__ bool gemm_phase(const PParams& p, const PPhase& ph, int pi, PBook* bk
 
 // Attention of item = this CTA: (request, kv head, key chunk); partial
 // (unnormalised output, max, sum) rows to global memory.
+constexpr int kAttnRingStages = 6;   // key tiles of 32 in flight, in the ring's shared memory
+
 template <int HD>
-__device__ void attn_phase(const PParams& p, const PPhase& ph, uint8_t* region, int cta, int ct) {
+__device__ void attn_phase(const PParams& p, const PPhase& ph, int pi, uint8_t* sm, int cta, int ct) {
   const AttnParams& ap = p.attn;
   const int nch = ap.splits;
   const int items = ap.B * ap.nkv * nch;
@@ -581,7 +587,8 @@ __device__ void attn_phase(const PParams& p, const PPhase& ph, uint8_t* region, 
   AttnParams a = ap;
   a.layer = ph.layer;
   attn::AttnAcc<HD> acc;
-  attn::attn_chunk<HD, 4, kAttnStages>(a, b, kvh, c, j0, j1, region, ct, ComputeSync{}, acc);
+  attn::attn_chunk<HD, 4, kAttnRingStages>(a, b, kvh, c, j0, j1, sm, ct, ComputeSync{}, acc);
+  if (ct == 0) trace_at(p, cta, pi, kTrM0);
   const int rows = (ap.nq / ap.nkv) * ap.block;
   const int lane = ct & 31, w = ct >> 5, g = lane >> 2, t = lane & 3;
   const int r_lo = w * 16 + g, r_hi = r_lo + 8;
@@ -597,12 +604,16 @@ __device__ void attn_phase(const PParams& p, const PPhase& ph, uint8_t* region, 
     if (r_lo < rows) ap.ml[(size_t)cta * kPAttnRows + r_lo] = make_float2(acc.m_a, acc.l_a);
     if (r_hi < rows) ap.ml[(size_t)cta * kPAttnRows + r_hi] = make_float2(acc.m_b, acc.l_b);
   }
+  if (ct == 0) trace_at(p, cta, pi, kTrM1);
 }
 
 // Merge the key chunks of every output row (request, q head, block row) into
-// the W_O GEMM's activation planes; one warp per row.
+// the W_O GEMM's activation planes; one warp per row.  Lane ch holds chunk
+// ch's (max, sum) and weight; lane l owns output elements [HD/32 * l, +HD/32)
+// and reads them from up to 16 chunks at once (vector loads).
 template <int HD>
 __device__ void merge_phase(const PParams& p, int G, int cta, int ct) {
+  constexpr int E = HD / 32;   // elements per lane: 4 (float4) or 2 (float2)
   const AttnParams& ap = p.attn;
   const int nch = ap.splits, Gq = ap.nq / ap.nkv;
   const int lane = ct & 31, w = ct >> 5;
@@ -613,31 +624,54 @@ __device__ void merge_phase(const PParams& p, int G, int cta, int ct) {
     const int qh = rem / ap.block, k = rem - qh * ap.block;
     const int kvh = qh / Gq, r = (qh - kvh * Gq) * ap.block + k;
     const size_t item0 = ((size_t)b * ap.nkv + kvh) * nch;
+    float L = 0.f, acc[E];
+#pragma unroll
+    for (int e = 0; e < E; ++e) acc[e] = 0.f;
+    // the chunks' maxima first (lanes 0..nch-1, 32 at a time), then the weighted sum
     float M = attn::kNegBig;
-    for (int ch = 0; ch < nch; ++ch) {
-      const float2 ml = __ldcg(ap.ml + (item0 + ch) * kPAttnRows + r);
+    for (int c0 = 0; c0 < nch; c0 += 32) {
+      const int ch = c0 + lane;
+      const float2 ml = ch < nch ? __ldcg(ap.ml + (item0 + ch) * kPAttnRows + r) : make_float2(attn::kNegBig, 0.f);
       if (ml.y > 0.f) M = fmaxf(M, ml.x);
     }
-    float L = 0.f, o[HD / 32];
-#pragma unroll
-    for (int j = 0; j < HD / 32; ++j) o[j] = 0.f;
-    for (int ch = 0; ch < nch; ++ch) {
-      const float2 ml = __ldcg(ap.ml + (item0 + ch) * kPAttnRows + r);
-      if (!(ml.y > 0.f)) continue;
-      const float wgt = exp2f(ml.x - M);
+    for (int o = 16; o; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    for (int c0 = 0; c0 < nch; c0 += 32) {
+      const int ch = c0 + lane, n = min(32, nch - c0);
+      const float2 ml = ch < nch ? __ldcg(ap.ml + (item0 + ch) * kPAttnRows + r) : make_float2(attn::kNegBig, 0.f);
+      const float wgt = ml.y > 0.f ? exp2f(ml.x - M) : 0.f;
       L += wgt * ml.y;
-      const float* src = ap.opart + ((item0 + ch) * kPAttnRows + r) * HD;
+      for (int u0 = 0; u0 < n; u0 += 16) {
+        float v[16][E], wu[16];
 #pragma unroll
-      for (int j = 0; j < HD / 32; ++j) o[j] += wgt * __ldcg(src + lane + 32 * j);
+        for (int u = 0; u < 16; ++u) {
+          wu[u] = __shfl_sync(0xffffffffu, wgt, (u0 + u) & 31);
+          const bool have = u0 + u < n && wu[u] != 0.f;
+          const float* src = ap.opart + ((item0 + c0 + u0 + u) * kPAttnRows + r) * HD + E * lane;
+          if constexpr (E == 4) {
+            const float4 x = have ? __ldcg(reinterpret_cast<const float4*>(src)) : make_float4(0.f, 0.f, 0.f, 0.f);
+            v[u][0] = x.x; v[u][1] = x.y; v[u][2] = x.z; v[u][3] = x.w;
+          } else {
+            const float2 x = have ? __ldcg(reinterpret_cast<const float2*>(src)) : make_float2(0.f, 0.f);
+            v[u][0] = x.x; v[u][1] = x.y;
+          }
+          if (!have) wu[u] = 0.f;
+        }
+#pragma unroll
+        for (int u = 0; u < 16; ++u)
+#pragma unroll
+          for (int e = 0; e < E; ++e) acc[e] += wu[u] * v[u][e];
+      }
     }
+    for (int o = 16; o; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
     const float inv = 1.f / L;
-    const size_t obase = ((size_t)b * ap.block + k) * ap.nq * HD + (size_t)qh * HD;
+    const size_t obase = ((size_t)b * ap.block + k) * ap.nq * HD + (size_t)qh * HD + E * lane;
 #pragma unroll
-    for (int j = 0; j < HD / 32; ++j) put_act(out, ap.out_plane, obase + lane + 32 * j, o[j] * inv);
+    for (int e = 0; e < E; ++e) put_act(out, ap.out_plane, obase + e, acc[e] * inv);
   }
 }
 
-__device__ void compute_warps(const PParams& p, PBook* bk, uint8_t* region, uint32_t tmem, int G, int cta) {
+__device__ void compute_warps(const PParams& p, PBook* bk, uint8_t* ring, uint8_t* region, uint32_t tmem, int G,
+                              int cta) {
   const int ct = threadIdx.x - 128;
   float* st = reinterpret_cast<float*>(region);
   int seq = 0;
@@ -647,10 +681,13 @@ __device__ void compute_warps(const PParams& p, PBook* bk, uint8_t* region, uint
     if (ph.kind == kPhGemm) {
       if (!gemm_phase(p, ph, pi, bk, st, tmem, G, cta, ct, seq)) return;
     } else if (ph.kind == kPhAttn) {
+      // the weight producers hold off until this phase releases the ring
       if (p.attn.hd == 64)
-        attn_phase<64>(p, ph, region, cta, ct);
+        attn_phase<64>(p, ph, pi, ring, cta, ct);
       else
-        attn_phase<128>(p, ph, region, cta, ct);
+        attn_phase<128>(p, ph, pi, ring, cta, ct);
+      csync();
+      if (ct == 0) ptx::mbar_arrive(&bk->ring_free);
     } else {
       if (p.attn.hd == 64)
         merge_phase<64>(p, G, cta, ct);
@@ -706,6 +743,7 @@ __global__ void __launch_bounds__(kThreads, 1) persist_kernel(const __grid_const
       ptx::mbar_init(&bk->accfree[b], 1);
     }
     ptx::mbar_init(&bk->mma_done, 1);
+    ptx::mbar_init(&bk->ring_free, 1);
     ptx::fence_mbar_init();
     for (int i = 0; i < kPXMaps; ++i) ptx::prefetch_tmap(&p.xmap[i]);
   }
@@ -730,7 +768,7 @@ __global__ void __launch_bounds__(kThreads, 1) persist_kernel(const __grid_const
     __syncwarp();
   } else if (warp >= 4) {
     griddep_wait();
-    compute_warps(p, bk, region, tmem, G, cta);
+    compute_warps(p, bk, ring, region, tmem, G, cta);
   }
 
   ptx::tc_fence_before();
@@ -807,9 +845,9 @@ cudaError_t launch_hd(const PParams& p, int grid, cudaStream_t s) {
 
 }  // namespace
 
-int persist_stages(int hd) {   // even: the two weight producers own alternate slots
+int persist_stages(int hd) {
   const size_t fixed = 1024 + region_bytes(hd) + sizeof(PBook);
-  return std::min<int>(kPMaxStages, (int)((kSmemMax - fixed) / kStage)) & ~1;
+  return std::min<int>(kPMaxStages, (int)((kSmemMax - fixed) / kStage));
 }
 
 size_t persist_smem(int stages, int hd) { return 1024 + (size_t)stages * kStage + region_bytes(hd) + sizeof(PBook); }
@@ -822,7 +860,10 @@ cudaError_t persist_prepare(int hd) {
 }
 
 cudaError_t persist_launch(const PParams& p, int grid, int hd, cudaStream_t s) {
-  if (p.stages < 2 || p.stages > kPMaxStages || (p.stages & 1) || p.M < 1 || p.M > kPRows || p.nphase < 1 || p.nphase > kPMaxPhases)
+  // attention borrows the ring and the staging region for its key tiles
+  const size_t attn_bytes = (size_t)kAttnRingStages * (hd == 64 ? attn::TileCfg<64>::kStageB : attn::TileCfg<128>::kStageB);
+  if (attn_bytes > (size_t)p.stages * kStage + region_bytes(hd)) return cudaErrorInvalidValue;
+  if (p.stages < 2 || p.stages > kPMaxStages || p.M < 1 || p.M > kPRows || p.nphase < 1 || p.nphase > kPMaxPhases)
     return cudaErrorInvalidValue;
   return hd == 64 ? launch_hd<64>(p, grid, s) : launch_hd<128>(p, grid, s);
 }
