@@ -264,12 +264,17 @@ int32_t dflash_synthetic_target(const int32_t* draft_dev, const uint8_t* match_d
  * every device), for launch accounting. */
 uint64_t dflash_launch_count(void);
 
-/* Per-CTA timestamps of one projection GEMM launch, for performance work.
- * When the environment variable DFLASH_TRACE_GEMM=<k> is set at model
- * creation, the model's k-th GEMM launch (counting from 0) records, for every
- * CTA c, 8 values at host[8c .. 8c+7]: globaltimer ns at start, after set-up,
- * when the first and the last K stage landed, when the accumulator was ready
- * and at the end; the SM id; 1 if the CTA ran the split-K reduction.
+/* Per-CTA timestamps, for performance work.  When the environment variable
+ * DFLASH_TRACE_GEMM=<k> is set at model creation, the model's k-th GEMM launch
+ * of the multi-kernel path (counting from 0) records, for every CTA c, 8
+ * values at host[8c .. 8c+7]: globaltimer ns at start, after set-up, when the
+ * first and the last K stage landed, when the accumulator was ready and at
+ * the end; the SM id; 1 if the CTA ran the split-K reduction.  With
+ * DFLASH_TRACE_PERSIST=1 instead, every persistent drafter launch records 18
+ * values per (CTA, phase) at host[(c*56 + phase)*18 ..]: phase start and end,
+ * first/last weight load issued, activation loads released, first/last MMA
+ * issued, the SM id, the cycles the MMA issuer and the producers waited, and
+ * the steps of the phase's last output tile (persist.cu lists them).
  * Copies min(n, 8*65536) values; DFLASH_ERR_UNSUPPORTED when tracing is off. */
 int32_t dflash_trace_read(const dflash_model* model, uint64_t* host, size_t n);
 
