@@ -160,7 +160,7 @@ TRAFFIC_PROFILES = {
     "gemm": (os.path.join(ROOT, "profiles", "gemm_traffic_8b_bs1.md"),
              ["gemm_tc.cu", "epilogue.cuh", "common.cuh", "ptx.cuh"]),
     "persist": (os.path.join(ROOT, "profiles", "persist_traffic_8b_bs1.md"),
-                ["persist.cu", "persist.cuh", "attn_core.cuh", "epilogue.cuh", "common.cuh", "ptx.cuh"]),
+                ["persist.cu", "persist.cuh", "attn_tc.cuh", "epilogue.cuh", "common.cuh", "ptx.cuh"]),
 }
 
 

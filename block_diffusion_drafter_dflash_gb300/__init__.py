@@ -105,13 +105,19 @@ class Cache:
         check(lib().dflash_cache_layout(h, ctypes.byref(k), ctypes.byref(v), ctypes.byref(ln)), "dflash_cache_layout")
         self.k_off, self.v_off, self.len_off = k.value, v.value, ln.value
 
-    def _kv_view(self, off: int) -> torch.Tensor:
+    def _kv_view(self, off: int, hd_major: bool = False) -> torch.Tensor:
         c = self.model.cfg
-        n = self.batch * c.layers * c.n_kv_heads * self.capacity * c.head_dim
-        raw = self.buffer[off:off + n * 4]
+        B, L, H, cap, hd = self.batch, c.layers, c.n_kv_heads, self.capacity, c.head_dim
         if self.model.dtype == torch.float32:
-            return raw.view(torch.float32).view(self.batch, c.layers, c.n_kv_heads, self.capacity, c.head_dim)
-        planes = raw.view(torch.bfloat16).view(self.batch, c.layers, c.n_kv_heads, 2, self.capacity, c.head_dim)
+            raw = self.buffer[off:off + B * L * H * cap * hd * 4]
+            return raw.view(torch.float32).view(B, L, H, cap, hd)
+        if hd_major:   # bf16 V: [B][L][H][2][hd][pitch], pitch = capacity rounded up to 8
+            pitch = (cap + 7) // 8 * 8
+            raw = self.buffer[off:off + B * L * H * 2 * hd * pitch * 2]
+            planes = raw.view(torch.bfloat16).view(B, L, H, 2, hd, pitch)[..., :cap].transpose(-1, -2)
+        else:
+            raw = self.buffer[off:off + B * L * H * 2 * cap * hd * 2]
+            planes = raw.view(torch.bfloat16).view(B, L, H, 2, cap, hd)
         return planes[:, :, :, 0].float() + planes[:, :, :, 1].float()
 
     def k(self) -> torch.Tensor:
@@ -120,7 +126,9 @@ class Cache:
         return self._kv_view(self.k_off)
 
     def v(self) -> torch.Tensor:
-        return self._kv_view(self.v_off)
+        """Context values as fp32 [batch][layers][n_kv_heads][capacity][head_dim]
+        (bf16 models store them head-dim-major; this returns them position-major)."""
+        return self._kv_view(self.v_off, hd_major=True)
 
     def ctx_len(self) -> torch.Tensor:
         return self.buffer[self.len_off:self.len_off + 4 * self.batch].view(torch.int32)

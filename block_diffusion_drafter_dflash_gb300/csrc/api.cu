@@ -14,6 +14,7 @@
 
 #include "gemm.cuh"
 #include "kernels.cuh"
+#include "attn_tc.cuh"
 #include "persist.cuh"
 
 using namespace dflash;
@@ -112,6 +113,8 @@ int32_t cuda_fail(cudaError_t e, const char* what) {
 constexpr size_t kTraceEntries = 8u << 16;   // 8 timestamps for up to 65536 CTAs
 
 size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
+// row pitch of hd-major V (bf16 models): positions rounded up to 8 (16-byte rows for TMA)
+int pad8(int n) { return (n + 7) & ~7; }
 
 int32_t check_config(const dflash_config* c) {
   if (!c) return fail(DFLASH_ERR_INVALID_ARG, "config is NULL");
@@ -199,7 +202,7 @@ WsPlan plan_ws(const dflash_model* m, int B, int cap, int block, int max_rows) {
       p.u = take(2 * 2 * (size_t)kPRows * D);
       p.q = take(sizeof(float) * (size_t)R * hq);
       p.kb = take(2 * 2 * (size_t)R * hk);
-      p.vb = take(2 * 2 * (size_t)R * hk);
+      p.vb = take(2 * 2 * (size_t)B * hk * pad8(block));   // hd-major, rows padded to 8
       p.o = take(2 * 2 * (size_t)kPRows * hq);
       p.a = take(2 * 2 * (size_t)kPRows * F);
       p.slots = take(sizeof(unsigned long long) * kPRows);
@@ -248,13 +251,19 @@ WsPlan plan_ws(const dflash_model* m, int B, int cap, int block, int max_rows) {
     chunk = std::max(64, (chunk + 31) / 32 * 32);
     p.attn_chunk = chunk;
     p.attn_splits = (keys + chunk - 1) / chunk;
+    if (c.dtype == DFLASH_DTYPE_BF16) {
+      // tensor-core attention: 128-key tiles (context tiles + the block tile)
+      // cut into splits so that there are ~4 CTAs per SM over all groups
+      const int tiles = (cap + 127) / 128 + 1;
+      p.attn_splits = std::max(1, std::min(tiles, (4 * m->sms + groups - 1) / groups));
+    }
     p.x = take(sizeof(float) * (size_t)R * D);
     p.u = take(ea * (size_t)R * D);
     p.q = take(sizeof(float) * (size_t)R * hq);
     p.kb = take(sizeof(float) * (size_t)R * hk);
-    p.vb = take(sizeof(float) * (size_t)R * hk);
-    // split partials of the CUDA-core attention (fp32 models); bf16 models merge in shared memory
-    const size_t nsplit = c.dtype == DFLASH_DTYPE_F32 ? (size_t)p.attn_splits : 0;
+    p.vb = take(sizeof(float) * (size_t)B * hk * pad8(block));   // bf16: hd-major, rows padded to 8
+    // split partials of the split-KV attention, merged by a second kernel
+    const size_t nsplit = (size_t)p.attn_splits;
     p.opart = take(sizeof(float) * (size_t)B * c.n_q_heads * block * nsplit * c.head_dim);
     p.ml = take(sizeof(float2) * (size_t)B * c.n_q_heads * block * nsplit);
     p.o = take(ea * (size_t)R * hq);
@@ -336,7 +345,7 @@ int32_t run_inject(const dflash_model* m, dflash_cache* cache, const void* feats
   apply_plan(pi, P.g_inject, partial, counters);
   EpiInject<T> ei{reinterpret_cast<T*>(cache->base + cache->k_off), reinterpret_cast<T*>(cache->base + cache->v_off),
                   rowinfo, reinterpret_cast<const float2*>(ws + P.rope_c), c.layers, c.n_kv_heads, c.head_dim,
-                  cache->cap};
+                  cache->cap, pad8(cache->cap)};
   DF_LAUNCH(DFLASH_STAGE_INJECT, 1, (gemm_launch<T, EpiInject<T>>(pi, P.g_inject, ei, s)), "injection GEMM");
   return DFLASH_OK;
 }
@@ -367,6 +376,12 @@ int32_t run_draft(const dflash_model* m, const dflash_cache* cache, const int32_
                                P.counters_n, m->status_dev, ctx_len, m->inv_freq_dev, c.head_dim,
                                reinterpret_cast<float2*>(ws + P.rope_q), s),
           "embedding");
+  attn_tc::Maps amaps;   // bf16 models: tensor maps of the K/V cache and of the block K/V
+  if constexpr (ActPlanes<T>::n == 2) {
+    if (!encode_attention_maps(&amaps, cache->base + cache->k_off, cache->base + cache->v_off, kb, vb, B, c.layers,
+                               c.n_kv_heads, c.head_dim, cache->cap, pad8(cache->cap), block, pad8(block)))
+      return fail(DFLASH_ERR_CUDA, "could not encode attention tensor maps");
+  }
   for (int l = 0; l < c.layers; ++l) {
     const dflash_layer_weights& L = m->layers[l];
     GemmProblem pq = make_problem(m, u, D, R, D, pl, (size_t)R * D);
@@ -375,7 +390,7 @@ int32_t run_draft(const dflash_model* m, const dflash_cache* cache, const int32_
     add_seg(pq, L.w_v, layer_map(l, kMapV), L.w_v, layer_map(l, kMapV), hk / kTileN, 0, 2);
     apply_plan(pq, P.g_qkv, partial, counters);
     EpiQKV<T> eq{q, kb, vb, reinterpret_cast<const float2*>(ws + P.rope_q), block, c.n_q_heads, c.n_kv_heads,
-                 c.head_dim};
+                 c.head_dim, pad8(block)};
     DF_LAUNCH(DFLASH_STAGE_QKV, 1, (gemm_launch<T, EpiQKV<T>>(pq, P.g_qkv, eq, s)), "QKV GEMM");
 
     AttnParams ap{};
@@ -391,7 +406,10 @@ int32_t run_draft(const dflash_model* m, const dflash_cache* cache, const int32_
     ap.out = o;
     ap.out_plane = (size_t)R * hq;
     ap.scale = 1.0f / sqrtf((float)c.head_dim);
-    DF_LAUNCH(DFLASH_STAGE_ATTN, (c.dtype == DFLASH_DTYPE_F32 ? 2 : 1), attention_launch<T>(ap, s), "attention");
+    if constexpr (ActPlanes<T>::n == 2)
+      DF_LAUNCH(DFLASH_STAGE_ATTN, 2, attention_bf16_launch(ap, amaps, m->status_dev, s), "attention");
+    else
+      DF_LAUNCH(DFLASH_STAGE_ATTN, 2, attention_launch<T>(ap, s), "attention");
 
     GemmProblem po = make_problem(m, o, hq, R, hq, pl, (size_t)R * hq);
     add_seg(po, L.w_o, layer_map(l, kMapO), L.w_o, layer_map(l, kMapO), D / kTileN, 0, 0);
@@ -510,7 +528,7 @@ int32_t run_inject_persist(const dflash_model* m, dflash_cache* cache, const voi
   pp.status = m->status_dev;
   pp.inject = EpiInject<__nv_bfloat16>{reinterpret_cast<__nv_bfloat16*>(cache->base + cache->k_off),
                                        reinterpret_cast<__nv_bfloat16*>(cache->base + cache->v_off), rowinfo, rope,
-                                       c.layers, c.n_kv_heads, c.head_dim, cache->cap};
+                                       c.layers, c.n_kv_heads, c.head_dim, cache->cap, pad8(cache->cap)};
   pp.block = 1;
   pp.attn.hd = c.head_dim;
   PhaseBuilder pb{pp};
@@ -568,7 +586,7 @@ int32_t run_draft_persist(const dflash_model* m, const dflash_cache* cache, cons
   float* q = reinterpret_cast<float*>(ws + P.q);
   __nv_bfloat16* kb = reinterpret_cast<__nv_bfloat16*>(ws + P.kb);
   __nv_bfloat16* vb = reinterpret_cast<__nv_bfloat16*>(ws + P.vb);
-  pp.qkv = EpiQKV<__nv_bfloat16>{q, kb, vb, rope, block, c.n_q_heads, c.n_kv_heads, c.head_dim};
+  pp.qkv = EpiQKV<__nv_bfloat16>{q, kb, vb, rope, block, c.n_q_heads, c.n_kv_heads, c.head_dim, pad8(block)};
   pp.swiglu = EpiSwiGLU<__nv_bfloat16>{a, F, (size_t)kPRows * F};
   pp.slots = slots;
   pp.logits = logits;
@@ -595,6 +613,9 @@ int32_t run_draft_persist(const dflash_model* m, const dflash_cache* cache, cons
   ap.out = o;
   ap.out_plane = (size_t)kPRows * hq;
   ap.scale = 1.0f / sqrtf((float)c.head_dim);
+  if (!encode_attention_maps(&pp.amaps, ap.kc, ap.vc, kb, vb, B, c.layers, c.n_kv_heads, c.head_dim, cache->cap,
+                             pad8(cache->cap), block, pad8(block)))
+    return fail(DFLASH_ERR_CUDA, "could not encode attention tensor maps");
 
   PhaseBuilder pb{pp};
   if (const char* w = std::getenv("DFLASH_PERSIST_WIDE")) pb.all_wide = std::strcmp(w, "1") == 0;
@@ -648,6 +669,15 @@ int32_t build_weight_maps(dflash_model* m) {
   DF_CUDA(cudaMalloc(&m->tmaps128_dev, host128.size()), "tensor maps");
   DF_CUDA(cudaMemcpy(m->tmaps128_dev, host128.data(), host128.size(), cudaMemcpyHostToDevice), "tensor maps");
   return DFLASH_OK;
+}
+
+// K [b][layer][kvh][cap][hd] fp32, or two bf16 planes [..][2][cap][hd]; V the
+// same for fp32 models and hd-major [..][2][hd][pad8(cap)] for bf16 models.
+size_t cache_k_bytes(const dflash_config* cfg, int batch, int capacity) {
+  return sizeof(float) * (size_t)batch * cfg->layers * cfg->n_kv_heads * (size_t)capacity * cfg->head_dim;
+}
+size_t cache_v_bytes(const dflash_config* cfg, int batch, int capacity) {
+  return cache_k_bytes(cfg, batch, cfg->dtype == DFLASH_DTYPE_BF16 ? pad8(capacity) : capacity);
 }
 
 }  // namespace
@@ -758,8 +788,8 @@ int32_t dflash_clear_status(const dflash_model* m, dflash_stream_t stream) {
 
 size_t dflash_cache_bytes(const dflash_config* cfg, int32_t batch, int32_t capacity) {
   if (check_config(cfg) != DFLASH_OK || batch < 0 || capacity < 0) return 0;
-  const size_t kv = sizeof(float) * (size_t)batch * cfg->layers * cfg->n_kv_heads * (size_t)capacity * cfg->head_dim;
-  return align256(kv) * 2 + align256(sizeof(int32_t) * std::max(batch, 1));
+  return align256(cache_k_bytes(cfg, batch, capacity)) + align256(cache_v_bytes(cfg, batch, capacity)) +
+         align256(sizeof(int32_t) * std::max(batch, 1));
 }
 
 int32_t dflash_cache_init(const dflash_model* m, void* dev_mem, size_t bytes, int32_t batch, int32_t capacity,
@@ -774,7 +804,8 @@ int32_t dflash_cache_init(const dflash_model* m, void* dev_mem, size_t bytes, in
   if (bytes < need) return fail(DFLASH_ERR_CAPACITY, "cache memory %zu bytes < %zu needed", bytes, need);
   int32_t rc = check_device(m);
   if (rc) return rc;
-  const size_t kv = sizeof(float) * (size_t)batch * m->cfg.layers * m->cfg.n_kv_heads * (size_t)capacity * m->cfg.head_dim;
+  const size_t kb = align256(cache_k_bytes(&m->cfg, batch, capacity));
+  const size_t vb = align256(cache_v_bytes(&m->cfg, batch, capacity));
   dflash_cache* c = new dflash_cache();
   c->model = m;
   c->base = static_cast<char*>(dev_mem);
@@ -782,11 +813,13 @@ int32_t dflash_cache_init(const dflash_model* m, void* dev_mem, size_t bytes, in
   c->batch = batch;
   c->cap = capacity;
   c->k_off = 0;
-  c->v_off = align256(kv);
-  c->len_off = 2 * align256(kv);
+  c->v_off = kb;
+  c->len_off = kb + vb;
   c->len_host.assign(batch, 0);
   c->len_known = true;
-  cudaError_t e = cudaMemsetAsync(c->base + c->len_off, 0, sizeof(int32_t) * batch, (cudaStream_t)stream);
+  // zeroed once: positions past a request's context are then always finite
+  // (the attention reads whole tiles and gives those keys probability 0)
+  cudaError_t e = cudaMemsetAsync(c->base, 0, c->len_off + sizeof(int32_t) * batch, (cudaStream_t)stream);
   if (e != cudaSuccess) {
     delete c;
     return cuda_fail(e, "cache init");

@@ -1,4 +1,5 @@
-// Non-causal block attention of the drafter (split-KV, online softmax).
+// Non-causal block attention of the drafter (split-KV, online softmax): the
+// CUDA-core kernels of fp32 models and the merge of the splits (all models).
 //
 // For request b and kv head h the query rows are the (nq/nkv) query heads of
 // the group times the block positions; the keys are the request's injected
@@ -14,9 +15,9 @@
 
 namespace dflash {
 
-// tensor-core cluster kernel for bf16 models (attention_mma.cu)
-cudaError_t attention_mma_prepare(int hd);
-cudaError_t attention_mma_launch(const AttnParams& p, cudaStream_t s);
+// tensor-core split kernel for bf16 models (attention_tc.cu)
+cudaError_t attention_tc_prepare(int hd);
+cudaError_t attention_tc_split_launch(const AttnParams& p, const attn_tc::Maps& maps, int32_t* status, cudaStream_t s);
 
 namespace {
 
@@ -183,17 +184,23 @@ int attention_max_rows() { return kMaxRows; }
 
 template <typename T>
 cudaError_t attention_prepare(int rows, int hd) {
-  if constexpr (std::is_same<T, __nv_bfloat16>::value) return attention_mma_prepare(hd);
+  if constexpr (std::is_same<T, __nv_bfloat16>::value) return attention_tc_prepare(hd);
   return cudaFuncSetAttribute(attn_split_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               (int)attn_smem_bytes(rows, hd));
+}
+
+cudaError_t attention_bf16_launch(const AttnParams& p, const attn_tc::Maps& maps, int32_t* status, cudaStream_t s) {
+  if (p.B <= 0) return cudaSuccess;
+  cudaError_t e = attention_tc_split_launch(p, maps, status, s);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(attn_combine_kernel<__nv_bfloat16>, dim3(p.B * p.nq * p.block), dim3(128),
+                    (p.splits + 8) * sizeof(float), s, p);
 }
 
 template <typename T>
 cudaError_t attention_launch(const AttnParams& p, cudaStream_t s) {
   if (p.B <= 0) return cudaSuccess;
-  if constexpr (std::is_same<T, __nv_bfloat16>::value) {
-    return attention_mma_launch(p, s);   // one launch: the cluster merges its own splits
-  }
+  if constexpr (std::is_same<T, __nv_bfloat16>::value) return cudaErrorInvalidValue;   // attention_bf16_launch
   const int rows = (p.nq / p.nkv) * p.block;
   cudaError_t e = launch_pdl(attn_split_kernel<T>, dim3(p.splits, p.nkv, p.B), dim3(kAttnThreads),
                              attn_smem_bytes(rows, p.hd), s, p);

@@ -1,0 +1,334 @@
+// Tensor-core (tcgen05) block attention for bf16 drafters at fp32-level
+// precision: one (request, kv head) group's query rows against a range of
+// 128-key tiles of its keys, online softmax, unnormalised output.  Used by the
+// split-KV attention kernel (attention_tc.cu) and by the persistent drafter
+// kernel (persist.cu).
+//
+// Operands.  Every value v is carried as two bf16 parts hi + lo.  The MMA's A
+// operand holds, in each 32-row quarter of its 128 rows, the hi parts of 16
+// query rows followed by their lo parts, so one instruction against Khi and
+// one against Klo give, summed over a row's hi and lo accumulator rows,
+//     S = (Qhi + Qlo)(Khi + Klo)^T
+// (all four products; the same for O = P V with P in A and V in B).  A query
+// row's two accumulator rows sit in one warp's TMEM lanes, 16 apart, so each
+// of the four warps reads back its own 16 rows and adds the halves with one
+// shuffle.  Scores are in the log2 domain (Q is pre-scaled by
+// log2(e)/sqrt(hd)).
+//
+// Keys.  A group's keys are its context keys 0..c-1 (cache) in tiles of 128,
+// then one tile of its block keys.  K is stored key-major ([pos][hd]) and V
+// hd-major ([hd][pos]), so that both products read their B operand K-major;
+// tiles arrive by TMA (128-byte swizzle).  Keys past the valid ones read
+// finite values (the cache is zeroed at creation; past the tensor end TMA
+// fills zeros) and get probability exactly 0 (score -inf).
+//
+// Softmax.  The running row max is only raised when a tile's max exceeds it
+// by more than 8 (log2 units), so the unnormalised output in TMEM is rescaled
+// rarely; probabilities stay below 2^8, well inside fp32 and bf16 range.
+#pragma once
+
+#include <cuda.h>
+
+#include "kernels.cuh"
+#include "ptx.cuh"
+
+namespace dflash {
+namespace attn_tc {
+
+constexpr int kKeys = 128;                 // keys per tile (MMA N of Q K^T)
+constexpr int kTile16 = 128 * 128;         // one 128-row x 128-byte operand tile
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kNegInf = -1.0e30f;
+constexpr float kLazy = 8.0f;              // raise the running max only beyond this margin
+constexpr long long kBudget = 200000000LL;
+
+// Tensor maps of one launch: K cache, V cache (hd-major), block K, block V (hd-major).
+struct Maps {
+  CUtensorMap kc, vc, kb, vb;
+};
+
+// Shared memory (1024-byte aligned base): Q A-tile per 64 columns of hd;
+// K B-tiles [plane][hd/64]; V B-tiles [plane][key half] (hd rows x 64 keys);
+// P A-tiles [key half].
+template <int HD>
+struct Cfg {
+  static constexpr int kSub = HD / 64;                       // 64-column blocks of hd
+  static constexpr int kQ = kSub * kTile16;
+  static constexpr int kK = 2 * kSub * kTile16;
+  static constexpr int kVHalf = HD * 128;                    // hd rows x 64 keys
+  static constexpr int kV = 2 * 2 * kVHalf;
+  static constexpr int kP = 2 * kTile16;
+  static constexpr int kOffK = kQ, kOffV = kOffK + kK, kOffP = kOffV + kV;
+  static constexpr int kBytes = kOffP + kP;
+  static constexpr int kTmemCols = kKeys + HD;               // S then O
+  static constexpr uint32_t kKBytes = 2u * kSub * kTile16;   // TMA bytes of a K tile
+  static constexpr uint32_t kVBytes = 2u * 2 * kVHalf;       // TMA bytes of a V tile
+};
+
+struct Bars {
+  uint64_t kfull, vfull, sdone, odone;
+};
+
+__device__ __forceinline__ void init_bars(Bars* b) {
+  ptx::mbar_init(&b->kfull, 1);
+  ptx::mbar_init(&b->vfull, 1);
+  ptx::mbar_init(&b->sdone, 1);
+  ptx::mbar_init(&b->odone, 1);
+}
+
+// A-tile row of query row i (0..63) of a pass: quarter i/16, hi part at +0, lo at +16
+__device__ __forceinline__ int a_row(int i, int lo) { return 32 * (i >> 4) + 16 * lo + (i & 15); }
+// byte offset of 16-byte chunk `ch` of row `r` in a 128-byte-swizzled K-major tile
+__device__ __forceinline__ int sw(int r, int ch) { return r * 128 + ((ch ^ (r & 7)) << 4); }
+
+__device__ __forceinline__ uint4 pack8(const float* v) {
+  __nv_bfloat162 a = __floats2bfloat162_rn(v[0], v[1]), b = __floats2bfloat162_rn(v[2], v[3]);
+  __nv_bfloat162 c = __floats2bfloat162_rn(v[4], v[5]), d = __floats2bfloat162_rn(v[6], v[7]);
+  return make_uint4(*reinterpret_cast<uint32_t*>(&a), *reinterpret_cast<uint32_t*>(&b),
+                    *reinterpret_cast<uint32_t*>(&c), *reinterpret_cast<uint32_t*>(&d));
+}
+// hi/lo parts of 8 values as two 16-byte chunks
+__device__ __forceinline__ void split8(const float* v, uint4& hi, uint4& lo) {
+  float h[8], l[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    h[j] = __bfloat162float(__float2bfloat16_rn(v[j]));
+    l[j] = v[j] - h[j];
+  }
+  hi = pack8(h);
+  lo = pack8(l);
+}
+
+// Q rows [64*pass, 64*pass+64) of group (b, kvh) into the A tiles, scaled into
+// the log2 domain; rows past the group's rows are zero.  nth threads.
+template <int HD>
+__device__ void stage_q(const AttnParams& p, int b, int kvh, int pass, uint8_t* sm, int tid, int nth) {
+  const int G = p.nq / p.nkv, rows = G * p.block;
+  const float qscale = p.scale * kLog2e;
+  for (int e = tid; e < 64 * (HD / 8); e += nth) {
+    const int i = e / (HD / 8), c8 = e - i * (HD / 8), s = c8 >> 3, ch = c8 & 7;
+    const int r = 64 * pass + i;
+    float v[8];
+    if (r < rows) {
+      const int gh = r / p.block, k = r - gh * p.block;
+      const float* src = p.q + (((size_t)b * p.nq + kvh * G + gh) * p.block + k) * HD + 8 * c8;
+      const float4 x0 = __ldcg(reinterpret_cast<const float4*>(src));
+      const float4 x1 = __ldcg(reinterpret_cast<const float4*>(src + 4));
+      v[0] = x0.x * qscale; v[1] = x0.y * qscale; v[2] = x0.z * qscale; v[3] = x0.w * qscale;
+      v[4] = x1.x * qscale; v[5] = x1.y * qscale; v[6] = x1.z * qscale; v[7] = x1.w * qscale;
+    } else {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) v[j] = 0.f;
+    }
+    uint4 hi, lo;
+    split8(v, hi, lo);
+    uint8_t* q = sm + s * kTile16;
+    *reinterpret_cast<uint4*>(q + sw(a_row(i, 0), ch)) = hi;
+    *reinterpret_cast<uint4*>(q + sw(a_row(i, 1), ch)) = lo;
+  }
+}
+
+// TMA of tile t of group (b, kvh) of layer p.layer: context keys [128t, 128t+128)
+// for t < nct, else the block's keys.  Issued by one thread.
+template <int HD>
+__device__ void load_k(const AttnParams& p, const Maps& m, int b, int kvh, int t, int nct, uint8_t* sm, Bars* bars) {
+  using C = Cfg<HD>;
+  uint8_t* kt = sm + C::kOffK;
+  ptx::mbar_arrive_expect_tx(&bars->kfull, C::kKBytes);
+  for (int pl = 0; pl < 2; ++pl)
+    for (int s = 0; s < C::kSub; ++s) {
+      uint8_t* dst = kt + (pl * C::kSub + s) * kTile16;
+      if (t < nct) {
+        const int row = ((((b * p.layers + p.layer) * p.nkv + kvh) * 2 + pl) * p.cap) + kKeys * t;
+        ptx::tma_load_2d(dst, &m.kc, &bars->kfull, 64 * s, row, ptx::policy_evict_first());
+      } else {
+        const int row = ((b * p.nkv + kvh) * 2 + pl) * p.block;
+        ptx::tma_load_2d(dst, &m.kb, &bars->kfull, 64 * s, row, ptx::policy_evict_last());
+      }
+    }
+}
+
+template <int HD>
+__device__ void load_v(const AttnParams& p, const Maps& m, int b, int kvh, int t, int nct, uint8_t* sm, Bars* bars) {
+  using C = Cfg<HD>;
+  uint8_t* vt = sm + C::kOffV;
+  ptx::mbar_arrive_expect_tx(&bars->vfull, C::kVBytes);
+  for (int pl = 0; pl < 2; ++pl)
+    for (int h = 0; h < 2; ++h) {
+      uint8_t* dst = vt + (pl * 2 + h) * C::kVHalf;
+      if (t < nct) {
+        const int row = (((b * p.layers + p.layer) * p.nkv + kvh) * 2 + pl) * HD;
+        ptx::tma_load_2d(dst, &m.vc, &bars->vfull, kKeys * t + 64 * h, row, ptx::policy_evict_first());
+      } else {
+        const int row = ((b * p.nkv + kvh) * 2 + pl) * HD;
+        ptx::tma_load_2d(dst, &m.vb, &bars->vfull, 64 * h, row, ptx::policy_evict_last());
+      }
+    }
+}
+
+// One item: query rows of pass `pass` of group (b, kvh) against tiles [t0, t1)
+// (nct context tiles, then the block tile).  128 participating threads
+// (tid 0..127, warp w = tid/32 reads TMEM lanes 32w..32w+31, which must be the
+// warp's own lane quarter); thread 0 issues the TMA loads and the MMAs.
+// `uses` counts the tiles this CTA ran before (mbarrier phases).  On return
+// out(row, d0, v32) has received, for every valid row of the pass, its
+// unnormalised output in chunks of 32 columns, and done(row, m_log2, l) its
+// running max and sum.  Returns false on a timeout.
+template <int HD, class Sync, class Out, class Done>
+__device__ bool run(const AttnParams& p, const Maps& m, int b, int kvh, int pass, int t0, int t1, int nct,
+                    uint8_t* sm, uint32_t tmem, Bars* bars, int& uses, int tid, Sync sync, int32_t* status, Out out,
+                    Done done) {
+  using C = Cfg<HD>;
+  const int lane = tid & 31, w = tid >> 5;
+  const int G = p.nq / p.nkv, rows = G * p.block;
+  const int c = p.ctx_len[b];
+  const uint32_t tS = tmem, tO = tmem + kKeys;
+  const uint32_t lanes = static_cast<uint32_t>(w * 32) << 16;
+  const uint32_t idS = ptx::idesc_bf16_f32(128, kKeys), idO = ptx::idesc_bf16_f32(128, HD);
+  bool ok = true;
+
+  if (tid == 0 && t0 < t1) {
+    load_k<HD>(p, m, b, kvh, t0, nct, sm, bars);
+    load_v<HD>(p, m, b, kvh, t0, nct, sm, bars);
+  }
+  stage_q<HD>(p, b, kvh, pass, sm, tid, 128);
+  ptx::fence_proxy_async_shared();
+  sync();
+
+  float m_used = kNegInf, l_sum = 0.f;
+  for (int t = t0; t < t1; ++t) {
+    const uint32_t par = static_cast<uint32_t>(uses + (t - t0)) & 1u;
+    const int nk = t < nct ? min(kKeys, c - kKeys * t) : p.block;   // valid keys of the tile
+    // ---- S = Q K^T (thread 0), then the K buffer is free for the next tile
+    if (tid == 0) {
+      ok = ptx::mbar_wait(&bars->kfull, par, kBudget, status);
+      if (ok) {
+        ptx::tc_fence_after();
+        for (int s = 0; s < C::kSub; ++s)
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const uint64_t ad = ptx::smem_desc_sw128(sm + s * kTile16) + 2 * k;
+#pragma unroll
+            for (int pl = 0; pl < 2; ++pl) {
+              const uint64_t bd = ptx::smem_desc_sw128(sm + C::kOffK + (pl * C::kSub + s) * kTile16) + 2 * k;
+              ptx::mma_bf16(tS, ad, bd, idS, (s | k | pl) != 0 ? 1u : 0u);
+            }
+          }
+        ptx::mma_commit(&bars->sdone);
+        if (t > t0) {   // the V buffer is free once the previous P V is done
+          ok = ptx::mbar_wait(&bars->odone, par ^ 1u, kBudget, status);
+          if (ok) load_v<HD>(p, m, b, kvh, t, nct, sm, bars);
+        }
+      }
+    }
+    ok = ptx::mbar_wait(&bars->sdone, par, kBudget, status) && ok;
+    ptx::tc_fence_after();
+    if (tid == 0 && ok && t + 1 < t1) load_k<HD>(p, m, b, kvh, t + 1, nct, sm, bars);
+
+    // ---- softmax of this warp's 16 rows: lanes l and l+16 hold a row's hi and
+    // lo accumulator rows; lane l < 16 keeps keys 0..63, lane l+16 keys 64..127
+    const int half = lane >> 4;
+    float pv[64];
+#pragma unroll
+    for (int c0 = 0; c0 < kKeys; c0 += 32) {
+      float v[32];
+      ptx::tmem_ld32(tS + lanes + c0, v);
+#pragma unroll
+      for (int j = 0; j < 32; ++j) v[j] += __shfl_xor_sync(0xffffffffu, v[j], 16);
+      if ((c0 >> 6) == half) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) pv[(c0 & 63) + j] = (c0 + j < nk) ? v[j] : kNegInf;
+      }
+    }
+    float mx = kNegInf;
+#pragma unroll
+    for (int j = 0; j < 64; ++j) mx = fmaxf(mx, pv[j]);
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+    float alpha = 1.f;
+    if (t == t0) {
+      m_used = mx;
+    } else if (mx > m_used + kLazy) {
+      alpha = exp2f(m_used - mx);
+      m_used = mx;
+    }
+    float sum = 0.f;
+#pragma unroll
+    for (int j = 0; j < 64; ++j) {
+      pv[j] = exp2f(pv[j] - m_used);
+      sum += pv[j];
+    }
+    sum += __shfl_xor_sync(0xffffffffu, sum, 16);
+    l_sum = l_sum * alpha + sum;
+
+    // the previous P V has finished: P may be overwritten, O rescaled
+    if (t > t0) ok = ptx::mbar_wait(&bars->odone, par ^ 1u, kBudget, status) && ok;
+    ptx::tc_fence_after();
+    if (__any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll 1
+      for (int d0 = 0; d0 < HD; d0 += 32) {
+        float v[32];
+        ptx::tmem_ld32(tO + lanes + d0, v);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] *= alpha;
+        ptx::tmem_st32(tO + lanes + d0, v);
+      }
+    }
+    {
+      const int i = 16 * w + (lane & 15);
+      uint8_t* pt = sm + C::kOffP + half * kTile16;
+      const int rh = a_row(i, 0), rl = a_row(i, 1);
+#pragma unroll
+      for (int ch = 0; ch < 8; ++ch) {
+        uint4 hi, lo;
+        split8(pv + 8 * ch, hi, lo);
+        *reinterpret_cast<uint4*>(pt + sw(rh, ch)) = hi;
+        *reinterpret_cast<uint4*>(pt + sw(rl, ch)) = lo;
+      }
+    }
+    ptx::fence_proxy_async_shared();
+    ptx::tc_fence_before();
+    sync();
+
+    // ---- O += P V (thread 0)
+    if (tid == 0 && ok) {
+      ptx::tc_fence_after();
+      ok = ptx::mbar_wait(&bars->vfull, par, kBudget, status);
+      if (ok) {
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const uint64_t ad = ptx::smem_desc_sw128(sm + C::kOffP + h * kTile16) + 2 * k;
+#pragma unroll
+            for (int pl = 0; pl < 2; ++pl) {
+              const uint64_t bd = ptx::smem_desc_sw128(sm + C::kOffV + (pl * 2 + h) * C::kVHalf) + 2 * k;
+              ptx::mma_bf16(tO, ad, bd, idO, (t > t0 || h | k | pl) ? 1u : 0u);
+            }
+          }
+        ptx::mma_commit(&bars->odone);
+      }
+    }
+    if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) ok = false;
+  }
+  if (t1 > t0) {
+    ok = ptx::mbar_wait(&bars->odone, static_cast<uint32_t>(uses + (t1 - 1 - t0)) & 1u, kBudget, status) && ok;
+    ptx::tc_fence_after();
+    const int i = 16 * w + (lane & 15), r = 64 * pass + i;
+#pragma unroll 1
+    for (int d0 = 0; d0 < HD; d0 += 32) {
+      float v[32];
+      ptx::tmem_ld32(tO + lanes + d0, v);
+#pragma unroll
+      for (int j = 0; j < 32; ++j) v[j] += __shfl_xor_sync(0xffffffffu, v[j], 16);
+      if (lane < 16 && r < rows) out(r, d0, v);
+    }
+    if (lane < 16 && r < rows) done(r, m_used, l_sum);
+    ptx::tc_fence_before();
+  }
+  uses += t1 - t0;
+  sync();
+  return ok;
+}
+
+}  // namespace attn_tc
+}  // namespace dflash

@@ -16,7 +16,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 PKG = os.path.dirname(HERE)
 ROOT = os.path.dirname(PKG)
 LIB_NAME = "libdflash_gb300.so"
-SOURCES = ["api.cu", "gemm.cu", "gemm_tc.cu", "attention.cu", "attention_mma.cu", "elementwise.cu", "persist.cu"]
+SOURCES = ["api.cu", "gemm.cu", "gemm_tc.cu", "attention.cu", "attention_tc.cu", "elementwise.cu", "persist.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
          "-I" + os.path.join(ROOT, "include")]

@@ -76,8 +76,10 @@ struct EpiSwiGLU {
 // Block Q/K/V of one draft layer: tag 0 = Q, 1 = K, 2 = V.  Row = b*block + k
 // sits at position ctx_len[b] + k, whose RoPE (cos, sin) table rope[row][hd/2]
 // was filled by the embedding kernel; Q and K get RoPE.  Q is fp32
-// [b][head][k][hd]; K and V are stored like the context cache, as
-// [b][head][plane][k][hd] of T (two bf16 planes hi, lo for bf16 models).
+// [b][head][k][hd]; K and V are stored like the context cache: K as
+// [b][head][plane][k][hd] of T (two bf16 planes hi, lo for bf16 models); V
+// likewise for fp32 models, hd-major [b][head][plane][hd][vpitch] for bf16
+// models (vpitch = block rounded up to 8).
 template <typename T>
 struct EpiQKV {
   float* q;
@@ -85,6 +87,7 @@ struct EpiQKV {
   T* vb;
   const float2* rope;
   int block, nq, nkv, hd;
+  int vpitch;
   // thread n owns feature n of the tile; the RoPE entries of 8 rows are
   // loaded before any store so that their loads overlap
   __device__ __forceinline__ void operator()(const float* t, int ld, int m0, int mc, int, const GemmSeg& sg,
@@ -113,6 +116,8 @@ struct EpiQKV {
         const float r = tag == 2 ? v : (d < half ? v * sc[j].x - pv * sc[j].y : v * sc[j].x + pv * sc[j].y);
         if (tag == 0)
           q[(((size_t)b * nh + head) * block + k) * hd + d] = r;
+        else if (tag == 2 && planes == 2)   // bf16 V: hd-major
+          put_act(dkv, (size_t)hd * vpitch, (((size_t)b * nh + head) * 2 * hd + d) * vpitch + k, r);
         else
           put_act(dkv, (size_t)block * hd, (((size_t)b * nh + head) * planes * block + k) * hd + d, r);
       }
@@ -123,7 +128,9 @@ struct EpiQKV {
 // Context K/V injection: tag = 2*layer + (0: K, 1: V).  rowinfo[row] =
 // (request, position) or (-1, -1) for padding rows; rope[row][hd/2] = (cos,
 // sin) at that position.  Writes the cache [b][layer][kvh][plane][pos][hd] of
-// T (fp32 one plane; bf16 two planes hi, lo); K gets RoPE at its position.
+// T (fp32 one plane; bf16 two planes hi, lo) — for bf16 models V hd-major,
+// [b][layer][kvh][plane][hd][vpitch] (vpitch = capacity rounded up to 8);
+// K gets RoPE at its position.
 template <typename T>
 struct EpiInject {
   T* kc;
@@ -131,6 +138,7 @@ struct EpiInject {
   const int2* rowinfo;
   const float2* rope;
   int layers, nkv, hd, cap;
+  int vpitch;
   __device__ __forceinline__ void operator()(const float* t, int ld, int m0, int mc, int, const GemmSeg& sg,
                                              int tis, int tid, int nth) const {
     const int layer = sg.tag >> 1, is_v = sg.tag & 1, half = hd >> 1;
@@ -156,8 +164,12 @@ struct EpiInject {
         if (ri[j].x < 0) continue;
         const float v = t[n * ld + m], pv = t[pn * ld + m];
         const float r = is_v ? v : (d < half ? v * sc[j].x - pv * sc[j].y : v * sc[j].x + pv * sc[j].y);
-        put_act(dst, (size_t)cap * hd,
-                ((((size_t)ri[j].x * layers + layer) * nkv + head) * planes * cap + ri[j].y) * hd + d, r);
+        if (is_v && planes == 2)   // bf16 V: hd-major
+          put_act(dst, (size_t)hd * vpitch,
+                  ((((size_t)ri[j].x * layers + layer) * nkv + head) * 2 * hd + d) * vpitch + ri[j].y, r);
+        else
+          put_act(dst, (size_t)cap * hd,
+                  ((((size_t)ri[j].x * layers + layer) * nkv + head) * planes * cap + ri[j].y) * hd + d, r);
       }
     }
   }

@@ -13,7 +13,7 @@ namespace dflash {
 struct AttnParams {
   const float* q;       // [B][nq][block][hd] fp32 (RoPE applied)
   const void* kb;       // [B][nkv][planes][block][hd]  (RoPE applied)
-  const void* vb;       // [B][nkv][planes][block][hd]
+  const void* vb;       // [B][nkv][planes][block][hd]; bf16 models: [B][nkv][planes][hd][pad8(block)]
   const void* kc;       // cache K [B][layers][nkv][planes][cap][hd]
   const void* vc;       // cache V
   const int32_t* ctx_len;
@@ -28,7 +28,18 @@ struct AttnParams {
   float scale;          // 1/sqrt(hd)
 };
 
+namespace attn_tc { struct Maps; }
+
+// fp32 models: CUDA-core split-KV attention and the merge of the splits.
 template <typename T> cudaError_t attention_launch(const AttnParams& p, cudaStream_t s);
+// bf16 models: tensor-core split-KV attention (tensor maps of the K/V cache and
+// of the block K/V, see attn_tc.cuh) and the merge; V is stored hd-major.
+cudaError_t attention_bf16_launch(const AttnParams& p, const attn_tc::Maps& maps, int32_t* status, cudaStream_t s);
+// Tensor maps of the bf16 attention: K cache [slabs*cap][hd], V cache
+// [slabs*hd][cap] (row pitch cap_pitch), block K [slabs*block][hd], block V
+// [slabs*hd][block] (row pitch block_pitch); 64 x rows boxes, 128-byte swizzle.
+bool encode_attention_maps(attn_tc::Maps* m, const void* kc, const void* vc, const void* kb, const void* vb, int B,
+                           int layers, int nkv, int hd, int cap, int cap_pitch, int block, int block_pitch);
 // One-time per-device setup (shared-memory opt-in) for up to `rows` query rows.
 template <typename T> cudaError_t attention_prepare(int rows, int hd);
 int attention_max_rows();   // largest (nq/nkv)*block the kernel accepts

@@ -62,7 +62,7 @@
 
 #include <algorithm>
 
-#include "attn_core.cuh"
+#include "attn_tc.cuh"
 #include "gemm.cuh"
 #include "persist.cuh"
 #include "ptx.cuh"
@@ -92,6 +92,7 @@ struct PBook {
   uint32_t tmem;
   int flag_acc, flag_tk, flag_bar;
   uint64_t ring_free;   // attention is done with the ring (one phase per attention phase)
+  attn_tc::Bars abars;  // the attention's TMA and MMA barriers
   float rs[kPRows];
 };
 
@@ -569,42 +570,41 @@ __device__ bool gemm_phase(const PParams& p, const PPhase& ph, int pi, PBook* bk
   return true;
 }
 
-// Attention of item = this CTA: (request, kv head, key chunk); partial
-// (unnormalised output, max, sum) rows to global memory.
-constexpr int kAttnRingStages = 6;   // key tiles of 32 in flight, in the ring's shared memory
-
+// Attention of item = this CTA: (request, kv head, chunk of key tiles) on the
+// tensor cores (attn_tc.cuh), using the ring's shared memory and TMEM columns
+// 0..255 (idle between projections); partial (unnormalised output, max, sum)
+// rows to global memory, maxima in log2 units.  Returns false on a timeout.
 template <int HD>
-__device__ void attn_phase(const PParams& p, const PPhase& ph, int pi, uint8_t* sm, int cta, int ct) {
+__device__ bool attn_phase(const PParams& p, const PPhase& ph, int pi, PBook* bk, uint8_t* sm, uint32_t tmem, int cta,
+                           int ct, int& uses) {
   const AttnParams& ap = p.attn;
   const int nch = ap.splits;
   const int items = ap.B * ap.nkv * nch;
-  if (cta >= items) return;
+  if (cta >= items) return true;
   const int b = cta / (ap.nkv * nch), r = cta - b * ap.nkv * nch, kvh = r / nch, ch = r - kvh * nch;
-  const int c = ap.ctx_len[b], total = c + ap.block;
-  const int per = (total + nch - 1) / nch;
-  const int chunk = (per + attn::kKeys - 1) / attn::kKeys * attn::kKeys;
-  const int j0 = min(total, ch * chunk), j1 = min(total, j0 + chunk);
+  const int c = ap.ctx_len[b];
+  const int nct = (c + attn_tc::kKeys - 1) / attn_tc::kKeys, T = nct + 1;
+  const int t0 = ch * T / nch, t1 = (ch + 1) * T / nch;
+  const int rows = (ap.nq / ap.nkv) * ap.block;
+  float* op = ap.opart + (size_t)cta * kPAttnRows * HD;
+  float2* ml = ap.ml + (size_t)cta * kPAttnRows;
+  if (t0 >= t1) {   // no tiles: an empty partial (weight 0 in the merge)
+    for (int i = ct; i < rows; i += 128) ml[i] = make_float2(attn_tc::kNegInf, 0.f);
+    if (ct == 0) trace_at(p, cta, pi, kTrM1);
+    return true;
+  }
   AttnParams a = ap;
   a.layer = ph.layer;
-  attn::AttnAcc<HD> acc;
-  attn::attn_chunk<HD, 4, kAttnRingStages>(a, b, kvh, c, j0, j1, sm, ct, ComputeSync{}, acc);
-  if (ct == 0) trace_at(p, cta, pi, kTrM0);
-  const int rows = (ap.nq / ap.nkv) * ap.block;
-  const int lane = ct & 31, w = ct >> 5, g = lane >> 2, t = lane & 3;
-  const int r_lo = w * 16 + g, r_hi = r_lo + 8;
-  float* op = ap.opart + (size_t)cta * kPAttnRows * HD;
+  auto out = [&](int row, int d0, const float* v) {
+    float* dst = op + (size_t)row * HD + d0;
 #pragma unroll
-  for (int nb = 0; nb < HD / 8; ++nb) {
-    if (r_lo < rows)
-      *reinterpret_cast<float2*>(op + r_lo * HD + nb * 8 + 2 * t) = make_float2(acc.o[nb][0], acc.o[nb][1]);
-    if (r_hi < rows)
-      *reinterpret_cast<float2*>(op + r_hi * HD + nb * 8 + 2 * t) = make_float2(acc.o[nb][2], acc.o[nb][3]);
-  }
-  if (t == 0) {
-    if (r_lo < rows) ap.ml[(size_t)cta * kPAttnRows + r_lo] = make_float2(acc.m_a, acc.l_a);
-    if (r_hi < rows) ap.ml[(size_t)cta * kPAttnRows + r_hi] = make_float2(acc.m_b, acc.l_b);
-  }
+    for (int j = 0; j < 32; j += 4) *reinterpret_cast<float4*>(dst + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+  };
+  auto done = [&](int row, float m_log2, float l) { ml[row] = make_float2(m_log2, l); };
+  const bool ok = attn_tc::run<HD>(a, p.amaps, b, kvh, 0, t0, t1, nct, sm, tmem, &bk->abars, uses, ct, ComputeSync{},
+                                   p.status, out, done);
   if (ct == 0) trace_at(p, cta, pi, kTrM1);
+  return ok;
 }
 
 // Merge the key chunks of every output row (request, q head, block row) into
@@ -628,16 +628,16 @@ __device__ void merge_phase(const PParams& p, int G, int cta, int ct) {
 #pragma unroll
     for (int e = 0; e < E; ++e) acc[e] = 0.f;
     // the chunks' maxima first (lanes 0..nch-1, 32 at a time), then the weighted sum
-    float M = attn::kNegBig;
+    float M = attn_tc::kNegInf;
     for (int c0 = 0; c0 < nch; c0 += 32) {
       const int ch = c0 + lane;
-      const float2 ml = ch < nch ? __ldcg(ap.ml + (item0 + ch) * kPAttnRows + r) : make_float2(attn::kNegBig, 0.f);
+      const float2 ml = ch < nch ? __ldcg(ap.ml + (item0 + ch) * kPAttnRows + r) : make_float2(attn_tc::kNegInf, 0.f);
       if (ml.y > 0.f) M = fmaxf(M, ml.x);
     }
     for (int o = 16; o; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
     for (int c0 = 0; c0 < nch; c0 += 32) {
       const int ch = c0 + lane, n = min(32, nch - c0);
-      const float2 ml = ch < nch ? __ldcg(ap.ml + (item0 + ch) * kPAttnRows + r) : make_float2(attn::kNegBig, 0.f);
+      const float2 ml = ch < nch ? __ldcg(ap.ml + (item0 + ch) * kPAttnRows + r) : make_float2(attn_tc::kNegInf, 0.f);
       const float wgt = ml.y > 0.f ? exp2f(ml.x - M) : 0.f;
       L += wgt * ml.y;
       for (int u0 = 0; u0 < n; u0 += 16) {
@@ -674,7 +674,7 @@ __device__ void compute_warps(const PParams& p, PBook* bk, uint8_t* ring, uint8_
                               int cta) {
   const int ct = threadIdx.x - 128;
   float* st = reinterpret_cast<float*>(region);
-  int seq = 0;
+  int seq = 0, attn_uses = 0;
   for (int pi = 0; pi < p.nphase; ++pi) {
     const PPhase& ph = p.ph[pi];
     if (ct == 0) trace_at(p, cta, pi, kTrStart);
@@ -682,12 +682,11 @@ __device__ void compute_warps(const PParams& p, PBook* bk, uint8_t* ring, uint8_
       if (!gemm_phase(p, ph, pi, bk, st, tmem, G, cta, ct, seq)) return;
     } else if (ph.kind == kPhAttn) {
       // the weight producers hold off until this phase releases the ring
-      if (p.attn.hd == 64)
-        attn_phase<64>(p, ph, pi, ring, cta, ct);
-      else
-        attn_phase<128>(p, ph, pi, ring, cta, ct);
+      const bool ok = p.attn.hd == 64 ? attn_phase<64>(p, ph, pi, bk, ring, tmem, cta, ct, attn_uses)
+                                      : attn_phase<128>(p, ph, pi, bk, ring, tmem, cta, ct, attn_uses);
       csync();
       if (ct == 0) ptx::mbar_arrive(&bk->ring_free);
+      if (!ok) return;
     } else {
       if (p.attn.hd == 64)
         merge_phase<64>(p, G, cta, ct);
@@ -744,6 +743,7 @@ __global__ void __launch_bounds__(kThreads, 1) persist_kernel(const __grid_const
     }
     ptx::mbar_init(&bk->mma_done, 1);
     ptx::mbar_init(&bk->ring_free, 1);
+    attn_tc::init_bars(&bk->abars);
     ptx::fence_mbar_init();
     for (int i = 0; i < kPXMaps; ++i) ptx::prefetch_tmap(&p.xmap[i]);
   }
@@ -861,7 +861,7 @@ cudaError_t persist_prepare(int hd) {
 
 cudaError_t persist_launch(const PParams& p, int grid, int hd, cudaStream_t s) {
   // attention borrows the ring and the staging region for its key tiles
-  const size_t attn_bytes = (size_t)kAttnRingStages * (hd == 64 ? attn::TileCfg<64>::kStageB : attn::TileCfg<128>::kStageB);
+  const size_t attn_bytes = hd == 64 ? attn_tc::Cfg<64>::kBytes : attn_tc::Cfg<128>::kBytes;
   if (attn_bytes > (size_t)p.stages * kStage + region_bytes(hd)) return cudaErrorInvalidValue;
   if (p.stages < 2 || p.stages > kPMaxStages || p.M < 1 || p.M > kPRows || p.nphase < 1 || p.nphase > kPMaxPhases)
     return cudaErrorInvalidValue;

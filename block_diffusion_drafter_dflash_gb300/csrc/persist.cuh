@@ -6,6 +6,7 @@
 
 #include "common.cuh"
 #include "epilogue.cuh"
+#include "attn_tc.cuh"
 #include "kernels.cuh"
 
 namespace dflash {
@@ -65,6 +66,7 @@ struct PParams {
   int32_t* drafts;             // [B][block-1] or nullptr
   int vocab, block;
   AttnParams attn;             // layer taken from the phase; opart/ml/out/splits = chunk partials, output
+  attn_tc::Maps amaps;         // tensor maps of the K/V cache and the block K/V
   unsigned long long* trace;    // optional timestamps [grid][kPMaxPhases][18] (see persist.cu) or nullptr
   PPhase ph[kPMaxPhases];
   GemmSeg seg[kPMaxSeg];

@@ -56,8 +56,10 @@ def test_cache_bytes_follow_the_documented_layout(L):
     kv = 4 * 3 * 2 * 2 * 100 * 64
     a = lambda v: (v + 255) // 256 * 256
     assert L.dflash_cache_bytes(ctypes.byref(c), 3, 100) == 2 * a(kv) + a(4 * 3)
-    c16 = _cfg(dtype=1)        # the cache is fp32 for bf16 models too
-    assert L.dflash_cache_bytes(ctypes.byref(c16), 3, 100) == 2 * a(kv) + a(4 * 3)
+    c16 = _cfg(dtype=1)        # fp32-sized for bf16 models too (two bf16 planes); V hd-major, rows padded to 8
+    kv8 = 4 * 3 * 2 * 2 * 104 * 64
+    assert L.dflash_cache_bytes(ctypes.byref(c16), 3, 100) == a(kv) + a(kv8) + a(4 * 3)
+    assert L.dflash_cache_bytes(ctypes.byref(c16), 3, 104) == 2 * a(kv8) + a(4 * 3)
 
 
 @pytest.mark.parametrize("bad", [dict(hidden=200), dict(head_dim=96), dict(n_kv_heads=3), dict(ffn=100),
