@@ -6,10 +6,13 @@
 //
 // Operands.  Every value v is carried as two bf16 parts hi + lo.  The MMA's A
 // operand holds, in each 32-row quarter of its 128 rows, the hi parts of 16
-// query rows followed by their lo parts, so one instruction against Khi and
-// one against Klo give, summed over a row's hi and lo accumulator rows,
+// query rows followed by their lo parts; its B operand stacks the hi plane of
+// the keys over their lo plane (N = 2 x 128 keys).  One instruction (a
+// tcgen05.mma costs about the same for any N up to 256) thus gives all four
+// products, and summed over a row's hi and lo accumulator rows and over a
+// key's hi and lo accumulator columns,
 //     S = (Qhi + Qlo)(Khi + Klo)^T
-// (all four products; the same for O = P V with P in A and V in B).  A query
+// (the same for O = P V with P in A and [Vhi; Vlo] in B, N = 2 hd).  A query
 // row's two accumulator rows sit in one warp's TMEM lanes, 16 apart, so each
 // of the four warps reads back its own 16 rows and adds the halves with one
 // shuffle.  Scores are in the log2 domain (Q is pre-scaled by
@@ -48,8 +51,10 @@ struct Maps {
 };
 
 // Shared memory (1024-byte aligned base): Q A-tile per 64 columns of hd;
-// K B-tiles [plane][hd/64]; V B-tiles [plane][key half] (hd rows x 64 keys);
-// P A-tiles [key half].
+// K B-tiles [hd/64][plane] (the two planes of a column block adjacent, one
+// 256-row operand); V B-tiles [key half][plane] (hd rows x 64 keys each, the
+// planes adjacent); P A-tiles [key half].  Tensor memory: S in columns
+// [0, 256) (Khi keys, then Klo keys), O in [256, 256 + 2 hd).
 template <int HD>
 struct Cfg {
   static constexpr int kSub = HD / 64;                       // 64-column blocks of hd
@@ -60,7 +65,7 @@ struct Cfg {
   static constexpr int kP = 2 * kTile16;
   static constexpr int kOffK = kQ, kOffV = kOffK + kK, kOffP = kOffV + kV;
   static constexpr int kBytes = kOffP + kP;
-  static constexpr int kTmemCols = kKeys + HD;               // S then O
+  static constexpr int kTmemCols = 2 * kKeys + 2 * HD;       // S then O, both planes
   static constexpr uint32_t kKBytes = 2u * kSub * kTile16;   // TMA bytes of a K tile
   static constexpr uint32_t kVBytes = 2u * 2 * kVHalf;       // TMA bytes of a V tile
 };
@@ -100,26 +105,33 @@ __device__ __forceinline__ void split8(const float* v, uint4& hi, uint4& lo) {
 }
 
 // Q rows [64*pass, 64*pass+64) of group (b, kvh) into the A tiles, scaled into
-// the log2 domain; rows past the group's rows are zero.  nth threads.
+// the log2 domain; rows past the group's rows are zero.  128 threads, each
+// with HD/16 chunks of 8 values: every load is issued before the first store,
+// so the whole tile costs one memory round trip.
 template <int HD>
-__device__ void stage_q(const AttnParams& p, int b, int kvh, int pass, uint8_t* sm, int tid, int nth) {
+__device__ void stage_q(const AttnParams& p, int b, int kvh, int pass, uint8_t* sm, int tid) {
+  constexpr int kPer = 64 * (HD / 8) / 128;   // 8-value chunks per thread
   const int G = p.nq / p.nkv, rows = G * p.block;
   const float qscale = p.scale * kLog2e;
-  for (int e = tid; e < 64 * (HD / 8); e += nth) {
-    const int i = e / (HD / 8), c8 = e - i * (HD / 8), s = c8 >> 3, ch = c8 & 7;
+  float4 x[kPer][2];
+#pragma unroll
+  for (int u = 0; u < kPer; ++u) {
+    const int e = tid + 128 * u, i = e / (HD / 8), c8 = e - i * (HD / 8);
     const int r = 64 * pass + i;
-    float v[8];
     if (r < rows) {
       const int gh = r / p.block, k = r - gh * p.block;
       const float* src = p.q + (((size_t)b * p.nq + kvh * G + gh) * p.block + k) * HD + 8 * c8;
-      const float4 x0 = __ldcg(reinterpret_cast<const float4*>(src));
-      const float4 x1 = __ldcg(reinterpret_cast<const float4*>(src + 4));
-      v[0] = x0.x * qscale; v[1] = x0.y * qscale; v[2] = x0.z * qscale; v[3] = x0.w * qscale;
-      v[4] = x1.x * qscale; v[5] = x1.y * qscale; v[6] = x1.z * qscale; v[7] = x1.w * qscale;
+      x[u][0] = __ldcg(reinterpret_cast<const float4*>(src));
+      x[u][1] = __ldcg(reinterpret_cast<const float4*>(src + 4));
     } else {
-#pragma unroll
-      for (int j = 0; j < 8; ++j) v[j] = 0.f;
+      x[u][0] = x[u][1] = make_float4(0.f, 0.f, 0.f, 0.f);
     }
+  }
+#pragma unroll
+  for (int u = 0; u < kPer; ++u) {
+    const int e = tid + 128 * u, i = e / (HD / 8), c8 = e - i * (HD / 8), s = c8 >> 3, ch = c8 & 7;
+    const float v[8] = {x[u][0].x * qscale, x[u][0].y * qscale, x[u][0].z * qscale, x[u][0].w * qscale,
+                        x[u][1].x * qscale, x[u][1].y * qscale, x[u][1].z * qscale, x[u][1].w * qscale};
     uint4 hi, lo;
     split8(v, hi, lo);
     uint8_t* q = sm + s * kTile16;
@@ -137,7 +149,7 @@ __device__ void load_k(const AttnParams& p, const Maps& m, int b, int kvh, int t
   ptx::mbar_arrive_expect_tx(&bars->kfull, C::kKBytes);
   for (int pl = 0; pl < 2; ++pl)
     for (int s = 0; s < C::kSub; ++s) {
-      uint8_t* dst = kt + (pl * C::kSub + s) * kTile16;
+      uint8_t* dst = kt + (s * 2 + pl) * kTile16;
       if (t < nct) {
         const int row = ((((b * p.layers + p.layer) * p.nkv + kvh) * 2 + pl) * p.cap) + kKeys * t;
         ptx::tma_load_2d(dst, &m.kc, &bars->kfull, 64 * s, row, ptx::policy_evict_first());
@@ -155,7 +167,7 @@ __device__ void load_v(const AttnParams& p, const Maps& m, int b, int kvh, int t
   ptx::mbar_arrive_expect_tx(&bars->vfull, C::kVBytes);
   for (int pl = 0; pl < 2; ++pl)
     for (int h = 0; h < 2; ++h) {
-      uint8_t* dst = vt + (pl * 2 + h) * C::kVHalf;
+      uint8_t* dst = vt + (h * 2 + pl) * C::kVHalf;
       if (t < nct) {
         const int row = (((b * p.layers + p.layer) * p.nkv + kvh) * 2 + pl) * HD;
         ptx::tma_load_2d(dst, &m.vc, &bars->vfull, kKeys * t + 64 * h, row, ptx::policy_evict_first());
@@ -173,27 +185,30 @@ __device__ void load_v(const AttnParams& p, const Maps& m, int b, int kvh, int t
 // `uses` counts the tiles this CTA ran before (mbarrier phases).  On return
 // out(row, d0, v32) has received, for every valid row of the pass, its
 // unnormalised output in chunks of 32 columns, and done(row, m_log2, l) its
-// running max and sum.  Returns false on a timeout.
+// running max and sum.  Optional `stamps` (globaltimer): [0] Q staged, [1] the
+// first tile's scores ready, [2] the last P V done, [3] output written.
+// Returns false on a timeout.
 template <int HD, class Sync, class Out, class Done>
 __device__ bool run(const AttnParams& p, const Maps& m, int b, int kvh, int pass, int t0, int t1, int nct,
                     uint8_t* sm, uint32_t tmem, Bars* bars, int& uses, int tid, Sync sync, int32_t* status, Out out,
-                    Done done) {
+                    Done done, unsigned long long* stamps = nullptr) {
   using C = Cfg<HD>;
   const int lane = tid & 31, w = tid >> 5;
   const int G = p.nq / p.nkv, rows = G * p.block;
   const int c = p.ctx_len[b];
-  const uint32_t tS = tmem, tO = tmem + kKeys;
   const uint32_t lanes = static_cast<uint32_t>(w * 32) << 16;
-  const uint32_t idS = ptx::idesc_bf16_f32(128, kKeys), idO = ptx::idesc_bf16_f32(128, HD);
+  const uint32_t tS = tmem + lanes, tO = tmem + lanes + 2 * kKeys;   // this warp's lanes
+  const uint32_t idS = ptx::idesc_bf16_f32(128, 2 * kKeys), idO = ptx::idesc_bf16_f32(128, 2 * HD);
   bool ok = true;
 
   if (tid == 0 && t0 < t1) {
     load_k<HD>(p, m, b, kvh, t0, nct, sm, bars);
     load_v<HD>(p, m, b, kvh, t0, nct, sm, bars);
   }
-  stage_q<HD>(p, b, kvh, pass, sm, tid, 128);
+  stage_q<HD>(p, b, kvh, pass, sm, tid);
   ptx::fence_proxy_async_shared();
   sync();
+  if (stamps && tid == 0) stamps[0] = ptx::globaltimer();
 
   float m_used = kNegInf, l_sum = 0.f;
   for (int t = t0; t < t1; ++t) {
@@ -208,11 +223,8 @@ __device__ bool run(const AttnParams& p, const Maps& m, int b, int kvh, int pass
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
             const uint64_t ad = ptx::smem_desc_sw128(sm + s * kTile16) + 2 * k;
-#pragma unroll
-            for (int pl = 0; pl < 2; ++pl) {
-              const uint64_t bd = ptx::smem_desc_sw128(sm + C::kOffK + (pl * C::kSub + s) * kTile16) + 2 * k;
-              ptx::mma_bf16(tS, ad, bd, idS, (s | k | pl) != 0 ? 1u : 0u);
-            }
+            const uint64_t bd = ptx::smem_desc_sw128(sm + C::kOffK + s * 2 * kTile16) + 2 * k;
+            ptx::mma_bf16(tmem, ad, bd, idS, (s | k) != 0 ? 1u : 0u);
           }
         ptx::mma_commit(&bars->sdone);
         if (t > t0) {   // the V buffer is free once the previous P V is done
@@ -223,21 +235,24 @@ __device__ bool run(const AttnParams& p, const Maps& m, int b, int kvh, int pass
     }
     ok = ptx::mbar_wait(&bars->sdone, par, kBudget, status) && ok;
     ptx::tc_fence_after();
+    if (stamps && tid == 0 && t == t0) stamps[1] = ptx::globaltimer();
     if (tid == 0 && ok && t + 1 < t1) load_k<HD>(p, m, b, kvh, t + 1, nct, sm, bars);
 
     // ---- softmax of this warp's 16 rows: lanes l and l+16 hold a row's hi and
-    // lo accumulator rows; lane l < 16 keeps keys 0..63, lane l+16 keys 64..127
+    // lo accumulator rows; lane l < 16 keeps keys 0..63, lane l+16 keys 64..127,
+    // and each sends the partner the half it does not keep (one shuffle a key)
     const int half = lane >> 4;
     float pv[64];
 #pragma unroll
-    for (int c0 = 0; c0 < kKeys; c0 += 32) {
-      float v[32];
-      ptx::tmem_ld32(tS + lanes + c0, v);
+    for (int c0 = 0; c0 < 64; c0 += 16) {
+      float v[64];   // [Khi keys c0.., Klo keys c0.., Khi keys 64+c0.., Klo keys 64+c0..]
+      ptx::tmem_ld16x4(tS + c0, tS + kKeys + c0, tS + 64 + c0, tS + kKeys + 64 + c0, v);
 #pragma unroll
-      for (int j = 0; j < 32; ++j) v[j] += __shfl_xor_sync(0xffffffffu, v[j], 16);
-      if ((c0 >> 6) == half) {
-#pragma unroll
-        for (int j = 0; j < 32; ++j) pv[(c0 & 63) + j] = (c0 + j < nk) ? v[j] : kNegInf;
+      for (int j = 0; j < 16; ++j) {
+        const float lo_keys = v[j] + v[16 + j], hi_keys = v[32 + j] + v[48 + j];
+        const float got = __shfl_xor_sync(0xffffffffu, half ? lo_keys : hi_keys, 16);
+        const float x = half ? hi_keys + got : lo_keys + got;
+        pv[c0 + j] = (64 * half + c0 + j < nk) ? x : kNegInf;
       }
     }
     float mx = kNegInf;
@@ -265,12 +280,12 @@ __device__ bool run(const AttnParams& p, const Maps& m, int b, int kvh, int pass
     ptx::tc_fence_after();
     if (__any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll 1
-      for (int d0 = 0; d0 < HD; d0 += 32) {
+      for (int d0 = 0; d0 < 2 * HD; d0 += 32) {
         float v[32];
-        ptx::tmem_ld32(tO + lanes + d0, v);
+        ptx::tmem_ld32(tO + d0, v);
 #pragma unroll
         for (int j = 0; j < 32; ++j) v[j] *= alpha;
-        ptx::tmem_st32(tO + lanes + d0, v);
+        ptx::tmem_st32(tO + d0, v);
       }
     }
     {
@@ -299,11 +314,8 @@ __device__ bool run(const AttnParams& p, const Maps& m, int b, int kvh, int pass
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
             const uint64_t ad = ptx::smem_desc_sw128(sm + C::kOffP + h * kTile16) + 2 * k;
-#pragma unroll
-            for (int pl = 0; pl < 2; ++pl) {
-              const uint64_t bd = ptx::smem_desc_sw128(sm + C::kOffV + (pl * 2 + h) * C::kVHalf) + 2 * k;
-              ptx::mma_bf16(tO, ad, bd, idO, (t > t0 || h | k | pl) ? 1u : 0u);
-            }
+            const uint64_t bd = ptx::smem_desc_sw128(sm + C::kOffV + h * 2 * C::kVHalf) + 2 * k;
+            ptx::mma_bf16(tmem + 2 * kKeys, ad, bd, idO, (t > t0 || h | k) ? 1u : 0u);
           }
         ptx::mma_commit(&bars->odone);
       }
@@ -313,17 +325,22 @@ __device__ bool run(const AttnParams& p, const Maps& m, int b, int kvh, int pass
   if (t1 > t0) {
     ok = ptx::mbar_wait(&bars->odone, static_cast<uint32_t>(uses + (t1 - 1 - t0)) & 1u, kBudget, status) && ok;
     ptx::tc_fence_after();
+    if (stamps && tid == 0) stamps[2] = ptx::globaltimer();
     const int i = 16 * w + (lane & 15), r = 64 * pass + i;
 #pragma unroll 1
     for (int d0 = 0; d0 < HD; d0 += 32) {
-      float v[32];
-      ptx::tmem_ld32(tO + lanes + d0, v);
+      float v[64];   // O columns d0.. of the Vhi and the Vlo products
+      ptx::tmem_ld32x2(tO + d0, tO + HD + d0, v);
 #pragma unroll
-      for (int j = 0; j < 32; ++j) v[j] += __shfl_xor_sync(0xffffffffu, v[j], 16);
+      for (int j = 0; j < 32; ++j) {
+        v[j] += v[32 + j];
+        v[j] += __shfl_xor_sync(0xffffffffu, v[j], 16);
+      }
       if (lane < 16 && r < rows) out(r, d0, v);
     }
     if (lane < 16 && r < rows) done(r, m_used, l_sum);
     ptx::tc_fence_before();
+    if (stamps && tid == 0) stamps[3] = ptx::globaltimer();
   }
   uses += t1 - t0;
   sync();

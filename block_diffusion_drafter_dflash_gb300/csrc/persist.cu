@@ -161,7 +161,8 @@ __device__ __forceinline__ void csync() { asm volatile("bar.sync 1, 128;" ::: "m
 // [8..11]: SM cycles the MMA issuer waited for weights / activations, and the
 // weight producer (even stages) / activation producer waited for free slots.
 // [12..15]: for the CTA's last piece of the phase: accumulator ready, tile
-// staged, epilogue done or partial published, reduction + epilogue done.
+// staged, epilogue done or partial published, reduction + epilogue done; in
+// an attention phase: Q staged, first scores ready, last P V done, written.
 enum { kTrStart = 0, kTrDone, kTrW0, kTrW1, kTrX0, kTrM0, kTrM1, kTrSm, kTrWaitW, kTrWaitX, kTrWaitWEmpty,
        kTrWaitXEmpty, kTrAcc, kTrStaged, kTrPub, kTrRed, kTrReadBack, kTrCombined, kTrSlots };
 __device__ __forceinline__ void trace_val(const PParams& p, int cta, int pi, int slot, unsigned long long v) {
@@ -199,6 +200,24 @@ __device__ void drain_slots(uint64_t* full, int issued, int S, int par, int32_t*
 // then the same 128 rows of w1 (up).
 __device__ __forceinline__ int box_row(const GemmSeg& sg, int tis, int h) {
   return sg.paired ? 128 * tis : sg.tw * tis + 128 * h;
+}
+
+// Attention work item of CTA `cta`: (request b, kv head, chunk of key tiles
+// [t0, t1)) of nct context tiles and one block tile; false if it has none.
+struct AttnItem {
+  int b, kvh, t0, t1, nct;
+};
+__device__ __forceinline__ bool attn_item(const AttnParams& ap, int cta, AttnItem& it) {
+  const int nch = ap.splits;
+  if (cta >= ap.B * ap.nkv * nch) return false;
+  const int r = cta % (ap.nkv * nch), ch = r % nch;
+  it.b = cta / (ap.nkv * nch);
+  it.kvh = r / nch;
+  it.nct = (ap.ctx_len[it.b] + attn_tc::kKeys - 1) / attn_tc::kKeys;
+  const int T = it.nct + 1;
+  it.t0 = ch * T / nch;
+  it.t1 = (ch + 1) * T / nch;
+  return true;
 }
 
 // Two weight producers (warps 0 and 3) own the even and the odd ring slots:
@@ -331,13 +350,27 @@ done:
 // 128 features starting at feature f0 of the output (rows of x / u):
 // out = acc (+ x): x keeps out, planes u keep out * gain, ssq[f0/128][m] = sum
 // of out^2 over the 128 features.  Thread ct owns feature f0 + ct.
-__device__ void epi_norm_out(const PParams& p, const PPhase& ph, int f0, float* st, int ct) {
+// Residual-stream values x[m][f0 + ct] of the rows (zero for the fusion, which
+// has no residual input).
+__device__ __forceinline__ void load_resid(const PParams& p, const PPhase& ph, int f0, int ct, float* v) {
+  const bool resid = ph.epi == kEpResid;
+#pragma unroll
+  for (int m = 0; m < kPRows; ++m) v[m] = (m < p.M && resid) ? __ldcg(p.x + (size_t)m * p.D + f0 + ct) : 0.f;
+}
+
+// `xr`: kPRows residual values of load_resid followed by the gain of feature
+// f0 + ct, or nullptr to load them here.
+__device__ void epi_norm_out(const PParams& p, const PPhase& ph, int f0, float* st, int ct, const float* xr) {
   const int f = f0 + ct;
-  const float g = __bfloat162float(ph.gain[f]);
+  const float g = xr ? xr[kPRows] : __bfloat162float(ph.gain[f]);
   const bool resid = ph.epi == kEpResid;
   float v[kPRows];
+  if (xr) {
 #pragma unroll
-  for (int m = 0; m < kPRows; ++m) v[m] = (m < p.M && resid) ? __ldcg(p.x + (size_t)m * p.D + f) : 0.f;
+    for (int m = 0; m < kPRows; ++m) v[m] = xr[m];
+  } else {
+    load_resid(p, ph, f0, ct, v);
+  }
 #pragma unroll
   for (int m = 0; m < kPRows; ++m) {
     if (m >= p.M) break;
@@ -398,14 +431,91 @@ __device__ void epi_lm(const PParams& p, int f0, int tw, const float* st, int ct
   }
 }
 
+// Partial tiles [16 rows][tw features] in global memory (row pitch kTwMax).
+// Thread ct moves feature quad 4(ct % (TW/4)) of rows ct / (TW/4) + k * 512/TW:
+// all 128 threads take part at either width.
+template <int TW>
+struct PieceMap {
+  static constexpr int kQ = TW / 4;              // feature quads of a row
+  static constexpr int kStep = 128 / kQ;         // rows between a thread's rows
+  static constexpr int kR = kPRows / kStep;      // rows of a thread
+  static constexpr int kU = 24 / kR;             // pieces loaded at once (24 float4 in flight per thread)
+};
+
+template <int TW>
+__device__ __forceinline__ void publish_tw(const PParams& p, const float* st, float* dst, int ct) {
+  using PM = PieceMap<TW>;
+  const int fq = 4 * (ct % PM::kQ), r0 = ct / PM::kQ;
+  for (int m = r0; m < p.M; m += PM::kStep)
+    *reinterpret_cast<float4*>(dst + m * kTwMax + fq) =
+        make_float4(st[fq * kLd + m], st[(fq + 1) * kLd + m], st[(fq + 2) * kLd + m], st[(fq + 3) * kLd + m]);
+}
+__device__ __forceinline__ void publish_piece(const PParams& p, int tw, const float* st, float* dst, int ct) {
+  if (tw == kTwMax)
+    publish_tw<kTwMax>(p, st, dst, ct);
+  else
+    publish_tw<128>(p, st, dst, ct);
+}
+
+// Sum of the pieces of tile t (CTAs cf..cl, in CTA order, so that the result
+// does not depend on timing) into the staging tile.
+template <int TW>
+__device__ void sum_pieces(const PParams& p, const PPhase& ph, int G, int t, float* st, int ct) {
+  using PM = PieceMap<TW>;
+  const int fq = 4 * (ct % PM::kQ), r0 = ct / PM::kQ;
+  const long long W = phase_iters(ph);
+  const int g = phase_ctas(ph, G);
+  const int cf = cta_of(ph, G, (long long)t * ph.kb), cl = cta_of(ph, G, (long long)(t + 1) * ph.kb - 1);
+  float4 acc[PM::kR];
+#pragma unroll
+  for (int j = 0; j < PM::kR; ++j) acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int c = cf; c <= cl; c += PM::kU) {
+    float4 a[PM::kU][PM::kR];
+#pragma unroll
+    for (int u = 0; u < PM::kU; ++u) {
+      const int cu = min(c + u, cl);
+      const float* src =
+          p.partial + (size_t)(cu * 2 + ((int)((cu * W / g) / ph.kb) == t ? 0 : 1)) * (kPRows * kTwMax) + fq;
+#pragma unroll
+      for (int j = 0; j < PM::kR; ++j) {
+        const int m = r0 + PM::kStep * j;
+        a[u][j] = (c + u <= cl && m < p.M) ? __ldcg(reinterpret_cast<const float4*>(src + m * kTwMax))
+                                           : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < PM::kR; ++j)
+#pragma unroll
+      for (int u = 0; u < PM::kU; ++u) {
+        acc[j].x += a[u][j].x;
+        acc[j].y += a[u][j].y;
+        acc[j].z += a[u][j].z;
+        acc[j].w += a[u][j].w;
+      }
+  }
+#pragma unroll
+  for (int j = 0; j < PM::kR; ++j) {
+    const int m = r0 + PM::kStep * j;
+    if (m < p.M) {
+      st[fq * kLd + m] = acc[j].x;
+      st[(fq + 1) * kLd + m] = acc[j].y;
+      st[(fq + 2) * kLd + m] = acc[j].z;
+      st[(fq + 3) * kLd + m] = acc[j].w;
+    }
+  }
+}
+
 // Epilogue of output tile t (all 128 compute threads; the tile is staged).
-__device__ void run_epilogue(const PParams& p, const PPhase& ph, int t, float* st, int ct) {
+// `xr`: this thread's residual values and gain for the tile's first 128
+// features (see epi_norm_out), or nullptr.
+__device__ void run_epilogue(const PParams& p, const PPhase& ph, int t, float* st, int ct, const float* xr = nullptr) {
   const GemmSeg& sg = p.seg[seg_of(p, ph, t)];
   const int tis = t - sg.tile_begin, halves = sg.tw / 128;
   switch (ph.epi) {
     case kEpFuse:
     case kEpResid:   // one segment starting at feature 0
-      for (int h = 0; h < halves; ++h) epi_norm_out(p, ph, tis * sg.tw + h * 128, st + h * 128 * kLd, ct);
+      for (int h = 0; h < halves; ++h)
+        epi_norm_out(p, ph, tis * sg.tw + h * 128, st + h * 128 * kLd, ct, h == 0 ? xr : nullptr);
       break;
     case kEpQKV:
       for (int h = 0; h < halves; ++h) p.qkv(st + h * 128 * kLd, kLd, 0, p.M, 0, sg, tis * halves + h, ct, 128);
@@ -434,6 +544,7 @@ __device__ bool gemm_phase(const PParams& p, const PPhase& ph, int pi, PBook* bk
   csync();
   const Span sp = cta_span(ph, G, cta);
   const int first_tile = sp.i0 / max(ph.kb, 1);
+  int pend[2], npend = 0;   // partial tiles this CTA reduces
   for (int i = sp.i0; i < sp.i1;) {
     const int t = i / ph.kb, k0 = i - t * ph.kb, k1 = min(sp.i1 - t * ph.kb, ph.kb);
     i = t * ph.kb + k1;
@@ -497,16 +608,10 @@ __device__ bool gemm_phase(const PParams& p, const PPhase& ph, int pi, PBook* bk
       if (ct == 0 && last) trace_at(p, cta, pi, kTrPub);
       continue;
     }
-    // partial tile [16 rows][256 features]: publish it; the last CTA of the tile
-    // reduces.  Thread ct moves features 4(ct%64)..+3 of rows ct/64, ct/64+2, ...
-    const int fq = 4 * (ct & 63), r0 = ct >> 6;
-    {
-      float* dst = p.partial + (size_t)(cta * 2 + (t == first_tile ? 0 : 1)) * (kPRows * kTwMax);
-      if (fq < tw)
-        for (int m = r0; m < p.M; m += 2)
-          *reinterpret_cast<float4*>(dst + m * kTwMax + fq) =
-              make_float4(st[fq * kLd + m], st[(fq + 1) * kLd + m], st[(fq + 2) * kLd + m], st[(fq + 3) * kLd + m]);
-    }
+    // partial tile: publish it; the last CTA of the tile to publish reduces it,
+    // once all of its own pieces of the phase are out (a reduction between two
+    // of its pieces would hold up the second piece, and so the second tile)
+    publish_piece(p, tw, st, p.partial + (size_t)(cta * 2 + (t == first_tile ? 0 : 1)) * (kPRows * kTwMax), ct);
     __threadfence();
     csync();
     const int cf = cta_of(ph, G, (long long)t * ph.kb), cl = cta_of(ph, G, (long long)(t + 1) * ph.kb - 1);
@@ -516,75 +621,50 @@ __device__ bool gemm_phase(const PParams& p, const PPhase& ph, int pi, PBook* bk
     }
     csync();
     if (ct == 0 && last) trace_at(p, cta, pi, kTrPub);
-    if (!bk->flag_tk) continue;
+    if (bk->flag_tk) pend[npend++] = t;   // only the first and the last tile of a span are partial
+  }
+  for (int j = 0; j < npend; ++j) {
+    const int t = pend[j];
+    const GemmSeg& sg = p.seg[seg_of(p, ph, t)];
     __threadfence();
-    if (fq < tw) {
-      const long long W = phase_iters(ph);
-      const int g = phase_ctas(ph, G);
-      constexpr int kR = kPRows / 2;   // rows of this thread
-      float4 acc[kR];
+    // the residual input and the gain do not depend on the pieces: their loads
+    // go out first, parked in the staging tile's upper half (unused at 128
+    // features; a row of kLd = kPRows + 1 floats holds both)
+    const bool norm = (ph.epi == kEpResid || ph.epi == kEpFuse) && sg.tw == 128;
+    float* xr = norm ? st + 128 * kLd + ct * kLd : nullptr;
+    if (xr) {
+      const int f0 = (t - sg.tile_begin) * sg.tw;
+      float v[kPRows];
+      load_resid(p, ph, f0, ct, v);
+      const float g = __bfloat162float(ph.gain[f0 + ct]);
 #pragma unroll
-      for (int j = 0; j < kR; ++j) acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
-      // pieces in CTA order, three at a time so that their loads overlap
-      for (int c = cf; c <= cl; c += 3) {
-        float4 a[3][kR];
-#pragma unroll
-        for (int u = 0; u < 3; ++u) {
-          const int cu = c + u <= cl ? c + u : c;
-          const float* src =
-              p.partial + (size_t)(cu * 2 + ((int)((cu * W / g) / ph.kb) == t ? 0 : 1)) * (kPRows * kTwMax) + fq;
-#pragma unroll
-          for (int j = 0; j < kR; ++j) {
-            const int m = r0 + 2 * j;
-            a[u][j] = (c + u <= cl && m < p.M) ? __ldcg(reinterpret_cast<const float4*>(src + m * kTwMax))
-                                               : make_float4(0.f, 0.f, 0.f, 0.f);
-          }
-        }
-#pragma unroll
-        for (int j = 0; j < kR; ++j)
-#pragma unroll
-          for (int u = 0; u < 3; ++u) {
-            acc[j].x += a[u][j].x;
-            acc[j].y += a[u][j].y;
-            acc[j].z += a[u][j].z;
-            acc[j].w += a[u][j].w;
-          }
-      }
-#pragma unroll
-      for (int j = 0; j < kR; ++j) {
-        const int m = r0 + 2 * j;
-        if (m < p.M) {
-          st[fq * kLd + m] = acc[j].x;
-          st[(fq + 1) * kLd + m] = acc[j].y;
-          st[(fq + 2) * kLd + m] = acc[j].z;
-          st[(fq + 3) * kLd + m] = acc[j].w;
-        }
-      }
+      for (int m = 0; m < kPRows; ++m) xr[m] = v[m];
+      xr[kPRows] = g;
     }
+    if (sg.tw == kTwMax)
+      sum_pieces<kTwMax>(p, ph, G, t, st, ct);
+    else
+      sum_pieces<128>(p, ph, G, t, st, ct);
     csync();
-    run_epilogue(p, ph, t, st, ct);
+    run_epilogue(p, ph, t, st, ct, xr);
     csync();
     if (ct == 0) p.tickets[t] = 0;
-    if (ct == 0 && last) trace_at(p, cta, pi, kTrRed);
   }
+  if (ct == 0 && npend) trace_at(p, cta, pi, kTrRed);
   return true;
 }
 
 // Attention of item = this CTA: (request, kv head, chunk of key tiles) on the
-// tensor cores (attn_tc.cuh), using the ring's shared memory and TMEM columns
-// 0..255 (idle between projections); partial (unnormalised output, max, sum)
+// tensor cores (attn_tc.cuh), using the ring's shared memory and all 512 TMEM
+// columns (idle between projections); partial (unnormalised output, max, sum)
 // rows to global memory, maxima in log2 units.  Returns false on a timeout.
 template <int HD>
 __device__ bool attn_phase(const PParams& p, const PPhase& ph, int pi, PBook* bk, uint8_t* sm, uint32_t tmem, int cta,
                            int ct, int& uses) {
   const AttnParams& ap = p.attn;
-  const int nch = ap.splits;
-  const int items = ap.B * ap.nkv * nch;
-  if (cta >= items) return true;
-  const int b = cta / (ap.nkv * nch), r = cta - b * ap.nkv * nch, kvh = r / nch, ch = r - kvh * nch;
-  const int c = ap.ctx_len[b];
-  const int nct = (c + attn_tc::kKeys - 1) / attn_tc::kKeys, T = nct + 1;
-  const int t0 = ch * T / nch, t1 = (ch + 1) * T / nch;
+  AttnItem item;
+  if (!attn_item(ap, cta, item)) return true;
+  const int b = item.b, kvh = item.kvh, t0 = item.t0, t1 = item.t1, nct = item.nct;
   const int rows = (ap.nq / ap.nkv) * ap.block;
   float* op = ap.opart + (size_t)cta * kPAttnRows * HD;
   float2* ml = ap.ml + (size_t)cta * kPAttnRows;
@@ -601,8 +681,10 @@ __device__ bool attn_phase(const PParams& p, const PPhase& ph, int pi, PBook* bk
     for (int j = 0; j < 32; j += 4) *reinterpret_cast<float4*>(dst + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
   };
   auto done = [&](int row, float m_log2, float l) { ml[row] = make_float2(m_log2, l); };
+  // trace slots kTrAcc..kTrRed of an attention phase: the core's stamps
+  unsigned long long* stamps = p.trace ? p.trace + ((size_t)cta * kPMaxPhases + pi) * kTrSlots + kTrAcc : nullptr;
   const bool ok = attn_tc::run<HD>(a, p.amaps, b, kvh, 0, t0, t1, nct, sm, tmem, &bk->abars, uses, ct, ComputeSync{},
-                                   p.status, out, done);
+                                   p.status, out, done, stamps);
   if (ct == 0) trace_at(p, cta, pi, kTrM1);
   return ok;
 }
