@@ -18,6 +18,8 @@ struct GemmPlan {
   size_t smem;            // dynamic shared memory per CTA
   size_t partial_floats;  // split-K scratch floats (0 if splits == 1)
   int counters;           // split-K tile counters (0 if splits == 1)
+  int dense;              // persistent many-row kernel: `grid` CTAs walk all tiles, no split-K
+  int grid;
 };
 
 // Decide the cut for an M x (tiles*128) x K product on a device with `sms` SMs.
@@ -25,6 +27,7 @@ struct GemmPlan {
 // `planes` = activation planes (2 for a hi/lo bf16 pair).
 GemmPlan plan_gemm(int dtype, int M, int K, int tiles, int sms, int tc, int planes);
 GemmPlan plan_gemm_tc(int M, int K, int tiles, int sms, int planes);
+size_t dense_smem(int stages);   // shared memory of the persistent many-row kernel
 
 // Tensor maps (CUtensorMap, 128 B each) for the tensor-core kernels: a weight
 // matrix [rows][inner] bf16 read in 64 x box_rows boxes (64 for the GEMM

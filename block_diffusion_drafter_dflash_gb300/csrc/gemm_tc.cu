@@ -19,6 +19,7 @@
 #include <cuda.h>
 
 #include <algorithm>
+#include <cstdio>
 #include <cstdlib>
 
 #include "gemm.cuh"
@@ -310,6 +311,185 @@ __global__ void __launch_bounds__(128, 1) gemm_tc_kernel(const __grid_constant__
   }
 }
 
+// ---------------------------------------------------------------- dense persistent kernel
+// Many token rows (tensor-bound): one CTA per SM walks the output tiles
+// (128 features x BN tokens) round-robin, tile = CTA + k * grid, the token
+// tiles of one weight tile adjacent so that CTAs running at the same time
+// read that weight tile from L2.  Roles (192 threads):
+//   warp 4 lane 0   TMA producer: weight halves and activation planes of every
+//                   K block into an S-stage ring
+//   warp 5          TMEM allocation (two 256-column accumulators); lane 0
+//                   issues tcgen05.mma, frees ring stages and signals each
+//                   finished accumulator with tcgen05.commit
+//   warps 0..3      epilogue of the previous tile (TMEM lanes 32w..32w+31)
+//                   while the MMAs of the next tile run
+// No split-K: every tile runs its whole K, so results match the one-tile
+// kernel's order of summation within a tile (fp32 accumulation in TMEM).
+constexpr int kDenseThreads = 192;
+
+template <int BN, int PL>
+struct DenseCfg {
+  using C = TcCfg<BN, PL>;
+  static constexpr int kLd = C::kChunk + 1;
+  static constexpr int kStBytes = kTileN * kLd * 4;   // epilogue staging tile
+  static size_t smem(int stages) {
+    return 1024 + (size_t)stages * C::kStageBytes + kStBytes + 8 * (2 * kMaxStages + 5) + 16;
+  }
+};
+
+template <int BN, int PL, class Epi>
+__global__ void __launch_bounds__(kDenseThreads, 1) gemm_dense_kernel(const __grid_constant__ CUtensorMap xmap,
+                                                                      const __grid_constant__ GemmProblem p,
+                                                                      const __grid_constant__ Epi epi,
+                                                                      int token_tiles, int32_t* status) {
+  using C = TcCfg<BN, PL>;
+  using D = DenseCfg<BN, PL>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int S = p.stages;
+  float* st = reinterpret_cast<float*>(smem + (size_t)S * C::kStageBytes);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)S * C::kStageBytes + D::kStBytes);
+  uint64_t* empty = full + kMaxStages;
+  uint64_t* accf = empty + kMaxStages;     // [2]
+  uint64_t* accfree = accf + 2;            // [2]
+  uint64_t* mdone = accfree + 2;           // every MMA of this CTA has finished
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mdone + 1);
+  int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int G = gridDim.x, ntiles = p.total_tiles * token_tiles, nk = p.K / 64;
+  const CUtensorMap* wmaps = static_cast<const CUtensorMap*>(p.wmaps);
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < S; ++i) {
+      ptx::mbar_init(full + i, 1);
+      ptx::mbar_init(empty + i, 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      ptx::mbar_init(accf + b, 1);
+      ptx::mbar_init(accfree + b, 1);
+    }
+    ptx::mbar_init(mdone, 1);
+    *abort_flag = 0;
+    ptx::fence_mbar_init();
+    ptx::prefetch_tmap(&xmap);
+  }
+  if (warp == 5) ptx::tmem_alloc(tmem_slot, 2 * C::kTmemCols);
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  griddep_trigger();
+
+  if (warp == 4) {
+    if (lane == 0) {
+      // ---- TMA producer
+      const uint64_t pol_w = ptx::policy_evict_first(), pol_x = ptx::policy_evict_last();
+      const int prow = static_cast<int>(p.plane_stride / p.ldx);
+      int it = 0;
+      bool waited = false;   // griddep_wait() done (activations of earlier kernels visible)
+      for (int tile = blockIdx.x; tile < ntiles && !*reinterpret_cast<volatile int*>(abort_flag); tile += G) {
+        const int gtile = tile / token_tiles, m0 = (tile - gtile * token_tiles) * BN;
+        const GemmSeg& sg = p.seg[find_seg(p, gtile)];
+        const int tis = gtile - sg.tile_begin;
+        const CUtensorMap* map0 = wmaps + sg.map0;
+        const CUtensorMap* map1 = wmaps + (sg.paired ? sg.map1 : sg.map0);
+        const int r0 = half_first_row(sg, tis, 0), r1 = half_first_row(sg, tis, 1);
+        for (int kb = 0; kb < nk; ++kb, ++it) {
+          const int s = it % S;
+          if (it >= S && !ptx::mbar_wait(empty + s, ((it / S) & 1) ^ 1, kWaitBudget, status)) {
+            *abort_flag = 1;
+            break;
+          }
+          uint8_t* a = smem + (size_t)s * C::kStageBytes;
+          ptx::mbar_arrive_expect_tx(full + s, C::kStageBytes);
+          // weights first: they do not depend on earlier kernels
+          ptx::tma_load_2d(a, map0, full + s, kb * 64, r0, pol_w);
+          ptx::tma_load_2d(a + kHalfN * 128, map1, full + s, kb * 64, r1, pol_w);
+          if (!waited) {
+            griddep_wait();
+            waited = true;
+          }
+#pragma unroll
+          for (int pl = 0; pl < PL; ++pl)
+            ptx::tma_load_2d(a + C::kABytes + pl * BN * 128, &xmap, full + s, kb * 64, pl * prow + m0, pol_x);
+        }
+      }
+      // every load issued lands before the CTA can exit
+      for (int j = max(0, it - S); j < it; ++j) ptx::mbar_wait(full + (j % S), (j / S) & 1, kWaitBudget, status);
+      if (!waited) griddep_wait();
+    }
+  } else if (warp == 5) {
+    if (lane == 0) {
+      // ---- MMA issuer
+      constexpr uint32_t idesc = ptx::idesc_bf16_f32(kTileN, C::kN);
+      int it = 0, seq = 0;
+      bool any = false;
+      for (int tile = blockIdx.x; tile < ntiles; tile += G, ++seq) {
+        const int buf = seq & 1, use = seq >> 1;
+        if (use >= 1 && !ptx::mbar_wait(accfree + buf, (use - 1) & 1, kWaitBudget, status)) break;
+        ptx::tc_fence_after();
+        const uint32_t d = tmem + buf * C::kTmemCols;
+        bool ok = true;
+        for (int kb = 0; kb < nk; ++kb, ++it) {
+          const int s = it % S;
+          if (!ptx::mbar_wait(full + s, (it / S) & 1, kWaitBudget, status)) {
+            ok = false;
+            break;
+          }
+          ptx::tc_fence_after();
+          const uint64_t ad = ptx::smem_desc_sw128(smem + (size_t)s * C::kStageBytes);
+          const uint64_t bd = ptx::smem_desc_sw128(smem + (size_t)s * C::kStageBytes + C::kABytes);
+#pragma unroll
+          for (int k = 0; k < 4; ++k) ptx::mma_bf16(d, ad + 2 * k, bd + 2 * k, idesc, (kb | k) != 0 ? 1u : 0u);
+          ptx::mma_commit(empty + s);
+          any = true;
+        }
+        if (!ok) break;
+        ptx::mma_commit(accf + buf);
+      }
+      if (any) {   // every MMA issued has finished before the tensor memory is freed
+        ptx::mma_commit(mdone);
+        ptx::mbar_wait(mdone, 0, kWaitBudget, status);
+      }
+    }
+  } else {
+    // ---- epilogue warps 0..3
+    const int tid = threadIdx.x, n = warp * 32 + lane;
+    constexpr int ld = D::kLd;
+    griddep_wait();   // outputs may be read by the kernel before this one
+    int seq = 0;
+    for (int tile = blockIdx.x; tile < ntiles; tile += G, ++seq) {
+      const int buf = seq & 1, use = seq >> 1;
+      if (!ptx::mbar_wait(accf + buf, use & 1, kWaitBudget, status)) break;
+      ptx::tc_fence_after();
+      const int gtile = tile / token_tiles, m0 = (tile - gtile * token_tiles) * BN, mc = min(BN, p.M - m0);
+      const GemmSeg& sg = p.seg[find_seg(p, gtile)];
+      const int tis = gtile - sg.tile_begin;
+      const uint32_t trow = tmem + buf * C::kTmemCols + (static_cast<uint32_t>(warp * 32) << 16);
+      for (int c0 = 0; c0 < mc; c0 += C::kChunk) {
+        float v[C::kChunk];
+        load_acc<BN, PL, C::kChunk>(trow, c0, v);
+#pragma unroll
+        for (int j = 0; j < C::kChunk; ++j) st[n * ld + j] = v[j];
+        if (c0 + C::kChunk >= mc) {   // the accumulator is read: the MMAs of tile + 2G may start
+          ptx::tc_fence_before();
+        }
+        asm volatile("bar.sync 1, 128;" ::: "memory");
+        if (c0 + C::kChunk >= mc && tid == 0) ptx::mbar_arrive(accfree + buf);
+        epi(st, ld, m0 + c0, min(C::kChunk, mc - c0), gtile, sg, tis, tid, 128);
+        asm volatile("bar.sync 1, 128;" ::: "memory");
+      }
+    }
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 5) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, 2 * C::kTmemCols);
+  }
+}
+
 // ---------------------------------------------------------------- host side
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
@@ -345,10 +525,40 @@ cudaError_t launch_bn(const GemmProblem& p, const GemmPlan& plan, const Epi& epi
   CUtensorMap xmap;
   if (!encode_activation_map(&xmap, p.x, p.K, rows, p.ldx, BN)) return cudaErrorInvalidValue;
   dim3 grid(p.total_tiles, plan.splits, plan.token_tiles);
+  static const bool log = std::getenv("DFLASH_GEMM_LOG") != nullptr;   // plan of every launch, to stderr
+  if (log)
+    std::fprintf(stderr, "gemm_tc M=%d K=%d tiles=%d BN=%d PL=%d splits=%d kb/split=%d stages=%d grid=%dx%dx%d%s\n",
+                 p.M, p.K, p.total_tiles, BN, PL, plan.splits, plan.kblocks_per_split, p.stages, grid.x, grid.y,
+                 grid.z, p.trace ? " [traced]" : "");
   return launch_pdl(gemm_tc_kernel<BN, PL, Epi>, grid, dim3(128), C::smem(p.stages), s, xmap, p, epi, p.status);
 }
 
+template <class Epi>
+cudaError_t launch_dense(const GemmProblem& p, const GemmPlan& plan, const Epi& epi, cudaStream_t s) {
+  using D = DenseCfg<128, 2>;
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(gemm_dense_kernel<128, 2, Epi>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)D::smem(4));
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  if (p.stages != 4 || plan.smem != D::smem(4) || p.planes != 2 || p.plane_stride % p.ldx || p.K % 64)
+    return cudaErrorInvalidValue;
+  const int rows = static_cast<int>(p.plane_stride / p.ldx) + p.M;
+  CUtensorMap xmap;
+  if (!encode_activation_map(&xmap, p.x, p.K, rows, p.ldx, 128)) return cudaErrorInvalidValue;
+  static const bool log = std::getenv("DFLASH_GEMM_LOG") != nullptr;
+  if (log)
+    std::fprintf(stderr, "gemm_dense M=%d K=%d tiles=%d token_tiles=%d grid=%d\n", p.M, p.K, p.total_tiles,
+                 plan.token_tiles, plan.grid);
+  return launch_pdl(gemm_dense_kernel<128, 2, Epi>, dim3(plan.grid), dim3(kDenseThreads), D::smem(4), s, xmap, p,
+                    epi, plan.token_tiles, p.status);
+}
+
 }  // namespace
+
+size_t dense_smem(int stages) { return DenseCfg<128, 2>::smem(stages); }
 
 bool encode_weight_map(void* map, const void* base, int inner, int rows, int box_rows) {
   EncodeTiledFn fn = encode_fn();
@@ -400,6 +610,21 @@ GemmPlan plan_gemm_tc(int M, int K, int tiles, int sms, int planes) {
   g.bm = M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : M <= 128 ? 128 : 256;
   g.bm = std::min(g.bm, bm_max);
   g.token_tiles = (M + g.bm - 1) / g.bm;
+  static const int env_dense = env_int("DFLASH_DENSE", 1);   // 0: never the persistent many-row kernel
+  const long dense_tiles = (long)tiles * g.token_tiles;
+  if (env_dense && planes == 2 && g.bm == 128 && g.token_tiles >= 2 && 4 * dense_tiles >= 3L * sms) {
+    // tensor-bound: a persistent kernel with every tile's whole K (no split-K
+    // reduction) and the epilogue overlapped with the next tile's MMAs
+    g.dense = 1;
+    g.grid = (int)std::min<long>(sms, dense_tiles);
+    g.stages = 4;
+    g.smem = dense_smem(g.stages);
+    g.splits = 1;
+    g.kblocks_per_split = K / 64;
+    g.partial_floats = 0;
+    g.counters = 0;
+    return g;
+  }
   const size_t sb = stage_bytes(g.bm, planes);
   const int s_max = std::min<int>(kMaxStages, (int)((kSmemMaxPerCta - 1024 - kBarBytes) / sb));
   const int kblocks = K / 64;
@@ -441,6 +666,7 @@ GemmPlan plan_gemm_tc(int M, int K, int tiles, int sms, int planes) {
 
 template <class Epi>
 cudaError_t gemm_tc_launch(const GemmProblem& p, const GemmPlan& plan, const Epi& epi, cudaStream_t s) {
+  if (plan.dense) return launch_dense<Epi>(p, plan, epi, s);
   if (plan.planes == 1) {   // operands that are exact in bf16 (target features)
     switch (plan.bm) {
       case 16: return launch_bn<16, 1, Epi>(p, plan, epi, s);
