@@ -3,7 +3,8 @@
 // output features n of global tile `gtile` and the token rows m0 .. m0+mc-1.
 // Threads tid = 0 .. nth-1 (a multiple of 128) call the functor together;
 // consecutive threads take consecutive features so that global stores are
-// coalesced.
+// coalesced (consecutive rows where the destination is feature-major: the
+// hd-major V of bf16 models).
 #pragma once
 
 #include "common.cuh"
@@ -96,6 +97,15 @@ struct EpiQKV {
     T* dkv = tag == 1 ? kb : vb;
     const int nh = tag == 0 ? nq : nkv, half = hd >> 1;
     const int planes = ActPlanes<T>::n;
+    if (tag == 2 && planes == 2) {   // bf16 V, hd-major: consecutive threads take consecutive rows
+      for (int idx = tid; idx < mc * kTileN; idx += nth) {
+        const int f = idx / mc, m = idx - f * mc;
+        const int row = m0 + m, b = row / block, k = row - b * block;
+        const int feat = tis * kTileN + f, head = feat / hd, d = feat - head * hd;
+        put_act(dkv, (size_t)hd * vpitch, (((size_t)b * nh + head) * 2 * hd + d) * vpitch + k, t[f * ld + m]);
+      }
+      return;
+    }
     const int n = tid & (kTileN - 1), step = nth / kTileN;
     const int feat = tis * kTileN + n, head = feat / hd, d = feat - head * hd;
     const int i = d < half ? d : d - half;
@@ -116,8 +126,6 @@ struct EpiQKV {
         const float r = tag == 2 ? v : (d < half ? v * sc[j].x - pv * sc[j].y : v * sc[j].x + pv * sc[j].y);
         if (tag == 0)
           q[(((size_t)b * nh + head) * block + k) * hd + d] = r;
-        else if (tag == 2 && planes == 2)   // bf16 V: hd-major
-          put_act(dkv, (size_t)hd * vpitch, (((size_t)b * nh + head) * 2 * hd + d) * vpitch + k, r);
         else
           put_act(dkv, (size_t)block * hd, (((size_t)b * nh + head) * planes * block + k) * hd + d, r);
       }
@@ -144,6 +152,19 @@ struct EpiInject {
     const int layer = sg.tag >> 1, is_v = sg.tag & 1, half = hd >> 1;
     T* dst = is_v ? vc : kc;
     const int planes = ActPlanes<T>::n;
+    if (is_v && planes == 2) {
+      // bf16 V is hd-major: consecutive threads take consecutive rows
+      // (positions) of one feature, so that a warp's stores are contiguous
+      for (int idx = tid; idx < mc * kTileN; idx += nth) {
+        const int f = idx / mc, m = idx - f * mc;
+        const int2 ri = __ldg(rowinfo + m0 + m);
+        if (ri.x < 0) continue;
+        const int feat = tis * kTileN + f, head = feat / hd, d = feat - head * hd;
+        put_act(dst, (size_t)hd * vpitch,
+                ((((size_t)ri.x * layers + layer) * nkv + head) * 2 * hd + d) * vpitch + ri.y, t[f * ld + m]);
+      }
+      return;
+    }
     const int n = tid & (kTileN - 1), step = nth / kTileN;
     const int feat = tis * kTileN + n, head = feat / hd, d = feat - head * hd;
     const int i = d < half ? d : d - half;
@@ -164,12 +185,8 @@ struct EpiInject {
         if (ri[j].x < 0) continue;
         const float v = t[n * ld + m], pv = t[pn * ld + m];
         const float r = is_v ? v : (d < half ? v * sc[j].x - pv * sc[j].y : v * sc[j].x + pv * sc[j].y);
-        if (is_v && planes == 2)   // bf16 V: hd-major
-          put_act(dst, (size_t)hd * vpitch,
-                  ((((size_t)ri[j].x * layers + layer) * nkv + head) * 2 * hd + d) * vpitch + ri[j].y, r);
-        else
-          put_act(dst, (size_t)cap * hd,
-                  ((((size_t)ri[j].x * layers + layer) * nkv + head) * planes * cap + ri[j].y) * hd + d, r);
+        put_act(dst, (size_t)cap * hd,
+                ((((size_t)ri[j].x * layers + layer) * nkv + head) * planes * cap + ri[j].y) * hd + d, r);
       }
     }
   }
