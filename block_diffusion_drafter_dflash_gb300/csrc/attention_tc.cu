@@ -1,11 +1,14 @@
 // Split-KV block attention of bf16 drafters on the tensor cores (tcgen05).
 //
-// One CTA of 128 threads per (split, kv head, request): the request's keys —
+// One CTA of 256 threads per (split, kv head, request): the request's keys —
 // its context in 128-key tiles, then one tile of the block's own keys — are
 // cut into `splits` ranges of whole tiles; the CTA runs the group's query rows
-// (64 per pass) over its range (attn_tc.cuh) and writes unnormalised partial
-// rows plus their (max, sum); attn_combine_kernel (attention.cu) merges the
-// splits.  Maxima are written in natural-log units, as the merge expects.
+// (64 per pass) over its range (attn_tc.cuh; the two warps of each TMEM lane
+// quarter split a tile's keys and output columns, since at one CTA per SM the
+// per-tile chain of read-back, softmax and P stores is the time) and writes
+// unnormalised partial rows plus their (max, sum); attn_combine_kernel
+// (attention.cu) merges the splits.  Maxima are written in natural-log units,
+// as the merge expects.
 #include <cuda.h>
 
 #include "attn_tc.cuh"
@@ -17,18 +20,23 @@ namespace {
 
 constexpr float kLn2 = 0.6931471805599453f;
 
+constexpr int kSplitThreads = 256;
+
 template <int HD>
 struct SplitSmem {
-  static constexpr size_t kBytes = 1024 + attn_tc::Cfg<HD>::kBytes + sizeof(attn_tc::Bars) + 16;
+  // operand tiles, barriers, the TMEM address slot, then 256 floats of
+  // row max / sum exchange between the two warps of a lane quarter
+  static constexpr size_t kXch = attn_tc::Cfg<HD>::kBytes + sizeof(attn_tc::Bars) + 16;
+  static constexpr size_t kBytes = 1024 + kXch + 256 * sizeof(float);
   static constexpr int kTmem = attn_tc::Cfg<HD>::kTmemCols <= 256 ? 256 : 512;
 };
 
-struct CtaSync128 {
+struct CtaSync {
   __device__ __forceinline__ void operator()() const { __syncthreads(); }
 };
 
 template <int HD>
-__global__ void __launch_bounds__(128, 1) attn_tc_split_kernel(const __grid_constant__ AttnParams p,
+__global__ void __launch_bounds__(kSplitThreads, 1) attn_tc_split_kernel(const __grid_constant__ AttnParams p,
                                                                const __grid_constant__ attn_tc::Maps maps,
                                                                int32_t* status) {
   using C = attn_tc::Cfg<HD>;
@@ -36,6 +44,7 @@ __global__ void __launch_bounds__(128, 1) attn_tc_split_kernel(const __grid_cons
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   attn_tc::Bars* bars = reinterpret_cast<attn_tc::Bars*>(sm + C::kBytes);
   uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 1);
+  float* xch = reinterpret_cast<float*>(sm + SplitSmem<HD>::kXch);
   const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x;
 
@@ -68,11 +77,11 @@ __global__ void __launch_bounds__(128, 1) attn_tc_split_kernel(const __grid_cons
   bool ok = true;
   for (int pass = 0; pass < passes && ok; ++pass) {
     if (t0 >= t1) {   // no keys here: an empty partial (weight 0 in the merge)
-      for (int e = tid; e < 64 * HD; e += 128) {
+      for (int e = tid; e < 64 * HD; e += kSplitThreads) {
         const int r = 64 * pass + e / HD;
         if (r < rows) p.opart[prow(r) * HD + e % HD] = 0.f;
       }
-      for (int i = tid; i < 64; i += 128)
+      for (int i = tid; i < 64; i += kSplitThreads)
         if (64 * pass + i < rows) p.ml[prow(64 * pass + i)] = make_float2(-3.0e38f, 0.f);
       continue;
     }
@@ -82,8 +91,8 @@ __global__ void __launch_bounds__(128, 1) attn_tc_split_kernel(const __grid_cons
       for (int j = 0; j < 32; j += 4) *reinterpret_cast<float4*>(dst + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
     };
     auto done = [&](int r, float m_log2, float l) { p.ml[prow(r)] = make_float2(m_log2 * kLn2, l); };
-    ok = attn_tc::run<HD>(p, maps, b, kvh, pass, t0, t1, nct, sm, tmem, bars, uses, tid, CtaSync128{}, status, out,
-                          done);
+    ok = attn_tc::run<HD, kSplitThreads>(p, maps, b, kvh, pass, t0, t1, nct, sm, tmem, bars, uses, tid, CtaSync{},
+                                         status, out, done, xch);
   }
   ptx::tc_fence_before();
   __syncthreads();
@@ -95,7 +104,7 @@ __global__ void __launch_bounds__(128, 1) attn_tc_split_kernel(const __grid_cons
 
 template <int HD>
 cudaError_t launch_hd(const AttnParams& p, const attn_tc::Maps& maps, int32_t* status, cudaStream_t s) {
-  return launch_pdl(attn_tc_split_kernel<HD>, dim3(p.splits, p.nkv, p.B), dim3(128), SplitSmem<HD>::kBytes, s, p,
+  return launch_pdl(attn_tc_split_kernel<HD>, dim3(p.splits, p.nkv, p.B), dim3(kSplitThreads), SplitSmem<HD>::kBytes, s, p,
                     maps, status);
 }
 

@@ -105,18 +105,18 @@ __device__ __forceinline__ void split8(const float* v, uint4& hi, uint4& lo) {
 }
 
 // Q rows [64*pass, 64*pass+64) of group (b, kvh) into the A tiles, scaled into
-// the log2 domain; rows past the group's rows are zero.  128 threads, each
-// with HD/16 chunks of 8 values: every load is issued before the first store,
-// so the whole tile costs one memory round trip.
-template <int HD>
+// the log2 domain; rows past the group's rows are zero.  NT threads (128 or
+// 256), each with 64*HD/(8*NT) chunks of 8 values: every load is issued before
+// the first store, so the whole tile costs one memory round trip.
+template <int HD, int NT>
 __device__ void stage_q(const AttnParams& p, int b, int kvh, int pass, uint8_t* sm, int tid) {
-  constexpr int kPer = 64 * (HD / 8) / 128;   // 8-value chunks per thread
+  constexpr int kPer = 64 * (HD / 8) / NT;   // 8-value chunks per thread
   const int G = p.nq / p.nkv, rows = G * p.block;
   const float qscale = p.scale * kLog2e;
   float4 x[kPer][2];
 #pragma unroll
   for (int u = 0; u < kPer; ++u) {
-    const int e = tid + 128 * u, i = e / (HD / 8), c8 = e - i * (HD / 8);
+    const int e = tid + NT * u, i = e / (HD / 8), c8 = e - i * (HD / 8);
     const int r = 64 * pass + i;
     if (r < rows) {
       const int gh = r / p.block, k = r - gh * p.block;
@@ -129,7 +129,7 @@ __device__ void stage_q(const AttnParams& p, int b, int kvh, int pass, uint8_t* 
   }
 #pragma unroll
   for (int u = 0; u < kPer; ++u) {
-    const int e = tid + 128 * u, i = e / (HD / 8), c8 = e - i * (HD / 8), s = c8 >> 3, ch = c8 & 7;
+    const int e = tid + NT * u, i = e / (HD / 8), c8 = e - i * (HD / 8), s = c8 >> 3, ch = c8 & 7;
     const float v[8] = {x[u][0].x * qscale, x[u][0].y * qscale, x[u][0].z * qscale, x[u][0].w * qscale,
                         x[u][1].x * qscale, x[u][1].y * qscale, x[u][1].z * qscale, x[u][1].w * qscale};
     uint4 hi, lo;
@@ -179,33 +179,42 @@ __device__ void load_v(const AttnParams& p, const Maps& m, int b, int kvh, int t
 }
 
 // One item: query rows of pass `pass` of group (b, kvh) against tiles [t0, t1)
-// (nct context tiles, then the block tile).  128 participating threads
-// (tid 0..127, warp w = tid/32 reads TMEM lanes 32w..32w+31, which must be the
-// warp's own lane quarter); thread 0 issues the TMA loads and the MMAs.
-// `uses` counts the tiles this CTA ran before (mbarrier phases).  On return
-// out(row, d0, v32) has received, for every valid row of the pass, its
-// unnormalised output in chunks of 32 columns, and done(row, m_log2, l) its
-// running max and sum.  Optional `stamps` (globaltimer): [0] Q staged, [1] the
-// first tile's scores ready, [2] the last P V done, [3] output written.
-// Returns false on a timeout.
-template <int HD, class Sync, class Out, class Done>
+// (nct context tiles, then the block tile).  NT participating threads (tid
+// 0..NT-1).  Warp w reads TMEM lanes 32(w%4)..32(w%4)+31, which must be its
+// own lane quarter.  With NT = 256 the two warps of a lane quarter split the
+// work of their 16 query rows: warp w < 4 takes keys 0..31 and 64..95 of every
+// tile, warp w+4 keys 32..63 and 96..127, and they halve the output columns;
+// the row maxima and sums go through `xch` (256 floats of shared memory).
+// Thread 0 issues the TMA loads and the MMAs.  `uses` counts the tiles this
+// CTA ran before (mbarrier phases).  On return out(row, d0, v32) has
+// received, for every valid row of the pass, its unnormalised output in
+// chunks of 32 columns, and done(row, m_log2, l) its running max and sum.
+// Optional `stamps` (globaltimer): [0] Q staged, [1] the first tile's scores
+// ready, [2] the last P V done, [3] output written, [4] the first V tile in
+// shared memory, [5] the first P tile stored.  Returns false on a timeout.
+template <int HD, int NT, class Sync, class Out, class Done>
 __device__ bool run(const AttnParams& p, const Maps& m, int b, int kvh, int pass, int t0, int t1, int nct,
                     uint8_t* sm, uint32_t tmem, Bars* bars, int& uses, int tid, Sync sync, int32_t* status, Out out,
-                    Done done, unsigned long long* stamps = nullptr) {
+                    Done done, float* xch = nullptr, unsigned long long* stamps = nullptr) {
+  static_assert(NT == 128 || NT == 256, "128 or 256 threads");
   using C = Cfg<HD>;
-  const int lane = tid & 31, w = tid >> 5;
+  constexpr int NP = NT / 128;        // warps per lane quarter
+  constexpr int KC = 64 / NP;         // keys of each 64-key half that one lane keeps
+  constexpr int DC = HD / NP;         // output columns one warp reads back
+  const int lane = tid & 31, w = tid >> 5, q4 = w & 3, part = w >> 2;
   const int G = p.nq / p.nkv, rows = G * p.block;
   const int c = p.ctx_len[b];
-  const uint32_t lanes = static_cast<uint32_t>(w * 32) << 16;
+  const uint32_t lanes = static_cast<uint32_t>(q4 * 32) << 16;
   const uint32_t tS = tmem + lanes, tO = tmem + lanes + 2 * kKeys;   // this warp's lanes
   const uint32_t idS = ptx::idesc_bf16_f32(128, 2 * kKeys), idO = ptx::idesc_bf16_f32(128, 2 * HD);
+  const int i = 16 * q4 + (lane & 15);   // query row of the pass held by this lane (hi part if lane < 16)
   bool ok = true;
 
   if (tid == 0 && t0 < t1) {
     load_k<HD>(p, m, b, kvh, t0, nct, sm, bars);
     load_v<HD>(p, m, b, kvh, t0, nct, sm, bars);
   }
-  stage_q<HD>(p, b, kvh, pass, sm, tid);
+  stage_q<HD, NT>(p, b, kvh, pass, sm, tid);
   ptx::fence_proxy_async_shared();
   sync();
   if (stamps && tid == 0) stamps[0] = ptx::globaltimer();
@@ -239,26 +248,33 @@ __device__ bool run(const AttnParams& p, const Maps& m, int b, int kvh, int pass
     if (tid == 0 && ok && t + 1 < t1) load_k<HD>(p, m, b, kvh, t + 1, nct, sm, bars);
 
     // ---- softmax of this warp's 16 rows: lanes l and l+16 hold a row's hi and
-    // lo accumulator rows; lane l < 16 keeps keys 0..63, lane l+16 keys 64..127,
-    // and each sends the partner the half it does not keep (one shuffle a key)
+    // lo accumulator rows; lane l < 16 keeps keys of the first 64-key half,
+    // lane l+16 of the second, and each sends the partner the half it does not
+    // keep (one shuffle a key).  This warp's keys: KC per half from KC*part.
     const int half = lane >> 4;
-    float pv[64];
+    float pv[KC];
 #pragma unroll
-    for (int c0 = 0; c0 < 64; c0 += 16) {
-      float v[64];   // [Khi keys c0.., Klo keys c0.., Khi keys 64+c0.., Klo keys 64+c0..]
-      ptx::tmem_ld16x4(tS + c0, tS + kKeys + c0, tS + 64 + c0, tS + kKeys + 64 + c0, v);
+    for (int c0 = 0; c0 < KC; c0 += 16) {
+      const int cc = KC * part + c0;
+      float v[64];   // [Khi keys cc.., Klo keys cc.., Khi keys 64+cc.., Klo keys 64+cc..]
+      ptx::tmem_ld16x4(tS + cc, tS + kKeys + cc, tS + 64 + cc, tS + kKeys + 64 + cc, v);
 #pragma unroll
       for (int j = 0; j < 16; ++j) {
         const float lo_keys = v[j] + v[16 + j], hi_keys = v[32 + j] + v[48 + j];
         const float got = __shfl_xor_sync(0xffffffffu, half ? lo_keys : hi_keys, 16);
         const float x = half ? hi_keys + got : lo_keys + got;
-        pv[c0 + j] = (64 * half + c0 + j < nk) ? x : kNegInf;
+        pv[c0 + j] = (64 * half + cc + j < nk) ? x : kNegInf;
       }
     }
     float mx = kNegInf;
 #pragma unroll
-    for (int j = 0; j < 64; ++j) mx = fmaxf(mx, pv[j]);
+    for (int j = 0; j < KC; ++j) mx = fmaxf(mx, pv[j]);
     mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+    if constexpr (NP == 2) {   // the row's maximum over both warps of the lane quarter
+      if (lane < 16) xch[64 * part + i] = mx;
+      sync();
+      mx = fmaxf(xch[i], xch[64 + i]);
+    }
     float alpha = 1.f;
     if (t == t0) {
       m_used = mx;
@@ -268,19 +284,19 @@ __device__ bool run(const AttnParams& p, const Maps& m, int b, int kvh, int pass
     }
     float sum = 0.f;
 #pragma unroll
-    for (int j = 0; j < 64; ++j) {
+    for (int j = 0; j < KC; ++j) {
       pv[j] = exp2f(pv[j] - m_used);
       sum += pv[j];
     }
     sum += __shfl_xor_sync(0xffffffffu, sum, 16);
-    l_sum = l_sum * alpha + sum;
+    l_sum = l_sum * alpha + sum;   // this warp's keys; the parts are added at the end
 
     // the previous P V has finished: P may be overwritten, O rescaled
     if (t > t0) ok = ptx::mbar_wait(&bars->odone, par ^ 1u, kBudget, status) && ok;
     ptx::tc_fence_after();
     if (__any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll 1
-      for (int d0 = 0; d0 < 2 * HD; d0 += 32) {
+      for (int d0 = 2 * DC * part; d0 < 2 * DC * (part + 1); d0 += 32) {
         float v[32];
         ptx::tmem_ld32(tO + d0, v);
 #pragma unroll
@@ -289,25 +305,27 @@ __device__ bool run(const AttnParams& p, const Maps& m, int b, int kvh, int pass
       }
     }
     {
-      const int i = 16 * w + (lane & 15);
       uint8_t* pt = sm + C::kOffP + half * kTile16;
       const int rh = a_row(i, 0), rl = a_row(i, 1);
 #pragma unroll
-      for (int ch = 0; ch < 8; ++ch) {
+      for (int cl = 0; cl < KC / 8; ++cl) {
+        const int ch = KC / 8 * part + cl;
         uint4 hi, lo;
-        split8(pv + 8 * ch, hi, lo);
+        split8(pv + 8 * cl, hi, lo);
         *reinterpret_cast<uint4*>(pt + sw(rh, ch)) = hi;
         *reinterpret_cast<uint4*>(pt + sw(rl, ch)) = lo;
       }
     }
     ptx::fence_proxy_async_shared();
     ptx::tc_fence_before();
+    if (stamps && tid == 0 && t == t0) stamps[5] = ptx::globaltimer();
     sync();
 
     // ---- O += P V (thread 0)
     if (tid == 0 && ok) {
       ptx::tc_fence_after();
       ok = ptx::mbar_wait(&bars->vfull, par, kBudget, status);
+      if (stamps && t == t0) stamps[4] = ptx::globaltimer();
       if (ok) {
 #pragma unroll
         for (int h = 0; h < 2; ++h)
@@ -326,9 +344,9 @@ __device__ bool run(const AttnParams& p, const Maps& m, int b, int kvh, int pass
     ok = ptx::mbar_wait(&bars->odone, static_cast<uint32_t>(uses + (t1 - 1 - t0)) & 1u, kBudget, status) && ok;
     ptx::tc_fence_after();
     if (stamps && tid == 0) stamps[2] = ptx::globaltimer();
-    const int i = 16 * w + (lane & 15), r = 64 * pass + i;
+    const int r = 64 * pass + i;
 #pragma unroll 1
-    for (int d0 = 0; d0 < HD; d0 += 32) {
+    for (int d0 = DC * part; d0 < DC * (part + 1); d0 += 32) {
       float v[64];   // O columns d0.. of the Vhi and the Vlo products
       ptx::tmem_ld32x2(tO + d0, tO + HD + d0, v);
 #pragma unroll
@@ -338,7 +356,12 @@ __device__ bool run(const AttnParams& p, const Maps& m, int b, int kvh, int pass
       }
       if (lane < 16 && r < rows) out(r, d0, v);
     }
-    if (lane < 16 && r < rows) done(r, m_used, l_sum);
+    if constexpr (NP == 2) {   // the row's sum over both warps of the lane quarter
+      if (lane < 16) xch[128 + 64 * part + i] = l_sum;
+      sync();
+      l_sum = xch[128 + i] + xch[192 + i];
+    }
+    if (lane < 16 && part == 0 && r < rows) done(r, m_used, l_sum);
     ptx::tc_fence_before();
     if (stamps && tid == 0) stamps[3] = ptx::globaltimer();
   }

@@ -683,8 +683,8 @@ __device__ bool attn_phase(const PParams& p, const PPhase& ph, int pi, PBook* bk
   auto done = [&](int row, float m_log2, float l) { ml[row] = make_float2(m_log2, l); };
   // trace slots kTrAcc..kTrRed of an attention phase: the core's stamps
   unsigned long long* stamps = p.trace ? p.trace + ((size_t)cta * kPMaxPhases + pi) * kTrSlots + kTrAcc : nullptr;
-  const bool ok = attn_tc::run<HD>(a, p.amaps, b, kvh, 0, t0, t1, nct, sm, tmem, &bk->abars, uses, ct, ComputeSync{},
-                                   p.status, out, done, stamps);
+  const bool ok = attn_tc::run<HD, 128>(a, p.amaps, b, kvh, 0, t0, t1, nct, sm, tmem, &bk->abars, uses, ct,
+                                        ComputeSync{}, p.status, out, done, nullptr, stamps);
   if (ct == 0) trace_at(p, cta, pi, kTrM1);
   return ok;
 }
