@@ -122,56 +122,70 @@ __global__ void __launch_bounds__(kAttnThreads) attn_split_kernel(const __grid_c
   }
 }
 
-// One CTA of 128 threads per (request, query head, block position): merge the
-// splits.  The per-split (max, sum) pairs are read in parallel and reduced in
-// shared memory; each thread then adds one output dimension over all splits.
+// Merge of the key splits: one warp per (request, query head, block
+// position) row, four rows per CTA of 128 threads.  Lane s holds split s's
+// (max, sum) and weight (32 splits at a time, broadcast by shuffles); lane l
+// owns output elements [E*l, E*l + E), E = hd / 32, read as one vector per
+// split.  Splits with weight 0 (no keys) are not read.
 template <typename T>
 __global__ void __launch_bounds__(128) attn_combine_kernel(const __grid_constant__ AttnParams p) {
-  extern __shared__ float w[];                 // [splits] weights, then 8 floats of scratch
-  float* red = w + p.splits;
   griddep_wait();
   griddep_trigger();
-  const int row = blockIdx.x;                  // ((b*nq + qh)*block + k)
+  const int lane = threadIdx.x & 31;
+  const int row = blockIdx.x * 4 + (threadIdx.x >> 5);   // ((b*nq + qh)*block + k)
+  if (row >= p.B * p.nq * p.block) return;
   const int k = row % p.block, qh = (row / p.block) % p.nq, b = row / (p.block * p.nq);
   const float2* ml = p.ml + (size_t)row * p.splits;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  float mx = -FLT_MAX;
-  for (int sp = threadIdx.x; sp < p.splits; sp += blockDim.x) {
+  float M = -FLT_MAX;
+  for (int sp = lane; sp < p.splits; sp += 32) {
     const float2 v = ml[sp];
-    w[sp] = v.y > 0.f ? v.x : -FLT_MAX;
-    mx = fmaxf(mx, w[sp]);
+    if (v.y > 0.f) M = fmaxf(M, v.x);
   }
-  for (int o = 16; o; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-  if (lane == 0) red[warp] = mx;
-  __syncthreads();
-  const float M = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
-  __syncthreads();
-  float l = 0.f;
-  for (int sp = threadIdx.x; sp < p.splits; sp += blockDim.x) {
-    const float2 v = ml[sp];
-    const float e = v.y > 0.f ? __expf(v.x - M) : 0.f;
-    w[sp] = e;
-    l += e * v.y;
+  for (int o = 16; o; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  const int E = p.hd >> 5;   // 2 or 4
+  float acc[4] = {0.f, 0.f, 0.f, 0.f}, l = 0.f;
+  const float* src = p.opart + (size_t)row * p.splits * p.hd + E * lane;
+  for (int s0 = 0; s0 < p.splits; s0 += 32) {
+    float wgt = 0.f;
+    if (s0 + lane < p.splits) {
+      const float2 v = ml[s0 + lane];
+      wgt = v.y > 0.f ? __expf(v.x - M) : 0.f;
+      l += wgt * v.y;
+    }
+    const int n = min(32, p.splits - s0);
+    for (int u0 = 0; u0 < n; u0 += 8) {   // eight splits' vectors in flight before any is used
+      float wu[8];
+      float4 x[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        wu[j] = __shfl_sync(0xffffffffu, wgt, (u0 + j) & 31);
+        if (u0 + j >= n) wu[j] = 0.f;
+        const float* sv = src + (size_t)(s0 + u0 + j) * p.hd;
+        x[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (wu[j] != 0.f) {   // the same for every lane
+          if (E == 4) {
+            x[j] = *reinterpret_cast<const float4*>(sv);
+          } else {
+            const float2 y = *reinterpret_cast<const float2*>(sv);
+            x[j].x = y.x;
+            x[j].y = y.y;
+          }
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        acc[0] += wu[j] * x[j].x;
+        acc[1] += wu[j] * x[j].y;
+        acc[2] += wu[j] * x[j].z;
+        acc[3] += wu[j] * x[j].w;
+      }
+    }
   }
   for (int o = 16; o; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
-  if (lane == 0) red[4 + warp] = l;
-  __syncthreads();
-  const float inv = 1.f / ((red[4] + red[5]) + (red[6] + red[7]));
-  const int d = threadIdx.x;
-  if (d >= p.hd) return;
-  const float* src = p.opart + (size_t)row * p.splits * p.hd + d;
-  float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
-  int sp = 0;
-  for (; sp + 4 <= p.splits; sp += 4) {
-    a0 += w[sp] * src[(size_t)sp * p.hd];
-    a1 += w[sp + 1] * src[(size_t)(sp + 1) * p.hd];
-    a2 += w[sp + 2] * src[(size_t)(sp + 2) * p.hd];
-    a3 += w[sp + 3] * src[(size_t)(sp + 3) * p.hd];
-  }
-  for (; sp < p.splits; ++sp) a0 += w[sp] * src[(size_t)sp * p.hd];
+  const float inv = 1.f / l;
   T* out = static_cast<T*>(p.out);
-  const size_t base = ((size_t)b * p.block + k) * p.nq * p.hd + (size_t)qh * p.hd;
-  put_act(out, p.out_plane, base + d, ((a0 + a1) + (a2 + a3)) * inv);
+  const size_t base = ((size_t)b * p.block + k) * p.nq * p.hd + (size_t)qh * p.hd + E * lane;
+  for (int e = 0; e < E; ++e) put_act(out, p.out_plane, base + e, acc[e] * inv);
 }
 
 size_t attn_smem_bytes(int rows, int hd) {
@@ -193,8 +207,7 @@ cudaError_t attention_bf16_launch(const AttnParams& p, const attn_tc::Maps& maps
   if (p.B <= 0) return cudaSuccess;
   cudaError_t e = attention_tc_split_launch(p, maps, status, s);
   if (e != cudaSuccess) return e;
-  return launch_pdl(attn_combine_kernel<__nv_bfloat16>, dim3(p.B * p.nq * p.block), dim3(128),
-                    (p.splits + 8) * sizeof(float), s, p);
+  return launch_pdl(attn_combine_kernel<__nv_bfloat16>, dim3((p.B * p.nq * p.block + 3) / 4), dim3(128), 0, s, p);
 }
 
 template <typename T>
@@ -205,8 +218,7 @@ cudaError_t attention_launch(const AttnParams& p, cudaStream_t s) {
   cudaError_t e = launch_pdl(attn_split_kernel<T>, dim3(p.splits, p.nkv, p.B), dim3(kAttnThreads),
                              attn_smem_bytes(rows, p.hd), s, p);
   if (e != cudaSuccess) return e;
-  return launch_pdl(attn_combine_kernel<T>, dim3(p.B * p.nq * p.block), dim3(128), (p.splits + 8) * sizeof(float), s,
-                    p);
+  return launch_pdl(attn_combine_kernel<T>, dim3((p.B * p.nq * p.block + 3) / 4), dim3(128), 0, s, p);
 }
 
 template cudaError_t attention_prepare<float>(int, int);

@@ -105,22 +105,23 @@ struct Span {
   int i0, i1;
 };
 
-__device__ __forceinline__ long long phase_iters(const PPhase& ph) { return (long long)ph.tiles * ph.kb; }
-__device__ __forceinline__ int phase_ctas(const PPhase& ph, int G) {
-  return (int)min((long long)G, phase_iters(ph));
-}
+// 32-bit arithmetic (a 64-bit division is a long software sequence, and the
+// reducer of a tile runs several before its first load): persist_launch
+// refuses a program whose tiles * kb * grid reaches 2^31.
+__device__ __forceinline__ int phase_iters(const PPhase& ph) { return ph.tiles * ph.kb; }
+__device__ __forceinline__ int phase_ctas(const PPhase& ph, int G) { return min(G, phase_iters(ph)); }
 // iterations [i0, i1) of CTA c (CTAs >= phase_ctas get none)
 __device__ __forceinline__ Span cta_span(const PPhase& ph, int G, int c) {
-  const long long W = phase_iters(ph);
+  const int W = phase_iters(ph);
   const int g = phase_ctas(ph, G);
   if (c >= g) return {0, 0};
-  return {(int)(c * W / g), (int)((c + 1) * W / g)};
+  return {c * W / g, (c + 1) * W / g};
 }
 // the CTA whose span holds iteration i
-__device__ __forceinline__ int cta_of(const PPhase& ph, int G, long long i) {
-  const long long W = phase_iters(ph);
+__device__ __forceinline__ int cta_of(const PPhase& ph, int G, int i) {
+  const int W = phase_iters(ph);
   const int g = phase_ctas(ph, G);
-  return (int)(((i + 1) * g - 1) / W);
+  return ((i + 1) * g - 1) / W;
 }
 __device__ __forceinline__ int seg_of(const PParams& p, const PPhase& ph, int t) {
   int s = ph.seg0;
@@ -463,9 +464,9 @@ template <int TW>
 __device__ void sum_pieces(const PParams& p, const PPhase& ph, int G, int t, float* st, int ct) {
   using PM = PieceMap<TW>;
   const int fq = 4 * (ct % PM::kQ), r0 = ct / PM::kQ;
-  const long long W = phase_iters(ph);
+  const int W = phase_iters(ph);
   const int g = phase_ctas(ph, G);
-  const int cf = cta_of(ph, G, (long long)t * ph.kb), cl = cta_of(ph, G, (long long)(t + 1) * ph.kb - 1);
+  const int cf = cta_of(ph, G, t * ph.kb), cl = cta_of(ph, G, (t + 1) * ph.kb - 1);
   float4 acc[PM::kR];
 #pragma unroll
   for (int j = 0; j < PM::kR; ++j) acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -475,7 +476,7 @@ __device__ void sum_pieces(const PParams& p, const PPhase& ph, int G, int t, flo
     for (int u = 0; u < PM::kU; ++u) {
       const int cu = min(c + u, cl);
       const float* src =
-          p.partial + (size_t)(cu * 2 + ((int)((cu * W / g) / ph.kb) == t ? 0 : 1)) * (kPRows * kTwMax) + fq;
+          p.partial + (size_t)(cu * 2 + ((cu * W / g) / ph.kb == t ? 0 : 1)) * (kPRows * kTwMax) + fq;
 #pragma unroll
       for (int j = 0; j < PM::kR; ++j) {
         const int m = r0 + PM::kStep * j;
@@ -614,7 +615,7 @@ __device__ bool gemm_phase(const PParams& p, const PPhase& ph, int pi, PBook* bk
     publish_piece(p, tw, st, p.partial + (size_t)(cta * 2 + (t == first_tile ? 0 : 1)) * (kPRows * kTwMax), ct);
     __threadfence();
     csync();
-    const int cf = cta_of(ph, G, (long long)t * ph.kb), cl = cta_of(ph, G, (long long)(t + 1) * ph.kb - 1);
+    const int cf = cta_of(ph, G, t * ph.kb), cl = cta_of(ph, G, (t + 1) * ph.kb - 1);
     if (ct == 0) {
       const int old = atomicAdd(p.tickets + t, 1);
       bk->flag_tk = old == cl - cf;
@@ -947,6 +948,8 @@ cudaError_t persist_launch(const PParams& p, int grid, int hd, cudaStream_t s) {
   if (attn_bytes > (size_t)p.stages * kStage + region_bytes(hd)) return cudaErrorInvalidValue;
   if (p.stages < 2 || p.stages > kPMaxStages || p.M < 1 || p.M > kPRows || p.nphase < 1 || p.nphase > kPMaxPhases)
     return cudaErrorInvalidValue;
+  for (int i = 0; i < p.nphase; ++i)   // the stream-K index arithmetic is 32-bit
+    if ((long long)p.ph[i].tiles * p.ph[i].kb * grid >= (1LL << 31)) return cudaErrorInvalidValue;
   return hd == 64 ? launch_hd<64>(p, grid, s) : launch_hd<128>(p, grid, s);
 }
 
