@@ -114,12 +114,22 @@ __device__ void stage_q(const AttnParams& p, int b, int kvh, int pass, uint8_t* 
   const int G = p.nq / p.nkv, rows = G * p.block;
   const float qscale = p.scale * kLog2e;
   float4 x[kPer][2];
+  // thread tid's chunks lie in rows r0, r0 + kRowStep, ...: (head, block
+  // position) of each follows from the previous one without a division
+  constexpr int kRowStep = NT / (HD / 8);
+  const int c8 = tid % (HD / 8), r0 = 64 * pass + tid / (HD / 8);
+  int gh = r0 / p.block, k = r0 - gh * p.block;
 #pragma unroll
   for (int u = 0; u < kPer; ++u) {
-    const int e = tid + NT * u, i = e / (HD / 8), c8 = e - i * (HD / 8);
-    const int r = 64 * pass + i;
+    const int r = r0 + kRowStep * u;
+    if (u > 0) {
+      k += kRowStep;
+      while (k >= p.block) {
+        k -= p.block;
+        ++gh;
+      }
+    }
     if (r < rows) {
-      const int gh = r / p.block, k = r - gh * p.block;
       const float* src = p.q + (((size_t)b * p.nq + kvh * G + gh) * p.block + k) * HD + 8 * c8;
       x[u][0] = __ldcg(reinterpret_cast<const float4*>(src));
       x[u][1] = __ldcg(reinterpret_cast<const float4*>(src + 4));
@@ -210,10 +220,9 @@ __device__ bool run(const AttnParams& p, const Maps& m, int b, int kvh, int pass
   const int i = 16 * q4 + (lane & 15);   // query row of the pass held by this lane (hi part if lane < 16)
   bool ok = true;
 
-  if (tid == 0 && t0 < t1) {
-    load_k<HD>(p, m, b, kvh, t0, nct, sm, bars);
-    load_v<HD>(p, m, b, kvh, t0, nct, sm, bars);
-  }
+  // the first tile's K now; its V once the scores are issued (it is needed
+  // only after the softmax, and the Q loads need not queue behind it)
+  if (tid == 0 && t0 < t1) load_k<HD>(p, m, b, kvh, t0, nct, sm, bars);
   stage_q<HD, NT>(p, b, kvh, pass, sm, tid);
   ptx::fence_proxy_async_shared();
   sync();
@@ -239,6 +248,8 @@ __device__ bool run(const AttnParams& p, const Maps& m, int b, int kvh, int pass
         if (t > t0) {   // the V buffer is free once the previous P V is done
           ok = ptx::mbar_wait(&bars->odone, par ^ 1u, kBudget, status);
           if (ok) load_v<HD>(p, m, b, kvh, t, nct, sm, bars);
+        } else {
+          load_v<HD>(p, m, b, kvh, t, nct, sm, bars);
         }
       }
     }

@@ -98,16 +98,26 @@ struct EpiQKV {
     const int nh = tag == 0 ? nq : nkv, half = hd >> 1;
     const int planes = ActPlanes<T>::n;
     if (tag == 2 && planes == 2) {   // bf16 V, hd-major: consecutive threads take consecutive rows
-      for (int idx = tid; idx < mc * kTileN; idx += nth) {
-        const int f = idx / mc, m = idx - f * mc;
+      if (mc <= 0) return;
+      const int hsh = 31 - __clz(hd);   // hd is a power of two
+      const int fstep = nth / mc, mstep = nth - fstep * mc;
+      int f = tid / mc, m = tid - f * mc;   // element tid, tid + nth, ... of the [feature][row] tile
+      while (f < kTileN) {
         const int row = m0 + m, b = row / block, k = row - b * block;
-        const int feat = tis * kTileN + f, head = feat / hd, d = feat - head * hd;
+        const int feat = tis * kTileN + f, head = feat >> hsh, d = feat & (hd - 1);
         put_act(dkv, (size_t)hd * vpitch, (((size_t)b * nh + head) * 2 * hd + d) * vpitch + k, t[f * ld + m]);
+        f += fstep;
+        m += mstep;
+        if (m >= mc) {
+          m -= mc;
+          ++f;
+        }
       }
       return;
     }
     const int n = tid & (kTileN - 1), step = nth / kTileN;
-    const int feat = tis * kTileN + n, head = feat / hd, d = feat - head * hd;
+    const int hsh = 31 - __clz(hd);   // hd is a power of two
+    const int feat = tis * kTileN + n, head = feat >> hsh, d = feat & (hd - 1);
     const int i = d < half ? d : d - half;
     const int pn = d < half ? n + half : n - half;
     for (int mb = tid / kTileN; mb < mc; mb += 8 * step) {
@@ -117,11 +127,18 @@ struct EpiQKV {
         const int m = mb + j * step;
         sc[j] = (tag != 2 && m < mc) ? __ldg(rope + (size_t)(m0 + m) * half + i) : make_float2(1.f, 0.f);
       }
+      int b = (m0 + mb) / block, k = m0 + mb - b * block;   // (request, block position) of row m0 + mb
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
         const int m = mb + j * step;
         if (m >= mc) break;
-        const int row = m0 + m, b = row / block, k = row - b * block;
+        if (j > 0) {   // the next row, `step` further on
+          k += step;
+          while (k >= block) {
+            k -= block;
+            ++b;
+          }
+        }
         const float v = t[n * ld + m], pv = t[pn * ld + m];
         const float r = tag == 2 ? v : (d < half ? v * sc[j].x - pv * sc[j].y : v * sc[j].x + pv * sc[j].y);
         if (tag == 0)
@@ -155,18 +172,29 @@ struct EpiInject {
     if (is_v && planes == 2) {
       // bf16 V is hd-major: consecutive threads take consecutive rows
       // (positions) of one feature, so that a warp's stores are contiguous
-      for (int idx = tid; idx < mc * kTileN; idx += nth) {
-        const int f = idx / mc, m = idx - f * mc;
+      if (mc <= 0) return;
+      const int hsh = 31 - __clz(hd);   // hd is a power of two
+      const int fstep = nth / mc, mstep = nth - fstep * mc;
+      int f = tid / mc, m = tid - f * mc;   // element tid, tid + nth, ... of the [feature][row] tile
+      while (f < kTileN) {
         const int2 ri = __ldg(rowinfo + m0 + m);
-        if (ri.x < 0) continue;
-        const int feat = tis * kTileN + f, head = feat / hd, d = feat - head * hd;
-        put_act(dst, (size_t)hd * vpitch,
-                ((((size_t)ri.x * layers + layer) * nkv + head) * 2 * hd + d) * vpitch + ri.y, t[f * ld + m]);
+        if (ri.x >= 0) {
+          const int feat = tis * kTileN + f, head = feat >> hsh, d = feat & (hd - 1);
+          put_act(dst, (size_t)hd * vpitch,
+                  ((((size_t)ri.x * layers + layer) * nkv + head) * 2 * hd + d) * vpitch + ri.y, t[f * ld + m]);
+        }
+        f += fstep;
+        m += mstep;
+        if (m >= mc) {
+          m -= mc;
+          ++f;
+        }
       }
       return;
     }
     const int n = tid & (kTileN - 1), step = nth / kTileN;
-    const int feat = tis * kTileN + n, head = feat / hd, d = feat - head * hd;
+    const int hsh = 31 - __clz(hd);   // hd is a power of two
+    const int feat = tis * kTileN + n, head = feat >> hsh, d = feat & (hd - 1);
     const int i = d < half ? d : d - half;
     const int pn = d < half ? n + half : n - half;
     for (int mb = tid / kTileN; mb < mc; mb += 8 * step) {
