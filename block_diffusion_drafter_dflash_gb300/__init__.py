@@ -20,7 +20,8 @@ from ._abi import DFlashError, check, lib
 __all__ = ["DFlashError", "Model", "Cache", "lib", "dflash_model_create", "dflash_cache_init",
            "dflash_workspace_bytes", "dflash_workspace", "dflash_inject_context", "dflash_draft_block",
            "dflash_verify_greedy", "dflash_get_status", "dflash_clear_status", "dflash_version",
-           "dflash_launch_count", "dflash_profile_start", "dflash_profile_stop", "dflash_inject_context_noalloc"]
+           "dflash_launch_count", "dflash_profile_start", "dflash_profile_stop", "dflash_inject_context_noalloc",
+           "dflash_selftest_wait_timeout"]
 
 
 def _stream_ptr(stream: Optional[torch.cuda.Stream]) -> ctypes.c_void_p:
@@ -245,6 +246,13 @@ def dflash_get_status(model: Model, stream=None) -> int:
 
 def dflash_clear_status(model: Model, stream=None) -> None:
     check(lib().dflash_clear_status(model.handle, _stream_ptr(stream)), "dflash_clear_status")
+
+
+def dflash_selftest_wait_timeout(model: Model, budget_cycles: int, stream=None) -> None:
+    """Run the bounded-wait self-test: a wait that nothing completes gives up
+    after budget_cycles SM cycles and sets the status word to DFLASH_ERR_TIMEOUT."""
+    check(lib().dflash_selftest_wait_timeout(model.handle, int(budget_cycles), _stream_ptr(stream)),
+          "dflash_selftest_wait_timeout")
 
 
 def dflash_launch_count() -> int:

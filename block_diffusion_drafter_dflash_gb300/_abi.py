@@ -49,6 +49,7 @@ SIGNATURES = {
     "dflash_model_destroy": (c_i32, [c_ptr]),
     "dflash_get_status": (c_i32, [c_ptr, c_ptr, c_i32p]),
     "dflash_clear_status": (c_i32, [c_ptr, c_ptr]),
+    "dflash_selftest_wait_timeout": (c_i32, [c_ptr, ctypes.c_int64, c_ptr]),
     "dflash_cache_bytes": (c_size, [ctypes.POINTER(Config), c_i32, c_i32]),
     "dflash_cache_init": (c_i32, [c_ptr, c_ptr, c_size, c_i32, c_i32, c_ptr, ctypes.POINTER(c_ptr)]),
     "dflash_cache_destroy": (c_i32, [c_ptr]),

@@ -786,6 +786,17 @@ int32_t dflash_clear_status(const dflash_model* m, dflash_stream_t stream) {
   return DFLASH_OK;
 }
 
+int32_t dflash_selftest_wait_timeout(const dflash_model* m, int64_t budget_cycles, dflash_stream_t stream) {
+  if (!m) return fail(DFLASH_ERR_INVALID_ARG, "model is NULL");
+  if (budget_cycles <= 0 || budget_cycles > (int64_t)4000000000LL)
+    return fail(DFLASH_ERR_INVALID_ARG, "budget_cycles %lld outside (0, 4e9]", (long long)budget_cycles);
+  int32_t rc = check_device(m);
+  if (rc) return rc;
+  DF_CUDA(wait_selftest_launch(budget_cycles, m->status_dev, (cudaStream_t)stream), "wait self-test");
+  g_launch_count += 1;
+  return DFLASH_OK;
+}
+
 size_t dflash_cache_bytes(const dflash_config* cfg, int32_t batch, int32_t capacity) {
   if (check_config(cfg) != DFLASH_OK || batch < 0 || capacity < 0) return 0;
   return align256(cache_k_bytes(cfg, batch, capacity)) + align256(cache_v_bytes(cfg, batch, capacity)) +

@@ -1,6 +1,7 @@
 // Row-wise kernels of the draft cycle: embedding gather, RMSNorms, the
 // injection row map, argmax read-out and greedy verification.
 #include "kernels.cuh"
+#include "ptx.cuh"
 
 namespace dflash {
 
@@ -362,5 +363,23 @@ cudaError_t verify_launch(const int32_t* draft, const int32_t* target, int B, in
 
 DFLASH_EW_INST(float)
 DFLASH_EW_INST(__nv_bfloat16)
+
+// Self-test of the bounded waits: one thread waits on a shared-memory
+// mbarrier that nothing ever arrives on, with the same bounded wait the
+// pipelines use; when `budget` SM cycles have passed it sets
+// DFLASH_ERR_TIMEOUT in the status word and the kernel returns.
+__global__ void wait_selftest_kernel(long long budget, int32_t* status) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(&bar, 1);
+    ptx::fence_mbar_init();
+    (void)ptx::mbar_wait(&bar, 0, budget, status);
+  }
+}
+
+cudaError_t wait_selftest_launch(long long budget_cycles, int32_t* status, cudaStream_t s) {
+  wait_selftest_kernel<<<1, 32, 0, s>>>(budget_cycles, status);
+  return cudaGetLastError();
+}
 
 }  // namespace dflash

@@ -88,6 +88,9 @@ cudaError_t synthetic_target_launch(const int32_t* draft, const uint8_t* match, 
                                     long long* tau_sum, int B, int g, int V, int32_t* y, cudaStream_t s);
 
 // Greedy verification, one warp per request.
+// One CTA whose bounded wait on an mbarrier that never completes runs out
+// after `budget_cycles` SM cycles and sets DFLASH_ERR_TIMEOUT in `status`.
+cudaError_t wait_selftest_launch(long long budget_cycles, int32_t* status, cudaStream_t s);
 cudaError_t verify_launch(const int32_t* draft, const int32_t* target, int B, int block, int32_t* accept_len,
                           int32_t* out_tokens, int32_t* next_anchor, cudaStream_t s);
 

@@ -134,6 +134,17 @@ int32_t dflash_model_destroy(dflash_model* model);
 int32_t dflash_get_status(const dflash_model* model, dflash_stream_t stream, int32_t* status_host);
 int32_t dflash_clear_status(const dflash_model* model, dflash_stream_t stream);
 
+/* Self-test of device-side failure detection (the paper has no counterpart).
+ * Launches one CTA on `stream` that waits, with the same bounded wait the
+ * kernels' pipelines use, on an mbarrier in its own shared memory that
+ * nothing ever arrives on.  After `budget_cycles` SM clock cycles (0 <
+ * budget_cycles <= 4e9; 2e6 is about a millisecond) the wait gives up, the
+ * kernel sets DFLASH_ERR_TIMEOUT in the model's status word and returns: no
+ * fault, and the context stays usable.  Read the result with
+ * dflash_get_status and clear it with dflash_clear_status.  Returns
+ * DFLASH_ERR_INVALID_ARG for a NULL model or a budget outside the range. */
+int32_t dflash_selftest_wait_timeout(const dflash_model* model, int64_t budget_cycles, dflash_stream_t stream);
+
 /* --- persistent draft KV cache (paper §4.1: context K/V stored in the draft
  * model's KV cache and reused across drafting iterations) ----------------------
  * Layout inside the caller's block of device memory (each region 256-B aligned):
