@@ -89,6 +89,7 @@ def test_null_handles_are_rejected(L):
     assert L.dflash_draft_block(None, None, None, 4, None, None, None, 0, None) == -1
     assert L.dflash_model_destroy(None) == 0
     assert L.dflash_workspace_bytes(None, 1, 1, 4, 4) == 0
+    assert L.dflash_selftest_wait_timeout(None, 1000, None) == -1
 
 
 def test_product_path_has_no_oracle_or_cpu_fallback():
