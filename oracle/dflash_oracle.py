@@ -30,7 +30,10 @@ complete dot product, unchanged by the chunking.
 Pins (tests/test_oracle_pins.py) tie each function to something other than
 itself: the printed mask matrix, the worked verification example, exhaustive
 brute force, the E[L] closed form by Monte Carlo, complex-number RoPE, library
-scaled-dot-product attention, invariants and special cases.  The end-to-end
+scaled-dot-product attention, invariants and special cases; the stochastic
+verification (verify_sampled) to the losslessness of speculative sampling
+(the first emitted token follows the target's distribution), the acceptance
+overlap sum_x min(p_t, p_d), its greedy limit and its special cases.  The end-to-end
 drafter logits have no printed values on the pages: beyond the component pins
 and the special cases in the tests, that composition is "parity unpinned".
 """
@@ -329,6 +332,53 @@ def verify_greedy(drafts: Sequence[int], target: Sequence[int]):
     out = [int(d) for d in drafts[:n]] + [int(target[n])]
     out = out + [-1] * (g - len(out))
     return n + 1, out, int(target[n])
+
+
+def sample_inverse_cdf(p: np.ndarray, u: float) -> int:
+    """The token a single uniform u in [0, 1) draws from distribution p: the
+    smallest id whose cumulative probability (ids in increasing order) exceeds
+    u; rounding that leaves u beyond the total falls back to the last id with
+    non-zero probability."""
+    p = np.asarray(p, dtype=F64)
+    c = np.cumsum(p)
+    idx = int(np.searchsorted(c, u, side="right"))   # c[idx] > u >= c[idx-1]: p[idx] > 0
+    if idx >= len(p):
+        idx = int(np.nonzero(p > 0.0)[0][-1])
+    return idx
+
+
+def verify_sampled(drafts: Sequence[int], p_draft: np.ndarray, p_target: np.ndarray,
+                   u_accept: Sequence[float], u_sample: float):
+    """Stochastic lossless verification of one block (explainer, "The Target
+    Verifier Remains the Correctness Anchor").
+
+    drafts d_1..d_n (n = block_size - 1), d_k drawn from the drafter's
+    distribution p_draft[k-1] ([n, V]); p_target [n+1, V], row k the target's
+    distribution for the token after block position k (row 0 judges d_1, as in
+    verify_greedy; row n gives the bonus).  Left to right, d_k is accepted iff
+    u_accept[k-1] < min(1, p_t(d_k) / p_d(d_k)); at the first rejection the
+    target draws a correction from its residual distribution and the rest of
+    the block is dropped; if every draft survives the target draws a bonus
+    token from p_target[n].  Reading of "residual distribution": the standard
+    one of lossless speculative sampling, max(0, p_t - p_d) normalised.  The
+    draw uses one uniform u_sample (sample_inverse_cdf).  The uniforms are
+    inputs.  Returns (tau, out[n+1] padded with -1, next_anchor) like
+    verify_greedy.
+    """
+    n = len(drafts)
+    p_draft, p_target = np.asarray(p_draft, dtype=F64), np.asarray(p_target, dtype=F64)
+    for k in range(n):
+        d = int(drafts[k])
+        pt, pd = p_target[k, d], p_draft[k, d]
+        accept = 1.0 if pd <= 0.0 else min(1.0, pt / pd)
+        if u_accept[k] < accept:
+            continue
+        resid = np.maximum(p_target[k] - p_draft[k], 0.0)
+        tok = sample_inverse_cdf(resid / resid.sum(), u_sample)
+        out = [int(x) for x in drafts[:k]] + [tok]
+        return k + 1, out + [-1] * (n + 1 - len(out)), tok
+    tok = sample_inverse_cdf(p_target[n], u_sample)
+    return n + 1, [int(x) for x in drafts] + [tok], tok
 
 
 def expected_accept_len(alpha: Sequence[float]) -> float:

@@ -414,3 +414,98 @@ def test_storage_mode_only_rounds_between_steps():
     assert np.max(np.abs(res["fp32"] - res["f64"])) / scale < 1e-5
     err = np.max(np.abs(res["bf16"] - res["f64"])) / scale
     assert 1e-5 < err < 5e-2
+
+
+# ---------------------------------------------------------------------------
+# Stochastic lossless verification (explainer, "The Target Verifier Remains the
+# Correctness Anchor"): pinned to the losslessness theorem of speculative
+# sampling and to its special cases, with the oracle's own decisions counted
+# over fine grids of the two uniforms (no random sampling, no retyped formula).
+# ---------------------------------------------------------------------------
+
+_GRID = (np.arange(4000) + 0.5) / 4000          # midpoints: fractions exact to 1/4000
+
+
+def _dist(rng, V, zeros=0):
+    p = rng.dirichlet(np.ones(V))
+    if zeros:
+        p[rng.choice(V, zeros, replace=False)] = 0.0
+        p /= p.sum()
+    return p
+
+
+def _accept_fraction(d, pd, pt):
+    """Share of u_accept values for which the oracle keeps draft d (block of 1 draft)."""
+    P_d, P_t = pd[None, :], np.stack([pt, pt])
+    return np.mean([oracle.verify_sampled([d], P_d, P_t, [u], 0.5)[0] == 2 for u in _GRID])
+
+
+def _correction_dist(d, pd, pt, V):
+    """Distribution of the correction after a rejection of draft d, over u_sample."""
+    P_d, P_t = pd[None, :], np.stack([pt, pt])
+    toks = [oracle.verify_sampled([d], P_d, P_t, [1.0 - 1e-12], u)[2] for u in _GRID]
+    return np.bincount(toks, minlength=V) / len(_GRID)
+
+
+@pytest.mark.parametrize("seed,zeros", [(0, 0), (1, 1), (2, 2)])
+def test_sampled_verify_is_lossless(seed, zeros):
+    """The first emitted token is distributed exactly as the target's p_t,
+    whatever the drafter's p_d: accepted drafts plus corrections."""
+    rng = np.random.default_rng(seed)
+    V = 5
+    pd, pt = _dist(rng, V, zeros), _dist(rng, V, zeros)
+    emitted = np.zeros(V)
+    for d in range(V):
+        if pd[d] == 0.0:
+            continue
+        a = _accept_fraction(d, pd, pt)
+        emitted[d] += pd[d] * a
+        if a < 1.0:
+            emitted += pd[d] * (1.0 - a) * _correction_dist(d, pd, pt, V)
+    assert np.allclose(emitted, pt, atol=2e-3), (emitted, pt)
+
+
+def test_sampled_verify_acceptance_is_the_overlap_of_the_distributions():
+    rng = np.random.default_rng(3)
+    V = 6
+    pd, pt = _dist(rng, V), _dist(rng, V)
+    accept = sum(pd[d] * _accept_fraction(d, pd, pt) for d in range(V))
+    assert abs(accept - np.minimum(pd, pt).sum()) < 1e-3
+
+
+def test_sampled_verify_bonus_follows_the_target_when_every_draft_survives():
+    rng = np.random.default_rng(4)
+    V, n = 5, 3
+    P = np.stack([_dist(rng, V) for _ in range(n + 1)])
+    drafts = [1, 3, 0]
+    toks = []
+    for u in _GRID:
+        tau, out, nxt = oracle.verify_sampled(drafts, P[:n], P, [0.999999] * n, u)   # p_d = p_t: always kept
+        assert tau == n + 1 and out[:n] == drafts and out[n] == nxt
+        toks.append(nxt)
+    assert np.allclose(np.bincount(toks, minlength=V) / len(_GRID), P[n], atol=1e-3)
+
+
+def test_sampled_verify_with_one_hot_distributions_is_greedy_verify():
+    rng = np.random.default_rng(5)
+    V = 4
+    for _ in range(300):
+        g = int(rng.integers(1, 6))
+        drafts = rng.integers(0, V, g - 1).tolist()
+        target = rng.integers(0, V, g).tolist()
+        P_d = np.eye(V)[drafts].reshape(g - 1, V)
+        P_t = np.eye(V)[target]
+        got = oracle.verify_sampled(drafts, P_d, P_t, rng.random(g - 1), float(rng.random()))
+        assert got == oracle.verify_greedy(drafts, target)
+
+
+def test_sampled_verify_rejects_a_token_the_target_never_emits():
+    """p_t(d) = 0: rejected for every u; with a one-hot drafter the residual is p_t itself."""
+    rng = np.random.default_rng(6)
+    V, d = 5, 2
+    pt = _dist(rng, V)
+    pt[d] = 0.0
+    pt /= pt.sum()
+    pd = np.eye(V)[d]
+    assert _accept_fraction(d, pd, pt) == 0.0
+    assert np.allclose(_correction_dist(d, pd, pt, V), pt, atol=1e-3)
