@@ -46,6 +46,7 @@ def parse():
     ap.add_argument("--workload", default="8b_bs1")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-bs32", action="store_true", help="skip the batch-32 sub-record of the default run")
     return ap.parse_args()
 
 
@@ -285,20 +286,50 @@ class Cycle:
         self.graph.replay()
 
 
-def run_gpu(args, rank, world, local):
+def method_bytes(wl, inject_rows: int) -> dict:
+    """Algorithmic DRAM bytes of one cycle as the method defines them: every
+    weight matrix read once (W_K/W_V count once: injection and drafter use the
+    same matrices), the context K/V of bf16 models at 2 bytes a value (20,480 B
+    per token at the 8B shape), the new tokens' target features."""
+    c = wl.cfg
+    es = c.elem_bytes
+    D, m, L = c.hidden, c.n_target_feats, c.layers
+    layers = es * L * c.layer_matrix_params()
+    lm = es * c.vocab * D
+    wc = es * D * m * D
+    kv = 2 * L * c.n_kv_heads * c.head_dim * es * sum(wl.ctx)
+    feats = es * inject_rows * m * D
+    return {"layers": layers, "lm_head": lm, "w_c": wc, "kv": kv, "features": feats,
+            "drafter": layers + lm + kv, "cycle": layers + lm + wc + kv + feats}
+
+
+def kv_storage_bytes(wl) -> int:
+    """Context K/V the attention reads as stored: fp32 precision (fp32 values,
+    or the hi and lo bf16 planes of bf16 models), 4 bytes a value."""
+    c = wl.cfg
+    return 2 * c.layers * c.n_kv_heads * c.head_dim * 4 * sum(wl.ctx)
+
+
+def kv_weight_bytes(cfg) -> int:
+    """Bytes of every layer's W_K and W_V (the injection's projection)."""
+    return cfg.elem_bytes * cfg.layers * 2 * cfg.n_kv_heads * cfg.head_dim * cfg.hidden
+
+
+def check_outputs(cyc) -> None:
+    """The timed cycle's results are valid: drafts are token ids, 1 <= tau <= block."""
+    d, t = cyc.drafts, cyc.tau
+    V, g = cyc.cfg.vocab, cyc.block
+    ok = bool(((d >= 0) & (d < V)).all().item()) and bool(((t >= 1) & (t <= g)).all().item())
+    if not ok:
+        raise RuntimeError("timed cycle produced invalid drafts or accepted lengths")
+
+
+def measure(wl, W, K, rank, world, local, barrier, want_e2e=True):
+    """Time whole cycles of workload `wl` (graph replay), then one profiled
+    eager pass; returns the bench record of that workload and the Cycle."""
     import block_diffusion_drafter_dflash_gb300 as df
-    torch.cuda.set_device(local)
-    wl = workloads()[args.workload]
-    W, K = args.warmup, args.steps
     total = W + 2 * K + 40
     cyc = Cycle(wl, total, rank)
-    dist = world > 1 and torch.distributed.is_initialized()
-
-    def barrier():
-        if dist:
-            torch.distributed.barrier()
-        torch.cuda.synchronize()
-
     for _ in range(W):
         cyc.step()
     n0 = df.dflash_launch_count()
@@ -319,6 +350,7 @@ def run_gpu(args, rank, world, local):
     barrier()
     launches = launches_per_cycle * K
     clk = clocks.stop()
+    check_outputs(cyc)
     ms = max_over_ranks(t0.elapsed_time(t1) / K, "cuda")
     mean_tau = float(cyc.tau_acc.item()) / (K * wl.batch)
     drafted = wl.batch * (wl.block - 1)
@@ -330,28 +362,38 @@ def run_gpu(args, rank, world, local):
     for _ in range(KP):
         cyc.step()
     prof = df.dflash_profile_stop(cyc.model)
+    # the synthetic target (a stand-in for the target model, not part of the
+    # method) timed on its own
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record()
+    for _ in range(KP):
+        df.dflash_synthetic_target(cyc.drafts, cyc.match, cyc.off, cyc.bonus, cyc.pidx, cyc.y, cyc.cfg.vocab)
+    ev1.record()
+    torch.cuda.synchronize()
+    target_ms = ev0.elapsed_time(ev1) / KP
     gb = gemm_bytes_per_cycle(wl.cfg, wl.batch, wl.block, cyc.rows)
     gf = gemm_flops_per_cycle(wl.cfg, wl.batch, wl.block, cyc.rows)
-    gemm_bytes = sum(gb.values())
+    mb = method_bytes(wl, int(round(mean_tau * wl.batch)))
     hbm, bf16, bf16_sus, src = load_peaks()
+    extra = {}
     if prof["draft_persist"][1] > 0:
         # one persistent launch runs the whole drafter pass: every layer's
         # projections and attention (context K/V read) and the LM head
-        kern_bytes = sum(gb[k] for k in ("qkv", "o", "gateup", "down", "lmhead")) + kv_bytes(wl)
+        kern_bytes = mb["drafter"]
+        stored = sum(gb[k] for k in ("qkv", "o", "gateup", "down", "lmhead")) + kv_storage_bytes(wl)
         kern_ms = prof["draft_persist"][0] / KP
         kern = "persist_kernel, drafter pass (one launch a cycle)"
         traffic = measured_traffic("persist", wl.name)
-        extra = {}
         if prof["inject_persist"][1] > 0:
-            inj_bytes, inj_ms = gb["fuse"] + gb["inject"], prof["inject_persist"][0] / KP
+            inj_bytes, inj_ms = mb["w_c"] + kv_weight_bytes(wl.cfg), prof["inject_persist"][0] / KP
             extra = {"injection_kernel_GBps": round(inj_bytes / (inj_ms / 1e3) / 1e9, 1),
                      "injection_kernel_ms_per_cycle": round(inj_ms, 4)}
     else:
-        kern_bytes = gemm_bytes
+        kern_bytes = sum(gb.values())
+        stored = kern_bytes
         kern_ms = sum(prof[s][0] for s in GEMM_STAGES) / KP
         kern = "projection GEMMs (all launches of one cycle)"
         traffic = measured_traffic("gemm", wl.name)
-        extra = {}
     kern_flops = sum(gf[k] for k in GEMM_STAGES) if prof["draft_persist"][1] == 0 else 0
     if kern_flops / (bf16_sus * 1e12) > kern_bytes / (hbm * 1e9):
         # many token rows: the projections are bound by the tensor cores; they
@@ -368,15 +410,15 @@ def run_gpu(args, rank, world, local):
         achieved = kern_bytes / (kern_ms / 1e3) / 1e9
         roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
                     "frac": round(achieved / hbm, 4), "traffic": traffic, "kernel": kern, "peak_source": src,
-                    "algorithmic_bytes_per_cycle": kern_bytes, "kernel_ms_per_cycle": round(kern_ms, 4), **extra}
+                    "algorithmic_bytes_per_cycle": kern_bytes,
+                    "stored_bytes_per_cycle": stored,
+                    "frac_of_stored_bytes": round(stored / (kern_ms / 1e3) / 1e9 / hbm, 4),
+                    "kernel_ms_per_cycle": round(kern_ms, 4), **extra}
     stages = {s: {"ms_per_cycle": round(v[0] / KP, 4), "launches_per_cycle": v[1] / KP} for s, v in prof.items()
               if v[1] > 0}
-    cycle_roof_ms = (gemm_bytes + kv_bytes(wl)) / (hbm * 1e9) * 1e3
+    cycle_roof_ms = mb["cycle"] / (hbm * 1e9) * 1e3
 
-    e2e = None
-    if not args.no_e2e:
-        e2e = run_e2e(cyc, K, wl, barrier, world)
-
+    e2e = run_e2e(cyc, K, wl, barrier, world) if want_e2e else None
     result = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": K, "warmup": W,
         "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
@@ -385,8 +427,13 @@ def run_gpu(args, rank, world, local):
         "config": {"workload": wl.name, "drafter": wl.cfg.name, "batch_per_gpu": wl.batch, "block": wl.block,
                    "ctx": wl.ctx if len(wl.ctx) <= 4 else f"{min(wl.ctx)}..{max(wl.ctx)} ({len(wl.ctx)} requests)",
                    "l2": "inputs larger than L2 (weights streamed every cycle)",
-                   "timing": "CUDA-graph replay of whole cycles; per-stage times from an eager pass with events",
-                   "mean_tau": round(mean_tau, 3), "accepted_tokens_per_s": round(world * mean_tau * wl.batch / (ms / 1e3), 1),
+                   "timing": "CUDA-graph replay of whole cycles (inject, draft, synthetic target, verify); "
+                             "per-stage times from an eager pass with events",
+                   "synthetic_target_ms_per_cycle": round(target_ms, 4),
+                   "ms_per_cycle_without_synthetic_target": round(ms - target_ms, 4),
+                   "mean_tau": round(mean_tau, 3),
+                   "accepted_tokens_per_s": round(world * mean_tau * wl.batch / (ms / 1e3), 1),
+                   "method_bytes_per_cycle": mb["cycle"],
                    "cycle_roofline_ms": round(cycle_roof_ms, 4),
                    "cycle_frac_of_hbm_roofline": round(cycle_roof_ms / ms, 4)},
         "roofline": roofline, "stages": stages, "gpu_launches": int(launches), "clocks": clk, "e2e": e2e,
@@ -394,10 +441,29 @@ def run_gpu(args, rank, world, local):
     return result, cyc
 
 
-def kv_bytes(wl) -> int:
-    """Context K/V read by the block attention in one cycle (fp32 cache)."""
-    c = wl.cfg
-    return 2 * c.layers * c.n_kv_heads * c.head_dim * 4 * sum(wl.ctx)
+def run_gpu(args, rank, world, local):
+    torch.cuda.set_device(local)
+    wl = workloads()[args.workload]
+    dist = world > 1 and torch.distributed.is_initialized()
+
+    def barrier():
+        if dist:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+
+    result, cyc = measure(wl, args.warmup, args.steps, rank, world, local, barrier, not args.no_e2e)
+    if args.workload == "8b_bs1" and not args.no_bs32:
+        # the metric's batch-32 half in the same run: the 8B-shaped drafter on
+        # 32 requests of ragged context (fewer cycles: each is ~4 ms)
+        result["_weights"] = cyc.weights
+        cyc = None
+        torch.cuda.empty_cache()
+        r32, c32 = measure(workloads()["8b_bs32"], 3, min(args.steps, 20), rank, world, local, barrier, False)
+        del c32
+        torch.cuda.empty_cache()
+        result["bs32"] = {k: r32[k] for k in ("value", "unit", "ms_per_step", "steps", "warmup", "config",
+                                               "roofline", "stages", "gpu_launches", "clocks")}
+    return result, cyc
 
 
 def run_e2e(cyc, K, wl, barrier, world):
@@ -522,8 +588,11 @@ def main():
         res = run_reference(args, rank, world, local)
     else:
         res, cyc = run_gpu(args, rank, world, local)
+        weights = res.pop("_weights", None)
+        if weights is None and cyc is not None:
+            weights = cyc.weights
         if rank == 0 and not args.no_cpu_baseline:
-            res["cpu_baseline"] = cpu_baseline(workloads()[args.workload], cyc.weights)
+            res["cpu_baseline"] = cpu_baseline(workloads()[args.workload], weights)
     if rank == 0 and res is not None:
         print(json.dumps(res), flush=True)
     if world > 1 and torch.distributed.is_initialized():

@@ -478,7 +478,7 @@ struct PhaseBuilder {
   // N side; a paired tile is 128 gate + 128 up rows; `ragged` lets the last
   // tile run past the matrix (its missing rows read as zeros).  The others
   // use 128-feature tiles with the weights on the M side.
-  bool all_wide = false;   // DFLASH_PERSIST_WIDE=1: every segment that allows it (experiments)
+  bool all_wide = false;   // DFLASH_DEBUG=1 DFLASH_PERSIST_WIDE=1: every segment that allows it (experiments)
   void seg(int map0, int map1, int features, int paired, int tag, bool wide = false, bool ragged = false) {
     PPhase& ph = p.ph[p.nphase - 1];
     GemmSeg& g = p.seg[ph.seg0 + ph.nseg++];
@@ -618,7 +618,7 @@ int32_t run_draft_persist(const dflash_model* m, const dflash_cache* cache, cons
     return fail(DFLASH_ERR_CUDA, "could not encode attention tensor maps");
 
   PhaseBuilder pb{pp};
-  if (const char* w = std::getenv("DFLASH_PERSIST_WIDE")) pb.all_wide = std::strcmp(w, "1") == 0;
+  if (const char* w = debug_env("DFLASH_PERSIST_WIDE")) pb.all_wide = std::strcmp(w, "1") == 0;
   for (int l = 0; l < c.layers; ++l) {
     const dflash_layer_weights& L = m->layers[l];
     pb.add_gemm(kEpQKV, D, 0, 2, kPRows, 1, nullptr);
@@ -1035,17 +1035,39 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratch
 constexpr int kMaxDevices = 64;
 std::mutex g_noalloc_mu;
 void* g_noalloc_ptr[kMaxDevices] = {};
+void* g_noalloc_ctx[kMaxDevices] = {};   // the context the address was looked up in
+
+// The current driver context (CUcontext), through the runtime's driver entry
+// point; nullptr if it cannot be had.
+void* current_context() {
+  using Fn = int (*)(void**);
+  static Fn fn = [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      f = nullptr;
+    return reinterpret_cast<Fn>(f);
+  }();
+  void* ctx = nullptr;
+  if (!fn || fn(&ctx) != 0) return nullptr;
+  return ctx;
+}
 
 // Device address of the scratch array on the current device, looked up once
-// per device (with that device current) and then reused.
+// per device and context (with that device current) and then reused; a
+// context created anew (after cudaDeviceReset, which unloads the module that
+// holds the array) gets a fresh look-up.
 int32_t noalloc_scratch(int dev, void** out) {
   if (dev < 0 || dev >= kMaxDevices) return fail(DFLASH_ERR_UNSUPPORTED, "device %d out of range", dev);
+  void* ctx = current_context();
   std::lock_guard<std::mutex> lock(g_noalloc_mu);
-  if (!g_noalloc_ptr[dev]) {
+  if (!g_noalloc_ptr[dev] || ctx == nullptr || ctx != g_noalloc_ctx[dev]) {
     void* p = nullptr;
     cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
     if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(noalloc scratch)");
     g_noalloc_ptr[dev] = p;
+    g_noalloc_ctx[dev] = ctx;
   }
   *out = g_noalloc_ptr[dev];
   return DFLASH_OK;

@@ -25,6 +25,17 @@ constexpr int kMaxBlock = 32;    // largest block_size (a warp per request in ve
 __device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void griddep_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
+// Experiment switches (ring depths, split factors, plan logging) are read
+// from the environment only when DFLASH_DEBUG=1: a normal process never has
+// its plans changed by a stray variable.  Returns the variable or nullptr.
+inline const char* debug_env(const char* name) {
+  static const bool on = [] {
+    const char* d = getenv("DFLASH_DEBUG");
+    return d && strcmp(d, "1") == 0;
+  }();
+  return on ? getenv(name) : nullptr;
+}
+
 inline bool pdl_enabled() {
   static int on = -1;
   if (on < 0) {

@@ -525,7 +525,7 @@ cudaError_t launch_bn(const GemmProblem& p, const GemmPlan& plan, const Epi& epi
   CUtensorMap xmap;
   if (!encode_activation_map(&xmap, p.x, p.K, rows, p.ldx, BN)) return cudaErrorInvalidValue;
   dim3 grid(p.total_tiles, plan.splits, plan.token_tiles);
-  static const bool log = std::getenv("DFLASH_GEMM_LOG") != nullptr;   // plan of every launch, to stderr
+  static const bool log = debug_env("DFLASH_GEMM_LOG") != nullptr;   // plan of every launch, to stderr
   if (log)
     std::fprintf(stderr, "gemm_tc M=%d K=%d tiles=%d BN=%d PL=%d splits=%d kb/split=%d stages=%d grid=%dx%dx%d%s\n",
                  p.M, p.K, p.total_tiles, BN, PL, plan.splits, plan.kblocks_per_split, p.stages, grid.x, grid.y,
@@ -548,7 +548,7 @@ cudaError_t launch_dense(const GemmProblem& p, const GemmPlan& plan, const Epi& 
   const int rows = static_cast<int>(p.plane_stride / p.ldx) + p.M;
   CUtensorMap xmap;
   if (!encode_activation_map(&xmap, p.x, p.K, rows, p.ldx, 128)) return cudaErrorInvalidValue;
-  static const bool log = std::getenv("DFLASH_GEMM_LOG") != nullptr;
+  static const bool log = debug_env("DFLASH_GEMM_LOG") != nullptr;
   if (log)
     std::fprintf(stderr, "gemm_dense M=%d K=%d tiles=%d token_tiles=%d grid=%d\n", p.M, p.K, p.total_tiles,
                  plan.token_tiles, plan.grid);
@@ -591,10 +591,11 @@ size_t tensor_map_bytes() { return sizeof(CUtensorMap); }
 // runs in waves of resident CTAs; a CTA streams its weight tiles at
 // min(HBM bandwidth / resident CTAs, bytes in flight / latency), and pays a
 // fixed start cost per wave plus a reduction tail when K is split.  The
-// cheapest plan wins.  DFLASH_TC_STAGES forces S; DFLASH_TC_KMIN is the fewest
-// 64-column K blocks per split (environment, read once).
-int env_int(const char* name, int dflt) {
-  const char* v = getenv(name);
+// cheapest plan wins.  With DFLASH_DEBUG=1, DFLASH_TC_STAGES forces S,
+// DFLASH_TC_KMIN is the fewest 64-column K blocks per split and
+// DFLASH_TC_SPLITS forces the split factor (environment, read once).
+int env_int(const char* name, int dflt, bool debug_only = true) {
+  const char* v = debug_only ? debug_env(name) : getenv(name);
   return v ? atoi(v) : dflt;
 }
 
@@ -610,7 +611,7 @@ GemmPlan plan_gemm_tc(int M, int K, int tiles, int sms, int planes) {
   g.bm = M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : M <= 128 ? 128 : 256;
   g.bm = std::min(g.bm, bm_max);
   g.token_tiles = (M + g.bm - 1) / g.bm;
-  static const int env_dense = env_int("DFLASH_DENSE", 1);   // 0: never the persistent many-row kernel
+  static const int env_dense = env_int("DFLASH_DENSE", 1, false);   // 0: never the persistent many-row kernel
   const long dense_tiles = (long)tiles * g.token_tiles;
   if (env_dense && planes == 2 && g.bm == 128 && g.token_tiles >= 2 && 4 * dense_tiles >= 3L * sms) {
     // tensor-bound: a persistent kernel with every tile's whole K (no split-K

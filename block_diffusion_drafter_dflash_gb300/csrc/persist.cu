@@ -61,6 +61,7 @@
 #include <cuda.h>
 
 #include <algorithm>
+#include <atomic>
 
 #include "attn_tc.cuh"
 #include "gemm.cuh"
@@ -910,15 +911,16 @@ cudaError_t launch_hd(const PParams& p, int grid, cudaStream_t s) {
   attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  // programmatic launch on top of the cooperative one where the runtime takes both
-  static int pdl_ok = 1;
-  cfg.numAttrs = (pdl_enabled() && pdl_ok) ? 2 : 1;
+  // programmatic launch on top of the cooperative one where the runtime takes
+  // both; once refused, never asked again (any host thread may launch)
+  static std::atomic<int> pdl_ok{1};
+  cfg.numAttrs = (pdl_enabled() && pdl_ok.load(std::memory_order_relaxed)) ? 2 : 1;
   cudaError_t e = cudaLaunchKernelEx(&cfg, persist_kernel<HD>, p);
   if (e != cudaSuccess && cfg.numAttrs == 2) {
     cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
     if (cudaStreamIsCapturing(s, &cs) == cudaSuccess && cs == cudaStreamCaptureStatusNone) {
       (void)cudaGetLastError();
-      pdl_ok = 0;
+      pdl_ok.store(0, std::memory_order_relaxed);
       cfg.numAttrs = 1;
       e = cudaLaunchKernelEx(&cfg, persist_kernel<HD>, p);
     }

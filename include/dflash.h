@@ -214,7 +214,10 @@ int32_t dflash_inject_context(const dflash_model* model, dflash_cache* cache, co
  *     DFLASH_ERR_CAPACITY without launching; inject fewer rows per call.
  *   - The first call on a device looks the array's device address up with
  *     cudaGetSymbolAddress (with that device current) and caches it; make that
- *     first call before any stream capture.
+ *     first call before any stream capture.  The cache is keyed on the
+ *     device's current context, so a call after cudaDeviceReset (which
+ *     unloads the module holding the array) looks the address up again —
+ *     that call, too, belongs before any capture.
  *   - Every call on a device shares the one array and leaves the last call's
  *     contents in it (what must start at zero is cleared by each call), so
  *     calls that overlap on the GPU — two streams, or two threads — race. */

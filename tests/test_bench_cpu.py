@@ -66,15 +66,28 @@ def test_8b_weight_bytes_match_the_documented_breakdown(bench):
     assert sum(got.values()) == drafter_and_fusion + got["inject"]
 
 
-def test_context_kv_bytes_count_both_planes_of_every_layer(bench):
+def test_context_kv_bytes_method_and_stored(bench):
     wl = workloads()["8b_bs1"]
-    # K and V, 5 layers, 8 kv heads of 128, 4 bytes a value (hi + lo bf16), 2048 tokens
-    assert bench.kv_bytes(wl) == 2 * 5 * 8 * 128 * 4 * 2048 == 83_886_080
+    # the method's cache: K and V, 5 layers, 8 kv heads of 128, bf16 (20,480 B a token), 2048 tokens
+    mb = bench.method_bytes(wl, inject_rows=8)
+    assert mb["kv"] == 2 * 5 * 8 * 128 * 2 * 2048 == 41_943_040
+    # as stored: hi and lo bf16 planes, 4 bytes a value
+    assert bench.kv_storage_bytes(wl) == 2 * 5 * 8 * 128 * 4 * 2048 == 83_886_080
+    # drafter launch: layer weights 1.929 GB + LM head 1.245 GB + K/V 41.9 MB = 3.216 GB
+    assert abs(mb["drafter"] / 1e9 - 3.216) < 1e-3
+    # whole cycle adds W_c and the 8 new tokens' 5 x 4096 bf16 features: 3.384 GB
+    assert mb["cycle"] == mb["drafter"] + 2 * 4096 * 20480 + 8 * 5 * 4096 * 2
+    assert abs(mb["cycle"] / 1e9 - 3.384) < 1e-3
+    assert bench.kv_weight_bytes(QWEN3_8B) == 2 * 5 * 2 * 1024 * 4096
 
 
-def test_traffic_profile_is_used_only_for_its_workload_and_sources(bench, monkeypatch):
-    value = bench.measured_traffic("persist", "8b_bs1")
-    assert value is not None and 3.2e9 < value < 3.5e9
+def test_traffic_profile_is_used_only_for_its_workload_and_sources(bench, monkeypatch, tmp_path):
+    prof = tmp_path / "traffic.md"
+    prof.write_text("# summary\n\nworkload: 8b_bs1\nsource_sha1: " + "a" * 40 + "\n"
+                    "traffic_bytes_per_cycle: 3323915712\n")
+    monkeypatch.setitem(bench.TRAFFIC_PROFILES, "persist", (str(prof), ["persist.cu"]))
+    monkeypatch.setattr(bench, "source_sha1", lambda names: "a" * 40)
+    assert bench.measured_traffic("persist", "8b_bs1") == 3323915712
     assert bench.measured_traffic("persist", "8b_bs32") is None
     monkeypatch.setattr(bench, "source_sha1", lambda names: "0" * 40)
     assert bench.measured_traffic("persist", "8b_bs1") is None

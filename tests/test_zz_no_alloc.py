@@ -55,6 +55,26 @@ def test_noalloc_injection_matches_workspace_injection_twice(cfg):
         _close(cache_b.v()[b, :, :, :c], a.cache.v()[b, :, :, :c], tol(cfg))
 
 
+def test_noalloc_8b_cycle_injection_of_32_rows():
+    """The largest injection of a cycle at batch 2 and block 16 is 32 rows;
+    the fixed scratch must hold its plan on this device (the split-K scratch
+    grows with the SM count), and the result must match the workspace path."""
+    cfg, rows = QWEN3_8B, 32
+    df, a, cache_b = _pair(cfg, rows, 16)
+    f = make_features(cfg, rows, seed=23, device="cuda")
+    counts = [20, 12]
+    n = torch.tensor(counts, dtype=torch.int32, device="cuda")
+    df.dflash_inject_context(a.model, a.cache, f, n, counts, rows, a.ws)
+    df.dflash_inject_context_noalloc(a.model, cache_b, f, n, counts, rows)
+    torch.cuda.synchronize()
+    assert df.dflash_get_status(a.model) == 0
+    assert a.cache.ctx_len().cpu().tolist() == cache_b.ctx_len().cpu().tolist() == counts
+    for b in range(2):
+        c = counts[b]
+        _close(cache_b.k()[b, :, :, :c], a.cache.k()[b, :, :, :c], tol(cfg))
+        _close(cache_b.v()[b, :, :, :c], a.cache.v()[b, :, :, :c], tol(cfg))
+
+
 def test_noalloc_rejects_launches_beyond_its_scratch():
     import block_diffusion_drafter_dflash_gb300 as df
     cfg = QWEN3_8B
