@@ -21,7 +21,8 @@ __all__ = ["DFlashError", "Model", "Cache", "lib", "dflash_model_create", "dflas
            "dflash_workspace_bytes", "dflash_workspace", "dflash_inject_context", "dflash_draft_block",
            "dflash_verify_greedy", "dflash_get_status", "dflash_clear_status", "dflash_version",
            "dflash_launch_count", "dflash_profile_start", "dflash_profile_stop", "dflash_inject_context_noalloc",
-           "dflash_selftest_wait_timeout"]
+           "dflash_selftest_wait_timeout", "dflash_sampling_workspace", "dflash_verify_sampled", "dflash_sample_tokens",
+           "BlockPolicy"]
 
 
 def _stream_ptr(stream: Optional[torch.cuda.Stream]) -> ctypes.c_void_p:
@@ -221,6 +222,98 @@ def dflash_verify_greedy(draft_dev: torch.Tensor, target_argmax_dev: torch.Tenso
     check(lib().dflash_verify_greedy(_ptr(draft_dev), _ptr(target_argmax_dev), B, g, _ptr(accept_len_dev),
                                      _ptr(out_tokens_dev), _ptr(next_anchor_dev), _stream_ptr(stream)),
           "dflash_verify_greedy")
+
+
+def dflash_sampling_workspace(rows: int, draws: int, vocab: int) -> torch.Tensor:
+    """Device scratch for dflash_verify_sampled / dflash_sample_tokens."""
+    n = int(lib().dflash_sampling_workspace_bytes(int(rows), int(draws), int(vocab)))
+    if n == 0:
+        raise ValueError("invalid sampling workspace shape")
+    return torch.empty(n, dtype=torch.uint8, device="cuda")
+
+
+def dflash_verify_sampled(draft_logits: Optional[torch.Tensor], target_logits: torch.Tensor,
+                          drafts: Optional[torch.Tensor], u_accept: Optional[torch.Tensor], u_sample: torch.Tensor,
+                          temperature: float, accept_len: torch.Tensor, out_tokens: torch.Tensor,
+                          next_anchor: torch.Tensor, workspace: Optional[torch.Tensor] = None, stream=None) -> None:
+    """Stochastic lossless verification: draft logits fp32 [B, g-1, V], target
+    logits fp32 [B, g, V], drafts int32 [B, g-1], uniforms fp32 u_accept
+    [B, g-1] and u_sample [B] -> tau [B], out [B, g], next anchor [B]."""
+    B, g, V = target_logits.shape
+    for t in (draft_logits, target_logits, u_accept, u_sample):
+        if t is not None and t.dtype != torch.float32:
+            raise ValueError("logits and uniforms must be float32")
+    for t in (drafts, accept_len, out_tokens, next_anchor):
+        if t is not None and t.dtype != torch.int32:
+            raise ValueError("token tensors must be int32")
+    if workspace is None:
+        workspace = dflash_sampling_workspace(B * (2 * g - 1), B, V)
+    check(lib().dflash_verify_sampled(_ptr(draft_logits), _ptr(target_logits), _ptr(drafts), _ptr(u_accept),
+                                      _ptr(u_sample), B, g, V, float(temperature), _ptr(accept_len),
+                                      _ptr(out_tokens), _ptr(next_anchor), _ptr(workspace), workspace.numel(),
+                                      _stream_ptr(stream)), "dflash_verify_sampled")
+
+
+def dflash_sample_tokens(logits: torch.Tensor, temperature: float, u: torch.Tensor, tokens: torch.Tensor,
+                         workspace: Optional[torch.Tensor] = None, stream=None) -> None:
+    """tokens[r] = inverse-CDF draw with uniform u[r] from softmax(logits[r] / T); logits fp32 [..., V]."""
+    V = logits.shape[-1]
+    rows = logits.numel() // V
+    if logits.dtype != torch.float32 or u.dtype != torch.float32 or tokens.dtype != torch.int32:
+        raise ValueError("logits and u must be float32, tokens int32")
+    if workspace is None:
+        workspace = dflash_sampling_workspace(rows, rows, V)
+    check(lib().dflash_sample_tokens(_ptr(logits), rows, V, float(temperature), _ptr(u), _ptr(tokens),
+                                     _ptr(workspace), workspace.numel(), _stream_ptr(stream)), "dflash_sample_tokens")
+
+
+class BlockPolicy:
+    """Host block-size scheduling policy (dflash_block_policy_*): observe each
+    cycle's accepted lengths, choose the next cycle's block size."""
+
+    def __init__(self, candidates, cost_fixed_ms: float, cost_per_row_ms: float, cost_per_request_ms: float = 0.0,
+                 decay: float = 0.9, prior_accept: float = 0.8, prior_weight: float = 2.0):
+        cfg = _abi.PolicyConfig()
+        cand = [int(c) for c in candidates]
+        if len(cand) > _abi.POLICY_MAX_CANDIDATES:
+            raise ValueError("too many candidates")
+        cfg.n_candidates = len(cand)
+        for i, c in enumerate(cand):
+            cfg.candidates[i] = c
+        cfg.cost_fixed_ms, cfg.cost_per_row_ms, cfg.cost_per_request_ms = cost_fixed_ms, cost_per_row_ms, \
+            cost_per_request_ms
+        cfg.decay, cfg.prior_accept, cfg.prior_weight = decay, prior_accept, prior_weight
+        h = ctypes.c_void_p()
+        check(lib().dflash_block_policy_create(ctypes.byref(cfg), ctypes.byref(h)), "dflash_block_policy_create")
+        self.handle = h
+        self.candidates = cand
+
+    def observe(self, block_size: int, taus) -> None:
+        arr = (ctypes.c_int32 * len(taus))(*[int(t) for t in taus])
+        check(lib().dflash_block_policy_observe(self.handle, int(block_size), arr, len(taus)),
+              "dflash_block_policy_observe")
+
+    def choose(self, batch: int):
+        g, e = ctypes.c_int32(0), ctypes.c_double(0.0)
+        check(lib().dflash_block_policy_choose(self.handle, int(batch), ctypes.byref(g), ctypes.byref(e)),
+              "dflash_block_policy_choose")
+        return g.value, e.value
+
+    def acceptance(self, n: int):
+        out = (ctypes.c_double * n)()
+        check(lib().dflash_block_policy_acceptance(self.handle, out, n), "dflash_block_policy_acceptance")
+        return list(out)
+
+    def close(self):
+        if getattr(self, "handle", None) is not None and self.handle.value:
+            lib().dflash_block_policy_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
 
 
 def dflash_synthetic_target(drafts: torch.Tensor, match: torch.Tensor, off: torch.Tensor, bonus: torch.Tensor,

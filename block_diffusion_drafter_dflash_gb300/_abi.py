@@ -41,6 +41,16 @@ class Weights(ctypes.Structure):
                 ("layers", ctypes.POINTER(LayerWeights))]
 
 
+POLICY_MAX_CANDIDATES = 16
+
+
+class PolicyConfig(ctypes.Structure):
+    _fields_ = [("n_candidates", c_i32), ("candidates", c_i32 * POLICY_MAX_CANDIDATES),
+                ("cost_fixed_ms", ctypes.c_float), ("cost_per_row_ms", ctypes.c_float),
+                ("cost_per_request_ms", ctypes.c_float), ("decay", ctypes.c_float),
+                ("prior_accept", ctypes.c_float), ("prior_weight", ctypes.c_float)]
+
+
 # name -> (restype, argtypes)
 SIGNATURES = {
     "dflash_version": (c_i32, []),
@@ -61,6 +71,15 @@ SIGNATURES = {
     "dflash_noalloc_scratch_bytes": (c_size, []),
     "dflash_inject_context_noalloc": (c_i32, [c_ptr, c_ptr, c_ptr, c_ptr, c_i32p, c_i32, c_ptr]),
     "dflash_verify_greedy": (c_i32, [c_ptr, c_ptr, c_i32, c_i32, c_ptr, c_ptr, c_ptr, c_ptr]),
+    "dflash_sampling_workspace_bytes": (c_size, [c_i32, c_i32, c_i32]),
+    "dflash_verify_sampled": (c_i32, [c_ptr, c_ptr, c_ptr, c_ptr, c_ptr, c_i32, c_i32, c_i32, ctypes.c_float, c_ptr,
+                                      c_ptr, c_ptr, c_ptr, c_size, c_ptr]),
+    "dflash_sample_tokens": (c_i32, [c_ptr, c_i32, c_i32, ctypes.c_float, c_ptr, c_ptr, c_ptr, c_size, c_ptr]),
+    "dflash_block_policy_create": (c_i32, [ctypes.POINTER(PolicyConfig), ctypes.POINTER(c_ptr)]),
+    "dflash_block_policy_destroy": (c_i32, [c_ptr]),
+    "dflash_block_policy_observe": (c_i32, [c_ptr, c_i32, c_i32p, c_i32]),
+    "dflash_block_policy_choose": (c_i32, [c_ptr, c_i32, c_i32p, ctypes.POINTER(ctypes.c_double)]),
+    "dflash_block_policy_acceptance": (c_i32, [c_ptr, ctypes.POINTER(ctypes.c_double), c_i32]),
     "dflash_launch_count": (ctypes.c_uint64, []),
     "dflash_synthetic_target": (c_i32, [c_ptr, c_ptr, c_ptr, c_ptr, c_i32, c_ptr, c_ptr, c_ptr, c_i32, c_i32, c_i32,
                                         c_ptr, c_ptr]),

@@ -16,6 +16,7 @@
 #include "kernels.cuh"
 #include "attn_tc.cuh"
 #include "persist.cuh"
+#include "sampling.cuh"
 
 using namespace dflash;
 
@@ -83,6 +84,14 @@ int32_t fail(int32_t code, const char* fmt, ...) {
   g_last_error = buf;
   return code;
 }
+
+}  // namespace
+
+namespace dflash {
+int32_t set_error(int32_t code, const char* msg) { return fail(code, "%s", msg); }
+}  // namespace dflash
+
+namespace {
 
 int32_t cuda_fail(cudaError_t e, const char* what) {
   return fail(DFLASH_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
@@ -948,6 +957,67 @@ int32_t dflash_verify_greedy(const int32_t* draft_dev, const int32_t* target_arg
   DF_CUDA(verify_launch(draft_dev, target_argmax_dev, batch, block_size, accept_len_dev, out_tokens_dev,
                         next_anchor_dev, (cudaStream_t)stream), "verify");
   g_launch_count += 1;
+  return DFLASH_OK;
+}
+
+size_t dflash_sampling_workspace_bytes(int32_t rows, int32_t draws, int32_t vocab) {
+  if (rows < 0 || draws < 0 || vocab <= 0) return 0;
+  return sampling_workspace_bytes(std::max(rows, 1), std::max(draws, 1), vocab);
+}
+
+namespace {
+int32_t check_sampling(const void* p_logits, int rows, int vocab, float temperature, const void* ws, size_t ws_bytes,
+                       int draws) {
+  if (vocab <= 0 || vocab % 4 || vocab > (1 << 24))
+    return fail(DFLASH_ERR_SHAPE, "vocab %d must be a positive multiple of 4, at most 2^24", vocab);
+  if (rows > 65535) return fail(DFLASH_ERR_SHAPE, "%d logits rows > 65535", rows);
+  if (!(temperature > 0.f) || !std::isfinite(temperature))
+    return fail(DFLASH_ERR_INVALID_ARG, "temperature must be positive and finite");
+  if (reinterpret_cast<uintptr_t>(p_logits) % 16) return fail(DFLASH_ERR_INVALID_ARG, "logits must be 16-byte aligned");
+  if (!ws) return fail(DFLASH_ERR_INVALID_ARG, "workspace is NULL");
+  const size_t need = sampling_workspace_bytes(rows, draws, vocab);
+  if (ws_bytes < need) return fail(DFLASH_ERR_WORKSPACE, "workspace %zu bytes < %zu needed", ws_bytes, need);
+  return DFLASH_OK;
+}
+}  // namespace
+
+int32_t dflash_verify_sampled(const float* draft_logits, const float* target_logits, const int32_t* drafts,
+                              const float* u_accept, const float* u_sample, int32_t batch, int32_t block_size,
+                              int32_t vocab, float temperature, int32_t* accept_len, int32_t* out_tokens,
+                              int32_t* next_anchor, void* workspace, size_t ws_bytes, dflash_stream_t stream) {
+  if (batch < 0) return fail(DFLASH_ERR_INVALID_ARG, "batch %d < 0", batch);
+  if (block_size < 1 || block_size > kMaxBlock)
+    return fail(DFLASH_ERR_SHAPE, "block_size %d outside [1, %d]", block_size, kMaxBlock);
+  if (batch == 0) return DFLASH_OK;
+  if ((block_size > 1 && (!draft_logits || !drafts || !u_accept)) || !target_logits || !u_sample || !accept_len ||
+      !out_tokens || !next_anchor)
+    return fail(DFLASH_ERR_INVALID_ARG, "a device pointer is NULL");
+  if (block_size > 1 && reinterpret_cast<uintptr_t>(draft_logits) % 16)
+    return fail(DFLASH_ERR_INVALID_ARG, "logits must be 16-byte aligned");
+  const int rows = batch * (2 * block_size - 1);
+  int32_t rc = check_sampling(target_logits, rows, vocab, temperature, workspace, ws_bytes, batch);
+  if (rc) return rc;
+  int launches = 0;
+  DF_CUDA(verify_sampled_launch(draft_logits, target_logits, drafts, u_accept, u_sample, batch, block_size, vocab,
+                                temperature, accept_len, out_tokens, next_anchor, workspace, &launches,
+                                (cudaStream_t)stream),
+          "sampled verification");
+  g_launch_count += launches;
+  return DFLASH_OK;
+}
+
+int32_t dflash_sample_tokens(const float* logits, int32_t rows, int32_t vocab, float temperature, const float* u,
+                             int32_t* tokens, void* workspace, size_t ws_bytes, dflash_stream_t stream) {
+  if (rows < 0) return fail(DFLASH_ERR_INVALID_ARG, "rows %d < 0", rows);
+  if (rows == 0) return DFLASH_OK;
+  if (!logits || !u || !tokens) return fail(DFLASH_ERR_INVALID_ARG, "a device pointer is NULL");
+  int32_t rc = check_sampling(logits, rows, vocab, temperature, workspace, ws_bytes, rows);
+  if (rc) return rc;
+  int launches = 0;
+  DF_CUDA(sample_tokens_launch(logits, rows, vocab, temperature, u, tokens, workspace, &launches,
+                               (cudaStream_t)stream),
+          "token sampling");
+  g_launch_count += launches;
   return DFLASH_OK;
 }
 

@@ -16,7 +16,8 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 PKG = os.path.dirname(HERE)
 ROOT = os.path.dirname(PKG)
 LIB_NAME = "libdflash_gb300.so"
-SOURCES = ["api.cu", "gemm.cu", "gemm_tc.cu", "attention.cu", "attention_tc.cu", "elementwise.cu", "persist.cu"]
+SOURCES = ["api.cu", "gemm.cu", "gemm_tc.cu", "attention.cu", "attention_tc.cu", "elementwise.cu", "persist.cu",
+           "sampling.cu", "block_policy.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
          "-I" + os.path.join(ROOT, "include")]
@@ -40,7 +41,7 @@ def build(verbose: bool = False, ptxas_info: bool = False) -> str:
     sources = [s for s in SOURCES if os.path.exists(os.path.join(HERE, s))]
 
     def compile_one(src):
-        obj = os.path.join(obj_dir, src.replace(".cu", ".o"))
+        obj = os.path.join(obj_dir, os.path.splitext(src)[0] + ".o")
         cmd = [nvcc, *ARCH, *FLAGS, "-c", os.path.join(HERE, src), "-o", obj]
         if ptxas_info:
             cmd.insert(1, "-Xptxas=-v")

@@ -1,0 +1,354 @@
+// Stochastic lossless verification and inverse-CDF sampling over the
+// vocabulary (explainer page "DFlash: Block Diffusion for Flash Speculative
+// Decoding", section "The Target Verifier Remains the Correctness Anchor":
+// a draft x drawn from p_d is kept with probability min(1, p_t(x) / p_d(x)),
+// verification stops at the first rejection, the target then draws a
+// correction from the residual distribution, and a bonus token when the whole
+// block survives; paper §5.1 reports the temperature-1 results).
+//
+// Every distribution is softmax(logits / T) of an fp32 logits row (V up to a
+// few hundred thousand).  The work is HBM-bound: the logits are read once to
+// get each row's (max, sum of exponentials), then only the one or two rows a
+// request draws from are read again.  Four launches:
+//
+//   row_stats   grid (chunks, rows): per 8192-logit chunk of a row, the max m
+//               of z = l * log2(e) / T and s = sum exp2(z - m) (online form);
+//   accept      one warp per request: merge the chunks of its rows, walk the
+//               drafts left to right with the acceptance test, pick the
+//               distribution to draw from (residual at the first rejection,
+//               or the target's row after the block) and write tau and the
+//               accepted tokens;
+//   draw_sums   grid (chunks, draws): per chunk, the unnormalised mass of
+//               the chosen distribution (max(0, p_t - p_d), or p_t);
+//   draw_pick   one CTA per draw: the chunk where the running mass first
+//               exceeds u * total, then the token inside it (block scan).
+//
+// Inverse CDF: the drawn token is the smallest id whose cumulative mass
+// (ids in increasing order) exceeds u times the total; when rounding leaves
+// u * total at or beyond the total, the last id with non-zero mass is taken.
+// Sampling a drafter row (dflash_sample_tokens) is the same draw with p_d
+// alone.
+#include <cstdint>
+
+#include "common.cuh"
+#include "sampling.cuh"
+
+namespace dflash {
+namespace {
+
+constexpr int kChunk = 8192;       // logits per chunk (32 KB of fp32)
+constexpr int kThreads = 256;      // kChunk / kThreads = 32 logits a thread
+constexpr float kLog2e = 1.4426950408889634f;
+
+__device__ __forceinline__ float2 merge_ms(float2 a, float2 b) {
+  // (max, sum exp2(z - max)) of the union of two sets
+  if (a.y == 0.f) return b;
+  if (b.y == 0.f) return a;
+  const float m = fmaxf(a.x, b.x);
+  return make_float2(m, a.y * exp2f(a.x - m) + b.y * exp2f(b.x - m));
+}
+
+__device__ __forceinline__ float2 warp_merge(float2 v) {
+  for (int o = 16; o; o >>= 1) {
+    float2 w = make_float2(__shfl_xor_sync(0xffffffffu, v.x, o), __shfl_xor_sync(0xffffffffu, v.y, o));
+    v = merge_ms(v, w);
+  }
+  return v;
+}
+
+// Row r < nd is drafter row r, otherwise target row r - nd.
+__device__ __forceinline__ const float* row_ptr(const float* draft, const float* target, int nd, int r, int V) {
+  return r < nd ? draft + (size_t)r * V : target + (size_t)(r - nd) * V;
+}
+
+__global__ void __launch_bounds__(kThreads) row_stats_kernel(const float* draft, const float* target, int nd, int V,
+                                                             float zscale, float2* part, int nchunk) {
+  const int c = blockIdx.x, r = blockIdx.y;
+  const float* x = row_ptr(draft, target, nd, r, V);
+  const int v0 = c * kChunk, v1 = min(V, v0 + kChunk);
+  // 8 float4 per thread, all loads issued before the arithmetic
+  float4 a[kChunk / kThreads / 4];
+#pragma unroll
+  for (int j = 0; j < kChunk / kThreads / 4; ++j) {
+    const int v = v0 + 4 * (threadIdx.x + j * kThreads);
+    a[j] = v < v1 ? __ldcs(reinterpret_cast<const float4*>(x + v)) : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+  }
+  float m = -INFINITY;
+#pragma unroll
+  for (int j = 0; j < kChunk / kThreads / 4; ++j) m = fmaxf(m, fmaxf(fmaxf(a[j].x, a[j].y), fmaxf(a[j].z, a[j].w)));
+  m *= zscale;
+  float s = 0.f;
+  if (m > -INFINITY) {
+#pragma unroll
+    for (int j = 0; j < kChunk / kThreads / 4; ++j) {
+      const int v = v0 + 4 * (threadIdx.x + j * kThreads);
+      if (v < v1)
+        s += exp2f(a[j].x * zscale - m) + exp2f(a[j].y * zscale - m) + exp2f(a[j].z * zscale - m) +
+             exp2f(a[j].w * zscale - m);
+    }
+  }
+  float2 t = warp_merge(make_float2(m, s));
+  __shared__ float2 ws[kThreads / 32];
+  if ((threadIdx.x & 31) == 0) ws[threadIdx.x >> 5] = t;
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    t = threadIdx.x < kThreads / 32 ? ws[threadIdx.x] : make_float2(-INFINITY, 0.f);
+    t = warp_merge(t);
+    if (threadIdx.x == 0) part[(size_t)r * nchunk + c] = t;
+  }
+}
+
+// (max, sum) of row r from its chunk partials, by one warp.
+__device__ __forceinline__ float2 row_total(const float2* part, int r, int nchunk) {
+  float2 t = make_float2(-INFINITY, 0.f);
+  for (int c = threadIdx.x & 31; c < nchunk; c += 32) t = merge_ms(t, part[(size_t)r * nchunk + c]);
+  return warp_merge(t);
+}
+
+// p(x) of one logit given its row's (max, sum).
+__device__ __forceinline__ float prob(float logit, float zscale, float2 ms) { return exp2f(logit * zscale - ms.x) / ms.y; }
+
+__global__ void __launch_bounds__(32) accept_kernel(const float* draft, const float* target, const int32_t* tokens,
+                                                    const float* u_accept, const float2* part, int nchunk, int B,
+                                                    int g, int V, float zscale, DrawSel* sel, int32_t* accept_len,
+                                                    int32_t* out_tokens) {
+  const int b = blockIdx.x, lane = threadIdx.x;
+  const int nd = B * (g - 1);
+  int kstar = g - 1;   // first rejected position (g - 1: none, the bonus)
+  float2 msd = make_float2(0.f, 1.f), mst = make_float2(0.f, 1.f);
+  for (int k = 0; k < g - 1; ++k) {
+    const int rd = b * (g - 1) + k, rt = nd + b * g + k;
+    const float2 md = row_total(part, rd, nchunk), mt = row_total(part, rt, nchunk);
+    const int d = tokens[rd];
+    bool keep = false;
+    if (d >= 0 && d < V) {   // an id outside the vocabulary is rejected
+      const float pd = prob(__ldg(draft + (size_t)rd * V + d), zscale, md);
+      const float pt = prob(__ldg(target + (size_t)(b * g + k) * V + d), zscale, mt);
+      const float a = pd <= 0.f ? 1.f : fminf(1.f, pt / pd);
+      keep = __ldg(u_accept + rd) < a;
+    }
+    if (!keep) {
+      kstar = k;
+      msd = md;
+      mst = mt;
+      break;
+    }
+  }
+  if (kstar == g - 1) mst = row_total(part, nd + b * g + g - 1, nchunk);
+  if (lane == 0) {
+    DrawSel s;
+    s.pt = target + (size_t)(b * g + kstar) * V;
+    s.pd = kstar < g - 1 ? draft + (size_t)(b * (g - 1) + kstar) * V : nullptr;
+    s.mst = mst;
+    s.msd = msd;
+    s.out = out_tokens + (size_t)b * g + kstar;
+    sel[b] = s;
+    accept_len[b] = kstar + 1;
+  }
+  for (int k = lane; k < g; k += 32)
+    if (k != kstar) out_tokens[(size_t)b * g + k] = k < kstar ? tokens[b * (g - 1) + k] : -1;
+}
+
+// Sampling rows on their own: draw i comes from softmax(row i).
+__global__ void __launch_bounds__(32) sample_sel_kernel(const float* logits, const float2* part, int nchunk, int V,
+                                                        DrawSel* sel, int32_t* tokens) {
+  const int r = blockIdx.x;
+  const float2 ms = row_total(part, r, nchunk);
+  if (threadIdx.x == 0) {
+    DrawSel s;
+    s.pt = logits + (size_t)r * V;
+    s.pd = nullptr;
+    s.mst = ms;
+    s.msd = make_float2(0.f, 1.f);
+    s.out = tokens + r;
+    sel[r] = s;
+  }
+}
+
+// Unnormalised mass of draw i's distribution at logit index v.
+__device__ __forceinline__ float mass(const DrawSel& s, int v, float zscale) {
+  const float pt = prob(__ldg(s.pt + v), zscale, s.mst);
+  return s.pd ? fmaxf(0.f, pt - prob(__ldg(s.pd + v), zscale, s.msd)) : pt;
+}
+
+__global__ void __launch_bounds__(kThreads) draw_sums_kernel(const DrawSel* sel, int V, float zscale, float* csum,
+                                                             int nchunk) {
+  const int c = blockIdx.x, i = blockIdx.y;
+  const DrawSel s = sel[i];
+  const int v0 = c * kChunk, v1 = min(V, v0 + kChunk);
+  float acc = 0.f;
+  for (int v = v0 + threadIdx.x; v < v1; v += kThreads) acc += mass(s, v, zscale);
+  for (int o = 16; o; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+  __shared__ float ws[kThreads / 32];
+  if ((threadIdx.x & 31) == 0) ws[threadIdx.x >> 5] = acc;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float t = 0.f;
+    for (int w = 0; w < kThreads / 32; ++w) t += ws[w];
+    csum[(size_t)i * nchunk + c] = t;
+  }
+}
+
+__global__ void __launch_bounds__(kThreads) draw_pick_kernel(const DrawSel* sel, int V, float zscale,
+                                                             const float* csum, int nchunk, const float* u,
+                                                             int32_t* next_anchor) {
+  const int i = blockIdx.x;
+  const DrawSel s = sel[i];
+  __shared__ int s_chunk;
+  __shared__ float s_rem;
+  __shared__ float s_tsum[kThreads];
+  __shared__ int s_tok;
+  if (threadIdx.x == 0) {
+    // running mass over the chunks in id order (double: the chunk sums are few)
+    double total = 0.0;
+    for (int c = 0; c < nchunk; ++c) total += csum[(size_t)i * nchunk + c];
+    const double target = (double)__ldg(u + i) * total;
+    double run = 0.0;
+    int pick = -1, last_nz = 0;
+    double before = 0.0;
+    for (int c = 0; c < nchunk; ++c) {
+      const double m = csum[(size_t)i * nchunk + c];
+      if (m > 0.0) last_nz = c;
+      if (pick < 0 && run + m > target && m > 0.0) {
+        pick = c;
+        before = run;
+      }
+      run += m;
+    }
+    if (pick < 0) {   // u * total at or past the total: the last chunk with mass
+      pick = last_nz;
+      s_rem = INFINITY;
+    } else {
+      s_rem = (float)(target - before);
+    }
+    s_chunk = pick;
+    s_tok = INT32_MAX;
+  }
+  __syncthreads();
+  const int v0 = s_chunk * kChunk, v1 = min(V, v0 + kChunk);
+  constexpr int kPer = kChunk / kThreads;
+  // thread t owns ids [v0 + kPer t, v0 + kPer (t+1)): its mass, then a block scan
+  float mv[kPer];
+  float own = 0.f;
+#pragma unroll
+  for (int j = 0; j < kPer; ++j) {
+    const int v = v0 + kPer * threadIdx.x + j;
+    mv[j] = v < v1 ? mass(s, v, zscale) : 0.f;
+    own += mv[j];
+  }
+  s_tsum[threadIdx.x] = own;
+  __syncthreads();
+  if (threadIdx.x == 0) {   // exclusive scan of 256 partial sums, in id order
+    float run = 0.f;
+    for (int t = 0; t < kThreads; ++t) {
+      const float m = s_tsum[t];
+      s_tsum[t] = run;
+      run += m;
+    }
+  }
+  __syncthreads();
+  const float rem = s_rem;
+  const float before = s_tsum[threadIdx.x];
+  if (rem != INFINITY && before <= rem && rem < before + own) {
+    // this thread's ids hold the remainder: the first whose running mass
+    // exceeds it (or, if rounding says none does, the last with mass)
+    float run = before;
+    int tok = -1, last = -1;
+    for (int j = 0; j < kPer; ++j) {
+      if (mv[j] > 0.f) last = v0 + kPer * threadIdx.x + j;
+      run += mv[j];
+      if (mv[j] > 0.f && run > rem) {
+        tok = v0 + kPer * threadIdx.x + j;
+        break;
+      }
+    }
+    if (tok < 0) tok = last;
+    if (tok >= 0) atomicMin(&s_tok, tok);
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int tok = s_tok;
+    if (tok == INT32_MAX) {
+      // the remainder lies beyond the chunk's mass (rounding, or u * total at
+      // or past the total): the chunk's last id with mass
+      tok = v0;
+      for (int v = v1 - 1; v >= v0; --v)
+        if (mass(s, v, zscale) > 0.f) {
+          tok = v;
+          break;
+        }
+    }
+    *s.out = tok;
+    if (next_anchor) next_anchor[i] = tok;
+  }
+}
+
+}  // namespace
+
+int sampling_chunks(int vocab) { return (vocab + kChunk - 1) / kChunk; }
+
+size_t sampling_workspace_bytes(int rows, int draws, int vocab) {
+  const size_t nc = (size_t)sampling_chunks(vocab);
+  auto a = [](size_t v) { return (v + 255) & ~(size_t)255; };
+  return a(sizeof(float2) * (size_t)rows * nc) + a(sizeof(DrawSel) * (size_t)draws) + a(sizeof(float) * (size_t)draws * nc);
+}
+
+namespace {
+struct SamplingWs {
+  float2* part;
+  DrawSel* sel;
+  float* csum;
+};
+SamplingWs carve(void* ws, int rows, int draws, int vocab) {
+  const size_t nc = (size_t)sampling_chunks(vocab);
+  auto a = [](size_t v) { return (v + 255) & ~(size_t)255; };
+  char* p = static_cast<char*>(ws);
+  SamplingWs w;
+  w.part = reinterpret_cast<float2*>(p);
+  p += a(sizeof(float2) * (size_t)rows * nc);
+  w.sel = reinterpret_cast<DrawSel*>(p);
+  p += a(sizeof(DrawSel) * (size_t)draws);
+  w.csum = reinterpret_cast<float*>(p);
+  return w;
+}
+}  // namespace
+
+cudaError_t verify_sampled_launch(const float* draft_logits, const float* target_logits, const int32_t* drafts,
+                                  const float* u_accept, const float* u_sample, int B, int g, int V,
+                                  float temperature, int32_t* accept_len, int32_t* out_tokens,
+                                  int32_t* next_anchor, void* ws, int* launches, cudaStream_t s) {
+  const int nchunk = sampling_chunks(V);
+  const int nd = B * (g - 1), rows = nd + B * g;
+  const float zscale = kLog2e / temperature;
+  SamplingWs w = carve(ws, rows, B, V);
+  *launches = 0;
+  row_stats_kernel<<<dim3(nchunk, rows), kThreads, 0, s>>>(draft_logits, target_logits, nd, V, zscale, w.part, nchunk);
+  ++*launches;
+  accept_kernel<<<B, 32, 0, s>>>(draft_logits, target_logits, drafts, u_accept, w.part, nchunk, B, g, V, zscale, w.sel,
+                                 accept_len, out_tokens);
+  ++*launches;
+  draw_sums_kernel<<<dim3(nchunk, B), kThreads, 0, s>>>(w.sel, V, zscale, w.csum, nchunk);
+  ++*launches;
+  draw_pick_kernel<<<B, kThreads, 0, s>>>(w.sel, V, zscale, w.csum, nchunk, u_sample, next_anchor);
+  ++*launches;
+  return cudaGetLastError();
+}
+
+cudaError_t sample_tokens_launch(const float* logits, int rows, int V, float temperature, const float* u,
+                                 int32_t* tokens, void* ws, int* launches, cudaStream_t s) {
+  const int nchunk = sampling_chunks(V);
+  const float zscale = kLog2e / temperature;
+  SamplingWs w = carve(ws, rows, rows, V);
+  *launches = 0;
+  row_stats_kernel<<<dim3(nchunk, rows), kThreads, 0, s>>>(logits, nullptr, rows, V, zscale, w.part, nchunk);
+  ++*launches;
+  sample_sel_kernel<<<rows, 32, 0, s>>>(logits, w.part, nchunk, V, w.sel, tokens);
+  ++*launches;
+  draw_sums_kernel<<<dim3(nchunk, rows), kThreads, 0, s>>>(w.sel, V, zscale, w.csum, nchunk);
+  ++*launches;
+  draw_pick_kernel<<<rows, kThreads, 0, s>>>(w.sel, V, zscale, w.csum, nchunk, u, nullptr);
+  ++*launches;
+  return cudaGetLastError();
+}
+
+}  // namespace dflash

@@ -256,6 +256,98 @@ int32_t dflash_verify_greedy(const int32_t* draft_dev, const int32_t* target_arg
                              int32_t block_size, int32_t* accept_len_dev, int32_t* out_tokens_dev,
                              int32_t* next_anchor_dev, dflash_stream_t stream);
 
+/* --- stage 5, sampled: stochastic lossless verification -----------------------
+ * Explainer, "The Target Verifier Remains the Correctness Anchor" (acceptance
+ * probability min(1, p_t/p_d), stop at the first rejection, correction from
+ * the residual distribution, bonus token when the whole block survives);
+ * paper §5.1 (temperature-1 results).  p_d and p_t are softmax(logits / T) of
+ * the drafter's and the target's fp32 logits rows.  Left to right, draft d_k
+ * (proposed from p_d row k-1) is kept iff u_accept[b][k-1] < min(1,
+ * p_t(d_k) / p_d(d_k)); a draft with p_d = 0 counts as kept, an id outside
+ * [0, vocab) as rejected.  At the first rejection, position k, the target
+ * draws the correction from max(0, p_t - p_d) of row k, normalised (the
+ * residual that makes the rule lossless), and the rest of the block is
+ * dropped; when every draft is kept it draws the bonus from target row
+ * block-1.  Each draw is an inverse-CDF draw with one uniform u: the smallest
+ * id (increasing order) whose cumulative mass exceeds u times the total mass
+ * (the last id with mass if rounding leaves none).
+ *   draft_logits_dev   fp32 [batch][block-1][vocab] (dflash_draft_block's logits)
+ *   target_logits_dev  fp32 [batch][block][vocab]; row k: the target's logits
+ *                      for the token after block position k (row 0 judges d_1)
+ *   draft_dev          int32 [batch][block-1]: the proposed tokens
+ *   u_accept_dev       fp32 [batch][block-1] and u_sample_dev fp32 [batch]:
+ *                      uniforms in [0, 1) from the caller (the library draws none)
+ *   accept_len_dev, out_tokens_dev, next_anchor_dev: as dflash_verify_greedy
+ *   workspace          >= dflash_sampling_workspace_bytes(batch*(2*block-1), batch, vocab)
+ * Requires vocab % 4 == 0, vocab <= 2^24, 16-byte aligned logits, batch *
+ * (2*block-1) <= 65535, 0 < temperature < inf; batch may be 0 (no launch).
+ * The logits are read once for the rows' normalisers and once more for the
+ * one or two rows each request draws from. */
+size_t dflash_sampling_workspace_bytes(int32_t rows, int32_t draws, int32_t vocab);
+int32_t dflash_verify_sampled(const float* draft_logits_dev, const float* target_logits_dev, const int32_t* draft_dev,
+                              const float* u_accept_dev, const float* u_sample_dev, int32_t batch, int32_t block_size,
+                              int32_t vocab, float temperature, int32_t* accept_len_dev, int32_t* out_tokens_dev,
+                              int32_t* next_anchor_dev, void* workspace, size_t workspace_bytes,
+                              dflash_stream_t stream);
+
+/* Inverse-CDF draw of one token per logits row: tokens[r] = the smallest id
+ * whose cumulative mass under softmax(logits[r] / T) exceeds u[r] — how a
+ * sampling drafter proposes its block from dflash_draft_block's logits before
+ * dflash_verify_sampled (explainer, same section: x_k drawn from p_d).
+ *   logits_dev fp32 [rows][vocab], u_dev fp32 [rows] in [0, 1), tokens_dev int32 [rows]
+ *   workspace >= dflash_sampling_workspace_bytes(rows, rows, vocab)
+ * Same requirements as dflash_verify_sampled (rows <= 65535). */
+int32_t dflash_sample_tokens(const float* logits_dev, int32_t rows, int32_t vocab, float temperature,
+                             const float* u_dev, int32_t* tokens_dev, void* workspace, size_t workspace_bytes,
+                             dflash_stream_t stream);
+
+/* --- block-size scheduling (host policy) ---------------------------------------
+ * Paper §5.5.4: a drafter trained at a large block size serves smaller
+ * inference-time block sizes nearly as well, and large blocks raise the
+ * verification cost when the target is compute-bound (large batches), so the
+ * block size can be chosen per cycle.  This policy runs on the host, between
+ * cycles, over the existing kernels:
+ *   - dflash_block_policy_observe records a cycle's accepted lengths tau
+ *     (one per request, read back from dflash_verify_greedy/_sampled): draft
+ *     position j was attempted when every earlier draft of its block was kept
+ *     and j < block_size, and kept when j <= tau - 1; the counts of earlier
+ *     cycles are first multiplied by `decay`.
+ *   - alpha_j = (kept_j + prior_accept * prior_weight) / (attempted_j + prior_weight)
+ *     estimates P(draft j kept | earlier drafts kept).
+ *   - dflash_block_policy_choose returns the candidate g maximising
+ *     batch * E[tau | g] / cost(g), E[tau | g] = 1 + sum_{i<g} prod_{j<=i}
+ *     alpha_j (blog "Inside DFlash ...", section 1), cost(g) = cost_fixed_ms +
+ *     cost_per_row_ms * batch * g + cost_per_request_ms * batch (a linear
+ *     model of drafting and verifying batch * g token rows, measured by the
+ *     caller); ties go to the smaller block.  Arithmetic in double precision.
+ * Candidates are strictly ascending in [1, DFLASH_POLICY_MAX_BLOCK];
+ * 0 < decay <= 1, prior_accept in [0, 1], prior_weight > 0, costs >= 0 with a
+ * positive sum.  A policy is plain host memory and is not thread-safe. */
+#define DFLASH_POLICY_MAX_CANDIDATES 16
+#define DFLASH_POLICY_MAX_BLOCK 32
+typedef struct {
+  int32_t n_candidates;
+  int32_t candidates[DFLASH_POLICY_MAX_CANDIDATES];
+  float cost_fixed_ms;
+  float cost_per_row_ms;
+  float cost_per_request_ms;
+  float decay;
+  float prior_accept;
+  float prior_weight;
+} dflash_block_policy_config;
+typedef struct dflash_block_policy dflash_block_policy;
+
+int32_t dflash_block_policy_create(const dflash_block_policy_config* cfg, dflash_block_policy** out);
+int32_t dflash_block_policy_destroy(dflash_block_policy* policy);
+/* accept_len_host: int32 [batch] HOST array of one cycle's tau, 1 <= tau <= block_size. */
+int32_t dflash_block_policy_observe(dflash_block_policy* policy, int32_t block_size, const int32_t* accept_len_host,
+                                    int32_t batch);
+/* *block_size_out = the chosen candidate; *expected_tau_out (may be NULL) = its E[tau]. */
+int32_t dflash_block_policy_choose(const dflash_block_policy* policy, int32_t batch, int32_t* block_size_out,
+                                   double* expected_tau_out);
+/* alpha_out[j] = the estimate for draft position j+1 (0 beyond the largest candidate - 1). */
+int32_t dflash_block_policy_acceptance(const dflash_block_policy* policy, double* alpha_out, int32_t n);
+
 /* --- benchmark utility (not part of the method) --------------------------------
  * The synthetic target the benchmark and tests put between dflash_draft_block
  * and dflash_verify_greedy in place of a real target model, as one kernel.

@@ -334,6 +334,18 @@ def verify_greedy(drafts: Sequence[int], target: Sequence[int]):
     return n + 1, out, int(target[n])
 
 
+def softmax(logits: np.ndarray, temperature: float = 1.0) -> np.ndarray:
+    """The distribution a row of logits stands for at a sampling temperature:
+    p_v = exp(l_v / T) / sum_w exp(l_w / T), in float64, over the last axis.
+    (The pages sample at temperature 1; T scales the logits before the
+    normalisation, the usual reading.)  The largest logit is subtracted first,
+    which changes nothing mathematically and keeps exp finite."""
+    z = np.asarray(logits, dtype=F64) / F64(temperature)
+    z = z - np.max(z, axis=-1, keepdims=True)
+    e = np.exp(z)
+    return e / np.sum(e, axis=-1, keepdims=True)
+
+
 def sample_inverse_cdf(p: np.ndarray, u: float) -> int:
     """The token a single uniform u in [0, 1) draws from distribution p: the
     smallest id whose cumulative probability (ids in increasing order) exceeds
@@ -389,6 +401,53 @@ def expected_accept_len(alpha: Sequence[float]) -> float:
         prod *= a
         total += prod
     return total
+
+
+# ---------------------------------------------------------------------------
+# Block-size scheduling  (paper §5.5.4: a drafter trained at a large block
+# size serves smaller ones about as well, which allows choosing the block size
+# per cycle; large blocks cost more verification when compute-bound)
+# ---------------------------------------------------------------------------
+
+def acceptance_update(accepts: np.ndarray, attempts: np.ndarray, block: int, taus: Sequence[int],
+                      decay: float):
+    """Per-position acceptance counts after one cycle of blocks of size
+    `block` with accepted lengths `taus` (one per request).  Draft position j
+    (1-based) of a block is attempted when every draft before it was kept and
+    j <= block - 1, and kept when j <= tau - 1.  Older counts are first
+    multiplied by `decay` (forgetting factor per cycle).  Returns new arrays."""
+    accepts = np.asarray(accepts, dtype=F64) * decay
+    attempts = np.asarray(attempts, dtype=F64) * decay
+    for tau in taus:
+        n = int(tau) - 1                      # drafts kept
+        for j in range(1, block):
+            if j <= n + 1:
+                attempts[j - 1] += 1.0
+            if j <= n:
+                accepts[j - 1] += 1.0
+    return accepts, attempts
+
+
+def acceptance_estimate(accepts: np.ndarray, attempts: np.ndarray, prior: float, weight: float) -> np.ndarray:
+    """alpha_j = P(draft j kept | drafts before it kept), estimated from the
+    counts with `weight` pseudo-observations of the prior probability."""
+    return (np.asarray(accepts, dtype=F64) + prior * weight) / (np.asarray(attempts, dtype=F64) + weight)
+
+
+def choose_block(candidates: Sequence[int], alpha: Sequence[float], batch: int, cost_fixed: float,
+                 cost_per_row: float, cost_per_request: float):
+    """The block size that maximises expected accepted tokens per unit of
+    cycle cost: E[tau | g] = expected_accept_len(alpha_1 .. alpha_{g-1}) per
+    request, cycle cost = cost_fixed + cost_per_row * batch * g +
+    cost_per_request * batch (a linear model of drafting plus verifying
+    batch * g token rows).  Ties go to the smaller block.  Returns (g, E[tau])."""
+    best = None
+    for g in sorted(candidates):
+        e = expected_accept_len(list(alpha[:g - 1]))
+        score = batch * e / (cost_fixed + cost_per_row * batch * g + cost_per_request * batch)
+        if best is None or score > best[0]:
+            best = (score, g, e)
+    return best[1], best[2]
 
 
 # ---------------------------------------------------------------------------

@@ -1,0 +1,240 @@
+"""Stochastic lossless verification and inverse-CDF sampling on the GPU
+(explainer, "The Target Verifier Remains the Correctness Anchor") against the
+float64 oracle (oracle.softmax, oracle.verify_sampled,
+oracle.sample_inverse_cdf) on the same fp32 logits and the same uniforms.
+
+The kernel computes the distributions in fp32, the oracle in float64, so a
+decision can differ only where a uniform falls within rounding distance of its
+threshold: an acceptance test with |u - min(1, p_t/p_d)| <= 1e-5, or a draw
+whose u lies within 1e-5 of a boundary of the cumulative distribution.  Such
+requests are excluded and counted (the count is asserted small); every other
+request must agree exactly: tau, every emitted token, the next anchor.
+Properties that hold at any size are checked on the kernel itself: the first
+emitted token follows the target's distribution (losslessness), the first
+draft is kept with probability sum_x min(p_t, p_d), and at a vanishing
+temperature the rule is greedy verification."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+
+pytestmark = pytest.mark.gpu
+
+MARGIN = 1e-5
+
+
+def _df():
+    import block_diffusion_drafter_dflash_gb300 as df
+    return df
+
+
+def _logits(B, rows, V, scale, seed, base=None, noise=0.0):
+    g = torch.Generator(device="cuda").manual_seed(seed)
+    if base is not None:
+        return (base + noise * torch.randn(base.shape, generator=g, device="cuda")).contiguous()
+    return (scale * torch.randn((B, rows, V), generator=g, device="cuda")).contiguous()
+
+
+def _uniform(shape, seed):
+    g = torch.Generator(device="cuda").manual_seed(seed)
+    return torch.rand(shape, generator=g, device="cuda", dtype=torch.float32)
+
+
+def _draw_margin(p, u):
+    """Distance of u from the nearest boundary of p's cumulative distribution."""
+    c = np.cumsum(p) / np.sum(p)
+    return float(np.min(np.abs(c - u)))
+
+
+def _oracle_request(dl, tl, drafts, ua, us, T):
+    """Oracle verification of one request and whether any of its decisions
+    lies within MARGIN of its threshold."""
+    g = tl.shape[0]
+    pt = oracle.softmax(tl, T)
+    pd = oracle.softmax(dl, T) if g > 1 else np.zeros((0, tl.shape[1]))
+    tau, out, nxt = oracle.verify_sampled(drafts, pd, pt, ua, us)
+    near = False
+    for k in range(tau - 1 if tau - 1 < g - 1 else g - 1):          # kept drafts
+        a = 1.0 if pd[k, drafts[k]] <= 0 else min(1.0, pt[k, drafts[k]] / pd[k, drafts[k]])
+        near |= abs(ua[k] - a) <= MARGIN
+    k = tau - 1
+    if k < g - 1:                                                      # the rejection and its residual draw
+        a = 1.0 if pd[k, drafts[k]] <= 0 else min(1.0, pt[k, drafts[k]] / pd[k, drafts[k]])
+        near |= abs(ua[k] - a) <= MARGIN
+        r = np.maximum(pt[k] - pd[k], 0.0)
+        near |= _draw_margin(r, us) <= MARGIN
+    else:
+        near |= _draw_margin(pt[g - 1], us) <= MARGIN
+    return (tau, out, nxt), near
+
+
+def _run_gpu(draft_logits, target_logits, drafts, ua, us, T):
+    df = _df()
+    B, g, V = target_logits.shape
+    tau = torch.full((B,), -9, dtype=torch.int32, device="cuda")
+    out = torch.full((B, g), -9, dtype=torch.int32, device="cuda")
+    nxt = torch.full((B,), -9, dtype=torch.int32, device="cuda")
+    df.dflash_verify_sampled(draft_logits if g > 1 else None, target_logits, drafts if g > 1 else None,
+                             ua if g > 1 else None, us, T, tau, out, nxt)
+    torch.cuda.synchronize()
+    return tau.cpu().numpy(), out.cpu().numpy(), nxt.cpu().numpy()
+
+
+def _sample_gpu(logits, T, u):
+    df = _df()
+    tok = torch.full(logits.shape[:-1], -9, dtype=torch.int32, device="cuda")
+    df.dflash_sample_tokens(logits, T, u, tok)
+    torch.cuda.synchronize()
+    return tok
+
+
+@pytest.mark.parametrize("V,g,T,scale", [(512, 16, 1.0, 2.0), (512, 4, 0.7, 1.0), (1024, 1, 1.0, 3.0),
+                                         (8192 + 512, 8, 1.0, 2.0)])
+def test_sampled_verify_matches_oracle(V, g, T, scale):
+    B = 256
+    tl = _logits(B, g, V, scale, seed=10 + g)
+    # a drafter that roughly agrees with the target: its logits are the target's plus noise
+    dl = _logits(B, g - 1, V, scale, seed=20 + g, base=tl[:, :g - 1], noise=0.7 * scale) if g > 1 else \
+        torch.zeros((B, 0, V), device="cuda")
+    drafts = _sample_gpu(dl, T, _uniform((B, g - 1), 30 + g)) if g > 1 else torch.zeros((B, 0), dtype=torch.int32,
+                                                                                          device="cuda")
+    ua, us = _uniform((B, max(g - 1, 0)), 40 + g), _uniform((B,), 50 + g)
+    tau, out, nxt = _run_gpu(dl, tl, drafts, ua, us, T)
+    dl_h, tl_h, d_h = dl.cpu().numpy(), tl.cpu().numpy(), drafts.cpu().numpy()
+    ua_h, us_h = ua.cpu().numpy().astype(np.float64), us.cpu().numpy().astype(np.float64)
+    excluded, rejected = 0, 0
+    for b in range(B):
+        (t_o, o_o, n_o), near = _oracle_request(dl_h[b], tl_h[b], d_h[b], ua_h[b], float(us_h[b]), T)
+        if near:
+            excluded += 1
+            continue
+        rejected += t_o < g
+        assert (int(tau[b]), out[b].tolist(), int(nxt[b])) == (t_o, o_o, n_o), (b, tau[b], t_o)
+    print(f"V={V} g={g} T={T}: {B - excluded} requests bit-exact, {excluded} excluded, {rejected} with a rejection")
+    assert excluded <= B // 20
+    if g > 1:
+        assert 0 < rejected < B - excluded          # both branches were exercised
+
+
+@pytest.mark.parametrize("V,T", [(512, 1.0), (151936, 1.0), (4096, 0.5)])
+def test_sample_tokens_matches_oracle_inverse_cdf(V, T):
+    rows = 512 if V < 100000 else 16
+    logits = _logits(1, rows, V, 2.0, seed=60)[0]
+    u = _uniform((rows,), 61)
+    tok = _sample_gpu(logits, T, u).cpu().numpy()
+    lh, uh = logits.cpu().numpy(), u.cpu().numpy().astype(np.float64)
+    checked = 0
+    for r in range(rows):
+        p = oracle.softmax(lh[r], T)
+        c = np.cumsum(p)
+        v = int(tok[r])
+        assert 0 <= v < V and p[v] > 0
+        # the drawn id's interval of the cumulative distribution holds u (up to rounding)
+        lo = c[v - 1] if v > 0 else 0.0
+        assert lo - MARGIN <= uh[r] < c[v] + MARGIN, (r, v, lo, c[v], uh[r])
+        if _draw_margin(p, uh[r]) > MARGIN:
+            assert v == oracle.sample_inverse_cdf(p, float(uh[r]))
+            checked += 1
+    assert checked >= rows // 2
+
+
+def test_sampled_verify_full_vocabulary_sampled_requests():
+    """The 8B shape's vocabulary (151,936) and block 16 at batch 8: tau and the
+    kept drafts exactly; the drawn token within rounding of its CDF interval."""
+    B, g, V, T = 8, 16, 151936, 1.0
+    tl = _logits(B, g, V, 2.0, seed=70)
+    dl = _logits(B, g - 1, V, 2.0, seed=71, base=tl[:, :g - 1], noise=0.3)
+    drafts = _sample_gpu(dl, T, _uniform((B, g - 1), 72))
+    ua, us = _uniform((B, g - 1), 73), _uniform((B,), 74)
+    tau, out, nxt = _run_gpu(dl, tl, drafts, ua, us, T)
+    dl_h, tl_h, d_h = dl.cpu().numpy(), tl.cpu().numpy(), drafts.cpu().numpy()
+    ua_h, us_h = ua.cpu().numpy().astype(np.float64), us.cpu().numpy().astype(np.float64)
+    for b in range(B):
+        pt, pd = oracle.softmax(tl_h[b], T), oracle.softmax(dl_h[b], T)
+        t_o, o_o, n_o = oracle.verify_sampled(d_h[b], pd, pt, ua_h[b], float(us_h[b]))
+        assert int(tau[b]) == t_o
+        k = t_o - 1
+        assert out[b, :k].tolist() == o_o[:k] and out[b, k + 1:].tolist() == o_o[k + 1:]
+        dist = np.maximum(pt[k] - pd[k], 0.0) if k < g - 1 else pt[g - 1]
+        c = np.cumsum(dist) / dist.sum()
+        v = int(nxt[b])
+        assert out[b, k] == v and dist[v] > 0
+        lo = c[v - 1] if v > 0 else 0.0
+        assert lo - MARGIN <= us_h[b] < c[v] + MARGIN
+
+
+def test_sampled_verify_is_lossless_on_the_gpu():
+    """One draft per block (g = 2) drawn by the kernel from p_d: over many
+    independent requests the first emitted token follows p_t (chi-square), the
+    draft survives with probability sum_x min(p_t, p_d), and a block whose draft
+    survived draws its bonus from the target's next row."""
+    scipy_stats = pytest.importorskip("scipy.stats")
+    V, T, n_call, calls = 8, 1.0, 21845, 4       # 3 logits rows per request, <= 65535 rows a call
+    lt = torch.tensor([[1.0, 0.2, -0.5, 2.0, 0.0, -1.0, 0.7, 1.4], [0.0, 1.0, 0.5, -0.3, 1.2, 0.1, -2.0, 0.4]],
+                      device="cuda")
+    ld = torch.tensor([0.5, 1.5, -0.2, 1.0, 0.3, -0.5, 1.6, 0.2], device="cuda")
+    firsts, kept, bonus = [], 0, []
+    for c in range(calls):
+        tl = lt.expand(n_call, 2, V).contiguous()
+        dl = ld.expand(n_call, 1, V).contiguous()
+        drafts = _sample_gpu(dl, T, _uniform((n_call, 1), 80 + c))
+        tau, out, nxt = _run_gpu(dl, tl, drafts, _uniform((n_call, 1), 90 + c), _uniform((n_call,), 100 + c), T)
+        firsts.append(out[:, 0])
+        kept += int(np.sum(tau == 2))
+        bonus.append(out[tau == 2, 1])
+    n = n_call * calls
+    pt = oracle.softmax(lt.cpu().numpy(), T)
+    pd = oracle.softmax(ld.cpu().numpy(), T)
+    first = np.concatenate(firsts)
+    obs = np.bincount(first, minlength=V)
+    stat = float(np.sum((obs - n * pt[0]) ** 2 / (n * pt[0])))
+    assert stat < scipy_stats.chi2.ppf(1 - 1e-4, V - 1), (stat, obs, n * pt[0])
+    overlap = float(np.sum(np.minimum(pt[0], pd)))
+    assert abs(kept / n - overlap) < 5 * math.sqrt(overlap * (1 - overlap) / n)
+    b = np.concatenate(bonus)
+    obs_b = np.bincount(b, minlength=V)
+    stat_b = float(np.sum((obs_b - len(b) * pt[1]) ** 2 / (len(b) * pt[1])))
+    assert stat_b < scipy_stats.chi2.ppf(1 - 1e-4, V - 1)
+
+
+def test_sampled_verify_at_vanishing_temperature_is_greedy_verification():
+    df = _df()
+    B, g, V = 64, 16, 4096
+    tl = _logits(B, g, V, 1.0, seed=110)
+    # drafts agree with the target's argmax on a random prefix of each block
+    dl = tl[:, :g - 1].clone()
+    gen = torch.Generator(device="cuda").manual_seed(111)
+    flip = torch.rand((B, g - 1), generator=gen, device="cuda") < 0.2
+    dl[flip] = dl[flip].roll(7, dims=-1)
+    T = 1e-3
+    drafts = _sample_gpu(dl, T, _uniform((B, g - 1), 112))
+    assert torch.equal(drafts, dl.argmax(-1).to(torch.int32))
+    tau, out, nxt = _run_gpu(dl, tl, drafts, _uniform((B, g - 1), 113), _uniform((B,), 114), T)
+    y = tl.argmax(-1).to(torch.int32).contiguous()
+    tg = torch.empty(B, dtype=torch.int32, device="cuda")
+    og = torch.empty((B, g), dtype=torch.int32, device="cuda")
+    ng = torch.empty(B, dtype=torch.int32, device="cuda")
+    df.dflash_verify_greedy(drafts, y, tg, og, ng)
+    assert tau.tolist() == tg.cpu().tolist() and out.tolist() == og.cpu().tolist() and nxt.tolist() == ng.cpu().tolist()
+    assert 1 < float(np.mean(tau)) < g
+
+
+def test_sampled_verify_rejects_bad_arguments():
+    df = _df()
+    B, g, V = 2, 4, 512
+    tl = torch.zeros((B, g, V), device="cuda")
+    dl = torch.zeros((B, g - 1, V), device="cuda")
+    d = torch.zeros((B, g - 1), dtype=torch.int32, device="cuda")
+    ua, us = torch.zeros((B, g - 1), device="cuda"), torch.zeros(B, device="cuda")
+    t, o, n = (torch.zeros(B, dtype=torch.int32, device="cuda"), torch.zeros((B, g), dtype=torch.int32, device="cuda"),
+               torch.zeros(B, dtype=torch.int32, device="cuda"))
+    with pytest.raises(df.DFlashError) as e:
+        df.dflash_verify_sampled(dl, tl, d, ua, us, 0.0, t, o, n)
+    assert e.value.code == -1
+    ws = torch.empty(16, dtype=torch.uint8, device="cuda")
+    with pytest.raises(df.DFlashError) as e:
+        df.dflash_verify_sampled(dl, tl, d, ua, us, 1.0, t, o, n, workspace=ws)
+    assert e.value.code == -7

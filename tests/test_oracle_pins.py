@@ -509,3 +509,104 @@ def test_sampled_verify_rejects_a_token_the_target_never_emits():
     pd = np.eye(V)[d]
     assert _accept_fraction(d, pd, pt) == 0.0
     assert np.allclose(_correction_dist(d, pd, pt, V), pt, atol=1e-3)
+
+
+# ---------------------------------------------------------------- softmax at a temperature
+def test_softmax_matches_library_and_two_token_closed_form():
+    scipy_special = pytest.importorskip("scipy.special")
+    rng = np.random.default_rng(7)
+    for T in (0.5, 1.0, 1.7):
+        x = rng.normal(0.0, 3.0, size=(5, 257))
+        np.testing.assert_allclose(oracle.softmax(x, T), scipy_special.softmax(x / T, axis=-1), rtol=1e-13, atol=0)
+    # two tokens: p_0 = 1 / (1 + exp((l_1 - l_0) / T)), the logistic function
+    for l0, l1, T in [(0.3, -1.2, 1.0), (5.0, 5.5, 0.25), (-2.0, 3.0, 2.0)]:
+        p = oracle.softmax(np.array([l0, l1]), T)
+        assert p[0] == pytest.approx(1.0 / (1.0 + math.exp((l1 - l0) / T)), rel=1e-14)
+        assert p.sum() == pytest.approx(1.0, abs=1e-15)
+
+
+def test_softmax_shift_invariance_and_zero_temperature_limit():
+    rng = np.random.default_rng(8)
+    x = rng.normal(0.0, 2.0, size=(3, 100))
+    np.testing.assert_allclose(oracle.softmax(x + 123.0, 1.0), oracle.softmax(x, 1.0), rtol=1e-12)
+    # T -> 0: all mass on the largest logit (greedy decoding)
+    p = oracle.softmax(x, 1e-4)
+    np.testing.assert_array_equal(np.argmax(p, axis=-1), np.argmax(x, axis=-1))
+    assert np.all(p.max(axis=-1) > 1.0 - 1e-12)
+
+
+# ---------------------------------------------------------------- block-size scheduling
+def _simulate_blocks(alpha, block, n, rng):
+    """Accepted lengths of n blocks whose draft j is kept with probability
+    alpha[j-1] given the drafts before it were (left to right, stop at the
+    first rejection)."""
+    taus = []
+    for _ in range(n):
+        k = 0
+        while k < block - 1 and rng.random() < alpha[k]:
+            k += 1
+        taus.append(k + 1)
+    return taus
+
+
+def test_acceptance_estimate_recovers_the_per_position_rates():
+    # with no prior and no forgetting the estimate converges to the rates
+    # that generated the blocks; a wrong attempt/keep index would bias it
+    rng = np.random.default_rng(21)
+    alpha = [0.95, 0.9, 0.85, 0.8, 0.7, 0.6, 0.5]
+    acc, att = np.zeros(7), np.zeros(7)
+    for block in (8, 6, 8):
+        acc, att = oracle.acceptance_update(acc, att, block, _simulate_blocks(alpha, block, 20000, rng), 1.0)
+    est = oracle.acceptance_estimate(acc, att, 0.5, 1e-9)
+    for j in range(7):
+        sd = math.sqrt(alpha[j] * (1 - alpha[j]) / att[j])
+        assert abs(est[j] - alpha[j]) < 5 * sd, (j, est[j], alpha[j])
+    # positions past a block's last draft are never attempted
+    acc2, att2 = oracle.acceptance_update(np.zeros(7), np.zeros(7), 3, [3, 3, 1], 1.0)
+    assert att2.tolist() == [3, 2, 0, 0, 0, 0, 0] and acc2.tolist() == [2, 2, 0, 0, 0, 0, 0]
+
+
+def test_acceptance_estimate_forgets_at_the_decay_rate():
+    rng = np.random.default_rng(22)
+    acc, att = np.zeros(3), np.zeros(3)
+    for _ in range(200):
+        acc, att = oracle.acceptance_update(acc, att, 4, _simulate_blocks([0.95] * 3, 4, 8, rng), 0.8)
+    for _ in range(60):
+        acc, att = oracle.acceptance_update(acc, att, 4, _simulate_blocks([0.3] * 3, 4, 8, rng), 0.8)
+    assert abs(oracle.acceptance_estimate(acc, att, 0.5, 1.0)[0] - 0.3) < 0.1
+    # one update with decay d scales earlier counts by d
+    a1, t1 = oracle.acceptance_update(np.array([4.0, 2.0]), np.array([5.0, 4.0]), 3, [], 0.5)
+    assert a1.tolist() == [2.0, 1.0] and t1.tolist() == [2.5, 2.0]
+
+
+def test_choose_block_maximises_simulated_throughput():
+    # brute force: accepted tokens per unit cost of each candidate by Monte
+    # Carlo; the choice must be the best one wherever the margin is clear
+    rng = np.random.default_rng(23)
+    cands = [4, 8, 10, 16]
+    checked = 0
+    for alpha0, c_row in [(0.98, 0.001), (0.9, 0.01), (0.6, 0.02), (0.3, 0.05), (0.8, 0.0), (0.95, 0.03)]:
+        alpha = [alpha0 * (0.99 ** j) for j in range(15)]
+        B, cf, creq = 8, 1.0, 0.01
+        thr = {}
+        for g in cands:
+            taus = _simulate_blocks(alpha, g, 20000, rng)
+            thr[g] = B * np.mean(taus) / (cf + c_row * B * g + creq * B)
+        g_best = max(thr, key=thr.get)
+        second = sorted(thr.values())[-2]
+        g, e = oracle.choose_block(cands, alpha, B, cf, c_row, creq)
+        assert e == pytest.approx(oracle.expected_accept_len(alpha[:g - 1]))
+        if thr[g_best] > 1.01 * second:
+            assert g == g_best, (alpha0, c_row, thr)
+            checked += 1
+    assert checked >= 4
+
+
+def test_choose_block_special_cases():
+    cands = [2, 4, 8, 16]
+    # free rows and any acceptance: the largest block (E[tau] never falls with g)
+    assert oracle.choose_block(cands, [0.5] * 15, 4, 1.0, 0.0, 0.0)[0] == 16
+    # nothing is ever accepted: E[tau] = 1 for every g, so the cheapest block
+    assert oracle.choose_block(cands, [0.0] * 15, 4, 1.0, 0.1, 0.0) == (2, 1.0)
+    # every draft accepted and rows free: tau = g
+    assert oracle.choose_block(cands, [1.0] * 15, 1, 1.0, 0.0, 0.0) == (16, 16.0)
