@@ -45,7 +45,8 @@ def _config_struct(cfg) -> _abi.Config:
     return _abi.Config(hidden=cfg.hidden, layers=cfg.layers, n_q_heads=cfg.n_q_heads, n_kv_heads=cfg.n_kv_heads,
                        head_dim=cfg.head_dim, ffn=cfg.ffn, vocab=cfg.vocab, n_target_feats=cfg.n_target_feats,
                        max_block=cfg.max_block, rope_theta=float(cfg.rope_theta), rms_eps=float(cfg.rms_eps),
-                       mask_token_id=int(mask), dtype=_abi.DTYPE_F32 if cfg.dtype == "fp32" else _abi.DTYPE_BF16)
+                       mask_token_id=int(mask), dtype=_abi.DTYPE_F32 if cfg.dtype == "fp32" else _abi.DTYPE_BF16,
+                       qk_norm=1 if getattr(cfg, "qk_norm", False) else 0)
 
 
 def dflash_version() -> int:
@@ -66,8 +67,9 @@ class Model:
             if t.dtype != self.dtype or not t.is_cuda or not t.is_contiguous():
                 raise ValueError("weights must be contiguous CUDA tensors of the model dtype")
         self._layers = (_abi.LayerWeights * cfg.layers)(*[
-            _abi.LayerWeights(**{k: lw[k].data_ptr() for k in ("g_in", "w_q", "w_k", "w_v", "w_o", "g_post",
-                                                                "w_g", "w_u", "w_d")})
+            _abi.LayerWeights(**{k: (lw[k].data_ptr() if k in lw else None)
+                                 for k in ("g_in", "w_q", "w_k", "w_v", "w_o", "g_post", "w_g", "w_u", "w_d", "g_q",
+                                           "g_k")})
             for lw in weights["layers"]])
         w = _abi.Weights(embed=weights["embed"].data_ptr(), lm_head=weights["lm_head"].data_ptr(),
                          w_c=weights["w_c"].data_ptr(), g_c=weights["g_c"].data_ptr(),

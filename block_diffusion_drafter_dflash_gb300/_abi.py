@@ -29,11 +29,11 @@ class Config(ctypes.Structure):
     _fields_ = [("hidden", c_i32), ("layers", c_i32), ("n_q_heads", c_i32), ("n_kv_heads", c_i32),
                 ("head_dim", c_i32), ("ffn", c_i32), ("vocab", c_i32), ("n_target_feats", c_i32),
                 ("max_block", c_i32), ("rope_theta", ctypes.c_float), ("rms_eps", ctypes.c_float),
-                ("mask_token_id", c_i32), ("dtype", c_i32)]
+                ("mask_token_id", c_i32), ("dtype", c_i32), ("qk_norm", c_i32)]
 
 
 class LayerWeights(ctypes.Structure):
-    _fields_ = [(n, c_ptr) for n in ("g_in", "w_q", "w_k", "w_v", "w_o", "g_post", "w_g", "w_u", "w_d")]
+    _fields_ = [(n, c_ptr) for n in ("g_in", "w_q", "w_k", "w_v", "w_o", "g_post", "w_g", "w_u", "w_d", "g_q", "g_k")]
 
 
 class Weights(ctypes.Structure):

@@ -145,6 +145,7 @@ int32_t check_config(const dflash_config* c) {
     return fail(DFLASH_ERR_SHAPE, "(n_q_heads/n_kv_heads)*max_block must be <= %d", attention_max_rows());
   if (c->mask_token_id < 0 || c->mask_token_id >= c->vocab) return fail(DFLASH_ERR_INVALID_ARG, "mask_token_id %d out of [0, vocab)", c->mask_token_id);
   if (!(c->rope_theta > 1.0f) || !(c->rms_eps >= 0.0f)) return fail(DFLASH_ERR_INVALID_ARG, "rope_theta must be > 1 and rms_eps >= 0");
+  if (c->qk_norm != 0 && c->qk_norm != 1) return fail(DFLASH_ERR_INVALID_ARG, "qk_norm %d must be 0 or 1", c->qk_norm);
   return DFLASH_OK;
 }
 
@@ -174,11 +175,11 @@ struct WsPlan {
 // attention groups fit 64 query rows.
 bool persist_draft_ok(const dflash_model* m, int B, int block) {
   const dflash_config& c = m->cfg;
-  return m->persist && B * block <= kPRows && (c.n_q_heads / c.n_kv_heads) * block <= kPAttnRows &&
+  return m->persist && !c.qk_norm && B * block <= kPRows && (c.n_q_heads / c.n_kv_heads) * block <= kPAttnRows &&
          6 * c.layers + 1 <= kPMaxPhases && c.ffn % kTileN == 0;
 }
 bool persist_inject_ok(const dflash_model* m, int max_rows) {
-  return m->persist && max_rows <= kPRows && 1 + 2 * m->cfg.layers <= kPMaxSeg;
+  return m->persist && !m->cfg.qk_norm && max_rows <= kPRows && 1 + 2 * m->cfg.layers <= kPMaxSeg;
 }
 
 // One call's scratch: the injection part when max_rows > 0, the drafter part
@@ -352,10 +353,17 @@ int32_t run_inject(const dflash_model* m, dflash_cache* cache, const void* feats
     add_seg(pi, m->layers[l].w_v, layer_map(l, kMapV), m->layers[l].w_v, layer_map(l, kMapV), hk / kTileN, 0, 2 * l + 1);
   }
   apply_plan(pi, P.g_inject, partial, counters);
-  EpiInject<T> ei{reinterpret_cast<T*>(cache->base + cache->k_off), reinterpret_cast<T*>(cache->base + cache->v_off),
-                  rowinfo, reinterpret_cast<const float2*>(ws + P.rope_c), c.layers, c.n_kv_heads, c.head_dim,
-                  cache->cap, pad8(cache->cap)};
+  const float2* rope_c = reinterpret_cast<const float2*>(ws + P.rope_c);
+  T* kc = reinterpret_cast<T*>(cache->base + cache->k_off);
+  EpiInject<T> ei{kc, reinterpret_cast<T*>(cache->base + cache->v_off), rowinfo, c.qk_norm ? nullptr : rope_c,
+                  c.layers, c.n_kv_heads, c.head_dim, cache->cap, pad8(cache->cap)};
   DF_LAUNCH(DFLASH_STAGE_INJECT, 1, (gemm_launch<T, EpiInject<T>>(pi, P.g_inject, ei, s)), "injection GEMM");
+  if (c.qk_norm)   // per-head key norm, then RoPE, of the injected keys
+    for (int l = 0; l < c.layers; ++l)
+      DF_LAUNCH(DFLASH_STAGE_OTHER, 1,
+                qknorm_cache_launch<T>(kc, rowinfo, max_rows, l, c.layers, c.n_kv_heads, c.head_dim, cache->cap,
+                                       static_cast<const T*>(m->layers[l].g_k), c.rms_eps, rope_c, s),
+                "injected key norm");
   return DFLASH_OK;
 }
 
@@ -398,9 +406,14 @@ int32_t run_draft(const dflash_model* m, const dflash_cache* cache, const int32_
     add_seg(pq, L.w_k, layer_map(l, kMapK), L.w_k, layer_map(l, kMapK), hk / kTileN, 0, 1);
     add_seg(pq, L.w_v, layer_map(l, kMapV), L.w_v, layer_map(l, kMapV), hk / kTileN, 0, 2);
     apply_plan(pq, P.g_qkv, partial, counters);
-    EpiQKV<T> eq{q, kb, vb, reinterpret_cast<const float2*>(ws + P.rope_q), block, c.n_q_heads, c.n_kv_heads,
-                 c.head_dim, pad8(block)};
+    const float2* rope_q = reinterpret_cast<const float2*>(ws + P.rope_q);
+    EpiQKV<T> eq{q, kb, vb, c.qk_norm ? nullptr : rope_q, block, c.n_q_heads, c.n_kv_heads, c.head_dim, pad8(block)};
     DF_LAUNCH(DFLASH_STAGE_QKV, 1, (gemm_launch<T, EpiQKV<T>>(pq, P.g_qkv, eq, s)), "QKV GEMM");
+    if (c.qk_norm)   // per-head query / key norm, then RoPE
+      DF_LAUNCH(DFLASH_STAGE_OTHER, 1,
+                qknorm_block_launch<T>(q, kb, static_cast<const T*>(L.g_q), static_cast<const T*>(L.g_k), B, block,
+                                       c.n_q_heads, c.n_kv_heads, c.head_dim, c.rms_eps, rope_q, s),
+                "query/key norm");
 
     AttnParams ap{};
     ap.q = q; ap.kb = kb; ap.vb = vb;
@@ -693,7 +706,7 @@ size_t cache_v_bytes(const dflash_config* cfg, int batch, int capacity) {
 
 extern "C" {
 
-int32_t dflash_version(void) { return 100; }
+int32_t dflash_version(void) { return 10100; }
 
 const char* dflash_last_error(void) { return g_last_error.c_str(); }
 
@@ -708,6 +721,7 @@ int32_t dflash_model_create(const dflash_config* cfg, const dflash_weights* w, d
     const dflash_layer_weights& L = w->layers[l];
     if (!L.g_in || !L.w_q || !L.w_k || !L.w_v || !L.w_o || !L.g_post || !L.w_g || !L.w_u || !L.w_d)
       return fail(DFLASH_ERR_INVALID_ARG, "a weight pointer of layer %d is NULL", l);
+    if (cfg->qk_norm && (!L.g_q || !L.g_k)) return fail(DFLASH_ERR_INVALID_ARG, "qk_norm: g_q or g_k of layer %d is NULL", l);
   }
   dflash_model* m = new dflash_model();
   m->cfg = *cfg;

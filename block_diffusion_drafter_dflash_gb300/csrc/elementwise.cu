@@ -289,7 +289,110 @@ __global__ void __launch_bounds__(1024) synthetic_target_kernel(const int32_t* d
   }
 }
 
+// QK-norm then RoPE of one head vector held by a warp: lane l holds
+// elements l, l + 32, ... (E = hd/32 of them), so each rotate-half pair
+// (d, d + hd/2) sits in one lane (elements e and e + E/2).
+template <int E>
+__device__ __forceinline__ void qknorm_rope_vec(float* v, const float* g, float eps, int hd, const float2* rope_row) {
+  float ss = 0.f;
+#pragma unroll
+  for (int e = 0; e < E; ++e) ss += v[e] * v[e];
+  for (int o = 16; o; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+  const float r = rsqrtf(ss / (float)hd + eps);
+#pragma unroll
+  for (int e = 0; e < E; ++e) v[e] *= r * g[e];
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int e = 0; e < E / 2; ++e) {
+    const float2 cs = rope_row[lane + 32 * e];   // (cos, sin) of pair i = lane + 32 e
+    const float a = v[e], b = v[e + E / 2];
+    v[e] = a * cs.x - b * cs.y;
+    v[e + E / 2] = b * cs.x + a * cs.y;
+  }
+}
+
+// Block queries (fp32 [b][head][k][hd]) and block keys (T planes
+// [b][kvh][plane][k][hd]) of one layer: one warp per head vector.
+template <typename T, int E>
+__global__ void __launch_bounds__(256) qknorm_block_kernel(float* q, T* kb, const T* g_q, const T* g_k, int B, int block,
+                                                           int nq, int nkv, float eps, const float2* rope) {
+  const int hd = 32 * E, half = hd / 2;
+  const int w = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+  const int nqv = B * nq * block, nkvv = B * nkv * block;
+  if (w >= nqv + nkvv) return;
+  const bool is_q = w < nqv;
+  const int idx = is_q ? w : w - nqv;
+  const int nh = is_q ? nq : nkv;
+  const int b = idx / (nh * block), rem = idx - b * nh * block, h = rem / block, k = rem - h * block;
+  const T* gain = is_q ? g_q : g_k;
+  float v[E], g[E];
+#pragma unroll
+  for (int e = 0; e < E; ++e) g[e] = to_f32(gain[lane + 32 * e]);
+  const size_t plane = (size_t)block * hd;
+  const size_t base = is_q ? (((size_t)b * nq + h) * block + k) * hd
+                           : (((size_t)b * nkv + h) * ActPlanes<T>::n * block + k) * hd;
+#pragma unroll
+  for (int e = 0; e < E; ++e) v[e] = is_q ? q[base + lane + 32 * e] : get_act(kb, plane, base + lane + 32 * e);
+  qknorm_rope_vec<E>(v, g, eps, hd, rope + (size_t)(b * block + k) * half);
+#pragma unroll
+  for (int e = 0; e < E; ++e) {
+    if (is_q)
+      q[base + lane + 32 * e] = v[e];
+    else
+      put_act(kb, plane, base + lane + 32 * e, v[e]);
+  }
+}
+
+// Injected context keys of layer `layer` in the cache (T planes
+// [b][layer][kvh][plane][cap][hd]) for the rows of rowinfo: one warp per
+// (row, kv head); padding rows are skipped.
+template <typename T, int E>
+__global__ void __launch_bounds__(256) qknorm_cache_kernel(T* kc, const int2* rowinfo, int rows, int layer, int layers,
+                                                           int nkv, int cap, const T* g_k, float eps,
+                                                           const float2* rope) {
+  const int hd = 32 * E, half = hd / 2;
+  const int w = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+  if (w >= rows * nkv) return;
+  const int row = w / nkv, h = w - row * nkv;
+  const int2 ri = rowinfo[row];
+  if (ri.x < 0) return;
+  float v[E], g[E];
+#pragma unroll
+  for (int e = 0; e < E; ++e) g[e] = to_f32(g_k[lane + 32 * e]);
+  const size_t plane = (size_t)cap * hd;
+  const size_t base = ((((size_t)ri.x * layers + layer) * nkv + h) * ActPlanes<T>::n * cap + ri.y) * hd;
+#pragma unroll
+  for (int e = 0; e < E; ++e) v[e] = get_act(kc, plane, base + lane + 32 * e);
+  qknorm_rope_vec<E>(v, g, eps, hd, rope + (size_t)row * half);
+#pragma unroll
+  for (int e = 0; e < E; ++e) put_act(kc, plane, base + lane + 32 * e, v[e]);
+}
+
 }  // namespace
+
+template <typename T>
+cudaError_t qknorm_block_launch(float* q, T* kb, const T* g_q, const T* g_k, int B, int block, int nq, int nkv, int hd,
+                                float eps, const float2* rope, cudaStream_t s) {
+  const int n = B * (nq + nkv) * block;
+  if (n == 0) return cudaSuccess;
+  if (hd == 64)
+    return launch_pdl(qknorm_block_kernel<T, 2>, dim3((n + 7) / 8), dim3(256), 0, s, q, kb, g_q, g_k, B, block, nq, nkv,
+                      eps, rope);
+  return launch_pdl(qknorm_block_kernel<T, 4>, dim3((n + 7) / 8), dim3(256), 0, s, q, kb, g_q, g_k, B, block, nq, nkv,
+                    eps, rope);
+}
+
+template <typename T>
+cudaError_t qknorm_cache_launch(T* kc, const int2* rowinfo, int rows, int layer, int layers, int nkv, int hd, int cap,
+                                const T* g_k, float eps, const float2* rope, cudaStream_t s) {
+  const int n = rows * nkv;
+  if (n == 0) return cudaSuccess;
+  if (hd == 64)
+    return launch_pdl(qknorm_cache_kernel<T, 2>, dim3((n + 7) / 8), dim3(256), 0, s, kc, rowinfo, rows, layer, layers,
+                      nkv, cap, g_k, eps, rope);
+  return launch_pdl(qknorm_cache_kernel<T, 4>, dim3((n + 7) / 8), dim3(256), 0, s, kc, rowinfo, rows, layer, layers, nkv,
+                    cap, g_k, eps, rope);
+}
 
 cudaError_t synthetic_target_launch(const int32_t* draft, const uint8_t* match, const int32_t* off,
                                     const int32_t* bonus, int npat, long long* pidx, const int32_t* tau,
@@ -359,7 +462,11 @@ cudaError_t verify_launch(const int32_t* draft, const int32_t* target, int B, in
   template cudaError_t final_norm_launch<T>(const float*, const T*, float, int, int, int, T*, size_t,              \
                                             unsigned long long*, cudaStream_t);                                   \
   template cudaError_t fuse_norm_launch<T>(const float*, const T*, float, const int2*, int, int, T*, size_t,      \
-                                           const double*, int, float2*, cudaStream_t);
+                                           const double*, int, float2*, cudaStream_t);                            \
+  template cudaError_t qknorm_block_launch<T>(float*, T*, const T*, const T*, int, int, int, int, int, float,      \
+                                              const float2*, cudaStream_t);                                       \
+  template cudaError_t qknorm_cache_launch<T>(T*, const int2*, int, int, int, int, int, int, const T*, float,      \
+                                              const float2*, cudaStream_t);
 
 DFLASH_EW_INST(float)
 DFLASH_EW_INST(__nv_bfloat16)

@@ -72,7 +72,9 @@ struct EpiSwiGLU {
 // RoPE in the Q/K/V and injection epilogues is rotate-half: feature d < hd/2
 // pairs with d + hd/2 of the same head (both in the same 128-feature tile),
 // x' = x cos - x_partner sin for the first half, x cos + x_partner sin for the
-// second, with (cos, sin) of the row's position from a per-row table.
+// second, with (cos, sin) of the row's position from a per-row table.  With
+// no table (rope == nullptr: QK-norm models, whose norm comes before RoPE and
+// needs a whole head) the values are stored unrotated for qknorm_rope.
 
 // Block Q/K/V of one draft layer: tag 0 = Q, 1 = K, 2 = V.  Row = b*block + k
 // sits at position ctx_len[b] + k, whose RoPE (cos, sin) table rope[row][hd/2]
@@ -125,7 +127,7 @@ struct EpiQKV {
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
         const int m = mb + j * step;
-        sc[j] = (tag != 2 && m < mc) ? __ldg(rope + (size_t)(m0 + m) * half + i) : make_float2(1.f, 0.f);
+        sc[j] = (rope && tag != 2 && m < mc) ? __ldg(rope + (size_t)(m0 + m) * half + i) : make_float2(1.f, 0.f);
       }
       int b = (m0 + mb) / block, k = m0 + mb - b * block;   // (request, block position) of row m0 + mb
 #pragma unroll
@@ -204,7 +206,7 @@ struct EpiInject {
       for (int j = 0; j < 8; ++j) {
         const int m = mb + j * step;
         ri[j] = m < mc ? __ldg(rowinfo + m0 + m) : make_int2(-1, -1);
-        sc[j] = (!is_v && m < mc) ? __ldg(rope + (size_t)(m0 + m) * half + i) : make_float2(1.f, 0.f);
+        sc[j] = (rope && !is_v && m < mc) ? __ldg(rope + (size_t)(m0 + m) * half + i) : make_float2(1.f, 0.f);
       }
 #pragma unroll
       for (int j = 0; j < 8; ++j) {

@@ -73,6 +73,19 @@ template <typename T>
 cudaError_t fuse_norm_launch(const float* y, const T* g, float eps, const int2* rowinfo, int rows, int D, T* ht,
                              size_t plane, const double* inv_freq, int hd, float2* rope, cudaStream_t s);
 
+// QK-norm models: per-head RMSNorm (gain g [hd], epsilon eps) then RoPE, in
+// place, of the block queries q (fp32 [B][nq][block][hd]) and block keys kb
+// (planes [B][nkv][plane][block][hd]) of one layer, (cos, sin) from
+// rope[b*block + k][hd/2] ...
+template <typename T>
+cudaError_t qknorm_block_launch(float* q, T* kb, const T* g_q, const T* g_k, int B, int block, int nq, int nkv, int hd,
+                                float eps, const float2* rope, cudaStream_t s);
+// ... and of the injected context keys of one layer in the cache
+// ([b][layer][kvh][plane][cap][hd]) at the rows of rowinfo, rope[row][hd/2].
+template <typename T>
+cudaError_t qknorm_cache_launch(T* kc, const int2* rowinfo, int rows, int layer, int layers, int nkv, int hd, int cap,
+                                const T* g_k, float eps, const float2* rope, cudaStream_t s);
+
 // Row -> (request, position) map of an injection and the ctx_len update;
 // with `rope`, also rope[row][hd/2] = (cos, sin) of the row's position.
 cudaError_t inject_prep_launch(const int32_t* n_new, int32_t* ctx_len, int B, int max_rows, int cap,

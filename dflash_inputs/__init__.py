@@ -38,6 +38,7 @@ class DraftConfig:
     dtype: str = "bf16"    # "fp32" or "bf16": storage type of weights and activations
     max_block: int = 32    # largest block_size the drafter is asked for
     mask_token_id: Optional[int] = None   # defaults to vocab - 1
+    qk_norm: bool = False  # per-head RMSNorm of queries and keys before RoPE (Qwen3's q_norm / k_norm)
 
     @property
     def mask_id(self) -> int:
@@ -131,7 +132,8 @@ def make_weights(cfg: DraftConfig, seed: int, device="cpu", std: float = 0.02) -
 
     Matrices are [out_features, in_features] row-major.  Keys:
     embed [V, D], lm_head [V, D], w_c [D, m*D], g_c [D], g_final [D] and
-    layers[i] with g_in, w_q, w_k, w_v, w_o, g_post, w_g, w_u, w_d.
+    layers[i] with g_in, w_q, w_k, w_v, w_o, g_post, w_g, w_u, w_d (and, when
+    cfg.qk_norm, g_q and g_k [head_dim] drawn as 1 + N(0, 0.1)).
     """
     g = _gen(seed, device)
     dt = cfg.torch_dtype
@@ -159,6 +161,14 @@ def make_weights(cfg: DraftConfig, seed: int, device="cpu", std: float = 0.02) -
             "w_d": _normal((D, F), std, g, device, dt),
         })
     w["layers"] = layers
+    if cfg.qk_norm:
+        # per-head query / key norm gains [head_dim], near one so that a
+        # missing gain is visible; a generator of their own keeps every other
+        # weight of the configuration unchanged
+        gq = _gen(seed + 7777, device)
+        for lw in layers:
+            lw["g_q"] = (1.0 + _normal((cfg.head_dim,), 0.1, gq, device, torch.float32)).to(dt)
+            lw["g_k"] = (1.0 + _normal((cfg.head_dim,), 0.1, gq, device, torch.float32)).to(dt)
     return w
 
 

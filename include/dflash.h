@@ -82,12 +82,17 @@ typedef struct {
   float rms_eps;
   int32_t mask_token_id;  /* embedding row used at every masked block position */
   int32_t dtype;          /* DFLASH_DTYPE_* */
+  int32_t qk_norm;        /* 0, or 1: every query and key head (block and injected context keys) is
+                             RMS-normalised over head_dim and scaled by the layer's g_q / g_k
+                             before RoPE (Qwen3's q_norm / k_norm; not on the pages, off in their
+                             configuration).  Models with it run the multi-kernel path. */
 } dflash_config;
 
 /* Device pointers of one draft layer (borrowed).  Shapes with
  * Hq = n_q_heads*head_dim, Hk = n_kv_heads*head_dim:
  *   g_in [D], w_q [Hq,D], w_k [Hk,D], w_v [Hk,D], w_o [D,Hq],
- *   g_post [D], w_g [F,D], w_u [F,D], w_d [D,F]. */
+ *   g_post [D], w_g [F,D], w_u [F,D], w_d [D,F],
+ *   g_q [head_dim], g_k [head_dim] (QK-norm gains; read only when qk_norm, else may be NULL). */
 typedef struct {
   const void* g_in;
   const void* w_q;
@@ -98,6 +103,8 @@ typedef struct {
   const void* w_g;
   const void* w_u;
   const void* w_d;
+  const void* g_q;
+  const void* g_k;
 } dflash_layer_weights;
 
 /* Device pointers of the whole drafter (borrowed): embed [V,D] and

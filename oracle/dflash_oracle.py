@@ -153,17 +153,22 @@ def fuse_context(feats: np.ndarray, w_c: np.ndarray, g_c: np.ndarray, eps: float
 # ---------------------------------------------------------------------------
 
 def inject_kv(h_t: np.ndarray, w_k: np.ndarray, w_v: np.ndarray, positions: Sequence[int],
-              n_kv_heads: int, head_dim: int, theta: float, mode: str = "f64"):
+              n_kv_heads: int, head_dim: int, theta: float, mode: str = "f64", g_k=None, eps: float = 1e-6):
     """Context keys and values of one draft layer: W^K H_t and W^V H_t.
 
     Only keys get the rotary embedding; a context token j injected for a
     request holding c tokens sits at absolute position c + j (reading: context
     positions count from 0 and the block continues after them).  No per-layer
     norm is applied to H_t — the equation feeds H_t straight into W^K, W^V.
-    Returns K, V as [n, n_kv_heads, head_dim].
+    With a QK-norm gain g_k (a Qwen3 option the pages do not mention; reading:
+    it belongs to the layer's key path, so context keys get it like block
+    keys) each key head is RMS-normalised over head_dim and scaled by g_k
+    before RoPE.  Returns K, V as [n, n_kv_heads, head_dim].
     """
     n = h_t.shape[0]
     k = linear(h_t, w_k).reshape(n, n_kv_heads, head_dim)
+    if g_k is not None:
+        k = rms_norm(k, g_k, eps)
     v = linear(h_t, w_v).reshape(n, n_kv_heads, head_dim)
     return store(rope(k, positions, theta), mode), store(v, mode)
 
@@ -189,8 +194,10 @@ def inject_context(weights: Dict, cfg, cache: RequestCache, feats: np.ndarray, m
     h_t = fuse_context(feats, weights["w_c"], weights["g_c"], cfg.rms_eps, mode)
     c = cache.length
     pos = np.arange(c, c + h_t.shape[0])
+    qk = getattr(cfg, "qk_norm", False)
     for i, lw in enumerate(weights["layers"]):
-        k, v = inject_kv(h_t, lw["w_k"], lw["w_v"], pos, cfg.n_kv_heads, cfg.head_dim, cfg.rope_theta, mode)
+        k, v = inject_kv(h_t, lw["w_k"], lw["w_v"], pos, cfg.n_kv_heads, cfg.head_dim, cfg.rope_theta, mode,
+                         g_k=lw["g_k"] if qk else None, eps=cfg.rms_eps)
         cache.k[i] = np.concatenate([cache.k[i], k], axis=0)
         cache.v[i] = np.concatenate([cache.v[i], v], axis=0)
     return h_t
@@ -273,7 +280,9 @@ def draft_forward(weights: Dict, cfg, cache: RequestCache, anchor: int, block: i
     last layer h = RMSNorm_final(x).  The block's own K/V is not kept.
     `mode` rounds every tensor handed from one step to the next (normed
     inputs, Q/K/V, attention output, SwiGLU product, h) to a storage type; the
-    residual stream x stays exact.
+    residual stream x stays exact.  With cfg.qk_norm, every query and key head
+    is RMS-normalised over head_dim and scaled by the layer's g_q / g_k before
+    RoPE (Qwen3's q_norm / k_norm).
     """
     D, nq, nkv, hd = cfg.hidden, cfg.n_q_heads, cfg.n_kv_heads, cfg.head_dim
     c = cache.length
@@ -283,8 +292,13 @@ def draft_forward(weights: Dict, cfg, cache: RequestCache, anchor: int, block: i
     mask_rows = dflash_mask(c, block)[c:, :]                       # block rows only
     for i, lw in enumerate(weights["layers"]):
         u = store(rms_norm(x, lw["g_in"], cfg.rms_eps), mode)
-        q = store(rope(linear(u, lw["w_q"]).reshape(block, nq, hd), pos, cfg.rope_theta), mode)
-        k = store(rope(linear(u, lw["w_k"]).reshape(block, nkv, hd), pos, cfg.rope_theta), mode)
+        q = linear(u, lw["w_q"]).reshape(block, nq, hd)
+        k = linear(u, lw["w_k"]).reshape(block, nkv, hd)
+        if getattr(cfg, "qk_norm", False):
+            q = rms_norm(q, lw["g_q"], cfg.rms_eps)
+            k = rms_norm(k, lw["g_k"], cfg.rms_eps)
+        q = store(rope(q, pos, cfg.rope_theta), mode)
+        k = store(rope(k, pos, cfg.rope_theta), mode)
         v = store(linear(u, lw["w_v"]).reshape(block, nkv, hd), mode)
         if use_mask:
             o = attention_masked(q, np.concatenate([cache.k[i], k]), np.concatenate([cache.v[i], v]), mask_rows)

@@ -239,10 +239,13 @@ def test_zero_output_projections_reduce_drafter_to_normed_embedding():
     np.testing.assert_allclose(r["logits"][0], logits, rtol=1e-12, atol=1e-12)
 
 
-def test_draft_forward_matches_torch_fp64_restatement():
-    """Independent restatement with torch library routines (SDPA, silu) in
-    float64 over the tiny config; RoPE via complex multiplication."""
-    cfg, w = _tiny_setup(seed=0)
+@pytest.mark.parametrize("qk_norm", [False, True])
+def test_draft_forward_matches_torch_fp64_restatement(qk_norm):
+    """Independent restatement with torch library routines (SDPA, silu,
+    functional rms_norm for the per-head QK-norm) in float64 over the tiny
+    config; RoPE via complex multiplication."""
+    cfg = replace(TINY, layers=2, qk_norm=qk_norm)
+    w = oracle.weights_to_numpy(make_weights(cfg, 0))
     feats = make_features(cfg, 64, seed=1).float().numpy()
     cache = oracle.RequestCache(cfg.layers, cfg.n_kv_heads, cfg.head_dim)
     oracle.inject_context(w, cfg, cache, feats)
@@ -266,12 +269,17 @@ def test_draft_forward_matches_torch_fp64_restatement():
     pos_c = torch.arange(64)
     pos_b = torch.arange(64, 64 + g)
     x = T(w["embed"])[[5] + [cfg.mask_id] * (g - 1)]
+    def qkn(x, gain):   # per-head norm of a Qwen3-style q_norm / k_norm (library routine)
+        if not qk_norm:
+            return x
+        return torch.nn.functional.rms_norm(x, (hd,), T(gain), eps=cfg.rms_eps)
+
     for lw in w["layers"]:
-        kc = rot((h_t @ T(lw["w_k"]).T).reshape(64, nkv, hd), pos_c)
+        kc = rot(qkn((h_t @ T(lw["w_k"]).T).reshape(64, nkv, hd), lw.get("g_k")), pos_c)
         vc = (h_t @ T(lw["w_v"]).T).reshape(64, nkv, hd)
         u = rms(x)
-        q = rot((u @ T(lw["w_q"]).T).reshape(g, nq, hd), pos_b)
-        kb = rot((u @ T(lw["w_k"]).T).reshape(g, nkv, hd), pos_b)
+        q = rot(qkn((u @ T(lw["w_q"]).T).reshape(g, nq, hd), lw.get("g_q")), pos_b)
+        kb = rot(qkn((u @ T(lw["w_k"]).T).reshape(g, nkv, hd), lw.get("g_k")), pos_b)
         vb = (u @ T(lw["w_v"]).T).reshape(g, nkv, hd)
         K = torch.cat([kc, kb]).permute(1, 0, 2).repeat_interleave(nq // nkv, 0)
         V = torch.cat([vc, vb]).permute(1, 0, 2).repeat_interleave(nq // nkv, 0)
@@ -610,3 +618,23 @@ def test_choose_block_special_cases():
     assert oracle.choose_block(cands, [0.0] * 15, 4, 1.0, 0.1, 0.0) == (2, 1.0)
     # every draft accepted and rows free: tau = g
     assert oracle.choose_block(cands, [1.0] * 15, 1, 1.0, 0.0, 0.0) == (16, 16.0)
+
+
+def test_qk_norm_makes_the_drafter_invariant_to_the_scale_of_w_q_and_w_k():
+    """Special case of the per-head norm: scaling W^Q or W^K by a positive
+    constant changes nothing once every query and key head is normalised
+    (without QK-norm the same scaling changes the logits).  Exact with
+    eps = 0: eps is what breaks the scale invariance of an RMS norm."""
+    for qk in (True, False):
+        cfg = replace(TINY, layers=2, qk_norm=qk, rms_eps=0.0)
+        w = oracle.weights_to_numpy(make_weights(cfg, 3))
+        feats = make_features(cfg, 16, seed=4).float().numpy()
+        w2 = dict(w, layers=[dict(lw, w_q=lw["w_q"] * 4.0, w_k=lw["w_k"] * 2.0) for lw in w["layers"]])
+        out = []
+        for ww in (w, w2):
+            cache = oracle.RequestCache(cfg.layers, cfg.n_kv_heads, cfg.head_dim)
+            out.append(oracle.draft_cycle(ww, cfg, cache, feats, anchor=9, block=4)["logits"])
+        if qk:
+            np.testing.assert_allclose(out[1], out[0], rtol=1e-9, atol=1e-11)
+        else:
+            assert np.max(np.abs(out[1] - out[0])) > 1e-4
