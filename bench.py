@@ -481,6 +481,43 @@ def measure_sampled_verify(K: int, W: int = 3, B: int = 32, g: int = 16, V: int 
             "mean_tau": round(float(tau.float().mean().item()), 3)}
 
 
+def measure_packed_attention(K: int, W: int = 3) -> dict:
+    """dflash_packed_block_attention at the training shape of paper §7.1: a
+    3072-token sequence, 512 anchor blocks of 16, 32 q / 8 kv heads of 128,
+    bf16 inputs.  Tensor-bound: algorithmic flops = 4 * nq * block * hd *
+    sum_n (a_n + block) (Q K^T and P V over each block's visible keys)."""
+    import numpy as np
+    import block_diffusion_drafter_dflash_gb300 as df
+    S, N, g, nq, nkv, hd = 3072, 512, 16, 32, 8, 128
+    rng = np.random.default_rng(7)
+    anchors = sorted(int(a) for a in rng.choice(np.arange(1, S - g), size=N, replace=False))
+    gen = torch.Generator(device="cuda").manual_seed(71)
+    r = lambda *shape: torch.randn(shape, generator=gen, device="cuda").to(torch.bfloat16)
+    q, kc, vc, kb, vb = r(N, g, nq, hd), r(S, nkv, hd), r(S, nkv, hd), r(N, g, nkv, hd), r(N, g, nkv, hd)
+    out = torch.empty((N, g, nq, hd), device="cuda")
+    ws = df.dflash_packed_attention_workspace(N, g, S, nq, nkv, hd)
+    a_dev = torch.tensor(anchors, dtype=torch.int32, device="cuda")
+    for _ in range(W):
+        df.dflash_packed_block_attention(q, kc, vc, kb, vb, a_dev, out, ws)
+    torch.cuda.synchronize()
+    n0 = df.dflash_launch_count()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(K):
+        df.dflash_packed_block_attention(q, kc, vc, kb, vb, a_dev, out, ws)
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / K
+    flops = 4 * nq * g * hd * sum(a + g for a in anchors)
+    _, _, bf16_sus, src = load_peaks()
+    tf = flops / (ms / 1e3) / 1e12
+    return {"shape": f"sequence {S}, {N} anchor blocks of {g}, {nq} q / {nkv} kv heads of {hd}, bf16",
+            "ms_per_call": round(ms, 4), "launches_per_call": int((df.dflash_launch_count() - n0) // K),
+            "algorithmic_flops": flops, "achieved_TFLOPs": round(tf, 2), "peak_TFLOPs": bf16_sus,
+            "frac": round(tf / bf16_sus, 4), "peak_source": f"{src} (sustained bf16)",
+            "status": df.dflash_packed_attention_status(ws), "finite": bool(torch.isfinite(out).all().item())}
+
+
 def run_gpu(args, rank, world, local):
     torch.cuda.set_device(local)
     wl = workloads()[args.workload]
@@ -505,6 +542,8 @@ def run_gpu(args, rank, world, local):
                                                "roofline", "stages", "gpu_launches", "clocks")}
         torch.cuda.empty_cache()
         result["verify_sampled"] = measure_sampled_verify(min(args.steps, 50))
+        torch.cuda.empty_cache()
+        result["packed_attention"] = measure_packed_attention(min(args.steps, 20))
     return result, cyc
 
 

@@ -22,7 +22,8 @@ __all__ = ["DFlashError", "Model", "Cache", "lib", "dflash_model_create", "dflas
            "dflash_verify_greedy", "dflash_get_status", "dflash_clear_status", "dflash_version",
            "dflash_launch_count", "dflash_profile_start", "dflash_profile_stop", "dflash_inject_context_noalloc",
            "dflash_selftest_wait_timeout", "dflash_sampling_workspace", "dflash_verify_sampled", "dflash_sample_tokens",
-           "BlockPolicy"]
+           "BlockPolicy", "dflash_packed_attention_workspace", "dflash_packed_block_attention",
+           "dflash_packed_attention_status"]
 
 
 def _stream_ptr(stream: Optional[torch.cuda.Stream]) -> ctypes.c_void_p:
@@ -267,6 +268,43 @@ def dflash_sample_tokens(logits: torch.Tensor, temperature: float, u: torch.Tens
         workspace = dflash_sampling_workspace(rows, rows, V)
     check(lib().dflash_sample_tokens(_ptr(logits), rows, V, float(temperature), _ptr(u), _ptr(tokens),
                                      _ptr(workspace), workspace.numel(), _stream_ptr(stream)), "dflash_sample_tokens")
+
+
+def dflash_packed_attention_workspace(n_blocks: int, block: int, seq_len: int, n_q_heads: int, n_kv_heads: int,
+                                      head_dim: int) -> torch.Tensor:
+    n = int(lib().dflash_packed_attention_workspace_bytes(n_blocks, block, seq_len, n_q_heads, n_kv_heads, head_dim))
+    if n == 0:
+        raise ValueError("invalid packed attention shape")
+    return torch.empty(n, dtype=torch.uint8, device="cuda")
+
+
+def dflash_packed_block_attention(q: torch.Tensor, k_ctx: torch.Tensor, v_ctx: torch.Tensor, k_blk: torch.Tensor,
+                                  v_blk: torch.Tensor, anchors_dev: torch.Tensor, out: torch.Tensor,
+                                  workspace: torch.Tensor, anchors_host=None, stream=None) -> None:
+    """Packed training attention: q [N, g, nq, hd], k_ctx / v_ctx [S, nkv, hd],
+    k_blk / v_blk [N, g, nkv, hd] (fp32 or bf16), anchors int32 [N] -> out fp32 [N, g, nq, hd]."""
+    N, g, nq, hd = q.shape
+    S, nkv = k_ctx.shape[0], k_blk.shape[2]
+    dt = _abi.DTYPE_F32 if q.dtype == torch.float32 else _abi.DTYPE_BF16
+    for t in (k_ctx, v_ctx, k_blk, v_blk):
+        if t.dtype != q.dtype:
+            raise ValueError("q, k and v must share one dtype")
+    if out.dtype != torch.float32 or anchors_dev.dtype != torch.int32:
+        raise ValueError("out must be float32 and anchors int32")
+    host = None
+    if anchors_host is not None:
+        host = (ctypes.c_int32 * N)(*[int(a) for a in anchors_host])
+    check(lib().dflash_packed_block_attention(_ptr(q), _ptr(k_ctx), _ptr(v_ctx), _ptr(k_blk), _ptr(v_blk),
+                                              _ptr(anchors_dev), host, N, g, S, nq, nkv, hd, dt, _ptr(out),
+                                              _ptr(workspace), workspace.numel(), _stream_ptr(stream)),
+          "dflash_packed_block_attention")
+
+
+def dflash_packed_attention_status(workspace: torch.Tensor, stream=None) -> int:
+    st = ctypes.c_int32(0)
+    check(lib().dflash_packed_attention_status(_ptr(workspace), _stream_ptr(stream), ctypes.byref(st)),
+          "dflash_packed_attention_status")
+    return st.value
 
 
 class BlockPolicy:

@@ -80,6 +80,10 @@ SIGNATURES = {
     "dflash_block_policy_observe": (c_i32, [c_ptr, c_i32, c_i32p, c_i32]),
     "dflash_block_policy_choose": (c_i32, [c_ptr, c_i32, c_i32p, ctypes.POINTER(ctypes.c_double)]),
     "dflash_block_policy_acceptance": (c_i32, [c_ptr, ctypes.POINTER(ctypes.c_double), c_i32]),
+    "dflash_packed_attention_workspace_bytes": (c_size, [c_i32, c_i32, c_i32, c_i32, c_i32, c_i32]),
+    "dflash_packed_block_attention": (c_i32, [c_ptr, c_ptr, c_ptr, c_ptr, c_ptr, c_ptr, c_i32p, c_i32, c_i32, c_i32,
+                                              c_i32, c_i32, c_i32, c_i32, c_ptr, c_ptr, c_size, c_ptr]),
+    "dflash_packed_attention_status": (c_i32, [c_ptr, c_ptr, c_i32p]),
     "dflash_launch_count": (ctypes.c_uint64, []),
     "dflash_synthetic_target": (c_i32, [c_ptr, c_ptr, c_ptr, c_ptr, c_i32, c_ptr, c_ptr, c_ptr, c_i32, c_i32, c_i32,
                                         c_ptr, c_ptr]),

@@ -17,6 +17,7 @@
 #include "attn_tc.cuh"
 #include "persist.cuh"
 #include "sampling.cuh"
+#include "packed_attention.cuh"
 
 using namespace dflash;
 
@@ -1032,6 +1033,81 @@ int32_t dflash_sample_tokens(const float* logits, int32_t rows, int32_t vocab, f
                                (cudaStream_t)stream),
           "token sampling");
   g_launch_count += launches;
+  return DFLASH_OK;
+}
+
+namespace {
+int32_t packed_shape(int32_t n_blocks, int32_t block, int32_t seq_len, int32_t nq, int32_t nkv, int32_t hd) {
+  if (n_blocks < 0 || block < 1 || block > kMaxBlock || seq_len < 0)
+    return fail(DFLASH_ERR_SHAPE, "n_blocks %d >= 0, block %d in [1, %d], seq_len %d >= 0 needed", n_blocks, block,
+                kMaxBlock, seq_len);
+  if (hd != 64 && hd != 128) return fail(DFLASH_ERR_SHAPE, "head_dim %d must be 64 or 128", hd);
+  if (nq <= 0 || nkv <= 0 || nq % nkv) return fail(DFLASH_ERR_SHAPE, "n_q_heads must be a positive multiple of n_kv_heads");
+  if ((long long)n_blocks * nkv > 65535) return fail(DFLASH_ERR_SHAPE, "n_blocks * n_kv_heads > 65535");
+  if ((long long)nkv * 2 * (seq_len + 1) * hd >= (1LL << 31) || (long long)n_blocks * nkv * 2 * hd * 64 >= (1LL << 31))
+    return fail(DFLASH_ERR_SHAPE, "packed attention operands exceed 2^31 rows");
+  return DFLASH_OK;
+}
+int current_sms() {
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return 0;
+  return sms;
+}
+}  // namespace
+
+size_t dflash_packed_attention_workspace_bytes(int32_t n_blocks, int32_t block, int32_t seq_len, int32_t nq,
+                                               int32_t nkv, int32_t hd) {
+  if (packed_shape(n_blocks, block, seq_len, nq, nkv, hd) != DFLASH_OK) return 0;
+  const int sms = current_sms();
+  if (sms <= 0) return 0;
+  return packed_workspace_bytes(std::max(n_blocks, 1), block, seq_len, nq, nkv, hd, sms);
+}
+
+int32_t dflash_packed_block_attention(const void* q, const void* k_ctx, const void* v_ctx, const void* k_blk,
+                                      const void* v_blk, const int32_t* anchors_dev, const int32_t* anchors_host,
+                                      int32_t n_blocks, int32_t block, int32_t seq_len, int32_t nq, int32_t nkv,
+                                      int32_t hd, int32_t dtype, float* out, void* workspace, size_t ws_bytes,
+                                      dflash_stream_t stream) {
+  int32_t rc = packed_shape(n_blocks, block, seq_len, nq, nkv, hd);
+  if (rc) return rc;
+  if (dtype != DFLASH_DTYPE_F32 && dtype != DFLASH_DTYPE_BF16) return fail(DFLASH_ERR_INVALID_ARG, "bad dtype %d", dtype);
+  if (n_blocks == 0) return DFLASH_OK;
+  if (!q || !k_blk || !v_blk || !anchors_dev || !out || !workspace || (seq_len > 0 && (!k_ctx || !v_ctx)))
+    return fail(DFLASH_ERR_INVALID_ARG, "a device pointer is NULL");
+  if (reinterpret_cast<uintptr_t>(workspace) % 256) return fail(DFLASH_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+  if (anchors_host)
+    for (int n = 0; n < n_blocks; ++n)
+      if (anchors_host[n] < 0 || anchors_host[n] > seq_len)
+        return fail(DFLASH_ERR_INVALID_ARG, "anchor[%d] = %d outside [0, %d]", n, anchors_host[n], seq_len);
+  const int sms = current_sms();
+  if (sms <= 0) return fail(DFLASH_ERR_CUDA, "no current device");
+  const size_t need = packed_workspace_bytes(n_blocks, block, seq_len, nq, nkv, hd, sms);
+  if (ws_bytes < need) return fail(DFLASH_ERR_WORKSPACE, "workspace %zu bytes < %zu needed", ws_bytes, need);
+  // shared-memory opt-in of the split kernel, once per device and head size
+  static std::atomic<unsigned> prepared[64];
+  int dev = 0;
+  DF_CUDA(cudaGetDevice(&dev), "cudaGetDevice");
+  const unsigned bit = hd == 64 ? 1u : 2u;
+  if (dev < 0 || dev >= 64 || !(prepared[dev].load() & bit)) {
+    DF_CUDA(attention_tc_prepare(hd), "packed attention set-up");
+    if (dev >= 0 && dev < 64) prepared[dev].fetch_or(bit);
+  }
+  // (with no context no block has a context tile: the one-row slabs are never read)
+  const PackedPlan pl = packed_plan(workspace, n_blocks, block, seq_len, nq, nkv, hd, sms);
+  int launches = 0;
+  DF_CUDA(packed_attention_run(pl, dtype == DFLASH_DTYPE_F32, q, seq_len ? k_ctx : nullptr, seq_len ? v_ctx : nullptr,
+                               k_blk, v_blk, anchors_dev, out, sms, &launches, (cudaStream_t)stream),
+          "packed block attention");
+  g_launch_count += launches;
+  return DFLASH_OK;
+}
+
+int32_t dflash_packed_attention_status(const void* workspace, dflash_stream_t stream, int32_t* status_host) {
+  if (!workspace || !status_host) return fail(DFLASH_ERR_INVALID_ARG, "workspace or status_host is NULL");
+  DF_CUDA(cudaMemcpyAsync(status_host, workspace, sizeof(int32_t), cudaMemcpyDeviceToHost, (cudaStream_t)stream),
+          "status read");
+  DF_CUDA(cudaStreamSynchronize((cudaStream_t)stream), "status sync");
   return DFLASH_OK;
 }
 

@@ -203,10 +203,14 @@ cudaError_t attention_prepare(int rows, int hd) {
                               (int)attn_smem_bytes(rows, hd));
 }
 
-cudaError_t attention_bf16_launch(const AttnParams& p, const attn_tc::Maps& maps, int32_t* status, cudaStream_t s) {
+cudaError_t attention_bf16_launch(const AttnParams& p, const attn_tc::Maps& maps, int32_t* status, cudaStream_t s,
+                                  bool out_f32) {
   if (p.B <= 0) return cudaSuccess;
   cudaError_t e = attention_tc_split_launch(p, maps, status, s);
   if (e != cudaSuccess) return e;
+  // the merge writes the W_O GEMM's bf16 hi/lo operand planes, or fp32 rows
+  if (out_f32)
+    return launch_pdl(attn_combine_kernel<float>, dim3((p.B * p.nq * p.block + 3) / 4), dim3(128), 0, s, p);
   return launch_pdl(attn_combine_kernel<__nv_bfloat16>, dim3((p.B * p.nq * p.block + 3) / 4), dim3(128), 0, s, p);
 }
 

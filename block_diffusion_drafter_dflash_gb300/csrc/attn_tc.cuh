@@ -19,7 +19,9 @@
 // log2(e)/sqrt(hd)).
 //
 // Keys.  A group's keys are its context keys 0..c-1 (cache) in tiles of 128,
-// then one tile of its block keys.  K is stored key-major ([pos][hd]) and V
+// then one tile of its block keys.  With ctx_shared every request reads the
+// context slab of request 0 (its own length c): the blocks of one packed
+// training sequence share that sequence's context.  K is stored key-major ([pos][hd]) and V
 // hd-major ([hd][pos]), so that both products read their B operand K-major;
 // tiles arrive by TMA (128-byte swizzle).  Keys past the valid ones read
 // finite values (the cache is zeroed at creation; past the tensor end TMA
@@ -156,12 +158,13 @@ template <int HD>
 __device__ void load_k(const AttnParams& p, const Maps& m, int b, int kvh, int t, int nct, uint8_t* sm, Bars* bars) {
   using C = Cfg<HD>;
   uint8_t* kt = sm + C::kOffK;
+  const int bc = p.ctx_shared ? 0 : b;   // the context slab
   ptx::mbar_arrive_expect_tx(&bars->kfull, C::kKBytes);
   for (int pl = 0; pl < 2; ++pl)
     for (int s = 0; s < C::kSub; ++s) {
       uint8_t* dst = kt + (s * 2 + pl) * kTile16;
       if (t < nct) {
-        const int row = ((((b * p.layers + p.layer) * p.nkv + kvh) * 2 + pl) * p.cap) + kKeys * t;
+        const int row = ((((bc * p.layers + p.layer) * p.nkv + kvh) * 2 + pl) * p.cap) + kKeys * t;
         ptx::tma_load_2d(dst, &m.kc, &bars->kfull, 64 * s, row, ptx::policy_evict_first());
       } else {
         const int row = ((b * p.nkv + kvh) * 2 + pl) * p.block;
@@ -174,12 +177,13 @@ template <int HD>
 __device__ void load_v(const AttnParams& p, const Maps& m, int b, int kvh, int t, int nct, uint8_t* sm, Bars* bars) {
   using C = Cfg<HD>;
   uint8_t* vt = sm + C::kOffV;
+  const int bc = p.ctx_shared ? 0 : b;   // the context slab
   ptx::mbar_arrive_expect_tx(&bars->vfull, C::kVBytes);
   for (int pl = 0; pl < 2; ++pl)
     for (int h = 0; h < 2; ++h) {
       uint8_t* dst = vt + (h * 2 + pl) * C::kVHalf;
       if (t < nct) {
-        const int row = (((b * p.layers + p.layer) * p.nkv + kvh) * 2 + pl) * HD;
+        const int row = (((bc * p.layers + p.layer) * p.nkv + kvh) * 2 + pl) * HD;
         ptx::tma_load_2d(dst, &m.vc, &bars->vfull, kKeys * t + 64 * h, row, ptx::policy_evict_first());
       } else {
         const int row = ((b * p.nkv + kvh) * 2 + pl) * HD;

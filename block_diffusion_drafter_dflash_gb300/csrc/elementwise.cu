@@ -316,6 +316,8 @@ __device__ __forceinline__ void qknorm_rope_vec(float* v, const float* g, float 
 template <typename T, int E>
 __global__ void __launch_bounds__(256) qknorm_block_kernel(float* q, T* kb, const T* g_q, const T* g_k, int B, int block,
                                                            int nq, int nkv, float eps, const float2* rope) {
+  griddep_wait();   // the projection that wrote q and kb has finished
+  griddep_trigger();
   const int hd = 32 * E, half = hd / 2;
   const int w = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
   const int nqv = B * nq * block, nkvv = B * nkv * block;
@@ -350,6 +352,8 @@ template <typename T, int E>
 __global__ void __launch_bounds__(256) qknorm_cache_kernel(T* kc, const int2* rowinfo, int rows, int layer, int layers,
                                                            int nkv, int cap, const T* g_k, float eps,
                                                            const float2* rope) {
+  griddep_wait();   // the injection projection (or the previous layer's pass) has finished
+  griddep_trigger();
   const int hd = 32 * E, half = hd / 2;
   const int w = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
   if (w >= rows * nkv) return;

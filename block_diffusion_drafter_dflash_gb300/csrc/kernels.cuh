@@ -21,6 +21,7 @@ struct AttnParams {
   int B, nq, nkv, hd, block;
   int chunk;            // keys per split (context + block keys counted together)
   int splits;
+  int ctx_shared;       // 1: every request reads request 0's context slab (packed training blocks of one sequence)
   float* opart;         // [B][nq][block][splits][hd] unnormalised partial outputs
   float2* ml;           // [B][nq][block][splits] (running max, running sum)
   void* out;            // [B*block][nq*hd]: the W_O GEMM's activation operand
@@ -34,12 +35,15 @@ namespace attn_tc { struct Maps; }
 template <typename T> cudaError_t attention_launch(const AttnParams& p, cudaStream_t s);
 // bf16 models: tensor-core split-KV attention (tensor maps of the K/V cache and
 // of the block K/V, see attn_tc.cuh) and the merge; V is stored hd-major.
-cudaError_t attention_bf16_launch(const AttnParams& p, const attn_tc::Maps& maps, int32_t* status, cudaStream_t s);
+cudaError_t attention_bf16_launch(const AttnParams& p, const attn_tc::Maps& maps, int32_t* status, cudaStream_t s,
+                                  bool out_f32 = false);
 // Tensor maps of the bf16 attention: K cache [slabs*cap][hd], V cache
 // [slabs*hd][cap] (row pitch cap_pitch), block K [slabs*block][hd], block V
 // [slabs*hd][block] (row pitch block_pitch); 64 x rows boxes, 128-byte swizzle.
 bool encode_attention_maps(attn_tc::Maps* m, const void* kc, const void* vc, const void* kb, const void* vb, int B,
                            int layers, int nkv, int hd, int cap, int cap_pitch, int block, int block_pitch);
+// Shared-memory opt-in of the tensor-core split-KV attention kernel for head size hd.
+cudaError_t attention_tc_prepare(int hd);
 // One-time per-device setup (shared-memory opt-in) for up to `rows` query rows.
 template <typename T> cudaError_t attention_prepare(int rows, int hd);
 int attention_max_rows();   // largest (nq/nkv)*block the kernel accepts

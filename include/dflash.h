@@ -308,6 +308,44 @@ int32_t dflash_sample_tokens(const float* logits_dev, int32_t rows, int32_t voca
                              const float* u_dev, int32_t* tokens_dev, void* workspace, size_t workspace_bytes,
                              dflash_stream_t stream);
 
+/* --- training-time packed block attention (forward) ---------------------------
+ * Paper §4.2: training samples anchors from a sequence, opens a block of
+ * block_size positions at each, concatenates all blocks and runs them in one
+ * pass under a sparse mask; explainer "Training Rehearses the Same Masked
+ * Blocks Used at Runtime" (Figure 4): clean target context features are
+ * visible to each block, positions attend bidirectionally inside their own
+ * block, and nothing crosses between blocks.  Reading (matches inference,
+ * where the block starts right after the injected context): block n, anchored
+ * at position a_n, sees context keys 0 .. a_n - 1 and its own block_size rows.
+ * softmax(q k^T / sqrt(head_dim)) v with grouped-query heads (q head h reads
+ * kv head h / (n_q_heads / n_kv_heads)); no mask is materialised.
+ *   q_dev       [n_blocks][block][n_q_heads][head_dim]   block queries (RoPE applied)
+ *   k_ctx_dev, v_ctx_dev  [seq_len][n_kv_heads][head_dim]  the sequence's context keys / values
+ *   k_blk_dev, v_blk_dev  [n_blocks][block][n_kv_heads][head_dim]  the blocks' own keys / values
+ *               (all five in `dtype`: DFLASH_DTYPE_F32 or DFLASH_DTYPE_BF16)
+ *   anchors_dev int32 [n_blocks] device; anchors_host: the same on the host, or
+ *               NULL.  Given, every anchor is checked to lie in [0, seq_len] and
+ *               DFLASH_ERR_INVALID_ARG is returned without a launch; otherwise
+ *               the device clamps an anchor outside and sets the status word.
+ *   out_dev     fp32 [n_blocks][block][n_q_heads][head_dim]
+ *   workspace   >= dflash_packed_attention_workspace_bytes(...) bytes, 256-byte
+ *               aligned; its first int32 is the call's status word (0, or
+ *               DFLASH_ERR_INVALID_ARG / DFLASH_ERR_TIMEOUT), read with
+ *               dflash_packed_attention_status.
+ * Operands run through the tensor cores at fp32 precision (hi/lo bf16 pairs).
+ * head_dim 64 or 128; 1 <= block <= 32; n_blocks * n_kv_heads <= 65535.
+ * The workspace size depends on the current device's SM count. */
+size_t dflash_packed_attention_workspace_bytes(int32_t n_blocks, int32_t block, int32_t seq_len, int32_t n_q_heads,
+                                               int32_t n_kv_heads, int32_t head_dim);
+int32_t dflash_packed_block_attention(const void* q_dev, const void* k_ctx_dev, const void* v_ctx_dev,
+                                      const void* k_blk_dev, const void* v_blk_dev, const int32_t* anchors_dev,
+                                      const int32_t* anchors_host, int32_t n_blocks, int32_t block, int32_t seq_len,
+                                      int32_t n_q_heads, int32_t n_kv_heads, int32_t head_dim, int32_t dtype,
+                                      float* out_dev, void* workspace, size_t workspace_bytes,
+                                      dflash_stream_t stream);
+/* Synchronises `stream` and copies the call's status word to *status_host. */
+int32_t dflash_packed_attention_status(const void* workspace, dflash_stream_t stream, int32_t* status_host);
+
 /* --- block-size scheduling (host policy) ---------------------------------------
  * Paper §5.5.4: a drafter trained at a large block size serves smaller
  * inference-time block sizes nearly as well, and large blocks raise the

@@ -418,6 +418,50 @@ def expected_accept_len(alpha: Sequence[float]) -> float:
 
 
 # ---------------------------------------------------------------------------
+# Training-time packed block attention  (paper §4.2 "all blocks are
+# concatenated into a single sequence and processed jointly using a sparse
+# attention mask"; explainer "Training Rehearses the Same Masked Blocks Used
+# at Runtime" and its Figure 4)
+# ---------------------------------------------------------------------------
+
+def packed_block_mask(seq_len: int, anchors: Sequence[int], block: int) -> np.ndarray:
+    """M[r, j] over keys [context positions 0..seq_len-1 ; block rows of every
+    block], for the query rows r of every block (block n's rows are n*block ..
+    n*block + block - 1).  A row of block n sees context position j iff
+    j < a_n (the clean target features before its anchor: the anchor itself is
+    the block's first row, as at inference, where the block starts right after
+    the injected context), every row of its own block (bidirectional), and no
+    row of another block.  Built element by element from those cases."""
+    N = len(anchors)
+    M = np.zeros((N * block, seq_len + N * block), dtype=np.int64)
+    for n, a in enumerate(anchors):
+        for i in range(block):
+            r = n * block + i
+            for j in range(seq_len):
+                if j < a:
+                    M[r, j] = 1
+            for m in range(N):
+                for l in range(block):
+                    if m == n:
+                        M[r, seq_len + m * block + l] = 1
+    return M
+
+
+def attention_packed(q: np.ndarray, k_ctx: np.ndarray, v_ctx: np.ndarray, k_blk: np.ndarray, v_blk: np.ndarray,
+                     anchors: Sequence[int]) -> np.ndarray:
+    """Forward attention of the packed training sequence: q [N*block, nq, hd]
+    (every block's rows, RoPE applied), k_ctx / v_ctx [S, nkv, hd] (the
+    sequence's injected context keys / values), k_blk / v_blk [N*block, nkv,
+    hd] (the blocks' own keys / values), through packed_block_mask; scale
+    1/sqrt(hd), grouped-query heads as in attention_masked."""
+    N, S = len(anchors), k_ctx.shape[0]
+    block = q.shape[0] // N
+    mask = packed_block_mask(S, anchors, block)
+    return attention_masked(np.asarray(q, dtype=F64), np.concatenate([k_ctx, k_blk]).astype(F64),
+                            np.concatenate([v_ctx, v_blk]).astype(F64), mask)
+
+
+# ---------------------------------------------------------------------------
 # Block-size scheduling  (paper §5.5.4: a drafter trained at a large block
 # size serves smaller ones about as well, which allows choosing the block size
 # per cycle; large blocks cost more verification when compute-bound)

@@ -638,3 +638,62 @@ def test_qk_norm_makes_the_drafter_invariant_to_the_scale_of_w_q_and_w_k():
             np.testing.assert_allclose(out[1], out[0], rtol=1e-9, atol=1e-11)
         else:
             assert np.max(np.abs(out[1] - out[0])) > 1e-4
+
+
+# ---------------------------------------------------------------- packed training attention
+def _packed_inputs(S, anchors, g, nq, nkv, hd, seed=31):
+    r = np.random.default_rng(seed)
+    N = len(anchors)
+    return (r.standard_normal((N * g, nq, hd)), r.standard_normal((S, nkv, hd)), r.standard_normal((S, nkv, hd)),
+            r.standard_normal((N * g, nkv, hd)), r.standard_normal((N * g, nkv, hd)))
+
+
+@pytest.mark.parametrize("S,anchors,g", [(20, [3, 11, 0, 19], 4), (9, [9, 2], 3), (40, [5, 6, 7, 30, 12], 5)])
+def test_packed_attention_equals_one_inference_block_per_anchor(S, anchors, g):
+    """The packed forward reproduces, block by block, the inference-time block
+    attention over the context truncated at the anchor (no mask involved)."""
+    nq, nkv, hd = 4, 2, 8
+    q, kc, vc, kb, vb = _packed_inputs(S, anchors, g, nq, nkv, hd)
+    out = oracle.attention_packed(q, kc, vc, kb, vb, anchors)
+    for n, a in enumerate(anchors):
+        rows = slice(n * g, (n + 1) * g)
+        ref = oracle.attention_block(q[rows], kc[:a], vc[:a], kb[rows], vb[rows])
+        np.testing.assert_allclose(out[rows], ref, rtol=1e-12, atol=1e-12)
+
+
+def test_packed_attention_matches_library_sdpa_with_the_mask():
+    S, anchors, g, nq, nkv, hd = 17, [4, 9, 16], 4, 4, 2, 8
+    q, kc, vc, kb, vb = _packed_inputs(S, anchors, g, nq, nkv, hd, seed=32)
+    M = oracle.packed_block_mask(S, anchors, g)
+    K, V = np.concatenate([kc, kb]), np.concatenate([vc, vb])
+    rep = nq // nkv
+    ref = torch.nn.functional.scaled_dot_product_attention(
+        torch.tensor(q).permute(1, 0, 2), torch.tensor(K).permute(1, 0, 2).repeat_interleave(rep, 0),
+        torch.tensor(V).permute(1, 0, 2).repeat_interleave(rep, 0), attn_mask=torch.tensor(M, dtype=torch.bool))
+    np.testing.assert_allclose(oracle.attention_packed(q, kc, vc, kb, vb, anchors), ref.permute(1, 0, 2).numpy(),
+                               rtol=1e-12, atol=1e-12)
+
+
+def test_packed_mask_follows_the_explainers_example():
+    """Explainer, "Training Rehearses the Same Masked Blocks...": a block
+    anchored at r_2 sees its own block (the anchor r_2 included) and the clean
+    context before it, never the neighbouring block that begins at r_3."""
+    S, g, r2, r3 = 12, 3, 4, 7
+    M = oracle.packed_block_mask(S, [r2, r3], g)
+    assert M.shape == (2 * g, S + 2 * g)
+    for i in range(g):
+        assert M[i, :r2].all() and not M[i, r2:S].any()            # context strictly before the anchor
+        assert M[i, S:S + g].all()                                  # its own block, bidirectionally
+        assert not M[i, S + g:].any()                               # not the block starting at r_3
+        assert M[g + i, :r3].all() and not M[g + i, r3:S].any() and M[g + i, S + g:].all() and not M[g + i, S:S + g].any()
+    # the same facts seen through the attention output: moving the r_3 block's
+    # keys and values, or context at or after r_2, leaves the r_2 block unchanged
+    q, kc, vc, kb, vb = _packed_inputs(S, [r2, r3], g, 2, 1, 8, seed=33)
+    base = oracle.attention_packed(q, kc, vc, kb, vb, [r2, r3])
+    kb2, vb2, vc2 = kb.copy(), vb.copy(), vc.copy()
+    kb2[g:] += 1.0
+    vb2[g:] -= 2.0
+    vc2[r2:] += 3.0
+    moved = oracle.attention_packed(q, kc, vc2, kb2, vb2, [r2, r3])
+    np.testing.assert_allclose(moved[:g], base[:g], rtol=0, atol=0)
+    assert np.max(np.abs(moved[g:] - base[g:])) > 1e-3
