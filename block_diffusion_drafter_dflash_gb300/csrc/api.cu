@@ -479,6 +479,7 @@ struct PhaseBuilder {
     ph = PPhase{};
     ph.kind = kPhGemm;
     ph.epi = epi;
+    ph.kw = 64;
     ph.kb = K / 64;
     ph.xmap = xmap;
     ph.planes = planes;
@@ -518,6 +519,21 @@ struct PhaseBuilder {
   }
   int segs = 0;
   int nseg_total() const { return segs; }
+  // Phases whose tiles are all 128 features wide (weights on the MMA's M side)
+  // take 128 K columns a stage, so that their stages carry as many weight
+  // bytes as the wide phases' (more in flight across the phase boundaries).
+  void finish() {
+    for (int i = 0; i < p.nphase; ++i) {
+      PPhase& ph = p.ph[i];
+      if (ph.kind != kPhGemm || ph.kb % 2) continue;
+      bool narrow = true;
+      for (int j = ph.seg0; j < ph.seg0 + ph.nseg; ++j) narrow = narrow && p.seg[j].tw == 128;
+      if (narrow) {
+        ph.kw = 128;
+        ph.kb /= 2;
+      }
+    }
+  }
 };
 
 int32_t run_inject_persist(const dflash_model* m, dflash_cache* cache, const void* feats, const int32_t* n_new,
@@ -562,6 +578,7 @@ int32_t run_inject_persist(const dflash_model* m, dflash_cache* cache, const voi
     pb.seg(layer_map(l, kMapK), layer_map(l, kMapK), hk, 0, 2 * l);
     pb.seg(layer_map(l, kMapV), layer_map(l, kMapV), hk, 0, 2 * l + 1);
   }
+  pb.finish();
   DF_LAUNCH(DFLASH_STAGE_INJECT_PERSIST, 1, persist_launch(pp, m->sms, c.head_dim, s), "persistent injection");
   return DFLASH_OK;
 }
@@ -661,6 +678,7 @@ int32_t run_draft_persist(const dflash_model* m, const dflash_cache* cache, cons
     pb.add_gemm(kEpLM, D, 0, 2, kPRows, 1, nullptr);
     pb.seg(kMapLm, kMapLm, c.vocab, 0, 0, true, true);
   }
+  pb.finish();
   pp.trace = m->trace_persist ? m->trace_dev : nullptr;
   DF_LAUNCH(DFLASH_STAGE_DRAFT_PERSIST, 1, persist_launch(pp, m->sms, c.head_dim, s), "persistent drafter");
   return DFLASH_OK;

@@ -25,7 +25,10 @@
 // the M side (128 features x 32 token columns an instruction): their tiles
 // are split over fewer CTAs and all four compute warps read the accumulator
 // back, which keeps the phase tail short where it matters more than the
-// tensor-pipe rate.  A stage is [4 KB activations][<=32 KB weights] either way.
+// tensor-pipe rate.  A stage is [8 KB activations][32 KB weights] either way:
+// 64 K columns of 256 features for the wide phases, 128 K columns of 128
+// features (two 64-column boxes of each operand) for the narrow ones, so
+// every phase keeps the same bytes in flight.
 //
 // Roles (256 threads):
 //   warps 0, 3      lane 0: weight producers (even / odd ring slots), TMA of the
@@ -40,9 +43,13 @@
 //
 // Work split (stream-K): the (tile, 64-column K block) iterations of a
 // projection are divided evenly over the CTAs.  A tile cut between CTAs
-// leaves fp32 partial tiles; the last of its CTAs to finish (atomic ticket)
-// sums them in CTA order and runs the epilogue, so results do not depend on
-// timing.
+// leaves fp32 partial tiles.  Its reducer is the CTA holding its first K
+// blocks: that piece ends the reducer's span, so it finishes last anyway.
+// The other CTAs publish their pieces and announce each with one atomic add;
+// the reducer keeps its own piece in shared memory, waits (bounded) for the
+// count, adds the others in CTA order and runs the epilogue — the sum does
+// not depend on timing, and the reducer's chain has no publish, fence or
+// ticket round trip of its own.
 //
 // RMSNorm folds into its neighbours: whoever produces a normed input (the
 // residual-stream epilogues, the fusion epilogue, the draft prologue) writes
@@ -73,10 +80,11 @@ namespace dflash {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kXBytes = 2 * kPRows * 128;         // activation tile: two 16-row planes (A rows 0..31)
+constexpr int kXHalf = 2 * kPRows * 128;          // activations of 64 K columns: two 16-row planes (A rows 0..31)
+constexpr int kXBytes = 2 * kXHalf;               // a stage holds up to 128 K columns of activations
 constexpr int kTwMax = 256;                       // features per tile (MMA N)
 constexpr int kWBox = 128 * 128;                  // one 128-row weight box
-constexpr int kStage = kXBytes + 2 * kWBox;       // 36 KB
+constexpr int kStage = kXBytes + 2 * kWBox;       // 40 KB
 constexpr int kLd = kPRows + 1;                   // staging tile pitch (floats)
 constexpr int kTmemCols = 2 * kTwMax;             // double-buffered 256-column accumulator
 constexpr long long kBudget = 200000000LL;        // SM cycles (~0.1 s): far beyond any legal wait
@@ -249,14 +257,19 @@ __device__ void weight_producer(const PParams& p, PBook* bk, uint8_t* ring, int 
       if (i - sp.i0 < 2) trace_at(p, cta, pi, kTrW0);
       if (i + 2 >= sp.i1) trace_at(p, cta, pi, kTrW1);
       {
-        const int t = i / ph.kb, kx = (i - t * ph.kb) * 64;
+        const int t = i / ph.kb, kx = (i - t * ph.kb) * ph.kw;
         const GemmSeg& sg = p.seg[seg_of(p, ph, t)];
-        const int tis = t - sg.tile_begin, nbox = sg.tw / 128;
+        const int tis = t - sg.tile_begin;
         uint8_t* w = ring + (size_t)s * kStage + kXBytes;
-        ptx::mbar_arrive_expect_tx(&bk->fullW[s], nbox * kWBox);
-        for (int h = 0; h < nbox; ++h)
-          ptx::tma_load_2d(w + h * kWBox, p.wmaps + ((sg.paired && h) ? sg.map1 : sg.map0), &bk->fullW[s], kx,
-                           box_row(sg, tis, h), pol);
+        ptx::mbar_arrive_expect_tx(&bk->fullW[s], 2 * kWBox);
+        if (ph.kw == 128) {   // 128 features x 128 K columns: one box per 64-column half of K
+          for (int h = 0; h < 2; ++h)
+            ptx::tma_load_2d(w + h * kWBox, p.wmaps + sg.map0, &bk->fullW[s], kx + 64 * h, box_row(sg, tis, 0), pol);
+        } else {              // 256 features x 64 K columns: two 128-row boxes
+          for (int h = 0; h < 2; ++h)
+            ptx::tma_load_2d(w + h * kWBox, p.wmaps + ((sg.paired && h) ? sg.map1 : sg.map0), &bk->fullW[s], kx,
+                             box_row(sg, tis, h), pol);
+        }
       }
     }
     if (par == 0) trace_val(p, cta, pi, kTrWaitWEmpty, we);
@@ -285,11 +298,13 @@ __device__ void activation_producer(const PParams& p, PBook* bk, uint8_t* ring, 
     for (int i = sp.i0; i < sp.i1; ++i, ++it) {
       const int s = it % S;
       if (it >= S && !wait_timed(&bk->empty[s], ((it / S) & 1) ^ 1, p.status, wx, true)) goto done;
-      const int kx = (i % ph.kb) * 64;
+      const int kx = (i % ph.kb) * ph.kw, halves = ph.kw / 64;
       uint8_t* x = ring + (size_t)s * kStage;
-      ptx::mbar_arrive_expect_tx(&bk->fullX[s], ph.planes * kPRows * 128);
-      for (int pl = 0; pl < ph.planes; ++pl)
-        ptx::tma_load_2d(x + pl * kPRows * 128, &p.xmap[ph.xmap], &bk->fullX[s], kx, pl * ph.prow, pol);
+      ptx::mbar_arrive_expect_tx(&bk->fullX[s], halves * ph.planes * kPRows * 128);
+      for (int hh = 0; hh < halves; ++hh)
+        for (int pl = 0; pl < ph.planes; ++pl)
+          ptx::tma_load_2d(x + hh * kXHalf + pl * kPRows * 128, &p.xmap[ph.xmap], &bk->fullX[s], kx + 64 * hh,
+                           pl * ph.prow, pol);
     }
     trace_val(p, cta, pi, kTrWaitXEmpty, wx);
   }
@@ -322,12 +337,14 @@ __device__ void mma_issuer(const PParams& p, PBook* bk, uint8_t* ring, uint32_t 
         ptx::tc_fence_after();
         if (i == sp.i0 && kk == k0) trace_at(p, cta, pi, kTrM0);
         uint8_t* st = ring + (size_t)s * kStage;
-        const uint64_t xd = ptx::smem_desc_sw128(st);             // activations (token rows 0..31)
-        const uint64_t wd = ptx::smem_desc_sw128(st + kXBytes);   // weights (tw rows)
-        const uint64_t ad = wide ? xd : wd, bd = wide ? wd : xd;
+        for (int hh = 0; hh < ph.kw / 64; ++hh) {   // 64 K columns at a time
+          const uint64_t xd = ptx::smem_desc_sw128(st + hh * kXHalf);             // activations (token rows 0..31)
+          const uint64_t wd = ptx::smem_desc_sw128(st + kXBytes + hh * kWBox);    // weights (tw rows)
+          const uint64_t ad = wide ? xd : wd, bd = wide ? wd : xd;
 #pragma unroll
-        for (int k = 0; k < 4; ++k)   // 4 x K=16 per 64-column stage; +32 B per step inside the swizzle row
-          ptx::mma_bf16(d, ad + 2 * k, bd + 2 * k, idesc, (kk > k0 || k > 0) ? 1u : 0u);
+          for (int k = 0; k < 4; ++k)   // 4 x K=16 per 64 columns; +32 B per step inside the swizzle row
+            ptx::mma_bf16(d, ad + 2 * k, bd + 2 * k, idesc, (kk > k0 || hh > 0 || k > 0) ? 1u : 0u);
+        }
         ptx::mma_commit(&bk->empty[s]);
         any = true;
       }
@@ -459,19 +476,24 @@ __device__ __forceinline__ void publish_piece(const PParams& p, int tw, const fl
     publish_tw<128>(p, st, dst, ct);
 }
 
-// Sum of the pieces of tile t (CTAs cf..cl, in CTA order, so that the result
-// does not depend on timing) into the staging tile.
+// Add the pieces of tile t from CTAs cf+1..cl (in CTA order) to the reducer's
+// own piece, staged in st: the sum runs in CTA order cf, cf+1, .., cl, so the
+// result does not depend on timing.
 template <int TW>
-__device__ void sum_pieces(const PParams& p, const PPhase& ph, int G, int t, float* st, int ct) {
+__device__ void add_pieces(const PParams& p, const PPhase& ph, int G, int t, int cf, int cl, float* st, int ct) {
   using PM = PieceMap<TW>;
   const int fq = 4 * (ct % PM::kQ), r0 = ct / PM::kQ;
   const int W = phase_iters(ph);
   const int g = phase_ctas(ph, G);
-  const int cf = cta_of(ph, G, t * ph.kb), cl = cta_of(ph, G, (t + 1) * ph.kb - 1);
   float4 acc[PM::kR];
 #pragma unroll
-  for (int j = 0; j < PM::kR; ++j) acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int c = cf; c <= cl; c += PM::kU) {
+  for (int j = 0; j < PM::kR; ++j) {
+    const int m = r0 + PM::kStep * j;
+    acc[j] = m < p.M ? make_float4(st[fq * kLd + m], st[(fq + 1) * kLd + m], st[(fq + 2) * kLd + m],
+                                   st[(fq + 3) * kLd + m])
+                     : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  for (int c = cf + 1; c <= cl; c += PM::kU) {
     float4 a[PM::kU][PM::kR];
 #pragma unroll
     for (int u = 0; u < PM::kU; ++u) {
@@ -486,9 +508,9 @@ __device__ void sum_pieces(const PParams& p, const PPhase& ph, int G, int t, flo
       }
     }
 #pragma unroll
-    for (int j = 0; j < PM::kR; ++j)
+    for (int u = 0; u < PM::kU; ++u)
 #pragma unroll
-      for (int u = 0; u < PM::kU; ++u) {
+      for (int j = 0; j < PM::kR; ++j) {
         acc[j].x += a[u][j].x;
         acc[j].y += a[u][j].y;
         acc[j].z += a[u][j].z;
@@ -503,6 +525,22 @@ __device__ void sum_pieces(const PParams& p, const PPhase& ph, int G, int t, flo
       st[(fq + 1) * kLd + m] = acc[j].y;
       st[(fq + 2) * kLd + m] = acc[j].z;
       st[(fq + 3) * kLd + m] = acc[j].w;
+    }
+  }
+}
+
+// Wait (bounded) until `n` pieces of a tile have been announced.
+__device__ bool wait_pieces(const int* counter, int n, int32_t* status) {
+  if ((int)ld_acquire(reinterpret_cast<const unsigned int*>(counter)) >= n) return true;
+  const long long t0 = clock64();
+  for (uint32_t it = 1;; ++it) {
+    if ((int)ld_acquire(reinterpret_cast<const unsigned int*>(counter)) >= n) return true;
+    if ((it & 63) == 0) {
+      if (*reinterpret_cast<volatile int32_t*>(status) == DFLASH_ERR_TIMEOUT) return false;
+      if (clock64() - t0 > kBudget) {
+        report_status(status, DFLASH_ERR_TIMEOUT);
+        return false;
+      }
     }
   }
 }
@@ -546,7 +584,6 @@ __device__ bool gemm_phase(const PParams& p, const PPhase& ph, int pi, PBook* bk
   csync();
   const Span sp = cta_span(ph, G, cta);
   const int first_tile = sp.i0 / max(ph.kb, 1);
-  int pend[2], npend = 0;   // partial tiles this CTA reduces
   for (int i = sp.i0; i < sp.i1;) {
     const int t = i / ph.kb, k0 = i - t * ph.kb, k1 = min(sp.i1 - t * ph.kb, ph.kb);
     i = t * ph.kb + k1;
@@ -610,28 +647,26 @@ __device__ bool gemm_phase(const PParams& p, const PPhase& ph, int pi, PBook* bk
       if (ct == 0 && last) trace_at(p, cta, pi, kTrPub);
       continue;
     }
-    // partial tile: publish it; the last CTA of the tile to publish reduces it,
-    // once all of its own pieces of the phase are out (a reduction between two
-    // of its pieces would hold up the second piece, and so the second tile)
-    publish_piece(p, tw, st, p.partial + (size_t)(cta * 2 + (t == first_tile ? 0 : 1)) * (kPRows * kTwMax), ct);
-    __threadfence();
-    csync();
     const int cf = cta_of(ph, G, t * ph.kb), cl = cta_of(ph, G, (t + 1) * ph.kb - 1);
-    if (ct == 0) {
-      const int old = atomicAdd(p.tickets + t, 1);
-      bk->flag_tk = old == cl - cf;
+    if (cta != cf) {
+      // a piece for the tile's reducer: publish it and announce it (release);
+      // nothing here waits for the reduction
+      publish_piece(p, tw, st, p.partial + (size_t)(cta * 2 + (t == first_tile ? 0 : 1)) * (kPRows * kTwMax), ct);
+      __threadfence();
+      csync();
+      if (ct == 0) {
+        atomicAdd(p.tickets + t, 1);
+        if (last) trace_at(p, cta, pi, kTrPub);
+      }
+      continue;
     }
-    csync();
-    if (ct == 0 && last) trace_at(p, cta, pi, kTrPub);
-    if (bk->flag_tk) pend[npend++] = t;   // only the first and the last tile of a span are partial
-  }
-  for (int j = 0; j < npend; ++j) {
-    const int t = pend[j];
+    // The designated reducer of tile t: the CTA holding its first K blocks.
+    // That piece ends this CTA's span (the tile continues into the next CTA),
+    // so it is this CTA's last one and is reduced at once, from shared memory.
+    // The residual input and the gain of a norm epilogue do not depend on the
+    // pieces: their loads go out first, parked in the staging tile's upper half
+    // (unused at 128 features; a row of kLd = kPRows + 1 floats holds both).
     const GemmSeg& sg = p.seg[seg_of(p, ph, t)];
-    __threadfence();
-    // the residual input and the gain do not depend on the pieces: their loads
-    // go out first, parked in the staging tile's upper half (unused at 128
-    // features; a row of kLd = kPRows + 1 floats holds both)
     const bool norm = (ph.epi == kEpResid || ph.epi == kEpFuse) && sg.tw == 128;
     float* xr = norm ? st + 128 * kLd + ct * kLd : nullptr;
     if (xr) {
@@ -643,16 +678,24 @@ __device__ bool gemm_phase(const PParams& p, const PPhase& ph, int pi, PBook* bk
       for (int m = 0; m < kPRows; ++m) xr[m] = v[m];
       xr[kPRows] = g;
     }
+    if (ct == 0) {
+      if (last) trace_at(p, cta, pi, kTrPub);
+      bk->flag_tk = wait_pieces(p.tickets + t, cl - cf, p.status);
+    }
+    csync();
+    if (!bk->flag_tk) return false;
     if (sg.tw == kTwMax)
-      sum_pieces<kTwMax>(p, ph, G, t, st, ct);
+      add_pieces<kTwMax>(p, ph, G, t, cf, cl, st, ct);
     else
-      sum_pieces<128>(p, ph, G, t, st, ct);
+      add_pieces<128>(p, ph, G, t, cf, cl, st, ct);
     csync();
     run_epilogue(p, ph, t, st, ct, xr);
     csync();
-    if (ct == 0) p.tickets[t] = 0;
+    if (ct == 0) {
+      p.tickets[t] = 0;   // every piece has arrived: ready for the next phase
+      trace_at(p, cta, pi, kTrRed);
+    }
   }
-  if (ct == 0 && npend) trace_at(p, cta, pi, kTrRed);
   return true;
 }
 

@@ -31,7 +31,8 @@ enum : int {
 
 struct PPhase {
   int kind, epi;
-  int kb;          // 64-column blocks of K
+  int kw;          // K columns per iteration (one ring stage): 64, or 128 for narrow phases
+  int kb;          // kw-column blocks of K
   int tiles;       // 128-feature output tiles
   int seg0, nseg;  // weight segments: seg[seg0 .. seg0+nseg), tile_begin relative to the phase
   int xmap;        // activation tensor map
