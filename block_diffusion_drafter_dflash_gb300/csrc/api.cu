@@ -168,8 +168,9 @@ struct WsPlan {
   GemmPlan g_fuse, g_inject, g_qkv, g_o, g_gu, g_down, g_lm;
   // persistent path: sums of squares, attention chunk partials, tickets + barrier
   int persist;
-  size_t ssq, aml, tickets;
+  size_t ssq, aml, tickets, qimg;
   int ntickets, nch;
+  size_t qimg_bytes;
 };
 
 // The persistent path serves bf16 calls of at most 16 token rows whose
@@ -220,6 +221,9 @@ WsPlan plan_ws(const dflash_model* m, int B, int cap, int block, int max_rows) {
       p.rope_q = take(sizeof(float2) * (size_t)kPRows * half);
       p.opart = take(sizeof(float) * (size_t)groups * p.nch * kPAttnRows * c.head_dim);
       p.aml = take(sizeof(float2) * (size_t)groups * p.nch * kPAttnRows);
+      // the queries as the attention's A-operand image, one pass of 64 rows a group
+      p.qimg_bytes = (size_t)groups * (c.head_dim / 64) * 16384;
+      p.qimg = take(p.qimg_bytes);
     }
     p.ssq = take(sizeof(float) * (size_t)(D / kTileN) * kPRows);
     p.partial = take(sizeof(float) * (size_t)m->sms * 2 * kPRows * 256);
@@ -603,7 +607,7 @@ int32_t run_draft_persist(const dflash_model* m, const dflash_cache* cache, cons
             persist_draft_prep_launch(static_cast<const __nv_bfloat16*>(m->embed), anchor, c.mask_token_id, c.vocab,
                                       B, block, D, static_cast<const __nv_bfloat16*>(m->layers[0].g_in), x, u,
                                       (size_t)kPRows * D, ssq, slots, tickets, P.ntickets + 1, m->status_dev, ctx_len,
-                                      m->inv_freq_dev, c.head_dim, rope, s),
+                                      m->inv_freq_dev, c.head_dim, rope, ws + P.qimg, P.qimg_bytes, s),
             "embedding");
   PParams pp{};
   if (!encode_activation_map(&pp.xmap[0], u, D, 2 * kPRows, D, kPRows) ||
@@ -626,7 +630,10 @@ int32_t run_draft_persist(const dflash_model* m, const dflash_cache* cache, cons
   float* q = reinterpret_cast<float*>(ws + P.q);
   __nv_bfloat16* kb = reinterpret_cast<__nv_bfloat16*>(ws + P.kb);
   __nv_bfloat16* vb = reinterpret_cast<__nv_bfloat16*>(ws + P.vb);
-  pp.qkv = EpiQKV<__nv_bfloat16>{q, kb, vb, rope, block, c.n_q_heads, c.n_kv_heads, c.head_dim, pad8(block)};
+  __nv_bfloat16* qimg = reinterpret_cast<__nv_bfloat16*>(ws + P.qimg);
+  const float att_scale = 1.0f / sqrtf((float)c.head_dim);
+  pp.qkv = EpiQKV<__nv_bfloat16>{q, kb, vb, rope, block, c.n_q_heads, c.n_kv_heads, c.head_dim, pad8(block),
+                                 qimg, att_scale * 1.4426950408889634f, c.n_q_heads / c.n_kv_heads};
   pp.swiglu = EpiSwiGLU<__nv_bfloat16>{a, F, (size_t)kPRows * F};
   pp.slots = slots;
   pp.logits = logits;
@@ -652,7 +659,8 @@ int32_t run_draft_persist(const dflash_model* m, const dflash_cache* cache, cons
   ap.ml = reinterpret_cast<float2*>(ws + P.aml);
   ap.out = o;
   ap.out_plane = (size_t)kPRows * hq;
-  ap.scale = 1.0f / sqrtf((float)c.head_dim);
+  ap.scale = att_scale;
+  ap.qimg = qimg;
   if (!encode_attention_maps(&pp.amaps, ap.kc, ap.vc, kb, vb, B, c.layers, c.n_kv_heads, c.head_dim, cache->cap,
                              pad8(cache->cap), block, pad8(block)))
     return fail(DFLASH_ERR_CUDA, "could not encode attention tensor maps");

@@ -73,7 +73,7 @@ struct Cfg {
 };
 
 struct Bars {
-  uint64_t kfull, vfull, sdone, odone;
+  uint64_t kfull, vfull, sdone, odone, qfull;
 };
 
 __device__ __forceinline__ void init_bars(Bars* b) {
@@ -81,6 +81,7 @@ __device__ __forceinline__ void init_bars(Bars* b) {
   ptx::mbar_init(&b->vfull, 1);
   ptx::mbar_init(&b->sdone, 1);
   ptx::mbar_init(&b->odone, 1);
+  ptx::mbar_init(&b->qfull, 1);
 }
 
 // A-tile row of query row i (0..63) of a pass: quarter i/16, hi part at +0, lo at +16
@@ -206,10 +207,13 @@ __device__ void load_v(const AttnParams& p, const Maps& m, int b, int kvh, int t
 // Optional `stamps` (globaltimer): [0] Q staged, [1] the first tile's scores
 // ready, [2] the last P V done, [3] output written, [4] the first V tile in
 // shared memory, [5] the first P tile stored.  Returns false on a timeout.
+// With p.qimg the Q tile arrives by one bulk copy of the group's prepared
+// image (qload: how many images this CTA loaded before, for the barrier
+// phase) instead of being staged from the fp32 queries.
 template <int HD, int NT, class Sync, class Out, class Done>
 __device__ bool run(const AttnParams& p, const Maps& m, int b, int kvh, int pass, int t0, int t1, int nct,
                     uint8_t* sm, uint32_t tmem, Bars* bars, int& uses, int tid, Sync sync, int32_t* status, Out out,
-                    Done done, float* xch = nullptr, unsigned long long* stamps = nullptr) {
+                    Done done, float* xch = nullptr, unsigned long long* stamps = nullptr, int qload = 0) {
   static_assert(NT == 128 || NT == 256, "128 or 256 threads");
   using C = Cfg<HD>;
   constexpr int NP = NT / 128;        // warps per lane quarter
@@ -226,9 +230,22 @@ __device__ bool run(const AttnParams& p, const Maps& m, int b, int kvh, int pass
 
   // the first tile's K now; its V once the scores are issued (it is needed
   // only after the softmax, and the Q loads need not queue behind it)
-  if (tid == 0 && t0 < t1) load_k<HD>(p, m, b, kvh, t0, nct, sm, bars);
-  stage_q<HD, NT>(p, b, kvh, pass, sm, tid);
-  ptx::fence_proxy_async_shared();
+  if (p.qimg) {
+    if (tid == 0) {
+      // the image was written by other CTAs through the generic proxy
+      ptx::fence_proxy_async_global();
+      ptx::mbar_arrive_expect_tx(&bars->qfull, C::kQ);
+      const int passes = (rows + 63) / 64;
+      ptx::bulk_load(sm, reinterpret_cast<const uint8_t*>(p.qimg) + ((size_t)(b * p.nkv + kvh) * passes + pass) * C::kQ,
+                     C::kQ, &bars->qfull);
+    }
+    if (tid == 0 && t0 < t1) load_k<HD>(p, m, b, kvh, t0, nct, sm, bars);
+    ok = ptx::mbar_wait(&bars->qfull, static_cast<uint32_t>(qload) & 1u, kBudget, status);
+  } else {
+    if (tid == 0 && t0 < t1) load_k<HD>(p, m, b, kvh, t0, nct, sm, bars);
+    stage_q<HD, NT>(p, b, kvh, pass, sm, tid);
+    ptx::fence_proxy_async_shared();
+  }
   sync();
   if (stamps && tid == 0) stamps[0] = ptx::globaltimer();
 

@@ -91,6 +91,15 @@ struct EpiQKV {
   const float2* rope;
   int block, nq, nkv, hd;
   int vpitch;
+  // Optional: the queries written instead as the block attention's A-operand
+  // image of each (request, kv head) group — row i = (head - kvh*G)*block + k
+  // of the group's 64 query rows, value q * qscale (log2-domain scores) as a
+  // bf16 hi part and lo residual (A rows 32(i/16) + i%16 and +16), 64-column
+  // subtiles of 128 rows x 128 bytes with the 128-byte swizzle — so that the
+  // attention loads it with one bulk copy.  Rows past G*block stay zero.
+  __nv_bfloat16* qimg;
+  float qscale;
+  int G;
   // thread n owns feature n of the tile; the RoPE entries of 8 rows are
   // loaded before any store so that their loads overlap
   __device__ __forceinline__ void operator()(const float* t, int ld, int m0, int mc, int, const GemmSeg& sg,
@@ -143,7 +152,18 @@ struct EpiQKV {
         }
         const float v = t[n * ld + m], pv = t[pn * ld + m];
         const float r = tag == 2 ? v : (d < half ? v * sc[j].x - pv * sc[j].y : v * sc[j].x + pv * sc[j].y);
-        if (tag == 0)
+        if (tag == 0 && qimg) {
+          const int kvh = head / G, i = (head - kvh * G) * block + k;
+          const float x = r * qscale;
+          const __nv_bfloat16 hi = __float2bfloat16_rn(x);
+          const __nv_bfloat16 lo = __float2bfloat16_rn(x - __bfloat162float(hi));
+          const int ch = (d & 63) >> 3;
+          const int rh = 32 * (i >> 4) + (i & 15), rl = rh + 16;
+          uint8_t* img = reinterpret_cast<uint8_t*>(qimg) + ((size_t)(b * nkv + kvh) * (hd >> 6) + (d >> 6)) * 16384 +
+                         2 * (d & 7);
+          *reinterpret_cast<__nv_bfloat16*>(img + rh * 128 + ((ch ^ (rh & 7)) << 4)) = hi;
+          *reinterpret_cast<__nv_bfloat16*>(img + rl * 128 + ((ch ^ (rl & 7)) << 4)) = lo;
+        } else if (tag == 0)
           q[(((size_t)b * nh + head) * block + k) * hd + d] = r;
         else
           put_act(dkv, (size_t)block * hd, (((size_t)b * nh + head) * planes * block + k) * hd + d, r);

@@ -705,7 +705,7 @@ __device__ bool gemm_phase(const PParams& p, const PPhase& ph, int pi, PBook* bk
 // rows to global memory, maxima in log2 units.  Returns false on a timeout.
 template <int HD>
 __device__ bool attn_phase(const PParams& p, const PPhase& ph, int pi, PBook* bk, uint8_t* sm, uint32_t tmem, int cta,
-                           int ct, int& uses) {
+                           int ct, int& uses, int& qloads) {
   const AttnParams& ap = p.attn;
   AttnItem item;
   if (!attn_item(ap, cta, item)) return true;
@@ -729,7 +729,8 @@ __device__ bool attn_phase(const PParams& p, const PPhase& ph, int pi, PBook* bk
   // trace slots kTrAcc..kTrRed of an attention phase: the core's stamps
   unsigned long long* stamps = p.trace ? p.trace + ((size_t)cta * kPMaxPhases + pi) * kTrSlots + kTrAcc : nullptr;
   const bool ok = attn_tc::run<HD, 128>(a, p.amaps, b, kvh, 0, t0, t1, nct, sm, tmem, &bk->abars, uses, ct,
-                                        ComputeSync{}, p.status, out, done, nullptr, stamps);
+                                        ComputeSync{}, p.status, out, done, nullptr, stamps, qloads);
+  ++qloads;
   if (ct == 0) trace_at(p, cta, pi, kTrM1);
   return ok;
 }
@@ -801,7 +802,7 @@ __device__ void compute_warps(const PParams& p, PBook* bk, uint8_t* ring, uint8_
                               int cta) {
   const int ct = threadIdx.x - 128;
   float* st = reinterpret_cast<float*>(region);
-  int seq = 0, attn_uses = 0;
+  int seq = 0, attn_uses = 0, qloads = 0;
   for (int pi = 0; pi < p.nphase; ++pi) {
     const PPhase& ph = p.ph[pi];
     if (ct == 0) trace_at(p, cta, pi, kTrStart);
@@ -809,8 +810,8 @@ __device__ void compute_warps(const PParams& p, PBook* bk, uint8_t* ring, uint8_
       if (!gemm_phase(p, ph, pi, bk, st, tmem, G, cta, ct, seq)) return;
     } else if (ph.kind == kPhAttn) {
       // the weight producers hold off until this phase releases the ring
-      const bool ok = p.attn.hd == 64 ? attn_phase<64>(p, ph, pi, bk, ring, tmem, cta, ct, attn_uses)
-                                      : attn_phase<128>(p, ph, pi, bk, ring, tmem, cta, ct, attn_uses);
+      const bool ok = p.attn.hd == 64 ? attn_phase<64>(p, ph, pi, bk, ring, tmem, cta, ct, attn_uses, qloads)
+                                      : attn_phase<128>(p, ph, pi, bk, ring, tmem, cta, ct, attn_uses, qloads);
       csync();
       if (ct == 0) ptx::mbar_arrive(&bk->ring_free);
       if (!ok) return;
@@ -910,12 +911,16 @@ __global__ void __launch_bounds__(kThreads, 1) persist_kernel(const __grid_const
 __global__ void __launch_bounds__(256) persist_draft_prep_kernel(
     const __nv_bfloat16* embed, const int32_t* anchor, int mask_id, int vocab, int block, int D,
     const __nv_bfloat16* g, float* x, __nv_bfloat16* u, size_t u_plane, float* ssq, unsigned long long* slots,
-    int* zero, int nzero, int32_t* status, const int32_t* ctx_len, const double* inv_freq, int hd, float2* rope) {
+    int* zero, int nzero, int32_t* status, const int32_t* ctx_len, const double* inv_freq, int hd, float2* rope,
+    uint4* qimg, int qimg16) {
   griddep_wait();
   griddep_trigger();
   const int row = blockIdx.x, b = row / block, k = row - b * block;
   if (row == 0)
     for (int i = threadIdx.x; i < nzero; i += blockDim.x) zero[i] = 0;
+  // query images: rows past a group's query rows must read as zero
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < qimg16; i += gridDim.x * blockDim.x)
+    qimg[i] = make_uint4(0u, 0u, 0u, 0u);
   if (threadIdx.x == 0) slots[row] = 0ull;
   const int pos = ctx_len[b] + k;
   for (int i = threadIdx.x; i < (hd >> 1); i += blockDim.x) {
@@ -1002,9 +1007,10 @@ cudaError_t persist_draft_prep_launch(const __nv_bfloat16* embed, const int32_t*
                                       int B, int block, int D, const __nv_bfloat16* g, float* x, __nv_bfloat16* u,
                                       size_t u_plane, float* ssq, unsigned long long* slots, int* zero, int nzero,
                                       int32_t* status, const int32_t* ctx_len, const double* inv_freq, int hd,
-                                      float2* rope, cudaStream_t s) {
+                                      float2* rope, void* qimg, size_t qimg_bytes, cudaStream_t s) {
   return launch_pdl(persist_draft_prep_kernel, dim3(B * block), dim3(256), 0, s, embed, anchor, mask_id, vocab, block,
-                    D, g, x, u, u_plane, ssq, slots, zero, nzero, status, ctx_len, inv_freq, hd, rope);
+                    D, g, x, u, u_plane, ssq, slots, zero, nzero, status, ctx_len, inv_freq, hd, rope,
+                    static_cast<uint4*>(qimg), (int)(qimg_bytes / 16));
 }
 
 }  // namespace dflash

@@ -82,11 +82,11 @@ cudaError_t persist_prepare(int hd);
 
 // Draft prologue: x[row] = E[token], planes of x * g_in (u), per-tile sums of
 // x^2 (ssq), RoPE table of the row's position, zeroed slots / tickets /
-// barrier (`nzero` ints at `zero`).
+// barrier (`nzero` ints at `zero`), zeroed query images (`qimg_bytes`).
 cudaError_t persist_draft_prep_launch(const __nv_bfloat16* embed, const int32_t* anchor, int mask_id, int vocab,
                                       int B, int block, int D, const __nv_bfloat16* g, float* x, __nv_bfloat16* u,
                                       size_t u_plane, float* ssq, unsigned long long* slots, int* zero, int nzero,
                                       int32_t* status, const int32_t* ctx_len, const double* inv_freq, int hd,
-                                      float2* rope, cudaStream_t s);
+                                      float2* rope, void* qimg, size_t qimg_bytes, cudaStream_t s);
 
 }  // namespace dflash

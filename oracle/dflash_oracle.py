@@ -55,15 +55,24 @@ def _f64(a) -> np.ndarray:
     return np.asarray(a, dtype=F64)
 
 
-def store(x: np.ndarray, mode: str = "f64") -> np.ndarray:
+# Tensor classes the storage study can round one at a time (see `store`).
+STORE_CLASSES = ("ht", "kv", "u", "qkv", "attn_out", "ffn_act", "h")
+
+
+def store(x: np.ndarray, mode="f64", cls: str = "") -> np.ndarray:
     """Round values to the storage type a drafter keeps its activations in.
 
     "f64": no rounding (the exact definition).  "fp32": round to float32.
     "bf16": round to float32, then to bfloat16 (round to nearest, ties to
     even, on the upper 16 bits) — a bf16 drafter keeps every tensor handed
     from one step to the next in bf16 while accumulating in float32.  The
-    result is returned as float64.
+    result is returned as float64.  `mode` may also map tensor classes
+    (STORE_CLASSES: the fused context H_t, the cached context K/V, the normed
+    projection inputs, block Q/K/V, the attention output, the SwiGLU product,
+    the final h) to modes, the rest staying exact: the per-tensor study.
     """
+    if isinstance(mode, dict):
+        mode = mode.get(cls, "f64")
     if mode == "f64":
         return x
     f = np.asarray(x, dtype=np.float32)
@@ -145,7 +154,7 @@ def fuse_context(feats: np.ndarray, w_c: np.ndarray, g_c: np.ndarray, eps: float
     feats = _f64(feats)
     n = feats.shape[0]
     x = feats.reshape(n, -1)                     # [n, m*D]: [H^(l1)_j ; ... ; H^(lm)_j]
-    return store(rms_norm(linear(x, w_c), g_c, eps), mode)
+    return store(rms_norm(linear(x, w_c), g_c, eps), mode, "ht")
 
 
 # ---------------------------------------------------------------------------
@@ -170,7 +179,7 @@ def inject_kv(h_t: np.ndarray, w_k: np.ndarray, w_v: np.ndarray, positions: Sequ
     if g_k is not None:
         k = rms_norm(k, g_k, eps)
     v = linear(h_t, w_v).reshape(n, n_kv_heads, head_dim)
-    return store(rope(k, positions, theta), mode), store(v, mode)
+    return store(rope(k, positions, theta), mode, "kv"), store(v, mode, "kv")
 
 
 class RequestCache:
@@ -291,23 +300,23 @@ def draft_forward(weights: Dict, cfg, cache: RequestCache, anchor: int, block: i
     pos = np.arange(c, c + block)
     mask_rows = dflash_mask(c, block)[c:, :]                       # block rows only
     for i, lw in enumerate(weights["layers"]):
-        u = store(rms_norm(x, lw["g_in"], cfg.rms_eps), mode)
+        u = store(rms_norm(x, lw["g_in"], cfg.rms_eps), mode, "u")
         q = linear(u, lw["w_q"]).reshape(block, nq, hd)
         k = linear(u, lw["w_k"]).reshape(block, nkv, hd)
         if getattr(cfg, "qk_norm", False):
             q = rms_norm(q, lw["g_q"], cfg.rms_eps)
             k = rms_norm(k, lw["g_k"], cfg.rms_eps)
-        q = store(rope(q, pos, cfg.rope_theta), mode)
-        k = store(rope(k, pos, cfg.rope_theta), mode)
-        v = store(linear(u, lw["w_v"]).reshape(block, nkv, hd), mode)
+        q = store(rope(q, pos, cfg.rope_theta), mode, "qkv")
+        k = store(rope(k, pos, cfg.rope_theta), mode, "qkv")
+        v = store(linear(u, lw["w_v"]).reshape(block, nkv, hd), mode, "qkv")
         if use_mask:
             o = attention_masked(q, np.concatenate([cache.k[i], k]), np.concatenate([cache.v[i], v]), mask_rows)
         else:
             o = attention_block(q, cache.k[i], cache.v[i], k, v)
-        x = x + linear(store(o, mode).reshape(block, nq * hd), lw["w_o"])
-        u = store(rms_norm(x, lw["g_post"], cfg.rms_eps), mode)
-        x = x + linear(store(silu(linear(u, lw["w_g"])) * linear(u, lw["w_u"]), mode), lw["w_d"])
-    h = store(rms_norm(x, weights["g_final"], cfg.rms_eps), mode)
+        x = x + linear(store(o, mode, "attn_out").reshape(block, nq * hd), lw["w_o"])
+        u = store(rms_norm(x, lw["g_post"], cfg.rms_eps), mode, "u")
+        x = x + linear(store(silu(linear(u, lw["w_g"])) * linear(u, lw["w_u"]), mode, "ffn_act"), lw["w_d"])
+    h = store(rms_norm(x, weights["g_final"], cfg.rms_eps), mode, "h")
     return {"h": h}
 
 

@@ -697,3 +697,18 @@ def test_packed_mask_follows_the_explainers_example():
     moved = oracle.attention_packed(q, kc, vc2, kb2, vb2, [r2, r3])
     np.testing.assert_allclose(moved[:g], base[:g], rtol=0, atol=0)
     assert np.max(np.abs(moved[g:] - base[g:])) > 1e-3
+
+
+def test_per_class_storage_rounding_covers_every_rounding_point():
+    """The study mode's classes partition the rounding points: every class in
+    bf16 equals the all-bf16 mode, every class exact equals the exact path."""
+    cfg, w = _tiny_setup(seed=2)
+    feats = make_features(cfg, 12, seed=3).float().numpy()
+    out = {}
+    for name, mode in [("all", "bf16"), ("each", {c: "bf16" for c in oracle.STORE_CLASSES}),
+                       ("exact", "f64"), ("none", {})]:
+        cache = oracle.RequestCache(cfg.layers, cfg.n_kv_heads, cfg.head_dim)
+        out[name] = oracle.draft_cycle(w, cfg, cache, feats, anchor=4, block=4, mode=mode)["logits"]
+    np.testing.assert_array_equal(out["each"], out["all"])
+    np.testing.assert_array_equal(out["none"], out["exact"])
+    assert np.max(np.abs(out["all"] - out["exact"])) > 0
