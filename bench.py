@@ -3,9 +3,9 @@
 
 One step = one whole draft cycle on device-resident inputs: inject the
 previous cycle's tau committed tokens (context fusion + K/V injection into
-every draft layer), draft a block (non-causal drafter pass + shared LM head
-argmax), let the synthetic target answer (seeded agreement pattern), verify
-greedily.  value = drafted tokens/s = batch * (block - 1) / cycle time, summed
+every draft layer) and draft a block (non-causal drafter pass + shared LM head
+argmax) — one dflash_draft_cycle call, one persistent launch at small batch —
+let the synthetic target answer (seeded agreement pattern), verify greedily.  value = drafted tokens/s = batch * (block - 1) / cycle time, summed
 over ranks (weak scaling: each rank drafts for its own requests; requests are
 independent, so there is no collective on the data path).
 
@@ -265,8 +265,10 @@ class Cycle:
 
     def step(self):
         df = self.df
-        df.dflash_inject_context(self.model, self.cache, self.feats, self.tau, None, self.rows, self.ws)
-        df.dflash_draft_block(self.model, self.cache, self.anchor, self.block, self.drafts, None, self.ws)
+        # inject the previous cycle's tau committed tokens, then draft: one
+        # persistent launch when both fit it, else the two calls in turn
+        df.dflash_draft_cycle(self.model, self.cache, self.feats, self.tau, self.anchor, self.block, self.drafts,
+                              None, max_rows=self.rows, workspace=self.ws)
         # the (synthetic) target's greedy tokens for this block; also adds the
         # previous cycle's accepted lengths to tau_acc
         df.dflash_synthetic_target(self.drafts, self.match, self.off, self.bonus, self.pidx, self.y,
@@ -376,7 +378,16 @@ def measure(wl, W, K, rank, world, local, barrier, want_e2e=True):
     mb = method_bytes(wl, int(round(mean_tau * wl.batch)))
     hbm, bf16, bf16_sus, src = load_peaks()
     extra = {}
-    if prof["draft_persist"][1] > 0:
+    if prof["cycle_persist"][1] > 0:
+        # one persistent launch runs the whole cycle up to the drafts: context
+        # fusion, every layer (Q/K/V also projecting the injected rows' K/V),
+        # attention over the context, the LM head
+        kern_bytes = mb["cycle"]
+        stored = sum(gb.values()) - gb["inject"] + kv_storage_bytes(wl)
+        kern_ms = prof["cycle_persist"][0] / KP
+        kern = "persist_kernel, injection + drafter pass (one launch a cycle)"
+        traffic = measured_traffic("persist", wl.name)
+    elif prof["draft_persist"][1] > 0:
         # one persistent launch runs the whole drafter pass: every layer's
         # projections and attention (context K/V read) and the LM head
         kern_bytes = mb["drafter"]
@@ -394,7 +405,8 @@ def measure(wl, W, K, rank, world, local, barrier, want_e2e=True):
         kern_ms = sum(prof[s][0] for s in GEMM_STAGES) / KP
         kern = "projection GEMMs (all launches of one cycle)"
         traffic = measured_traffic("gemm", wl.name)
-    kern_flops = sum(gf[k] for k in GEMM_STAGES) if prof["draft_persist"][1] == 0 else 0
+    persistent = prof["draft_persist"][1] > 0 or prof["cycle_persist"][1] > 0
+    kern_flops = sum(gf[k] for k in GEMM_STAGES) if not persistent else 0
     if kern_flops / (bf16_sus * 1e12) > kern_bytes / (hbm * 1e9):
         # many token rows: the projections are bound by the tensor cores; they
         # run back to back inside a long cycle, so the sustained peak applies

@@ -19,7 +19,7 @@ from ._abi import DFlashError, check, lib
 
 __all__ = ["DFlashError", "Model", "Cache", "lib", "dflash_model_create", "dflash_cache_init",
            "dflash_workspace_bytes", "dflash_workspace", "dflash_inject_context", "dflash_draft_block",
-           "dflash_verify_greedy", "dflash_get_status", "dflash_clear_status", "dflash_version",
+           "dflash_verify_greedy", "dflash_draft_cycle", "dflash_get_status", "dflash_clear_status", "dflash_version",
            "dflash_launch_count", "dflash_profile_start", "dflash_profile_stop", "dflash_inject_context_noalloc",
            "dflash_selftest_wait_timeout", "dflash_sampling_workspace", "dflash_verify_sampled", "dflash_sample_tokens",
            "BlockPolicy", "dflash_packed_attention_workspace", "dflash_packed_block_attention",
@@ -47,7 +47,8 @@ def _config_struct(cfg) -> _abi.Config:
                        head_dim=cfg.head_dim, ffn=cfg.ffn, vocab=cfg.vocab, n_target_feats=cfg.n_target_feats,
                        max_block=cfg.max_block, rope_theta=float(cfg.rope_theta), rms_eps=float(cfg.rms_eps),
                        mask_token_id=int(mask), dtype=_abi.DTYPE_F32 if cfg.dtype == "fp32" else _abi.DTYPE_BF16,
-                       qk_norm=1 if getattr(cfg, "qk_norm", False) else 0)
+                       qk_norm=1 if getattr(cfg, "qk_norm", False) else 0,
+                       input_fusion=1 if getattr(cfg, "input_fusion", False) else 0)
 
 
 def dflash_version() -> int:
@@ -213,6 +214,26 @@ def dflash_draft_block(model: Model, cache: Cache, anchor_dev: torch.Tensor, blo
     check(lib().dflash_draft_block(model.handle, cache.handle, _ptr(anchor_dev), int(block_size), _ptr(draft_dev),
                                    _ptr(logits_dev), _ptr(workspace), workspace.numel(), _stream_ptr(stream)),
           "dflash_draft_block")
+
+
+def dflash_draft_cycle(model: Model, cache: Cache, feats: torch.Tensor, n_new_dev: torch.Tensor, anchor_dev: torch.Tensor,
+                       block_size: int, draft_dev: torch.Tensor, logits_dev: Optional[torch.Tensor] = None,
+                       n_new_host=None, max_rows: Optional[int] = None, workspace: torch.Tensor = None,
+                       stream=None) -> None:
+    """Injection of feats [max_rows, m, D] (n_new_dev rows per request) then a
+    drafter pass of block_size from anchor_dev; one persistent launch when
+    both fit it."""
+    if n_new_dev.dtype != torch.int32 or anchor_dev.dtype != torch.int32 or draft_dev.dtype != torch.int32:
+        raise ValueError("n_new_dev, anchor_dev and draft_dev must be int32")
+    if feats.dtype != model.dtype:
+        raise ValueError("feats must be of the model dtype")
+    rows = feats.shape[0] if max_rows is None else int(max_rows)
+    host = None
+    if n_new_host is not None:
+        host = (ctypes.c_int32 * cache.batch)(*[int(v) for v in n_new_host])
+    check(lib().dflash_draft_cycle(model.handle, cache.handle, _ptr(feats), _ptr(n_new_dev), host, rows,
+                                   _ptr(anchor_dev), int(block_size), _ptr(draft_dev), _ptr(logits_dev),
+                                   _ptr(workspace), workspace.numel(), _stream_ptr(stream)), "dflash_draft_cycle")
 
 
 def dflash_verify_greedy(draft_dev: torch.Tensor, target_argmax_dev: torch.Tensor, accept_len_dev: torch.Tensor,

@@ -29,7 +29,7 @@ class Config(ctypes.Structure):
     _fields_ = [("hidden", c_i32), ("layers", c_i32), ("n_q_heads", c_i32), ("n_kv_heads", c_i32),
                 ("head_dim", c_i32), ("ffn", c_i32), ("vocab", c_i32), ("n_target_feats", c_i32),
                 ("max_block", c_i32), ("rope_theta", ctypes.c_float), ("rms_eps", ctypes.c_float),
-                ("mask_token_id", c_i32), ("dtype", c_i32), ("qk_norm", c_i32)]
+                ("mask_token_id", c_i32), ("dtype", c_i32), ("qk_norm", c_i32), ("input_fusion", c_i32)]
 
 
 class LayerWeights(ctypes.Structure):
@@ -68,6 +68,8 @@ SIGNATURES = {
     "dflash_workspace_bytes": (c_size, [c_ptr, c_i32, c_i32, c_i32, c_i32]),
     "dflash_inject_context": (c_i32, [c_ptr, c_ptr, c_ptr, c_ptr, c_i32p, c_i32, c_ptr, c_size, c_ptr]),
     "dflash_draft_block": (c_i32, [c_ptr, c_ptr, c_ptr, c_i32, c_ptr, c_ptr, c_ptr, c_size, c_ptr]),
+    "dflash_draft_cycle": (c_i32, [c_ptr, c_ptr, c_ptr, c_ptr, c_i32p, c_i32, c_ptr, c_i32, c_ptr, c_ptr, c_ptr, c_size,
+                                   c_ptr]),
     "dflash_noalloc_scratch_bytes": (c_size, []),
     "dflash_inject_context_noalloc": (c_i32, [c_ptr, c_ptr, c_ptr, c_ptr, c_i32p, c_i32, c_ptr]),
     "dflash_verify_greedy": (c_i32, [c_ptr, c_ptr, c_i32, c_i32, c_ptr, c_ptr, c_ptr, c_ptr]),
@@ -93,7 +95,7 @@ SIGNATURES = {
 }
 
 STAGES = ["fuse", "inject", "qkv", "attn", "o", "gateup", "down", "lmhead", "other", "inject_persist",
-          "draft_persist"]
+          "draft_persist", "cycle_persist"]
 
 
 def lib_path() -> str:

@@ -147,6 +147,9 @@ int32_t check_config(const dflash_config* c) {
   if (c->mask_token_id < 0 || c->mask_token_id >= c->vocab) return fail(DFLASH_ERR_INVALID_ARG, "mask_token_id %d out of [0, vocab)", c->mask_token_id);
   if (!(c->rope_theta > 1.0f) || !(c->rms_eps >= 0.0f)) return fail(DFLASH_ERR_INVALID_ARG, "rope_theta must be > 1 and rms_eps >= 0");
   if (c->qk_norm != 0 && c->qk_norm != 1) return fail(DFLASH_ERR_INVALID_ARG, "qk_norm %d must be 0 or 1", c->qk_norm);
+  if (c->input_fusion != 0 && c->input_fusion != 1)
+    return fail(DFLASH_ERR_INVALID_ARG, "input_fusion %d must be 0 or 1", c->input_fusion);
+  if (c->input_fusion && c->qk_norm) return fail(DFLASH_ERR_UNSUPPORTED, "input_fusion with qk_norm is not built");
   return DFLASH_OK;
 }
 
@@ -166,9 +169,13 @@ struct WsPlan {
   int counters_n;
   int attn_splits, attn_chunk;
   GemmPlan g_fuse, g_inject, g_qkv, g_o, g_gu, g_down, g_lm;
+  // input-fusion injection: context rows through the layers
+  GemmPlan gf_q, gf_kv, gf_o, gf_gu, gf_down;
+  size_t xc, uc, qc, oc, ac;
   // persistent path: sums of squares, attention chunk partials, tickets + barrier
   int persist;
-  size_t ssq, aml, tickets, qimg;
+  int fused;   // one persistent launch runs the injection and the drafter pass
+  size_t ssq, ssq2, aml, tickets, qimg;
   int ntickets, nch;
   size_t qimg_bytes;
 };
@@ -181,7 +188,7 @@ bool persist_draft_ok(const dflash_model* m, int B, int block) {
          6 * c.layers + 1 <= kPMaxPhases && c.ffn % kTileN == 0;
 }
 bool persist_inject_ok(const dflash_model* m, int max_rows) {
-  return m->persist && !m->cfg.qk_norm && max_rows <= kPRows && 1 + 2 * m->cfg.layers <= kPMaxSeg;
+  return m->persist && !m->cfg.qk_norm && !m->cfg.input_fusion && max_rows <= kPRows && 1 + 2 * m->cfg.layers <= kPMaxSeg;
 }
 
 // One call's scratch: the injection part when max_rows > 0, the drafter part
@@ -197,17 +204,23 @@ WsPlan plan_ws(const dflash_model* m, int B, int cap, int block, int max_rows) {
   WsPlan p{};
   size_t off = 0;
   auto take = [&](size_t bytes) { size_t o = off; off += align256(std::max<size_t>(bytes, 1)); return o; };
-  if ((max_rows > 0 && persist_inject_ok(m, max_rows)) || (block > 0 && persist_draft_ok(m, B, block))) {
-    // one persistent launch: activation planes padded to 16 rows, stream-K scratch per CTA
+  const bool inj_p = max_rows > 0 && persist_inject_ok(m, max_rows);
+  const bool drf_p = block > 0 && persist_draft_ok(m, B, block);
+  if ((max_rows > 0 && block > 0) ? (inj_p && drf_p) : (inj_p || drf_p)) {
+    // one persistent launch: activation planes padded to 16 rows, stream-K scratch per CTA;
+    // with both an injection and a block, one launch runs the whole cycle
     const int half = c.head_dim / 2;
     p.persist = 1;
+    p.fused = max_rows > 0 && block > 0;
     if (max_rows > 0) {
       p.ntickets = std::max(D / kTileN, c.layers * 2 * (hk / kTileN));
       p.rowinfo = take(sizeof(int2) * (size_t)max_rows);
       p.ht = take(2 * 2 * (size_t)kPRows * D);
       p.rope_c = take(sizeof(float2) * (size_t)kPRows * half);
-    } else {
-      p.ntickets = std::max({(hq + 2 * hk) / kTileN, D / kTileN, F / kTileN, (c.vocab + 255) / 256});
+      if (p.fused) p.ssq2 = take(sizeof(float) * (size_t)(D / kTileN) * kPRows);
+    }
+    if (block > 0) {
+      p.ntickets = std::max({p.ntickets, (hq + 2 * hk) / kTileN, D / kTileN, F / kTileN, (c.vocab + 255) / 256});
       const int groups = B * c.n_kv_heads;
       p.nch = std::max(1, std::min(m->sms / groups, (cap + block + 31) / 32));
       p.x = take(sizeof(float) * (size_t)kPRows * D);
@@ -236,6 +249,14 @@ WsPlan plan_ws(const dflash_model* m, int B, int cap, int block, int max_rows) {
     p.g_fuse = plan_gemm(c.dtype, max_rows, c.n_target_feats * D, D / kTileN, m->sms, m->use_tc, 1);
     p.g_inject = plan_gemm(c.dtype, max_rows, D, c.layers * 2 * (hk / kTileN), m->sms, m->use_tc, pl);
     used = {&p.g_fuse, &p.g_inject};
+    if (c.input_fusion) {
+      p.gf_q = plan_gemm(c.dtype, max_rows, D, hq / kTileN, m->sms, m->use_tc, pl);
+      p.gf_kv = plan_gemm(c.dtype, max_rows, D, 2 * (hk / kTileN), m->sms, m->use_tc, pl);
+      p.gf_o = plan_gemm(c.dtype, max_rows, hq, D / kTileN, m->sms, m->use_tc, pl);
+      p.gf_gu = plan_gemm(c.dtype, max_rows, D, F / kHalfN, m->sms, m->use_tc, pl);
+      p.gf_down = plan_gemm(c.dtype, max_rows, F, D / kTileN, m->sms, m->use_tc, pl);
+      used.insert(used.end(), {&p.gf_q, &p.gf_kv, &p.gf_o, &p.gf_gu, &p.gf_down});
+    }
   }
   if (block > 0) {
     p.g_qkv = plan_gemm(c.dtype, R, D, (hq + 2 * hk) / kTileN, m->sms, m->use_tc, pl);
@@ -256,6 +277,13 @@ WsPlan plan_ws(const dflash_model* m, int B, int cap, int block, int max_rows) {
     p.yf = take(sizeof(float) * (size_t)max_rows * D);
     p.ht = take(ea * (size_t)max_rows * D);
     p.rope_c = take(sizeof(float2) * (size_t)max_rows * (c.head_dim / 2));
+    if (c.input_fusion) {   // the context rows' residual stream and operands
+      p.xc = take(sizeof(float) * (size_t)max_rows * D);
+      p.uc = take(ea * (size_t)max_rows * D);
+      p.qc = take(sizeof(float) * (size_t)max_rows * hq);
+      p.oc = take(ea * (size_t)max_rows * hq);
+      p.ac = take(ea * (size_t)max_rows * F);
+    }
   }
   if (block > 0) {
     // attention splits: enough CTAs to cover the device twice over
@@ -326,6 +354,74 @@ void add_seg(GemmProblem& p, const void* w0, int map0, const void* w1, int map1,
   p.total_tiles += tiles;
 }
 
+// Input-fusion ablation: the injected rows' hidden states start at H_t (x_c,
+// fp32) and go through the draft layers like sequence positions; layer l's
+// K/V projection of its context rows is appended to the cache (RoPE on K at
+// each row's position), then the rows attend causally to the cache (keys up
+// to their own position) and take the layer's W_O, norm and SwiGLU FFN.  The
+// last layer needs only its K/V: its outputs feed nothing.
+template <typename T>
+int32_t run_context_layers(const dflash_model* m, dflash_cache* cache, int max_rows, char* ws, const WsPlan& P,
+                           cudaStream_t s) {
+  const dflash_config& c = m->cfg;
+  const int D = c.hidden, F = c.ffn, hq = c.n_q_heads * c.head_dim, hk = c.n_kv_heads * c.head_dim;
+  const int pl = ActPlanes<T>::n;
+  const size_t R = (size_t)max_rows;
+  int2* rowinfo = reinterpret_cast<int2*>(ws + P.rowinfo);
+  const float2* rope_c = reinterpret_cast<const float2*>(ws + P.rope_c);
+  float* xc = reinterpret_cast<float*>(ws + P.xc);
+  T* uc = reinterpret_cast<T*>(ws + P.uc);
+  float* qc = reinterpret_cast<float*>(ws + P.qc);
+  T* oc = reinterpret_cast<T*>(ws + P.oc);
+  T* ac = reinterpret_cast<T*>(ws + P.ac);
+  float* partial = reinterpret_cast<float*>(ws + P.partial);
+  int* counters = reinterpret_cast<int*>(ws + P.counters);
+  T* kc = reinterpret_cast<T*>(cache->base + cache->k_off);
+  T* vc = reinterpret_cast<T*>(cache->base + cache->v_off);
+  for (int l = 0; l < c.layers; ++l) {
+    const dflash_layer_weights& L = m->layers[l];
+    DF_LAUNCH(DFLASH_STAGE_OTHER, 1,
+              rmsnorm_launch<T>(xc, static_cast<const T*>(L.g_in), c.rms_eps, max_rows, D, uc, R * D, s),
+              "context input norm");
+    GemmProblem pkv = make_problem(m, uc, D, max_rows, D, pl, R * D);
+    add_seg(pkv, L.w_k, layer_map(l, kMapK), L.w_k, layer_map(l, kMapK), hk / kTileN, 0, 2 * l);
+    add_seg(pkv, L.w_v, layer_map(l, kMapV), L.w_v, layer_map(l, kMapV), hk / kTileN, 0, 2 * l + 1);
+    apply_plan(pkv, P.gf_kv, partial, counters);
+    EpiInject<T> ei{kc, vc, rowinfo, rope_c, c.layers, c.n_kv_heads, c.head_dim, cache->cap, pad8(cache->cap)};
+    DF_LAUNCH(DFLASH_STAGE_INJECT, 1, (gemm_launch<T, EpiInject<T>>(pkv, P.gf_kv, ei, s)), "context K/V GEMM");
+    if (l + 1 == c.layers) break;
+    GemmProblem pq = make_problem(m, uc, D, max_rows, D, pl, R * D);
+    add_seg(pq, L.w_q, layer_map(l, kMapQ), L.w_q, layer_map(l, kMapQ), hq / kTileN, 0, 0);
+    apply_plan(pq, P.gf_q, partial, counters);
+    DF_LAUNCH(DFLASH_STAGE_INJECT, 1,
+              (gemm_launch<T, EpiRowsRope>(pq, P.gf_q, EpiRowsRope{qc, hq, rope_c, c.head_dim}, s)),
+              "context Q GEMM");
+    DF_LAUNCH(DFLASH_STAGE_ATTN, 1,
+              ctx_attention_launch<T>(qc, kc, vc, rowinfo, max_rows, l, c.layers, c.n_q_heads, c.n_kv_heads,
+                                      c.head_dim, cache->cap, pad8(cache->cap), 1.0f / sqrtf((float)c.head_dim), oc,
+                                      R * hq, s),
+              "context attention");
+    GemmProblem po = make_problem(m, oc, hq, max_rows, hq, pl, R * hq);
+    add_seg(po, L.w_o, layer_map(l, kMapO), L.w_o, layer_map(l, kMapO), D / kTileN, 0, 0);
+    apply_plan(po, P.gf_o, partial, counters);
+    DF_LAUNCH(DFLASH_STAGE_INJECT, 1, (gemm_launch<T, EpiResidual>(po, P.gf_o, EpiResidual{xc, D}, s)), "context O GEMM");
+    DF_LAUNCH(DFLASH_STAGE_OTHER, 1,
+              rmsnorm_launch<T>(xc, static_cast<const T*>(L.g_post), c.rms_eps, max_rows, D, uc, R * D, s),
+              "context post-attention norm");
+    GemmProblem pg = make_problem(m, uc, D, max_rows, D, pl, R * D);
+    add_seg(pg, L.w_g, layer_map(l, kMapG), L.w_u, layer_map(l, kMapU), F / kHalfN, 1, 0);
+    apply_plan(pg, P.gf_gu, partial, counters);
+    DF_LAUNCH(DFLASH_STAGE_INJECT, 1,
+              (gemm_launch<T, EpiSwiGLU<T>>(pg, P.gf_gu, EpiSwiGLU<T>{ac, F, R * F}, s)), "context gate/up GEMM");
+    GemmProblem pd = make_problem(m, ac, F, max_rows, F, pl, R * F);
+    add_seg(pd, L.w_d, layer_map(l, kMapD), L.w_d, layer_map(l, kMapD), D / kTileN, 0, 0);
+    apply_plan(pd, P.gf_down, partial, counters);
+    DF_LAUNCH(DFLASH_STAGE_INJECT, 1, (gemm_launch<T, EpiResidual>(pd, P.gf_down, EpiResidual{xc, D}, s)),
+              "context down GEMM");
+  }
+  return DFLASH_OK;
+}
+
 template <typename T>
 int32_t run_inject(const dflash_model* m, dflash_cache* cache, const void* feats, const int32_t* n_new, int max_rows,
                    char* ws, const WsPlan& P, cudaStream_t s) {
@@ -349,8 +445,10 @@ int32_t run_inject(const dflash_model* m, dflash_cache* cache, const void* feats
   DF_LAUNCH(DFLASH_STAGE_OTHER, 1,
             fuse_norm_launch<T>(yf, static_cast<const T*>(m->g_c), c.rms_eps, rowinfo, max_rows, D, ht,
                                 (size_t)max_rows * D, m->inv_freq_dev, c.head_dim,
-                                reinterpret_cast<float2*>(ws + P.rope_c), s),
+                                reinterpret_cast<float2*>(ws + P.rope_c), s,
+                                c.input_fusion ? reinterpret_cast<float*>(ws + P.xc) : nullptr),
             "fusion norm");
+  if (c.input_fusion) return run_context_layers<T>(m, cache, max_rows, ws, P, s);
 
   GemmProblem pi = make_problem(m, ht, D, max_rows, D, pl, (size_t)max_rows * D);
   for (int l = 0; l < c.layers; ++l) {
@@ -492,6 +590,12 @@ struct PhaseBuilder {
     ph.layer = -1;
     ph.gain = static_cast<const __nv_bfloat16*>(gain);
     ph.seg0 = nseg_total();
+    ph.mrows = p.M;
+    ph.xmap2 = -1;
+    ph.ssq_in = p.ssq;
+    ph.ssq_in2 = nullptr;
+    ph.u_out = p.u;
+    ph.ssq_out = p.ssq;
     return p.nphase - 1;
   }
   void add_other(int kind, int layer) {
@@ -529,7 +633,7 @@ struct PhaseBuilder {
   void finish() {
     for (int i = 0; i < p.nphase; ++i) {
       PPhase& ph = p.ph[i];
-      if (ph.kind != kPhGemm || ph.kb % 2) continue;
+      if (ph.kind != kPhGemm || ph.kb % 2 || ph.xmap2 >= 0) continue;   // two row groups fill a 64-column stage
       bool narrow = true;
       for (int j = ph.seg0; j < ph.seg0 + ph.nseg; ++j) narrow = narrow && p.seg[j].tw == 128;
       if (narrow) {
@@ -587,12 +691,28 @@ int32_t run_inject_persist(const dflash_model* m, dflash_cache* cache, const voi
   return DFLASH_OK;
 }
 
+// The drafter pass as one persistent launch.  With inj_rows > 0 (a plan with
+// P.fused) the same launch first runs the injection of those rows: a fusion
+// phase (W_c) writes H_t's planes, and each layer's Q/K/V phase carries the
+// injected rows as a second row group, so that W_K and W_V are read once for
+// the block's keys and values and for the context's.
 int32_t run_draft_persist(const dflash_model* m, const dflash_cache* cache, const int32_t* anchor, int block,
-                          int32_t* drafts, float* logits, char* ws, const WsPlan& P, cudaStream_t s) {
+                          int32_t* drafts, float* logits, char* ws, const WsPlan& P, cudaStream_t s,
+                          const void* feats = nullptr, const int32_t* n_new = nullptr, int inj_rows = 0) {
   const dflash_config& c = m->cfg;
   const int B = cache->batch, D = c.hidden, F = c.ffn;
   const int hq = c.n_q_heads * c.head_dim, hk = c.n_kv_heads * c.head_dim;
   const int R = B * block;
+  const bool fused = inj_rows > 0;
+  const int F5 = c.n_target_feats * D;
+  if (fused) {   // the injection's row map, ctx_len update and RoPE table come first
+    DF_LAUNCH(DFLASH_STAGE_OTHER, 1,
+              inject_prep_launch(n_new, reinterpret_cast<int32_t*>(cache->base + cache->len_off), B, inj_rows,
+                                 cache->cap, reinterpret_cast<int2*>(ws + P.rowinfo),
+                                 reinterpret_cast<int*>(ws + P.tickets), P.ntickets + 1, m->status_dev, s,
+                                 m->inv_freq_dev, c.head_dim, reinterpret_cast<float2*>(ws + P.rope_c)),
+              "inject_prep");
+  }
   float* x = reinterpret_cast<float*>(ws + P.x);
   __nv_bfloat16* u = reinterpret_cast<__nv_bfloat16*>(ws + P.u);
   __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(ws + P.o);
@@ -614,6 +734,10 @@ int32_t run_draft_persist(const dflash_model* m, const dflash_cache* cache, cons
       !encode_activation_map(&pp.xmap[1], o, hq, 2 * kPRows, hq, kPRows) ||
       !encode_activation_map(&pp.xmap[2], a, F, 2 * kPRows, F, kPRows))
     return fail(DFLASH_ERR_CUDA, "could not encode activation tensor maps");
+  __nv_bfloat16* ht = fused ? reinterpret_cast<__nv_bfloat16*>(ws + P.ht) : nullptr;
+  if (fused && (!encode_activation_map(&pp.xmap[3], feats, F5, inj_rows, F5, kPRows) ||
+                !encode_activation_map(&pp.xmap[4], ht, D, 2 * kPRows, D, kPRows)))
+    return fail(DFLASH_ERR_INVALID_ARG, "could not encode activation tensor maps (16-B aligned features needed)");
   pp.wmaps = static_cast<const CUtensorMap*>(m->tmaps128_dev);
   pp.M = R;
   pp.D = D;
@@ -662,14 +786,37 @@ int32_t run_draft_persist(const dflash_model* m, const dflash_cache* cache, cons
   ap.scale = att_scale;
   ap.qimg = qimg;
   if (!encode_attention_maps(&pp.amaps, ap.kc, ap.vc, kb, vb, B, c.layers, c.n_kv_heads, c.head_dim, cache->cap,
-                             pad8(cache->cap), block, pad8(block)))
+                             pad8(cache->cap), block, pad8(block)) ||
+      !encode_activation_map(&pp.amaps.qm, qimg, c.head_dim, B * c.n_kv_heads * 128, c.head_dim, 128))
     return fail(DFLASH_ERR_CUDA, "could not encode attention tensor maps");
+
+  float* ssq_ht = fused ? reinterpret_cast<float*>(ws + P.ssq2) : nullptr;
+  if (fused) {
+    pp.M2 = inj_rows;
+    pp.inject = EpiInject<__nv_bfloat16>{reinterpret_cast<__nv_bfloat16*>(cache->base + cache->k_off),
+                                         reinterpret_cast<__nv_bfloat16*>(cache->base + cache->v_off),
+                                         reinterpret_cast<const int2*>(ws + P.rowinfo),
+                                         reinterpret_cast<const float2*>(ws + P.rope_c), c.layers, c.n_kv_heads,
+                                         c.head_dim, cache->cap, pad8(cache->cap)};
+  }
 
   PhaseBuilder pb{pp};
   if (const char* w = debug_env("DFLASH_PERSIST_WIDE")) pb.all_wide = std::strcmp(w, "1") == 0;
+  if (fused) {   // context fusion: H_t planes * g_c and their sums of squares
+    const int ph = pb.add_gemm(kEpFuse, F5, 3, 1, 0, 0, m->g_c);
+    pp.ph[ph].mrows = inj_rows;
+    pp.ph[ph].u_out = ht;
+    pp.ph[ph].ssq_out = ssq_ht;
+    pb.seg(kMapWc, kMapWc, D, 0, 0);
+  }
   for (int l = 0; l < c.layers; ++l) {
     const dflash_layer_weights& L = m->layers[l];
-    pb.add_gemm(kEpQKV, D, 0, 2, kPRows, 1, nullptr);
+    const int qph = pb.add_gemm(fused ? kEpQKVInj : kEpQKV, D, 0, 2, kPRows, 1, nullptr);
+    if (fused) {   // the injected rows (H_t planes) as the second row group
+      pp.ph[qph].xmap2 = 4;
+      pp.ph[qph].ssq_in2 = ssq_ht;
+      pp.ph[qph].layer = l;
+    }
     pb.seg(layer_map(l, kMapQ), layer_map(l, kMapQ), hq, 0, 0);
     pb.seg(layer_map(l, kMapK), layer_map(l, kMapK), hk, 0, 1);
     pb.seg(layer_map(l, kMapV), layer_map(l, kMapV), hk, 0, 2);
@@ -688,7 +835,10 @@ int32_t run_draft_persist(const dflash_model* m, const dflash_cache* cache, cons
   }
   pb.finish();
   pp.trace = m->trace_persist ? m->trace_dev : nullptr;
-  DF_LAUNCH(DFLASH_STAGE_DRAFT_PERSIST, 1, persist_launch(pp, m->sms, c.head_dim, s), "persistent drafter");
+  if (fused)
+    DF_LAUNCH(DFLASH_STAGE_CYCLE_PERSIST, 1, persist_launch(pp, m->sms, c.head_dim, s), "persistent cycle");
+  else
+    DF_LAUNCH(DFLASH_STAGE_DRAFT_PERSIST, 1, persist_launch(pp, m->sms, c.head_dim, s), "persistent drafter");
   return DFLASH_OK;
 }
 
@@ -922,7 +1072,11 @@ size_t dflash_workspace_bytes(const dflash_model* m, int32_t batch, int32_t capa
   size_t need = plan_ws(m, batch, capacity, 0, max_inject_rows).total;
   if (max_inject_rows > 0)
     need = std::max(need, plan_ws(m, batch, capacity, 0, std::min(max_inject_rows, kPRows)).total);
-  for (int b = 1; b <= block_size; ++b) need = std::max(need, plan_ws(m, batch, capacity, b, 0).total);
+  for (int b = 1; b <= block_size; ++b) {
+    need = std::max(need, plan_ws(m, batch, capacity, b, 0).total);
+    // dflash_draft_cycle: injection and drafter pass in one launch
+    if (max_inject_rows > 0) need = std::max(need, plan_ws(m, batch, capacity, b, std::min(max_inject_rows, kPRows)).total);
+  }
   return need;
 }
 
@@ -985,6 +1139,51 @@ int32_t dflash_draft_block(const dflash_model* m, const dflash_cache* cache, con
              ? run_draft<float>(m, cache, anchor_dev, block_size, draft_dev, logits_dev, static_cast<char*>(workspace), P, s)
              : run_draft<__nv_bfloat16>(m, cache, anchor_dev, block_size, draft_dev, logits_dev,
                                         static_cast<char*>(workspace), P, s);
+}
+
+int32_t dflash_draft_cycle(const dflash_model* m, dflash_cache* cache, const void* feats, const int32_t* n_new_dev,
+                           const int32_t* n_new_host, int32_t max_rows, const int32_t* anchor_dev, int32_t block_size,
+                           int32_t* draft_dev, float* logits_dev, void* workspace, size_t ws_bytes,
+                           dflash_stream_t stream) {
+  if (!m || !cache) return fail(DFLASH_ERR_INVALID_ARG, "model or cache is NULL");
+  if (cache->model != m) return fail(DFLASH_ERR_INVALID_ARG, "cache was made for another model");
+  if (max_rows < 0) return fail(DFLASH_ERR_INVALID_ARG, "max_rows %d < 0", max_rows);
+  if (!n_new_dev) return fail(DFLASH_ERR_INVALID_ARG, "n_new_dev is NULL");
+  if (block_size < 1 || block_size > m->cfg.max_block)
+    return fail(DFLASH_ERR_SHAPE, "block_size %d outside [1, %d]", block_size, m->cfg.max_block);
+  if (!anchor_dev || !workspace || (max_rows > 0 && !feats))
+    return fail(DFLASH_ERR_INVALID_ARG, "anchor_dev, feats or workspace is NULL");
+  if (block_size > 1 && !draft_dev) return fail(DFLASH_ERR_INVALID_ARG, "draft_dev is NULL");
+  int32_t rc = check_device(m);
+  if (rc) return rc;
+  const WsPlan P = plan_ws(m, cache->batch, cache->cap, block_size, max_rows);
+  if (max_rows == 0 || !P.fused) {   // the two calls one after the other
+    rc = dflash_inject_context(m, cache, feats, n_new_dev, n_new_host, max_rows, workspace, ws_bytes, stream);
+    if (rc) return rc;
+    return dflash_draft_block(m, cache, anchor_dev, block_size, draft_dev, logits_dev, workspace, ws_bytes, stream);
+  }
+  if (n_new_host) {
+    long total = 0;
+    for (int b = 0; b < cache->batch; ++b) {
+      if (n_new_host[b] < 0) return fail(DFLASH_ERR_INVALID_ARG, "n_new[%d] = %d < 0", b, n_new_host[b]);
+      total += n_new_host[b];
+      if (cache->len_known && cache->len_host[b] + (long)n_new_host[b] > cache->cap)
+        return fail(DFLASH_ERR_CAPACITY, "request %d: %d + %d tokens exceed capacity %d", b, cache->len_host[b],
+                    n_new_host[b], cache->cap);
+    }
+    if (total > max_rows) return fail(DFLASH_ERR_SHAPE, "sum of n_new (%ld) > max_rows (%d)", total, max_rows);
+  }
+  if (ws_bytes < P.total) return fail(DFLASH_ERR_WORKSPACE, "workspace %zu bytes < %zu needed", ws_bytes, P.total);
+  rc = run_draft_persist(m, cache, anchor_dev, block_size, draft_dev, logits_dev, static_cast<char*>(workspace), P,
+                         (cudaStream_t)stream, feats, n_new_dev, max_rows);
+  if (rc) return rc;
+  if (n_new_host) {
+    if (cache->len_known)
+      for (int b = 0; b < cache->batch; ++b) cache->len_host[b] += n_new_host[b];
+  } else {
+    cache->len_known = false;
+  }
+  return DFLASH_OK;
 }
 
 int32_t dflash_verify_greedy(const int32_t* draft_dev, const int32_t* target_argmax_dev, int32_t batch,

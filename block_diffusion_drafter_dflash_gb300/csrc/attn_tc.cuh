@@ -47,9 +47,11 @@ constexpr float kNegInf = -1.0e30f;
 constexpr float kLazy = 8.0f;              // raise the running max only beyond this margin
 constexpr long long kBudget = 200000000LL;
 
-// Tensor maps of one launch: K cache, V cache (hd-major), block K, block V (hd-major).
+// Tensor maps of one launch: K cache, V cache (hd-major), block K, block V
+// (hd-major), and (with AttnParams::qimg) the prepared query operands
+// [groups * 128 A rows][hd] bf16, 64 x 128 boxes.
 struct Maps {
-  CUtensorMap kc, vc, kb, vb;
+  CUtensorMap kc, vc, kb, vb, qm;
 };
 
 // Shared memory (1024-byte aligned base): Q A-tile per 64 columns of hd;
@@ -232,12 +234,14 @@ __device__ bool run(const AttnParams& p, const Maps& m, int b, int kvh, int pass
   // only after the softmax, and the Q loads need not queue behind it)
   if (p.qimg) {
     if (tid == 0) {
-      // the image was written by other CTAs through the generic proxy
+      // the operand rows were written by other CTAs through the generic proxy;
+      // TMA swizzles them into the A tiles (one 128-row box per 64 columns)
       ptx::fence_proxy_async_global();
       ptx::mbar_arrive_expect_tx(&bars->qfull, C::kQ);
       const int passes = (rows + 63) / 64;
-      ptx::bulk_load(sm, reinterpret_cast<const uint8_t*>(p.qimg) + ((size_t)(b * p.nkv + kvh) * passes + pass) * C::kQ,
-                     C::kQ, &bars->qfull);
+      const int row0 = ((b * p.nkv + kvh) * passes + pass) * 128;
+      for (int s = 0; s < C::kSub; ++s)
+        ptx::tma_load_2d(sm + s * kTile16, &m.qm, &bars->qfull, 64 * s, row0, ptx::policy_evict_first());
     }
     if (tid == 0 && t0 < t1) load_k<HD>(p, m, b, kvh, t0, nct, sm, bars);
     ok = ptx::mbar_wait(&bars->qfull, static_cast<uint32_t>(qload) & 1u, kBudget, status);

@@ -18,7 +18,7 @@ ROOT = os.path.dirname(PKG)
 LIB_NAME = "libdflash_gb300.so"
 SOURCES = ["api.cu", "gemm.cu", "gemm_tc.cu", "attention.cu", "attention_tc.cu", "elementwise.cu", "persist.cu",
            "sampling.cu", "block_policy.cpp",
-           "packed_attention.cu"]
+           "packed_attention.cu", "ctx_attention.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
          "-I" + os.path.join(ROOT, "include")]

@@ -42,9 +42,11 @@ __device__ __forceinline__ float row_sumsq(const RowRegs& r, int nv) {
 
 // u = x * rsqrt(mean(x^2) + eps) * g for a row held in registers; u is a GEMM
 // activation operand (planes `plane` elements apart).
+// With `xf`, the normed row is also stored in fp32 (a residual stream that
+// starts at the normed value: the context rows of the input-fusion path).
 template <typename T>
 __device__ __forceinline__ void norm_store(const RowRegs& r, const T* g, float eps, int D, T* u, size_t plane,
-                                           float* red) {
+                                           float* red, float* xf = nullptr) {
   const int nv = D >> 2;
   const float rs = rsqrtf(block_sum(row_sumsq(r, nv), red) / (float)D + eps);
 #pragma unroll
@@ -53,7 +55,9 @@ __device__ __forceinline__ void norm_store(const RowRegs& r, const T* g, float e
     if (idx < nv) {
       const float4 gg = load4(g + 4 * idx);
       const float4 x = r.v[i];
-      put_act4(u, plane, 4 * (size_t)idx, make_float4(x.x * rs * gg.x, x.y * rs * gg.y, x.z * rs * gg.z, x.w * rs * gg.w));
+      const float4 o = make_float4(x.x * rs * gg.x, x.y * rs * gg.y, x.z * rs * gg.z, x.w * rs * gg.w);
+      put_act4(u, plane, 4 * (size_t)idx, o);
+      if (xf) *reinterpret_cast<float4*>(xf + 4 * (size_t)idx) = o;
     }
   }
 }
@@ -131,7 +135,8 @@ __global__ void __launch_bounds__(kRowThreads) final_norm_kernel(const float* x,
 template <typename T>
 __global__ void __launch_bounds__(kRowThreads) fuse_norm_kernel(const float* y, const T* g, float eps,
                                                                 const int2* rowinfo, int D, T* ht, size_t plane,
-                                                                const double* inv_freq, int hd, float2* rope) {
+                                                                const double* inv_freq, int hd, float2* rope,
+                                                                float* xf) {
   __shared__ float red[32];
   griddep_wait();
   griddep_trigger();
@@ -145,13 +150,15 @@ __global__ void __launch_bounds__(kRowThreads) fuse_norm_kernel(const float* y, 
     }
   }
   if (rowinfo[row].x < 0) {
-    for (int i = threadIdx.x; i < (D >> 2); i += blockDim.x)
+    for (int i = threadIdx.x; i < (D >> 2); i += blockDim.x) {
       put_act4(ht, plane, (size_t)row * D + 4 * i, make_float4(0.f, 0.f, 0.f, 0.f));
+      if (xf) *reinterpret_cast<float4*>(xf + (size_t)row * D + 4 * i) = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
     return;
   }
   RowRegs r;
   load_row(y + (size_t)row * D, D, r);
-  norm_store(r, g, eps, D, ht + (size_t)row * D, plane, red);
+  norm_store(r, g, eps, D, ht + (size_t)row * D, plane, red, xf ? xf + (size_t)row * D : nullptr);
 }
 
 // One CTA: exclusive scan of n_new, per-row (request, position), ctx_len
@@ -432,10 +439,10 @@ cudaError_t final_norm_launch(const float* x, const T* g, float eps, int B, int 
 
 template <typename T>
 cudaError_t fuse_norm_launch(const float* y, const T* g, float eps, const int2* rowinfo, int rows, int D, T* ht,
-                             size_t plane, const double* inv_freq, int hd, float2* rope, cudaStream_t s) {
+                             size_t plane, const double* inv_freq, int hd, float2* rope, cudaStream_t s, float* xf) {
   if (rows == 0) return cudaSuccess;
   return launch_pdl(fuse_norm_kernel<T>, dim3(rows), dim3(kRowThreads), 0, s, y, g, eps, rowinfo, D, ht, plane,
-                    inv_freq, hd, rope);
+                    inv_freq, hd, rope, xf);
 }
 
 cudaError_t inject_prep_launch(const int32_t* n_new, int32_t* ctx_len, int B, int max_rows, int cap, int2* rowinfo,
@@ -466,7 +473,7 @@ cudaError_t verify_launch(const int32_t* draft, const int32_t* target, int B, in
   template cudaError_t final_norm_launch<T>(const float*, const T*, float, int, int, int, T*, size_t,              \
                                             unsigned long long*, cudaStream_t);                                   \
   template cudaError_t fuse_norm_launch<T>(const float*, const T*, float, const int2*, int, int, T*, size_t,      \
-                                           const double*, int, float2*, cudaStream_t);                            \
+                                           const double*, int, float2*, cudaStream_t, float*);                    \
   template cudaError_t qknorm_block_launch<T>(float*, T*, const T*, const T*, int, int, int, int, int, float,      \
                                               const float2*, cudaStream_t);                                       \
   template cudaError_t qknorm_cache_launch<T>(T*, const int2*, int, int, int, int, int, int, const T*, float,      \

@@ -91,12 +91,13 @@ struct EpiQKV {
   const float2* rope;
   int block, nq, nkv, hd;
   int vpitch;
-  // Optional: the queries written instead as the block attention's A-operand
-  // image of each (request, kv head) group — row i = (head - kvh*G)*block + k
-  // of the group's 64 query rows, value q * qscale (log2-domain scores) as a
-  // bf16 hi part and lo residual (A rows 32(i/16) + i%16 and +16), 64-column
-  // subtiles of 128 rows x 128 bytes with the 128-byte swizzle — so that the
-  // attention loads it with one bulk copy.  Rows past G*block stay zero.
+  // Optional: the queries written instead as the block attention's A operand
+  // of each (request, kv head) group, row-major bf16 [128 A rows][hd]: query
+  // row i = (head - kvh*G)*block + k of the group's 64, value q * qscale
+  // (log2-domain scores) as a bf16 hi part in A row 32(i/16) + i%16 and its lo
+  // residual 16 rows further — so that the attention loads it with TMA, which
+  // applies the 128-byte swizzle.  Consecutive threads store consecutive
+  // columns.  Rows past G*block stay zero.
   __nv_bfloat16* qimg;
   float qscale;
   int G;
@@ -157,12 +158,9 @@ struct EpiQKV {
           const float x = r * qscale;
           const __nv_bfloat16 hi = __float2bfloat16_rn(x);
           const __nv_bfloat16 lo = __float2bfloat16_rn(x - __bfloat162float(hi));
-          const int ch = (d & 63) >> 3;
-          const int rh = 32 * (i >> 4) + (i & 15), rl = rh + 16;
-          uint8_t* img = reinterpret_cast<uint8_t*>(qimg) + ((size_t)(b * nkv + kvh) * (hd >> 6) + (d >> 6)) * 16384 +
-                         2 * (d & 7);
-          *reinterpret_cast<__nv_bfloat16*>(img + rh * 128 + ((ch ^ (rh & 7)) << 4)) = hi;
-          *reinterpret_cast<__nv_bfloat16*>(img + rl * 128 + ((ch ^ (rl & 7)) << 4)) = lo;
+          __nv_bfloat16* img = qimg + ((size_t)(b * nkv + kvh) * 128 + 32 * (i >> 4) + (i & 15)) * hd + d;
+          img[0] = hi;
+          img[(size_t)16 * hd] = lo;
         } else if (tag == 0)
           q[(((size_t)b * nh + head) * block + k) * hd + d] = r;
         else
@@ -238,6 +236,28 @@ struct EpiInject {
         put_act(dst, (size_t)cap * hd,
                 ((((size_t)ri[j].x * layers + layer) * nkv + head) * planes * cap + ri[j].y) * hd + d, r);
       }
+    }
+  }
+};
+
+// Query projection of injected context rows (input-fusion path): y[row][f]
+// fp32 with RoPE at the row's position (rope[row][hd/2], as filled with the
+// injection's row map); rows keep the injection's packed order.
+struct EpiRowsRope {
+  float* y;
+  int ldy;
+  const float2* rope;
+  int hd;
+  __device__ __forceinline__ void operator()(const float* t, int ld, int m0, int mc, int gtile, const GemmSeg&,
+                                             int, int tid, int nth) const {
+    const int n = tid & (kTileN - 1), step = nth / kTileN, half = hd >> 1;
+    const int feat = gtile * kTileN + n, d = feat & (hd - 1);
+    const int i = d < half ? d : d - half;
+    const int pn = d < half ? n + half : n - half;
+    for (int m = tid / kTileN; m < mc; m += step) {
+      const float2 sc = __ldg(rope + (size_t)(m0 + m) * half + i);
+      const float v = t[n * ld + m], pv = t[pn * ld + m];
+      y[(size_t)(m0 + m) * ldy + feat] = d < half ? v * sc.x - pv * sc.y : v * sc.x + pv * sc.y;
     }
   }
 };

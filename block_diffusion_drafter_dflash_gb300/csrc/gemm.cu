@@ -154,7 +154,9 @@ cudaError_t gemm_launch(const GemmProblem& p, const GemmPlan& plan, const Epi& e
   template cudaError_t gemm_launch<T, EpiInject<T>>(const GemmProblem&, const GemmPlan&,                 \
                                                     const EpiInject<T>&, cudaStream_t);                 \
   template cudaError_t gemm_launch<T, EpiArgmax>(const GemmProblem&, const GemmPlan&, const EpiArgmax&,  \
-                                                 cudaStream_t);
+                                                 cudaStream_t);                                         \
+  template cudaError_t gemm_launch<T, EpiRowsRope>(const GemmProblem&, const GemmPlan&, const EpiRowsRope&, \
+                                                   cudaStream_t);
 
 DFLASH_GEMM_INST(float)
 DFLASH_GEMM_INST(__nv_bfloat16)

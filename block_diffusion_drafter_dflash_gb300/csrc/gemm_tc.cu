@@ -696,5 +696,6 @@ template cudaError_t gemm_tc_launch<EpiQKV<__nv_bfloat16>>(const GemmProblem&, c
 template cudaError_t gemm_tc_launch<EpiInject<__nv_bfloat16>>(const GemmProblem&, const GemmPlan&,
                                                               const EpiInject<__nv_bfloat16>&, cudaStream_t);
 template cudaError_t gemm_tc_launch<EpiArgmax>(const GemmProblem&, const GemmPlan&, const EpiArgmax&, cudaStream_t);
+template cudaError_t gemm_tc_launch<EpiRowsRope>(const GemmProblem&, const GemmPlan&, const EpiRowsRope&, cudaStream_t);
 
 }  // namespace dflash

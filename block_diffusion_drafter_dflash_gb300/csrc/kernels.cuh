@@ -74,10 +74,20 @@ cudaError_t final_norm_launch(const float* x, const T* g, float eps, int B, int 
                               unsigned long long* slots, cudaStream_t s);
 
 // H_t[row] = RMSNorm(y[row]) * g_c for rows with rowinfo[row].x >= 0, 0 otherwise;
-// rope[row][hd/2] = (cos, sin) of the row's position.
+// rope[row][hd/2] = (cos, sin) of the row's position; with xf, H_t also in fp32.
 template <typename T>
 cudaError_t fuse_norm_launch(const float* y, const T* g, float eps, const int2* rowinfo, int rows, int D, T* ht,
-                             size_t plane, const double* inv_freq, int hd, float2* rope, cudaStream_t s);
+                             size_t plane, const double* inv_freq, int hd, float2* rope, cudaStream_t s,
+                             float* xf = nullptr);
+
+// Input-fusion context rows: causal attention of each injected row (request,
+// position p) over its request's cached keys 0..p of layer `layer`; q fp32
+// [rows][nq*hd] (RoPE applied), output the W_O GEMM operand [rows][nq*hd]
+// (planes `out_plane` apart; zero for padding rows).
+template <typename T>
+cudaError_t ctx_attention_launch(const float* q, const T* kc, const T* vc, const int2* rowinfo, int rows, int layer,
+                                 int layers, int nq, int nkv, int hd, int cap, int vpitch, float scale, T* out,
+                                 size_t out_plane, cudaStream_t s);
 
 // QK-norm models: per-head RMSNorm (gain g [hd], epsilon eps) then RoPE, in
 // place, of the block queries q (fp32 [B][nq][block][hd]) and block keys kb

@@ -103,6 +103,7 @@ struct PBook {
   uint64_t ring_free;   // attention is done with the ring (one phase per attention phase)
   attn_tc::Bars abars;  // the attention's TMA and MMA barriers
   float rs[kPRows];
+  float rs2[kPRows];    // 1/rms of the second row group (injected rows of a fused cycle)
 };
 
 static_assert(kStage % 1024 == 0 && kXBytes % 1024 == 0, "stages keep the 1024-byte swizzle alignment");
@@ -300,11 +301,19 @@ __device__ void activation_producer(const PParams& p, PBook* bk, uint8_t* ring, 
       if (it >= S && !wait_timed(&bk->empty[s], ((it / S) & 1) ^ 1, p.status, wx, true)) goto done;
       const int kx = (i % ph.kb) * ph.kw, halves = ph.kw / 64;
       uint8_t* x = ring + (size_t)s * kStage;
-      ptx::mbar_arrive_expect_tx(&bk->fullX[s], halves * ph.planes * kPRows * 128);
-      for (int hh = 0; hh < halves; ++hh)
-        for (int pl = 0; pl < ph.planes; ++pl)
-          ptx::tma_load_2d(x + hh * kXHalf + pl * kPRows * 128, &p.xmap[ph.xmap], &bk->fullX[s], kx + 64 * hh,
-                           pl * ph.prow, pol);
+      if (ph.xmap2 >= 0) {   // two row groups of two planes: B rows 0..31 and 32..63 (64 K columns a stage)
+        ptx::mbar_arrive_expect_tx(&bk->fullX[s], 4 * kPRows * 128);
+        for (int pl = 0; pl < 2; ++pl) {
+          ptx::tma_load_2d(x + pl * kPRows * 128, &p.xmap[ph.xmap], &bk->fullX[s], kx, pl * ph.prow, pol);
+          ptx::tma_load_2d(x + (2 + pl) * kPRows * 128, &p.xmap[ph.xmap2], &bk->fullX[s], kx, pl * ph.prow, pol);
+        }
+      } else {
+        ptx::mbar_arrive_expect_tx(&bk->fullX[s], halves * ph.planes * kPRows * 128);
+        for (int hh = 0; hh < halves; ++hh)
+          for (int pl = 0; pl < ph.planes; ++pl)
+            ptx::tma_load_2d(x + hh * kXHalf + pl * kPRows * 128, &p.xmap[ph.xmap], &bk->fullX[s], kx + 64 * hh,
+                             pl * ph.prow, pol);
+      }
     }
     trace_val(p, cta, pi, kTrWaitXEmpty, wx);
   }
@@ -324,7 +333,8 @@ __device__ void mma_issuer(const PParams& p, PBook* bk, uint8_t* ring, uint32_t 
     for (int i = sp.i0; i < sp.i1;) {
       const int t = i / ph.kb, k0 = i - t * ph.kb, k1 = min(sp.i1 - t * ph.kb, ph.kb);
       const bool wide = p.seg[seg_of(p, ph, t)].tw == kTwMax;   // weights on N
-      const uint32_t idesc = wide ? ptx::idesc_bf16_f32(128, kTwMax) : ptx::idesc_bf16_f32(128, kPRows * ph.planes);
+      const int bcols = kPRows * (ph.planes + (ph.xmap2 >= 0 ? 2 : 0));   // token columns (weights on M)
+      const uint32_t idesc = wide ? ptx::idesc_bf16_f32(128, kTwMax) : ptx::idesc_bf16_f32(128, bcols);
       const int buf = seq & 1, use = seq >> 1;
       if (use >= 1 && !ptx::mbar_wait(&bk->accfree[buf], (use - 1) & 1, kBudget, p.status)) goto done;
       ptx::tc_fence_after();
@@ -374,7 +384,7 @@ done:
 __device__ __forceinline__ void load_resid(const PParams& p, const PPhase& ph, int f0, int ct, float* v) {
   const bool resid = ph.epi == kEpResid;
 #pragma unroll
-  for (int m = 0; m < kPRows; ++m) v[m] = (m < p.M && resid) ? __ldcg(p.x + (size_t)m * p.D + f0 + ct) : 0.f;
+  for (int m = 0; m < kPRows; ++m) v[m] = (m < ph.mrows && resid) ? __ldcg(p.x + (size_t)m * p.D + f0 + ct) : 0.f;
 }
 
 // `xr`: kPRows residual values of load_resid followed by the gain of feature
@@ -392,30 +402,30 @@ __device__ void epi_norm_out(const PParams& p, const PPhase& ph, int f0, float* 
   }
 #pragma unroll
   for (int m = 0; m < kPRows; ++m) {
-    if (m >= p.M) break;
+    if (m >= ph.mrows) break;
     const float o = v[m] + st[ct * kLd + m];
     if (resid) p.x[(size_t)m * p.D + f] = o;
-    put_act(p.u, p.u_plane, (size_t)m * p.D + f, o * g);
+    put_act(ph.u_out, p.u_plane, (size_t)m * p.D + f, o * g);
     st[ct * kLd + m] = o * o;
   }
   csync();
   // row m = ct / 8 sums features ct%8, ct%8 + 8, ... then across the 8 lanes
   const int m = ct >> 3, part = ct & 7;
   float a = 0.f;
-  if (m < p.M)
+  if (m < ph.mrows)
     for (int n = part; n < 128; n += 8) a += st[n * kLd + m];
   a += __shfl_xor_sync(0xffffffffu, a, 1);
   a += __shfl_xor_sync(0xffffffffu, a, 2);
   a += __shfl_xor_sync(0xffffffffu, a, 4);
-  if (part == 0 && m < p.M) p.ssq[(f0 / 128) * kPRows + m] = a;
+  if (part == 0 && m < ph.mrows) ph.ssq_out[(f0 / 128) * kPRows + m] = a;
   csync();
 }
 
 // silu(gate) * up for a paired tile (features 0..127 gate, 128..255 up) into
 // the W_D GEMM's activation planes.
-__device__ void epi_swiglu(const PParams& p, int tis, const float* st, int ct) {
+__device__ void epi_swiglu(const PParams& p, const PPhase& ph, int tis, const float* st, int ct) {
   const EpiSwiGLU<__nv_bfloat16>& e = p.swiglu;
-  for (int idx = ct; idx < p.M * 128; idx += 128) {
+  for (int idx = ct; idx < ph.mrows * 128; idx += 128) {
     const int m = idx >> 7, c = idx & 127;
     const float g = st[c * kLd + m], u = st[(128 + c) * kLd + m];
     put_act(e.a, e.plane, (size_t)m * e.lda + (size_t)tis * 128 + c, g / (1.0f + __expf(-g)) * u);
@@ -424,10 +434,10 @@ __device__ void epi_swiglu(const PParams& p, int tis, const float* st, int ct) {
 
 // Argmax of the tile's logits (features f0 .. f0+tw-1 below the vocabulary)
 // for every mask row (block position >= 1) into slots[row]; optional logits.
-__device__ void epi_lm(const PParams& p, int f0, int tw, const float* st, int ct) {
+__device__ void epi_lm(const PParams& p, const PPhase& ph, int f0, int tw, const float* st, int ct) {
   const int lane = ct & 31, w = ct >> 5;
   const int nv = min(tw, p.vocab - f0);
-  for (int m = w; m < p.M; m += 4) {
+  for (int m = w; m < ph.mrows; m += 4) {
     if (m % p.block == 0) continue;
     unsigned long long best = 0ull;
     for (int n = lane; n < nv; n += 32) {
@@ -441,7 +451,7 @@ __device__ void epi_lm(const PParams& p, int f0, int tw, const float* st, int ct
     if (lane == 0) atomicMax(p.slots + m, best);
   }
   if (p.logits) {
-    for (int idx = ct; idx < p.M * tw; idx += 128) {
+    for (int idx = ct; idx < ph.mrows * tw; idx += 128) {
       const int m = idx / tw, n = idx - m * tw;
       const int b = m / p.block, k = m - b * p.block;
       if (k == 0 || n >= nv) continue;
@@ -462,18 +472,22 @@ struct PieceMap {
 };
 
 template <int TW>
-__device__ __forceinline__ void publish_tw(const PParams& p, const float* st, float* dst, int ct) {
+__device__ __forceinline__ void publish_tw(int rows, const float* st, float* dst, int ct) {
   using PM = PieceMap<TW>;
   const int fq = 4 * (ct % PM::kQ), r0 = ct / PM::kQ;
-  for (int m = r0; m < p.M; m += PM::kStep)
+  for (int m = r0; m < rows; m += PM::kStep)
     *reinterpret_cast<float4*>(dst + m * kTwMax + fq) =
         make_float4(st[fq * kLd + m], st[(fq + 1) * kLd + m], st[(fq + 2) * kLd + m], st[(fq + 3) * kLd + m]);
 }
-__device__ __forceinline__ void publish_piece(const PParams& p, int tw, const float* st, float* dst, int ct) {
+// Rows a stream-K piece of phase ph carries: its row group, or both groups.
+__device__ __forceinline__ int piece_rows(const PParams& p, const PPhase& ph) {
+  return ph.xmap2 >= 0 ? max(ph.mrows, p.M2) : ph.mrows;
+}
+__device__ __forceinline__ void publish_piece(int rows, int tw, const float* st, float* dst, int ct) {
   if (tw == kTwMax)
-    publish_tw<kTwMax>(p, st, dst, ct);
+    publish_tw<kTwMax>(rows, st, dst, ct);
   else
-    publish_tw<128>(p, st, dst, ct);
+    publish_tw<128>(rows, st, dst, ct);
 }
 
 // Add the pieces of tile t from CTAs cf+1..cl (in CTA order) to the reducer's
@@ -485,11 +499,12 @@ __device__ void add_pieces(const PParams& p, const PPhase& ph, int G, int t, int
   const int fq = 4 * (ct % PM::kQ), r0 = ct / PM::kQ;
   const int W = phase_iters(ph);
   const int g = phase_ctas(ph, G);
+  const int rows = piece_rows(p, ph);
   float4 acc[PM::kR];
 #pragma unroll
   for (int j = 0; j < PM::kR; ++j) {
     const int m = r0 + PM::kStep * j;
-    acc[j] = m < p.M ? make_float4(st[fq * kLd + m], st[(fq + 1) * kLd + m], st[(fq + 2) * kLd + m],
+    acc[j] = m < rows ? make_float4(st[fq * kLd + m], st[(fq + 1) * kLd + m], st[(fq + 2) * kLd + m],
                                    st[(fq + 3) * kLd + m])
                      : make_float4(0.f, 0.f, 0.f, 0.f);
   }
@@ -503,7 +518,7 @@ __device__ void add_pieces(const PParams& p, const PPhase& ph, int G, int t, int
 #pragma unroll
       for (int j = 0; j < PM::kR; ++j) {
         const int m = r0 + PM::kStep * j;
-        a[u][j] = (c + u <= cl && m < p.M) ? __ldcg(reinterpret_cast<const float4*>(src + m * kTwMax))
+        a[u][j] = (c + u <= cl && m < rows) ? __ldcg(reinterpret_cast<const float4*>(src + m * kTwMax))
                                            : make_float4(0.f, 0.f, 0.f, 0.f);
       }
     }
@@ -520,7 +535,7 @@ __device__ void add_pieces(const PParams& p, const PPhase& ph, int G, int t, int
 #pragma unroll
   for (int j = 0; j < PM::kR; ++j) {
     const int m = r0 + PM::kStep * j;
-    if (m < p.M) {
+    if (m < rows) {
       st[fq * kLd + m] = acc[j].x;
       st[(fq + 1) * kLd + m] = acc[j].y;
       st[(fq + 2) * kLd + m] = acc[j].z;
@@ -558,13 +573,21 @@ __device__ void run_epilogue(const PParams& p, const PPhase& ph, int t, float* s
         epi_norm_out(p, ph, tis * sg.tw + h * 128, st + h * 128 * kLd, ct, h == 0 ? xr : nullptr);
       break;
     case kEpQKV:
-      for (int h = 0; h < halves; ++h) p.qkv(st + h * 128 * kLd, kLd, 0, p.M, 0, sg, tis * halves + h, ct, 128);
+      for (int h = 0; h < halves; ++h) p.qkv(st + h * 128 * kLd, kLd, 0, ph.mrows, 0, sg, tis * halves + h, ct, 128);
+      break;
+    case kEpQKVInj:   // 128-feature tiles; the injected rows' values staged as features 128..255
+      p.qkv(st, kLd, 0, ph.mrows, 0, sg, tis, ct, 128);
+      if (sg.tag > 0) {   // K (tag 1) or V (tag 2) of layer ph.layer: context K/V into the cache
+        GemmSeg si = sg;
+        si.tag = 2 * ph.layer + (sg.tag - 1);
+        p.inject(st + 128 * kLd, kLd, 0, p.M2, 0, si, tis, ct, 128);
+      }
       break;
     case kEpInject:
-      for (int h = 0; h < halves; ++h) p.inject(st + h * 128 * kLd, kLd, 0, p.M, 0, sg, tis * halves + h, ct, 128);
+      for (int h = 0; h < halves; ++h) p.inject(st + h * 128 * kLd, kLd, 0, ph.mrows, 0, sg, tis * halves + h, ct, 128);
       break;
-    case kEpSwiGLU: epi_swiglu(p, tis, st, ct); break;
-    default: epi_lm(p, tis * sg.tw, sg.tw, st, ct); break;
+    case kEpSwiGLU: epi_swiglu(p, ph, tis, st, ct); break;
+    default: epi_lm(p, ph, tis * sg.tw, sg.tw, st, ct); break;
   }
 }
 
@@ -573,13 +596,19 @@ __device__ bool gemm_phase(const PParams& p, const PPhase& ph, int pi, PBook* bk
                            int cta, int ct, int& seq) {
   if (ph.scaled) {
     const int m = ct >> 3, part = ct & 7, nt = p.D / 128;
-    float a = 0.f;
-    if (m < p.M)
-      for (int t = part; t < nt; t += 8) a += __ldcg(p.ssq + t * kPRows + m);
-    a += __shfl_xor_sync(0xffffffffu, a, 1);
-    a += __shfl_xor_sync(0xffffffffu, a, 2);
-    a += __shfl_xor_sync(0xffffffffu, a, 4);
-    if (part == 0) bk->rs[m] = m < p.M ? rsqrtf(a / (float)p.D + p.eps) : 0.f;
+    float a = 0.f, a2 = 0.f;
+    if (m < ph.mrows)
+      for (int t = part; t < nt; t += 8) a += __ldcg(ph.ssq_in + t * kPRows + m);
+    if (ph.xmap2 >= 0 && m < p.M2)
+      for (int t = part; t < nt; t += 8) a2 += __ldcg(ph.ssq_in2 + t * kPRows + m);
+    for (int o = 1; o < 8; o <<= 1) {
+      a += __shfl_xor_sync(0xffffffffu, a, o);
+      a2 += __shfl_xor_sync(0xffffffffu, a2, o);
+    }
+    if (part == 0) {
+      bk->rs[m] = m < ph.mrows ? rsqrtf(a / (float)p.D + p.eps) : 0.f;
+      bk->rs2[m] = (ph.xmap2 >= 0 && m < p.M2) ? rsqrtf(a2 / (float)p.D + p.eps) : 0.f;
+    }
   }
   csync();
   const Span sp = cta_span(ph, G, cta);
@@ -600,7 +629,7 @@ __device__ bool gemm_phase(const PParams& p, const PPhase& ph, int pi, PBook* bk
       // weights on N: token rows in TMEM lanes 0..15 (hi) and 16..31 (lo), warp 4
       if (ct < 32) {
         ptx::tc_fence_after();
-        const float sc = (ct < p.M && ph.scaled) ? bk->rs[ct] : 1.f;
+        const float sc = (ct < ph.mrows && ph.scaled) ? bk->rs[ct] : 1.f;
         for (int c0 = 0; c0 < kTwMax; c0 += 64) {
           float v[64];
           ptx::tmem_ld32x2(tb + c0, tb + c0 + 32, v);
@@ -608,7 +637,7 @@ __device__ bool gemm_phase(const PParams& p, const PPhase& ph, int pi, PBook* bk
 #pragma unroll
             for (int j = 0; j < 64; ++j) v[j] += __shfl_xor_sync(0xffffffffu, v[j], 16);
           }
-          if (ct < p.M) {
+          if (ct < ph.mrows) {
 #pragma unroll
             for (int j = 0; j < 64; ++j) st[(c0 + j) * kLd + ct] = v[j] * sc;
           }
@@ -631,6 +660,13 @@ __device__ bool gemm_phase(const PParams& p, const PPhase& ph, int pi, PBook* bk
 #pragma unroll
         for (int m = 0; m < kPRows; ++m) v[m] += w[m];
       }
+      if (ph.xmap2 >= 0) {   // the second row group: token columns 32..47 (hi) and 48..63 (lo), staged
+        float h[kPRows], w[kPRows];   // as features 128..255 of the tile
+        ptx::tmem_ld16(ta + 2 * kPRows, h);
+        ptx::tmem_ld16(ta + 3 * kPRows, w);
+#pragma unroll
+        for (int m = 0; m < kPRows; ++m) st[(128 + ct) * kLd + m] = (h[m] + w[m]) * bk->rs2[m];
+      }
       ptx::tc_fence_before();
 #pragma unroll
       for (int m = 0; m < kPRows; ++m) st[ct * kLd + m] = ph.scaled ? v[m] * bk->rs[m] : v[m];
@@ -651,7 +687,8 @@ __device__ bool gemm_phase(const PParams& p, const PPhase& ph, int pi, PBook* bk
     if (cta != cf) {
       // a piece for the tile's reducer: publish it and announce it (release);
       // nothing here waits for the reduction
-      publish_piece(p, tw, st, p.partial + (size_t)(cta * 2 + (t == first_tile ? 0 : 1)) * (kPRows * kTwMax), ct);
+      publish_piece(piece_rows(p, ph), ph.xmap2 >= 0 ? kTwMax : tw, st,
+                    p.partial + (size_t)(cta * 2 + (t == first_tile ? 0 : 1)) * (kPRows * kTwMax), ct);
       __threadfence();
       csync();
       if (ct == 0) {
@@ -684,7 +721,7 @@ __device__ bool gemm_phase(const PParams& p, const PPhase& ph, int pi, PBook* bk
     }
     csync();
     if (!bk->flag_tk) return false;
-    if (sg.tw == kTwMax)
+    if (sg.tw == kTwMax || ph.xmap2 >= 0)
       add_pieces<kTwMax>(p, ph, G, t, cf, cl, st, ct);
     else
       add_pieces<128>(p, ph, G, t, cf, cl, st, ct);

@@ -14,7 +14,7 @@ namespace dflash {
 constexpr int kPRows = 16;         // token rows one launch serves (one MMA column block per plane)
 constexpr int kPMaxPhases = 56;    // 6 per draft layer + the LM head, up to 9 layers
 constexpr int kPMaxSeg = 64;
-constexpr int kPXMaps = 4;
+constexpr int kPXMaps = 6;
 constexpr int kPAttnRows = 64;     // query rows of one (request, kv head) group: 4 warps x 16
 constexpr int kPMaxStages = 10;
 
@@ -26,7 +26,9 @@ enum : int {
   kEpQKV,        // block Q/K/V (EpiQKV), scaled by 1/rms
   kEpResid,      // x += acc: planes of x * gain, per-tile sums of x^2 (W_O, W_D)
   kEpSwiGLU,     // silu(gate) * up (EpiSwiGLU), scaled by 1/rms
-  kEpLM          // argmax (and optional logits) of the mask rows, scaled by 1/rms
+  kEpLM,         // argmax (and optional logits) of the mask rows, scaled by 1/rms
+  kEpQKVInj      // block Q/K/V of the first row group and, for the K and V tiles, the
+                 // context K/V of the second group (injected rows) into the cache
 };
 
 struct PPhase {
@@ -39,8 +41,14 @@ struct PPhase {
   int planes;      // activation planes (1: exact bf16 input, 2: hi/lo pair)
   int prow;        // map rows from plane 0 to plane 1
   int scaled;      // multiply the accumulator of row m by 1/rms(row m) before the epilogue
-  int layer;       // draft layer of an attention phase
+  int layer;       // draft layer of an attention phase or of a kEpQKVInj phase
   const __nv_bfloat16* gain;  // kEpFuse / kEpResid: gain of the RMSNorm that reads the planes written
+  int mrows;       // token rows of the phase's (first) row group
+  int xmap2;       // -1, or the map of a second 16-row group (2 planes) after the first: B rows 32..63
+  const float* ssq_in;        // scaled phases: sums of squares of the first group's normed input
+  const float* ssq_in2;       // ... and of the second group's
+  __nv_bfloat16* u_out;       // kEpFuse / kEpResid: planes written ([2][16][D], u_plane apart)
+  float* ssq_out;             // kEpFuse / kEpResid: their per-tile sums of squares [D/128][16]
 };
 
 struct PParams {
@@ -48,13 +56,14 @@ struct PParams {
   const CUtensorMap* wmaps;    // weight maps of the model (device memory)
   int nphase;
   int M;                       // token rows (<= 16)
+  int M2;                      // rows of a second group (the injected rows of a fused cycle), or 0
   int D;                       // hidden size (RMSNorm width)
   float eps;
   int stages;                  // ring depth
   float* x;                    // residual stream [M][D] fp32 (nullptr when no phase keeps one)
-  __nv_bfloat16* u;            // planes written by kEpFuse / kEpResid: [2][16][D]
-  size_t u_plane;
-  float* ssq;                  // [D/128][16] sums of squares of the last normed input
+  __nv_bfloat16* u;            // default planes of kEpFuse / kEpResid: [2][16][D]
+  size_t u_plane;              // elements between the hi and lo planes of u (and of every u_out)
+  float* ssq;                  // default [D/128][16] sums of squares of the last normed input
   float* partial;              // [grid][2][16][128] stream-K partial tiles
   int* tickets;                // [largest tile count] stream-K tickets, zero at launch
   unsigned int* bar;           // grid barrier counter, zero at launch (follows tickets)

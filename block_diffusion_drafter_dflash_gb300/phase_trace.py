@@ -1,10 +1,11 @@
-"""Phase timeline of the persistent drafter launch (a diagnostic).
+"""Phase timeline of the persistent cycle launch (a diagnostic).
 
-Runs a few draft cycles of a bf16 workload whose calls have at most 16 token
-rows with DFLASH_TRACE_PERSIST=1, so that every persistent launch records
-per-CTA globaltimer stamps, reads the stamps of the last drafter launch and
-prints one line per phase: when its first CTA started it, the median and the
-latest CTA's last MMA issue, and the median and the latest CTA's end.
+Runs a few draft cycles (dflash_draft_cycle: injection and drafter pass in one
+launch) of a bf16 workload whose calls have at most 16 token rows with
+DFLASH_TRACE_PERSIST=1, so that every persistent drafter launch records
+per-CTA globaltimer stamps, reads the stamps of the last one and prints one
+line per phase: when its first CTA started it, the median and the latest
+CTA's last MMA issue, and the median and the latest CTA's end.
 
     python -m block_diffusion_drafter_dflash_gb300.phase_trace [workload] [--raw out.npy]
 """
@@ -21,8 +22,10 @@ GRID_MAX, PHASES, SLOTS = 512, 56, 18           # the kernel's trace layout [cta
 START, DONE, MMA_LAST = 0, 1, 6                  # slots used here
 
 
-def phase_names(layers: int, lm_head: bool = True) -> List[str]:
-    names = []
+def phase_names(layers: int, lm_head: bool = True, fusion: bool = False) -> List[str]:
+    """Phases of a persistent drafter launch; `fusion`: the launch of a whole
+    cycle (dflash_draft_cycle), which starts with the context fusion."""
+    names = ["fusion"] if fusion else []
     for l in range(layers):
         names += [f"L{l} qkv", f"L{l} attn", f"L{l} merge", f"L{l} o", f"L{l} gateup", f"L{l} down"]
     return names + (["lmhead"] if lm_head else [])
@@ -84,16 +87,15 @@ def run(workload: str = "8b_bs1", cycles: int = 4):
     tau = torch.full((B,), wl.first_inject, dtype=torch.int32, device="cuda")
     anchor = make_tokens(cfg, B, seed=wl.seed + 3, device="cuda")
     drafts = torch.empty((B, block - 1), dtype=torch.int32, device="cuda")
-    for _ in range(cycles):
-        df.dflash_inject_context(model, cache, new, tau, None, B * block, ws)
-        df.dflash_draft_block(model, cache, anchor, block, drafts, None, ws)
+    for _ in range(cycles):   # the benchmark's cycle: injection and drafter pass in one launch
+        df.dflash_draft_cycle(model, cache, new, tau, anchor, block, drafts, None, max_rows=B * block, workspace=ws)
     torch.cuda.synchronize()
     n = GRID_MAX * PHASES * SLOTS
     buf = (ctypes.c_uint64 * n)()
     df.check(df.lib().dflash_trace_read(model.handle, buf, n), "dflash_trace_read")
     t = np.frombuffer(buf, dtype=np.uint64).reshape(GRID_MAX, PHASES, SLOTS)
     t = t[: torch.cuda.get_device_properties(0).multi_processor_count]
-    return t, phase_names(cfg.layers)
+    return t, phase_names(cfg.layers, fusion=True)
 
 
 def main(argv: List[str]) -> None:

@@ -39,6 +39,7 @@ class DraftConfig:
     max_block: int = 32    # largest block_size the drafter is asked for
     mask_token_id: Optional[int] = None   # defaults to vocab - 1
     qk_norm: bool = False  # per-head RMSNorm of queries and keys before RoPE (Qwen3's q_norm / k_norm)
+    input_fusion: bool = False  # ablation: the fused context enters once, at the input, instead of every layer's K/V
 
     @property
     def mask_id(self) -> int:

@@ -86,6 +86,12 @@ typedef struct {
                              RMS-normalised over head_dim and scaled by the layer's g_q / g_k
                              before RoPE (Qwen3's q_norm / k_norm; not on the pages, off in their
                              configuration).  Models with it run the multi-kernel path. */
+  int32_t input_fusion;   /* 0, or 1: the ablation of paper §5.5.5 — the fused context enters once, as
+                             the context positions' input hidden states, and every draft layer
+                             processes those positions (causal among the context) to produce its own
+                             context K/V, instead of projecting H_t straight into every layer's K/V.
+                             Changes dflash_inject_context only (multi-kernel path); drafting is the
+                             same.  Not combined with qk_norm. */
 } dflash_config;
 
 /* Device pointers of one draft layer (borrowed).  Shapes with
@@ -247,6 +253,23 @@ int32_t dflash_inject_context_noalloc(const dflash_model* model, dflash_cache* c
 int32_t dflash_draft_block(const dflash_model* model, const dflash_cache* cache, const int32_t* anchor_dev,
                            int32_t block_size, int32_t* draft_dev, float* logits_dev, void* workspace,
                            size_t workspace_bytes, dflash_stream_t stream);
+
+/* --- stages 1-4 in one call ---------------------------------------------------
+ * dflash_inject_context(feats, n_new, max_rows) followed by
+ * dflash_draft_block(anchor, block_size): the cycle of the explainer's
+ * "Putting It Together" from the committed tokens' features to the drafts,
+ * with the same arguments, checks and results (up to the order of fp32
+ * additions).  When both fit one persistent launch (bf16 model without
+ * qk_norm or input_fusion, max_rows <= 16, batch * block_size <= 16) they run
+ * as ONE launch: the fusion projection first, then every layer's Q/K/V
+ * projection computes the block's queries, keys and values and the injected
+ * rows' context keys and values from one read of W_K and W_V.  Otherwise the
+ * two calls run one after the other.  The workspace must hold
+ * dflash_workspace_bytes(model, batch, capacity, block_size, max_rows). */
+int32_t dflash_draft_cycle(const dflash_model* model, dflash_cache* cache, const void* feats,
+                           const int32_t* n_new_dev, const int32_t* n_new_host, int32_t max_rows,
+                           const int32_t* anchor_dev, int32_t block_size, int32_t* draft_dev, float* logits_dev,
+                           void* workspace, size_t workspace_bytes, dflash_stream_t stream);
 
 /* --- stage 5: greedy lossless verification -----------------------------------
  * Explainer, "The Target Verifier Remains the Correctness Anchor": accept drafts
@@ -441,7 +464,8 @@ int32_t dflash_trace_read(const dflash_model* model, uint64_t* host, size_t n);
 #define DFLASH_STAGE_OTHER 8    /* embedding, norms, row maps, argmax read-out */
 #define DFLASH_STAGE_INJECT_PERSIST 9  /* one-launch injection (fusion + K/V), <= 16 rows */
 #define DFLASH_STAGE_DRAFT_PERSIST 10  /* one-launch drafter pass (layers + LM head), <= 16 rows */
-#define DFLASH_NUM_STAGES 11
+#define DFLASH_STAGE_CYCLE_PERSIST 11  /* one-launch injection + drafter pass (dflash_draft_cycle) */
+#define DFLASH_NUM_STAGES 12
 
 /* Start recording a CUDA event pair around each launch the model's entry
  * points make (up to max_launches launches), on the stream each call is given.

@@ -199,7 +199,10 @@ class RequestCache:
 def inject_context(weights: Dict, cfg, cache: RequestCache, feats: np.ndarray, mode: str = "f64") -> np.ndarray:
     """Stages 1+2 for one request: fuse the new tokens' target features and
     append their K/V to every layer of the cache.  Returns H_t.  `mode` is the
-    storage rounding of H_t and of the cached K/V (see `store`)."""
+    storage rounding of H_t and of the cached K/V (see `store`).  With
+    cfg.input_fusion the ablation path inject_context_input_fusion runs."""
+    if getattr(cfg, "input_fusion", False):
+        return inject_context_input_fusion(weights, cfg, cache, feats)
     h_t = fuse_context(feats, weights["w_c"], weights["g_c"], cfg.rms_eps, mode)
     c = cache.length
     pos = np.arange(c, c + h_t.shape[0])
@@ -209,6 +212,42 @@ def inject_context(weights: Dict, cfg, cache: RequestCache, feats: np.ndarray, m
                          g_k=lw["g_k"] if qk else None, eps=cfg.rms_eps)
         cache.k[i] = np.concatenate([cache.k[i], k], axis=0)
         cache.v[i] = np.concatenate([cache.v[i], v], axis=0)
+    return h_t
+
+
+def inject_context_input_fusion(weights: Dict, cfg, cache: RequestCache, feats: np.ndarray) -> np.ndarray:
+    """The input-fusion ablation (paper §5.5.5, against KV injection; explainer
+    "Per-Layer K/V Injection Prevents Context Dilution": with input fusion the
+    target context enters only at the first layer).  Reading: the new context
+    tokens' layer-0 hidden states are H_t itself (no extra weights), and every
+    draft layer processes them like sequence positions, causally among the
+    context (the DFlash mask's context rows, j <= i); layer i's context keys
+    and values are that layer's own projections of its context hidden states.
+    Earlier context rows never see later ones, so the per-layer K/V of the
+    context can be cached and extended: this function appends the new rows'
+    K/V of every layer to the cache.  Drafting is unchanged (draft_forward).
+    draft_forward_full_sequence is the same computation without a cache."""
+    h_t = fuse_context(feats, weights["w_c"], weights["g_c"], cfg.rms_eps)
+    D, nq, nkv, hd = cfg.hidden, cfg.n_q_heads, cfg.n_kv_heads, cfg.head_dim
+    c, n = cache.length, h_t.shape[0]
+    pos = np.arange(c, c + n)
+    rows = dflash_mask(c + n, 0)[c:, :]                          # causal context rows over keys 0..c+n-1
+    x = h_t.copy()
+    for i, lw in enumerate(weights["layers"]):
+        u = rms_norm(x, lw["g_in"], cfg.rms_eps)
+        q = linear(u, lw["w_q"]).reshape(n, nq, hd)
+        k = linear(u, lw["w_k"]).reshape(n, nkv, hd)
+        if getattr(cfg, "qk_norm", False):
+            q = rms_norm(q, lw["g_q"], cfg.rms_eps)
+            k = rms_norm(k, lw["g_k"], cfg.rms_eps)
+        q, k = rope(q, pos, cfg.rope_theta), rope(k, pos, cfg.rope_theta)
+        v = linear(u, lw["w_v"]).reshape(n, nkv, hd)
+        cache.k[i] = np.concatenate([cache.k[i], k], axis=0)
+        cache.v[i] = np.concatenate([cache.v[i], v], axis=0)
+        o = attention_masked(q, cache.k[i], cache.v[i], rows)
+        x = x + linear(o.reshape(n, nq * hd), lw["w_o"])
+        u = rms_norm(x, lw["g_post"], cfg.rms_eps)
+        x = x + linear(silu(linear(u, lw["w_g"])) * linear(u, lw["w_u"]), lw["w_d"])
     return h_t
 
 
@@ -318,6 +357,36 @@ def draft_forward(weights: Dict, cfg, cache: RequestCache, anchor: int, block: i
         x = x + linear(store(silu(linear(u, lw["w_g"])) * linear(u, lw["w_u"]), mode, "ffn_act"), lw["w_d"])
     h = store(rms_norm(x, weights["g_final"], cfg.rms_eps), mode, "h")
     return {"h": h}
+
+
+def draft_forward_full_sequence(weights: Dict, cfg, ctx_feats: np.ndarray, anchor: int, block: int) -> Dict:
+    """The input-fusion drafter written out over the whole sequence, with no
+    cache: x = [H_t of every context token ; E[anchor, mask, ..]]; every layer
+    processes every position under the full DFlash mask (context rows causal,
+    block rows see all context and the whole block); h = RMSNorm_final of the
+    block rows.  Equal to inject_context_input_fusion + draft_forward."""
+    D, nq, nkv, hd = cfg.hidden, cfg.n_q_heads, cfg.n_kv_heads, cfg.head_dim
+    h_t = fuse_context(ctx_feats, weights["w_c"], weights["g_c"], cfg.rms_eps)
+    c = h_t.shape[0]
+    tokens = [int(anchor)] + [cfg.mask_id] * (block - 1)
+    x = np.concatenate([h_t, _f64(weights["embed"][tokens])], axis=0)
+    n = c + block
+    pos = np.arange(n)
+    M = dflash_mask(c, block)
+    for lw in weights["layers"]:
+        u = rms_norm(x, lw["g_in"], cfg.rms_eps)
+        q = linear(u, lw["w_q"]).reshape(n, nq, hd)
+        k = linear(u, lw["w_k"]).reshape(n, nkv, hd)
+        if getattr(cfg, "qk_norm", False):
+            q = rms_norm(q, lw["g_q"], cfg.rms_eps)
+            k = rms_norm(k, lw["g_k"], cfg.rms_eps)
+        q, k = rope(q, pos, cfg.rope_theta), rope(k, pos, cfg.rope_theta)
+        v = linear(u, lw["w_v"]).reshape(n, nkv, hd)
+        o = attention_masked(q, k, v, M)
+        x = x + linear(o.reshape(n, nq * hd), lw["w_o"])
+        u = rms_norm(x, lw["g_post"], cfg.rms_eps)
+        x = x + linear(silu(linear(u, lw["w_g"])) * linear(u, lw["w_u"]), lw["w_d"])
+    return {"h": rms_norm(x[c:], weights["g_final"], cfg.rms_eps)}
 
 
 # ---------------------------------------------------------------------------

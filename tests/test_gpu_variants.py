@@ -10,7 +10,11 @@ regression bar, drafts identical wherever the oracle's top-2 margin exceeds
 * 8 draft layers (the paper's Qwen3-Coder drafter depth), 8B-shaped: batch 1
   runs the persistent one-launch path (6 x 8 + 1 phases), batch 2 the
   multi-kernel path.
-* 3 target features instead of 5 (W_c 12288 -> 4096), 8B-shaped, both paths."""
+* 3 target features instead of 5 (W_c 12288 -> 4096), 8B-shaped, both paths.
+* Input fusion instead of per-layer KV injection (paper §5.5.5): the injected
+  context rows run through every draft layer (causal among the context) and
+  each layer caches its own context K/V; tiny drafter in fp32 and bf16 and
+  4B-shaped bf16, a setup injection and then per-cycle injections."""
 import pytest
 import torch
 
@@ -75,3 +79,15 @@ def test_eight_layer_drafter_8b_shaped(B):
 def test_three_target_features_8b_shaped(B):
     cfg = replace(QWEN3_8B, name="qwen3-8b-shaped-3-features", n_target_feats=3)
     _cycle(cfg, B=B, ctx=384, block=16, seed=530 + B, cycles=1)
+
+
+@pytest.mark.parametrize("dtype", ["fp32", "bf16"])
+def test_input_fusion_tiny(dtype):
+    cfg = replace(TINY, name=f"tiny-input-fusion-{dtype}", dtype=dtype, input_fusion=True)
+    _cycle(cfg, B=2, ctx=64, block=4, seed=540)
+
+
+@pytest.mark.parametrize("B", [1, 3])
+def test_input_fusion_4b_shaped(B):
+    cfg = replace(QWEN3_4B, name="qwen3-4b-shaped-input-fusion", input_fusion=True)
+    _cycle(cfg, B=B, ctx=256, block=16, seed=550 + B, cycles=2)

@@ -712,3 +712,60 @@ def test_per_class_storage_rounding_covers_every_rounding_point():
     np.testing.assert_array_equal(out["each"], out["all"])
     np.testing.assert_array_equal(out["none"], out["exact"])
     assert np.max(np.abs(out["all"] - out["exact"])) > 0
+
+
+# ---------------------------------------------------------------- input-fusion ablation
+def test_input_fusion_cached_form_equals_the_full_sequence_definition():
+    """Injecting the context through the layers once (cached per-layer K/V,
+    extended incrementally) and then drafting equals running every layer over
+    the whole [context ; block] sequence under the DFlash mask."""
+    cfg = replace(TINY, layers=2, input_fusion=True)
+    w = oracle.weights_to_numpy(make_weights(cfg, 5))
+    feats = make_features(cfg, 23, seed=6).float().numpy()
+    cache = oracle.RequestCache(cfg.layers, cfg.n_kv_heads, cfg.head_dim)
+    for s0, s1 in [(0, 9), (9, 10), (10, 23)]:                  # three injections
+        oracle.inject_context(w, cfg, cache, feats[s0:s1])
+    r = oracle.draft_cycle(w, cfg, cache, None, anchor=7, block=5)
+    full = oracle.draft_forward_full_sequence(w, cfg, feats, anchor=7, block=5)
+    logits_full, _ = oracle.lm_head_argmax(full["h"][1:], w["lm_head"])
+    np.testing.assert_allclose(r["logits"], logits_full, rtol=1e-10, atol=1e-12)
+
+
+def test_input_fusion_with_zero_output_projections_gives_the_injected_cache():
+    """Special case linking the two conditioning modes: with W_O = W_D = 0 the
+    context hidden states stay H_t through every layer, so layer i's context
+    keys and values are W^K_i, W^V_i applied to RMSNorm(H_t) — KV injection's
+    cache up to the norm's epsilon (exact with eps = 0, H_t having unit RMS)."""
+    base = replace(TINY, layers=2, rms_eps=0.0)
+    w = oracle.weights_to_numpy(make_weights(base, 8))
+    w0 = dict(w, layers=[dict(lw, w_o=np.zeros_like(lw["w_o"]), w_d=np.zeros_like(lw["w_d"])) for lw in w["layers"]])
+    feats = make_features(base, 11, seed=9).float().numpy()
+    caches = []
+    for cfg in (base, replace(base, input_fusion=True)):
+        cache = oracle.RequestCache(cfg.layers, cfg.n_kv_heads, cfg.head_dim)
+        oracle.inject_context(w0, cfg, cache, feats)
+        caches.append(cache)
+    for i in range(base.layers):
+        np.testing.assert_allclose(caches[1].k[i], caches[0].k[i], rtol=1e-11, atol=1e-12)
+        np.testing.assert_allclose(caches[1].v[i], caches[0].v[i], rtol=1e-11, atol=1e-12)
+    # and with the projections on, the two modes differ (the ablation is not a no-op)
+    c2 = oracle.RequestCache(base.layers, base.n_kv_heads, base.head_dim)
+    oracle.inject_context(w, replace(base, input_fusion=True), c2, feats)
+    assert np.max(np.abs(c2.k[1] - caches[0].k[1])) > 1e-3
+
+
+def test_input_fusion_context_rows_are_causal():
+    """A later context token never changes an earlier one's cached K/V."""
+    cfg = replace(TINY, layers=2, input_fusion=True)
+    w = oracle.weights_to_numpy(make_weights(cfg, 10))
+    feats = make_features(cfg, 12, seed=11).float().numpy()
+    f2 = feats.copy()
+    f2[8:] += 1.0
+    cs = []
+    for f in (feats, f2):
+        cache = oracle.RequestCache(cfg.layers, cfg.n_kv_heads, cfg.head_dim)
+        oracle.inject_context(w, cfg, cache, f)
+        cs.append(cache)
+    for i in range(cfg.layers):
+        np.testing.assert_array_equal(cs[0].k[i][:8], cs[1].k[i][:8])
+        assert np.max(np.abs(cs[0].k[i][8:] - cs[1].k[i][8:])) > 1e-3
