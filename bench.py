@@ -47,6 +47,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-bs32", action="store_true", help="skip the batch-32 sub-record of the default run")
+    ap.add_argument("--only", choices=["verify_sampled", "packed_attention"],
+                    help="run and print only this sub-benchmark (1 GPU)")
     return ap.parse_args()
 
 
@@ -677,6 +679,12 @@ def main():
         if backend == "nccl":
             torch.cuda.set_device(local)
         torch.distributed.init_process_group(backend)
+    if args.only:
+        torch.cuda.set_device(local)
+        if rank == 0:
+            fn = measure_sampled_verify if args.only == "verify_sampled" else measure_packed_attention
+            print(json.dumps({"only": args.only, **fn(args.steps, max(args.warmup, 1))}), flush=True)
+        return
     if args.impl == "reference":
         res = run_reference(args, rank, world, local)
     else:

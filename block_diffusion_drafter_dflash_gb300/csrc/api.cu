@@ -175,9 +175,8 @@ struct WsPlan {
   // persistent path: sums of squares, attention chunk partials, tickets + barrier
   int persist;
   int fused;   // one persistent launch runs the injection and the drafter pass
-  size_t ssq, ssq2, aml, tickets, qimg;
+  size_t ssq, ssq2, aml, tickets;
   int ntickets, nch;
-  size_t qimg_bytes;
 };
 
 // The persistent path serves bf16 calls of at most 16 token rows whose
@@ -186,6 +185,12 @@ bool persist_draft_ok(const dflash_model* m, int B, int block) {
   const dflash_config& c = m->cfg;
   return m->persist && !c.qk_norm && B * block <= kPRows && (c.n_q_heads / c.n_kv_heads) * block <= kPAttnRows &&
          6 * c.layers + 1 <= kPMaxPhases && c.ffn % kTileN == 0;
+}
+// A whole cycle in one launch: fusion and injection phases before the drafter's
+// (6 layers' worth of phases + 3; segments: 6 a layer, 2 a layer for the
+// injection, the fusion and the LM head).
+bool persist_cycle_ok(const dflash_model* m) {
+  return 6 * m->cfg.layers + 3 <= kPMaxPhases && 8 * m->cfg.layers + 2 <= kPMaxSeg;
 }
 bool persist_inject_ok(const dflash_model* m, int max_rows) {
   return m->persist && !m->cfg.qk_norm && !m->cfg.input_fusion && max_rows <= kPRows && 1 + 2 * m->cfg.layers <= kPMaxSeg;
@@ -206,7 +211,7 @@ WsPlan plan_ws(const dflash_model* m, int B, int cap, int block, int max_rows) {
   auto take = [&](size_t bytes) { size_t o = off; off += align256(std::max<size_t>(bytes, 1)); return o; };
   const bool inj_p = max_rows > 0 && persist_inject_ok(m, max_rows);
   const bool drf_p = block > 0 && persist_draft_ok(m, B, block);
-  if ((max_rows > 0 && block > 0) ? (inj_p && drf_p) : (inj_p || drf_p)) {
+  if ((max_rows > 0 && block > 0) ? (inj_p && drf_p && persist_cycle_ok(m)) : (inj_p || drf_p)) {
     // one persistent launch: activation planes padded to 16 rows, stream-K scratch per CTA;
     // with both an injection and a block, one launch runs the whole cycle
     const int half = c.head_dim / 2;
@@ -234,9 +239,6 @@ WsPlan plan_ws(const dflash_model* m, int B, int cap, int block, int max_rows) {
       p.rope_q = take(sizeof(float2) * (size_t)kPRows * half);
       p.opart = take(sizeof(float) * (size_t)groups * p.nch * kPAttnRows * c.head_dim);
       p.aml = take(sizeof(float2) * (size_t)groups * p.nch * kPAttnRows);
-      // the queries as the attention's A-operand image, one pass of 64 rows a group
-      p.qimg_bytes = (size_t)groups * (c.head_dim / 64) * 16384;
-      p.qimg = take(p.qimg_bytes);
     }
     p.ssq = take(sizeof(float) * (size_t)(D / kTileN) * kPRows);
     p.partial = take(sizeof(float) * (size_t)m->sms * 2 * kPRows * 256);
@@ -591,9 +593,7 @@ struct PhaseBuilder {
     ph.gain = static_cast<const __nv_bfloat16*>(gain);
     ph.seg0 = nseg_total();
     ph.mrows = p.M;
-    ph.xmap2 = -1;
     ph.ssq_in = p.ssq;
-    ph.ssq_in2 = nullptr;
     ph.u_out = p.u;
     ph.ssq_out = p.ssq;
     return p.nphase - 1;
@@ -633,7 +633,7 @@ struct PhaseBuilder {
   void finish() {
     for (int i = 0; i < p.nphase; ++i) {
       PPhase& ph = p.ph[i];
-      if (ph.kind != kPhGemm || ph.kb % 2 || ph.xmap2 >= 0) continue;   // two row groups fill a 64-column stage
+      if (ph.kind != kPhGemm || ph.kb % 2) continue;
       bool narrow = true;
       for (int j = ph.seg0; j < ph.seg0 + ph.nseg; ++j) narrow = narrow && p.seg[j].tw == 128;
       if (narrow) {
@@ -693,9 +693,9 @@ int32_t run_inject_persist(const dflash_model* m, dflash_cache* cache, const voi
 
 // The drafter pass as one persistent launch.  With inj_rows > 0 (a plan with
 // P.fused) the same launch first runs the injection of those rows: a fusion
-// phase (W_c) writes H_t's planes, and each layer's Q/K/V phase carries the
-// injected rows as a second row group, so that W_K and W_V are read once for
-// the block's keys and values and for the context's.
+// phase (W_c) writes H_t's planes and sums of squares, an injection phase
+// projects every layer's context K/V into the cache, then the drafter's
+// phases follow.
 int32_t run_draft_persist(const dflash_model* m, const dflash_cache* cache, const int32_t* anchor, int block,
                           int32_t* drafts, float* logits, char* ws, const WsPlan& P, cudaStream_t s,
                           const void* feats = nullptr, const int32_t* n_new = nullptr, int inj_rows = 0) {
@@ -727,7 +727,7 @@ int32_t run_draft_persist(const dflash_model* m, const dflash_cache* cache, cons
             persist_draft_prep_launch(static_cast<const __nv_bfloat16*>(m->embed), anchor, c.mask_token_id, c.vocab,
                                       B, block, D, static_cast<const __nv_bfloat16*>(m->layers[0].g_in), x, u,
                                       (size_t)kPRows * D, ssq, slots, tickets, P.ntickets + 1, m->status_dev, ctx_len,
-                                      m->inv_freq_dev, c.head_dim, rope, ws + P.qimg, P.qimg_bytes, s),
+                                      m->inv_freq_dev, c.head_dim, rope, s),
             "embedding");
   PParams pp{};
   if (!encode_activation_map(&pp.xmap[0], u, D, 2 * kPRows, D, kPRows) ||
@@ -754,10 +754,7 @@ int32_t run_draft_persist(const dflash_model* m, const dflash_cache* cache, cons
   float* q = reinterpret_cast<float*>(ws + P.q);
   __nv_bfloat16* kb = reinterpret_cast<__nv_bfloat16*>(ws + P.kb);
   __nv_bfloat16* vb = reinterpret_cast<__nv_bfloat16*>(ws + P.vb);
-  __nv_bfloat16* qimg = reinterpret_cast<__nv_bfloat16*>(ws + P.qimg);
-  const float att_scale = 1.0f / sqrtf((float)c.head_dim);
-  pp.qkv = EpiQKV<__nv_bfloat16>{q, kb, vb, rope, block, c.n_q_heads, c.n_kv_heads, c.head_dim, pad8(block),
-                                 qimg, att_scale * 1.4426950408889634f, c.n_q_heads / c.n_kv_heads};
+  pp.qkv = EpiQKV<__nv_bfloat16>{q, kb, vb, rope, block, c.n_q_heads, c.n_kv_heads, c.head_dim, pad8(block)};
   pp.swiglu = EpiSwiGLU<__nv_bfloat16>{a, F, (size_t)kPRows * F};
   pp.slots = slots;
   pp.logits = logits;
@@ -783,16 +780,13 @@ int32_t run_draft_persist(const dflash_model* m, const dflash_cache* cache, cons
   ap.ml = reinterpret_cast<float2*>(ws + P.aml);
   ap.out = o;
   ap.out_plane = (size_t)kPRows * hq;
-  ap.scale = att_scale;
-  ap.qimg = qimg;
+  ap.scale = 1.0f / sqrtf((float)c.head_dim);
   if (!encode_attention_maps(&pp.amaps, ap.kc, ap.vc, kb, vb, B, c.layers, c.n_kv_heads, c.head_dim, cache->cap,
-                             pad8(cache->cap), block, pad8(block)) ||
-      !encode_activation_map(&pp.amaps.qm, qimg, c.head_dim, B * c.n_kv_heads * 128, c.head_dim, 128))
+                             pad8(cache->cap), block, pad8(block)))
     return fail(DFLASH_ERR_CUDA, "could not encode attention tensor maps");
 
   float* ssq_ht = fused ? reinterpret_cast<float*>(ws + P.ssq2) : nullptr;
   if (fused) {
-    pp.M2 = inj_rows;
     pp.inject = EpiInject<__nv_bfloat16>{reinterpret_cast<__nv_bfloat16*>(cache->base + cache->k_off),
                                          reinterpret_cast<__nv_bfloat16*>(cache->base + cache->v_off),
                                          reinterpret_cast<const int2*>(ws + P.rowinfo),
@@ -808,15 +802,18 @@ int32_t run_draft_persist(const dflash_model* m, const dflash_cache* cache, cons
     pp.ph[ph].u_out = ht;
     pp.ph[ph].ssq_out = ssq_ht;
     pb.seg(kMapWc, kMapWc, D, 0, 0);
+    // every layer's context K/V of the injected rows
+    const int ip = pb.add_gemm(kEpInject, D, 4, 2, kPRows, 1, nullptr);
+    pp.ph[ip].mrows = inj_rows;
+    pp.ph[ip].ssq_in = ssq_ht;
+    for (int l = 0; l < c.layers; ++l) {
+      pb.seg(layer_map(l, kMapK), layer_map(l, kMapK), hk, 0, 2 * l);
+      pb.seg(layer_map(l, kMapV), layer_map(l, kMapV), hk, 0, 2 * l + 1);
+    }
   }
   for (int l = 0; l < c.layers; ++l) {
     const dflash_layer_weights& L = m->layers[l];
-    const int qph = pb.add_gemm(fused ? kEpQKVInj : kEpQKV, D, 0, 2, kPRows, 1, nullptr);
-    if (fused) {   // the injected rows (H_t planes) as the second row group
-      pp.ph[qph].xmap2 = 4;
-      pp.ph[qph].ssq_in2 = ssq_ht;
-      pp.ph[qph].layer = l;
-    }
+    pb.add_gemm(kEpQKV, D, 0, 2, kPRows, 1, nullptr);
     pb.seg(layer_map(l, kMapQ), layer_map(l, kMapQ), hq, 0, 0);
     pb.seg(layer_map(l, kMapK), layer_map(l, kMapK), hk, 0, 1);
     pb.seg(layer_map(l, kMapV), layer_map(l, kMapV), hk, 0, 2);

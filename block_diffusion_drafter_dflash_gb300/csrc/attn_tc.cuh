@@ -21,8 +21,9 @@
 // Keys.  A group's keys are its context keys 0..c-1 (cache) in tiles of 128,
 // then one tile of its block keys.  With ctx_shared every request reads the
 // context slab of request 0 (its own length c): the blocks of one packed
-// training sequence share that sequence's context.  K is stored key-major ([pos][hd]) and V
-// hd-major ([hd][pos]), so that both products read their B operand K-major;
+// training sequence share that sequence's context.  K is stored key-major
+// ([pos][hd]) and V hd-major ([hd][pos]), so that both products read their B
+// operand K-major;
 // tiles arrive by TMA (128-byte swizzle).  Keys past the valid ones read
 // finite values (the cache is zeroed at creation; past the tensor end TMA
 // fills zeros) and get probability exactly 0 (score -inf).
@@ -47,11 +48,9 @@ constexpr float kNegInf = -1.0e30f;
 constexpr float kLazy = 8.0f;              // raise the running max only beyond this margin
 constexpr long long kBudget = 200000000LL;
 
-// Tensor maps of one launch: K cache, V cache (hd-major), block K, block V
-// (hd-major), and (with AttnParams::qimg) the prepared query operands
-// [groups * 128 A rows][hd] bf16, 64 x 128 boxes.
+// Tensor maps of one launch: K cache, V cache (hd-major), block K, block V (hd-major).
 struct Maps {
-  CUtensorMap kc, vc, kb, vb, qm;
+  CUtensorMap kc, vc, kb, vb;
 };
 
 // Shared memory (1024-byte aligned base): Q A-tile per 64 columns of hd;
@@ -75,7 +74,7 @@ struct Cfg {
 };
 
 struct Bars {
-  uint64_t kfull, vfull, sdone, odone, qfull;
+  uint64_t kfull, vfull, sdone, odone;
 };
 
 __device__ __forceinline__ void init_bars(Bars* b) {
@@ -83,7 +82,6 @@ __device__ __forceinline__ void init_bars(Bars* b) {
   ptx::mbar_init(&b->vfull, 1);
   ptx::mbar_init(&b->sdone, 1);
   ptx::mbar_init(&b->odone, 1);
-  ptx::mbar_init(&b->qfull, 1);
 }
 
 // A-tile row of query row i (0..63) of a pass: quarter i/16, hi part at +0, lo at +16
@@ -209,13 +207,10 @@ __device__ void load_v(const AttnParams& p, const Maps& m, int b, int kvh, int t
 // Optional `stamps` (globaltimer): [0] Q staged, [1] the first tile's scores
 // ready, [2] the last P V done, [3] output written, [4] the first V tile in
 // shared memory, [5] the first P tile stored.  Returns false on a timeout.
-// With p.qimg the Q tile arrives by one bulk copy of the group's prepared
-// image (qload: how many images this CTA loaded before, for the barrier
-// phase) instead of being staged from the fp32 queries.
 template <int HD, int NT, class Sync, class Out, class Done>
 __device__ bool run(const AttnParams& p, const Maps& m, int b, int kvh, int pass, int t0, int t1, int nct,
                     uint8_t* sm, uint32_t tmem, Bars* bars, int& uses, int tid, Sync sync, int32_t* status, Out out,
-                    Done done, float* xch = nullptr, unsigned long long* stamps = nullptr, int qload = 0) {
+                    Done done, float* xch = nullptr, unsigned long long* stamps = nullptr) {
   static_assert(NT == 128 || NT == 256, "128 or 256 threads");
   using C = Cfg<HD>;
   constexpr int NP = NT / 128;        // warps per lane quarter
@@ -232,24 +227,9 @@ __device__ bool run(const AttnParams& p, const Maps& m, int b, int kvh, int pass
 
   // the first tile's K now; its V once the scores are issued (it is needed
   // only after the softmax, and the Q loads need not queue behind it)
-  if (p.qimg) {
-    if (tid == 0) {
-      // the operand rows were written by other CTAs through the generic proxy;
-      // TMA swizzles them into the A tiles (one 128-row box per 64 columns)
-      ptx::fence_proxy_async_global();
-      ptx::mbar_arrive_expect_tx(&bars->qfull, C::kQ);
-      const int passes = (rows + 63) / 64;
-      const int row0 = ((b * p.nkv + kvh) * passes + pass) * 128;
-      for (int s = 0; s < C::kSub; ++s)
-        ptx::tma_load_2d(sm + s * kTile16, &m.qm, &bars->qfull, 64 * s, row0, ptx::policy_evict_first());
-    }
-    if (tid == 0 && t0 < t1) load_k<HD>(p, m, b, kvh, t0, nct, sm, bars);
-    ok = ptx::mbar_wait(&bars->qfull, static_cast<uint32_t>(qload) & 1u, kBudget, status);
-  } else {
-    if (tid == 0 && t0 < t1) load_k<HD>(p, m, b, kvh, t0, nct, sm, bars);
-    stage_q<HD, NT>(p, b, kvh, pass, sm, tid);
-    ptx::fence_proxy_async_shared();
-  }
+  if (tid == 0 && t0 < t1) load_k<HD>(p, m, b, kvh, t0, nct, sm, bars);
+  stage_q<HD, NT>(p, b, kvh, pass, sm, tid);
+  ptx::fence_proxy_async_shared();
   sync();
   if (stamps && tid == 0) stamps[0] = ptx::globaltimer();
 

@@ -91,16 +91,6 @@ struct EpiQKV {
   const float2* rope;
   int block, nq, nkv, hd;
   int vpitch;
-  // Optional: the queries written instead as the block attention's A operand
-  // of each (request, kv head) group, row-major bf16 [128 A rows][hd]: query
-  // row i = (head - kvh*G)*block + k of the group's 64, value q * qscale
-  // (log2-domain scores) as a bf16 hi part in A row 32(i/16) + i%16 and its lo
-  // residual 16 rows further — so that the attention loads it with TMA, which
-  // applies the 128-byte swizzle.  Consecutive threads store consecutive
-  // columns.  Rows past G*block stay zero.
-  __nv_bfloat16* qimg;
-  float qscale;
-  int G;
   // thread n owns feature n of the tile; the RoPE entries of 8 rows are
   // loaded before any store so that their loads overlap
   __device__ __forceinline__ void operator()(const float* t, int ld, int m0, int mc, int, const GemmSeg& sg,
@@ -153,15 +143,7 @@ struct EpiQKV {
         }
         const float v = t[n * ld + m], pv = t[pn * ld + m];
         const float r = tag == 2 ? v : (d < half ? v * sc[j].x - pv * sc[j].y : v * sc[j].x + pv * sc[j].y);
-        if (tag == 0 && qimg) {
-          const int kvh = head / G, i = (head - kvh * G) * block + k;
-          const float x = r * qscale;
-          const __nv_bfloat16 hi = __float2bfloat16_rn(x);
-          const __nv_bfloat16 lo = __float2bfloat16_rn(x - __bfloat162float(hi));
-          __nv_bfloat16* img = qimg + ((size_t)(b * nkv + kvh) * 128 + 32 * (i >> 4) + (i & 15)) * hd + d;
-          img[0] = hi;
-          img[(size_t)16 * hd] = lo;
-        } else if (tag == 0)
+        if (tag == 0)
           q[(((size_t)b * nh + head) * block + k) * hd + d] = r;
         else
           put_act(dkv, (size_t)block * hd, (((size_t)b * nh + head) * planes * block + k) * hd + d, r);

@@ -22,8 +22,6 @@ struct AttnParams {
   int chunk;            // keys per split (context + block keys counted together)
   int splits;
   int ctx_shared;       // 1: every request reads request 0's context slab (packed training blocks of one sequence)
-  const __nv_bfloat16* qimg;   // or nullptr: the queries already as the attention's A-operand images,
-                               // [B][nkv][hd/64][128 rows x 64 columns] per group (one pass), see EpiQKV
   float* opart;         // [B][nq][block][splits][hd] unnormalised partial outputs
   float2* ml;           // [B][nq][block][splits] (running max, running sum)
   void* out;            // [B*block][nq*hd]: the W_O GEMM's activation operand

@@ -103,7 +103,6 @@ struct PBook {
   uint64_t ring_free;   // attention is done with the ring (one phase per attention phase)
   attn_tc::Bars abars;  // the attention's TMA and MMA barriers
   float rs[kPRows];
-  float rs2[kPRows];    // 1/rms of the second row group (injected rows of a fused cycle)
 };
 
 static_assert(kStage % 1024 == 0 && kXBytes % 1024 == 0, "stages keep the 1024-byte swizzle alignment");
@@ -301,19 +300,11 @@ __device__ void activation_producer(const PParams& p, PBook* bk, uint8_t* ring, 
       if (it >= S && !wait_timed(&bk->empty[s], ((it / S) & 1) ^ 1, p.status, wx, true)) goto done;
       const int kx = (i % ph.kb) * ph.kw, halves = ph.kw / 64;
       uint8_t* x = ring + (size_t)s * kStage;
-      if (ph.xmap2 >= 0) {   // two row groups of two planes: B rows 0..31 and 32..63 (64 K columns a stage)
-        ptx::mbar_arrive_expect_tx(&bk->fullX[s], 4 * kPRows * 128);
-        for (int pl = 0; pl < 2; ++pl) {
-          ptx::tma_load_2d(x + pl * kPRows * 128, &p.xmap[ph.xmap], &bk->fullX[s], kx, pl * ph.prow, pol);
-          ptx::tma_load_2d(x + (2 + pl) * kPRows * 128, &p.xmap[ph.xmap2], &bk->fullX[s], kx, pl * ph.prow, pol);
-        }
-      } else {
-        ptx::mbar_arrive_expect_tx(&bk->fullX[s], halves * ph.planes * kPRows * 128);
-        for (int hh = 0; hh < halves; ++hh)
-          for (int pl = 0; pl < ph.planes; ++pl)
-            ptx::tma_load_2d(x + hh * kXHalf + pl * kPRows * 128, &p.xmap[ph.xmap], &bk->fullX[s], kx + 64 * hh,
-                             pl * ph.prow, pol);
-      }
+      ptx::mbar_arrive_expect_tx(&bk->fullX[s], halves * ph.planes * kPRows * 128);
+      for (int hh = 0; hh < halves; ++hh)
+        for (int pl = 0; pl < ph.planes; ++pl)
+          ptx::tma_load_2d(x + hh * kXHalf + pl * kPRows * 128, &p.xmap[ph.xmap], &bk->fullX[s], kx + 64 * hh,
+                           pl * ph.prow, pol);
     }
     trace_val(p, cta, pi, kTrWaitXEmpty, wx);
   }
@@ -333,8 +324,7 @@ __device__ void mma_issuer(const PParams& p, PBook* bk, uint8_t* ring, uint32_t 
     for (int i = sp.i0; i < sp.i1;) {
       const int t = i / ph.kb, k0 = i - t * ph.kb, k1 = min(sp.i1 - t * ph.kb, ph.kb);
       const bool wide = p.seg[seg_of(p, ph, t)].tw == kTwMax;   // weights on N
-      const int bcols = kPRows * (ph.planes + (ph.xmap2 >= 0 ? 2 : 0));   // token columns (weights on M)
-      const uint32_t idesc = wide ? ptx::idesc_bf16_f32(128, kTwMax) : ptx::idesc_bf16_f32(128, bcols);
+      const uint32_t idesc = wide ? ptx::idesc_bf16_f32(128, kTwMax) : ptx::idesc_bf16_f32(128, kPRows * ph.planes);
       const int buf = seq & 1, use = seq >> 1;
       if (use >= 1 && !ptx::mbar_wait(&bk->accfree[buf], (use - 1) & 1, kBudget, p.status)) goto done;
       ptx::tc_fence_after();
@@ -479,10 +469,6 @@ __device__ __forceinline__ void publish_tw(int rows, const float* st, float* dst
     *reinterpret_cast<float4*>(dst + m * kTwMax + fq) =
         make_float4(st[fq * kLd + m], st[(fq + 1) * kLd + m], st[(fq + 2) * kLd + m], st[(fq + 3) * kLd + m]);
 }
-// Rows a stream-K piece of phase ph carries: its row group, or both groups.
-__device__ __forceinline__ int piece_rows(const PParams& p, const PPhase& ph) {
-  return ph.xmap2 >= 0 ? max(ph.mrows, p.M2) : ph.mrows;
-}
 __device__ __forceinline__ void publish_piece(int rows, int tw, const float* st, float* dst, int ct) {
   if (tw == kTwMax)
     publish_tw<kTwMax>(rows, st, dst, ct);
@@ -499,7 +485,7 @@ __device__ void add_pieces(const PParams& p, const PPhase& ph, int G, int t, int
   const int fq = 4 * (ct % PM::kQ), r0 = ct / PM::kQ;
   const int W = phase_iters(ph);
   const int g = phase_ctas(ph, G);
-  const int rows = piece_rows(p, ph);
+  const int rows = ph.mrows;
   float4 acc[PM::kR];
 #pragma unroll
   for (int j = 0; j < PM::kR; ++j) {
@@ -575,14 +561,6 @@ __device__ void run_epilogue(const PParams& p, const PPhase& ph, int t, float* s
     case kEpQKV:
       for (int h = 0; h < halves; ++h) p.qkv(st + h * 128 * kLd, kLd, 0, ph.mrows, 0, sg, tis * halves + h, ct, 128);
       break;
-    case kEpQKVInj:   // 128-feature tiles; the injected rows' values staged as features 128..255
-      p.qkv(st, kLd, 0, ph.mrows, 0, sg, tis, ct, 128);
-      if (sg.tag > 0) {   // K (tag 1) or V (tag 2) of layer ph.layer: context K/V into the cache
-        GemmSeg si = sg;
-        si.tag = 2 * ph.layer + (sg.tag - 1);
-        p.inject(st + 128 * kLd, kLd, 0, p.M2, 0, si, tis, ct, 128);
-      }
-      break;
     case kEpInject:
       for (int h = 0; h < halves; ++h) p.inject(st + h * 128 * kLd, kLd, 0, ph.mrows, 0, sg, tis * halves + h, ct, 128);
       break;
@@ -596,19 +574,11 @@ __device__ bool gemm_phase(const PParams& p, const PPhase& ph, int pi, PBook* bk
                            int cta, int ct, int& seq) {
   if (ph.scaled) {
     const int m = ct >> 3, part = ct & 7, nt = p.D / 128;
-    float a = 0.f, a2 = 0.f;
+    float a = 0.f;
     if (m < ph.mrows)
       for (int t = part; t < nt; t += 8) a += __ldcg(ph.ssq_in + t * kPRows + m);
-    if (ph.xmap2 >= 0 && m < p.M2)
-      for (int t = part; t < nt; t += 8) a2 += __ldcg(ph.ssq_in2 + t * kPRows + m);
-    for (int o = 1; o < 8; o <<= 1) {
-      a += __shfl_xor_sync(0xffffffffu, a, o);
-      a2 += __shfl_xor_sync(0xffffffffu, a2, o);
-    }
-    if (part == 0) {
-      bk->rs[m] = m < ph.mrows ? rsqrtf(a / (float)p.D + p.eps) : 0.f;
-      bk->rs2[m] = (ph.xmap2 >= 0 && m < p.M2) ? rsqrtf(a2 / (float)p.D + p.eps) : 0.f;
-    }
+    for (int o = 1; o < 8; o <<= 1) a += __shfl_xor_sync(0xffffffffu, a, o);
+    if (part == 0) bk->rs[m] = m < ph.mrows ? rsqrtf(a / (float)p.D + p.eps) : 0.f;
   }
   csync();
   const Span sp = cta_span(ph, G, cta);
@@ -660,13 +630,6 @@ __device__ bool gemm_phase(const PParams& p, const PPhase& ph, int pi, PBook* bk
 #pragma unroll
         for (int m = 0; m < kPRows; ++m) v[m] += w[m];
       }
-      if (ph.xmap2 >= 0) {   // the second row group: token columns 32..47 (hi) and 48..63 (lo), staged
-        float h[kPRows], w[kPRows];   // as features 128..255 of the tile
-        ptx::tmem_ld16(ta + 2 * kPRows, h);
-        ptx::tmem_ld16(ta + 3 * kPRows, w);
-#pragma unroll
-        for (int m = 0; m < kPRows; ++m) st[(128 + ct) * kLd + m] = (h[m] + w[m]) * bk->rs2[m];
-      }
       ptx::tc_fence_before();
 #pragma unroll
       for (int m = 0; m < kPRows; ++m) st[ct * kLd + m] = ph.scaled ? v[m] * bk->rs[m] : v[m];
@@ -687,8 +650,8 @@ __device__ bool gemm_phase(const PParams& p, const PPhase& ph, int pi, PBook* bk
     if (cta != cf) {
       // a piece for the tile's reducer: publish it and announce it (release);
       // nothing here waits for the reduction
-      publish_piece(piece_rows(p, ph), ph.xmap2 >= 0 ? kTwMax : tw, st,
-                    p.partial + (size_t)(cta * 2 + (t == first_tile ? 0 : 1)) * (kPRows * kTwMax), ct);
+      publish_piece(ph.mrows, tw, st, p.partial + (size_t)(cta * 2 + (t == first_tile ? 0 : 1)) * (kPRows * kTwMax),
+                    ct);
       __threadfence();
       csync();
       if (ct == 0) {
@@ -721,7 +684,7 @@ __device__ bool gemm_phase(const PParams& p, const PPhase& ph, int pi, PBook* bk
     }
     csync();
     if (!bk->flag_tk) return false;
-    if (sg.tw == kTwMax || ph.xmap2 >= 0)
+    if (sg.tw == kTwMax)
       add_pieces<kTwMax>(p, ph, G, t, cf, cl, st, ct);
     else
       add_pieces<128>(p, ph, G, t, cf, cl, st, ct);
@@ -742,7 +705,7 @@ __device__ bool gemm_phase(const PParams& p, const PPhase& ph, int pi, PBook* bk
 // rows to global memory, maxima in log2 units.  Returns false on a timeout.
 template <int HD>
 __device__ bool attn_phase(const PParams& p, const PPhase& ph, int pi, PBook* bk, uint8_t* sm, uint32_t tmem, int cta,
-                           int ct, int& uses, int& qloads) {
+                           int ct, int& uses) {
   const AttnParams& ap = p.attn;
   AttnItem item;
   if (!attn_item(ap, cta, item)) return true;
@@ -766,8 +729,7 @@ __device__ bool attn_phase(const PParams& p, const PPhase& ph, int pi, PBook* bk
   // trace slots kTrAcc..kTrRed of an attention phase: the core's stamps
   unsigned long long* stamps = p.trace ? p.trace + ((size_t)cta * kPMaxPhases + pi) * kTrSlots + kTrAcc : nullptr;
   const bool ok = attn_tc::run<HD, 128>(a, p.amaps, b, kvh, 0, t0, t1, nct, sm, tmem, &bk->abars, uses, ct,
-                                        ComputeSync{}, p.status, out, done, nullptr, stamps, qloads);
-  ++qloads;
+                                        ComputeSync{}, p.status, out, done, nullptr, stamps);
   if (ct == 0) trace_at(p, cta, pi, kTrM1);
   return ok;
 }
@@ -839,7 +801,7 @@ __device__ void compute_warps(const PParams& p, PBook* bk, uint8_t* ring, uint8_
                               int cta) {
   const int ct = threadIdx.x - 128;
   float* st = reinterpret_cast<float*>(region);
-  int seq = 0, attn_uses = 0, qloads = 0;
+  int seq = 0, attn_uses = 0;
   for (int pi = 0; pi < p.nphase; ++pi) {
     const PPhase& ph = p.ph[pi];
     if (ct == 0) trace_at(p, cta, pi, kTrStart);
@@ -847,8 +809,8 @@ __device__ void compute_warps(const PParams& p, PBook* bk, uint8_t* ring, uint8_
       if (!gemm_phase(p, ph, pi, bk, st, tmem, G, cta, ct, seq)) return;
     } else if (ph.kind == kPhAttn) {
       // the weight producers hold off until this phase releases the ring
-      const bool ok = p.attn.hd == 64 ? attn_phase<64>(p, ph, pi, bk, ring, tmem, cta, ct, attn_uses, qloads)
-                                      : attn_phase<128>(p, ph, pi, bk, ring, tmem, cta, ct, attn_uses, qloads);
+      const bool ok = p.attn.hd == 64 ? attn_phase<64>(p, ph, pi, bk, ring, tmem, cta, ct, attn_uses)
+                                      : attn_phase<128>(p, ph, pi, bk, ring, tmem, cta, ct, attn_uses);
       csync();
       if (ct == 0) ptx::mbar_arrive(&bk->ring_free);
       if (!ok) return;
@@ -948,16 +910,12 @@ __global__ void __launch_bounds__(kThreads, 1) persist_kernel(const __grid_const
 __global__ void __launch_bounds__(256) persist_draft_prep_kernel(
     const __nv_bfloat16* embed, const int32_t* anchor, int mask_id, int vocab, int block, int D,
     const __nv_bfloat16* g, float* x, __nv_bfloat16* u, size_t u_plane, float* ssq, unsigned long long* slots,
-    int* zero, int nzero, int32_t* status, const int32_t* ctx_len, const double* inv_freq, int hd, float2* rope,
-    uint4* qimg, int qimg16) {
+    int* zero, int nzero, int32_t* status, const int32_t* ctx_len, const double* inv_freq, int hd, float2* rope) {
   griddep_wait();
   griddep_trigger();
   const int row = blockIdx.x, b = row / block, k = row - b * block;
   if (row == 0)
     for (int i = threadIdx.x; i < nzero; i += blockDim.x) zero[i] = 0;
-  // query images: rows past a group's query rows must read as zero
-  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < qimg16; i += gridDim.x * blockDim.x)
-    qimg[i] = make_uint4(0u, 0u, 0u, 0u);
   if (threadIdx.x == 0) slots[row] = 0ull;
   const int pos = ctx_len[b] + k;
   for (int i = threadIdx.x; i < (hd >> 1); i += blockDim.x) {
@@ -1044,10 +1002,9 @@ cudaError_t persist_draft_prep_launch(const __nv_bfloat16* embed, const int32_t*
                                       int B, int block, int D, const __nv_bfloat16* g, float* x, __nv_bfloat16* u,
                                       size_t u_plane, float* ssq, unsigned long long* slots, int* zero, int nzero,
                                       int32_t* status, const int32_t* ctx_len, const double* inv_freq, int hd,
-                                      float2* rope, void* qimg, size_t qimg_bytes, cudaStream_t s) {
+                                      float2* rope, cudaStream_t s) {
   return launch_pdl(persist_draft_prep_kernel, dim3(B * block), dim3(256), 0, s, embed, anchor, mask_id, vocab, block,
-                    D, g, x, u, u_plane, ssq, slots, zero, nzero, status, ctx_len, inv_freq, hd, rope,
-                    static_cast<uint4*>(qimg), (int)(qimg_bytes / 16));
+                    D, g, x, u, u_plane, ssq, slots, zero, nzero, status, ctx_len, inv_freq, hd, rope);
 }
 
 }  // namespace dflash

@@ -26,9 +26,7 @@ enum : int {
   kEpQKV,        // block Q/K/V (EpiQKV), scaled by 1/rms
   kEpResid,      // x += acc: planes of x * gain, per-tile sums of x^2 (W_O, W_D)
   kEpSwiGLU,     // silu(gate) * up (EpiSwiGLU), scaled by 1/rms
-  kEpLM,         // argmax (and optional logits) of the mask rows, scaled by 1/rms
-  kEpQKVInj      // block Q/K/V of the first row group and, for the K and V tiles, the
-                 // context K/V of the second group (injected rows) into the cache
+  kEpLM          // argmax (and optional logits) of the mask rows, scaled by 1/rms
 };
 
 struct PPhase {
@@ -41,12 +39,10 @@ struct PPhase {
   int planes;      // activation planes (1: exact bf16 input, 2: hi/lo pair)
   int prow;        // map rows from plane 0 to plane 1
   int scaled;      // multiply the accumulator of row m by 1/rms(row m) before the epilogue
-  int layer;       // draft layer of an attention phase or of a kEpQKVInj phase
+  int layer;       // draft layer of an attention phase
   const __nv_bfloat16* gain;  // kEpFuse / kEpResid: gain of the RMSNorm that reads the planes written
-  int mrows;       // token rows of the phase's (first) row group
-  int xmap2;       // -1, or the map of a second 16-row group (2 planes) after the first: B rows 32..63
-  const float* ssq_in;        // scaled phases: sums of squares of the first group's normed input
-  const float* ssq_in2;       // ... and of the second group's
+  int mrows;       // token rows of the phase (the injected rows for the fusion and injection phases)
+  const float* ssq_in;        // scaled phases: sums of squares of the normed input
   __nv_bfloat16* u_out;       // kEpFuse / kEpResid: planes written ([2][16][D], u_plane apart)
   float* ssq_out;             // kEpFuse / kEpResid: their per-tile sums of squares [D/128][16]
 };
@@ -55,8 +51,7 @@ struct PParams {
   CUtensorMap xmap[kPXMaps];   // activation maps: 64 x 16 boxes, 128-byte swizzle
   const CUtensorMap* wmaps;    // weight maps of the model (device memory)
   int nphase;
-  int M;                       // token rows (<= 16)
-  int M2;                      // rows of a second group (the injected rows of a fused cycle), or 0
+  int M;                       // token rows of the drafter pass (<= 16)
   int D;                       // hidden size (RMSNorm width)
   float eps;
   int stages;                  // ring depth
@@ -91,11 +86,11 @@ cudaError_t persist_prepare(int hd);
 
 // Draft prologue: x[row] = E[token], planes of x * g_in (u), per-tile sums of
 // x^2 (ssq), RoPE table of the row's position, zeroed slots / tickets /
-// barrier (`nzero` ints at `zero`), zeroed query images (`qimg_bytes`).
+// barrier (`nzero` ints at `zero`).
 cudaError_t persist_draft_prep_launch(const __nv_bfloat16* embed, const int32_t* anchor, int mask_id, int vocab,
                                       int B, int block, int D, const __nv_bfloat16* g, float* x, __nv_bfloat16* u,
                                       size_t u_plane, float* ssq, unsigned long long* slots, int* zero, int nzero,
                                       int32_t* status, const int32_t* ctx_len, const double* inv_freq, int hd,
-                                      float2* rope, void* qimg, size_t qimg_bytes, cudaStream_t s);
+                                      float2* rope, cudaStream_t s);
 
 }  // namespace dflash

@@ -24,8 +24,9 @@ START, DONE, MMA_LAST = 0, 1, 6                  # slots used here
 
 def phase_names(layers: int, lm_head: bool = True, fusion: bool = False) -> List[str]:
     """Phases of a persistent drafter launch; `fusion`: the launch of a whole
-    cycle (dflash_draft_cycle), which starts with the context fusion."""
-    names = ["fusion"] if fusion else []
+    cycle (dflash_draft_cycle), which starts with the context fusion and the
+    injection of every layer's context K/V."""
+    names = ["fusion", "inject"] if fusion else []
     for l in range(layers):
         names += [f"L{l} qkv", f"L{l} attn", f"L{l} merge", f"L{l} o", f"L{l} gateup", f"L{l} down"]
     return names + (["lmhead"] if lm_head else [])
