@@ -13,11 +13,12 @@
 //
 //   row_stats   grid (chunks, rows): per 8192-logit chunk of a row, the max m
 //               of z = l * log2(e) / T and s = sum exp2(z - m) (online form);
-//   accept      one warp per request: merge the chunks of its rows, walk the
-//               drafts left to right with the acceptance test, pick the
-//               distribution to draw from (residual at the first rejection,
-//               or the target's row after the block) and write tau and the
-//               accepted tokens;
+//   accept      one warp per request: lane k merges the chunks of draft
+//               position k's two rows and reads its token's two logits (all
+//               positions at once), takes the acceptance test, and a ballot
+//               finds the first rejection; the distribution to draw from is
+//               the residual there, or the target's row after the block;
+//               writes tau and the accepted tokens;
 //   draw_sums   grid (chunks, draws): per chunk, the unnormalised mass of
 //               the chosen distribution (max(0, p_t - p_d), or p_t);
 //   draw_pick   one CTA per draw: the chunk where the running mass first
@@ -63,6 +64,8 @@ __device__ __forceinline__ const float* row_ptr(const float* draft, const float*
 
 __global__ void __launch_bounds__(kThreads) row_stats_kernel(const float* draft, const float* target, int nd, int V,
                                                              float zscale, float2* part, int nchunk) {
+  griddep_wait();
+  griddep_trigger();
   const int c = blockIdx.x, r = blockIdx.y;
   const float* x = row_ptr(draft, target, nd, r, V);
   const int v0 = c * kChunk, v1 = min(V, v0 + kChunk);
@@ -112,35 +115,52 @@ __global__ void __launch_bounds__(32) accept_kernel(const float* draft, const fl
                                                     const float* u_accept, const float2* part, int nchunk, int B,
                                                     int g, int V, float zscale, DrawSel* sel, int32_t* accept_len,
                                                     int32_t* out_tokens) {
+  griddep_wait();
+  griddep_trigger();
   const int b = blockIdx.x, lane = threadIdx.x;
   const int nd = B * (g - 1);
-  int kstar = g - 1;   // first rejected position (g - 1: none, the bonus)
-  float2 msd = make_float2(0.f, 1.f), mst = make_float2(0.f, 1.f);
-  for (int k = 0; k < g - 1; ++k) {
-    const int rd = b * (g - 1) + k, rt = nd + b * g + k;
-    const float2 md = row_total(part, rd, nchunk), mt = row_total(part, rt, nchunk);
-    const int d = tokens[rd];
-    bool keep = false;
-    if (d >= 0 && d < V) {   // an id outside the vocabulary is rejected
-      const float pd = prob(__ldg(draft + (size_t)rd * V + d), zscale, md);
-      const float pt = prob(__ldg(target + (size_t)(b * g + k) * V + d), zscale, mt);
-      const float a = pd <= 0.f ? 1.f : fminf(1.f, pt / pd);
-      keep = __ldg(u_accept + rd) < a;
-    }
-    if (!keep) {
-      kstar = k;
-      msd = md;
-      mst = mt;
-      break;
+  // every input of the walk first, in parallel: lane k < g-1 takes draft
+  // position k (its two rows' (max, sum) and the two logits of its token),
+  // lane g-1 the target row after the block; g <= 32
+  float2 md = make_float2(0.f, 1.f), mt = make_float2(0.f, 1.f);
+  float ld = 0.f, lt = 0.f, ua = 0.f;
+  int d = -1;
+  if (lane < g) {
+    const int rt = nd + b * g + lane;
+    float2 t = make_float2(-INFINITY, 0.f);
+    for (int c = 0; c < nchunk; ++c) t = merge_ms(t, part[(size_t)rt * nchunk + c]);
+    mt = t;
+    if (lane < g - 1) {
+      const int rd = b * (g - 1) + lane;
+      float2 q = make_float2(-INFINITY, 0.f);
+      for (int c = 0; c < nchunk; ++c) q = merge_ms(q, part[(size_t)rd * nchunk + c]);
+      md = q;
+      d = tokens[rd];
+      ua = u_accept[rd];
+      if (d >= 0 && d < V) {
+        ld = draft[(size_t)rd * V + d];
+        lt = target[(size_t)(b * g + lane) * V + d];
+      }
     }
   }
-  if (kstar == g - 1) mst = row_total(part, nd + b * g + g - 1, nchunk);
+  // lane k keeps its draft iff u < min(1, p_t / p_d); the first lane that does
+  // not is the first rejection (an id outside the vocabulary is rejected)
+  bool keep = false;
+  if (lane < g - 1 && d >= 0 && d < V) {
+    const float pd = prob(ld, zscale, md), pt = prob(lt, zscale, mt);
+    const float a = pd <= 0.f ? 1.f : fminf(1.f, pt / pd);
+    keep = ua < a;
+  }
+  const unsigned rejected = __ballot_sync(0xffffffffu, lane < g - 1 && !keep);
+  const int kstar = rejected ? __ffs(rejected) - 1 : g - 1;   // g - 1: none rejected, the bonus
+  const float2 mst = make_float2(__shfl_sync(0xffffffffu, mt.x, kstar), __shfl_sync(0xffffffffu, mt.y, kstar));
+  const float2 msd = make_float2(__shfl_sync(0xffffffffu, md.x, kstar), __shfl_sync(0xffffffffu, md.y, kstar));
   if (lane == 0) {
     DrawSel s;
     s.pt = target + (size_t)(b * g + kstar) * V;
     s.pd = kstar < g - 1 ? draft + (size_t)(b * (g - 1) + kstar) * V : nullptr;
     s.mst = mst;
-    s.msd = msd;
+    s.msd = kstar < g - 1 ? msd : make_float2(0.f, 1.f);
     s.out = out_tokens + (size_t)b * g + kstar;
     sel[b] = s;
     accept_len[b] = kstar + 1;
@@ -152,6 +172,8 @@ __global__ void __launch_bounds__(32) accept_kernel(const float* draft, const fl
 // Sampling rows on their own: draw i comes from softmax(row i).
 __global__ void __launch_bounds__(32) sample_sel_kernel(const float* logits, const float2* part, int nchunk, int V,
                                                         DrawSel* sel, int32_t* tokens) {
+  griddep_wait();
+  griddep_trigger();
   const int r = blockIdx.x;
   const float2 ms = row_total(part, r, nchunk);
   if (threadIdx.x == 0) {
@@ -173,6 +195,8 @@ __device__ __forceinline__ float mass(const DrawSel& s, int v, float zscale) {
 
 __global__ void __launch_bounds__(kThreads) draw_sums_kernel(const DrawSel* sel, int V, float zscale, float* csum,
                                                              int nchunk) {
+  griddep_wait();
+  griddep_trigger();
   const int c = blockIdx.x, i = blockIdx.y;
   const DrawSel s = sel[i];
   const int v0 = c * kChunk, v1 = min(V, v0 + kChunk);
@@ -192,11 +216,13 @@ __global__ void __launch_bounds__(kThreads) draw_sums_kernel(const DrawSel* sel,
 __global__ void __launch_bounds__(kThreads) draw_pick_kernel(const DrawSel* sel, int V, float zscale,
                                                              const float* csum, int nchunk, const float* u,
                                                              int32_t* next_anchor) {
+  griddep_wait();
+  griddep_trigger();
   const int i = blockIdx.x;
   const DrawSel s = sel[i];
   __shared__ int s_chunk;
   __shared__ float s_rem;
-  __shared__ float s_tsum[kThreads];
+  __shared__ float s_tsum[kThreads / 32];
   __shared__ int s_tok;
   if (threadIdx.x == 0) {
     // running mass over the chunks in id order (double: the chunk sums are few)
@@ -236,19 +262,20 @@ __global__ void __launch_bounds__(kThreads) draw_pick_kernel(const DrawSel* sel,
     mv[j] = v < v1 ? mass(s, v, zscale) : 0.f;
     own += mv[j];
   }
-  s_tsum[threadIdx.x] = own;
-  __syncthreads();
-  if (threadIdx.x == 0) {   // exclusive scan of 256 partial sums, in id order
-    float run = 0.f;
-    for (int t = 0; t < kThreads; ++t) {
-      const float m = s_tsum[t];
-      s_tsum[t] = run;
-      run += m;
-    }
+  // exclusive scan of the 256 partial sums in id order: within each warp by
+  // shuffles, then across the 8 warp totals
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  float inc = own;
+  for (int o = 1; o < 32; o <<= 1) {
+    const float y = __shfl_up_sync(0xffffffffu, inc, o);
+    if (lane >= o) inc += y;
   }
+  if (lane == 31) s_tsum[wid] = inc;
   __syncthreads();
+  float wbase = 0.f;
+  for (int w = 0; w < wid; ++w) wbase += s_tsum[w];
   const float rem = s_rem;
-  const float before = s_tsum[threadIdx.x];
+  const float before = wbase + inc - own;
   if (rem != INFINITY && before <= rem && rem < before + own) {
     // this thread's ids hold the remainder: the first whose running mass
     // exceeds it (or, if rounding says none does, the last with mass)
@@ -322,16 +349,23 @@ cudaError_t verify_sampled_launch(const float* draft_logits, const float* target
   const float zscale = kLog2e / temperature;
   SamplingWs w = carve(ws, rows, B, V);
   *launches = 0;
-  row_stats_kernel<<<dim3(nchunk, rows), kThreads, 0, s>>>(draft_logits, target_logits, nd, V, zscale, w.part, nchunk);
+  cudaError_t e = launch_pdl(row_stats_kernel, dim3(nchunk, rows), dim3(kThreads), 0, s, draft_logits, target_logits,
+                             nd, V, zscale, w.part, nchunk);
+  if (e != cudaSuccess) return e;
   ++*launches;
-  accept_kernel<<<B, 32, 0, s>>>(draft_logits, target_logits, drafts, u_accept, w.part, nchunk, B, g, V, zscale, w.sel,
-                                 accept_len, out_tokens);
+  e = launch_pdl(accept_kernel, dim3(B), dim3(32), 0, s, draft_logits, target_logits, drafts, u_accept,
+                 static_cast<const float2*>(w.part), nchunk, B, g, V, zscale, w.sel, accept_len, out_tokens);
+  if (e != cudaSuccess) return e;
   ++*launches;
-  draw_sums_kernel<<<dim3(nchunk, B), kThreads, 0, s>>>(w.sel, V, zscale, w.csum, nchunk);
+  e = launch_pdl(draw_sums_kernel, dim3(nchunk, B), dim3(kThreads), 0, s, static_cast<const DrawSel*>(w.sel), V, zscale,
+                 w.csum, nchunk);
+  if (e != cudaSuccess) return e;
   ++*launches;
-  draw_pick_kernel<<<B, kThreads, 0, s>>>(w.sel, V, zscale, w.csum, nchunk, u_sample, next_anchor);
+  e = launch_pdl(draw_pick_kernel, dim3(B), dim3(kThreads), 0, s, static_cast<const DrawSel*>(w.sel), V, zscale,
+                 static_cast<const float*>(w.csum), nchunk, u_sample, next_anchor);
+  if (e != cudaSuccess) return e;
   ++*launches;
-  return cudaGetLastError();
+  return cudaSuccess;
 }
 
 cudaError_t sample_tokens_launch(const float* logits, int rows, int V, float temperature, const float* u,
@@ -340,15 +374,23 @@ cudaError_t sample_tokens_launch(const float* logits, int rows, int V, float tem
   const float zscale = kLog2e / temperature;
   SamplingWs w = carve(ws, rows, rows, V);
   *launches = 0;
-  row_stats_kernel<<<dim3(nchunk, rows), kThreads, 0, s>>>(logits, nullptr, rows, V, zscale, w.part, nchunk);
+  cudaError_t e = launch_pdl(row_stats_kernel, dim3(nchunk, rows), dim3(kThreads), 0, s, logits,
+                             static_cast<const float*>(nullptr), rows, V, zscale, w.part, nchunk);
+  if (e != cudaSuccess) return e;
   ++*launches;
-  sample_sel_kernel<<<rows, 32, 0, s>>>(logits, w.part, nchunk, V, w.sel, tokens);
+  e = launch_pdl(sample_sel_kernel, dim3(rows), dim3(32), 0, s, logits, static_cast<const float2*>(w.part), nchunk, V,
+                 w.sel, tokens);
+  if (e != cudaSuccess) return e;
   ++*launches;
-  draw_sums_kernel<<<dim3(nchunk, rows), kThreads, 0, s>>>(w.sel, V, zscale, w.csum, nchunk);
+  e = launch_pdl(draw_sums_kernel, dim3(nchunk, rows), dim3(kThreads), 0, s, static_cast<const DrawSel*>(w.sel), V,
+                 zscale, w.csum, nchunk);
+  if (e != cudaSuccess) return e;
   ++*launches;
-  draw_pick_kernel<<<rows, kThreads, 0, s>>>(w.sel, V, zscale, w.csum, nchunk, u, nullptr);
+  e = launch_pdl(draw_pick_kernel, dim3(rows), dim3(kThreads), 0, s, static_cast<const DrawSel*>(w.sel), V, zscale,
+                 static_cast<const float*>(w.csum), nchunk, u, static_cast<int32_t*>(nullptr));
+  if (e != cudaSuccess) return e;
   ++*launches;
-  return cudaGetLastError();
+  return cudaSuccess;
 }
 
 }  // namespace dflash
