@@ -15,6 +15,7 @@ independent, so there is no collective on the data path).
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import json
 import os
 import statistics
@@ -49,6 +50,8 @@ def parse():
     ap.add_argument("--no-bs32", action="store_true", help="skip the batch-32 sub-record of the default run")
     ap.add_argument("--only", choices=["verify_sampled", "packed_attention"],
                     help="run and print only this sub-benchmark (1 GPU)")
+    ap.add_argument("--kv-bf16", action="store_true",
+                    help="the context cache keeps one bf16 per value (else a hi and a lo bf16 plane)")
     return ap.parse_args()
 
 
@@ -308,10 +311,11 @@ def method_bytes(wl, inject_rows: int) -> dict:
 
 
 def kv_storage_bytes(wl) -> int:
-    """Context K/V the attention reads as stored: fp32 precision (fp32 values,
-    or the hi and lo bf16 planes of bf16 models), 4 bytes a value."""
+    """Context K/V the attention reads as stored: 4 bytes a value (fp32, or the
+    hi and lo bf16 planes of bf16 models), 2 with a one-plane bf16 cache."""
     c = wl.cfg
-    return 2 * c.layers * c.n_kv_heads * c.head_dim * 4 * sum(wl.ctx)
+    per = 2 if getattr(c, "kv_bf16", False) else 4
+    return 2 * c.layers * c.n_kv_heads * c.head_dim * per * sum(wl.ctx)
 
 
 def kv_weight_bytes(cfg) -> int:
@@ -440,6 +444,8 @@ def measure(wl, W, K, rank, world, local, barrier, want_e2e=True):
                                        "seeded target agreement)",
         "config": {"workload": wl.name, "drafter": wl.cfg.name, "batch_per_gpu": wl.batch, "block": wl.block,
                    "ctx": wl.ctx if len(wl.ctx) <= 4 else f"{min(wl.ctx)}..{max(wl.ctx)} ({len(wl.ctx)} requests)",
+                   "kv_cache": ("one bf16 per value" if getattr(wl.cfg, "kv_bf16", False)
+                                else "hi and lo bf16 planes per value (fp32-level)"),
                    "l2": "inputs larger than L2 (weights streamed every cycle)",
                    "timing": "CUDA-graph replay of whole cycles (inject, draft, synthetic target, verify); "
                              "per-stage times from an eager pass with events",
@@ -532,9 +538,17 @@ def measure_packed_attention(K: int, W: int = 3) -> dict:
             "status": df.dflash_packed_attention_status(ws), "finite": bool(torch.isfinite(out).all().item())}
 
 
+def workload_for(args, name: str):
+    """The named workload, with the one-plane bf16 cache under --kv-bf16."""
+    wl = workloads()[name]
+    if getattr(args, "kv_bf16", False):
+        wl = dataclasses.replace(wl, cfg=dataclasses.replace(wl.cfg, kv_bf16=True))
+    return wl
+
+
 def run_gpu(args, rank, world, local):
     torch.cuda.set_device(local)
-    wl = workloads()[args.workload]
+    wl = workload_for(args, args.workload)
     dist = world > 1 and torch.distributed.is_initialized()
 
     def barrier():
@@ -549,7 +563,8 @@ def run_gpu(args, rank, world, local):
         result["_weights"] = cyc.weights
         cyc = None
         torch.cuda.empty_cache()
-        r32, c32 = measure(workloads()["8b_bs32"], 3, min(args.steps, 20), rank, world, local, barrier, False)
+        r32, c32 = measure(workload_for(args, "8b_bs32"), 3, min(args.steps, 20), rank, world, local, barrier,
+                           False)
         del c32
         torch.cuda.empty_cache()
         result["bs32"] = {k: r32[k] for k in ("value", "unit", "ms_per_step", "steps", "warmup", "config",

@@ -48,7 +48,8 @@ def _config_struct(cfg) -> _abi.Config:
                        max_block=cfg.max_block, rope_theta=float(cfg.rope_theta), rms_eps=float(cfg.rms_eps),
                        mask_token_id=int(mask), dtype=_abi.DTYPE_F32 if cfg.dtype == "fp32" else _abi.DTYPE_BF16,
                        qk_norm=1 if getattr(cfg, "qk_norm", False) else 0,
-                       input_fusion=1 if getattr(cfg, "input_fusion", False) else 0)
+                       input_fusion=1 if getattr(cfg, "input_fusion", False) else 0,
+                       kv_bf16=1 if getattr(cfg, "kv_bf16", False) else 0)
 
 
 def dflash_version() -> int:
@@ -117,18 +118,19 @@ class Cache:
         if self.model.dtype == torch.float32:
             raw = self.buffer[off:off + B * L * H * cap * hd * 4]
             return raw.view(torch.float32).view(B, L, H, cap, hd)
-        if hd_major:   # bf16 V: [B][L][H][2][hd][pitch], pitch = capacity rounded up to 8
+        P = 1 if getattr(c, "kv_bf16", False) else 2   # bf16 planes of each value
+        if hd_major:   # bf16 V: [B][L][H][P][hd][pitch], pitch = capacity rounded up to 8
             pitch = (cap + 7) // 8 * 8
-            raw = self.buffer[off:off + B * L * H * 2 * hd * pitch * 2]
-            planes = raw.view(torch.bfloat16).view(B, L, H, 2, hd, pitch)[..., :cap].transpose(-1, -2)
+            raw = self.buffer[off:off + B * L * H * P * hd * pitch * 2]
+            planes = raw.view(torch.bfloat16).view(B, L, H, P, hd, pitch)[..., :cap].transpose(-1, -2)
         else:
-            raw = self.buffer[off:off + B * L * H * 2 * cap * hd * 2]
-            planes = raw.view(torch.bfloat16).view(B, L, H, 2, cap, hd)
-        return planes[:, :, :, 0].float() + planes[:, :, :, 1].float()
+            raw = self.buffer[off:off + B * L * H * P * cap * hd * 2]
+            planes = raw.view(torch.bfloat16).view(B, L, H, P, cap, hd)
+        return planes.float().sum(dim=3)
 
     def k(self) -> torch.Tensor:
         """Context keys as fp32 [batch][layers][n_kv_heads][capacity][head_dim]
-        (a view for fp32 models; hi + lo of the two bf16 planes otherwise)."""
+        (a view for fp32 models; the sum of the bf16 planes otherwise)."""
         return self._kv_view(self.k_off)
 
     def v(self) -> torch.Tensor:

@@ -125,6 +125,10 @@ constexpr size_t kTraceEntries = 8u << 16;   // 8 timestamps for up to 65536 CTA
 size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
 // row pitch of hd-major V (bf16 models): positions rounded up to 8 (16-byte rows for TMA)
 int pad8(int n) { return (n + 7) & ~7; }
+// bf16 planes of every cached context K/V value: hi and lo, or one rounded value
+int kv_planes(const dflash_config& c) { return c.kv_bf16 ? 1 : 2; }
+// planes of the cache of a T model (an fp32 cache is one fp32 plane)
+template <typename T> int cache_planes(const dflash_config& c) { return ActPlanes<T>::n == 2 ? kv_planes(c) : 1; }
 
 int32_t check_config(const dflash_config* c) {
   if (!c) return fail(DFLASH_ERR_INVALID_ARG, "config is NULL");
@@ -150,6 +154,9 @@ int32_t check_config(const dflash_config* c) {
   if (c->input_fusion != 0 && c->input_fusion != 1)
     return fail(DFLASH_ERR_INVALID_ARG, "input_fusion %d must be 0 or 1", c->input_fusion);
   if (c->input_fusion && c->qk_norm) return fail(DFLASH_ERR_UNSUPPORTED, "input_fusion with qk_norm is not built");
+  if (c->kv_bf16 != 0 && c->kv_bf16 != 1) return fail(DFLASH_ERR_INVALID_ARG, "kv_bf16 %d must be 0 or 1", c->kv_bf16);
+  if (c->kv_bf16 && c->dtype != DFLASH_DTYPE_BF16) return fail(DFLASH_ERR_INVALID_ARG, "kv_bf16 needs a bf16 model");
+  if (c->kv_bf16 && c->qk_norm) return fail(DFLASH_ERR_UNSUPPORTED, "kv_bf16 with qk_norm is not built");
   return DFLASH_OK;
 }
 
@@ -389,7 +396,8 @@ int32_t run_context_layers(const dflash_model* m, dflash_cache* cache, int max_r
     add_seg(pkv, L.w_k, layer_map(l, kMapK), L.w_k, layer_map(l, kMapK), hk / kTileN, 0, 2 * l);
     add_seg(pkv, L.w_v, layer_map(l, kMapV), L.w_v, layer_map(l, kMapV), hk / kTileN, 0, 2 * l + 1);
     apply_plan(pkv, P.gf_kv, partial, counters);
-    EpiInject<T> ei{kc, vc, rowinfo, rope_c, c.layers, c.n_kv_heads, c.head_dim, cache->cap, pad8(cache->cap)};
+    EpiInject<T> ei{kc, vc, rowinfo, rope_c, c.layers, c.n_kv_heads, c.head_dim, cache->cap, pad8(cache->cap),
+                    cache_planes<T>(c)};
     DF_LAUNCH(DFLASH_STAGE_INJECT, 1, (gemm_launch<T, EpiInject<T>>(pkv, P.gf_kv, ei, s)), "context K/V GEMM");
     if (l + 1 == c.layers) break;
     GemmProblem pq = make_problem(m, uc, D, max_rows, D, pl, R * D);
@@ -400,8 +408,8 @@ int32_t run_context_layers(const dflash_model* m, dflash_cache* cache, int max_r
               "context Q GEMM");
     DF_LAUNCH(DFLASH_STAGE_ATTN, 1,
               ctx_attention_launch<T>(qc, kc, vc, rowinfo, max_rows, l, c.layers, c.n_q_heads, c.n_kv_heads,
-                                      c.head_dim, cache->cap, pad8(cache->cap), 1.0f / sqrtf((float)c.head_dim), oc,
-                                      R * hq, s),
+                                      c.head_dim, cache->cap, pad8(cache->cap), cache_planes<T>(c),
+                                      1.0f / sqrtf((float)c.head_dim), oc, R * hq, s),
               "context attention");
     GemmProblem po = make_problem(m, oc, hq, max_rows, hq, pl, R * hq);
     add_seg(po, L.w_o, layer_map(l, kMapO), L.w_o, layer_map(l, kMapO), D / kTileN, 0, 0);
@@ -461,13 +469,14 @@ int32_t run_inject(const dflash_model* m, dflash_cache* cache, const void* feats
   const float2* rope_c = reinterpret_cast<const float2*>(ws + P.rope_c);
   T* kc = reinterpret_cast<T*>(cache->base + cache->k_off);
   EpiInject<T> ei{kc, reinterpret_cast<T*>(cache->base + cache->v_off), rowinfo, c.qk_norm ? nullptr : rope_c,
-                  c.layers, c.n_kv_heads, c.head_dim, cache->cap, pad8(cache->cap)};
+                  c.layers, c.n_kv_heads, c.head_dim, cache->cap, pad8(cache->cap), cache_planes<T>(c)};
   DF_LAUNCH(DFLASH_STAGE_INJECT, 1, (gemm_launch<T, EpiInject<T>>(pi, P.g_inject, ei, s)), "injection GEMM");
   if (c.qk_norm)   // per-head key norm, then RoPE, of the injected keys
     for (int l = 0; l < c.layers; ++l)
       DF_LAUNCH(DFLASH_STAGE_OTHER, 1,
                 qknorm_cache_launch<T>(kc, rowinfo, max_rows, l, c.layers, c.n_kv_heads, c.head_dim, cache->cap,
-                                       static_cast<const T*>(m->layers[l].g_k), c.rms_eps, rope_c, s),
+                                       cache_planes<T>(c), static_cast<const T*>(m->layers[l].g_k), c.rms_eps,
+                                       rope_c, s),
                 "injected key norm");
   return DFLASH_OK;
 }
@@ -501,7 +510,8 @@ int32_t run_draft(const dflash_model* m, const dflash_cache* cache, const int32_
   attn_tc::Maps amaps;   // bf16 models: tensor maps of the K/V cache and of the block K/V
   if constexpr (ActPlanes<T>::n == 2) {
     if (!encode_attention_maps(&amaps, cache->base + cache->k_off, cache->base + cache->v_off, kb, vb, B, c.layers,
-                               c.n_kv_heads, c.head_dim, cache->cap, pad8(cache->cap), block, pad8(block)))
+                               c.n_kv_heads, c.head_dim, cache->cap, pad8(cache->cap), kv_planes(c), block,
+                               pad8(block)))
       return fail(DFLASH_ERR_CUDA, "could not encode attention tensor maps");
   }
   for (int l = 0; l < c.layers; ++l) {
@@ -525,7 +535,7 @@ int32_t run_draft(const dflash_model* m, const dflash_cache* cache, const int32_
     ap.kc = cache->base + cache->k_off;
     ap.vc = cache->base + cache->v_off;
     ap.ctx_len = ctx_len;
-    ap.layer = l; ap.layers = c.layers; ap.cap = cache->cap;
+    ap.layer = l; ap.layers = c.layers; ap.cap = cache->cap; ap.kvp = cache_planes<T>(c);
     ap.B = B; ap.nq = c.n_q_heads; ap.nkv = c.n_kv_heads; ap.hd = c.head_dim; ap.block = block;
     ap.chunk = P.attn_chunk; ap.splits = P.attn_splits;
     ap.opart = reinterpret_cast<float*>(ws + P.opart);
@@ -675,7 +685,8 @@ int32_t run_inject_persist(const dflash_model* m, dflash_cache* cache, const voi
   pp.status = m->status_dev;
   pp.inject = EpiInject<__nv_bfloat16>{reinterpret_cast<__nv_bfloat16*>(cache->base + cache->k_off),
                                        reinterpret_cast<__nv_bfloat16*>(cache->base + cache->v_off), rowinfo, rope,
-                                       c.layers, c.n_kv_heads, c.head_dim, cache->cap, pad8(cache->cap)};
+                                       c.layers, c.n_kv_heads, c.head_dim, cache->cap, pad8(cache->cap),
+                                       kv_planes(c)};
   pp.block = 1;
   pp.attn.hd = c.head_dim;
   PhaseBuilder pb{pp};
@@ -770,6 +781,7 @@ int32_t run_draft_persist(const dflash_model* m, const dflash_cache* cache, cons
   ap.ctx_len = ctx_len;
   ap.layers = c.layers;
   ap.cap = cache->cap;
+  ap.kvp = kv_planes(c);
   ap.B = B;
   ap.nq = c.n_q_heads;
   ap.nkv = c.n_kv_heads;
@@ -782,7 +794,7 @@ int32_t run_draft_persist(const dflash_model* m, const dflash_cache* cache, cons
   ap.out_plane = (size_t)kPRows * hq;
   ap.scale = 1.0f / sqrtf((float)c.head_dim);
   if (!encode_attention_maps(&pp.amaps, ap.kc, ap.vc, kb, vb, B, c.layers, c.n_kv_heads, c.head_dim, cache->cap,
-                             pad8(cache->cap), block, pad8(block)))
+                             pad8(cache->cap), ap.kvp, block, pad8(block)))
     return fail(DFLASH_ERR_CUDA, "could not encode attention tensor maps");
 
   float* ssq_ht = fused ? reinterpret_cast<float*>(ws + P.ssq2) : nullptr;
@@ -791,7 +803,7 @@ int32_t run_draft_persist(const dflash_model* m, const dflash_cache* cache, cons
                                          reinterpret_cast<__nv_bfloat16*>(cache->base + cache->v_off),
                                          reinterpret_cast<const int2*>(ws + P.rowinfo),
                                          reinterpret_cast<const float2*>(ws + P.rope_c), c.layers, c.n_kv_heads,
-                                         c.head_dim, cache->cap, pad8(cache->cap)};
+                                         c.head_dim, cache->cap, pad8(cache->cap), kv_planes(c)};
   }
 
   PhaseBuilder pb{pp};
@@ -867,10 +879,11 @@ int32_t build_weight_maps(dflash_model* m) {
   return DFLASH_OK;
 }
 
-// K [b][layer][kvh][cap][hd] fp32, or two bf16 planes [..][2][cap][hd]; V the
-// same for fp32 models and hd-major [..][2][hd][pad8(cap)] for bf16 models.
+// K [b][layer][kvh][cap][hd] fp32, or kv_planes bf16 planes [..][P][cap][hd];
+// V the same for fp32 models and hd-major [..][P][hd][pad8(cap)] for bf16 models.
 size_t cache_k_bytes(const dflash_config* cfg, int batch, int capacity) {
-  return sizeof(float) * (size_t)batch * cfg->layers * cfg->n_kv_heads * (size_t)capacity * cfg->head_dim;
+  const size_t elem = cfg->dtype == DFLASH_DTYPE_BF16 ? 2 * (size_t)kv_planes(*cfg) : sizeof(float);
+  return elem * (size_t)batch * cfg->layers * cfg->n_kv_heads * (size_t)capacity * cfg->head_dim;
 }
 size_t cache_v_bytes(const dflash_config* cfg, int batch, int capacity) {
   return cache_k_bytes(cfg, batch, cfg->dtype == DFLASH_DTYPE_BF16 ? pad8(capacity) : capacity);

@@ -124,8 +124,8 @@ cudaError_t attention_tc_split_launch(const AttnParams& p, const attn_tc::Maps& 
 }
 
 bool encode_attention_maps(attn_tc::Maps* m, const void* kc, const void* vc, const void* kb, const void* vb, int B,
-                           int layers, int nkv, int hd, int cap, int cap_pitch, int block, int block_pitch) {
-  const int slabs_c = B * layers * nkv * 2, slabs_b = B * nkv * 2;
+                           int layers, int nkv, int hd, int cap, int cap_pitch, int kvp, int block, int block_pitch) {
+  const int slabs_c = B * layers * nkv * kvp, slabs_b = B * nkv * 2;
   return encode_activation_map(&m->kc, kc, hd, slabs_c * cap, hd, attn_tc::kKeys) &&
          encode_activation_map(&m->vc, vc, cap, slabs_c * hd, cap_pitch, hd) &&
          encode_activation_map(&m->kb, kb, hd, slabs_b * block, hd, attn_tc::kKeys) &&

@@ -18,6 +18,11 @@
 // shuffle.  Scores are in the log2 domain (Q is pre-scaled by
 // log2(e)/sqrt(hd)).
 //
+// A cache of one rounded bf16 per value (kvp = 1) gives its tiles' keys and
+// values one plane: N = 128 keys for S and N = hd for that tile's P V; the
+// block tile keeps both planes, and its lo-plane product goes to the O lo
+// columns, which then hold nothing else.
+//
 // Keys.  A group's keys are its context keys 0..c-1 (cache) in tiles of 128,
 // then one tile of its block keys.  With ctx_shared every request reads the
 // context slab of request 0 (its own length c): the blocks of one packed
@@ -153,6 +158,9 @@ __device__ void stage_q(const AttnParams& p, int b, int kvh, int pass, uint8_t* 
   }
 }
 
+// Planes of tile t: the cache's for a context tile, two for the block tile.
+__device__ __forceinline__ int tile_planes(const AttnParams& p, int t, int nct) { return t < nct ? p.kvp : 2; }
+
 // TMA of tile t of group (b, kvh) of layer p.layer: context keys [128t, 128t+128)
 // for t < nct, else the block's keys.  Issued by one thread.
 template <int HD>
@@ -160,12 +168,13 @@ __device__ void load_k(const AttnParams& p, const Maps& m, int b, int kvh, int t
   using C = Cfg<HD>;
   uint8_t* kt = sm + C::kOffK;
   const int bc = p.ctx_shared ? 0 : b;   // the context slab
-  ptx::mbar_arrive_expect_tx(&bars->kfull, C::kKBytes);
-  for (int pl = 0; pl < 2; ++pl)
+  const int np = tile_planes(p, t, nct);
+  ptx::mbar_arrive_expect_tx(&bars->kfull, np * (C::kKBytes / 2));
+  for (int pl = 0; pl < np; ++pl)
     for (int s = 0; s < C::kSub; ++s) {
       uint8_t* dst = kt + (s * 2 + pl) * kTile16;
       if (t < nct) {
-        const int row = ((((bc * p.layers + p.layer) * p.nkv + kvh) * 2 + pl) * p.cap) + kKeys * t;
+        const int row = ((((bc * p.layers + p.layer) * p.nkv + kvh) * p.kvp + pl) * p.cap) + kKeys * t;
         ptx::tma_load_2d(dst, &m.kc, &bars->kfull, 64 * s, row, ptx::policy_evict_first());
       } else {
         const int row = ((b * p.nkv + kvh) * 2 + pl) * p.block;
@@ -179,12 +188,13 @@ __device__ void load_v(const AttnParams& p, const Maps& m, int b, int kvh, int t
   using C = Cfg<HD>;
   uint8_t* vt = sm + C::kOffV;
   const int bc = p.ctx_shared ? 0 : b;   // the context slab
-  ptx::mbar_arrive_expect_tx(&bars->vfull, C::kVBytes);
-  for (int pl = 0; pl < 2; ++pl)
+  const int np = tile_planes(p, t, nct);
+  ptx::mbar_arrive_expect_tx(&bars->vfull, np * (C::kVBytes / 2));
+  for (int pl = 0; pl < np; ++pl)
     for (int h = 0; h < 2; ++h) {
       uint8_t* dst = vt + (h * 2 + pl) * C::kVHalf;
       if (t < nct) {
-        const int row = (((bc * p.layers + p.layer) * p.nkv + kvh) * 2 + pl) * HD;
+        const int row = (((bc * p.layers + p.layer) * p.nkv + kvh) * p.kvp + pl) * HD;
         ptx::tma_load_2d(dst, &m.vc, &bars->vfull, kKeys * t + 64 * h, row, ptx::policy_evict_first());
       } else {
         const int row = ((b * p.nkv + kvh) * 2 + pl) * HD;
@@ -221,7 +231,11 @@ __device__ bool run(const AttnParams& p, const Maps& m, int b, int kvh, int pass
   const int c = p.ctx_len[b];
   const uint32_t lanes = static_cast<uint32_t>(q4 * 32) << 16;
   const uint32_t tS = tmem + lanes, tO = tmem + lanes + 2 * kKeys;   // this warp's lanes
-  const uint32_t idS = ptx::idesc_bf16_f32(128, 2 * kKeys), idO = ptx::idesc_bf16_f32(128, 2 * HD);
+  const uint32_t idS2 = ptx::idesc_bf16_f32(128, 2 * kKeys), idO2 = ptx::idesc_bf16_f32(128, 2 * HD);
+  const uint32_t idS1 = ptx::idesc_bf16_f32(128, kKeys), idO1 = ptx::idesc_bf16_f32(128, HD);
+  // O columns a rescale touches: the lo half holds only the block tile's
+  // product when the cache has one plane, and that tile comes last
+  const int ocols = (p.kvp == 2 ? 2 * HD : HD) / NP;
   const int i = 16 * q4 + (lane & 15);   // query row of the pass held by this lane (hi part if lane < 16)
   bool ok = true;
 
@@ -237,6 +251,7 @@ __device__ bool run(const AttnParams& p, const Maps& m, int b, int kvh, int pass
   for (int t = t0; t < t1; ++t) {
     const uint32_t par = static_cast<uint32_t>(uses + (t - t0)) & 1u;
     const int nk = t < nct ? min(kKeys, c - kKeys * t) : p.block;   // valid keys of the tile
+    const int np = tile_planes(p, t, nct);
     // ---- S = Q K^T (thread 0), then the K buffer is free for the next tile
     if (tid == 0) {
       ok = ptx::mbar_wait(&bars->kfull, par, kBudget, status);
@@ -247,7 +262,7 @@ __device__ bool run(const AttnParams& p, const Maps& m, int b, int kvh, int pass
           for (int k = 0; k < 4; ++k) {
             const uint64_t ad = ptx::smem_desc_sw128(sm + s * kTile16) + 2 * k;
             const uint64_t bd = ptx::smem_desc_sw128(sm + C::kOffK + s * 2 * kTile16) + 2 * k;
-            ptx::mma_bf16(tmem, ad, bd, idS, (s | k) != 0 ? 1u : 0u);
+            ptx::mma_bf16(tmem, ad, bd, np == 2 ? idS2 : idS1, (s | k) != 0 ? 1u : 0u);
           }
         ptx::mma_commit(&bars->sdone);
         if (t > t0) {   // the V buffer is free once the previous P V is done
@@ -269,17 +284,35 @@ __device__ bool run(const AttnParams& p, const Maps& m, int b, int kvh, int pass
     // keep (one shuffle a key).  This warp's keys: KC per half from KC*part.
     const int half = lane >> 4;
     float pv[KC];
+    if (np == 2) {
 #pragma unroll
-    for (int c0 = 0; c0 < KC; c0 += 16) {
-      const int cc = KC * part + c0;
-      float v[64];   // [Khi keys cc.., Klo keys cc.., Khi keys 64+cc.., Klo keys 64+cc..]
-      ptx::tmem_ld16x4(tS + cc, tS + kKeys + cc, tS + 64 + cc, tS + kKeys + 64 + cc, v);
+      for (int c0 = 0; c0 < KC; c0 += 16) {
+        const int cc = KC * part + c0;
+        float v[64];   // [Khi keys cc.., Klo keys cc.., Khi keys 64+cc.., Klo keys 64+cc..]
+        ptx::tmem_ld16x4(tS + cc, tS + kKeys + cc, tS + 64 + cc, tS + kKeys + 64 + cc, v);
 #pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        const float lo_keys = v[j] + v[16 + j], hi_keys = v[32 + j] + v[48 + j];
-        const float got = __shfl_xor_sync(0xffffffffu, half ? lo_keys : hi_keys, 16);
-        const float x = half ? hi_keys + got : lo_keys + got;
-        pv[c0 + j] = (64 * half + cc + j < nk) ? x : kNegInf;
+        for (int j = 0; j < 16; ++j) {
+          const float lo_keys = v[j] + v[16 + j], hi_keys = v[32 + j] + v[48 + j];
+          const float got = __shfl_xor_sync(0xffffffffu, half ? lo_keys : hi_keys, 16);
+          const float x = half ? hi_keys + got : lo_keys + got;
+          pv[c0 + j] = (64 * half + cc + j < nk) ? x : kNegInf;
+        }
+      }
+    } else {   // one key plane: two 16-key steps per load
+#pragma unroll
+      for (int c0 = 0; c0 < KC; c0 += 32) {
+        const int cc = KC * part + c0;
+        float v[64];   // [keys cc.., keys 64+cc.., keys cc+16.., keys 64+cc+16..]
+        ptx::tmem_ld16x4(tS + cc, tS + 64 + cc, tS + cc + 16, tS + 64 + cc + 16, v);
+#pragma unroll
+        for (int u = 0; u < 2; ++u)
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const float lo_keys = v[32 * u + j], hi_keys = v[32 * u + 16 + j];
+            const float got = __shfl_xor_sync(0xffffffffu, half ? lo_keys : hi_keys, 16);
+            const float x = half ? hi_keys + got : lo_keys + got;
+            pv[c0 + 16 * u + j] = (64 * half + cc + 16 * u + j < nk) ? x : kNegInf;
+          }
       }
     }
     float mx = kNegInf;
@@ -312,7 +345,7 @@ __device__ bool run(const AttnParams& p, const Maps& m, int b, int kvh, int pass
     ptx::tc_fence_after();
     if (__any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll 1
-      for (int d0 = 2 * DC * part; d0 < 2 * DC * (part + 1); d0 += 32) {
+      for (int d0 = ocols * part; d0 < ocols * (part + 1); d0 += 32) {
         float v[32];
         ptx::tmem_ld32(tO + d0, v);
 #pragma unroll
@@ -343,13 +376,25 @@ __device__ bool run(const AttnParams& p, const Maps& m, int b, int kvh, int pass
       ok = ptx::mbar_wait(&bars->vfull, par, kBudget, status);
       if (stamps && t == t0) stamps[4] = ptx::globaltimer();
       if (ok) {
+        // both planes in one N = 2 hd product, or the hi plane alone; the
+        // block tile of a one-plane cache adds its lo plane to the O lo columns
+        const bool split_lo = np == 2 && p.kvp == 1;
 #pragma unroll
         for (int h = 0; h < 2; ++h)
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
             const uint64_t ad = ptx::smem_desc_sw128(sm + C::kOffP + h * kTile16) + 2 * k;
             const uint64_t bd = ptx::smem_desc_sw128(sm + C::kOffV + h * 2 * C::kVHalf) + 2 * k;
-            ptx::mma_bf16(tmem + 2 * kKeys, ad, bd, idO, (t > t0 || h | k) ? 1u : 0u);
+            const uint32_t acc = (t > t0 || h | k) ? 1u : 0u;
+            if (np == 2 && !split_lo) {
+              ptx::mma_bf16(tmem + 2 * kKeys, ad, bd, idO2, acc);
+            } else {
+              ptx::mma_bf16(tmem + 2 * kKeys, ad, bd, idO1, acc);
+              if (split_lo) {
+                const uint64_t bl = ptx::smem_desc_sw128(sm + C::kOffV + (h * 2 + 1) * C::kVHalf) + 2 * k;
+                ptx::mma_bf16(tmem + 2 * kKeys + HD, ad, bl, idO1, (h | k) ? 1u : 0u);
+              }
+            }
           }
         ptx::mma_commit(&bars->odone);
       }
@@ -361,15 +406,21 @@ __device__ bool run(const AttnParams& p, const Maps& m, int b, int kvh, int pass
     ptx::tc_fence_after();
     if (stamps && tid == 0) stamps[2] = ptx::globaltimer();
     const int r = 64 * pass + i;
+    // the O lo columns hold something when the cache has two planes or the
+    // block tile (always the last) was among this item's tiles
+    const bool lo_cols = p.kvp == 2 || t1 > nct;
 #pragma unroll 1
     for (int d0 = DC * part; d0 < DC * (part + 1); d0 += 32) {
       float v[64];   // O columns d0.. of the Vhi and the Vlo products
-      ptx::tmem_ld32x2(tO + d0, tO + HD + d0, v);
+      if (lo_cols) {
+        ptx::tmem_ld32x2(tO + d0, tO + HD + d0, v);
 #pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        v[j] += v[32 + j];
-        v[j] += __shfl_xor_sync(0xffffffffu, v[j], 16);
+        for (int j = 0; j < 32; ++j) v[j] += v[32 + j];
+      } else {
+        ptx::tmem_ld32(tO + d0, v);
       }
+#pragma unroll
+      for (int j = 0; j < 32; ++j) v[j] += __shfl_xor_sync(0xffffffffu, v[j], 16);
       if (lane < 16 && r < rows) out(r, d0, v);
     }
     if constexpr (NP == 2) {   // the row's sum over both warps of the lane quarter

@@ -86,6 +86,14 @@ __device__ __forceinline__ void put_act(__nv_bfloat16* base, size_t plane, size_
   base[i] = hi;
   base[plane + i] = __float2bfloat16_rn(v - __bfloat162float(hi));
 }
+// One cached context K/V value: the hi and lo bf16 planes (kvp = 2) or the
+// value rounded to one bf16 (kvp = 1); fp32 caches keep the value.
+__device__ __forceinline__ void put_kv(float* base, size_t /*plane*/, size_t i, float v, int /*kvp*/) { base[i] = v; }
+__device__ __forceinline__ void put_kv(__nv_bfloat16* base, size_t plane, size_t i, float v, int kvp) {
+  const __nv_bfloat16 hi = __float2bfloat16_rn(v);
+  base[i] = hi;
+  if (kvp == 2) base[plane + i] = __float2bfloat16_rn(v - __bfloat162float(hi));
+}
 // four consecutive values (i a multiple of 4)
 __device__ __forceinline__ void put_act4(float* base, size_t /*plane*/, size_t i, float4 v) {
   *reinterpret_cast<float4*>(base + i) = v;
@@ -112,6 +120,11 @@ __device__ __forceinline__ float4 load4(const __nv_bfloat16* p) {
 __device__ __forceinline__ float get_act(const float* base, size_t /*plane*/, size_t i) { return base[i]; }
 __device__ __forceinline__ float get_act(const __nv_bfloat16* base, size_t plane, size_t i) {
   return __bfloat162float(base[i]) + __bfloat162float(base[plane + i]);
+}
+// a cached context K/V value of `kvp` planes (see put_kv)
+__device__ __forceinline__ float get_kv(const float* base, size_t /*plane*/, size_t i, int /*kvp*/) { return base[i]; }
+__device__ __forceinline__ float get_kv(const __nv_bfloat16* base, size_t plane, size_t i, int kvp) {
+  return kvp == 2 ? get_act(base, plane, i) : __bfloat162float(base[i]);
 }
 
 // ---------------------------------------------------------------- device status

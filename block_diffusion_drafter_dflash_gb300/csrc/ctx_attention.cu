@@ -11,7 +11,7 @@
 // memory), the warp keeps the running max and sum (base-2 exponent, scores
 // pre-scaled by log2(e)/sqrt(hd)), and lane l accumulates output dimensions
 // l, l+32, ... over the chunk's keys.  Keys and values are read as stored:
-// fp32, or the hi and lo bf16 planes (values head-dim-major) of bf16 models.
+// fp32, or the kvp bf16 planes (values head-dim-major) of bf16 models.
 #include "common.cuh"
 #include "kernels.cuh"
 
@@ -20,15 +20,10 @@ namespace {
 
 constexpr float kLog2e = 1.4426950408889634f;
 
-template <typename T>
-__device__ __forceinline__ float kv_at(const T* base, size_t plane, size_t i) {
-  return get_act(base, plane, i);
-}
-
 template <typename T, int HD>
 __global__ void __launch_bounds__(128) ctx_attn_kernel(const float* q, const T* kc, const T* vc, const int2* rowinfo,
                                                        int rows, int layer, int layers, int nq, int nkv, int cap,
-                                                       int vpitch, float qscale, T* out, size_t out_plane) {
+                                                       int vpitch, int kvp, float qscale, T* out, size_t out_plane) {
   griddep_wait();   // the K/V projection of this layer has written the cache
   griddep_trigger();
   constexpr int E = HD / 32;
@@ -46,13 +41,13 @@ __global__ void __launch_bounds__(128) ctx_attn_kernel(const float* q, const T* 
     return;
   }
   const int b = ri.x, pos = ri.y, kvh = h / (nq / nkv);
-  constexpr int planes = ActPlanes<T>::n;
+  constexpr bool bf16 = ActPlanes<T>::n == 2;
   const size_t slab = ((size_t)b * layers + layer) * nkv + kvh;
-  const T* kb = kc + slab * planes * (size_t)cap * HD;              // [plane][cap][HD]
+  const T* kb = kc + slab * kvp * (size_t)cap * HD;                  // [plane][cap][HD]
   const size_t kplane = (size_t)cap * HD;
-  const T* vb = planes == 2 ? vc + slab * 2 * (size_t)HD * vpitch   // [plane][HD][vpitch]
-                            : vc + slab * (size_t)cap * HD;         // [cap][HD]
-  const size_t vplane = planes == 2 ? (size_t)HD * vpitch : 0;
+  const T* vb = bf16 ? vc + slab * kvp * (size_t)HD * vpitch         // [plane][HD][vpitch]
+                     : vc + slab * (size_t)cap * HD;                 // [cap][HD]
+  const size_t vplane = bf16 ? (size_t)HD * vpitch : 0;
 #pragma unroll
   for (int e = 0; e < E; ++e) qs[warp][lane + 32 * e] = q[obase + lane + 32 * e] * qscale;
   __syncwarp();
@@ -66,7 +61,7 @@ __global__ void __launch_bounds__(128) ctx_attn_kernel(const float* q, const T* 
       float a = 0.f;
       const size_t kr = (size_t)key * HD;
 #pragma unroll 8
-      for (int d = 0; d < HD; ++d) a += qs[warp][d] * kv_at(kb, kplane, kr + d);
+      for (int d = 0; d < HD; ++d) a += qs[warp][d] * get_kv(kb, kplane, kr + d, kvp);
       sc = a;
     }
     float mx = sc;
@@ -87,7 +82,8 @@ __global__ void __launch_bounds__(128) ctx_attn_kernel(const float* q, const T* 
 #pragma unroll
       for (int e = 0; e < E; ++e) {
         const int d = lane + 32 * e;
-        const float v = planes == 2 ? kv_at(vb, vplane, (size_t)d * vpitch + kj) : kv_at(vb, vplane, (size_t)kj * HD + d);
+        const float v = bf16 ? get_kv(vb, vplane, (size_t)d * vpitch + kj, kvp)
+                             : get_kv(vb, vplane, (size_t)kj * HD + d, kvp);
         acc[e] += pj * v;
       }
     }
@@ -101,22 +97,22 @@ __global__ void __launch_bounds__(128) ctx_attn_kernel(const float* q, const T* 
 
 template <typename T>
 cudaError_t ctx_attention_launch(const float* q, const T* kc, const T* vc, const int2* rowinfo, int rows, int layer,
-                                 int layers, int nq, int nkv, int hd, int cap, int vpitch, float scale, T* out,
-                                 size_t out_plane, cudaStream_t s) {
+                                 int layers, int nq, int nkv, int hd, int cap, int vpitch, int kvp, float scale,
+                                 T* out, size_t out_plane, cudaStream_t s) {
   const int warps = rows * nq;
   if (warps == 0) return cudaSuccess;
   const float qscale = scale * kLog2e;
   if (hd == 64)
     return launch_pdl(ctx_attn_kernel<T, 64>, dim3((warps + 3) / 4), dim3(128), 0, s, q, kc, vc, rowinfo, rows, layer,
-                      layers, nq, nkv, cap, vpitch, qscale, out, out_plane);
+                      layers, nq, nkv, cap, vpitch, kvp, qscale, out, out_plane);
   return launch_pdl(ctx_attn_kernel<T, 128>, dim3((warps + 3) / 4), dim3(128), 0, s, q, kc, vc, rowinfo, rows, layer,
-                    layers, nq, nkv, cap, vpitch, qscale, out, out_plane);
+                    layers, nq, nkv, cap, vpitch, kvp, qscale, out, out_plane);
 }
 
 template cudaError_t ctx_attention_launch<float>(const float*, const float*, const float*, const int2*, int, int, int,
-                                                 int, int, int, int, int, float, float*, size_t, cudaStream_t);
+                                                 int, int, int, int, int, int, float, float*, size_t, cudaStream_t);
 template cudaError_t ctx_attention_launch<__nv_bfloat16>(const float*, const __nv_bfloat16*, const __nv_bfloat16*,
-                                                         const int2*, int, int, int, int, int, int, int, int, float,
-                                                         __nv_bfloat16*, size_t, cudaStream_t);
+                                                         const int2*, int, int, int, int, int, int, int, int, int,
+                                                         float, __nv_bfloat16*, size_t, cudaStream_t);
 
 }  // namespace dflash

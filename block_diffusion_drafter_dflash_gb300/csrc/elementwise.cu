@@ -352,12 +352,12 @@ __global__ void __launch_bounds__(256) qknorm_block_kernel(float* q, T* kb, cons
   }
 }
 
-// Injected context keys of layer `layer` in the cache (T planes
+// Injected context keys of layer `layer` in the cache (kvp T planes
 // [b][layer][kvh][plane][cap][hd]) for the rows of rowinfo: one warp per
 // (row, kv head); padding rows are skipped.
 template <typename T, int E>
 __global__ void __launch_bounds__(256) qknorm_cache_kernel(T* kc, const int2* rowinfo, int rows, int layer, int layers,
-                                                           int nkv, int cap, const T* g_k, float eps,
+                                                           int nkv, int cap, int kvp, const T* g_k, float eps,
                                                            const float2* rope) {
   griddep_wait();   // the injection projection (or the previous layer's pass) has finished
   griddep_trigger();
@@ -371,12 +371,12 @@ __global__ void __launch_bounds__(256) qknorm_cache_kernel(T* kc, const int2* ro
 #pragma unroll
   for (int e = 0; e < E; ++e) g[e] = to_f32(g_k[lane + 32 * e]);
   const size_t plane = (size_t)cap * hd;
-  const size_t base = ((((size_t)ri.x * layers + layer) * nkv + h) * ActPlanes<T>::n * cap + ri.y) * hd;
+  const size_t base = ((((size_t)ri.x * layers + layer) * nkv + h) * kvp * cap + ri.y) * hd;
 #pragma unroll
-  for (int e = 0; e < E; ++e) v[e] = get_act(kc, plane, base + lane + 32 * e);
+  for (int e = 0; e < E; ++e) v[e] = get_kv(kc, plane, base + lane + 32 * e, kvp);
   qknorm_rope_vec<E>(v, g, eps, hd, rope + (size_t)row * half);
 #pragma unroll
-  for (int e = 0; e < E; ++e) put_act(kc, plane, base + lane + 32 * e, v[e]);
+  for (int e = 0; e < E; ++e) put_kv(kc, plane, base + lane + 32 * e, v[e], kvp);
 }
 
 }  // namespace
@@ -395,14 +395,14 @@ cudaError_t qknorm_block_launch(float* q, T* kb, const T* g_q, const T* g_k, int
 
 template <typename T>
 cudaError_t qknorm_cache_launch(T* kc, const int2* rowinfo, int rows, int layer, int layers, int nkv, int hd, int cap,
-                                const T* g_k, float eps, const float2* rope, cudaStream_t s) {
+                                int kvp, const T* g_k, float eps, const float2* rope, cudaStream_t s) {
   const int n = rows * nkv;
   if (n == 0) return cudaSuccess;
   if (hd == 64)
     return launch_pdl(qknorm_cache_kernel<T, 2>, dim3((n + 7) / 8), dim3(256), 0, s, kc, rowinfo, rows, layer, layers,
-                      nkv, cap, g_k, eps, rope);
+                      nkv, cap, kvp, g_k, eps, rope);
   return launch_pdl(qknorm_cache_kernel<T, 4>, dim3((n + 7) / 8), dim3(256), 0, s, kc, rowinfo, rows, layer, layers, nkv,
-                    cap, g_k, eps, rope);
+                    cap, kvp, g_k, eps, rope);
 }
 
 cudaError_t synthetic_target_launch(const int32_t* draft, const uint8_t* match, const int32_t* off,
@@ -476,7 +476,7 @@ cudaError_t verify_launch(const int32_t* draft, const int32_t* target, int B, in
                                            const double*, int, float2*, cudaStream_t, float*);                    \
   template cudaError_t qknorm_block_launch<T>(float*, T*, const T*, const T*, int, int, int, int, int, float,      \
                                               const float2*, cudaStream_t);                                       \
-  template cudaError_t qknorm_cache_launch<T>(T*, const int2*, int, int, int, int, int, int, const T*, float,      \
+  template cudaError_t qknorm_cache_launch<T>(T*, const int2*, int, int, int, int, int, int, int, const T*, float, \
                                               const float2*, cudaStream_t);
 
 DFLASH_EW_INST(float)

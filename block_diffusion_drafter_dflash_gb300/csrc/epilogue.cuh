@@ -166,12 +166,13 @@ struct EpiInject {
   const float2* rope;
   int layers, nkv, hd, cap;
   int vpitch;
+  int kvp;   // bf16 planes of each cached value (2: hi and lo, 1: rounded); 1 for fp32 caches
   __device__ __forceinline__ void operator()(const float* t, int ld, int m0, int mc, int, const GemmSeg& sg,
                                              int tis, int tid, int nth) const {
     const int layer = sg.tag >> 1, is_v = sg.tag & 1, half = hd >> 1;
     T* dst = is_v ? vc : kc;
-    const int planes = ActPlanes<T>::n;
-    if (is_v && planes == 2) {
+    const int planes = kvp;
+    if (is_v && ActPlanes<T>::n == 2) {
       // bf16 V is hd-major: consecutive threads take consecutive rows
       // (positions) of one feature, so that a warp's stores are contiguous
       if (mc <= 0) return;
@@ -182,8 +183,9 @@ struct EpiInject {
         const int2 ri = __ldg(rowinfo + m0 + m);
         if (ri.x >= 0) {
           const int feat = tis * kTileN + f, head = feat >> hsh, d = feat & (hd - 1);
-          put_act(dst, (size_t)hd * vpitch,
-                  ((((size_t)ri.x * layers + layer) * nkv + head) * 2 * hd + d) * vpitch + ri.y, t[f * ld + m]);
+          put_kv(dst, (size_t)hd * vpitch,
+                 ((((size_t)ri.x * layers + layer) * nkv + head) * planes * hd + d) * vpitch + ri.y, t[f * ld + m],
+                 planes);
         }
         f += fstep;
         m += mstep;
@@ -215,8 +217,8 @@ struct EpiInject {
         if (ri[j].x < 0) continue;
         const float v = t[n * ld + m], pv = t[pn * ld + m];
         const float r = is_v ? v : (d < half ? v * sc[j].x - pv * sc[j].y : v * sc[j].x + pv * sc[j].y);
-        put_act(dst, (size_t)cap * hd,
-                ((((size_t)ri[j].x * layers + layer) * nkv + head) * planes * cap + ri[j].y) * hd + d, r);
+        put_kv(dst, (size_t)cap * hd,
+               ((((size_t)ri[j].x * layers + layer) * nkv + head) * planes * cap + ri[j].y) * hd + d, r, planes);
       }
     }
   }

@@ -8,16 +8,18 @@ namespace dflash {
 // ---------------------------------------------------------------- attention
 // Block queries of one draft layer against [context K/V of the cache ; block K/V]
 // (no mask: every block row sees all context and the whole block).
-// K/V (block and cache) are stored as `planes` planes of the model dtype
-// (fp32: one plane; bf16: hi and lo planes): index [..][plane][pos][hd].
+// K/V are stored as planes of the model dtype, index [..][plane][pos][hd]:
+// fp32 one plane; bf16 block K/V hi and lo planes, the bf16 cache `kvp`
+// planes (hi and lo, or one rounded value).
 struct AttnParams {
   const float* q;       // [B][nq][block][hd] fp32 (RoPE applied)
   const void* kb;       // [B][nkv][planes][block][hd]  (RoPE applied)
   const void* vb;       // [B][nkv][planes][block][hd]; bf16 models: [B][nkv][planes][hd][pad8(block)]
-  const void* kc;       // cache K [B][layers][nkv][planes][cap][hd]
-  const void* vc;       // cache V
+  const void* kc;       // cache K [B][layers][nkv][kvp][cap][hd]
+  const void* vc;       // cache V (bf16 models: [B][layers][nkv][kvp][hd][pad8(cap)])
   const int32_t* ctx_len;
   int layer, layers, cap;
+  int kvp;              // planes of the cache (fp32 models: 1)
   int B, nq, nkv, hd, block;
   int chunk;            // keys per split (context + block keys counted together)
   int splits;
@@ -38,10 +40,11 @@ template <typename T> cudaError_t attention_launch(const AttnParams& p, cudaStre
 cudaError_t attention_bf16_launch(const AttnParams& p, const attn_tc::Maps& maps, int32_t* status, cudaStream_t s,
                                   bool out_f32 = false);
 // Tensor maps of the bf16 attention: K cache [slabs*cap][hd], V cache
-// [slabs*hd][cap] (row pitch cap_pitch), block K [slabs*block][hd], block V
-// [slabs*hd][block] (row pitch block_pitch); 64 x rows boxes, 128-byte swizzle.
+// [slabs*hd][cap] (row pitch cap_pitch) with B*layers*nkv*kvp slabs, block K
+// [slabs*block][hd], block V [slabs*hd][block] (row pitch block_pitch) with
+// B*nkv*2 slabs; 64 x rows boxes, 128-byte swizzle.
 bool encode_attention_maps(attn_tc::Maps* m, const void* kc, const void* vc, const void* kb, const void* vb, int B,
-                           int layers, int nkv, int hd, int cap, int cap_pitch, int block, int block_pitch);
+                           int layers, int nkv, int hd, int cap, int cap_pitch, int kvp, int block, int block_pitch);
 // Shared-memory opt-in of the tensor-core split-KV attention kernel for head size hd.
 cudaError_t attention_tc_prepare(int hd);
 // One-time per-device setup (shared-memory opt-in) for up to `rows` query rows.
@@ -84,8 +87,8 @@ cudaError_t fuse_norm_launch(const float* y, const T* g, float eps, const int2* 
 // (planes `out_plane` apart; zero for padding rows).
 template <typename T>
 cudaError_t ctx_attention_launch(const float* q, const T* kc, const T* vc, const int2* rowinfo, int rows, int layer,
-                                 int layers, int nq, int nkv, int hd, int cap, int vpitch, float scale, T* out,
-                                 size_t out_plane, cudaStream_t s);
+                                 int layers, int nq, int nkv, int hd, int cap, int vpitch, int kvp, float scale,
+                                 T* out, size_t out_plane, cudaStream_t s);
 
 // QK-norm models: per-head RMSNorm (gain g [hd], epsilon eps) then RoPE, in
 // place, of the block queries q (fp32 [B][nq][block][hd]) and block keys kb
@@ -95,10 +98,11 @@ template <typename T>
 cudaError_t qknorm_block_launch(float* q, T* kb, const T* g_q, const T* g_k, int B, int block, int nq, int nkv, int hd,
                                 float eps, const float2* rope, cudaStream_t s);
 // ... and of the injected context keys of one layer in the cache
-// ([b][layer][kvh][plane][cap][hd]) at the rows of rowinfo, rope[row][hd/2].
+// ([b][layer][kvh][plane][cap][hd], kvp planes) at the rows of rowinfo,
+// rope[row][hd/2].
 template <typename T>
 cudaError_t qknorm_cache_launch(T* kc, const int2* rowinfo, int rows, int layer, int layers, int nkv, int hd, int cap,
-                                const T* g_k, float eps, const float2* rope, cudaStream_t s);
+                                int kvp, const T* g_k, float eps, const float2* rope, cudaStream_t s);
 
 // Row -> (request, position) map of an injection and the ctx_len update;
 // with `rope`, also rope[row][hd/2] = (cos, sin) of the row's position.

@@ -191,6 +191,7 @@ cudaError_t packed_attention_run(const PackedPlan& pl, int dtype_f32, const void
   ap.layer = 0;
   ap.layers = 1;
   ap.cap = pl.Sa;
+  ap.kvp = 2;   // the packed context keeps hi and lo planes
   ap.B = pl.N;
   ap.nq = pl.nq;
   ap.nkv = pl.nkv;

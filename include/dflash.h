@@ -92,6 +92,13 @@ typedef struct {
                              context K/V, instead of projecting H_t straight into every layer's K/V.
                              Changes dflash_inject_context only (multi-kernel path); drafting is the
                              same.  Not combined with qk_norm. */
+  int32_t kv_bf16;        /* bf16 models: 0 keeps every cached context K/V value as a hi and a lo bf16
+                             plane (fp32-level precision, 4 bytes a value); 1 keeps it rounded to one
+                             bf16 (2 bytes a value: for the 8B shape 20,480 bytes a token over the 5
+                             layers, the storage paper §7.3 counts).  Halves the cache and the bytes
+                             the attention reads; the logits then follow the exact definition within
+                             the bf16 rounding of the cache.  fp32 models: must be 0.  Not combined
+                             with qk_norm. */
 } dflash_config;
 
 /* Device pointers of one draft layer (borrowed).  Shapes with

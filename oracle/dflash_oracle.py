@@ -202,7 +202,7 @@ def inject_context(weights: Dict, cfg, cache: RequestCache, feats: np.ndarray, m
     storage rounding of H_t and of the cached K/V (see `store`).  With
     cfg.input_fusion the ablation path inject_context_input_fusion runs."""
     if getattr(cfg, "input_fusion", False):
-        return inject_context_input_fusion(weights, cfg, cache, feats)
+        return inject_context_input_fusion(weights, cfg, cache, feats, mode)
     h_t = fuse_context(feats, weights["w_c"], weights["g_c"], cfg.rms_eps, mode)
     c = cache.length
     pos = np.arange(c, c + h_t.shape[0])
@@ -215,7 +215,8 @@ def inject_context(weights: Dict, cfg, cache: RequestCache, feats: np.ndarray, m
     return h_t
 
 
-def inject_context_input_fusion(weights: Dict, cfg, cache: RequestCache, feats: np.ndarray) -> np.ndarray:
+def inject_context_input_fusion(weights: Dict, cfg, cache: RequestCache, feats: np.ndarray,
+                                mode="f64") -> np.ndarray:
     """The input-fusion ablation (paper §5.5.5, against KV injection; explainer
     "Per-Layer K/V Injection Prevents Context Dilution": with input fusion the
     target context enters only at the first layer).  Reading: the new context
@@ -226,7 +227,9 @@ def inject_context_input_fusion(weights: Dict, cfg, cache: RequestCache, feats: 
     Earlier context rows never see later ones, so the per-layer K/V of the
     context can be cached and extended: this function appends the new rows'
     K/V of every layer to the cache.  Drafting is unchanged (draft_forward).
-    draft_forward_full_sequence is the same computation without a cache."""
+    draft_forward_full_sequence is the same computation without a cache.
+    `mode` rounds the cached K/V (storage class "kv", see `store`) before the
+    context rows' own attention reads them, as the cache holds them."""
     h_t = fuse_context(feats, weights["w_c"], weights["g_c"], cfg.rms_eps)
     D, nq, nkv, hd = cfg.hidden, cfg.n_q_heads, cfg.n_kv_heads, cfg.head_dim
     c, n = cache.length, h_t.shape[0]
@@ -242,8 +245,8 @@ def inject_context_input_fusion(weights: Dict, cfg, cache: RequestCache, feats: 
             k = rms_norm(k, lw["g_k"], cfg.rms_eps)
         q, k = rope(q, pos, cfg.rope_theta), rope(k, pos, cfg.rope_theta)
         v = linear(u, lw["w_v"]).reshape(n, nkv, hd)
-        cache.k[i] = np.concatenate([cache.k[i], k], axis=0)
-        cache.v[i] = np.concatenate([cache.v[i], v], axis=0)
+        cache.k[i] = np.concatenate([cache.k[i], store(k, mode, "kv")], axis=0)
+        cache.v[i] = np.concatenate([cache.v[i], store(v, mode, "kv")], axis=0)
         o = attention_masked(q, cache.k[i], cache.v[i], rows)
         x = x + linear(o.reshape(n, nq * hd), lw["w_o"])
         u = rms_norm(x, lw["g_post"], cfg.rms_eps)

@@ -40,7 +40,8 @@ def main():
     ap.add_argument("--drafter", default="8b", choices=["8b", "4b"])
     ap.add_argument("--block", type=int, default=16)
     ap.add_argument("--classes", default=",".join(o.STORE_CLASSES) + ",all",
-                    help="comma-separated classes to study (all: every class at once)")
+                    help="comma-separated classes to study (all: every class at once; a+b: "
+                         "classes a and b at once)")
     args = ap.parse_args()
     cfg = QWEN3_8B if args.drafter == "8b" else QWEN3_4B
     torch.set_num_threads(max(1, torch.get_num_threads()))
@@ -49,6 +50,11 @@ def main():
     feats = make_features(cfg, args.ctx, seed=1001)
     wanted = args.classes.split(",")
     modes = [("exact", "f64")] + [(c, {c: "bf16"}) for c in o.STORE_CLASSES if c in wanted]
+    for combo in (c for c in wanted if "+" in c):
+        parts = combo.split("+")
+        if any(p not in o.STORE_CLASSES for p in parts):
+            raise SystemExit(f"unknown class in {combo}")
+        modes.append((combo, {p: "bf16" for p in parts}))
     if "all" in wanted:
         modes.append(("all", "bf16"))
     rows = {name: [] for name, _ in modes}

@@ -21,6 +21,17 @@ ARGMAX_MARGIN = 1e-2
 # definition; a change that quietly lost that precision would still pass the
 # contract bar but not this one.
 BF16_REGRESSION_TOL = 1e-3
+# A one-plane bf16 cache (kv_bf16) rounds every cached value to the nearest
+# bf16 (8 significant bits, unit roundoff 2^-8): at most 2^-8 of the value off
+# the exact definition, plus the fp32-level error of computing it.
+KV_BF16_CACHE_TOL = 2.0 ** -8 + 1e-5
+# Regression bar of a one-plane cache against the oracle whose cache is rounded
+# the same way: the GPU rounds fp32-level values, the oracle float64 ones, so
+# ~0.5 % of the cached values (those within the operands' hi/lo error of a bf16
+# rounding boundary) land one bf16 step apart, and at the 4B/8B shapes those
+# steps alone move logits by up to ~2e-3; the bar keeps a margin over that and
+# stays 4x inside the contract bar.
+KV_BF16_REGRESSION_TOL = 5e-3
 
 
 def tol(cfg: DraftConfig) -> float:
@@ -107,27 +118,43 @@ def oracle_caches(cfg: DraftConfig, batch: int) -> List[oracle.RequestCache]:
 
 
 class OracleSide:
-    """The exact float64 oracle for each request of a batch."""
+    """The exact float64 oracle for each request of a batch.  For a model whose
+    cache keeps one bf16 per value (kv_bf16) it also keeps `stored`: the same
+    oracle with its cached context K/V rounded to bf16 (the oracle's "kv"
+    storage class), the computation the GPU path performs."""
 
     def __init__(self, cfg: DraftConfig, weights_host: dict, batch: int):
         self.cfg, self.w = cfg, weights_host
         self.exact = oracle_caches(cfg, batch)
+        self.kv_mode = {"kv": "bf16"} if getattr(cfg, "kv_bf16", False) else None
+        self.stored = oracle_caches(cfg, batch) if self.kv_mode else self.exact
 
     def inject(self, b: int, feats) -> None:
         oracle.inject_context(self.w, self.cfg, self.exact[b], feats)
+        if self.kv_mode:
+            oracle.inject_context(self.w, self.cfg, self.stored[b], feats, self.kv_mode)
 
     def check_request(self, b: int, anchor: int, block: int, gpu_logits: np.ndarray, gpu_drafts: np.ndarray):
         """Assert the logits tolerance and argmax parity (drafts identical where
-        the oracle's top-2 margin exceeds 1e-2); returns the statistics."""
+        the oracle's top-2 margin exceeds 1e-2); returns the statistics.  The
+        contract bars hold against the exact oracle; the regression bar and
+        the argmax against the oracle with the model's cache precision."""
         r = oracle.draft_cycle(self.w, self.cfg, self.exact[b], None, anchor, block)
+        rs = oracle.draft_cycle(self.w, self.cfg, self.stored[b], None, anchor, block) if self.kv_mode else r
         err = row_rel_err(gpu_logits, r["logits"]) if block > 1 else 0.0
-        checked, mism, excl = argmax_check(gpu_drafts, r["logits"]) if block > 1 else (0, 0, 0)
+        err_s = row_rel_err(gpu_logits, rs["logits"]) if block > 1 else 0.0
+        checked, mism, excl = argmax_check(gpu_drafts, rs["logits"]) if block > 1 else (0, 0, 0)
         agree = int(np.sum(np.asarray(gpu_drafts).reshape(-1) == r["drafts"])) if block > 1 else 0
         distinct = len(set(np.asarray(gpu_drafts).reshape(-1).tolist())) if block > 1 else 0
         stats = dict(request=b, rel_err=err, checked=checked, mismatched=mism, excluded=excl, agree_all_rows=agree,
                      distinct_drafts=distinct)
+        if self.kv_mode:
+            _, mism_exact, _ = argmax_check(gpu_drafts, r["logits"]) if block > 1 else (0, 0, 0)
+            stats.update(rel_err_vs_stored=err_s, mismatched_vs_exact=mism_exact)
+            assert mism_exact == 0, f"drafts differ from the exact oracle: {stats}"
         assert err <= tol(self.cfg), f"logits relative error {stats}"
-        assert err <= regression_tol(self.cfg), f"logits relative error above the regression bar: {stats}"
+        bar = KV_BF16_REGRESSION_TOL if self.kv_mode else regression_tol(self.cfg)
+        assert err_s <= bar, f"logits relative error above the regression bar: {stats}"
         assert mism == 0, f"drafts differ from the oracle: {stats}"
         return stats
 
@@ -155,7 +182,8 @@ def compare_cache(g: GpuSide, caches: List[oracle.RequestCache], t: float, layer
             worst = max(worst, row_rel_err(K[b, l, :, :c, :].reshape(-1, c * ok.shape[-1]), ok.reshape(-1, c * ok.shape[-1])))
             worst = max(worst, row_rel_err(V[b, l, :, :c, :].reshape(-1, c * ov.shape[-1]), ov.reshape(-1, c * ov.shape[-1])))
     assert worst <= t, f"cache relative error {worst:.3e} > {t:.1e}"
-    assert worst <= min(t, BF16_REGRESSION_TOL), f"cache relative error {worst:.3e} above the regression bar"
+    bar = KV_BF16_CACHE_TOL if getattr(g.model.cfg, "kv_bf16", False) else BF16_REGRESSION_TOL
+    assert worst <= min(t, bar), f"cache relative error {worst:.3e} above the regression bar {bar:.2e}"
     return worst
 
 

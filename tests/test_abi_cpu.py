@@ -60,11 +60,14 @@ def test_cache_bytes_follow_the_documented_layout(L):
     kv8 = 4 * 3 * 2 * 2 * 104 * 64
     assert L.dflash_cache_bytes(ctypes.byref(c16), 3, 100) == a(kv) + a(kv8) + a(4 * 3)
     assert L.dflash_cache_bytes(ctypes.byref(c16), 3, 104) == 2 * a(kv8) + a(4 * 3)
+    c1 = _cfg(dtype=1, kv_bf16=1)   # one rounded bf16 per value: half the K/V bytes
+    assert L.dflash_cache_bytes(ctypes.byref(c1), 3, 100) == a(kv // 2) + a(kv8 // 2) + a(4 * 3)
 
 
 @pytest.mark.parametrize("bad", [dict(hidden=200), dict(head_dim=96), dict(n_kv_heads=3), dict(ffn=100),
                                  dict(vocab=1000), dict(max_block=33), dict(max_block=0), dict(dtype=5),
-                                 dict(mask_token_id=1024), dict(layers=0), dict(n_target_feats=0)])
+                                 dict(mask_token_id=1024), dict(layers=0), dict(n_target_feats=0),
+                                 dict(kv_bf16=1), dict(dtype=1, kv_bf16=2)])
 def test_bad_configs_are_rejected_on_the_host(L, bad):
     c = _cfg(**bad)
     assert L.dflash_cache_bytes(ctypes.byref(c), 1, 16) == 0
@@ -100,3 +103,14 @@ def test_product_path_has_no_oracle_or_cpu_fallback():
             if f.endswith((".py", ".cu", ".cuh", ".h", ".cpp")):
                 text = open(os.path.join(dirpath, f)).read()
                 assert "import oracle" not in text and "from oracle" not in text, f
+
+
+def test_one_plane_cache_is_20480_bytes_a_token_at_the_8b_shape(L):
+    from block_diffusion_drafter_dflash_gb300 import _config_struct
+    from dflash_inputs import QWEN3_8B, replace
+    cap = 32768 + 512
+    two = L.dflash_cache_bytes(ctypes.byref(_config_struct(QWEN3_8B)), 4, cap)
+    one = L.dflash_cache_bytes(ctypes.byref(_config_struct(replace(QWEN3_8B, kv_bf16=True))), 4, cap)
+    assert abs(two - 2 * one) < 4096
+    # 5 layers x 8 kv heads x 128 x (K and V) x 2 bytes = 20,480 bytes a token
+    assert abs(one - 4 * cap * 20480) < 4096

@@ -754,6 +754,29 @@ def test_input_fusion_with_zero_output_projections_gives_the_injected_cache():
     assert np.max(np.abs(c2.k[1] - caches[0].k[1])) > 1e-3
 
 
+def test_input_fusion_cache_storage_rounding():
+    """With the cached K/V stored in bf16 (storage class "kv"), the input-fusion
+    path caches what the exact path computes, rounded: layer 0's context K/V
+    (which depend on nothing cached) are exactly the rounded exact values,
+    every cached value is a bf16, and deeper layers read the rounded cache
+    (so they differ from merely rounding the exact deeper layers)."""
+    cfg = replace(TINY, layers=2, input_fusion=True)
+    w = oracle.weights_to_numpy(make_weights(cfg, 12))
+    feats = make_features(cfg, 14, seed=13).float().numpy()
+    ex = oracle.RequestCache(cfg.layers, cfg.n_kv_heads, cfg.head_dim)
+    st = oracle.RequestCache(cfg.layers, cfg.n_kv_heads, cfg.head_dim)
+    for s0, s1 in [(0, 9), (9, 14)]:
+        oracle.inject_context(w, cfg, ex, feats[s0:s1])
+        oracle.inject_context(w, cfg, st, feats[s0:s1], {"kv": "bf16"})
+    for i in range(cfg.layers):
+        for a in (st.k[i], st.v[i]):
+            np.testing.assert_array_equal(a, oracle.store(a, "bf16"))
+    np.testing.assert_array_equal(st.k[0], oracle.store(ex.k[0], "bf16"))
+    np.testing.assert_array_equal(st.v[0], oracle.store(ex.v[0], "bf16"))
+    assert not np.array_equal(st.k[1], oracle.store(ex.k[1], "bf16"))
+    assert np.max(np.abs(st.k[1] - ex.k[1]) / np.max(np.abs(ex.k[1]))) < 2.0 ** -7
+
+
 def test_input_fusion_context_rows_are_causal():
     """A later context token never changes an earlier one's cached K/V."""
     cfg = replace(TINY, layers=2, input_fusion=True)
