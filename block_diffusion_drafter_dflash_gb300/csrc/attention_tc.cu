@@ -91,7 +91,7 @@ __global__ void __launch_bounds__(kSplitThreads, 1) attn_tc_split_kernel(const _
       for (int j = 0; j < 32; j += 4) *reinterpret_cast<float4*>(dst + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
     };
     auto done = [&](int r, float m_log2, float l) { p.ml[prow(r)] = make_float2(m_log2 * kLn2, l); };
-    ok = attn_tc::run<HD, kSplitThreads>(p, maps, b, kvh, pass, t0, t1, nct, sm, tmem, bars, uses, tid, CtaSync{},
+    ok = attn_tc::run<HD, kSplitThreads>(p, maps, b, kvh, pass, t0, t1, nct, c, sm, tmem, bars, uses, tid, CtaSync{},
                                          status, out, done, xch);
   }
   ptx::tc_fence_before();

@@ -115,13 +115,20 @@ __device__ __forceinline__ void split8(const float* v, uint4& hi, uint4& lo) {
 // Q rows [64*pass, 64*pass+64) of group (b, kvh) into the A tiles, scaled into
 // the log2 domain; rows past the group's rows are zero.  NT threads (128 or
 // 256), each with 64*HD/(8*NT) chunks of 8 values: every load is issued before
-// the first store, so the whole tile costs one memory round trip.
+// the first store, so the whole tile costs one memory round trip.  In two
+// halves: stage_q_load issues the loads, stage_q_store converts and stores, so
+// that other work can be issued while the loads are in flight.
 template <int HD, int NT>
-__device__ void stage_q(const AttnParams& p, int b, int kvh, int pass, uint8_t* sm, int tid) {
-  constexpr int kPer = 64 * (HD / 8) / NT;   // 8-value chunks per thread
-  const int G = p.nq / p.nkv, rows = G * p.block;
-  const float qscale = p.scale * kLog2e;
+struct QRegs {
+  static constexpr int kPer = 64 * (HD / 8) / NT;   // 8-value chunks per thread
   float4 x[kPer][2];
+};
+
+template <int HD, int NT>
+__device__ __forceinline__ void stage_q_load(const AttnParams& p, int b, int kvh, int pass, int tid, QRegs<HD, NT>& qr) {
+  constexpr int kPer = QRegs<HD, NT>::kPer;
+  const int G = p.nq / p.nkv, rows = G * p.block;
+  float4(&x)[kPer][2] = qr.x;
   // thread tid's chunks lie in rows r0, r0 + kRowStep, ...: (head, block
   // position) of each follows from the previous one without a division
   constexpr int kRowStep = NT / (HD / 8);
@@ -145,6 +152,13 @@ __device__ void stage_q(const AttnParams& p, int b, int kvh, int pass, uint8_t* 
       x[u][0] = x[u][1] = make_float4(0.f, 0.f, 0.f, 0.f);
     }
   }
+}
+
+template <int HD, int NT>
+__device__ __forceinline__ void stage_q_store(const AttnParams& p, uint8_t* sm, int tid, const QRegs<HD, NT>& qr) {
+  constexpr int kPer = QRegs<HD, NT>::kPer;
+  const float qscale = p.scale * kLog2e;
+  const float4(&x)[kPer][2] = qr.x;
 #pragma unroll
   for (int u = 0; u < kPer; ++u) {
     const int e = tid + NT * u, i = e / (HD / 8), c8 = e - i * (HD / 8), s = c8 >> 3, ch = c8 & 7;
@@ -160,6 +174,14 @@ __device__ void stage_q(const AttnParams& p, int b, int kvh, int pass, uint8_t* 
 
 // Planes of tile t: the cache's for a context tile, two for the block tile.
 __device__ __forceinline__ int tile_planes(const AttnParams& p, int t, int nct) { return t < nct ? p.kvp : 2; }
+
+// Warm the descriptor cache for the attention's tensor maps (one thread).
+__device__ __forceinline__ void prefetch_maps(const Maps& m) {
+  ptx::prefetch_tmap(&m.kc);
+  ptx::prefetch_tmap(&m.vc);
+  ptx::prefetch_tmap(&m.kb);
+  ptx::prefetch_tmap(&m.vb);
+}
 
 // TMA of tile t of group (b, kvh) of layer p.layer: context keys [128t, 128t+128)
 // for t < nct, else the block's keys.  Issued by one thread.
@@ -204,7 +226,7 @@ __device__ void load_v(const AttnParams& p, const Maps& m, int b, int kvh, int t
 }
 
 // One item: query rows of pass `pass` of group (b, kvh) against tiles [t0, t1)
-// (nct context tiles, then the block tile).  NT participating threads (tid
+// (nct context tiles of the c context keys, then the block tile).  NT participating threads (tid
 // 0..NT-1).  Warp w reads TMEM lanes 32(w%4)..32(w%4)+31, which must be its
 // own lane quarter.  With NT = 256 the two warps of a lane quarter split the
 // work of their 16 query rows: warp w < 4 takes keys 0..31 and 64..95 of every
@@ -218,7 +240,7 @@ __device__ void load_v(const AttnParams& p, const Maps& m, int b, int kvh, int t
 // ready, [2] the last P V done, [3] output written, [4] the first V tile in
 // shared memory, [5] the first P tile stored.  Returns false on a timeout.
 template <int HD, int NT, class Sync, class Out, class Done>
-__device__ bool run(const AttnParams& p, const Maps& m, int b, int kvh, int pass, int t0, int t1, int nct,
+__device__ bool run(const AttnParams& p, const Maps& m, int b, int kvh, int pass, int t0, int t1, int nct, int c,
                     uint8_t* sm, uint32_t tmem, Bars* bars, int& uses, int tid, Sync sync, int32_t* status, Out out,
                     Done done, float* xch = nullptr, unsigned long long* stamps = nullptr) {
   static_assert(NT == 128 || NT == 256, "128 or 256 threads");
@@ -228,7 +250,6 @@ __device__ bool run(const AttnParams& p, const Maps& m, int b, int kvh, int pass
   constexpr int DC = HD / NP;         // output columns one warp reads back
   const int lane = tid & 31, w = tid >> 5, q4 = w & 3, part = w >> 2;
   const int G = p.nq / p.nkv, rows = G * p.block;
-  const int c = p.ctx_len[b];
   const uint32_t lanes = static_cast<uint32_t>(q4 * 32) << 16;
   const uint32_t tS = tmem + lanes, tO = tmem + lanes + 2 * kKeys;   // this warp's lanes
   const uint32_t idS2 = ptx::idesc_bf16_f32(128, 2 * kKeys), idO2 = ptx::idesc_bf16_f32(128, 2 * HD);
@@ -239,10 +260,14 @@ __device__ bool run(const AttnParams& p, const Maps& m, int b, int kvh, int pass
   const int i = 16 * q4 + (lane & 15);   // query row of the pass held by this lane (hi part if lane < 16)
   bool ok = true;
 
-  // the first tile's K now; its V once the scores are issued (it is needed
-  // only after the softmax, and the Q loads need not queue behind it)
-  if (tid == 0 && t0 < t1) load_k<HD>(p, m, b, kvh, t0, nct, sm, bars);
-  stage_q<HD, NT>(p, b, kvh, pass, sm, tid);
+  // the first tile's K while the Q loads are in flight; its V once the
+  // scores are issued (it is needed only after the softmax)
+  {
+    QRegs<HD, NT> qr;
+    stage_q_load<HD, NT>(p, b, kvh, pass, tid, qr);
+    if (tid == 0 && t0 < t1) load_k<HD>(p, m, b, kvh, t0, nct, sm, bars);
+    stage_q_store<HD, NT>(p, sm, tid, qr);
+  }
   ptx::fence_proxy_async_shared();
   sync();
   if (stamps && tid == 0) stamps[0] = ptx::globaltimer();

@@ -102,6 +102,7 @@ struct PBook {
   int flag_acc, flag_tk, flag_bar;
   uint64_t ring_free;   // attention is done with the ring (one phase per attention phase)
   attn_tc::Bars abars;  // the attention's TMA and MMA barriers
+  int ctx_len[kPRows];  // context length of every request (constant during the launch)
   float rs[kPRows];
 };
 
@@ -215,15 +216,16 @@ __device__ __forceinline__ int box_row(const GemmSeg& sg, int tis, int h) {
 // Attention work item of CTA `cta`: (request b, kv head, chunk of key tiles
 // [t0, t1)) of nct context tiles and one block tile; false if it has none.
 struct AttnItem {
-  int b, kvh, t0, t1, nct;
+  int b, kvh, t0, t1, nct, c;
 };
-__device__ __forceinline__ bool attn_item(const AttnParams& ap, int cta, AttnItem& it) {
+__device__ __forceinline__ bool attn_item(const AttnParams& ap, const int* ctx_len, int cta, AttnItem& it) {
   const int nch = ap.splits;
   if (cta >= ap.B * ap.nkv * nch) return false;
   const int r = cta % (ap.nkv * nch), ch = r % nch;
   it.b = cta / (ap.nkv * nch);
   it.kvh = r / nch;
-  it.nct = (ap.ctx_len[it.b] + attn_tc::kKeys - 1) / attn_tc::kKeys;
+  it.c = ctx_len[it.b];
+  it.nct = (it.c + attn_tc::kKeys - 1) / attn_tc::kKeys;
   const int T = it.nct + 1;
   it.t0 = ch * T / nch;
   it.t1 = (ch + 1) * T / nch;
@@ -708,7 +710,7 @@ __device__ bool attn_phase(const PParams& p, const PPhase& ph, int pi, PBook* bk
                            int ct, int& uses) {
   const AttnParams& ap = p.attn;
   AttnItem item;
-  if (!attn_item(ap, cta, item)) return true;
+  if (!attn_item(ap, bk->ctx_len, cta, item)) return true;
   const int b = item.b, kvh = item.kvh, t0 = item.t0, t1 = item.t1, nct = item.nct;
   const int rows = (ap.nq / ap.nkv) * ap.block;
   float* op = ap.opart + (size_t)cta * kPAttnRows * HD;
@@ -728,7 +730,7 @@ __device__ bool attn_phase(const PParams& p, const PPhase& ph, int pi, PBook* bk
   auto done = [&](int row, float m_log2, float l) { ml[row] = make_float2(m_log2, l); };
   // trace slots kTrAcc..kTrRed of an attention phase: the core's stamps
   unsigned long long* stamps = p.trace ? p.trace + ((size_t)cta * kPMaxPhases + pi) * kTrSlots + kTrAcc : nullptr;
-  const bool ok = attn_tc::run<HD, 128>(a, p.amaps, b, kvh, 0, t0, t1, nct, sm, tmem, &bk->abars, uses, ct,
+  const bool ok = attn_tc::run<HD, 128>(a, p.amaps, b, kvh, 0, t0, t1, nct, item.c, sm, tmem, &bk->abars, uses, ct,
                                         ComputeSync{}, p.status, out, done, nullptr, stamps);
   if (ct == 0) trace_at(p, cta, pi, kTrM1);
   return ok;
@@ -802,9 +804,15 @@ __device__ void compute_warps(const PParams& p, PBook* bk, uint8_t* ring, uint8_
   const int ct = threadIdx.x - 128;
   float* st = reinterpret_cast<float*>(region);
   int seq = 0, attn_uses = 0;
+  // the requests' context lengths, read once (nothing in the launch changes them)
+  if (p.attn.ctx_len)
+    for (int i = ct; i < p.attn.B && i < kPRows; i += 128) bk->ctx_len[i] = p.attn.ctx_len[i];
+  csync();
   for (int pi = 0; pi < p.nphase; ++pi) {
     const PPhase& ph = p.ph[pi];
     if (ct == 0) trace_at(p, cta, pi, kTrStart);
+    // the next phase's attention: its tensor maps into the descriptor cache now
+    if (ct == 0 && pi + 1 < p.nphase && p.ph[pi + 1].kind == kPhAttn) attn_tc::prefetch_maps(p.amaps);
     if (ph.kind == kPhGemm) {
       if (!gemm_phase(p, ph, pi, bk, st, tmem, G, cta, ct, seq)) return;
     } else if (ph.kind == kPhAttn) {
