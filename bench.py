@@ -52,6 +52,8 @@ def parse():
                     help="run and print only this sub-benchmark (1 GPU)")
     ap.add_argument("--kv-bf16", action="store_true",
                     help="the context cache keeps one bf16 per value (else a hi and a lo bf16 plane)")
+    ap.add_argument("--head-bf16", action="store_true",
+                    help="the LM head reads the final normed state as one bf16 (multi-kernel path)")
     return ap.parse_args()
 
 
@@ -446,6 +448,8 @@ def measure(wl, W, K, rank, world, local, barrier, want_e2e=True):
                    "ctx": wl.ctx if len(wl.ctx) <= 4 else f"{min(wl.ctx)}..{max(wl.ctx)} ({len(wl.ctx)} requests)",
                    "kv_cache": ("one bf16 per value" if getattr(wl.cfg, "kv_bf16", False)
                                 else "hi and lo bf16 planes per value (fp32-level)"),
+                   "lm_head_input": ("one bf16" if getattr(wl.cfg, "head_bf16", False)
+                                     else "hi and lo bf16 planes"),
                    "l2": "inputs larger than L2 (weights streamed every cycle)",
                    "timing": "CUDA-graph replay of whole cycles (inject, draft, synthetic target, verify); "
                              "per-stage times from an eager pass with events",
@@ -539,10 +543,11 @@ def measure_packed_attention(K: int, W: int = 3) -> dict:
 
 
 def workload_for(args, name: str):
-    """The named workload, with the one-plane bf16 cache under --kv-bf16."""
+    """The named workload, with the one-bf16 options of --kv-bf16 / --head-bf16."""
     wl = workloads()[name]
-    if getattr(args, "kv_bf16", False):
-        wl = dataclasses.replace(wl, cfg=dataclasses.replace(wl.cfg, kv_bf16=True))
+    opts = {k: True for k in ("kv_bf16", "head_bf16") if getattr(args, k, False)}
+    if opts:
+        wl = dataclasses.replace(wl, cfg=dataclasses.replace(wl.cfg, **opts))
     return wl
 
 

@@ -49,7 +49,8 @@ def _config_struct(cfg) -> _abi.Config:
                        mask_token_id=int(mask), dtype=_abi.DTYPE_F32 if cfg.dtype == "fp32" else _abi.DTYPE_BF16,
                        qk_norm=1 if getattr(cfg, "qk_norm", False) else 0,
                        input_fusion=1 if getattr(cfg, "input_fusion", False) else 0,
-                       kv_bf16=1 if getattr(cfg, "kv_bf16", False) else 0)
+                       kv_bf16=1 if getattr(cfg, "kv_bf16", False) else 0,
+                       head_bf16=1 if getattr(cfg, "head_bf16", False) else 0)
 
 
 def dflash_version() -> int:

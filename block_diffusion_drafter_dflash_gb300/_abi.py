@@ -30,7 +30,7 @@ class Config(ctypes.Structure):
                 ("head_dim", c_i32), ("ffn", c_i32), ("vocab", c_i32), ("n_target_feats", c_i32),
                 ("max_block", c_i32), ("rope_theta", ctypes.c_float), ("rms_eps", ctypes.c_float),
                 ("mask_token_id", c_i32), ("dtype", c_i32), ("qk_norm", c_i32), ("input_fusion", c_i32),
-                ("kv_bf16", c_i32)]
+                ("kv_bf16", c_i32), ("head_bf16", c_i32)]
 
 
 class LayerWeights(ctypes.Structure):

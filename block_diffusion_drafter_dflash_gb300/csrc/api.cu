@@ -127,6 +127,9 @@ size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
 int pad8(int n) { return (n + 7) & ~7; }
 // bf16 planes of every cached context K/V value: hi and lo, or one rounded value
 int kv_planes(const dflash_config& c) { return c.kv_bf16 ? 1 : 2; }
+// operand planes the LM head reads: 1 with head_bf16 (the hi plane of the pair
+// the final norm writes is the value rounded to nearest bf16)
+int head_planes(const dflash_config& c) { return c.dtype == DFLASH_DTYPE_F32 ? 1 : (c.head_bf16 ? 1 : 2); }
 // planes of the cache of a T model (an fp32 cache is one fp32 plane)
 template <typename T> int cache_planes(const dflash_config& c) { return ActPlanes<T>::n == 2 ? kv_planes(c) : 1; }
 
@@ -157,6 +160,9 @@ int32_t check_config(const dflash_config* c) {
   if (c->kv_bf16 != 0 && c->kv_bf16 != 1) return fail(DFLASH_ERR_INVALID_ARG, "kv_bf16 %d must be 0 or 1", c->kv_bf16);
   if (c->kv_bf16 && c->dtype != DFLASH_DTYPE_BF16) return fail(DFLASH_ERR_INVALID_ARG, "kv_bf16 needs a bf16 model");
   if (c->kv_bf16 && c->qk_norm) return fail(DFLASH_ERR_UNSUPPORTED, "kv_bf16 with qk_norm is not built");
+  if (c->head_bf16 != 0 && c->head_bf16 != 1)
+    return fail(DFLASH_ERR_INVALID_ARG, "head_bf16 %d must be 0 or 1", c->head_bf16);
+  if (c->head_bf16 && c->dtype != DFLASH_DTYPE_BF16) return fail(DFLASH_ERR_INVALID_ARG, "head_bf16 needs a bf16 model");
   return DFLASH_OK;
 }
 
@@ -190,7 +196,7 @@ struct WsPlan {
 // attention groups fit 64 query rows.
 bool persist_draft_ok(const dflash_model* m, int B, int block) {
   const dflash_config& c = m->cfg;
-  return m->persist && !c.qk_norm && B * block <= kPRows && (c.n_q_heads / c.n_kv_heads) * block <= kPAttnRows &&
+  return m->persist && !c.qk_norm && !c.head_bf16 && B * block <= kPRows && (c.n_q_heads / c.n_kv_heads) * block <= kPAttnRows &&
          6 * c.layers + 1 <= kPMaxPhases && c.ffn % kTileN == 0;
 }
 // A whole cycle in one launch: fusion and injection phases before the drafter's
@@ -272,7 +278,7 @@ WsPlan plan_ws(const dflash_model* m, int B, int cap, int block, int max_rows) {
     p.g_o = plan_gemm(c.dtype, R, hq, D / kTileN, m->sms, m->use_tc, pl);
     p.g_gu = plan_gemm(c.dtype, R, D, F / kHalfN, m->sms, m->use_tc, pl);
     p.g_down = plan_gemm(c.dtype, R, F, D / kTileN, m->sms, m->use_tc, pl);
-    p.g_lm = plan_gemm(c.dtype, std::max(Rm, 1), D, c.vocab / kTileN, m->sms, m->use_tc, pl);
+    p.g_lm = plan_gemm(c.dtype, std::max(Rm, 1), D, c.vocab / kTileN, m->sms, m->use_tc, head_planes(c));
     used.insert(used.end(), {&p.g_qkv, &p.g_o, &p.g_gu, &p.g_down, &p.g_lm});
   }
   size_t partial = 0;
@@ -576,7 +582,7 @@ int32_t run_draft(const dflash_model* m, const dflash_cache* cache, const int32_
             final_norm_launch<T>(x, static_cast<const T*>(m->g_final), c.rms_eps, B, block, D, hm, (size_t)Rm * D, slots,
                                  s),
             "final norm");
-  GemmProblem plm = make_problem(m, hm, D, Rm, D, pl, (size_t)Rm * D);
+  GemmProblem plm = make_problem(m, hm, D, Rm, D, head_planes(c), (size_t)Rm * D);
   add_seg(plm, m->lm_head, kMapLm, m->lm_head, kMapLm, c.vocab / kTileN, 0, 0);
   apply_plan(plm, P.g_lm, partial, counters);
   DF_LAUNCH(DFLASH_STAGE_LMHEAD, 1, (gemm_launch<T, EpiArgmax>(plm, P.g_lm, EpiArgmax{slots, logits, c.vocab}, s)),

@@ -332,7 +332,7 @@ struct DenseCfg {
   using C = TcCfg<BN, PL>;
   static constexpr int kLd = C::kChunk + 1;
   static constexpr int kStBytes = kTileN * kLd * 4;   // epilogue staging tile
-  static size_t smem(int stages) {
+  static constexpr size_t smem(int stages) {
     return 1024 + (size_t)stages * C::kStageBytes + kStBytes + 8 * (2 * kMaxStages + 5) + 16;
   }
 };
@@ -533,27 +533,34 @@ cudaError_t launch_bn(const GemmProblem& p, const GemmPlan& plan, const Epi& epi
   return launch_pdl(gemm_tc_kernel<BN, PL, Epi>, grid, dim3(128), C::smem(p.stages), s, xmap, p, epi, p.status);
 }
 
-template <class Epi>
-cudaError_t launch_dense(const GemmProblem& p, const GemmPlan& plan, const Epi& epi, cudaStream_t s) {
-  using D = DenseCfg<128, 2>;
+template <int BN, int PL, class Epi>
+cudaError_t launch_dense_cfg(const GemmProblem& p, const GemmPlan& plan, const Epi& epi, cudaStream_t s) {
+  using D = DenseCfg<BN, PL>;
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_dense_kernel<128, 2, Epi>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(gemm_dense_kernel<BN, PL, Epi>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)D::smem(4));
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  if (p.stages != 4 || plan.smem != D::smem(4) || p.planes != 2 || p.plane_stride % p.ldx || p.K % 64)
+  if (p.stages != 4 || plan.smem != D::smem(4) || p.planes != PL || plan.bm != BN || (PL == 2 && p.plane_stride % p.ldx) ||
+      p.K % 64)
     return cudaErrorInvalidValue;
-  const int rows = static_cast<int>(p.plane_stride / p.ldx) + p.M;
+  const int rows = PL == 1 ? p.M : static_cast<int>(p.plane_stride / p.ldx) + p.M;
   CUtensorMap xmap;
-  if (!encode_activation_map(&xmap, p.x, p.K, rows, p.ldx, 128)) return cudaErrorInvalidValue;
+  if (!encode_activation_map(&xmap, p.x, p.K, rows, p.ldx, BN)) return cudaErrorInvalidValue;
   static const bool log = debug_env("DFLASH_GEMM_LOG") != nullptr;
   if (log)
-    std::fprintf(stderr, "gemm_dense M=%d K=%d tiles=%d token_tiles=%d grid=%d\n", p.M, p.K, p.total_tiles,
-                 plan.token_tiles, plan.grid);
-  return launch_pdl(gemm_dense_kernel<128, 2, Epi>, dim3(plan.grid), dim3(kDenseThreads), D::smem(4), s, xmap, p,
+    std::fprintf(stderr, "gemm_dense M=%d K=%d tiles=%d BN=%d PL=%d token_tiles=%d grid=%d\n", p.M, p.K,
+                 p.total_tiles, BN, PL, plan.token_tiles, plan.grid);
+  return launch_pdl(gemm_dense_kernel<BN, PL, Epi>, dim3(plan.grid), dim3(kDenseThreads), D::smem(4), s, xmap, p,
                     epi, plan.token_tiles, p.status);
+}
+
+template <class Epi>
+cudaError_t launch_dense(const GemmProblem& p, const GemmPlan& plan, const Epi& epi, cudaStream_t s) {
+  static_assert(DenseCfg<128, 2>::smem(4) == DenseCfg<256, 1>::smem(4), "one plan size for both shapes");
+  return p.planes == 2 ? launch_dense_cfg<128, 2, Epi>(p, plan, epi, s) : launch_dense_cfg<256, 1, Epi>(p, plan, epi, s);
 }
 
 }  // namespace
@@ -613,7 +620,9 @@ GemmPlan plan_gemm_tc(int M, int K, int tiles, int sms, int planes) {
   g.token_tiles = (M + g.bm - 1) / g.bm;
   static const int env_dense = env_int("DFLASH_DENSE", 1, false);   // 0: never the persistent many-row kernel
   const long dense_tiles = (long)tiles * g.token_tiles;
-  if (env_dense && planes == 2 && g.bm == 128 && g.token_tiles >= 2 && 4 * dense_tiles >= 3L * sms) {
+  // (both shapes have MMA N = 256: 128 rows of a hi/lo pair, or 256 one-plane rows)
+  if (env_dense && ((planes == 2 && g.bm == 128) || (planes == 1 && g.bm == 256)) && g.token_tiles >= 2 &&
+      4 * dense_tiles >= 3L * sms) {
     // tensor-bound: a persistent kernel with every tile's whole K (no split-K
     // reduction) and the epilogue overlapped with the next tile's MMAs
     g.dense = 1;

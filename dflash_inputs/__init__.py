@@ -41,6 +41,7 @@ class DraftConfig:
     qk_norm: bool = False  # per-head RMSNorm of queries and keys before RoPE (Qwen3's q_norm / k_norm)
     input_fusion: bool = False  # ablation: the fused context enters once, at the input, instead of every layer's K/V
     kv_bf16: bool = False  # bf16 models: the context K/V cache holds one bf16 per value (else a hi/lo pair)
+    head_bf16: bool = False  # bf16 models: the LM head reads the final normed state as one bf16 (else a hi/lo pair)
 
     @property
     def mask_id(self) -> int:

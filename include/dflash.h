@@ -99,6 +99,11 @@ typedef struct {
                              the attention reads; the logits then follow the exact definition within
                              the bf16 rounding of the cache.  fp32 models: must be 0.  Not combined
                              with qk_norm. */
+  int32_t head_bf16;      /* bf16 models: 1 hands the final normed hidden state to the LM head as one
+                             bf16 (rounded to nearest) instead of a hi/lo pair, so the 151,936-wide
+                             head projection runs at twice the tensor rate at batch scale; every other
+                             tensor keeps fp32-level precision.  Models with it run the multi-kernel
+                             path.  fp32 models: must be 0. */
 } dflash_config;
 
 /* Device pointers of one draft layer (borrowed).  Shapes with

@@ -67,7 +67,8 @@ def test_cache_bytes_follow_the_documented_layout(L):
 @pytest.mark.parametrize("bad", [dict(hidden=200), dict(head_dim=96), dict(n_kv_heads=3), dict(ffn=100),
                                  dict(vocab=1000), dict(max_block=33), dict(max_block=0), dict(dtype=5),
                                  dict(mask_token_id=1024), dict(layers=0), dict(n_target_feats=0),
-                                 dict(kv_bf16=1), dict(dtype=1, kv_bf16=2)])
+                                 dict(kv_bf16=1), dict(dtype=1, kv_bf16=2), dict(head_bf16=1),
+                                 dict(dtype=1, head_bf16=2)])
 def test_bad_configs_are_rejected_on_the_host(L, bad):
     c = _cfg(**bad)
     assert L.dflash_cache_bytes(ctypes.byref(c), 1, 16) == 0
