@@ -575,6 +575,14 @@ def run_gpu(args, rank, world, local):
         result["bs32"] = {k: r32[k] for k in ("value", "unit", "ms_per_step", "steps", "warmup", "config",
                                                "roofline", "stages", "gpu_launches", "clocks")}
         torch.cuda.empty_cache()
+        # the same batch-32 cycle with the bf16 storage options (one-bf16 cache
+        # and LM-head input: the precision the method itself states)
+        opts = argparse.Namespace(kv_bf16=True, head_bf16=True)
+        r32b, c32b = measure(workload_for(opts, "8b_bs32"), 3, min(args.steps, 20), rank, world, local, barrier, False)
+        del c32b
+        result["bs32_bf16_storage"] = {k: r32b[k] for k in ("value", "unit", "ms_per_step", "steps", "warmup", "config",
+                                                             "roofline", "stages", "gpu_launches", "clocks")}
+        torch.cuda.empty_cache()
         result["verify_sampled"] = measure_sampled_verify(min(args.steps, 50))
         torch.cuda.empty_cache()
         result["packed_attention"] = measure_packed_attention(min(args.steps, 20))

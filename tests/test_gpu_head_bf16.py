@@ -88,3 +88,9 @@ def test_head_bf16_8b_batch_32_sampled_requests():
     # 480 mask rows: the LM head runs the dense GEMM with 256-row one-plane tiles
     ctx = [160 + 37 * b for b in range(32)]
     _cycles(_head(QWEN3_8B), ctx=ctx, block=16, seed=820, cycles=1, check=[0, 31])
+
+
+def test_head_bf16_with_the_one_plane_cache_4b_batch_4():
+    # both one-bf16 options at once (the oracle rounds the kv and h classes)
+    cfg = replace(_head(QWEN3_4B), name="qwen3-4b-shaped-head-kv-bf16", kv_bf16=True)
+    _cycles(cfg, ctx=[300, 1000, 77, 512], block=10, seed=830)
