@@ -190,6 +190,7 @@ struct WsPlan {
   int fused;   // one persistent launch runs the injection and the drafter pass
   size_t ssq, ssq2, aml, tickets;
   int ntickets, nch;
+  int ngcnt;   // persistent drafter: per (layer, request, kv head) attention chunk counters after the barrier
 };
 
 // The persistent path serves bf16 calls of at most 16 token rows whose
@@ -197,13 +198,13 @@ struct WsPlan {
 bool persist_draft_ok(const dflash_model* m, int B, int block) {
   const dflash_config& c = m->cfg;
   return m->persist && !c.qk_norm && !c.head_bf16 && B * block <= kPRows && (c.n_q_heads / c.n_kv_heads) * block <= kPAttnRows &&
-         6 * c.layers + 1 <= kPMaxPhases && c.ffn % kTileN == 0;
+         5 * c.layers + 1 <= kPMaxPhases && c.ffn % kTileN == 0;
 }
 // A whole cycle in one launch: fusion and injection phases before the drafter's
-// (6 layers' worth of phases + 3; segments: 6 a layer, 2 a layer for the
-// injection, the fusion and the LM head).
+// (5 phases a layer + 3; segments: 6 a layer, 2 a layer for the injection, the
+// fusion and the LM head).
 bool persist_cycle_ok(const dflash_model* m) {
-  return 6 * m->cfg.layers + 3 <= kPMaxPhases && 8 * m->cfg.layers + 2 <= kPMaxSeg;
+  return 5 * m->cfg.layers + 3 <= kPMaxPhases && 8 * m->cfg.layers + 2 <= kPMaxSeg;
 }
 bool persist_inject_ok(const dflash_model* m, int max_rows) {
   return m->persist && !m->cfg.qk_norm && !m->cfg.input_fusion && max_rows <= kPRows && 1 + 2 * m->cfg.layers <= kPMaxSeg;
@@ -255,7 +256,9 @@ WsPlan plan_ws(const dflash_model* m, int B, int cap, int block, int max_rows) {
     }
     p.ssq = take(sizeof(float) * (size_t)(D / kTileN) * kPRows);
     p.partial = take(sizeof(float) * (size_t)m->sms * 2 * kPRows * 256);
-    p.tickets = take(sizeof(int) * (size_t)(p.ntickets + 1));   // tickets, then the barrier counter
+    p.ngcnt = block > 0 ? c.layers * B * c.n_kv_heads : 0;
+    // tickets, then the barrier counter, then the attention chunk counters
+    p.tickets = take(sizeof(int) * (size_t)(p.ntickets + 1 + p.ngcnt));
     p.total = off;
     return p;
   }
@@ -726,7 +729,7 @@ int32_t run_draft_persist(const dflash_model* m, const dflash_cache* cache, cons
     DF_LAUNCH(DFLASH_STAGE_OTHER, 1,
               inject_prep_launch(n_new, reinterpret_cast<int32_t*>(cache->base + cache->len_off), B, inj_rows,
                                  cache->cap, reinterpret_cast<int2*>(ws + P.rowinfo),
-                                 reinterpret_cast<int*>(ws + P.tickets), P.ntickets + 1, m->status_dev, s,
+                                 reinterpret_cast<int*>(ws + P.tickets), P.ntickets + 1 + P.ngcnt, m->status_dev, s,
                                  m->inv_freq_dev, c.head_dim, reinterpret_cast<float2*>(ws + P.rope_c)),
               "inject_prep");
   }
@@ -743,7 +746,8 @@ int32_t run_draft_persist(const dflash_model* m, const dflash_cache* cache, cons
   DF_LAUNCH(DFLASH_STAGE_OTHER, 1,
             persist_draft_prep_launch(static_cast<const __nv_bfloat16*>(m->embed), anchor, c.mask_token_id, c.vocab,
                                       B, block, D, static_cast<const __nv_bfloat16*>(m->layers[0].g_in), x, u,
-                                      (size_t)kPRows * D, ssq, slots, tickets, P.ntickets + 1, m->status_dev, ctx_len,
+                                      (size_t)kPRows * D, ssq, slots, tickets, P.ntickets + 1 + P.ngcnt, m->status_dev,
+                                      ctx_len,
                                       m->inv_freq_dev, c.head_dim, rope, s),
             "embedding");
   PParams pp{};
@@ -767,6 +771,7 @@ int32_t run_draft_persist(const dflash_model* m, const dflash_cache* cache, cons
   pp.partial = reinterpret_cast<float*>(ws + P.partial);
   pp.tickets = tickets;
   pp.bar = reinterpret_cast<unsigned int*>(tickets + P.ntickets);
+  pp.gcnt = tickets + P.ntickets + 1;
   pp.status = m->status_dev;
   float* q = reinterpret_cast<float*>(ws + P.q);
   __nv_bfloat16* kb = reinterpret_cast<__nv_bfloat16*>(ws + P.kb);
@@ -836,7 +841,6 @@ int32_t run_draft_persist(const dflash_model* m, const dflash_cache* cache, cons
     pb.seg(layer_map(l, kMapK), layer_map(l, kMapK), hk, 0, 1);
     pb.seg(layer_map(l, kMapV), layer_map(l, kMapV), hk, 0, 2);
     pb.add_other(kPhAttn, l);
-    pb.add_other(kPhMerge, l);
     pb.add_gemm(kEpResid, hq, 1, 2, kPRows, 0, L.g_post);
     pb.seg(layer_map(l, kMapO), layer_map(l, kMapO), D, 0, 0);
     pb.add_gemm(kEpSwiGLU, D, 0, 2, kPRows, 1, nullptr);

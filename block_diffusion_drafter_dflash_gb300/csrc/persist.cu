@@ -736,67 +736,96 @@ __device__ bool attn_phase(const PParams& p, const PPhase& ph, int pi, PBook* bk
   return ok;
 }
 
-// Merge the key chunks of every output row (request, q head, block row) into
-// the W_O GEMM's activation planes; one warp per row.  Lane ch holds chunk
-// ch's (max, sum) and weight; lane l owns output elements [HD/32 * l, +HD/32)
-// and reads them from up to 16 chunks at once (vector loads).
+// Merge of the key chunks of one output row (request b, q head qh, block row
+// k) into the W_O GEMM's activation planes, by one warp.  Lane ch holds chunk
+// ch's (max, sum) and weight; lane l owns output elements [HD/32 * l, +HD/32).
 template <int HD>
-__device__ void merge_phase(const PParams& p, int G, int cta, int ct) {
+__device__ void merge_row(const PParams& p, int b, int qh, int k, int lane) {
   constexpr int E = HD / 32;   // elements per lane: 4 (float4) or 2 (float2)
   const AttnParams& ap = p.attn;
   const int nch = ap.splits, Gq = ap.nq / ap.nkv;
-  const int lane = ct & 31, w = ct >> 5;
-  const int total = ap.B * ap.nq * ap.block;
   __nv_bfloat16* out = static_cast<__nv_bfloat16*>(ap.out);
-  for (int idx = cta * 4 + w; idx < total; idx += G * 4) {
-    const int b = idx / (ap.nq * ap.block), rem = idx - b * ap.nq * ap.block;
-    const int qh = rem / ap.block, k = rem - qh * ap.block;
-    const int kvh = qh / Gq, r = (qh - kvh * Gq) * ap.block + k;
-    const size_t item0 = ((size_t)b * ap.nkv + kvh) * nch;
-    float L = 0.f, acc[E];
+  const int kvh = qh / Gq, r = (qh - kvh * Gq) * ap.block + k;
+  const size_t item0 = ((size_t)b * ap.nkv + kvh) * nch;
+  float L = 0.f, acc[E];
 #pragma unroll
-    for (int e = 0; e < E; ++e) acc[e] = 0.f;
-    // the chunks' maxima first (lanes 0..nch-1, 32 at a time), then the weighted sum
-    float M = attn_tc::kNegInf;
-    for (int c0 = 0; c0 < nch; c0 += 32) {
-      const int ch = c0 + lane;
-      const float2 ml = ch < nch ? __ldcg(ap.ml + (item0 + ch) * kPAttnRows + r) : make_float2(attn_tc::kNegInf, 0.f);
-      if (ml.y > 0.f) M = fmaxf(M, ml.x);
+  for (int e = 0; e < E; ++e) acc[e] = 0.f;
+  // 32 chunks at a time: their (max, sum) once, the running maximum (a batch
+  // beyond the first rescales what was accumulated), then their partial rows,
+  // 16 chunks' vector loads in flight at once
+  float M = attn_tc::kNegInf;
+  for (int c0 = 0; c0 < nch; c0 += 32) {
+    const int ch = c0 + lane, n = min(32, nch - c0);
+    const float2 ml = ch < nch ? __ldcg(ap.ml + (item0 + ch) * kPAttnRows + r) : make_float2(attn_tc::kNegInf, 0.f);
+    float mb = ml.y > 0.f ? ml.x : attn_tc::kNegInf;
+    for (int o = 16; o; o >>= 1) mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, o));
+    const float Mn = fmaxf(M, mb);
+    if (c0 > 0 && Mn > M) {
+      const float sc = exp2f(M - Mn);
+      L *= sc;
+#pragma unroll
+      for (int e = 0; e < E; ++e) acc[e] *= sc;
     }
-    for (int o = 16; o; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-    for (int c0 = 0; c0 < nch; c0 += 32) {
-      const int ch = c0 + lane, n = min(32, nch - c0);
-      const float2 ml = ch < nch ? __ldcg(ap.ml + (item0 + ch) * kPAttnRows + r) : make_float2(attn_tc::kNegInf, 0.f);
-      const float wgt = ml.y > 0.f ? exp2f(ml.x - M) : 0.f;
-      L += wgt * ml.y;
-      for (int u0 = 0; u0 < n; u0 += 16) {
-        float v[16][E], wu[16];
+    M = Mn;
+    const float wgt = ml.y > 0.f ? exp2f(ml.x - M) : 0.f;
+    L += wgt * ml.y;
+    for (int u0 = 0; u0 < n; u0 += 16) {
+      float v[16][E], wu[16];
 #pragma unroll
-        for (int u = 0; u < 16; ++u) {
-          wu[u] = __shfl_sync(0xffffffffu, wgt, (u0 + u) & 31);
-          const bool have = u0 + u < n && wu[u] != 0.f;
-          const float* src = ap.opart + ((item0 + c0 + u0 + u) * kPAttnRows + r) * HD + E * lane;
-          if constexpr (E == 4) {
-            const float4 x = have ? __ldcg(reinterpret_cast<const float4*>(src)) : make_float4(0.f, 0.f, 0.f, 0.f);
-            v[u][0] = x.x; v[u][1] = x.y; v[u][2] = x.z; v[u][3] = x.w;
-          } else {
-            const float2 x = have ? __ldcg(reinterpret_cast<const float2*>(src)) : make_float2(0.f, 0.f);
-            v[u][0] = x.x; v[u][1] = x.y;
-          }
-          if (!have) wu[u] = 0.f;
+      for (int u = 0; u < 16; ++u) {
+        wu[u] = __shfl_sync(0xffffffffu, wgt, (u0 + u) & 31);
+        const bool have = u0 + u < n && wu[u] != 0.f;
+        const float* src = ap.opart + ((item0 + c0 + u0 + u) * kPAttnRows + r) * HD + E * lane;
+        if constexpr (E == 4) {
+          const float4 x = have ? __ldcg(reinterpret_cast<const float4*>(src)) : make_float4(0.f, 0.f, 0.f, 0.f);
+          v[u][0] = x.x; v[u][1] = x.y; v[u][2] = x.z; v[u][3] = x.w;
+        } else {
+          const float2 x = have ? __ldcg(reinterpret_cast<const float2*>(src)) : make_float2(0.f, 0.f);
+          v[u][0] = x.x; v[u][1] = x.y;
         }
-#pragma unroll
-        for (int u = 0; u < 16; ++u)
-#pragma unroll
-          for (int e = 0; e < E; ++e) acc[e] += wu[u] * v[u][e];
+        if (!have) wu[u] = 0.f;
       }
-    }
-    for (int o = 16; o; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
-    const float inv = 1.f / L;
-    const size_t obase = ((size_t)b * ap.block + k) * ap.nq * HD + (size_t)qh * HD + E * lane;
 #pragma unroll
-    for (int e = 0; e < E; ++e) put_act(out, ap.out_plane, obase + e, acc[e] * inv);
+      for (int u = 0; u < 16; ++u)
+#pragma unroll
+        for (int e = 0; e < E; ++e) acc[e] += wu[u] * v[u][e];
+    }
   }
+  for (int o = 16; o; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
+  const float inv = 1.f / L;
+  const size_t obase = ((size_t)b * ap.block + k) * ap.nq * HD + (size_t)qh * HD + E * lane;
+#pragma unroll
+  for (int e = 0; e < E; ++e) put_act(out, ap.out_plane, obase + e, acc[e] * inv);
+}
+
+// After this CTA's attention chunk: announce it on its (request, kv head)
+// group's counter (release), wait (bounded) for the group's other chunks,
+// then merge this chunk's share of the group's output rows (rows
+// [ch R / nch, (ch + 1) R / nch) of R = q heads per kv head x block), one warp
+// per row.  No grid barrier and no phase of its own: the W_O phase follows.
+// Returns false on a timeout.
+template <int HD>
+__device__ bool attn_merge(const PParams& p, const PPhase& ph, PBook* bk, int cta, int ct) {
+  const AttnParams& ap = p.attn;
+  AttnItem item;
+  if (!attn_item(ap, bk->ctx_len, cta, item)) return true;
+  const int nch = ap.splits, Gq = ap.nq / ap.nkv, R = Gq * ap.block;
+  const int ch = cta % nch;
+  int* cnt = p.gcnt + (size_t)ph.layer * ap.B * ap.nkv + item.b * ap.nkv + item.kvh;
+  __threadfence();   // this chunk's partial rows are visible before the count says so
+  csync();
+  if (ct == 0) {
+    atomicAdd(cnt, 1);
+    bk->flag_tk = wait_pieces(cnt, nch, p.status);
+  }
+  csync();
+  if (!bk->flag_tk) return false;
+  const int r1 = (ch + 1) * R / nch;
+  for (int r = ch * R / nch + (ct >> 5); r < r1; r += 4) {
+    const int gh = r / ap.block, k = r - gh * ap.block;
+    merge_row<HD>(p, item.b, item.kvh * Gq + gh, k, ct & 31);
+  }
+  return true;
 }
 
 __device__ void compute_warps(const PParams& p, PBook* bk, uint8_t* ring, uint8_t* region, uint32_t tmem, int G,
@@ -815,18 +844,15 @@ __device__ void compute_warps(const PParams& p, PBook* bk, uint8_t* ring, uint8_
     if (ct == 0 && pi + 1 < p.nphase && p.ph[pi + 1].kind == kPhAttn) attn_tc::prefetch_maps(p.amaps);
     if (ph.kind == kPhGemm) {
       if (!gemm_phase(p, ph, pi, bk, st, tmem, G, cta, ct, seq)) return;
-    } else if (ph.kind == kPhAttn) {
-      // the weight producers hold off until this phase releases the ring
+    } else {
+      // attention; the weight producers hold off until it releases the ring,
+      // which happens before its chunks are merged
       const bool ok = p.attn.hd == 64 ? attn_phase<64>(p, ph, pi, bk, ring, tmem, cta, ct, attn_uses)
                                       : attn_phase<128>(p, ph, pi, bk, ring, tmem, cta, ct, attn_uses);
       csync();
       if (ct == 0) ptx::mbar_arrive(&bk->ring_free);
       if (!ok) return;
-    } else {
-      if (p.attn.hd == 64)
-        merge_phase<64>(p, G, cta, ct);
-      else
-        merge_phase<128>(p, G, cta, ct);
+      if (!(p.attn.hd == 64 ? attn_merge<64>(p, ph, bk, cta, ct) : attn_merge<128>(p, ph, bk, cta, ct))) return;
     }
     // ---- grid barrier: this CTA's writes of the phase are published
     ptx::fence_proxy_async_global();

@@ -12,13 +12,13 @@
 namespace dflash {
 
 constexpr int kPRows = 16;         // token rows one launch serves (one MMA column block per plane)
-constexpr int kPMaxPhases = 56;    // 6 per draft layer + the LM head, up to 9 layers
+constexpr int kPMaxPhases = 56;    // 5 per draft layer + the LM head (+ fusion, injection)
 constexpr int kPMaxSeg = 64;
 constexpr int kPXMaps = 6;
 constexpr int kPAttnRows = 64;     // query rows of one (request, kv head) group: 4 warps x 16
 constexpr int kPMaxStages = 10;
 
-enum : int { kPhGemm = 0, kPhAttn = 1, kPhMerge = 2 };
+enum : int { kPhGemm = 0, kPhAttn = 1 };   // an attention phase ends with the merge of its key chunks
 // epilogue of a projection phase
 enum : int {
   kEpFuse = 0,   // y = acc: planes of y * gain, per-tile sums of y^2 (context fusion)
@@ -62,6 +62,7 @@ struct PParams {
   float* partial;              // [grid][2][16][128] stream-K partial tiles
   int* tickets;                // [largest tile count] stream-K tickets, zero at launch
   unsigned int* bar;           // grid barrier counter, zero at launch (follows tickets)
+  int* gcnt;                   // [layers][B][nkv] finished attention chunks, zero at launch (follows bar)
   int32_t* status;
   EpiQKV<__nv_bfloat16> qkv;
   EpiSwiGLU<__nv_bfloat16> swiglu;

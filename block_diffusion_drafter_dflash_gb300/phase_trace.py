@@ -28,7 +28,7 @@ def phase_names(layers: int, lm_head: bool = True, fusion: bool = False) -> List
     injection of every layer's context K/V."""
     names = ["fusion", "inject"] if fusion else []
     for l in range(layers):
-        names += [f"L{l} qkv", f"L{l} attn", f"L{l} merge", f"L{l} o", f"L{l} gateup", f"L{l} down"]
+        names += [f"L{l} qkv", f"L{l} attn", f"L{l} o", f"L{l} gateup", f"L{l} down"]   # attn: chunks and their merge
     return names + (["lmhead"] if lm_head else [])
 
 

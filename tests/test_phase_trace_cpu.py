@@ -8,9 +8,9 @@ from block_diffusion_drafter_dflash_gb300.phase_trace import DONE, MMA_LAST, STA
 
 
 def test_phase_names_follow_the_drafter_program():
-    assert phase_names(1) == ["L0 qkv", "L0 attn", "L0 merge", "L0 o", "L0 gateup", "L0 down", "lmhead"]
-    assert len(phase_names(5)) == 31
-    assert phase_names(5, fusion=True)[:3] == ["fusion", "inject", "L0 qkv"] and len(phase_names(5, fusion=True)) == 33
+    assert phase_names(1) == ["L0 qkv", "L0 attn", "L0 o", "L0 gateup", "L0 down", "lmhead"]
+    assert len(phase_names(5)) == 26
+    assert phase_names(5, fusion=True)[:3] == ["fusion", "inject", "L0 qkv"] and len(phase_names(5, fusion=True)) == 28
 
 
 def test_phase_table_on_a_hand_made_trace():
