@@ -187,10 +187,21 @@ __global__ void __launch_bounds__(32) sample_sel_kernel(const float* logits, con
   }
 }
 
-// Unnormalised mass of draw i's distribution at logit index v.
-__device__ __forceinline__ float mass(const DrawSel& s, int v, float zscale) {
-  const float pt = prob(__ldg(s.pt + v), zscale, s.mst);
-  return s.pd ? fmaxf(0.f, pt - prob(__ldg(s.pd + v), zscale, s.msd)) : pt;
+// Unnormalised mass of draw i's distribution at the four logit indices of a
+// float4 (lt: the target's or sampled row's logits there, ld: the drafter's).
+__device__ __forceinline__ float mass1(const DrawSel& s, float lt, float ld, float zscale) {
+  const float pt = prob(lt, zscale, s.mst);
+  return s.pd ? fmaxf(0.f, pt - prob(ld, zscale, s.msd)) : pt;
+}
+__device__ __forceinline__ float4 mass4(const DrawSel& s, float4 lt, float4 ld, float zscale) {
+  return make_float4(mass1(s, lt.x, ld.x, zscale), mass1(s, lt.y, ld.y, zscale), mass1(s, lt.z, ld.z, zscale),
+                     mass1(s, lt.w, ld.w, zscale));
+}
+// The logits of draw i's rows at v (a multiple of 4; vocab % 4 == 0 and the
+// rows are 16-byte aligned, so a float4 never crosses the row's end).
+__device__ __forceinline__ void load4(const DrawSel& s, int v, float4& lt, float4& ld) {
+  lt = __ldg(reinterpret_cast<const float4*>(s.pt + v));
+  ld = s.pd ? __ldg(reinterpret_cast<const float4*>(s.pd + v)) : make_float4(0.f, 0.f, 0.f, 0.f);
 }
 
 __global__ void __launch_bounds__(kThreads) draw_sums_kernel(const DrawSel* sel, int V, float zscale, float* csum,
@@ -200,8 +211,23 @@ __global__ void __launch_bounds__(kThreads) draw_sums_kernel(const DrawSel* sel,
   const int c = blockIdx.x, i = blockIdx.y;
   const DrawSel s = sel[i];
   const int v0 = c * kChunk, v1 = min(V, v0 + kChunk);
+  // 8 float4 of each row per thread, all loads issued before the arithmetic
+  constexpr int kV4 = kChunk / kThreads / 4;
+  float4 lt[kV4], ld[kV4];
+#pragma unroll
+  for (int j = 0; j < kV4; ++j) {
+    const int v = v0 + 4 * (threadIdx.x + j * kThreads);
+    if (v < v1) load4(s, v, lt[j], ld[j]);
+  }
   float acc = 0.f;
-  for (int v = v0 + threadIdx.x; v < v1; v += kThreads) acc += mass(s, v, zscale);
+#pragma unroll
+  for (int j = 0; j < kV4; ++j) {
+    const int v = v0 + 4 * (threadIdx.x + j * kThreads);
+    if (v < v1) {
+      const float4 m = mass4(s, lt[j], ld[j], zscale);
+      acc += (m.x + m.y) + (m.z + m.w);
+    }
+  }
   for (int o = 16; o; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
   __shared__ float ws[kThreads / 32];
   if ((threadIdx.x & 31) == 0) ws[threadIdx.x >> 5] = acc;
@@ -256,11 +282,23 @@ __global__ void __launch_bounds__(kThreads) draw_pick_kernel(const DrawSel* sel,
   // thread t owns ids [v0 + kPer t, v0 + kPer (t+1)): its mass, then a block scan
   float mv[kPer];
   float own = 0.f;
+  {
+    float4 lt[kPer / 4], ld[kPer / 4];   // all loads first (float4: kPer and the chunk end are multiples of 4)
 #pragma unroll
-  for (int j = 0; j < kPer; ++j) {
-    const int v = v0 + kPer * threadIdx.x + j;
-    mv[j] = v < v1 ? mass(s, v, zscale) : 0.f;
-    own += mv[j];
+    for (int j = 0; j < kPer / 4; ++j) {
+      const int v = v0 + kPer * threadIdx.x + 4 * j;
+      if (v < v1) load4(s, v, lt[j], ld[j]);
+    }
+#pragma unroll
+    for (int j = 0; j < kPer / 4; ++j) {
+      const int v = v0 + kPer * threadIdx.x + 4 * j;
+      const float4 m = v < v1 ? mass4(s, lt[j], ld[j], zscale) : make_float4(0.f, 0.f, 0.f, 0.f);
+      mv[4 * j] = m.x;
+      mv[4 * j + 1] = m.y;
+      mv[4 * j + 2] = m.z;
+      mv[4 * j + 3] = m.w;
+      own += (m.x + m.y) + (m.z + m.w);
+    }
   }
   // exclusive scan of the 256 partial sums in id order: within each warp by
   // shuffles, then across the 8 warp totals
@@ -300,7 +338,7 @@ __global__ void __launch_bounds__(kThreads) draw_pick_kernel(const DrawSel* sel,
       // or past the total): the chunk's last id with mass
       tok = v0;
       for (int v = v1 - 1; v >= v0; --v)
-        if (mass(s, v, zscale) > 0.f) {
+        if (mass1(s, __ldg(s.pt + v), s.pd ? __ldg(s.pd + v) : 0.f, zscale) > 0.f) {
           tok = v;
           break;
         }
