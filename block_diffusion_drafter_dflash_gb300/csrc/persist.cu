@@ -752,11 +752,29 @@ __device__ void merge_row(const PParams& p, int b, int qh, int k, int lane) {
   for (int e = 0; e < E; ++e) acc[e] = 0.f;
   // 32 chunks at a time: their (max, sum) once, the running maximum (a batch
   // beyond the first rescales what was accumulated), then their partial rows,
-  // 16 chunks' vector loads in flight at once
+  // 16 chunks' vector loads in flight at once.  The first 16 partial rows are
+  // loaded together with the (max, sum) pairs, before their weights are known;
+  // a chunk of weight 0 (no keys) is then dropped by a select, so whatever its
+  // unwritten row holds never enters the sum.
   float M = attn_tc::kNegInf;
+  auto load16 = [&](float (&v)[16][E], int c0, int u0, int n) {
+#pragma unroll
+    for (int u = 0; u < 16; ++u) {
+      const float* src = ap.opart + ((item0 + c0 + u0 + u) * kPAttnRows + r) * HD + E * lane;
+      if constexpr (E == 4) {
+        const float4 x = u0 + u < n ? __ldcg(reinterpret_cast<const float4*>(src)) : make_float4(0.f, 0.f, 0.f, 0.f);
+        v[u][0] = x.x; v[u][1] = x.y; v[u][2] = x.z; v[u][3] = x.w;
+      } else {
+        const float2 x = u0 + u < n ? __ldcg(reinterpret_cast<const float2*>(src)) : make_float2(0.f, 0.f);
+        v[u][0] = x.x; v[u][1] = x.y;
+      }
+    }
+  };
   for (int c0 = 0; c0 < nch; c0 += 32) {
     const int ch = c0 + lane, n = min(32, nch - c0);
     const float2 ml = ch < nch ? __ldcg(ap.ml + (item0 + ch) * kPAttnRows + r) : make_float2(attn_tc::kNegInf, 0.f);
+    float v[16][E];
+    load16(v, c0, 0, n);
     float mb = ml.y > 0.f ? ml.x : attn_tc::kNegInf;
     for (int o = 16; o; o >>= 1) mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, o));
     const float Mn = fmaxf(M, mb);
@@ -770,25 +788,14 @@ __device__ void merge_row(const PParams& p, int b, int qh, int k, int lane) {
     const float wgt = ml.y > 0.f ? exp2f(ml.x - M) : 0.f;
     L += wgt * ml.y;
     for (int u0 = 0; u0 < n; u0 += 16) {
-      float v[16][E], wu[16];
+      if (u0 > 0) load16(v, c0, u0, n);
 #pragma unroll
       for (int u = 0; u < 16; ++u) {
-        wu[u] = __shfl_sync(0xffffffffu, wgt, (u0 + u) & 31);
-        const bool have = u0 + u < n && wu[u] != 0.f;
-        const float* src = ap.opart + ((item0 + c0 + u0 + u) * kPAttnRows + r) * HD + E * lane;
-        if constexpr (E == 4) {
-          const float4 x = have ? __ldcg(reinterpret_cast<const float4*>(src)) : make_float4(0.f, 0.f, 0.f, 0.f);
-          v[u][0] = x.x; v[u][1] = x.y; v[u][2] = x.z; v[u][3] = x.w;
-        } else {
-          const float2 x = have ? __ldcg(reinterpret_cast<const float2*>(src)) : make_float2(0.f, 0.f);
-          v[u][0] = x.x; v[u][1] = x.y;
-        }
-        if (!have) wu[u] = 0.f;
+        const float wu = __shfl_sync(0xffffffffu, wgt, (u0 + u) & 31);
+        const bool have = u0 + u < n && wu != 0.f;
+#pragma unroll
+        for (int e = 0; e < E; ++e) acc[e] += have ? wu * v[u][e] : 0.f;
       }
-#pragma unroll
-      for (int u = 0; u < 16; ++u)
-#pragma unroll
-        for (int e = 0; e < E; ++e) acc[e] += wu[u] * v[u][e];
     }
   }
   for (int o = 16; o; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
