@@ -652,6 +652,12 @@ GemmPlan plan_gemm_tc(int M, int K, int tiles, int sms, int planes) {
       const int splits = (kblocks + kbps - 1) / kbps;
       if (splits != sp && env_splits <= 0) continue;
       const long ctas = base * splits;
+      // One-plane 256-row tiles (exact target features): a stage's activation
+      // tile is twice its weight tile, and a split that runs in more than one
+      // wave costs more than this model says (512 rows x 20,480 x 4,096 on 152
+      // SMs: 7 splits in three waves 174 us, 2 splits in one wave 105 us), so
+      // split-K stays within one wave there.
+      if (planes == 1 && g.bm == 256 && splits > 1 && ctas > slots && env_splits <= 0) continue;
       // HBM side: the weight tile of each stage (activation tiles come from L2)
       const double wtile = kTileN * 128.0;
       const double bytes = kbps * wtile, inflight = std::min(S, kbps) * wtile;
