@@ -13,9 +13,10 @@
 //
 //   row_stats   grid (chunks, rows): per 8192-logit chunk of a row, the max m
 //               of z = l * log2(e) / T and s = sum exp2(z - m) (online form);
-//   accept      one warp per request: lane k merges the chunks of draft
-//               position k's two rows and reads its token's two logits (all
-//               positions at once), takes the acceptance test, and a ballot
+//   accept      one CTA per request: the (max, sum) of its rows from their
+//               chunks (all warps, loads first), then one warp: lane k takes
+//               draft position k's two rows and reads its token's two logits
+//               (all positions at once), takes the acceptance test, and a ballot
 //               finds the first rejection; the distribution to draw from is
 //               the residual there, or the target's row after the block;
 //               writes tau and the accepted tokens;
@@ -38,6 +39,7 @@ namespace dflash {
 namespace {
 
 constexpr int kChunk = 8192;       // logits per chunk (32 KB of fp32)
+constexpr int kMaxChunks = (1 << 24) / kChunk;   // the vocabulary is at most 2^24 ids
 constexpr int kThreads = 256;      // kChunk / kThreads = 32 logits a thread
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -111,30 +113,54 @@ __device__ __forceinline__ float2 row_total(const float2* part, int r, int nchun
 // p(x) of one logit given its row's (max, sum).
 __device__ __forceinline__ float prob(float logit, float zscale, float2 ms) { return exp2f(logit * zscale - ms.x) / ms.y; }
 
-__global__ void __launch_bounds__(32) accept_kernel(const float* draft, const float* target, const int32_t* tokens,
-                                                    const float* u_accept, const float2* part, int nchunk, int B,
-                                                    int g, int V, float zscale, DrawSel* sel, int32_t* accept_len,
-                                                    int32_t* out_tokens) {
+// One CTA per request.  First the (max, sum) of its 2g-1 rows from their
+// chunk partials, by all warps (every warp issues the loads of its rows, one
+// row a round, before merging any; lane c takes chunk c, then a warp merge):
+// tot[k] draft position k (k < g-1), tot[32 + k] the target's row k (k < g).
+// Then warp 0 walks the block.  g <= 32.
+__global__ void __launch_bounds__(kThreads) accept_kernel(const float* draft, const float* target,
+                                                          const int32_t* tokens, const float* u_accept,
+                                                          const float2* part, int nchunk, int B, int g, int V,
+                                                          float zscale, DrawSel* sel, int32_t* accept_len,
+                                                          int32_t* out_tokens) {
   griddep_wait();
   griddep_trigger();
-  const int b = blockIdx.x, lane = threadIdx.x;
-  const int nd = B * (g - 1);
+  const int b = blockIdx.x, lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int nd = B * (g - 1), nrow = 2 * g - 1;
+  __shared__ float2 tot[64];
+  {
+    constexpr int kW = kThreads / 32, kRounds = (63 + kW - 1) / kW;
+    float2 first[kRounds];
+#pragma unroll
+    for (int u = 0; u < kRounds; ++u) {
+      const int j = warp + kW * u;   // draft rows first, then the target's
+      const int r = j < g - 1 ? b * (g - 1) + j : nd + b * g + (j - (g - 1));
+      first[u] = j < nrow && lane < nchunk ? part[(size_t)r * nchunk + lane] : make_float2(-INFINITY, 0.f);
+    }
+#pragma unroll
+    for (int u = 0; u < kRounds; ++u) {
+      const int j = warp + kW * u;
+      if (j >= nrow) break;
+      const int r = j < g - 1 ? b * (g - 1) + j : nd + b * g + (j - (g - 1));
+      float2 t = first[u];
+      for (int c = lane + 32; c < nchunk; c += 32) t = merge_ms(t, part[(size_t)r * nchunk + c]);
+      t = warp_merge(t);
+      if (lane == 0) tot[j < g - 1 ? j : 32 + (j - (g - 1))] = t;
+    }
+  }
+  __syncthreads();
+  if (warp > 0) return;
   // every input of the walk first, in parallel: lane k < g-1 takes draft
   // position k (its two rows' (max, sum) and the two logits of its token),
-  // lane g-1 the target row after the block; g <= 32
+  // lane g-1 the target row after the block
   float2 md = make_float2(0.f, 1.f), mt = make_float2(0.f, 1.f);
   float ld = 0.f, lt = 0.f, ua = 0.f;
   int d = -1;
   if (lane < g) {
-    const int rt = nd + b * g + lane;
-    float2 t = make_float2(-INFINITY, 0.f);
-    for (int c = 0; c < nchunk; ++c) t = merge_ms(t, part[(size_t)rt * nchunk + c]);
-    mt = t;
+    mt = tot[32 + lane];
     if (lane < g - 1) {
       const int rd = b * (g - 1) + lane;
-      float2 q = make_float2(-INFINITY, 0.f);
-      for (int c = 0; c < nchunk; ++c) q = merge_ms(q, part[(size_t)rd * nchunk + c]);
-      md = q;
+      md = tot[lane];
       d = tokens[rd];
       ua = u_accept[rd];
       if (d >= 0 && d < V) {
@@ -250,16 +276,19 @@ __global__ void __launch_bounds__(kThreads) draw_pick_kernel(const DrawSel* sel,
   __shared__ float s_rem;
   __shared__ float s_tsum[kThreads / 32];
   __shared__ int s_tok;
+  __shared__ float s_cs[kMaxChunks];
+  for (int c = threadIdx.x; c < nchunk; c += kThreads) s_cs[c] = csum[(size_t)i * nchunk + c];   // all loads at once
+  __syncthreads();
   if (threadIdx.x == 0) {
     // running mass over the chunks in id order (double: the chunk sums are few)
     double total = 0.0;
-    for (int c = 0; c < nchunk; ++c) total += csum[(size_t)i * nchunk + c];
+    for (int c = 0; c < nchunk; ++c) total += s_cs[c];
     const double target = (double)__ldg(u + i) * total;
     double run = 0.0;
     int pick = -1, last_nz = 0;
     double before = 0.0;
     for (int c = 0; c < nchunk; ++c) {
-      const double m = csum[(size_t)i * nchunk + c];
+      const double m = s_cs[c];
       if (m > 0.0) last_nz = c;
       if (pick < 0 && run + m > target && m > 0.0) {
         pick = c;
@@ -391,7 +420,7 @@ cudaError_t verify_sampled_launch(const float* draft_logits, const float* target
                              nd, V, zscale, w.part, nchunk);
   if (e != cudaSuccess) return e;
   ++*launches;
-  e = launch_pdl(accept_kernel, dim3(B), dim3(32), 0, s, draft_logits, target_logits, drafts, u_accept,
+  e = launch_pdl(accept_kernel, dim3(B), dim3(kThreads), 0, s, draft_logits, target_logits, drafts, u_accept,
                  static_cast<const float2*>(w.part), nchunk, B, g, V, zscale, w.sel, accept_len, out_tokens);
   if (e != cudaSuccess) return e;
   ++*launches;
