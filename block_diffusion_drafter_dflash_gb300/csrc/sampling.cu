@@ -64,7 +64,7 @@ __device__ __forceinline__ const float* row_ptr(const float* draft, const float*
   return r < nd ? draft + (size_t)r * V : target + (size_t)(r - nd) * V;
 }
 
-__global__ void __launch_bounds__(kThreads) row_stats_kernel(const float* draft, const float* target, int nd, int V,
+__global__ void __launch_bounds__(kThreads, 6) row_stats_kernel(const float* draft, const float* target, int nd, int V,
                                                              float zscale, float2* part, int nchunk) {
   griddep_wait();
   griddep_trigger();
