@@ -64,6 +64,8 @@ __device__ __forceinline__ const float* row_ptr(const float* draft, const float*
   return r < nd ? draft + (size_t)r * V : target + (size_t)(r - nd) * V;
 }
 
+// At most 40 registers a thread, so that 6 CTAs share an SM: 192 KB of loads
+// in flight per SM instead of 160 KB at 5 (112 -> 106 us for 603 MB).
 __global__ void __launch_bounds__(kThreads, 6) row_stats_kernel(const float* draft, const float* target, int nd, int V,
                                                              float zscale, float2* part, int nchunk) {
   griddep_wait();
